@@ -1,0 +1,173 @@
+// C-ABI entry points of libpkv that touch the GPU: argument validation on the
+// host, TMA tensor-map encoding, kernel launches on the caller's stream, and
+// the one synchronising call that reads the device status word.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "pkv.h"
+#include "pkv_internal.h"
+
+namespace {
+
+using EncodeFn = PFN_cuTensorMapEncodeTiled_v12000;
+
+EncodeFn encoder() {
+  static EncodeFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeFn>(p);
+  });
+  return fn;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+bool supported_shape(int32_t block_size, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim) {
+  if (num_kv_heads <= 0 || num_q_heads <= 0 || num_q_heads % num_kv_heads != 0) return false;
+  const int32_t g = num_q_heads / num_kv_heads;
+  return g >= 1 && g <= 16 && (head_dim == 64 || head_dim == 128) &&
+         (block_size == 16 || block_size == 32 || block_size == 64);
+}
+
+// Pool tensor [num_blocks*Hkv*bs rows][D] -> boxes of 16 rows x 64 columns, 128B swizzle.
+bool encode_pool(CUtensorMap *m, const void *pool, int64_t rows, int32_t head_dim) {
+  EncodeFn enc = encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(head_dim) * 2};
+  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(pkv::kSubKeys)};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(pool), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// q [T][Hq][D] -> boxes of (64 columns, G heads, P positions), 128B swizzle.
+bool encode_q(CUtensorMap *m, const void *q, int64_t total_q, int32_t hq, int32_t d, int32_t g, int32_t p) {
+  EncodeFn enc = encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(hq), static_cast<cuuint64_t>(total_q)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(hq) * d * 2};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(g), static_cast<cuuint32_t>(p)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(q), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+uint64_t align256(uint64_t x) { return (x + 255) & ~uint64_t(255); }
+
+}  // namespace
+
+extern "C" {
+
+pkv_status pkv_cache_write(const void *k_new, const void *v_new, const int64_t *slot_mapping,
+                           int64_t num_tokens, void *k_pool, void *v_pool, int64_t num_blocks,
+                           int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
+                           uint32_t *device_status, pkv_stream_t stream) {
+  if (num_tokens < 0 || num_blocks <= 0 || block_size <= 0 || num_kv_heads <= 0) return PKV_ERR_INVALID_ARG;
+  if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return PKV_OK;
+  if (!k_new || !v_new || !slot_mapping || !k_pool || !v_pool) return PKV_ERR_INVALID_ARG;
+  if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) ||
+      !aligned(slot_mapping, 8))
+    return PKV_ERR_INVALID_ARG;
+  cudaError_t e = pkv::launch_cache_write(k_new, v_new, slot_mapping, num_tokens, k_pool, v_pool, num_blocks,
+                                          block_size, num_kv_heads, head_dim, device_status,
+                                          reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+pkv_status pkv_attention(const void *q, const int32_t *cu_seqlens_q, int32_t num_seqs, int64_t total_q,
+                         const int32_t *seq_slot, const int32_t *context_lens, const int32_t *block_tables,
+                         int32_t max_slots, int32_t max_blocks_per_slot, int32_t block_size,
+                         const void *k_pool, const void *v_pool, int64_t num_blocks, int32_t num_q_heads,
+                         int32_t num_kv_heads, int32_t head_dim, float scale, const int32_t *work,
+                         const pkv_work_info *info, void *out, void *workspace, uint64_t workspace_bytes,
+                         uint32_t *device_status, pkv_stream_t stream) {
+  if (!info || num_seqs < 0 || total_q < 0 || max_slots <= 0 || max_blocks_per_slot <= 0 || num_blocks <= 0)
+    return PKV_ERR_INVALID_ARG;
+  if (!supported_shape(block_size, num_q_heads, num_kv_heads, head_dim)) return PKV_ERR_UNSUPPORTED;
+  const int64_t rows = num_blocks * num_kv_heads * block_size;
+  if (rows > INT32_MAX || total_q > INT32_MAX) return PKV_ERR_UNSUPPORTED;
+  const int64_t items = static_cast<int64_t>(info->num_decode_items) + info->num_prefill_items +
+                        info->num_combine_items;
+  if (info->num_decode_items < 0 || info->num_prefill_items < 0 || info->num_combine_items < 0 ||
+      info->num_partials < 0 || info->work_words != items * PKV_WORK_WORDS_PER_ITEM)
+    return PKV_ERR_INVALID_ARG;
+  if (items == 0 || total_q == 0) return PKV_OK;
+  if (!q || !cu_seqlens_q || !seq_slot || !context_lens || !block_tables || !k_pool || !v_pool || !work || !out)
+    return PKV_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(out, 16) ||
+      !aligned(work, 16))
+    return PKV_ERR_INVALID_ARG;
+  const uint64_t acc_bytes = align256(uint64_t(info->num_partials) * num_q_heads * head_dim * 4);
+  const uint64_t need = info->num_partials == 0 ? 0 : acc_bytes + align256(uint64_t(info->num_partials) * num_q_heads * 8);
+  if (need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 256)))
+    return PKV_ERR_WORKSPACE_TOO_SMALL;
+  if ((info->num_combine_items > 0) != (info->num_partials > 0)) return PKV_ERR_INVALID_ARG;
+
+  pkv::StepArgs a{};
+  a.q = q;
+  a.cu_seqlens_q = cu_seqlens_q;
+  a.seq_slot = seq_slot;
+  a.context_lens = context_lens;
+  a.block_tables = block_tables;
+  a.num_seqs = num_seqs;
+  a.max_slots = max_slots;
+  a.max_blocks_per_slot = max_blocks_per_slot;
+  a.block_size = block_size;
+  a.num_blocks = num_blocks;
+  a.total_q = total_q;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.group = num_q_heads / num_kv_heads;
+  a.head_dim = head_dim;
+  const float s = scale > 0.f ? scale : 1.0f / std::sqrt(static_cast<float>(head_dim));
+  a.scale_log2 = s * 1.4426950408889634f;
+  a.work = work;
+  a.out = out;
+  a.partial_acc = static_cast<float *>(workspace);
+  a.partial_ml = need ? reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + acc_bytes) : nullptr;
+  a.status = device_status;
+
+  CUtensorMap tk, tv, tq;
+  if (!encode_pool(&tk, k_pool, rows, head_dim) || !encode_pool(&tv, v_pool, rows, head_dim))
+    return PKV_ERR_CUDA;
+  const int32_t rpt = pkv::prefill_rows_per_tile(a.group);
+  if (info->num_prefill_items > 0 && !encode_q(&tq, q, total_q, num_q_heads, head_dim, a.group, rpt))
+    return PKV_ERR_CUDA;
+
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int32_t *dec = work;
+  const int32_t *pre = dec + static_cast<int64_t>(info->num_decode_items) * PKV_WORK_WORDS_PER_ITEM;
+  const int32_t *comb = pre + static_cast<int64_t>(info->num_prefill_items) * PKV_WORK_WORDS_PER_ITEM;
+  cudaError_t e = pkv::launch_prefill(a, tq, tk, tv, rpt, info->num_prefill_items, pre, st);
+  if (e == cudaSuccess) e = pkv::launch_decode(a, tk, tv, info->num_decode_items, dec, st);
+  if (e == cudaSuccess) e = pkv::launch_combine(a, info->num_combine_items, comb, st);
+  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+pkv_status pkv_check_device_status(uint32_t *device_status, pkv_stream_t stream, uint32_t *bits_out) {
+  if (!device_status) return PKV_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint32_t bits = 0;
+  if (cudaMemcpyAsync(&bits, device_status, sizeof(bits), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaMemsetAsync(device_status, 0, sizeof(bits), st) != cudaSuccess || cudaStreamSynchronize(st) != cudaSuccess)
+    return PKV_ERR_CUDA;
+  if (bits_out) *bits_out = bits;
+  if (bits == 0) return PKV_OK;
+  return (bits & PKV_DEV_TIMEOUT) ? PKV_ERR_DEVICE_TIMEOUT : PKV_ERR_DEVICE_INDEX;
+}
+
+}  // extern "C"

@@ -1,0 +1,51 @@
+// Internal interfaces between the C-ABI layer (pkv_api.cu) and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pkv.h"
+
+namespace pkv {
+
+// Keys per 16-row sub-tile: the unit every kernel loads with one TMA box per
+// 64-column half of head_dim.
+constexpr int kSubKeys = 16;
+
+struct StepArgs {
+  const void *q;
+  const int32_t *cu_seqlens_q;
+  const int32_t *seq_slot;
+  const int32_t *context_lens;
+  const int32_t *block_tables;
+  int32_t num_seqs, max_slots, max_blocks_per_slot, block_size;
+  int64_t num_blocks, total_q;
+  int32_t num_q_heads, num_kv_heads, group, head_dim;
+  float scale_log2;  // softmax scale times log2(e)
+  const int32_t *work;
+  void *out;
+  float *partial_acc;  // [num_partials][Hq][D]
+  float *partial_ml;   // [num_partials][Hq][2]  (running max in log2 units, sum)
+  uint32_t *status;
+};
+
+cudaError_t launch_cache_write(const void *k_new, const void *v_new, const int64_t *slot_mapping,
+                               int64_t num_tokens, void *k_pool, void *v_pool, int64_t num_blocks,
+                               int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
+                               uint32_t *status, cudaStream_t stream);
+
+cudaError_t launch_decode(const StepArgs &a, const CUtensorMap &tmap_k, const CUtensorMap &tmap_v,
+                          int32_t num_items, const int32_t *items, cudaStream_t stream);
+
+cudaError_t launch_combine(const StepArgs &a, int32_t num_items, const int32_t *items,
+                           cudaStream_t stream);
+
+cudaError_t launch_prefill(const StepArgs &a, const CUtensorMap &tmap_q, const CUtensorMap &tmap_k,
+                           const CUtensorMap &tmap_v, int32_t rows_per_tile, int32_t num_items,
+                           const int32_t *items, cudaStream_t stream);
+
+// Positions per prefill tile: whole GQA groups fit one 128-row MMA tile.
+inline int32_t prefill_rows_per_tile(int32_t group) { return 128 / group; }
+
+}  // namespace pkv

@@ -1,0 +1,147 @@
+"""Device-side set-up of one step through the library's own host API.
+
+Given a step description (slots with their physical blocks and key/value
+histories, and the packed query rows), this module:
+
+1. creates the library's block pool and hands each slot its blocks
+   (``pkv_pool_admit_blocks``);
+2. writes each slot's cached history into a sentinel-filled device pool with
+   ``pkv_cache_write``, through a slot mapping from ``pkv_plan_lower``;
+3. lowers the step plan itself, builds the work list (``pkv_plan_work``) and
+   uploads the step's metadata, queries and new keys/values.
+
+``run_cache_write`` and ``run_attention`` then issue the step's two device
+calls. Nothing here computes attention; it only moves arguments.
+"""
+
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+
+from . import binding as B
+
+SENTINEL_BITS = 0x7FC1  # quiet bfloat16 NaN in pool rows never written
+
+
+def _bf16_tensor(bits: np.ndarray, device):
+    import torch
+
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16))
+    return t.to(device).view(torch.bfloat16)
+
+
+def _i32(a, device):
+    import torch
+
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(device)
+
+
+def _i64(a, device):
+    import torch
+
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int64)).to(device)
+
+
+def empty_pool(num_blocks, num_kv_heads, block_size, head_dim, device):
+    import torch
+
+    k = torch.empty((num_blocks, num_kv_heads, block_size, head_dim), dtype=torch.bfloat16, device=device)
+    v = torch.empty_like(k)
+    k.view(torch.int16).fill_(SENTINEL_BITS)
+    v.view(torch.int16).fill_(SENTINEL_BITS)
+    return k, v
+
+
+@dataclass
+class DeviceStep:
+    w: object                 # the step description (workloads.StepInputs)
+    pool: B.Pool
+    lowered: B.Lowered        # this step's packed metadata (host)
+    k_pool: object
+    v_pool: object
+    q: object
+    k_new: object
+    v_new: object
+    slot_mapping: object
+    cu_seqlens_q: object
+    seq_slot: object
+    context_lens: object
+    block_tables: object
+    work: object
+    info: B.WorkInfo
+    workspace: object
+    out: object
+    status: object
+
+    @property
+    def scale(self) -> float:
+        return self.w.scale
+
+
+def prepare(w, device="cuda", *, pools=None) -> DeviceStep:
+    """Build the pool state before the step and upload the step's inputs."""
+    import torch
+
+    pool = B.Pool(w.num_blocks, w.block_size, w.max_slots, w.max_blocks_per_slot)
+    for slot in sorted(w.blocks):
+        pool.admit_blocks(slot, w.blocks[slot])
+    k_pool, v_pool = pools if pools is not None else empty_pool(
+        w.num_blocks, w.num_kv_heads, w.block_size, w.head_dim, device)
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+
+    # Cached history: every segment's positions before this step's rows.
+    hist_plan = [(s.slot, s.ctx - s.q_len) for s in w.segments]
+    hist = pool.lower(hist_plan)
+    if len(hist.slot_mapping):
+        hk = np.concatenate([w.hist_k[s.slot][: s.ctx - s.q_len] for s in w.segments])
+        hv = np.concatenate([w.hist_v[s.slot][: s.ctx - s.q_len] for s in w.segments])
+        B.pkv_cache_write(_bf16_tensor(hk, device), _bf16_tensor(hv, device), _i64(hist.slot_mapping, device),
+                          k_pool, v_pool, device_status=status)
+
+    low = pool.lower([(s.slot, s.q_len) for s in w.segments])
+    work, info = B.pkv_plan_work(low.cu_seqlens_q, low.seq_slot, low.context_lens, max_slots=w.max_slots,
+                                 max_blocks_per_slot=w.max_blocks_per_slot, block_size=w.block_size,
+                                 num_q_heads=w.num_q_heads, num_kv_heads=w.num_kv_heads, head_dim=w.head_dim)
+    ws = None
+    if info.workspace_bytes:
+        ws = torch.empty(int(info.workspace_bytes), dtype=torch.uint8, device=device)
+    out = torch.empty((w.total_q, w.num_q_heads, w.head_dim), dtype=torch.bfloat16, device=device)
+    out.view(torch.int16).fill_(SENTINEL_BITS)
+    return DeviceStep(
+        w=w, pool=pool, lowered=low, k_pool=k_pool, v_pool=v_pool,
+        q=_bf16_tensor(w.q, device), k_new=_bf16_tensor(w.new_k(), device), v_new=_bf16_tensor(w.new_v(), device),
+        slot_mapping=_i64(low.slot_mapping, device), cu_seqlens_q=_i32(low.cu_seqlens_q, device),
+        seq_slot=_i32(low.seq_slot, device), context_lens=_i32(low.context_lens, device),
+        block_tables=_i32(pool.block_tables(), device), work=_i32(work, device), info=info, workspace=ws,
+        out=out, status=status)
+
+
+def run_cache_write(ds: DeviceStep, stream=None) -> None:
+    B.pkv_cache_write(ds.k_new, ds.v_new, ds.slot_mapping, ds.k_pool, ds.v_pool,
+                      device_status=ds.status, stream=stream)
+
+
+def run_attention(ds: DeviceStep, stream=None) -> None:
+    B.pkv_attention(ds.q, ds.cu_seqlens_q, ds.seq_slot, ds.context_lens, ds.block_tables, ds.k_pool,
+                    ds.v_pool, ds.work, ds.info, ds.out, ds.workspace, scale=ds.scale,
+                    device_status=ds.status, stream=stream)
+
+
+def run_step(ds: DeviceStep, stream=None) -> None:
+    run_cache_write(ds, stream)
+    run_attention(ds, stream)
+
+
+def out_f32(ds: DeviceStep) -> np.ndarray:
+    import torch
+
+    return ds.out.to(torch.float32).cpu().numpy()
+
+
+def pool_bits(ds: DeviceStep):
+    import torch
+
+    return (ds.k_pool.view(torch.int16).cpu().numpy().view(np.uint16),
+            ds.v_pool.view(torch.int16).cpu().numpy().view(np.uint16))

@@ -1,0 +1,302 @@
+/*
+ * pkv.h -- C ABI of libpkv: one model step of paged-KV attention for
+ * continuous batching, on NVIDIA GB300 (sm_103a).
+ *
+ * Sources (pages on continuous batching; no code is taken from them):
+ *   [LB]  Lucebox, "Continuous batching: Qwen3.8-27B at 301 tok/s across five
+ *         clients, up to 1.97x llama.cpp"
+ *   [T15] "Tutorial 15: Continuous Batching and Scheduling"
+ *   [MX]  mlxcel manual, "Continuous batching"
+ *
+ * One step, in stream order on the caller's stream:
+ *   1. pkv_plan_lower (host) turns the scheduler's step plan -- which slots
+ *      advance by how many rows, prompt chunks first, decode rows after --
+ *      into one packed token axis with segment metadata, growing each slot's
+ *      block table from the shared free pool ([LB] §Packing unequal prompt
+ *      chunks together; §Paged KV and paged attention).
+ *   2. pkv_plan_work (host) splits the step's attention into work items.
+ *   3. pkv_cache_write appends each new row's key and value to the pool.
+ *   4. pkv_attention computes grouped-query attention for every packed row,
+ *      causal inside prompt chunks, reading the pool through block tables.
+ *
+ * Conventions for every call:
+ *   - bf16 tensors are passed as `void*`/`const void*` to 16-bit storage
+ *     (IEEE bfloat16 bit patterns). All device tensors are row-major and
+ *     contiguous, with the shapes given per argument.
+ *   - The caller owns every buffer. The library allocates no device memory
+ *     and never synchronises, except pkv_check_device_status.
+ *   - Device calls are asynchronous on `stream` (a cudaStream_t; NULL is the
+ *     legacy default stream). Arguments are validated on the host before any
+ *     launch; a call that returns an error has launched nothing.
+ *   - Index errors only visible on the device (a block ID outside the pool, a
+ *     slot mapping past the pool, metadata that disagrees with the work list)
+ *     never fault: the kernel skips the access and ORs a PKV_DEV_* bit into
+ *     `device_status` (if non-NULL). Read it with pkv_check_device_status.
+ *   - Supported shapes: head_dim 64 or 128; block_size 16, 32 or 64;
+ *     num_q_heads a multiple of num_kv_heads with group size 1..16.
+ */
+#ifndef PKV_H_
+#define PKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *pkv_stream_t; /* identical to cudaStream_t */
+
+typedef enum pkv_status {
+    PKV_OK = 0,
+    PKV_ERR_INVALID_ARG = 1,          /* a pointer, size or shape is wrong */
+    PKV_ERR_OUT_OF_RANGE = 2,         /* an index (slot, position, block) is outside its table */
+    PKV_ERR_UNSUPPORTED = 3,          /* a valid shape this build has no kernel for */
+    PKV_ERR_WORKSPACE_TOO_SMALL = 4,  /* a caller buffer is smaller than required */
+    PKV_ERR_CUDA = 5,                 /* a CUDA runtime call failed */
+    PKV_ERR_DEVICE_TIMEOUT = 6,       /* a kernel's bounded wait gave up (device_status) */
+    PKV_ERR_NO_BLOCKS = 7,            /* the pool cannot satisfy a reservation */
+    PKV_ERR_DEVICE_INDEX = 8          /* a kernel met an invalid index and skipped it */
+} pkv_status;
+
+/* Bits a kernel ORs into *device_status. */
+#define PKV_DEV_BAD_SLOT_MAPPING 0x1u /* slot_mapping entry >= num_blocks * block_size */
+#define PKV_DEV_BAD_BLOCK 0x2u        /* block-table entry outside [0, num_blocks) */
+#define PKV_DEV_BAD_SEGMENT 0x4u      /* segment metadata disagrees with the work list */
+#define PKV_DEV_TIMEOUT 0x8u          /* a bounded mbarrier wait expired */
+
+/* Static text for a status code. */
+const char *pkv_status_string(pkv_status status);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int32_t pkv_version(void);
+
+/* ------------------------------------------------------------------------
+ * Block pool (host side). [LB] §Paged KV and paged attention: KV is divided
+ * into fixed-size physical blocks shared by all sequences; each sequence owns
+ * a block table mapping logical positions to physical blocks; finished
+ * requests return their blocks, which a new request may take without moving
+ * anyone else. [LB] §Admission and step planning are different decisions:
+ * admission reserves KV capacity atomically. [LB] §Keeping track of each
+ * request: each admitted request gets a stable sequence slot.
+ *
+ * The free list is a stack: released blocks go on top and are handed out
+ * first. All calls are host-only, not thread-safe, and never touch a GPU.
+ * ---------------------------------------------------------------------- */
+typedef struct pkv_pool pkv_pool;
+
+typedef struct pkv_pool_stats {
+    int64_t num_blocks;     /* blocks in the pool */
+    int32_t block_size;     /* tokens per block */
+    int32_t max_slots;      /* sequence slots */
+    int64_t free_blocks;    /* on the free stack */
+    int64_t owned_blocks;   /* held by live slots */
+    int32_t live_slots;     /* slots currently admitted */
+    int64_t live_tokens;    /* sum of live slots' lengths */
+} pkv_pool_stats;
+
+/*
+ * Create a pool of `num_blocks` blocks of `block_size` tokens for
+ * `max_slots` slots of at most `max_blocks_per_slot` blocks each.
+ * `free_order` (nullable) gives the initial free stack, top LAST, as
+ * `free_order_len` distinct block IDs; blocks not listed start out
+ * unavailable. NULL means all blocks, block 0 on top.
+ * Returns NULL on invalid arguments or allocation failure.
+ */
+pkv_pool *pkv_pool_create(int64_t num_blocks, int32_t block_size, int32_t max_slots,
+                          int32_t max_blocks_per_slot, const int32_t *free_order,
+                          int64_t free_order_len);
+void pkv_pool_destroy(pkv_pool *pool);
+
+/*
+ * Admit a request into free slot `slot`: reserve ceil(reserve_tokens /
+ * block_size) blocks off the free stack, all or nothing, as the first
+ * entries of the slot's block table. The slot's length starts at 0.
+ * Errors: PKV_ERR_OUT_OF_RANGE (bad slot or too many blocks for one slot),
+ * PKV_ERR_INVALID_ARG (slot already live), PKV_ERR_NO_BLOCKS (not enough free
+ * blocks; nothing is taken).
+ */
+pkv_status pkv_pool_admit(pkv_pool *pool, int32_t slot, int64_t reserve_tokens);
+
+/*
+ * Admit into `slot` with the given physical blocks (in logical order), each
+ * of which must be on the free stack. All or nothing.
+ */
+pkv_status pkv_pool_admit_blocks(pkv_pool *pool, int32_t slot, const int32_t *blocks,
+                                 int32_t num);
+
+/*
+ * Retire `slot`: its blocks go back on the free stack with the slot's first
+ * block on top, and the slot becomes free. Other slots are untouched.
+ * Errors: PKV_ERR_OUT_OF_RANGE, PKV_ERR_INVALID_ARG (slot not live).
+ */
+pkv_status pkv_pool_release(pkv_pool *pool, int32_t slot);
+
+/* Current length (tokens appended) of a live slot, or -1. */
+int64_t pkv_pool_slot_length(const pkv_pool *pool, int32_t slot);
+
+/* Blocks currently in the slot's table, or -1. */
+int32_t pkv_pool_slot_blocks(const pkv_pool *pool, int32_t slot);
+
+/* Counters in the spirit of [MX] §Paged KV cache and prefix sharing (block
+ * size, allocated/free blocks). */
+pkv_status pkv_pool_get_stats(const pkv_pool *pool, pkv_pool_stats *stats);
+
+/*
+ * Copy the block tables, int32 [max_slots][max_blocks_per_slot] with -1 in
+ * unused entries, to host memory `out` of `capacity` entries.
+ */
+pkv_status pkv_pool_copy_block_tables(const pkv_pool *pool, int32_t *out, int64_t capacity);
+
+/* ------------------------------------------------------------------------
+ * Step-plan lowering (host side).
+ * [LB] §One scheduler, model-specific execution: the engine lowers the
+ * selected prompt chunks and decode rows into its backend's layout.
+ * [LB] §Packing unequal prompt chunks together: one token axis, no padding,
+ * segment metadata saying where each chunk ends and which slot owns it.
+ * [LB] §Chunked prefill is a slot phase: each chunk appends to its slot's KV.
+ * ---------------------------------------------------------------------- */
+typedef struct pkv_segment {
+    int32_t slot;       /* live slot whose sequence advances */
+    int32_t num_tokens; /* new rows this step (1 for a decode row; a chunk otherwise) */
+} pkv_segment;
+
+/*
+ * Lower a step plan (segments in packed order). For segment s with n rows
+ * in slot c of current length len: rows take positions len .. len+n-1, the
+ * slot's length becomes len+n, and blocks are taken off the free stack when
+ * a position opens a block the table does not have yet (all or nothing for
+ * the whole plan). Host outputs:
+ *   cu_seqlens_q  int32 [num_segments+1]  row offsets of each segment
+ *   seq_slot      int32 [num_segments]    row-to-slot map
+ *   context_lens  int32 [max_slots]       every slot's length after the step (0 if free)
+ *   slot_mapping  int64 [capacity]        pool row of each new row:
+ *                 table[c][p / block_size] * block_size + p % block_size
+ *   total_q       number of packed rows written to slot_mapping
+ * Errors: PKV_ERR_INVALID_ARG (slot not live, duplicate slot, negative n),
+ * PKV_ERR_OUT_OF_RANGE (slot beyond max_blocks_per_slot),
+ * PKV_ERR_WORKSPACE_TOO_SMALL (slot_mapping capacity), PKV_ERR_NO_BLOCKS.
+ * On error nothing changes.
+ */
+pkv_status pkv_plan_lower(pkv_pool *pool, const pkv_segment *plan, int32_t num_segments,
+                          int32_t *cu_seqlens_q, int32_t *seq_slot, int32_t *context_lens,
+                          int64_t *slot_mapping, int64_t slot_mapping_capacity,
+                          int64_t *total_q);
+
+/* ------------------------------------------------------------------------
+ * Attention work list (host side).
+ * Rows of a segment with one row go to the split-KV decode kernel: the
+ * segment's keys are cut into fixed spans of PKV_SPLIT_KEYS (the cut depends
+ * only on that segment's context, so a row's result does not depend on what
+ * else is in the batch), and a combine kernel merges spans in order.
+ * Segments with several rows (prompt chunks) go to the tensor-core chunk
+ * kernel, in tiles of query rows. The pages leave this split open; it is
+ * this library's design.
+ * ---------------------------------------------------------------------- */
+#define PKV_SPLIT_KEYS 512
+#define PKV_WORK_WORDS_PER_ITEM 4
+
+typedef struct pkv_work_info {
+    int32_t num_decode_items;  /* (segment, key span) items */
+    int32_t num_prefill_items; /* (segment, query tile) items */
+    int32_t num_combine_items; /* decode segments with more than one span */
+    int32_t num_partials;      /* span results kept in the workspace */
+    int64_t work_words;        /* int32 words of the item array */
+    uint64_t workspace_bytes;  /* device workspace pkv_attention needs (may be 0) */
+} pkv_work_info;
+
+/*
+ * Build the item array for a step from HOST copies of the step metadata
+ * (the same values later passed to pkv_attention on the device).
+ * Validates: cu_seqlens_q starts at 0 and never decreases; seq_slot in
+ * [0, max_slots) with no slot twice; every segment's rows <= its context
+ * length <= max_blocks_per_slot * block_size; supported head shape.
+ * `work` receives info->work_words int32 values; if `work_capacity` is too
+ * small (or `work` is NULL) the call fills `info` and returns
+ * PKV_ERR_WORKSPACE_TOO_SMALL, so it can size the array first.
+ */
+pkv_status pkv_plan_work(const int32_t *cu_seqlens_q, int32_t num_seqs,
+                         const int32_t *seq_slot, const int32_t *context_lens,
+                         int32_t max_slots, int32_t max_blocks_per_slot, int32_t block_size,
+                         int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                         int32_t *work, int64_t work_capacity, pkv_work_info *info);
+
+/* ------------------------------------------------------------------------
+ * Device calls.
+ * ---------------------------------------------------------------------- */
+
+/*
+ * Append new keys and values to the pool.
+ * [LB] §Chunked prefill is a slot phase: each selected chunk (and each
+ * decode row) appends directly to its slot's paged KV. [LB] §Paged KV and
+ * paged attention: the pool is fixed-size blocks addressed through tables.
+ *
+ *   k_new, v_new  bf16 [num_tokens][num_kv_heads][head_dim]   device
+ *   slot_mapping  int64 [num_tokens]  pool row per token; < 0 = skip   device
+ *   k_pool, v_pool bf16 [num_blocks][num_kv_heads][block_size][head_dim] device
+ * For token t with s = slot_mapping[t] >= 0, for every kv head h:
+ *   k_pool[s / block_size][h][s % block_size][:] = k_new[t][h][:]  (same for v)
+ * A bit-exact copy. Entries >= num_blocks * block_size are skipped and set
+ * PKV_DEV_BAD_SLOT_MAPPING. Two tokens naming one row race (undefined which
+ * wins); pkv_plan_lower never produces that. num_tokens == 0 launches nothing.
+ */
+pkv_status pkv_cache_write(const void *k_new, const void *v_new, const int64_t *slot_mapping,
+                           int64_t num_tokens, void *k_pool, void *v_pool, int64_t num_blocks,
+                           int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
+                           uint32_t *device_status, pkv_stream_t stream);
+
+/*
+ * Paged grouped-query attention over one packed step.
+ * [LB] §Paged KV and paged attention: attention reads each sequence's cached
+ * history by following its block table in logical order, directly over the
+ * shared pool. [LB] §Packing unequal prompt chunks together: per-query
+ * causal positions and block-table metadata let prompt and decode rows share
+ * one call. [LB] §Keeping track of each request: outputs follow the explicit
+ * row-to-slot map, so slot reuse moves no other sequence's state.
+ * [MX] §Paged KV cache and prefix sharing: a native block-table kernel in
+ * place of a gather.
+ *
+ * Device inputs:
+ *   q             bf16 [total_q][num_q_heads][head_dim]
+ *   cu_seqlens_q  int32 [num_seqs+1]   packed row offsets per segment
+ *   seq_slot      int32 [num_seqs]     slot of each segment
+ *   context_lens  int32 [max_slots]    per-slot length INCLUDING this step's rows
+ *   block_tables  int32 [max_slots][max_blocks_per_slot]
+ *   k_pool, v_pool bf16 [num_blocks][num_kv_heads][block_size][head_dim]
+ *   work          int32 [info->work_words]  pkv_plan_work's array, copied to the device
+ * Host inputs: info (from pkv_plan_work for the same metadata), shapes,
+ *   scale (<= 0 selects 1/sqrt(head_dim)).
+ * Output: out bf16 [total_q][num_q_heads][head_dim], in packed row order.
+ *
+ * Row i of segment s (n rows, slot c, L = context_lens[c]) sits at position
+ * p = L - n + i and attends keys 0..p of slot c; q head h reads kv head
+ * h / (num_q_heads / num_kv_heads). Softmax in fp32 with fp32 accumulation,
+ * output rounded to bf16 (nearest even). Results are deterministic and do
+ * not depend on the other segments in the step or on their order.
+ * `workspace` (device, >= info->workspace_bytes, 256-byte aligned) holds the
+ * key-span partial results; it needs no initialisation. The pool must
+ * already hold this step's rows (pkv_cache_write first, same stream).
+ */
+pkv_status pkv_attention(const void *q, const int32_t *cu_seqlens_q, int32_t num_seqs,
+                         int64_t total_q, const int32_t *seq_slot, const int32_t *context_lens,
+                         const int32_t *block_tables, int32_t max_slots,
+                         int32_t max_blocks_per_slot, int32_t block_size, const void *k_pool,
+                         const void *v_pool, int64_t num_blocks, int32_t num_q_heads,
+                         int32_t num_kv_heads, int32_t head_dim, float scale, const int32_t *work,
+                         const pkv_work_info *info, void *out, void *workspace,
+                         uint64_t workspace_bytes, uint32_t *device_status, pkv_stream_t stream);
+
+/*
+ * Synchronise `stream`, read *device_status (device memory), clear it, and
+ * map it to a status: PKV_OK if zero; PKV_ERR_DEVICE_TIMEOUT if the timeout
+ * bit is set; otherwise PKV_ERR_DEVICE_INDEX. `bits_out` (nullable, host)
+ * receives the raw bits. The only call that blocks the host.
+ */
+pkv_status pkv_check_device_status(uint32_t *device_status, pkv_stream_t stream,
+                                   uint32_t *bits_out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H_ */

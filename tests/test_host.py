@@ -1,0 +1,245 @@
+"""Host-side tests of libpkv (no GPU): exports, block pool, lowering, work list, scheduler.
+
+The library's host code is checked against the pages' worked examples and
+against the oracle (slot mapping recomputed independently; the scheduler's
+plans against the oracle's own replay of the same trace).
+"""
+
+import ctypes
+
+import numpy as np
+import pytest
+
+import oracle
+from continuous_batching_paged_pkv_gb300 import binding as B
+from continuous_batching_paged_pkv_gb300 import build as libbuild
+from continuous_batching_paged_pkv_gb300 import scheduler as S
+from continuous_batching_paged_pkv_gb300 import workloads as W
+from oracle import churn
+from tests.conftest import golden
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    libbuild.build()
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ctypes.CDLL(B.LIB_PATH)
+    names = B.declared_functions()
+    assert {"pkv_cache_write", "pkv_attention", "pkv_plan_lower", "pkv_plan_work"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/pkv.h but not exported"
+    assert B.pkv_version() > 0
+    assert B.pkv_status_string(7) == "not enough free KV blocks"
+
+
+# ---- block pool ---------------------------------------------------------------
+
+def test_pool_block_table_example_from_the_page():
+    """A [7,2,9,4], B [1,8], free [0,3,5,6]; B finishes; its blocks go to a new request; A stays."""
+    g = golden("block_table_example.json")
+    pool = B.Pool(10, 16, 3, 4)
+    pool.admit_blocks(0, g["tables"]["A"])
+    pool.admit_blocks(1, g["tables"]["B"])
+    assert pool.stats().free_blocks == len(g["free_pool"])
+    before = pool.block_tables()[0].copy()
+    pool.release(1)
+    assert pool.admit(2, 2 * 16) == B.PKV_OK
+    bt = pool.block_tables()
+    assert sorted(bt[2, :2]) == sorted(g["released_when_B_finishes"])
+    assert list(bt[2, :2]) == g["tables"]["B"]  # last released first block is on top
+    np.testing.assert_array_equal(bt[0], before)
+
+
+def test_pool_admission_is_all_or_nothing():
+    pool = B.Pool(8, 16, 4, 8)
+    assert pool.admit(0, 5 * 16) == B.PKV_OK
+    before = pool.block_tables().copy()
+    assert pool.admit(1, 4 * 16) == B.PKV_ERR_NO_BLOCKS
+    assert pool.stats().free_blocks == 3 and pool.slot_blocks(1) == -1
+    np.testing.assert_array_equal(pool.block_tables(), before)
+    assert pool.admit(1, 3 * 16) == B.PKV_OK
+    assert pool.stats().free_blocks == 0
+
+
+def test_pool_rejects_double_release_and_owned_blocks():
+    pool = B.Pool(8, 16, 2, 8)
+    pool.admit_blocks(0, [3, 5])
+    with pytest.raises(B.PkvError):
+        pool.admit_blocks(1, [5])
+    pool.release(0)
+    with pytest.raises(B.PkvError):
+        pool.release(0)
+
+
+def test_pool_each_block_owned_once():
+    rng = np.random.default_rng(0)
+    pool = B.Pool(200, 16, 16, 64, free_order=rng.permutation(200).astype(np.int32))
+    live = set()
+    for step in range(300):
+        slot = int(rng.integers(16))
+        if slot in live and rng.random() < 0.5:
+            pool.release(slot)
+            live.discard(slot)
+        elif slot not in live:
+            if pool.admit(slot, int(rng.integers(1, 400))) == B.PKV_OK:
+                live.add(slot)
+        bt = pool.block_tables()
+        used = bt[bt >= 0]
+        assert len(used) == len(set(used.tolist()))
+        st = pool.stats()
+        assert st.free_blocks + st.owned_blocks == 200
+
+
+# ---- lowering ----------------------------------------------------------------
+
+def test_lowering_packing_example_from_the_page():
+    g = golden("packing_example.json")
+    pool = B.Pool(1000, 16, 8, 64)
+    plan = []
+    for i, seg in enumerate(g["segments"]):
+        assert pool.admit(i, 600) == B.PKV_OK
+        if seg["kind"] == "decode":
+            pool.lower([(i, 30)])  # some history before the decode row
+        plan.append((i, seg["rows"]))
+    low = pool.lower(plan)
+    np.testing.assert_array_equal(np.diff(low.cu_seqlens_q), [s["rows"] for s in g["segments"]])
+    assert low.cu_seqlens_q[-1] == len(low.slot_mapping) == 1206
+    np.testing.assert_array_equal(low.seq_slot, np.arange(5))
+
+
+def _oracle_mapping(pool, plan, ctx_before):
+    segs = [(s, n, ctx_before[s] + n) for s, n in plan]
+    p = oracle.pack(segs)
+    return oracle.slot_mapping(pool.block_tables(), p.token_slot, p.token_pos, pool.block_size, pool.num_blocks)
+
+
+@pytest.mark.parametrize("bs", [16, 32, 64])
+def test_lowering_slot_mapping_matches_oracle(bs):
+    rng = np.random.default_rng(bs)
+    pool = B.Pool(4096, bs, 12, 128, free_order=rng.permutation(4096).astype(np.int32))
+    lens = {}
+    for slot in range(12):
+        assert pool.admit(slot, int(rng.integers(1, 300))) == B.PKV_OK
+        lens[slot] = 0
+    for step in range(25):
+        slots = rng.permutation(12)[: int(rng.integers(1, 12))]
+        plan = [(int(s), int(rng.integers(0, 70)) if rng.random() < 0.4 else 1) for s in slots]
+        before = dict(lens)
+        low = pool.lower(plan)
+        np.testing.assert_array_equal(low.slot_mapping, _oracle_mapping(pool, plan, before))
+        for s, n in plan:
+            lens[s] += n
+            assert low.context_lens[s] == lens[s] == pool.slot_length(s)
+        assert len(set(low.slot_mapping.tolist())) == len(low.slot_mapping)
+
+
+def test_lowering_grows_blocks_at_boundaries_and_is_all_or_nothing():
+    pool = B.Pool(4, 16, 2, 4)
+    assert pool.admit(0, 16) == B.PKV_OK and pool.admit(1, 16) == B.PKV_OK
+    pool.lower([(0, 16), (1, 15)])
+    assert pool.slot_blocks(0) == 1 and pool.stats().free_blocks == 2
+    pool.lower([(0, 1), (1, 1)])  # slot 0 opens block 1; slot 1 fills row 15
+    assert pool.slot_blocks(0) == 2 and pool.slot_blocks(1) == 1
+    with pytest.raises(B.PkvError) as e:
+        pool.lower([(0, 40), (1, 20)])  # needs 2 + 2 blocks, only 1 free
+    assert e.value.status == B.PKV_ERR_NO_BLOCKS
+    assert pool.slot_length(0) == 17 and pool.slot_length(1) == 16 and pool.stats().free_blocks == 1
+
+
+def test_lowering_rejects_bad_plans():
+    pool = B.Pool(64, 16, 4, 8)
+    assert pool.admit(0, 10) == B.PKV_OK
+    for plan in ([(0, 1), (0, 1)], [(1, 1)], [(9, 1)], [(0, -1)], [(0, 200)]):
+        with pytest.raises(B.PkvError):
+            pool.lower(plan)
+    assert pool.slot_length(0) == 0
+
+
+# ---- work list ---------------------------------------------------------------
+
+def _work(cu, slots, ctx, **kw):
+    args = dict(max_slots=8, max_blocks_per_slot=64, block_size=16, num_q_heads=32, num_kv_heads=8, head_dim=128)
+    args.update(kw)
+    return B.pkv_plan_work(np.array(cu), np.array(slots), np.array(ctx), **args)
+
+
+def test_work_list_items():
+    ctx = np.zeros(8, np.int32)
+    ctx[[3, 1, 6, 2]] = [1536, 513, 512, 1]
+    work, info = _work([0, 512, 513, 514, 515], [3, 1, 6, 2], ctx, max_blocks_per_slot=128)
+    assert (info.num_decode_items, info.num_prefill_items, info.num_combine_items) == (4, 16, 1)
+    items = work.reshape(-1, 4)
+    dec, pre, comb = items[:4], items[4:20], items[20:]
+    assert sorted(map(tuple, dec[:, :3].tolist())) == [(1, 1, 0), (1, 1, 1), (2, 6, 0), (3, 2, 0)]
+    assert list(dec[0, :2]) in ([1, 1], [2, 6])       # full 512-key spans first
+    assert list(dec[-1, :3]) == [3, 2, 0]              # the 1-key span last
+    assert list(comb[0]) == [1, 1, 2, 0] and info.num_partials == 2
+    assert sorted(pre[:, 2].tolist()) == list(range(16)) and (pre[:, :2] == [0, 3]).all()
+    assert pre[0, 2] == 15  # the tile that sees the most keys first
+    assert info.workspace_bytes == 2 * 32 * 128 * 4 + 2 * 32 * 2 * 4
+
+
+@pytest.mark.parametrize("cu,slots,ctx_pairs,err", [
+    ([0, 5], [0], {0: 4}, B.STATUS_NAMES[1]),            # rows > context
+    ([0, 1, 2], [1, 1], {1: 9}, B.STATUS_NAMES[1]),      # duplicate slot
+    ([0, 1], [9], {}, B.STATUS_NAMES[2]),                # slot out of range
+    ([1, 2], [0], {0: 3}, B.STATUS_NAMES[1]),            # cu does not start at 0
+    ([0, 1], [0], {0: 64 * 16 + 1}, B.STATUS_NAMES[2]),  # context beyond the table
+])
+def test_work_list_validation(cu, slots, ctx_pairs, err):
+    ctx = np.zeros(8, np.int32)
+    for k, v in ctx_pairs.items():
+        ctx[k] = v
+    with pytest.raises(B.PkvError, match=err):
+        _work(cu, slots, ctx)
+
+
+def test_work_list_unsupported_shapes():
+    ctx = np.array([5] + [0] * 7, np.int32)
+    for kw in (dict(head_dim=96), dict(block_size=8), dict(num_q_heads=34 * 8, num_kv_heads=8)):
+        with pytest.raises(B.PkvError, match="UNSUPPORTED"):
+            _work([0, 1], [0], ctx, **kw)
+
+
+# ---- scheduler vs the oracle's replay -------------------------------------------
+
+def _compare_trace(reqs, spec_steps, num_blocks, max_slots, bs=16):
+    pool = B.Pool(num_blocks, bs, max_slots, 1024, free_order=W.churn_free_order(0, num_blocks))
+    sch = S.ChurnScheduler(reqs, pool)
+    ref = churn.ChurnReplay(reqs, max_slots=max_slots, num_blocks=num_blocks, block_size=bs)
+    for step in range(spec_steps):
+        rows = sch.plan()
+        want = ref.plan()
+        assert [(r.rid, r.begin, r.n, r.prefill) for r in rows] == \
+               [(r.rid, r.begin, r.n, r.prefill) for r in want], f"step {step}"
+        low = pool.lower([(r.slot, r.n) for r in rows])
+        assert len(low.slot_mapping) == sum(r.n for r in rows)
+        assert sch.commit(rows) == ref.commit(want)
+        assert pool.stats().free_blocks == ref.free_blocks
+    return sch
+
+
+def test_scheduler_matches_oracle_replay_on_churn_trace():
+    spec = W.ChurnSpec(num_steps=120)
+    reqs = W.churn_trace(0, spec)
+    sch = _compare_trace(reqs, 120, spec.num_blocks, spec.max_slots)
+    assert sch.step_index == 120
+
+
+def test_scheduler_matches_oracle_under_pool_pressure():
+    """Small pool: admission is limited by KV capacity, FIFO head-of-line blocking shows up."""
+    spec = W.ChurnSpec(num_steps=80, prompt_max=3000)
+    reqs = W.churn_trace(3, spec)
+    _compare_trace(reqs, 80, 900, 16)
+
+
+def test_scheduler_fifo_example_from_the_page():
+    g = golden("fifo_admission_example.json")
+    d_tokens = g["queue"][0]["blocks"] * 16 - 1
+    e_tokens = g["queue"][1]["blocks"] * 16 - 1
+    reqs = [W.Request(0, 0, d_tokens, 1), W.Request(1, 0, e_tokens, 1)]
+    pool = B.Pool(g["free_blocks"], 16, 4, 200)
+    sch = S.ChurnScheduler(reqs, pool)
+    assert sch.plan() == [] and len(sch.queue) == 2 and pool.stats().free_blocks == g["free_blocks"]
