@@ -1,0 +1,480 @@
+#!/usr/bin/env python
+"""Benchmark of one paged-KV attention step (cache write + attention) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload decode5|mixed|decode256|tiny]
+
+Prints one JSON line. The default workload is one decode step for five
+clients (40 q / 8 kv heads, head_dim 128, block 16, contexts U[1024, 8192],
+65,536-block pool). Metric: KV bytes the attention must read (each sequence's
+K and V once per kv head, plus Q in and O out) per second of device time.
+
+Timing: W untimed warm-up steps, then K timed steps. Before each step a
+256 MiB buffer is overwritten (larger than the 129 MB L2) so no step finds its
+K/V in L2, and a second 256 MiB buffer is then read so that L2 holds clean
+lines (otherwise the flush's dirty lines would be written back to HBM inside
+the timed step). Both are outside the CUDA events that bracket the step. Each
+library call is bracketed by its own events on the launching stream, so the
+attention kernel's own duration is known. Under torchrun (N > 1) every rank
+runs an independent replica (the step has no exchange between GPUs); the
+job's time is the maximum over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged-attn KV GB/s & % of HBM peak; step rows/s (decode + prefill mix)"
+L2_FLUSH_BYTES = 256 << 20
+
+
+class L2Flush:
+    """Write a buffer larger than L2, then read another one (clean lines)."""
+
+    def __init__(self, device):
+        import torch
+
+        self.dirty = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+        self.clean = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+        self.sink = torch.empty((), dtype=torch.float32, device=device)
+
+    def __call__(self):
+        self.dirty.zero_()
+        self.sink.copy_(self.clean.sum())
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+WORKLOAD_TEXT = {
+    "decode5": "decode step, 5 slots x 1 row, 40 q / 8 kv heads, head_dim 128, block 16, "
+               "contexts U[1024, 8192], 65,536-block pool",
+    "mixed": "mixed step, one 512-row prompt chunk at offset 1024 of a 3000-token prompt + 4 decode rows "
+             "(contexts U[200, 4000]), 32 q / 8 kv heads, head_dim 128, block 16, 65,536-block pool",
+    "decode256": "decode step, 256 slots x 1 row, 64 q / 8 kv heads, head_dim 128, block 16, "
+                 "lognormal contexts (median 2048, clip [16, 32768]), fragmented 131,072-block pool",
+    "tiny": "tiny mixed step, 4 q / 2 kv heads, head_dim 64, block 16, 32 blocks",
+}
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=4000)
+    p.add_argument("--warmup", type=int, default=50)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", choices=sorted(WORKLOAD_TEXT), default="decode5")
+    p.add_argument("--seed", type=int, default=0)
+    p.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle CPU-baseline budget")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--e2e-steps", type=int, default=300)
+    p.add_argument("--pool-blocks", type=int, default=None,
+                   help="smaller synthetic pool (same contexts) for profiling captures")
+    return p.parse_args(argv)
+
+
+# ---------------------------------------------------------------------------
+# Work accounting (from the workload's shapes only).
+# ---------------------------------------------------------------------------
+
+def kv_bytes(w) -> int:
+    """Algorithmic bytes of the attention: K and V of every visible key once per kv head, Q in, O out."""
+    kv = sum(s.ctx for s in w.segments) * w.num_kv_heads * w.head_dim * 2 * 2
+    return kv + w.total_q * w.num_q_heads * w.head_dim * 2 * 2
+
+
+def write_bytes(w) -> int:
+    return w.total_q * w.num_kv_heads * w.head_dim * 2 * 2 * 2  # K+V read and written
+
+
+def chunk_flops(w) -> int:
+    """Causal-only flops of the prompt-chunk rows: 4 * D * Hq * sum over rows of visible keys."""
+    tot = 0
+    for s in w.segments:
+        if s.q_len > 1:
+            first = s.ctx - s.q_len + 1
+            tot += s.q_len * first + s.q_len * (s.q_len - 1) // 2
+    return 4 * w.head_dim * w.num_q_heads * tot
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def profiled_traffic(kernel_file: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel source is unchanged since."""
+    src = os.path.join(ROOT, "continuous_batching_paged_pkv_gb300", "csrc", kernel_file)
+    summary = os.path.join(ROOT, "profiles", f"{os.path.splitext(kernel_file)[0]}_{workload}.md")
+    try:
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        for line in open(summary):
+            if line.startswith("TRAFFIC "):
+                fields = dict(kv.split("=", 1) for kv in line.split()[1:])
+                if fields.get("source_sha") == sha:
+                    return int(fields["bytes_per_launch"])
+    except OSError:
+        pass
+    return None
+
+
+# ---------------------------------------------------------------------------
+# Clocks during the timed region.
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+        if self.gpu_id:
+            cmd += ["-i", self.gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.4)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.3)
+        self.proc.terminate()
+        self.proc.wait(timeout=10)
+        rows = [r.split(", ") for r in open(self.path).read().strip().splitlines() if r.strip()]
+        os.unlink(self.path)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+            except (ValueError, IndexError):
+                continue
+            for nm, val in zip(names, r[5:9]):
+                if val.strip() == "Active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# Multi-rank plumbing (replicas: one independent step per GPU).
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), \
+        int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def aggregate(local_ms: float, local_units: float, world: int):
+    """Max time over ranks, units summed over ranks (every rank does the same work)."""
+    if world == 1:
+        return local_ms, local_units
+    import torch
+    import torch.distributed as dist
+
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([local_ms], dtype=torch.float64, device=dev)
+    u = torch.tensor([local_units], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# CPU baseline: the oracle as it stands, on the host's cores.
+# ---------------------------------------------------------------------------
+
+def cpu_baseline(w, seconds: float, rows_per_run=None):
+    import oracle
+
+    oracle.build()
+    cores = oracle.default_threads()
+    st = oracle.prepare_step(w)
+    seg_rows = []
+    start = 0
+    for s in w.segments:
+        seg_rows.append((start, s))
+        start += s.q_len
+    done_bytes, runs = 0, 0
+    t0 = time.perf_counter()
+    while True:
+        if rows_per_run is None:
+            oracle.step_attention(w, st, threads=cores)
+            done_bytes += kv_bytes(w)
+        else:
+            r0, s = seg_rows[runs % len(seg_rows)]
+            oracle.step_attention(w, st, rows=list(range(r0, r0 + s.q_len)), threads=cores)
+            done_bytes += s.ctx * w.num_kv_heads * w.head_dim * 4 + s.q_len * w.num_q_heads * w.head_dim * 4
+        runs += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return {"value": done_bytes / el / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{runs} run(s) of the oracle over " +
+                      ("the whole step" if rows_per_run is None else "one segment at a time, in turn") +
+                      f" in {el:.1f} s (fp64, {cores} threads)"}
+
+
+# ---------------------------------------------------------------------------
+# Arms.
+# ---------------------------------------------------------------------------
+
+def run_reference(args, rank, world):
+    """The oracle timed on the host as the reference arm (rank 0 only)."""
+    if rank != 0:
+        return None
+    from continuous_batching_paged_pkv_gb300 import workloads as W
+    import oracle
+
+    oracle.build()
+    w = W.make_step(args.workload, args.seed)
+    st = oracle.prepare_step(w)
+    cores = oracle.default_threads()
+    segs, start = [], 0
+    for s in w.segments:
+        segs.append((start, s))
+        start += s.q_len
+    # Each step is one segment of the workload (rotating), so K steps stay bounded.
+    def one(i):
+        r0, s = segs[i % len(segs)]
+        oracle.step_attention(w, st, rows=list(range(r0, r0 + s.q_len)), threads=cores)
+        return s.ctx * w.num_kv_heads * w.head_dim * 4 + s.q_len * w.num_q_heads * w.head_dim * 4
+
+    for i in range(args.warmup):
+        one(i)
+    total_b, t0 = 0, time.perf_counter()
+    for i in range(args.steps):
+        total_b += one(i)
+    el = time.perf_counter() - t0
+    val = total_b / el / 1e9
+    return {"metric": METRIC, "value": val, "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": el * 1e3 / max(args.steps, 1), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{args.workload}: {WORKLOAD_TEXT[args.workload]}",
+                       "sample": "one segment of the step per timed step, rotating"},
+            "impl": "reference",
+            "cpu_baseline": {"value": val, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                             "sample": f"{args.steps} steps of one segment each, fp64, {cores} threads"},
+            "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def run_ours(args, rank, world, local_rank):
+    import numpy as np
+    import torch
+
+    from continuous_batching_paged_pkv_gb300 import binding as B
+    from continuous_batching_paged_pkv_gb300 import build as libbuild
+    from continuous_batching_paged_pkv_gb300 import runtime as R
+    from continuous_batching_paged_pkv_gb300 import workloads as W
+
+    libbuild.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    w = W.make_step(args.workload, args.seed, pool_blocks=args.pool_blocks)
+    ds = R.prepare(w, dev)
+    stream = torch.cuda.current_stream()
+    flush = L2Flush(dev)
+    launches_per_step = int(w.total_q > 0) + int(ds.info.num_decode_items > 0) + int(ds.info.num_prefill_items > 0)
+
+    for _ in range(args.warmup):
+        flush()
+        R.run_step(ds)
+    torch.cuda.synchronize()
+    if B.pkv_check_device_status(ds.status) != 0:
+        raise RuntimeError("device status reported an error during warm-up")
+
+    props = torch.cuda.get_device_properties(dev)
+    uuid = str(getattr(props, "uuid", "")) or None
+    clocks = ClockSampler(("GPU-" + uuid) if uuid and not uuid.startswith("GPU-") else uuid)
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    step_ms, write_ms, attn_ms = [], [], []
+    chunk = 500
+    done = 0
+    while done < args.steps:
+        n = min(chunk, args.steps - done)
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+        for e0, e1, e2 in ev:
+            flush()
+            e0.record(stream)
+            R.run_cache_write(ds)
+            e1.record(stream)
+            R.run_attention(ds)
+            e2.record(stream)
+        torch.cuda.synchronize()
+        for e0, e1, e2 in ev:
+            write_ms.append(e0.elapsed_time(e1))
+            attn_ms.append(e1.elapsed_time(e2))
+            step_ms.append(e0.elapsed_time(e2))
+        done += n
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    if B.pkv_check_device_status(ds.status) != 0:
+        raise RuntimeError("device status reported an error during the timed steps")
+
+    total_ms, total_bytes = aggregate(sum(step_ms), kv_bytes(w) * args.steps, world)
+    hbm, tflops, peak_src = peaks()
+    value = total_bytes / (total_ms / 1e3) / 1e9
+    attn_mean = sum(attn_ms) / len(attn_ms)
+    achieved = kv_bytes(w) / (attn_mean / 1e3) / 1e9
+    res = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{args.workload}: {WORKLOAD_TEXT[args.workload]}",
+                   "rows_per_step": w.total_q, "kv_bytes_per_step": kv_bytes(w),
+                   "l2": "flushed before every step: 256 MiB written, then 256 MiB read so L2 holds clean lines; "
+                         "both outside the timed events",
+                   "parallelism": f"replicas x{world} (no exchange between GPUs)", "seed": args.seed,
+                   "pool_blocks": w.num_blocks},
+        "pct_hbm_peak": 100.0 * value / world / hbm,
+        "rows_per_s": world * w.total_q / (total_ms / args.steps / 1e3),
+        "step_breakdown_ms": {"cache_write": statistics.median(write_ms), "attention": statistics.median(attn_ms),
+                              "step": statistics.median(step_ms)},
+    }
+    if ds.info.num_prefill_items and ds.info.num_decode_items:
+        bound, unit, kernel = "hbm", "GB/s", "attention call (chunk + decode kernels)"
+    elif ds.info.num_prefill_items:
+        bound, unit, kernel = "tensor", "TFLOP/s", "prefill_kernel"
+    else:
+        bound, unit, kernel = "hbm", "GB/s", "decode_kernel"
+    if bound == "tensor":
+        ach = chunk_flops(w) / (attn_mean / 1e3) / 1e12
+        res["roofline"] = {"bound": "tensor", "kernel": kernel, "achieved": ach, "peak": tflops,
+                           "unit": "TFLOP/s", "frac": ach / tflops, "traffic": None,
+                           "peak_source": f"{peak_src} bf16 burst"}
+    else:
+        traffic = profiled_traffic("pkv_decode.cu", args.workload) if kernel == "decode_kernel" else None
+        res["roofline"] = {"bound": "hbm", "kernel": kernel, "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                           "frac": achieved / hbm, "traffic": traffic,
+                           "algorithmic_bytes_per_launch": kv_bytes(w), "mean_launch_ms": attn_mean,
+                           "peak_source": f"{peak_src} HBM copy bandwidth"}
+    if chunk_flops(w):
+        res["chunk_tflops"] = chunk_flops(w) / (attn_mean / 1e3) / 1e12
+    res["gpu_launches"] = launches_per_step * args.steps
+    res["clocks"] = clk
+
+    # ---- end to end through the C ABI, inputs from pinned host memory ----
+    e2e = run_e2e(args, w, ds, dev, flush)
+    if e2e:
+        e_ms, e_units = aggregate(e2e["ms_total"], kv_bytes(w) * e2e["steps"], world)
+        res["e2e"] = {"value": e_units / (e_ms / 1e3) / 1e9, "unit": "GB/s",
+                      "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
+                      "steps": e2e["steps"], "ms_per_step": e_ms / e2e["steps"],
+                      "timed": "wall clock per step: work list on the host, H2D copies, cache write, "
+                               "attention, D2H of the output, stream synchronised"}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+    res["impl"] = "ours"
+    return res
+
+
+def run_e2e(args, w, ds, dev, flush):
+    import numpy as np
+    import torch
+
+    from continuous_batching_paged_pkv_gb300 import binding as B
+
+    if args.e2e_steps <= 0:
+        return None
+    low = ds.lowered
+    bt = ds.pool.block_tables()
+
+    def pinned(a, dtype):
+        t = torch.from_numpy(np.ascontiguousarray(a).view(dtype)).pin_memory()
+        return t
+
+    h = {
+        "q": pinned(w.q, np.int16), "k": pinned(w.new_k(), np.int16), "v": pinned(w.new_v(), np.int16),
+        "sm": pinned(low.slot_mapping.astype(np.int64), np.int64), "cu": pinned(low.cu_seqlens_q, np.int32),
+        "ss": pinned(low.seq_slot, np.int32), "cl": pinned(low.context_lens, np.int32), "bt": pinned(bt, np.int32),
+    }
+    d = {k: torch.empty_like(v, device=dev) for k, v in h.items()}
+    work_dev = torch.empty_like(ds.work)
+    out_host = torch.empty(ds.out.shape, dtype=torch.bfloat16).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in h.values()) + ds.work.numel() * 4
+    d2h = out_host.numel() * 2
+    stream = torch.cuda.current_stream()
+    times = []
+    for i in range(args.e2e_steps + 5):
+        flush()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        work, info = B.pkv_plan_work(low.cu_seqlens_q, low.seq_slot, low.context_lens, max_slots=w.max_slots,
+                                     max_blocks_per_slot=w.max_blocks_per_slot, block_size=w.block_size,
+                                     num_q_heads=w.num_q_heads, num_kv_heads=w.num_kv_heads, head_dim=w.head_dim)
+        wh = torch.from_numpy(work)
+        for k in h:
+            d[k].copy_(h[k], non_blocking=True)
+        work_dev.copy_(wh, non_blocking=True)
+        B.pkv_cache_write(d["k"].view(torch.bfloat16), d["v"].view(torch.bfloat16), d["sm"], ds.k_pool, ds.v_pool,
+                          device_status=ds.status)
+        B.pkv_attention(d["q"].view(torch.bfloat16), d["cu"], d["ss"], d["cl"], d["bt"], ds.k_pool, ds.v_pool,
+                        work_dev, info, ds.out, ds.workspace, scale=w.scale, device_status=ds.status)
+        out_host.copy_(ds.out, non_blocking=True)
+        stream.synchronize()
+        if i >= 5:
+            times.append((time.perf_counter() - t0) * 1e3)
+    return {"ms_total": sum(times), "steps": len(times), "h2d": h2d, "d2h": d2h}
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    rank, world, local_rank = dist_env()
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if args.impl == "reference":
+            backend = "gloo"
+        dist.init_process_group(backend=backend)
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+    else:
+        res = run_ours(args, rank, world, local_rank)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -29,7 +29,7 @@ STATUS_NAMES = {
 }
 PKV_ERR_WORKSPACE_TOO_SMALL = 4
 PKV_ERR_NO_BLOCKS = 7
-PKV_SPLIT_KEYS = 512
+PKV_SPLIT_KEYS = 256
 PKV_WORK_WORDS_PER_ITEM = 4
 
 

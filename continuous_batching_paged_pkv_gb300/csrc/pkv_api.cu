@@ -112,7 +112,8 @@ pkv_status pkv_attention(const void *q, const int32_t *cu_seqlens_q, int32_t num
       !aligned(work, 16))
     return PKV_ERR_INVALID_ARG;
   const uint64_t acc_bytes = align256(uint64_t(info->num_partials) * num_q_heads * head_dim * 4);
-  const uint64_t need = info->num_partials == 0 ? 0 : acc_bytes + align256(uint64_t(info->num_partials) * num_q_heads * 8);
+  const uint64_t ml_bytes = align256(uint64_t(info->num_partials) * num_q_heads * 8);
+  const uint64_t need = info->num_partials == 0 ? 0 : acc_bytes + ml_bytes;
   if (need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 256)))
     return PKV_ERR_WORKSPACE_TOO_SMALL;
   if ((info->num_combine_items > 0) != (info->num_partials > 0)) return PKV_ERR_INVALID_ARG;
@@ -154,7 +155,7 @@ pkv_status pkv_attention(const void *q, const int32_t *cu_seqlens_q, int32_t num
   const int32_t *comb = pre + static_cast<int64_t>(info->num_prefill_items) * PKV_WORK_WORDS_PER_ITEM;
   cudaError_t e = pkv::launch_prefill(a, tq, tk, tv, rpt, info->num_prefill_items, pre, st);
   if (e == cudaSuccess) e = pkv::launch_decode(a, tk, tv, info->num_decode_items, dec, st);
-  if (e == cudaSuccess) e = pkv::launch_combine(a, info->num_combine_items, comb, st);
+  if (e == cudaSuccess) e = pkv::launch_merge(a, info->num_combine_items, comb, st);
   return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 

@@ -1,4 +1,4 @@
-// Split-KV decode attention and the span combine.
+// Split-KV decode attention (persistent warps) and the span merge.
 //
 // Lucebox, "Continuous batching: Qwen3.8-27B at 301 tok/s across five
 // clients, up to 1.97x llama.cpp", §Paged KV and paged attention: attention
@@ -7,23 +7,35 @@
 // batched paged decode reads blocks in place (a block-table kernel) instead
 // of rebuilding a contiguous window every step.
 //
-// Work: one CTA per (decode segment, key span of PKV_SPLIT_KEYS keys, kv head).
-// The span is cut into 16-key sub-tiles; warp w takes sub-tiles w, w+4, ...
-// Each warp keeps its own 3-stage ring in shared memory: lane 0 issues two TMA
-// boxes (64 columns x 16 rows, 128-byte swizzle) per half of head_dim for K
-// and V of the next sub-tile, straight from the pool row the block table
-// names. The math is warp-level bf16 MMA (m16n8k16) with fp32 accumulation:
+// Decode kernel. A task is one (decode segment, key span of PKV_SPLIT_KEYS
+// keys, kv head). The grid is one CTA per SM with eight warps; every warp is
+// an independent worker taking tasks t = w, w + W, w + 2W, ... (W = all warps;
+// the work list is sorted longest first and consecutive tasks go to different
+// SMs). A warp streams its tasks' 16-key K/V sub-tiles through its own
+// three-stage ring in shared memory with TMA (64-column x 16-row boxes,
+// 128-byte swizzle) straight from the pool rows the block table names. The
+// ring keeps flowing across task boundaries: the next task's metadata and
+// block IDs load while the current task computes, and its first sub-tiles are
+// requested before the current task ends. Eight warps x three 8 KiB stages
+// keep ~192 KiB of K/V in flight per SM, enough to cover HBM latency.
+//
+// Math per sub-tile: warp-level bf16 MMA (m16n8k16), fp32 accumulation,
 //   S^T[16 keys][8 heads] = K[16 keys][D] * Q^T[D][8 heads]   (GQA group on N)
 //   O^T[D][8 heads]      += V^T[D][16 keys] * P^T[16 keys][8 heads]
-// with an online softmax per head in the exp2 domain. P^T reaches the B
-// operand of the second MMA through an in-register 8x8 transpose (movmatrix).
-// The four warps merge in a fixed order; spans merge in span order in the
-// combine kernel. Nothing depends on timing or on the other segments, so the
-// result is deterministic and independent of batch composition.
+// with an online softmax per head in the exp2 domain; P^T reaches the second
+// MMA's B operand through an in-register 8x8 transpose (movmatrix). The
+// running output is rescaled only when a head's max grows by more than 2^8.
 //
-// Keys past the context in a partially filled block are masked to -inf in S
-// and their V values are zeroed in registers, so stale or NaN pool rows never
-// reach the output.
+// A single-span segment's result goes straight to the output; otherwise each
+// span writes a partial (unnormalised sum, reference max, denominator) and the
+// merge kernel, launched right behind the decode kernel (programmatic
+// dependent launch), combines the spans of each (segment, q head) in a fixed
+// order. Nothing depends on timing or on other segments: results are
+// deterministic and independent of the rest of the batch.
+//
+// Keys past the context in a partly filled block are masked to -inf in S and
+// their V values zeroed in registers, so stale or NaN pool rows never reach
+// the output.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -34,359 +46,544 @@
 namespace pkv {
 namespace {
 
-constexpr int kWarps = 4;
-constexpr int kStages = 3;
+constexpr int kWarps = 8;  // independent workers per CTA
+constexpr uint32_t kFull = 0xffffffffu;
+constexpr float kRescale = 8.0f;  // log2 units
 
 template <int D>
-struct DecodeLayout {
+struct DecodeCfg {
   static constexpr int kHalves = D / 64;
-  static constexpr int kHalfBytes = kSubKeys * 128;           // 16 rows x 128 B
-  static constexpr int kTileBytes = kHalves * kHalfBytes;     // one K (or V) sub-tile
-  static constexpr int kStageBytes = 2 * kTileBytes;          // K then V
-  static constexpr int kRingBytes = kWarps * kStages * kStageBytes;
+  static constexpr int kHalfBytes = kSubKeys * 128;        // 16 rows x 128 B
+  static constexpr int kTileBytes = kHalves * kHalfBytes;  // one K (or V) sub-tile
+  static constexpr int kStageBytes = 2 * kTileBytes;       // K then V
+  static constexpr int kStages = (24 * 1024) / kStageBytes;  // 3 (D=128) or 6 (D=64)
+  static constexpr int kWarpRing = kStages * kStageBytes;
+  static constexpr int kSmem = kWarps * kWarpRing + kWarps * kStages * 8 + 1024;
 };
-
-template <int NT>
-__host__ __device__ constexpr int merge_bytes(int d) {
-  return kWarps * 8 * NT * d * 4;
-}
-
-template <int D, int NT>
-constexpr int decode_smem_bytes() {
-  constexpr int ring = DecodeLayout<D>::kRingBytes;
-  constexpr int merge = merge_bytes<NT>(D);
-  constexpr int body = ring > merge ? ring : merge;
-  // + barriers + per-warp (m, l) + 1 KiB for manual 1024-byte alignment
-  return body + kWarps * kStages * 8 + 2 * kWarps * 8 * NT * 4 + 1024;
-}
 
 __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
   return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
-__device__ __forceinline__ void store_bf16(void *out, size_t idx, float x) {
-  reinterpret_cast<__nv_bfloat16 *>(out)[idx] = __float2bfloat16_rn(x);
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// One task's metadata. Scalars are uniform across the warp; `bid` is per lane:
+// the physical block of the task's sub-tile number `lane`.
+struct Task {
+  int t;  // task index, -1 if none
+  int seg, slot, span, pbase, g;
+  int row0, row1, L, sslot;
+  int key0, key1, units;
+  int bid;  // per lane: block of sub-tile `lane`
+  int row;  // per lane: tensor-map row of sub-tile `lane`, -1 if its block ID is outside the pool
+  bool raw_ok, finalized, ok;
+};
+
+__device__ __forceinline__ int4 load_item(const int32_t *items, int t, int hkv) {
+  return __ldg(reinterpret_cast<const int4 *>(items) + t / hkv);
 }
 
-__device__ __forceinline__ float bf16_round(float x) {
-  return __bfloat162float(__float2bfloat16_rn(x));
+// Issue every load the task needs; nothing here waits for a result.
+__device__ __forceinline__ void expand(Task &T, int t, int4 raw, const StepArgs &a, int lane) {
+  T.t = t;
+  T.finalized = false;
+  T.ok = false;
+  T.units = 0;
+  T.bid = 0;
+  T.row = -1;
+  if (t < 0) return;
+  T.seg = raw.x;
+  T.slot = raw.y;
+  T.span = raw.z;
+  T.pbase = raw.w;
+  T.g = t % a.num_kv_heads;
+  T.key0 = T.span * PKV_SPLIT_KEYS;
+  T.raw_ok = T.seg >= 0 && T.seg < a.num_seqs && T.slot >= 0 && T.slot < a.max_slots && T.span >= 0;
+  if (!T.raw_ok) return;
+  T.row0 = __ldg(a.cu_seqlens_q + T.seg);
+  T.row1 = __ldg(a.cu_seqlens_q + T.seg + 1);
+  T.L = __ldg(a.context_lens + T.slot);
+  T.sslot = __ldg(a.seq_slot + T.seg);
+  const int64_t key = static_cast<int64_t>(T.key0) + lane * kSubKeys;
+  if (lane * kSubKeys < PKV_SPLIT_KEYS && key < static_cast<int64_t>(a.max_blocks_per_slot) * a.block_size)
+    T.bid = __ldg(a.block_tables + static_cast<int64_t>(T.slot) * a.max_blocks_per_slot + key / a.block_size);
+}
+
+// Check the metadata against the work item and derive the key range.
+__device__ __forceinline__ void finalize(Task &T, const StepArgs &a, int lane) {
+  if (T.finalized) return;
+  T.finalized = true;
+  if (T.t < 0) return;
+  T.ok = T.raw_ok && T.sslot == T.slot && T.row1 - T.row0 == 1 && T.L >= 1 &&
+         static_cast<int64_t>(T.L) <= static_cast<int64_t>(a.max_blocks_per_slot) * a.block_size &&
+         T.key0 < T.L && T.row0 >= 0 && T.row0 < a.total_q;
+  if (!T.ok) {
+    if (lane == 0 && a.status) atomicOr(a.status, PKV_DEV_BAD_SEGMENT);
+    return;
+  }
+  T.key1 = min(T.L, T.key0 + PKV_SPLIT_KEYS);
+  T.units = (T.key1 - T.key0 + kSubKeys - 1) / kSubKeys;
+  const bool in_pool = T.bid >= 0 && T.bid < a.num_blocks;
+  T.row = in_pool ? (T.bid * a.num_kv_heads + T.g) * a.block_size + (T.key0 + lane * kSubKeys) % a.block_size : -1;
+  if (lane < T.units && !in_pool && a.status) atomicOr(a.status, PKV_DEV_BAD_BLOCK);
+}
+
+// Q^T fragments (B operand): head = nt*8 + lane/4, d = kk*16 + (lane%4)*2 (+8).
+template <int D, int NT>
+__device__ __forceinline__ void load_q(uint32_t (&qf)[NT][D / 16][2], const Task &T, const StepArgs &a,
+                                       int lane) {
+  const uint16_t *qrow = static_cast<const uint16_t *>(a.q) +
+                         (static_cast<size_t>(T.row0) * a.num_q_heads + T.g * a.group) * D;
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int head = nt * 8 + (lane >> 2);
+    const uint32_t *qp = reinterpret_cast<const uint32_t *>(qrow + head * D) + (lane & 3);
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      qf[nt][kk][0] = head < a.group ? __ldg(qp + kk * 8) : 0u;
+      qf[nt][kk][1] = head < a.group ? __ldg(qp + kk * 8 + 4) : 0u;
+    }
+  }
 }
 
 template <int D, int NT>
-__global__ void __launch_bounds__(128) decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
-                                                     const __grid_constant__ CUtensorMap tmap_v,
-                                                     const StepArgs a,
-                                                     const int32_t *__restrict__ items) {
-  using Lay = DecodeLayout<D>;
+__global__ void __launch_bounds__(kWarps * 32, 1)
+    decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
+                  const StepArgs a, const int32_t *__restrict__ items, int num_items) {
+  using Cfg = DecodeCfg<D>;
   constexpr int KT = D / 16;  // k-steps of QK^T, m-tiles of PV
+  constexpr int NST = Cfg::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = align1024(smem_raw);
-  constexpr int kBody = Lay::kRingBytes > merge_bytes<NT>(D) ? Lay::kRingBytes : merge_bytes<NT>(D);
-  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kBody);
-  float *red_m = reinterpret_cast<float *>(bars + kWarps * kStages);
-  float *red_l = red_m + kWarps * 8 * NT;
-
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = blockIdx.y;
-  const int4 it = reinterpret_cast<const int4 *>(items)[blockIdx.x];
-  const int seg = it.x, slot = it.y, span = it.z, pbase = it.w;
+  uint8_t *ring = smem + warp * Cfg::kWarpRing;
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + kWarps * Cfg::kWarpRing) + warp * NST;
 
-  // ---- segment metadata (uniform across the CTA) ----
-  bool bad = seg < 0 || seg >= a.num_seqs || slot < 0 || slot >= a.max_slots;
-  int row0 = 0, L = 0;
-  if (!bad) {
-    row0 = a.cu_seqlens_q[seg];
-    const int n = a.cu_seqlens_q[seg + 1] - row0;
-    L = a.context_lens[slot];
-    bad = a.seq_slot[seg] != slot || n != 1 || L < 1 ||
-          static_cast<int64_t>(L) > static_cast<int64_t>(a.max_blocks_per_slot) * a.block_size ||
-          span * PKV_SPLIT_KEYS >= L || row0 < 0 || row0 >= a.total_q;
-  }
-  if (bad) {
-    if (threadIdx.x == 0 && a.status) atomicOr(a.status, PKV_DEV_BAD_SEGMENT);
-    return;
-  }
-  const int key0 = span * PKV_SPLIT_KEYS;
-  const int key1 = min(L, key0 + PKV_SPLIT_KEYS);
-  const int units = (key1 - key0 + kSubKeys - 1) / kSubKeys;
-  const int my_units = units > warp ? (units - warp + kWarps - 1) / kWarps : 0;
-
-  // Lane i holds the physical block of this warp's i-th sub-tile.
-  const int32_t *bt_row = a.block_tables + static_cast<int64_t>(slot) * a.max_blocks_per_slot;
-  int my_block = 0;
-  bool my_ok = true;
-  if (lane < my_units) {
-    my_block = __ldg(bt_row + (key0 + kSubKeys * (warp + kWarps * lane)) / a.block_size);
-    my_ok = my_block >= 0 && my_block < a.num_blocks;
-    if (!my_ok && a.status) atomicOr(a.status, PKV_DEV_BAD_BLOCK);
-  }
-
-  uint64_t *wbar = bars + warp * kStages;
-  uint8_t *wring = smem + warp * kStages * Lay::kStageBytes;
+  // The span merge may launch now; it waits for this grid before reading.
+  launch_dependents();
+  const int hkv = a.num_kv_heads;
+  const int num_tasks = num_items * hkv;
+  const int stride = gridDim.x * kWarps;
+  const int t0 = warp * gridDim.x + blockIdx.x;
+  if (t0 >= num_tasks) return;
   if (lane == 0) {
-    for (int s = 0; s < kStages; ++s) mbar_init(wbar + s, 1);
+    for (int s = 0; s < NST; ++s) mbar_init(full + s, 1);
     fence_barrier_init();
-  }
-  __syncwarp();
-
-  // Q^T fragments (B operand): head = nt*8 + lane/4, d = kk*16 + (lane%4)*2 (+8).
-  uint32_t qf[NT][KT][2];
-  {
-    const uint16_t *qrow = static_cast<const uint16_t *>(a.q) +
-                           (static_cast<size_t>(row0) * a.num_q_heads + g * a.group) * D;
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      const int head = nt * 8 + (lane >> 2);
-      const uint32_t *qp = reinterpret_cast<const uint32_t *>(qrow + head * D) + (lane & 3);
-#pragma unroll
-      for (int kk = 0; kk < KT; ++kk) {
-        qf[nt][kk][0] = head < a.group ? __ldg(qp + kk * 8) : 0u;
-        qf[nt][kk][1] = head < a.group ? __ldg(qp + kk * 8 + 4) : 0u;
-      }
-    }
-  }
-
-  auto issue = [&](int i) {
-    const int blk = __shfl_sync(0xffffffffu, my_block, i);
-    const bool ok = __shfl_sync(0xffffffffu, my_ok ? 1 : 0, i) != 0;
-    if (lane == 0) {
-      const int stage = i % kStages;
-      uint8_t *dst = wring + stage * Lay::kStageBytes;
-      uint64_t *bar = wbar + stage;
-      const int key = key0 + kSubKeys * (warp + kWarps * i);
-      if (ok) {
-        const int row = (blk * a.num_kv_heads + g) * a.block_size + key % a.block_size;
-        mbar_arrive_expect_tx(bar, Lay::kStageBytes);
-#pragma unroll
-        for (int h = 0; h < Lay::kHalves; ++h) {
-          tma_load_2d(dst + h * Lay::kHalfBytes, &tmap_k, h * 64, row, bar);
-          tma_load_2d(dst + Lay::kTileBytes + h * Lay::kHalfBytes, &tmap_v, h * 64, row, bar);
-        }
-      } else {
-        mbar_arrive(bar);  // nothing to load; the consumer skips this sub-tile
-      }
-    }
-  };
-
-  float m[NT][2], l[NT][2], acc[NT][KT][4];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    m[nt][0] = m[nt][1] = -INFINITY;
-    l[nt][0] = l[nt][1] = 0.f;
-#pragma unroll
-    for (int mt = 0; mt < KT; ++mt) acc[nt][mt][0] = acc[nt][mt][1] = acc[nt][mt][2] = acc[nt][mt][3] = 0.f;
-  }
-
-  if (lane == 0 && warp == 0) {
     prefetch_tensormap(&tmap_k);
     prefetch_tensormap(&tmap_v);
   }
-  for (int i = 0; i < my_units && i < kStages; ++i) issue(i);
+  __syncwarp();
+  // Every input may come from the kernel before this one in the stream.
+  grid_dependency_wait();
 
-  bool timed_out = false;
-  const float sl2 = a.scale_log2;
-  for (int i = 0; i < my_units; ++i) {
-    const int stage = i % kStages;
-    if (!mbar_wait(wbar + stage, (i / kStages) & 1)) {
-      timed_out = true;
-      break;
+  Task A, B;
+  int4 rawC = make_int4(0, 0, 0, 0);
+  expand(A, t0, load_item(items, t0, hkv), a, lane);
+  {
+    const int t1 = t0 + stride;
+    expand(B, t1 < num_tasks ? t1 : -1, t1 < num_tasks ? load_item(items, t1, hkv) : rawC, a, lane);
+    const int t2 = t1 + stride;
+    if (t2 < num_tasks) rawC = load_item(items, t2, hkv);
+  }
+  finalize(A, a, lane);
+  uint32_t qA[NT][KT][2], qB[NT][KT][2];
+  if (A.ok) load_q<D, NT>(qA, A, a, lane);
+  bool qB_loaded = false;
+
+  int P = 0, C = 0, pa = 0, pb = 0;
+  int pstage = 0;  // P % NST
+  auto issue = [&](const Task &T, int u) {
+    const int row = __shfl_sync(kFull, T.row, u);
+    if (lane == 0) {
+      uint64_t *bar = full + pstage;
+      uint8_t *dst = ring + pstage * Cfg::kStageBytes;
+      if (row >= 0) {
+        mbar_arrive_expect_tx(bar, Cfg::kStageBytes);
+#pragma unroll
+        for (int h = 0; h < Cfg::kHalves; ++h) {
+          tma_load_2d(dst + h * Cfg::kHalfBytes, &tmap_k, h * 64, row, bar);
+          tma_load_2d(dst + Cfg::kTileBytes + h * Cfg::kHalfBytes, &tmap_v, h * 64, row, bar);
+        }
+      } else {
+        mbar_arrive(bar);  // nothing loaded; the consumer masks this sub-tile out
+      }
     }
-    const bool ok = __shfl_sync(0xffffffffu, my_ok ? 1 : 0, i) != 0;
-    const int kbase = key0 + kSubKeys * (warp + kWarps * i);
-    const int valid = min(kSubKeys, key1 - kbase);
-    if (ok) {
-      const uint32_t kaddr = smem_addr(wring + stage * Lay::kStageBytes);
-      const uint32_t vaddr = kaddr + Lay::kTileBytes;
-      const int j = lane >> 3;
-
-      // S^T = K Q^T : A = K sub-tile rows (keys), 16 columns of d per k-step.
-      float s[NT][4];
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
-      {
-        const int r = (lane & 7) + ((j & 1) << 3);
-#pragma unroll
-        for (int kk = 0; kk < KT; ++kk) {
-          const int chunk = ((kk & 3) << 1) + (j >> 1);
-          uint32_t af[4];
-          ldmatrix_x4(af, kaddr + (kk >> 2) * Lay::kHalfBytes + r * 128 + ((chunk ^ (r & 7)) << 4));
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(s[nt], af, qf[nt][kk][0], qf[nt][kk][1]);
+    ++P;
+    pstage = pstage + 1 == NST ? 0 : pstage + 1;
+  };
+  auto issue_next = [&]() -> bool {
+    if (pa < A.units) {
+      issue(A, pa++);
+      return true;
+    }
+    if (B.t >= 0) {
+      if (!B.finalized) {
+        finalize(B, a, lane);
+        if (B.ok) {
+          load_q<D, NT>(qB, B, a, lane);
+          qB_loaded = true;
         }
       }
+      if (pb < B.units) {
+        issue(B, pb++);
+        return true;
+      }
+    }
+    return false;
+  };
+  while (P - C < NST && issue_next()) {
+  }
 
-      // Online softmax; thread holds keys lane/4 (+8) for heads (lane%4)*2 + {0,1}.
-      const int ka = lane >> 2, kb = ka + 8;
-      uint32_t pb[NT][2];
+  // Per-lane byte offsets of the swizzled ldmatrix rows inside a 64-column
+  // half, for K (A operand, rows = keys) and V (transposed A operand).
+  // Row r's 16-byte chunk c sits at chunk c ^ (r % 8) (128-byte swizzle).
+  uint32_t koff[4], voff[4];
+  {
+    const int j = lane >> 3;
+    const int rk = (lane & 7) + ((j & 1) << 3), rv = (lane & 7) + ((j >> 1) << 3);
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
+    for (int q = 0; q < 4; ++q) {
+      koff[q] = rk * 128 + ((((q << 1) + (j >> 1)) ^ (rk & 7)) << 4);
+      voff[q] = rv * 128 + ((((q << 1) + (j & 1)) ^ (rv & 7)) << 4);
+    }
+  }
+  const uint32_t ring_addr = smem_addr(ring);
+  const float sl2 = a.scale_log2;
+  const int G = a.group;
+  const int ka = lane >> 2, kb = ka + 8, k0 = (lane & 3) * 2;
+  int cstage = 0;
+  uint32_t cphase = 0;  // (C / NST) & 1
+
+  while (A.t >= 0) {
+    // m: the reference max each head's sums are scaled to (log2 units); it is
+    // only raised when a head's running max exceeds it by more than 2^8, so
+    // exp2(x - m) <= 256 and the sums stay exact up to rounding.
+    float m[NT][2], l[NT][2], acc[NT][KT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      m[nt][0] = m[nt][1] = -INFINITY;
+      l[nt][0] = l[nt][1] = 0.f;
+#pragma unroll
+      for (int mt = 0; mt < KT; ++mt) acc[nt][mt][0] = acc[nt][mt][1] = acc[nt][mt][2] = acc[nt][mt][3] = 0.f;
+    }
+
+    for (int u = 0; u < A.units; ++u) {
+      const int stage = cstage;
+      if (!mbar_wait(full + stage, cphase)) {
+        if (lane == 0 && a.status) atomicOr(a.status, PKV_DEV_TIMEOUT);
+        return;
+      }
+      const int row = __shfl_sync(kFull, A.row, u);
+      const int kbase = A.key0 + u * kSubKeys;
+      // keys of the sub-tile that take part (0 for a block ID outside the pool)
+      const int v = row >= 0 ? min(kSubKeys, A.key1 - kbase) : 0;
+      const uint32_t kaddr = ring_addr + stage * Cfg::kStageBytes;
+
+      // S^T = K Q^T, split over two accumulators to halve the MMA chain.
+      float s0[NT][4], s1[NT][4];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) s0[nt][i] = s1[nt][i] = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < KT; ++kk) {
+        uint32_t af[4];
+        ldmatrix_x4(af, kaddr + (kk >> 2) * Cfg::kHalfBytes + koff[kk & 3]);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) mma_bf16_16816((kk & 1) ? s1[nt] : s0[nt], af, qA[nt][kk][0], qA[nt][kk][1]);
+      }
+
+      // Online softmax; this thread holds keys lane/4 and lane/4 + 8 of heads
+      // (lane%4)*2 + {0, 1}.
+      float x[NT][2][2], mx[NT][2];
+      bool need = false;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-          const float xa = ka < valid ? s[nt][c] * sl2 : -INFINITY;
-          const float xb = kb < valid ? s[nt][c + 2] * sl2 : -INFINITY;
-          float mx = fmaxf(xa, xb);
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-          const float mnew = fmaxf(m[nt][c], mx);
-          const float corr = exp2f(m[nt][c] - mnew);
-          m[nt][c] = mnew;
-          const float pa = bf16_round(exp2f(xa - mnew));
-          const float pbv = bf16_round(exp2f(xb - mnew));
-          l[nt][c] = l[nt][c] * corr + pa + pbv;
-#pragma unroll
-          for (int mt = 0; mt < KT; ++mt) {
-            acc[nt][mt][c] *= corr;
-            acc[nt][mt][c + 2] *= corr;
-          }
-          s[nt][c] = pa;
-          s[nt][c + 2] = pbv;
+          x[nt][c][0] = ka < v ? (s0[nt][c] + s1[nt][c]) * sl2 : -INFINITY;
+          x[nt][c][1] = kb < v ? (s0[nt][c + 2] + s1[nt][c + 2]) * sl2 : -INFINITY;
+          float t = fmaxf(x[nt][c][0], x[nt][c][1]);
+          t = fmaxf(t, __shfl_xor_sync(kFull, t, 4));
+          t = fmaxf(t, __shfl_xor_sync(kFull, t, 8));
+          t = fmaxf(t, __shfl_xor_sync(kFull, t, 16));
+          mx[nt][c] = t;
+          need |= t > m[nt][c] + kRescale;
         }
-        pb[nt][0] = movmatrix_trans(pack_bf16x2(s[nt][0], s[nt][1]));
-        pb[nt][1] = movmatrix_trans(pack_bf16x2(s[nt][2], s[nt][3]));
+      if (__any_sync(kFull, need)) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int c = 0; c < 2; ++c)
+            if (mx[nt][c] > m[nt][c] + kRescale) {
+              const float corr = exp2f(m[nt][c] - mx[nt][c]);
+              m[nt][c] = mx[nt][c];
+              l[nt][c] *= corr;
+#pragma unroll
+              for (int mt = 0; mt < KT; ++mt) {
+                acc[nt][mt][c] *= corr;
+                acc[nt][mt][c + 2] *= corr;
+              }
+            }
+      }
+      uint32_t pf[NT][2];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const float m0 = m[nt][0] == -INFINITY ? 0.f : m[nt][0];
+        const float m1 = m[nt][1] == -INFINITY ? 0.f : m[nt][1];
+        uint32_t pk[2];  // keys ka / kb: heads (c=0, c=1) packed as bf16x2
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          pk[i] = pack_bf16x2(exp2f(x[nt][0][i] - m0), exp2f(x[nt][1][i] - m1));
+          l[nt][0] += __uint_as_float(pk[i] << 16);
+          l[nt][1] += __uint_as_float(pk[i] & 0xFFFF0000u);
+        }
+        pf[nt][0] = movmatrix_trans(pk[0]);
+        pf[nt][1] = movmatrix_trans(pk[1]);
       }
 
-      // O^T += V^T P^T : A = V^T via transposed ldmatrix of the V sub-tile.
-      const int k0 = (lane & 3) * 2;
-      const uint32_t mlo = (k0 < valid ? 0x0000FFFFu : 0u) | (k0 + 1 < valid ? 0xFFFF0000u : 0u);
-      const uint32_t mhi = (k0 + 8 < valid ? 0x0000FFFFu : 0u) | (k0 + 9 < valid ? 0xFFFF0000u : 0u);
-      const int r = (lane & 7) + ((j >> 1) << 3);
+      // O^T += V^T P^T; V rows of keys that do not take part are zeroed.
+      const bool part = v < kSubKeys;
+      const uint32_t mlo = (k0 < v ? 0x0000FFFFu : 0u) | (k0 + 1 < v ? 0xFFFF0000u : 0u);
+      const uint32_t mhi = (k0 + 8 < v ? 0x0000FFFFu : 0u) | (k0 + 9 < v ? 0xFFFF0000u : 0u);
 #pragma unroll
       for (int mt = 0; mt < KT; ++mt) {
-        const int chunk = ((mt & 3) << 1) + (j & 1);
         uint32_t af[4];
-        ldmatrix_x4_trans(af, vaddr + (mt >> 2) * Lay::kHalfBytes + r * 128 + ((chunk ^ (r & 7)) << 4));
-        af[0] &= mlo;
-        af[1] &= mlo;
-        af[2] &= mhi;
-        af[3] &= mhi;
+        ldmatrix_x4_trans(af, kaddr + Cfg::kTileBytes + (mt >> 2) * Cfg::kHalfBytes + voff[mt & 3]);
+        if (part) {
+          af[0] &= mlo;
+          af[1] &= mlo;
+          af[2] &= mhi;
+          af[3] &= mhi;
+        }
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(acc[nt][mt], af, pb[nt][0], pb[nt][1]);
+        for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(acc[nt][mt], af, pf[nt][0], pf[nt][1]);
       }
-    }
-    // Release the stage: order this warp's reads before the next TMA write.
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (i + kStages < my_units) issue(i + kStages);
-  }
-
-  const bool any_timeout = __syncthreads_or(timed_out);
-  if (any_timeout) {
-    if (threadIdx.x == 0 && a.status) atomicOr(a.status, PKV_DEV_TIMEOUT);
-    return;
-  }
-
-  // Row sums over the 8 lanes that share a head column.
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-    for (int c = 0; c < 2; ++c) {
-      float v = l[nt][c];
-      v += __shfl_xor_sync(0xffffffffu, v, 4);
-      v += __shfl_xor_sync(0xffffffffu, v, 8);
-      v += __shfl_xor_sync(0xffffffffu, v, 16);
-      l[nt][c] = v;
+      // Refill the ring by one. The stage's shared-memory reads are complete:
+      // every ldmatrix result has been consumed by an MMA before the warp
+      // converges here, so the next TMA write cannot overtake them.
+      __syncwarp();
+      ++C;
+      if (++cstage == NST) {
+        cstage = 0;
+        cphase ^= 1u;
+      }
+      issue_next();
     }
 
-  // ---- merge the four warps (fixed order), reusing the ring as scratch ----
-  float *red_acc = reinterpret_cast<float *>(smem);  // [warp][8*NT heads][D]
+    // ---- finish task A: the output row, or this span's partial ----
+    if (A.ok) {
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
+      for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-    for (int c = 0; c < 2; ++c) {
-      const int hh = nt * 8 + (lane & 3) * 2 + c;
-      if (lane < 4) {
-        red_m[warp * 8 * NT + hh] = m[nt][c];
-        red_l[warp * 8 * NT + hh] = l[nt][c];
-      }
-      float *dst = red_acc + (warp * 8 * NT + hh) * D + (lane >> 2);
+        for (int c = 0; c < 2; ++c) {
+          float t = l[nt][c];
+          t += __shfl_xor_sync(kFull, t, 4);
+          t += __shfl_xor_sync(kFull, t, 8);
+          t += __shfl_xor_sync(kFull, t, 16);
+          l[nt][c] = t;
+        }
+      const int hbase = A.g * G;
+      if (A.pbase < 0) {
+        __nv_bfloat16 *out = reinterpret_cast<__nv_bfloat16 *>(a.out) +
+                             (static_cast<size_t>(A.row0) * a.num_q_heads + hbase) * D + (lane >> 2);
 #pragma unroll
-      for (int mt = 0; mt < KT; ++mt) {
-        dst[mt * 16] = acc[nt][mt][c];
-        dst[mt * 16 + 8] = acc[nt][mt][c + 2];
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            const int hh = nt * 8 + (lane & 3) * 2 + c;
+            if (hh < G) {
+              const float inv = 1.f / l[nt][c];
+#pragma unroll
+              for (int mt = 0; mt < KT; ++mt) {
+                out[static_cast<size_t>(hh) * D + mt * 16] = __float2bfloat16_rn(acc[nt][mt][c] * inv);
+                out[static_cast<size_t>(hh) * D + mt * 16 + 8] = __float2bfloat16_rn(acc[nt][mt][c + 2] * inv);
+              }
+            }
+          }
+      } else {
+        const size_t pi = static_cast<size_t>(A.pbase + A.span) * a.num_q_heads + hbase;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            const int hh = nt * 8 + (lane & 3) * 2 + c;
+            if (hh < G) {
+              float *pacc = a.partial_acc + (pi + hh) * D + (lane >> 2);
+#pragma unroll
+              for (int mt = 0; mt < KT; ++mt) {
+                pacc[mt * 16] = acc[nt][mt][c];
+                pacc[mt * 16 + 8] = acc[nt][mt][c + 2];
+              }
+              if (lane < 4) {
+                a.partial_ml[(pi + hh) * 2] = m[nt][c];
+                a.partial_ml[(pi + hh) * 2 + 1] = l[nt][c];
+              }
+            }
+          }
       }
     }
-  __syncthreads();
 
-  const int G = a.group;
-  for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
-    const int hh = idx / D, d = idx % D;
-    float mmax = -INFINITY;
+    // ---- advance: B becomes current, the task after it is expanded ----
+    const int next_t = B.t >= 0 ? B.t + stride : num_tasks;
+    A = B;
+    pa = pb;
+    pb = 0;
+    if (A.t >= 0) {
+      if (!A.finalized) finalize(A, a, lane);
+      if (qB_loaded) {
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) mmax = fmaxf(mmax, red_m[w * 8 * NT + hh]);
-    float lsum = 0.f, o = 0.f;
+        for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-      const float f = exp2f(red_m[w * 8 * NT + hh] - mmax);
-      lsum += red_l[w * 8 * NT + hh] * f;
-      o += red_acc[(w * 8 * NT + hh) * D + d] * f;
-    }
-    const int head = g * G + hh;
-    if (pbase < 0) {
-      store_bf16(a.out, (static_cast<size_t>(row0) * a.num_q_heads + head) * D + d, o / lsum);
-    } else {
-      const size_t pi = static_cast<size_t>(pbase + span) * a.num_q_heads + head;
-      a.partial_acc[pi * D + d] = o;
-      if (d == 0) {
-        a.partial_ml[pi * 2] = mmax;
-        a.partial_ml[pi * 2 + 1] = lsum;
+          for (int kk = 0; kk < KT; ++kk) {
+            qA[nt][kk][0] = qB[nt][kk][0];
+            qA[nt][kk][1] = qB[nt][kk][1];
+          }
+      } else if (A.ok) {
+        load_q<D, NT>(qA, A, a, lane);
       }
+    }
+    qB_loaded = false;
+    expand(B, next_t < num_tasks ? next_t : -1, rawC, a, lane);
+    if (next_t + stride < num_tasks) rawC = load_item(items, next_t + stride, hkv);
+    while (P - C < NST && issue_next()) {
     }
   }
 }
 
-// One CTA per (segment with several spans, q head); one thread per column.
-__global__ void __launch_bounds__(128) combine_kernel(const StepArgs a,
-                                                      const int32_t *__restrict__ items) {
-  const int4 it = reinterpret_cast<const int4 *>(items)[blockIdx.x];
+// Span merge: one CTA of four warps per (multi-span segment, q head). Worker
+// u of the CTA takes spans u, u + U, ... and columns (float4) lane % F; the
+// per-head max is a CTA-wide max, and the workers' sums are added in worker
+// order, so the result is deterministic.
+template <int D>
+__global__ void __launch_bounds__(128) merge_kernel(const StepArgs a, const int32_t *__restrict__ items) {
+  constexpr int F = D / 4;          // float4 per output row
+  constexpr int PER_WARP = 32 / F;  // workers per warp
+  constexpr int U = 4 * PER_WARP;   // workers per CTA
+  __shared__ float s_max[4];
+  __shared__ float4 s_acc[U][F];
+  __shared__ float s_l[U];
+  grid_dependency_wait();  // partials come from the decode kernel
+
+  const int4 it = __ldg(reinterpret_cast<const int4 *>(items) + blockIdx.x);
   const int seg = it.x, slot = it.y, spans = it.z, pbase = it.w;
-  const int h = blockIdx.y, d = threadIdx.x;
-  const int D = a.head_dim;
-  bool bad = seg < 0 || seg >= a.num_seqs || slot < 0 || slot >= a.max_slots || spans < 1;
+  const int h = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  bool bad = seg < 0 || seg >= a.num_seqs || slot < 0 || slot >= a.max_slots || spans < 2 || pbase < 0;
   int row0 = 0;
   if (!bad) {
-    row0 = a.cu_seqlens_q[seg];
-    bad = a.seq_slot[seg] != slot || a.cu_seqlens_q[seg + 1] - row0 != 1 || row0 >= a.total_q;
+    row0 = __ldg(a.cu_seqlens_q + seg);
+    const int L = __ldg(a.context_lens + slot);
+    bad = __ldg(a.seq_slot + seg) != slot || __ldg(a.cu_seqlens_q + seg + 1) - row0 != 1 ||
+          (L + PKV_SPLIT_KEYS - 1) / PKV_SPLIT_KEYS != spans || row0 < 0 || row0 >= a.total_q;
   }
   if (bad) {
     if (threadIdx.x == 0 && a.status) atomicOr(a.status, PKV_DEV_BAD_SEGMENT);
     return;
   }
-  if (d >= D) return;
-  const size_t base = static_cast<size_t>(pbase) * a.num_q_heads + h;
-  float mmax = -INFINITY;
-  for (int i = 0; i < spans; ++i)
-    mmax = fmaxf(mmax, a.partial_ml[(base + static_cast<size_t>(i) * a.num_q_heads) * 2]);
-  float lsum = 0.f, o = 0.f;
-  for (int i = 0; i < spans; ++i) {
-    const size_t pi = base + static_cast<size_t>(i) * a.num_q_heads;
-    const float f = exp2f(a.partial_ml[pi * 2] - mmax);
-    lsum += a.partial_ml[pi * 2 + 1] * f;
-    o += a.partial_acc[pi * D + d] * f;
+  const int u = warp * PER_WARP + lane / F, d4 = lane % F;
+  const size_t hq = static_cast<size_t>(a.num_q_heads);
+  const size_t base = static_cast<size_t>(pbase) * hq + h;
+
+  float mx = -INFINITY;
+  for (int i = u; i < spans; i += U) mx = fmaxf(mx, __ldg(a.partial_ml + (base + i * hq) * 2));
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+  if (lane == 0) s_max[warp] = mx;
+  __syncthreads();
+  const float M = fmaxf(fmaxf(s_max[0], s_max[1]), fmaxf(s_max[2], s_max[3]));
+
+  float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+  float lsum = 0.f;
+#pragma unroll 4
+  for (int i = u; i < spans; i += U) {
+    const size_t p = base + static_cast<size_t>(i) * hq;
+    const float w = exp2f(__ldg(a.partial_ml + p * 2) - M);
+    lsum += __ldg(a.partial_ml + p * 2 + 1) * w;
+    const float4 v = __ldg(reinterpret_cast<const float4 *>(a.partial_acc + p * D) + d4);
+    o.x += v.x * w;
+    o.y += v.y * w;
+    o.z += v.z * w;
+    o.w += v.w * w;
   }
-  store_bf16(a.out, (static_cast<size_t>(row0) * a.num_q_heads + h) * D + d, o / lsum);
+  s_acc[u][d4] = o;
+  if (d4 == 0) s_l[u] = lsum;
+  __syncthreads();
+  if (threadIdx.x < F) {
+    float4 r = s_acc[0][threadIdx.x];
+    float L = s_l[0];
+    for (int k = 1; k < U; ++k) {
+      const float4 t = s_acc[k][threadIdx.x];
+      r.x += t.x;
+      r.y += t.y;
+      r.z += t.z;
+      r.w += t.w;
+      L += s_l[k];
+    }
+    const float inv = 1.f / L;
+    uint2 packed;
+    packed.x = pack_bf16x2(r.x * inv, r.y * inv);
+    packed.y = pack_bf16x2(r.z * inv, r.w * inv);
+    *reinterpret_cast<uint2 *>(reinterpret_cast<__nv_bfloat16 *>(a.out) + (static_cast<size_t>(row0) * hq + h) * D +
+                               4 * threadIdx.x) = packed;
+  }
+}
+
+int sm_count() {
+  static int count[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return 148;
+  if (count[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    count[dev] = n;
+  }
+  return count[dev];
+}
+
+// Launch with programmatic stream serialization: the kernel may start while
+// the previous kernel in the stream drains; it calls griddepcontrol.wait
+// before touching any input.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
 template <int D, int NT>
-cudaError_t launch_decode_t(const StepArgs &a, const CUtensorMap &tk, const CUtensorMap &tv,
-                            int32_t num_items, const int32_t *items, cudaStream_t stream) {
-  constexpr int smem = decode_smem_bytes<D, NT>();
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, NT>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+cudaError_t launch_decode_t(const StepArgs &a, const CUtensorMap &tk, const CUtensorMap &tv, int32_t num_items,
+                            const int32_t *items, cudaStream_t stream) {
+  constexpr int smem = DecodeCfg<D>::kSmem;
+  static uint64_t configured = 0;  // one bit per device
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(configured & bit)) {
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    configured = true;
+    configured |= bit;
   }
-  dim3 grid(static_cast<unsigned>(num_items), static_cast<unsigned>(a.num_kv_heads));
-  decode_kernel<D, NT><<<grid, 128, smem, stream>>>(tk, tv, a, items);
-  return cudaGetLastError();
+  const int64_t tasks = static_cast<int64_t>(num_items) * a.num_kv_heads;
+  const int grid = static_cast<int>(tasks < sm_count() ? tasks : sm_count());
+  return launch_pdl(decode_kernel<D, NT>, dim3(grid), dim3(kWarps * 32), smem, stream, tk, tv, a, items, num_items);
 }
 
 }  // namespace
 
-cudaError_t launch_decode(const StepArgs &a, const CUtensorMap &tk, const CUtensorMap &tv,
-                          int32_t num_items, const int32_t *items, cudaStream_t stream) {
+cudaError_t launch_decode(const StepArgs &a, const CUtensorMap &tk, const CUtensorMap &tv, int32_t num_items,
+                          const int32_t *items, cudaStream_t stream) {
   if (num_items <= 0) return cudaSuccess;
   const bool wide = a.group > 8;
   if (a.head_dim == 128)
@@ -396,12 +593,11 @@ cudaError_t launch_decode(const StepArgs &a, const CUtensorMap &tk, const CUtens
               : launch_decode_t<64, 1>(a, tk, tv, num_items, items, stream);
 }
 
-cudaError_t launch_combine(const StepArgs &a, int32_t num_items, const int32_t *items,
-                           cudaStream_t stream) {
+cudaError_t launch_merge(const StepArgs &a, int32_t num_items, const int32_t *items, cudaStream_t stream) {
   if (num_items <= 0) return cudaSuccess;
-  dim3 grid(static_cast<unsigned>(num_items), static_cast<unsigned>(a.num_q_heads));
-  combine_kernel<<<grid, 128, 0, stream>>>(a, items);
-  return cudaGetLastError();
+  const dim3 grid(static_cast<unsigned>(num_items), static_cast<unsigned>(a.num_q_heads));
+  if (a.head_dim == 128) return launch_pdl(merge_kernel<128>, grid, dim3(128), 0, stream, a, items);
+  return launch_pdl(merge_kernel<64>, grid, dim3(128), 0, stream, a, items);
 }
 
 }  // namespace pkv

@@ -38,8 +38,8 @@ cudaError_t launch_cache_write(const void *k_new, const void *v_new, const int64
 cudaError_t launch_decode(const StepArgs &a, const CUtensorMap &tmap_k, const CUtensorMap &tmap_v,
                           int32_t num_items, const int32_t *items, cudaStream_t stream);
 
-cudaError_t launch_combine(const StepArgs &a, int32_t num_items, const int32_t *items,
-                           cudaStream_t stream);
+// One CTA per (multi-span segment, q head): merges the segment's span partials.
+cudaError_t launch_merge(const StepArgs &a, int32_t num_items, const int32_t *items, cudaStream_t stream);
 
 cudaError_t launch_prefill(const StepArgs &a, const CUtensorMap &tmap_q, const CUtensorMap &tmap_k,
                            const CUtensorMap &tmap_v, int32_t rows_per_tile, int32_t num_items,

@@ -182,22 +182,23 @@ def tiny(seed: int = 0, threads=None) -> StepInputs:
                    np.asarray(free, dtype=np.int32), threads)
 
 
-def decode5(seed: int = 0, threads=None) -> StepInputs:
+def decode5(seed: int = 0, threads=None, pool_blocks: int = 65536) -> StepInputs:
     """Decode-only step, five clients: 40 q / 8 kv heads, head_dim 128, 65,536 blocks.
 
     Five slots each decode one row; contexts are uniform in [1024, 8192] and
-    block tables come off a shuffled free list.
+    block tables come off a shuffled free list. ``pool_blocks`` shrinks the
+    pool (same contexts, other physical blocks) for profiling captures.
     """
     rt, rl = _rngs(seed, 2, 0)
-    free = [int(b) for b in rt.permutation(65536)]
+    free = [int(b) for b in rt.permutation(pool_blocks)]
     ctx = rl.integers(1024, 8193, size=5)
     segs = [Segment(i, 1, int(c)) for i, c in enumerate(ctx)]
     blocks = {s.slot: _take(free, -(-s.ctx // 16)) for s in segs}
-    return _finish("decode5", seed, 40, 8, 128, 16, 65536, 8, 512, segs, blocks,
+    return _finish("decode5", seed, 40, 8, 128, 16, pool_blocks, 8, 512, segs, blocks,
                    np.asarray(free, dtype=np.int32), threads)
 
 
-def mixed(seed: int = 0, threads=None) -> StepInputs:
+def mixed(seed: int = 0, threads=None, pool_blocks: int = 65536) -> StepInputs:
     """Mixed step: 32 q / 8 kv heads, head_dim 128; one 512-row chunk + 4 decode rows.
 
     Slot 0 runs the chunk [1024, 1536) of a 3000-token prompt; its admission
@@ -205,18 +206,18 @@ def mixed(seed: int = 0, threads=None) -> StepInputs:
     contexts uniform in [200, 4000]. Packed [chunk x512][d1][d2][d3][d4].
     """
     rt, rl = _rngs(seed, 2, 0)
-    free = [int(b) for b in rt.permutation(65536)]
+    free = [int(b) for b in rt.permutation(pool_blocks)]
     ctx = rl.integers(200, 4001, size=4)
     segs = [Segment(0, 512, 1536)] + [Segment(1 + i, 1, int(c)) for i, c in enumerate(ctx)]
     blocks = {0: _take(free, 188)}
     for s in segs[1:]:
         blocks[s.slot] = _take(free, -(-s.ctx // 16))
-    return _finish("mixed", seed, 32, 8, 128, 16, 65536, 8, 256, segs, blocks,
+    return _finish("mixed", seed, 32, 8, 128, 16, pool_blocks, 8, 256, segs, blocks,
                    np.asarray(free, dtype=np.int32), threads,
                    notes={"prompt_len": 3000, "chunk": (1024, 1536)})
 
 
-def decode256(seed: int = 0, threads=None) -> StepInputs:
+def decode256(seed: int = 0, threads=None, pool_blocks: int = 131072) -> StepInputs:
     """Large decode batch: 256 slots, 64 q / 8 kv heads, head_dim 128, 131,072 blocks.
 
     Contexts are lognormal with median 2048 (sigma 1), clipped to [16, 32768].
@@ -225,7 +226,7 @@ def decode256(seed: int = 0, threads=None) -> StepInputs:
     tables are then drawn from what the free stack holds.
     """
     rt, rl, rf = _rngs(seed, 3, 0)
-    free = [int(b) for b in rt.permutation(131072)]
+    free = [int(b) for b in rt.permutation(pool_blocks)]
     for _ in range(4):
         held = [_take(free, int(n)) for n in rf.integers(1, 513, size=64)]
         for i in rf.permutation(64)[:32]:
@@ -234,7 +235,7 @@ def decode256(seed: int = 0, threads=None) -> StepInputs:
     ctx = np.clip(np.round(2048.0 * np.exp(z)), 16, 32768).astype(np.int64)
     segs = [Segment(i, 1, int(c)) for i, c in enumerate(ctx)]
     blocks = {s.slot: _take(free, -(-s.ctx // 16)) for s in segs}
-    return _finish("decode256", seed, 64, 8, 128, 16, 131072, 256, 2048, segs, blocks,
+    return _finish("decode256", seed, 64, 8, 128, 16, pool_blocks, 256, 2048, segs, blocks,
                    np.asarray(free, dtype=np.int32), threads)
 
 
@@ -263,7 +264,9 @@ def random_step(seed: int, shapes: list[tuple[int, int]], *, num_q_heads=4, num_
 WORKLOADS = {"tiny": tiny, "decode5": decode5, "mixed": mixed, "decode256": decode256}
 
 
-def make_step(name: str, seed: int = 0, threads=None) -> StepInputs:
+def make_step(name: str, seed: int = 0, threads=None, pool_blocks: int | None = None) -> StepInputs:
+    if pool_blocks:
+        return WORKLOADS[name](seed, threads=threads, pool_blocks=pool_blocks)
     return WORKLOADS[name](seed, threads=threads)
 
 

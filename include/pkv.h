@@ -188,20 +188,20 @@ pkv_status pkv_plan_lower(pkv_pool *pool, const pkv_segment *plan, int32_t num_s
  * Rows of a segment with one row go to the split-KV decode kernel: the
  * segment's keys are cut into fixed spans of PKV_SPLIT_KEYS (the cut depends
  * only on that segment's context, so a row's result does not depend on what
- * else is in the batch), and a combine kernel merges spans in order.
+ * else is in the batch); a merge kernel combines a segment's spans in order.
  * Segments with several rows (prompt chunks) go to the tensor-core chunk
  * kernel, in tiles of query rows. The pages leave this split open; it is
  * this library's design.
  * ---------------------------------------------------------------------- */
-#define PKV_SPLIT_KEYS 512
+#define PKV_SPLIT_KEYS 256
 #define PKV_WORK_WORDS_PER_ITEM 4
 
 typedef struct pkv_work_info {
     int32_t num_decode_items;  /* (segment, key span) items */
     int32_t num_prefill_items; /* (segment, query tile) items */
-    int32_t num_combine_items; /* decode segments with more than one span */
+    int32_t num_combine_items; /* (segment) merge items: decode segments with more than one span */
     int32_t num_partials;      /* span results kept in the workspace */
-    int64_t work_words;        /* int32 words of the item array */
+    int64_t work_words;        /* int32 words of the item array: decode, prefill, then merge items */
     uint64_t workspace_bytes;  /* device workspace pkv_attention needs (may be 0) */
 } pkv_work_info;
 
@@ -274,8 +274,12 @@ pkv_status pkv_cache_write(const void *k_new, const void *v_new, const int64_t *
  * output rounded to bf16 (nearest even). Results are deterministic and do
  * not depend on the other segments in the step or on their order.
  * `workspace` (device, >= info->workspace_bytes, 256-byte aligned) holds the
- * key-span partial results; it needs no initialisation. The pool must
- * already hold this step's rows (pkv_cache_write first, same stream).
+ * key-span partial results between the decode kernel and the merge kernel;
+ * it needs no initialisation. Calls that share a workspace must not overlap
+ * on the GPU. The pool must already hold this step's rows (pkv_cache_write
+ * first, same stream). The kernels are launched with programmatic dependent
+ * launch, so they may start while the previous kernel in the stream drains;
+ * each waits for it before reading any argument.
  */
 pkv_status pkv_attention(const void *q, const int32_t *cu_seqlens_q, int32_t num_seqs,
                          int64_t total_q, const int32_t *seq_slot, const int32_t *context_lens,

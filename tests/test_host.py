@@ -166,19 +166,29 @@ def _work(cu, slots, ctx, **kw):
 
 
 def test_work_list_items():
+    S = B.PKV_SPLIT_KEYS
     ctx = np.zeros(8, np.int32)
-    ctx[[3, 1, 6, 2]] = [1536, 513, 512, 1]
+    ctx[[3, 1, 6, 2]] = [1536, 2 * S + 1, 2 * S, 1]
     work, info = _work([0, 512, 513, 514, 515], [3, 1, 6, 2], ctx, max_blocks_per_slot=128)
-    assert (info.num_decode_items, info.num_prefill_items, info.num_combine_items) == (4, 16, 1)
+    # decode spans: 3 for slot 1 (S, S, 1 keys), 2 for slot 6, 1 for slot 2; the chunk has 16 tiles
+    assert (info.num_decode_items, info.num_prefill_items, info.num_combine_items) == (6, 16, 2)
     items = work.reshape(-1, 4)
-    dec, pre, comb = items[:4], items[4:20], items[20:]
-    assert sorted(map(tuple, dec[:, :3].tolist())) == [(1, 1, 0), (1, 1, 1), (2, 6, 0), (3, 2, 0)]
-    assert list(dec[0, :2]) in ([1, 1], [2, 6])       # full 512-key spans first
-    assert list(dec[-1, :3]) == [3, 2, 0]              # the 1-key span last
-    assert list(comb[0]) == [1, 1, 2, 0] and info.num_partials == 2
+    assert len(items) == 24
+    dec, pre, comb = items[:6], items[6:22], items[22:]
+    assert [list(c) for c in comb] == [[1, 1, 3, 0], [2, 6, 2, 3]]  # (seg, slot, spans, partial base)
+    assert sorted(map(tuple, dec[:, :3].tolist())) == [(1, 1, 0), (1, 1, 1), (1, 1, 2), (2, 6, 0), (2, 6, 1),
+                                                        (3, 2, 0)]
+    full = {(1, 1, 0), (1, 1, 1), (2, 6, 0), (2, 6, 1)}
+    assert {tuple(x) for x in dec[:4, :3].tolist()} == full      # full spans first
+    assert [tuple(x) for x in dec[4:, :3].tolist()] == [(1, 1, 2), (3, 2, 0)]  # 1-key spans, stable
+    bases = {tuple(x[:3]): x[3] for x in dec.tolist()}
+    assert bases[(1, 1, 0)] == bases[(1, 1, 1)] == bases[(1, 1, 2)] == 0
+    assert bases[(2, 6, 0)] == bases[(2, 6, 1)] == 3 and bases[(3, 2, 0)] == -1
+    assert info.num_partials == 5
     assert sorted(pre[:, 2].tolist()) == list(range(16)) and (pre[:, :2] == [0, 3]).all()
     assert pre[0, 2] == 15  # the tile that sees the most keys first
-    assert info.workspace_bytes == 2 * 32 * 128 * 4 + 2 * 32 * 2 * 4
+    a256 = lambda x: (x + 255) // 256 * 256
+    assert info.workspace_bytes == a256(5 * 32 * 128 * 4) + a256(5 * 32 * 2 * 4)
 
 
 @pytest.mark.parametrize("cu,slots,ctx_pairs,err", [
