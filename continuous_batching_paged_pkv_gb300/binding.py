@@ -30,6 +30,7 @@ STATUS_NAMES = {
 PKV_ERR_WORKSPACE_TOO_SMALL = 4
 PKV_ERR_NO_BLOCKS = 7
 PKV_SPLIT_KEYS = 256
+PKV_NO_ALLOC_SCRATCH_BYTES = 32 << 20
 PKV_WORK_WORDS_PER_ITEM = 4
 
 
@@ -86,6 +87,8 @@ def _lib():
             "pkv_attention": ([p, p, i32, i64, p, p, p, i32, i32, i32, p, p, i64, i32, i32, i32, f32, p,
                                ctypes.POINTER(WorkInfo), p, p, u64, p, p], ctypes.c_int),
             "pkv_check_device_status": ([p, p, ctypes.POINTER(ctypes.c_uint32)], ctypes.c_int),
+            "pkv_attention_no_alloc": ([p, p, i32, i64, p, p, p, i32, i32, i32, p, p, i64, i32, i32, i32, f32, p,
+                                        ctypes.POINTER(WorkInfo), p, p, p], ctypes.c_int),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -262,6 +265,27 @@ def pkv_attention(q, cu_seqlens_q, seq_slot, context_lens, block_tables, k_pool,
                                 _t_ptr(k_pool), _t_ptr(v_pool), nb, q.shape[1], hkv, d, float(scale),
                                 _t_ptr(work), ctypes.byref(info), _t_ptr(out), _t_ptr(workspace), ws_bytes,
                                 _t_ptr(device_status), _stream(stream)), "pkv_attention")
+
+
+def pkv_attention_no_alloc(q, cu_seqlens_q, seq_slot, context_lens, block_tables, k_pool, v_pool, work,
+                           info: WorkInfo, out, *, scale: float = 0.0, device_status=None, stream=None) -> None:
+    """``pkv_attention`` with the library's own fixed scratch array instead of a workspace.
+
+    For callers that cannot allocate device memory; the step's partials must
+    fit in PKV_NO_ALLOC_SCRATCH_BYTES. Concurrent calls on one device race.
+    """
+    _need(q, "torch.bfloat16", "q")
+    _need(out, "torch.bfloat16", "out")
+    for t, nm in ((cu_seqlens_q, "cu_seqlens_q"), (seq_slot, "seq_slot"), (context_lens, "context_lens"),
+                  (block_tables, "block_tables"), (work, "work")):
+        _need(t, "torch.int32", nm)
+    nb, hkv, bs, d = k_pool.shape
+    ms, mbps = block_tables.shape
+    _check(_lib().pkv_attention_no_alloc(_t_ptr(q), _t_ptr(cu_seqlens_q), cu_seqlens_q.numel() - 1, q.shape[0],
+                                         _t_ptr(seq_slot), _t_ptr(context_lens), _t_ptr(block_tables), ms, mbps,
+                                         bs, _t_ptr(k_pool), _t_ptr(v_pool), nb, q.shape[1], hkv, d, float(scale),
+                                         _t_ptr(work), ctypes.byref(info), _t_ptr(out), _t_ptr(device_status),
+                                         _stream(stream)), "pkv_attention_no_alloc")
 
 
 def pkv_check_device_status(device_status, stream=None) -> int:

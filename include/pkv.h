@@ -291,6 +291,36 @@ pkv_status pkv_attention(const void *q, const int32_t *cu_seqlens_q, int32_t num
                          uint64_t workspace_bytes, uint32_t *device_status, pkv_stream_t stream);
 
 /*
+ * pkv_attention without a caller-provided workspace. The pages have no
+ * counterpart to this call; it exists for callers that cannot allocate
+ * device memory (a process whose device memory is all reserved up front in
+ * its own arena, or a serving loop that may not allocate between steps).
+ *
+ * Same arguments and results as pkv_attention, minus `workspace` and
+ * `workspace_bytes`: the span partials live in a file-scope device array of
+ * PKV_NO_ALLOC_SCRATCH_BYTES bytes that every GPU loading the library holds
+ * until the process exits. The call allocates nothing.
+ *   - A step whose info->workspace_bytes exceeds PKV_NO_ALLOC_SCRATCH_BYTES
+ *     is rejected with PKV_ERR_WORKSPACE_TOO_SMALL before any GPU work.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current) and caches it; make that first call before any
+ *     stream capture. PKV_ERR_CUDA if the lookup fails.
+ *   - Every call on a device shares the one array and leaves its contents
+ *     behind; nothing in it needs to start at zero. Calls that overlap on the
+ *     GPU (other streams, other host threads) race on it: serialise them.
+ */
+#define PKV_NO_ALLOC_SCRATCH_BYTES (32u << 20)
+
+pkv_status pkv_attention_no_alloc(const void *q, const int32_t *cu_seqlens_q, int32_t num_seqs,
+                                  int64_t total_q, const int32_t *seq_slot,
+                                  const int32_t *context_lens, const int32_t *block_tables,
+                                  int32_t max_slots, int32_t max_blocks_per_slot, int32_t block_size,
+                                  const void *k_pool, const void *v_pool, int64_t num_blocks,
+                                  int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                  float scale, const int32_t *work, const pkv_work_info *info,
+                                  void *out, uint32_t *device_status, pkv_stream_t stream);
+
+/*
  * Synchronise `stream`, read *device_status (device memory), clear it, and
  * map it to a status: PKV_OK if zero; PKV_ERR_DEVICE_TIMEOUT if the timeout
  * bit is set; otherwise PKV_ERR_DEVICE_INDEX. `bits_out` (nullable, host)
