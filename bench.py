@@ -13,9 +13,11 @@ Timing: W untimed warm-up steps, then K timed steps. Before each step a
 256 MiB buffer is overwritten (larger than the 129 MB L2) so no step finds its
 K/V in L2, and a second 256 MiB buffer is then read so that L2 holds clean
 lines (otherwise the flush's dirty lines would be written back to HBM inside
-the timed step). Both are outside the CUDA events that bracket the step. Each
-library call is bracketed by its own events on the launching stream, so the
-attention kernel's own duration is known. Under torchrun (N > 1) every rank
+the timed step). Both are outside the CUDA events that bracket the step. The
+timed region brackets whole steps only, so the step's kernels may overlap
+their launches; a second pass brackets each library call with its own events
+on the launching stream to give the attention call's own duration (the
+roofline figure) and the per-call breakdown. Under torchrun (N > 1) every rank
 runs an independent replica (the step has no exchange between GPUs); the
 job's time is the maximum over ranks.
 """
@@ -53,6 +55,8 @@ class L2Flush:
     def __call__(self):
         self.dirty.zero_()
         self.sink.copy_(self.clean.sum())
+
+
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 
@@ -307,7 +311,8 @@ def run_ours(args, rank, world, local_rank):
     ds = R.prepare(w, dev)
     stream = torch.cuda.current_stream()
     flush = L2Flush(dev)
-    launches_per_step = int(w.total_q > 0) + int(ds.info.num_decode_items > 0) + int(ds.info.num_prefill_items > 0)
+    launches_per_step = (int(w.total_q > 0) + int(ds.info.num_decode_items > 0) + int(ds.info.num_prefill_items > 0)
+                         + int(ds.info.num_combine_items > 0))
 
     for _ in range(args.warmup):
         flush()
@@ -322,28 +327,41 @@ def run_ours(args, rank, world, local_rank):
     clocks.start()
     barrier(world)
     torch.cuda.synchronize()
-    step_ms, write_ms, attn_ms = [], [], []
+    # Timed region: one event pair around each whole step (cache write +
+    # attention), so the step's kernels may overlap their launches.
+    step_ms = []
     chunk = 500
     done = 0
     while done < args.steps:
         n = min(chunk, args.steps - done)
-        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
-        for e0, e1, e2 in ev:
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+        for e0, e2 in ev:
             flush()
             e0.record(stream)
             R.run_cache_write(ds)
-            e1.record(stream)
             R.run_attention(ds)
             e2.record(stream)
         torch.cuda.synchronize()
-        for e0, e1, e2 in ev:
-            write_ms.append(e0.elapsed_time(e1))
-            attn_ms.append(e1.elapsed_time(e2))
-            step_ms.append(e0.elapsed_time(e2))
+        step_ms.extend(e0.elapsed_time(e2) for e0, e2 in ev)
         done += n
     torch.cuda.synchronize()
     barrier(world)
     clk = clocks.stop()
+    # Breakdown pass (same stream, same flush): events between the two calls
+    # give each call's own duration; the attention call is the roofline kernel.
+    write_ms, attn_ms = [], []
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(max(args.steps // 4, 20))]
+    for e0, e1, e2 in ev:
+        flush()
+        e0.record(stream)
+        R.run_cache_write(ds)
+        e1.record(stream)
+        R.run_attention(ds)
+        e2.record(stream)
+    torch.cuda.synchronize()
+    for e0, e1, e2 in ev:
+        write_ms.append(e0.elapsed_time(e1))
+        attn_ms.append(e1.elapsed_time(e2))
     if B.pkv_check_device_status(ds.status) != 0:
         raise RuntimeError("device status reported an error during the timed steps")
 
@@ -371,6 +389,8 @@ def run_ours(args, rank, world, local_rank):
         bound, unit, kernel = "hbm", "GB/s", "attention call (chunk + decode kernels)"
     elif ds.info.num_prefill_items:
         bound, unit, kernel = "tensor", "TFLOP/s", "prefill_kernel"
+    elif ds.info.num_combine_items:
+        bound, unit, kernel = "hbm", "GB/s", "attention call: decode_kernel + merge_kernel"
     else:
         bound, unit, kernel = "hbm", "GB/s", "decode_kernel"
     if bound == "tensor":
@@ -379,7 +399,7 @@ def run_ours(args, rank, world, local_rank):
                            "unit": "TFLOP/s", "frac": ach / tflops, "traffic": None,
                            "peak_source": f"{peak_src} bf16 burst"}
     else:
-        traffic = profiled_traffic("pkv_decode.cu", args.workload) if kernel == "decode_kernel" else None
+        traffic = profiled_traffic("pkv_decode.cu", args.workload) if kernel.startswith("attention call: decode") or kernel == "decode_kernel" else None
         res["roofline"] = {"bound": "hbm", "kernel": kernel, "achieved": achieved, "peak": hbm, "unit": "GB/s",
                            "frac": achieved / hbm, "traffic": traffic,
                            "algorithmic_bytes_per_launch": kv_bytes(w), "mean_launch_ms": attn_mean,

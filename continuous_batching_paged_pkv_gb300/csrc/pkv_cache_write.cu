@@ -12,6 +12,7 @@
 #include <cuda_runtime.h>
 
 #include "pkv_internal.h"
+#include "pkv_ptx.cuh"
 
 namespace pkv {
 namespace {
@@ -21,6 +22,8 @@ __global__ void __launch_bounds__(256) cache_write_kernel(
     const int64_t *__restrict__ slot_mapping, int64_t num_tokens, uint4 *__restrict__ k_pool,
     uint4 *__restrict__ v_pool, int64_t pool_rows, int32_t block_size, int32_t num_kv_heads,
     int32_t vec_per_row, uint32_t *__restrict__ status) {
+  launch_dependents();
+  grid_dependency_wait();  // k_new / v_new / slot_mapping may come from the previous kernel
   // Vector index over [2 (k, v)][num_tokens][num_kv_heads][vec_per_row].
   const int64_t per_tensor = num_tokens * num_kv_heads * vec_per_row;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -58,11 +61,10 @@ cudaError_t launch_cache_write(const void *k_new, const void *v_new, const int64
   const int threads = 256;
   int64_t blocks = (vectors + threads - 1) / threads;
   if (blocks > 152 * 16) blocks = 152 * 16;  // grid-stride beyond 16 CTAs per SM
-  cache_write_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
-      static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new), slot_mapping,
-      num_tokens, static_cast<uint4 *>(k_pool), static_cast<uint4 *>(v_pool),
-      num_blocks * block_size, block_size, num_kv_heads, vec_per_row, status);
-  return cudaGetLastError();
+  return launch_pdl(cache_write_kernel, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, stream,
+                    static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new), slot_mapping, num_tokens,
+                    static_cast<uint4 *>(k_pool), static_cast<uint4 *>(v_pool), num_blocks * block_size, block_size,
+                    num_kv_heads, vec_per_row, status);
 }
 
 }  // namespace pkv

@@ -65,9 +65,6 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
   return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
-__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
-
 // One task's metadata. Scalars are uniform across the warp; `bid` is per lane:
 // the physical block of the task's sub-tile number `lane`.
 struct Task {
@@ -453,17 +450,18 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
 }
 
 // Span merge: one CTA of four warps per (multi-span segment, q head). Worker
-// u of the CTA takes spans u, u + U, ... and columns (float4) lane % F; the
-// per-head max is a CTA-wide max, and the workers' sums are added in worker
-// order, so the result is deterministic.
+// u of the CTA takes spans u, u + U, ... and columns (float4) lane % F. Each
+// worker loads up to kChunk spans at once and folds them into a running
+// (max, denominator, sum); the workers are then folded together in worker
+// order. The order of every addition is fixed, so the result is deterministic.
 template <int D>
 __global__ void __launch_bounds__(128) merge_kernel(const StepArgs a, const int32_t *__restrict__ items) {
   constexpr int F = D / 4;          // float4 per output row
   constexpr int PER_WARP = 32 / F;  // workers per warp
   constexpr int U = 4 * PER_WARP;   // workers per CTA
-  __shared__ float s_max[4];
+  constexpr int kChunk = 8;
   __shared__ float4 s_acc[U][F];
-  __shared__ float s_l[U];
+  __shared__ float s_m[U], s_l[U];
   grid_dependency_wait();  // partials come from the decode kernel
 
   const int4 it = __ldg(reinterpret_cast<const int4 *>(items) + blockIdx.x);
@@ -486,40 +484,65 @@ __global__ void __launch_bounds__(128) merge_kernel(const StepArgs a, const int3
   const size_t hq = static_cast<size_t>(a.num_q_heads);
   const size_t base = static_cast<size_t>(pbase) * hq + h;
 
-  float mx = -INFINITY;
-  for (int i = u; i < spans; i += U) mx = fmaxf(mx, __ldg(a.partial_ml + (base + i * hq) * 2));
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
-  if (lane == 0) s_max[warp] = mx;
-  __syncthreads();
-  const float M = fmaxf(fmaxf(s_max[0], s_max[1]), fmaxf(s_max[2], s_max[3]));
-
+  float M = -INFINITY, lsum = 0.f;
   float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-  float lsum = 0.f;
-#pragma unroll 4
-  for (int i = u; i < spans; i += U) {
-    const size_t p = base + static_cast<size_t>(i) * hq;
-    const float w = exp2f(__ldg(a.partial_ml + p * 2) - M);
-    lsum += __ldg(a.partial_ml + p * 2 + 1) * w;
-    const float4 v = __ldg(reinterpret_cast<const float4 *>(a.partial_acc + p * D) + d4);
-    o.x += v.x * w;
-    o.y += v.y * w;
-    o.z += v.z * w;
-    o.w += v.w * w;
+  for (int c0 = u; c0 < spans; c0 += U * kChunk) {
+    float mi[kChunk], li[kChunk];
+    float4 ai[kChunk];
+#pragma unroll
+    for (int k = 0; k < kChunk; ++k) {
+      const int i = c0 + k * U;
+      mi[k] = -INFINITY;
+      li[k] = 0.f;
+      ai[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (i < spans) {
+        const size_t p = base + static_cast<size_t>(i) * hq;
+        mi[k] = __ldg(a.partial_ml + p * 2);
+        li[k] = __ldg(a.partial_ml + p * 2 + 1);
+        ai[k] = __ldg(reinterpret_cast<const float4 *>(a.partial_acc + p * D) + d4);
+      }
+    }
+    float cm = M;
+#pragma unroll
+    for (int k = 0; k < kChunk; ++k) cm = fmaxf(cm, mi[k]);
+    const float corr = M == -INFINITY ? 0.f : exp2f(M - cm);
+    lsum *= corr;
+    o.x *= corr;
+    o.y *= corr;
+    o.z *= corr;
+    o.w *= corr;
+    M = cm;
+#pragma unroll
+    for (int k = 0; k < kChunk; ++k) {
+      const float w = mi[k] == -INFINITY ? 0.f : exp2f(mi[k] - M);
+      lsum += li[k] * w;
+      o.x += ai[k].x * w;
+      o.y += ai[k].y * w;
+      o.z += ai[k].z * w;
+      o.w += ai[k].w * w;
+    }
   }
   s_acc[u][d4] = o;
-  if (d4 == 0) s_l[u] = lsum;
+  if (d4 == 0) {
+    s_m[u] = M;
+    s_l[u] = lsum;
+  }
   __syncthreads();
   if (threadIdx.x < F) {
-    float4 r = s_acc[0][threadIdx.x];
-    float L = s_l[0];
-    for (int k = 1; k < U; ++k) {
+    float Mx = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < U; ++k) Mx = fmaxf(Mx, s_m[k]);
+    float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
+    float L = 0.f;
+#pragma unroll
+    for (int k = 0; k < U; ++k) {
+      const float w = s_m[k] == -INFINITY ? 0.f : exp2f(s_m[k] - Mx);
       const float4 t = s_acc[k][threadIdx.x];
-      r.x += t.x;
-      r.y += t.y;
-      r.z += t.z;
-      r.w += t.w;
-      L += s_l[k];
+      r.x += t.x * w;
+      r.y += t.y * w;
+      r.z += t.z * w;
+      r.w += t.w * w;
+      L += s_l[k] * w;
     }
     const float inv = 1.f / L;
     uint2 packed;
@@ -541,25 +564,6 @@ int sm_count() {
     count[dev] = n;
   }
   return count[dev];
-}
-
-// Launch with programmatic stream serialization: the kernel may start while
-// the previous kernel in the stream drains; it calls griddepcontrol.wait
-// before touching any input.
-template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
-                       Args... args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
 template <int D, int NT>

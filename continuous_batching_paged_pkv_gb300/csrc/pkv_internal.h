@@ -45,6 +45,25 @@ cudaError_t launch_prefill(const StepArgs &a, const CUtensorMap &tmap_q, const C
                            const CUtensorMap &tmap_v, int32_t rows_per_tile, int32_t num_items,
                            const int32_t *items, cudaStream_t stream);
 
+// Launch with programmatic stream serialization: the kernel may start while
+// the previous kernel in the stream drains; it calls griddepcontrol.wait
+// before touching any input.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Positions per prefill tile: whole GQA groups fit one 128-row MMA tile.
 inline int32_t prefill_rows_per_tile(int32_t group) { return 128 / group; }
 

@@ -101,6 +101,8 @@ __global__ void __launch_bounds__(192, 1) prefill_kernel(const __grid_constant__
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = blockIdx.y;
+  launch_dependents();
+  grid_dependency_wait();  // every input may come from the previous kernel in the stream
   const int4 it = reinterpret_cast<const int4 *>(items)[blockIdx.x];
   const int seg = it.x, slot = it.y, tile = it.z;
   const int G = a.group, P = rows_per_tile;
@@ -353,8 +355,7 @@ cudaError_t launch_prefill_t(const StepArgs &a, const CUtensorMap &tq, const CUt
     configured = true;
   }
   dim3 grid(static_cast<unsigned>(num_items), static_cast<unsigned>(a.num_kv_heads));
-  prefill_kernel<D><<<grid, 192, smem, stream>>>(tq, tk, tv, a, items, rows_per_tile);
-  return cudaGetLastError();
+  return launch_pdl(prefill_kernel<D>, grid, dim3(192), smem, stream, tq, tk, tv, a, items, rows_per_tile);
 }
 
 }  // namespace
