@@ -120,6 +120,8 @@ pkv_status pkv_attention(const void *q, const int32_t *cu_seqlens_q, int32_t num
 
   pkv::StepArgs a{};
   a.q = q;
+  a.k_pool = k_pool;
+  a.v_pool = v_pool;
   a.cu_seqlens_q = cu_seqlens_q;
   a.seq_slot = seq_slot;
   a.context_lens = context_lens;
@@ -153,7 +155,8 @@ pkv_status pkv_attention(const void *q, const int32_t *cu_seqlens_q, int32_t num
   const int32_t *dec = work;
   const int32_t *pre = dec + static_cast<int64_t>(info->num_decode_items) * PKV_WORK_WORDS_PER_ITEM;
   const int32_t *comb = pre + static_cast<int64_t>(info->num_prefill_items) * PKV_WORK_WORDS_PER_ITEM;
-  cudaError_t e = pkv::launch_prefill(a, tq, tk, tv, rpt, info->num_prefill_items, pre, st);
+  cudaError_t e = head_dim == 128 ? pkv::launch_prefill_pair(a, tq, tk, tv, rpt, info->num_prefill_items, pre, st)
+                                  : pkv::launch_prefill(a, tq, rpt, info->num_prefill_items, pre, st);
   if (e == cudaSuccess) e = pkv::launch_decode(a, tk, tv, info->num_decode_items, dec, st);
   if (e == cudaSuccess) e = pkv::launch_merge(a, info->num_combine_items, comb, st);
   return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;

@@ -309,10 +309,13 @@ pkv_status pkv_plan_work(const int32_t *cu, int32_t num_seqs, const int32_t *seq
         partials += spans;
       }
     } else {
+      // head_dim 128 runs tiles in pairs on two SMs (the second may be past the segment's end).
       const int32_t tiles = static_cast<int32_t>(ceil_div(n, rows_per_tile));
-      for (int32_t t = 0; t < tiles; ++t) {
-        const int64_t last_row = std::min<int64_t>(n, static_cast<int64_t>(t + 1) * rows_per_tile);
-        pre.push_back({{s, slot, t, 0}, L - n + last_row});
+      const int32_t step = head_dim == 128 ? 2 : 1;
+      for (int32_t t = 0; t < tiles; t += step) {
+        const int32_t count = std::min(step, tiles - t);
+        const int64_t last_row = std::min<int64_t>(n, static_cast<int64_t>(t + count) * rows_per_tile);
+        pre.push_back({{s, slot, t, count}, L - n + last_row});
       }
     }
   }

@@ -15,6 +15,8 @@ constexpr int kSubKeys = 16;
 
 struct StepArgs {
   const void *q;
+  const void *k_pool;
+  const void *v_pool;
   const int32_t *cu_seqlens_q;
   const int32_t *seq_slot;
   const int32_t *context_lens;
@@ -41,9 +43,12 @@ cudaError_t launch_decode(const StepArgs &a, const CUtensorMap &tmap_k, const CU
 // One CTA per (multi-span segment, q head): merges the segment's span partials.
 cudaError_t launch_merge(const StepArgs &a, int32_t num_items, const int32_t *items, cudaStream_t stream);
 
-cudaError_t launch_prefill(const StepArgs &a, const CUtensorMap &tmap_q, const CUtensorMap &tmap_k,
-                           const CUtensorMap &tmap_v, int32_t rows_per_tile, int32_t num_items,
-                           const int32_t *items, cudaStream_t stream);
+cudaError_t launch_prefill(const StepArgs &a, const CUtensorMap &tmap_q, int32_t rows_per_tile,
+                           int32_t num_items, const int32_t *items, cudaStream_t stream);
+// head_dim 128: items are tile pairs, run by clusters of two CTAs.
+cudaError_t launch_prefill_pair(const StepArgs &a, const CUtensorMap &tmap_q, const CUtensorMap &tmap_k,
+                                const CUtensorMap &tmap_v, int32_t rows_per_tile, int32_t num_items,
+                                const int32_t *items, cudaStream_t stream);
 
 // Launch with programmatic stream serialization: the kernel may start while
 // the previous kernel in the stream drains; it calls griddepcontrol.wait

@@ -1,0 +1,442 @@
+// Prompt-chunk attention for head_dim 128 on SM pairs (tcgen05 cta_group::2).
+//
+// Lucebox, "Continuous batching: Qwen3.8-27B at 301 tok/s across five
+// clients, up to 1.97x llama.cpp", §Chunked prefill is a slot phase (a chunk
+// of a prompt appends to its slot and attends the slot's whole history) and
+// §Packing unequal prompt chunks together (per-query causal positions let
+// prompt rows share the call with decode rows). Tutorial 15, "Continuous
+// Batching and Scheduling", §9 Summary: prefill is large matrix products.
+//
+// A cluster of two CTAs on two SMs runs two consecutive 128-row query tiles
+// of one (segment, kv head): rows are P query positions x G grouped q heads
+// (row m = position m/G, head m%G). The even CTA issues M = 256 MMAs that
+// span both tiles. B operands are split by N between the CTAs, so each SM
+// loads half of every K/V tile: the keys [64r, 64r+64) of K and the head_dim
+// columns [64r, 64r+64) of V, for CTA r. With 2 KiB TMA boxes (the largest
+// this pool layout allows) one SM receives about 27 B/clk; a 128-row tile
+// alone would need about 60 B/clk to keep its tensor core busy, a pair needs
+// half of that per SM.
+//
+//   warp 0 (32 lanes)  TMA producer, both CTAs: Q once, then per 128-key tile
+//                      16 boxes of this CTA's halves, counted on the even
+//                      CTA's barriers; four stages.
+//   warp 1 (one lane)  MMA issuer, even CTA only:
+//                        S_j = Q K_j^T    (SS, M 256, N 128 keys)
+//                        O  += P_j V_j    (TS, A = P in TMEM, N 128 = head_dim)
+//                        l  += P_j 1      (TS, N 32, B = ones)
+//                      commits arrive on the barrier of both CTAs.
+//   warps 2-5          softmax, both CTAs: thread = TMEM lane = row; masks the
+//                      causal/ragged edge, writes P_j = 2^(s*scale*log2e - m)
+//                      as bf16 over S_j, rescales O and l only when the running
+//                      max grew by more than 2^8; final normalisation and store.
+//
+// The rows past a segment's last tile (an odd tile count) belong to a CTA that
+// still loads its halves and runs the softmax, but stores nothing.
+//
+// TMEM columns (same in both CTAs): [0,128) S/P buffer 0, [128,256) S/P buffer
+// 1, [256,384) O, [384,416) l (all 32 columns equal). Every mbarrier wait is
+// bounded; on expiry the CTA records PKV_DEV_TIMEOUT and both CTAs still meet
+// at the closing cluster barrier, after the MMAs drained, before TMEM is freed.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+
+#include "pkv_internal.h"
+#include "pkv_ptx.cuh"
+
+namespace pkv {
+namespace {
+
+constexpr int D = 128;
+constexpr int kKeysPerTile = 128;
+constexpr int kSubPerTile = kKeysPerTile / kSubKeys;  // 8 sub-tiles of 16 keys
+constexpr int kStages = 4;
+constexpr int kTmemCols = 512;
+constexpr int kOCol = 256;
+constexpr int kLCol = kOCol + D;
+constexpr int kThreads = 192;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when the max grows by > 256x
+constexpr uint32_t kFull = 0xffffffffu;
+constexpr uint32_t kNegInfBits = 0xff800000u;
+constexpr uint32_t kSleepNs = 20000;
+
+struct Layout {
+  static constexpr int kQHalf = 128 * 128;                 // 128 rows x 128 B: one 64-column half of D
+  static constexpr int kQBytes = 2 * kQHalf;
+  static constexpr int kKHalf = (kKeysPerTile / 2) * 128;  // this CTA's 64 keys x 128 B
+  static constexpr int kKBytes = 2 * kKHalf;
+  static constexpr int kVBytes = kKeysPerTile * 128;       // 128 keys x this CTA's 64 columns
+  static constexpr int kStageBytes = kKBytes + kVBytes;    // 32 KiB: 16 boxes of 2 KiB
+  static constexpr int kOnesOffset = kQBytes + kStages * kStageBytes;
+  static constexpr int kBarOffset = kOnesOffset + 1024;
+  static constexpr int kSmem = kBarOffset + 256 + 1024;    // barriers/flags + alignment slack
+};
+
+enum Bar : int {
+  kQFull = 0,      // even CTA: both Q tiles
+  kKVFull = 1,     // +stage; even CTA: both CTAs' halves of a K/V tile
+  kKVEmpty = 5,    // +stage; both CTAs
+  kSFull = 9,      // +buffer; both CTAs
+  kPReady = 11,    // +buffer; even CTA: one arrival per softmax warp of the pair
+  kPVDone = 13,    // +buffer; both CTAs
+  kDrain = 15,
+  kNumBars = 16
+};
+
+__device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
+  return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+// Wait that also gives up as soon as another role of this CTA has aborted.
+// `cluster` selects cluster-scope acquire (barriers the other CTA arrives on).
+template <bool cluster = false>
+__device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, volatile int *abort) {
+  auto poll = [&]() {
+    return cluster ? mbar_try_wait_cluster(bar, parity, kSleepNs) : mbar_try_wait_sleep(bar, parity, kSleepNs);
+  };
+  if (poll()) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (poll()) return true;
+    if ((i & 15u) == 0) {
+      if (*abort) return false;
+      if (global_timer_ns() - t0 > 1000000000ull) {
+        *abort = 1;
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ bool warp_wait_or_abort(uint64_t *bar, uint32_t parity, volatile int *abort) {
+  return __all_sync(kFull, wait_or_abort(bar, parity, abort));
+}
+
+__global__ void __launch_bounds__(kThreads, 1) prefill_pair_kernel(const __grid_constant__ CUtensorMap tmap_q,
+                                                                   const __grid_constant__ CUtensorMap tmap_k,
+                                                                   const __grid_constant__ CUtensorMap tmap_v,
+                                                                   const StepArgs a,
+                                                                   const int32_t *__restrict__ items,
+                                                                   int rows_per_tile) {
+  using Lay = Layout;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = align1024(smem_raw);
+  uint8_t *sQ = smem;
+  uint8_t *sKV = smem + Lay::kQBytes;
+  uint8_t *sOnes = smem + Lay::kOnesOffset;
+  uint64_t *bar = reinterpret_cast<uint64_t *>(smem + Lay::kBarOffset);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + kNumBars);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = blockIdx.y;
+  const uint32_t rank = cluster_ctarank();  // 0 issues the MMAs
+  launch_dependents();
+  grid_dependency_wait();  // every input may come from the previous kernel in the stream
+  const int4 it = reinterpret_cast<const int4 *>(items)[blockIdx.x >> 1];
+  const int seg = it.x, slot = it.y, tile0 = it.z;
+  const int G = a.group, P = rows_per_tile;
+
+  // Both CTAs of the pair read the same item, so they agree on `bad` and leave together.
+  bool bad = seg < 0 || seg >= a.num_seqs || slot < 0 || slot >= a.max_slots || tile0 < 0;
+  int row0 = 0, n = 0, L = 0;
+  if (!bad) {
+    row0 = a.cu_seqlens_q[seg];
+    n = a.cu_seqlens_q[seg + 1] - row0;
+    L = a.context_lens[slot];
+    bad = a.seq_slot[seg] != slot || n < 2 || n > L ||
+          static_cast<int64_t>(L) > static_cast<int64_t>(a.max_blocks_per_slot) * a.block_size ||
+          tile0 * P >= n || row0 < 0 || static_cast<int64_t>(row0) + n > a.total_q;
+  }
+  if (bad) {
+    if (threadIdx.x == 0 && rank == 0 && a.status) atomicOr(a.status, PKV_DEV_BAD_SEGMENT);
+    return;
+  }
+  const int q_tiles = (n + P - 1) / P;
+  const int tile = tile0 + static_cast<int>(rank);
+  const bool present = tile < q_tiles;              // else: rows past the segment, nothing stored
+  const int pos0 = (present ? tile : tile0) * P;    // first query row of this CTA's tile
+  const int rows = present ? min(P, n - pos0) : 0;
+  const int last = min(tile0 + 1, q_tiles - 1);     // the pair's last present tile
+  const int kv_end = L - n + min(n, (last + 1) * P);  // keys [0, kv_end) are visible to some row of the pair
+  const int ntiles = (kv_end + kKeysPerTile - 1) / kKeysPerTile;
+  const int32_t *bt_row = a.block_tables + static_cast<int64_t>(slot) * a.max_blocks_per_slot;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kNumBars; ++i) mbar_init(bar + i, (i == kPReady || i == kPReady + 1) ? 8 : 1);
+    fence_barrier_init();
+    *abort_flag = 0;
+  }
+  // Rows of the Q tile beyond G*P whole groups stay zero; the ones tile for the row sums.
+  {
+    const int qrows = G * P;
+    const int chunks = (128 - qrows) * 8;  // 16-byte chunks per half
+    for (int i = threadIdx.x; i < chunks * 2; i += blockDim.x) {
+      const int h = i / chunks, rem = i % chunks;
+      *reinterpret_cast<uint4 *>(sQ + h * Lay::kQHalf + (qrows + rem / 8) * 128 + (rem % 8) * 16) =
+          make_uint4(0, 0, 0, 0);
+    }
+    const uint32_t one2 = 0x3F803F80u;  // two bf16 1.0
+    for (int i = threadIdx.x; i < 1024 / 16; i += blockDim.x)
+      *reinterpret_cast<uint4 *>(sOnes + i * 16) = make_uint4(one2, one2, one2, one2);
+    fence_proxy_async_smem();
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_slot, kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync();  // barriers initialised and zero/ones tiles written in both CTAs
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    // Lane u < 8 holds the pool row of sub-tile u of a tile (0 when the block
+    // ID is outside the pool: the load stays in bounds, the status word
+    // reports it), loaded one tile ahead.
+    auto tile_row = [&](int j) -> int {
+      const int key = j * kKeysPerTile + lane * kSubKeys;
+      if (lane >= kSubPerTile || key >= kv_end) return 0;
+      const int blk = __ldg(bt_row + key / a.block_size);
+      if (blk < 0 || blk >= a.num_blocks) {
+        if (a.status) atomicOr(a.status, PKV_DEV_BAD_BLOCK);
+        return 0;
+      }
+      return (blk * a.num_kv_heads + g) * a.block_size + key % a.block_size;
+    };
+    int row_next = tile_row(0);
+    const uint32_t q_full = cluster_addr(bar + kQFull, 0);
+    if (lane == 0) {
+      prefetch_tensormap(&tmap_q);
+      prefetch_tensormap(&tmap_k);
+      prefetch_tensormap(&tmap_v);
+      if (rank == 0) mbar_arrive_expect_tx(bar + kQFull, 2 * 2 * G * P * 128);
+      for (int h = 0; h < 2; ++h)
+        tma_load_3d_pair(sQ + h * Lay::kQHalf, &tmap_q, h * 64, g * G, row0 + pos0, q_full);
+    }
+    // Lane l < 8 loads K sub-tile 4r + l/2, half l%2; lane 8 <= l < 16 loads
+    // V sub-tile l-8, this CTA's half of head_dim.
+    const bool is_k = lane < 8;
+    const int u = is_k ? static_cast<int>(rank) * 4 + (lane >> 1) : lane - 8;
+    const int x = is_k ? (lane & 1) * 64 : static_cast<int>(rank) * 64;
+    const int dst_off = is_k ? (lane & 1) * Lay::kKHalf + (lane >> 1) * kSubKeys * 128
+                             : Lay::kKBytes + (lane - 8) * kSubKeys * 128;
+    for (int j = 0; j < ntiles; ++j) {
+      const int s = j % kStages;
+      if (j >= kStages && !warp_wait_or_abort(bar + kKVEmpty + s, ((j - kStages) / kStages) & 1, abort_flag)) break;
+      const int row_cur = row_next;
+      if (j + 1 < ntiles) row_next = tile_row(j + 1);
+      const int kt0 = j * kKeysPerTile;
+      const int vs = min(kSubPerTile, (kv_end - kt0 + kSubKeys - 1) / kSubKeys);  // sub-tiles with a visible key
+      const uint32_t kv_full = cluster_addr(bar + kKVFull + s, 0);
+      // The pair loads 4 boxes per visible sub-tile: two K halves (one CTA) and two V halves (one each).
+      if (rank == 0 && lane == 0) mbar_arrive_expect_tx(bar + kKVFull + s, vs * 4 * 2048);
+      const int urow = __shfl_sync(kFull, row_cur, u & 7);
+      if (lane < 16 && u < vs)
+        tma_load_2d_pair(sKV + s * Lay::kStageBytes + dst_off, is_k ? &tmap_k : &tmap_v, x, urow, kv_full);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (rank == 0 && lane == 0) {
+      constexpr uint32_t idesc_qk = idesc_bf16_f32(256, kKeysPerTile, 0, 0);
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(256, D, 0, 1);
+      constexpr uint32_t idesc_l = idesc_bf16_f32(256, 32, 0, 0);
+      const uint32_t q_base = smem_addr(sQ);
+      const uint64_t ones_desc = smem_desc_noswz(smem_addr(sOnes), 128, 256);
+      auto issue_pv = [&](int jj) -> bool {
+        const int sp = jj & 1;
+        if (!wait_or_abort<true>(bar + kPReady + sp, (jj >> 1) & 1, abort_flag)) return false;
+        tc_fence_after();
+        const int valid = min(kKeysPerTile, kv_end - jj * kKeysPerTile);
+        const int ksteps = (valid + kSubKeys - 1) / kSubKeys;
+        const uint32_t v_base = smem_addr(sKV + (jj % kStages) * Lay::kStageBytes + Lay::kKBytes);
+        for (int ks = 0; ks < ksteps; ++ks) {
+          const uint64_t bdesc = smem_desc_sw128(v_base + ks * kSubKeys * 128, Lay::kVBytes, 1024);
+          const uint32_t acc = (jj > 0 || ks > 0) ? 1u : 0u;
+          tc_mma_ts_pair(tmem + kOCol, tmem + sp * 128 + ks * 8, bdesc, idesc_pv, acc);
+          tc_mma_ts_pair(tmem + kLCol, tmem + sp * 128 + ks * 8, ones_desc, idesc_l, acc);
+        }
+        tc_commit_pair(bar + kPVDone + sp);
+        tc_commit_pair(bar + kKVEmpty + jj % kStages);
+        return true;
+      };
+      bool ok = wait_or_abort(bar + kQFull, 0, abort_flag);
+      tc_fence_after();
+      for (int j = 0; ok && j < ntiles; ++j) {
+        const int s = j & 1;
+        if (j >= 2 && !(ok = wait_or_abort(bar + kPVDone + s, ((j - 2) >> 1) & 1, abort_flag))) break;
+        if (!(ok = wait_or_abort(bar + kKVFull + j % kStages, (j / kStages) & 1, abort_flag))) break;
+        tc_fence_after();
+        const uint32_t k_base = smem_addr(sKV + (j % kStages) * Lay::kStageBytes);
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t qoff = (kk >> 2) * Lay::kQHalf + (kk & 3) * 32;
+          const uint32_t koff = (kk >> 2) * Lay::kKHalf + (kk & 3) * 32;
+          tc_mma_ss_pair(tmem + s * 128, smem_desc_sw128(q_base + qoff, 16, 1024),
+                         smem_desc_sw128(k_base + koff, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+        }
+        tc_commit_pair(bar + kSFull + s);
+        if (j >= 1 && !(ok = issue_pv(j - 1))) break;
+      }
+      if (ok) issue_pv(ntiles - 1);
+      tc_commit_pair(bar + kDrain);
+      if (!wait_or_abort(bar + kDrain, 0, abort_flag) && a.status) atomicOr(a.status, PKV_DEV_TIMEOUT);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int qw = warp & 3;
+    const int mrow = qw * 32 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(qw * 32) << 16;
+    const int pos = mrow / G, hh = mrow % G;
+    const bool row_valid = mrow < G * P && pos < rows;
+    const int p_row = L - n + pos0 + pos;  // last visible key of this row (inclusive)
+    const float sl2 = a.scale_log2;
+    const uint32_t p_ready0 = cluster_addr(bar + kPReady, 0);
+    float m_used = -INFINITY;  // log2 units
+    bool ok = true;
+    for (int j = 0; j < ntiles; ++j) {
+      const int s = j & 1;
+      if (!(ok = warp_wait_or_abort(bar + kSFull + s, (j >> 1) & 1, abort_flag))) break;
+      tc_fence_after();
+      uint32_t sv[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lane_base + s * 128 + c * 32, sv[c]);
+      tmem_wait_ld();
+      // Causal / ragged edge: only tiles that reach past some row's last key need a mask.
+      const int lim = min(p_row, kv_end - 1) - j * kKeysPerTile;
+      if (!__all_sync(kFull, lim >= kKeysPerTile - 1)) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (c * 32 + i > lim) sv[c][i] = kNegInfBits;
+      }
+      float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int i = 0; i < 32; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], __uint_as_float(sv[c][i]));
+      const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * sl2;
+      const float m_new = fmaxf(m_used, mx);
+      const bool need = j > 0 && m_new > m_used + kRescaleThreshold;
+      if (j == 0) m_used = m_new;
+      if (__any_sync(kFull, need)) {
+        // O and l must hold tile j-1's products before they are rescaled.
+        if (!(ok = warp_wait_or_abort(bar + kPVDone + ((j - 1) & 1), ((j - 1) >> 1) & 1, abort_flag))) break;
+        tc_fence_after();
+        const float corr = need ? ex2_approx(m_used - m_new) : 1.f;
+        if (need) m_used = m_new;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t ov[32];
+          tmem_ld32(tmem + lane_base + kOCol + c * 32, ov);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * corr);
+          tmem_st32(tmem + lane_base + kOCol + c * 32, ov);
+        }
+        uint32_t lv[32];
+        tmem_ld32(tmem + lane_base + kLCol, lv);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) lv[i] = __float_as_uint(__uint_as_float(lv[i]) * corr);
+        tmem_st32(tmem + lane_base + kLCol, lv);
+      }
+      const float nm = -m_used;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          pk[i] = pack_bf16x2(ex2_approx(fmaf(__uint_as_float(sv[c][2 * i]), sl2, nm)),
+                              ex2_approx(fmaf(__uint_as_float(sv[c][2 * i + 1]), sl2, nm)));
+        tmem_st16(tmem + lane_base + s * 128 + c * 16, pk);
+      }
+      if (j == ntiles - 1) {
+        // Zero this CTA's V rows past the last visible key inside the final
+        // 16-key step: a partly filled block may hold stale or NaN rows there,
+        // and 0 * NaN would reach O. The tile's data has landed (S_j exists).
+        const int valid = kv_end - j * kKeysPerTile;
+        const int tail = (kSubKeys - valid % kSubKeys) % kSubKeys;
+        if (tail) {
+          uint8_t *sV = sKV + (j % kStages) * Lay::kStageBytes + Lay::kKBytes;
+          for (int i = threadIdx.x - 64; i < tail * 8; i += 128)
+            *reinterpret_cast<uint4 *>(sV + (valid + i / 8) * 128 + (i % 8) * 16) = make_uint4(0, 0, 0, 0);
+          fence_proxy_async_smem();
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(p_ready0 + s * 8);
+    }
+    if (ok && warp_wait_or_abort(bar + kPVDone + ((ntiles - 1) & 1), ((ntiles - 1) >> 1) & 1, abort_flag)) {
+      tc_fence_after();
+      uint32_t lv[16];
+      tmem_ld16(tmem + lane_base + kLCol, lv);
+      tmem_wait_ld();
+      const float inv = 1.f / __uint_as_float(lv[0]);
+      __nv_bfloat16 *orow = reinterpret_cast<__nv_bfloat16 *>(a.out) +
+                            (static_cast<size_t>(row0 + pos0 + pos) * a.num_q_heads + g * G + hh) * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t ov[32];
+        tmem_ld32(tmem + lane_base + kOCol + c * 32, ov);
+        tmem_wait_ld();
+        if (row_valid) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            pk[i] = pack_bf16x2(__uint_as_float(ov[2 * i]) * inv, __uint_as_float(ov[2 * i + 1]) * inv);
+          uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  cluster_sync();  // both CTAs are done with TMEM and the MMAs have drained
+  if (*abort_flag && threadIdx.x == 0 && a.status) atomicOr(a.status, PKV_DEV_TIMEOUT);
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_pair(const StepArgs &a, const CUtensorMap &tq, const CUtensorMap &tk,
+                                const CUtensorMap &tv, int32_t rows_per_tile, int32_t num_items,
+                                const int32_t *items, cudaStream_t stream) {
+  if (num_items <= 0) return cudaSuccess;
+  constexpr int smem = Layout::kSmem;
+  static uint64_t configured = 0;  // one bit per device
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(configured & bit)) {
+    cudaError_t e = cudaFuncSetAttribute(prefill_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    configured |= bit;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * num_items), static_cast<unsigned>(a.num_kv_heads));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, prefill_pair_kernel, tq, tk, tv, a, items, rows_per_tile);
+}
+
+}  // namespace pkv

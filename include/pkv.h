@@ -190,15 +190,20 @@ pkv_status pkv_plan_lower(pkv_pool *pool, const pkv_segment *plan, int32_t num_s
  * only on that segment's context, so a row's result does not depend on what
  * else is in the batch); a merge kernel combines a segment's spans in order.
  * Segments with several rows (prompt chunks) go to the tensor-core chunk
- * kernel, in tiles of query rows. The pages leave this split open; it is
- * this library's design.
+ * kernel, in tiles of 128 / (num_q_heads / num_kv_heads) query rows; with
+ * head_dim 128 one item is a pair of consecutive tiles run by two SMs
+ * together. The pages leave this split open; it is this library's design.
+ *
+ * Item words: decode (segment, slot, key span, first partial or -1);
+ * prefill (segment, slot, first query tile, tiles in the item: 1 or 2);
+ * merge (segment, slot, spans, first partial).
  * ---------------------------------------------------------------------- */
 #define PKV_SPLIT_KEYS 256
 #define PKV_WORK_WORDS_PER_ITEM 4
 
 typedef struct pkv_work_info {
     int32_t num_decode_items;  /* (segment, key span) items */
-    int32_t num_prefill_items; /* (segment, query tile) items */
+    int32_t num_prefill_items; /* (segment, query tile or tile pair) items */
     int32_t num_combine_items; /* (segment) merge items: decode segments with more than one span */
     int32_t num_partials;      /* span results kept in the workspace */
     int64_t work_words;        /* int32 words of the item array: decode, prefill, then merge items */

@@ -170,11 +170,12 @@ def test_work_list_items():
     ctx = np.zeros(8, np.int32)
     ctx[[3, 1, 6, 2]] = [1536, 2 * S + 1, 2 * S, 1]
     work, info = _work([0, 512, 513, 514, 515], [3, 1, 6, 2], ctx, max_blocks_per_slot=128)
-    # decode spans: 3 for slot 1 (S, S, 1 keys), 2 for slot 6, 1 for slot 2; the chunk has 16 tiles
-    assert (info.num_decode_items, info.num_prefill_items, info.num_combine_items) == (6, 16, 2)
+    # decode spans: 3 for slot 1 (S, S, 1 keys), 2 for slot 6, 1 for slot 2; the chunk has 16 tiles,
+    # run as 8 pairs at head_dim 128
+    assert (info.num_decode_items, info.num_prefill_items, info.num_combine_items) == (6, 8, 2)
     items = work.reshape(-1, 4)
-    assert len(items) == 24
-    dec, pre, comb = items[:6], items[6:22], items[22:]
+    assert len(items) == 16
+    dec, pre, comb = items[:6], items[6:14], items[14:]
     assert [list(c) for c in comb] == [[1, 1, 3, 0], [2, 6, 2, 3]]  # (seg, slot, spans, partial base)
     assert sorted(map(tuple, dec[:, :3].tolist())) == [(1, 1, 0), (1, 1, 1), (1, 1, 2), (2, 6, 0), (2, 6, 1),
                                                         (3, 2, 0)]
@@ -185,8 +186,9 @@ def test_work_list_items():
     assert bases[(1, 1, 0)] == bases[(1, 1, 1)] == bases[(1, 1, 2)] == 0
     assert bases[(2, 6, 0)] == bases[(2, 6, 1)] == 3 and bases[(3, 2, 0)] == -1
     assert info.num_partials == 5
-    assert sorted(pre[:, 2].tolist()) == list(range(16)) and (pre[:, :2] == [0, 3]).all()
-    assert pre[0, 2] == 15  # the tile that sees the most keys first
+    assert sorted(pre[:, 2].tolist()) == list(range(0, 16, 2)) and (pre[:, :2] == [0, 3]).all()
+    assert (pre[:, 3] == 2).all()
+    assert pre[0, 2] == 14  # the pair that sees the most keys first
     a256 = lambda x: (x + 255) // 256 * 256
     assert info.workspace_bytes == a256(5 * 32 * 128 * 4) + a256(5 * 32 * 2 * 4)
 
@@ -204,6 +206,23 @@ def test_work_list_validation(cu, slots, ctx_pairs, err):
         ctx[k] = v
     with pytest.raises(B.PkvError, match=err):
         _work(cu, slots, ctx)
+
+
+def test_work_list_tile_pairs():
+    """head_dim 128 pairs consecutive tiles; an odd tile count leaves a single at the end; head_dim 64 does not pair."""
+    ctx = np.zeros(8, np.int32)
+    ctx[[0, 1]] = [100, 90]
+    # group 4: 32 rows per tile; 80 and 70 rows are 3 tiles each: a pair and a single
+    work, info = _work([0, 80, 150], [0, 1], ctx)
+    pre = work.reshape(-1, 4)
+    assert info.num_prefill_items == 4
+    by_seg = {}
+    for seg, slot, t, c in pre.tolist():
+        by_seg.setdefault(seg, []).append((t, c))
+    assert sorted(by_seg[0]) == [(0, 2), (2, 1)]          # 80 rows: 3 tiles
+    assert sorted(by_seg[1]) == [(0, 2), (2, 1)]          # 70 rows: 3 tiles
+    work64, info64 = _work([0, 80, 150], [0, 1], ctx, head_dim=64)
+    assert info64.num_prefill_items == 6 and (work64.reshape(-1, 4)[:, 3] == 1).all()
 
 
 def test_work_list_unsupported_shapes():
