@@ -20,21 +20,26 @@
 //   warp 0 (32 lanes)  TMA producer, both CTAs: Q once, then per 128-key tile
 //                      16 boxes of this CTA's halves, counted on the even
 //                      CTA's barriers; four stages.
-//   warp 1 (one lane)  MMA issuer, even CTA only:
-//                        S_j = Q K_j^T    (SS, M 256, N 128 keys)
-//                        O  += P_j V_j    (TS, A = P in TMEM, N 128 = head_dim)
-//                        l  += P_j 1      (TS, N 32, B = ones)
-//                      commits arrive on the barrier of both CTAs.
+//   warp 1 (one lane)  QK issuer, even CTA only: S_j = Q K_j^T (SS, M 256,
+//                      N 128 keys) into S/P buffer j % 3, as soon as that
+//                      buffer's previous P V product has finished.
+//   warp 6 (one lane)  PV issuer, even CTA only: O += P_j V_j (TS, A = P in
+//                      TMEM, N 128 = head_dim) as soon as P_j is written.
+//                      A tcgen05.mma issue blocks its thread until the tensor
+//                      pipe takes it, so one thread issuing both streams would
+//                      serialise them with its waits; two issuers keep the
+//                      pipe fed. Commits arrive on the barriers of both CTAs.
 //   warps 2-5          softmax, both CTAs: thread = TMEM lane = row; masks the
 //                      causal/ragged edge, writes P_j = 2^(s*scale*log2e - m)
-//                      as bf16 over S_j, rescales O and l only when the running
-//                      max grew by more than 2^8; final normalisation and store.
+//                      as bf16 over S_j, keeps the row sum l in fp32 registers,
+//                      rescales O and l only when the running max grew by more
+//                      than 2^8; final normalisation and store.
 //
 // The rows past a segment's last tile (an odd tile count) belong to a CTA that
 // still loads its halves and runs the softmax, but stores nothing.
 //
-// TMEM columns (same in both CTAs): [0,128) S/P buffer 0, [128,256) S/P buffer
-// 1, [256,384) O, [384,416) l (all 32 columns equal). Every mbarrier wait is
+// TMEM columns (same in both CTAs): [128b, 128b+128) S/P buffer b for b < 3,
+// [384,512) O. Every mbarrier wait is
 // bounded; on expiry the CTA records PKV_DEV_TIMEOUT and both CTAs still meet
 // at the closing cluster barrier, after the MMAs drained, before TMEM is freed.
 #include <cuda_bf16.h>
@@ -52,13 +57,12 @@ constexpr int kKeysPerTile = 128;
 constexpr int kSubPerTile = kKeysPerTile / kSubKeys;  // 8 sub-tiles of 16 keys
 constexpr int kStages = 4;
 constexpr int kTmemCols = 512;
-constexpr int kOCol = 256;
-constexpr int kLCol = kOCol + D;
-constexpr int kThreads = 192;
+constexpr int kSBufs = 3;      // S/P buffers in TMEM
+constexpr int kOCol = 384;
+constexpr int kThreads = 224;  // producer, QK issuer, 4 softmax warps, PV issuer
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when the max grows by > 256x
 constexpr uint32_t kFull = 0xffffffffu;
 constexpr uint32_t kNegInfBits = 0xff800000u;
-constexpr uint32_t kSleepNs = 20000;
 
 struct Layout {
   static constexpr int kQHalf = 128 * 128;                 // 128 rows x 128 B: one 64-column half of D
@@ -67,8 +71,7 @@ struct Layout {
   static constexpr int kKBytes = 2 * kKHalf;
   static constexpr int kVBytes = kKeysPerTile * 128;       // 128 keys x this CTA's 64 columns
   static constexpr int kStageBytes = kKBytes + kVBytes;    // 32 KiB: 16 boxes of 2 KiB
-  static constexpr int kOnesOffset = kQBytes + kStages * kStageBytes;
-  static constexpr int kBarOffset = kOnesOffset + 1024;
+  static constexpr int kBarOffset = kQBytes + kStages * kStageBytes;
   static constexpr int kSmem = kBarOffset + 256 + 1024;    // barriers/flags + alignment slack
 };
 
@@ -76,11 +79,12 @@ enum Bar : int {
   kQFull = 0,      // even CTA: both Q tiles
   kKVFull = 1,     // +stage; even CTA: both CTAs' halves of a K/V tile
   kKVEmpty = 5,    // +stage; both CTAs
-  kSFull = 9,      // +buffer; both CTAs
-  kPReady = 11,    // +buffer; even CTA: one arrival per softmax warp of the pair
-  kPVDone = 13,    // +buffer; both CTAs
-  kDrain = 15,
-  kNumBars = 16
+  kSFull = 9,      // +buffer (3); both CTAs
+  kPReady = 12,    // +buffer (3); even CTA: one arrival per softmax warp of the pair
+  kPVDone = 15,    // +buffer (3); both CTAs
+  kDrain = 18,     // QK issuer's MMAs complete
+  kDrainPV = 19,   // PV issuer's MMAs complete
+  kNumBars = 20
 };
 
 __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
@@ -89,11 +93,11 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
 
 // Wait that also gives up as soon as another role of this CTA has aborted.
 // `cluster` selects cluster-scope acquire (barriers the other CTA arrives on).
+// Plain try_wait (no suspend-time hint): every wait here is on the critical
+// path of the tile pipeline, and a suspended thread can resume late.
 template <bool cluster = false>
 __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, volatile int *abort) {
-  auto poll = [&]() {
-    return cluster ? mbar_try_wait_cluster(bar, parity, kSleepNs) : mbar_try_wait_sleep(bar, parity, kSleepNs);
-  };
+  auto poll = [&]() { return cluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
   if (poll()) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t i = 1;; ++i) {
@@ -123,7 +127,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_pair_kernel(const __grid_
   uint8_t *smem = align1024(smem_raw);
   uint8_t *sQ = smem;
   uint8_t *sKV = smem + Lay::kQBytes;
-  uint8_t *sOnes = smem + Lay::kOnesOffset;
   uint64_t *bar = reinterpret_cast<uint64_t *>(smem + Lay::kBarOffset);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + kNumBars);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
@@ -163,11 +166,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_pair_kernel(const __grid_
   const int32_t *bt_row = a.block_tables + static_cast<int64_t>(slot) * a.max_blocks_per_slot;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kNumBars; ++i) mbar_init(bar + i, (i == kPReady || i == kPReady + 1) ? 8 : 1);
+    for (int i = 0; i < kNumBars; ++i) mbar_init(bar + i, (i >= kPReady && i < kPReady + kSBufs) ? 8 : 1);
     fence_barrier_init();
     *abort_flag = 0;
   }
-  // Rows of the Q tile beyond G*P whole groups stay zero; the ones tile for the row sums.
+  // Rows of the Q tile beyond G*P whole groups stay zero.
   {
     const int qrows = G * P;
     const int chunks = (128 - qrows) * 8;  // 16-byte chunks per half
@@ -176,9 +179,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_pair_kernel(const __grid_
       *reinterpret_cast<uint4 *>(sQ + h * Lay::kQHalf + (qrows + rem / 8) * 128 + (rem % 8) * 16) =
           make_uint4(0, 0, 0, 0);
     }
-    const uint32_t one2 = 0x3F803F80u;  // two bf16 1.0
-    for (int i = threadIdx.x; i < 1024 / 16; i += blockDim.x)
-      *reinterpret_cast<uint4 *>(sOnes + i * 16) = make_uint4(one2, one2, one2, one2);
     fence_proxy_async_smem();
   }
   if (warp == 1) {
@@ -186,7 +186,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_pair_kernel(const __grid_
     tmem_relinquish_pair();
   }
   tc_fence_before();
-  cluster_sync();  // barriers initialised and zero/ones tiles written in both CTAs
+  cluster_sync();  // barriers initialised and Q padding written in both CTAs
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
@@ -237,35 +237,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_pair_kernel(const __grid_
         tma_load_2d_pair(sKV + s * Lay::kStageBytes + dst_off, is_k ? &tmap_k : &tmap_v, x, urow, kv_full);
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ QK issuer
     if (rank == 0 && lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(256, kKeysPerTile, 0, 0);
-      constexpr uint32_t idesc_pv = idesc_bf16_f32(256, D, 0, 1);
-      constexpr uint32_t idesc_l = idesc_bf16_f32(256, 32, 0, 0);
       const uint32_t q_base = smem_addr(sQ);
-      const uint64_t ones_desc = smem_desc_noswz(smem_addr(sOnes), 128, 256);
-      auto issue_pv = [&](int jj) -> bool {
-        const int sp = jj & 1;
-        if (!wait_or_abort<true>(bar + kPReady + sp, (jj >> 1) & 1, abort_flag)) return false;
-        tc_fence_after();
-        const int valid = min(kKeysPerTile, kv_end - jj * kKeysPerTile);
-        const int ksteps = (valid + kSubKeys - 1) / kSubKeys;
-        const uint32_t v_base = smem_addr(sKV + (jj % kStages) * Lay::kStageBytes + Lay::kKBytes);
-        for (int ks = 0; ks < ksteps; ++ks) {
-          const uint64_t bdesc = smem_desc_sw128(v_base + ks * kSubKeys * 128, Lay::kVBytes, 1024);
-          const uint32_t acc = (jj > 0 || ks > 0) ? 1u : 0u;
-          tc_mma_ts_pair(tmem + kOCol, tmem + sp * 128 + ks * 8, bdesc, idesc_pv, acc);
-          tc_mma_ts_pair(tmem + kLCol, tmem + sp * 128 + ks * 8, ones_desc, idesc_l, acc);
-        }
-        tc_commit_pair(bar + kPVDone + sp);
-        tc_commit_pair(bar + kKVEmpty + jj % kStages);
-        return true;
-      };
       bool ok = wait_or_abort(bar + kQFull, 0, abort_flag);
       tc_fence_after();
       for (int j = 0; ok && j < ntiles; ++j) {
-        const int s = j & 1;
-        if (j >= 2 && !(ok = wait_or_abort(bar + kPVDone + s, ((j - 2) >> 1) & 1, abort_flag))) break;
+        const int s = j % kSBufs;
+        // S buffer s last held P_{j-3}: its product with V must have finished.
+        if (j >= kSBufs && !(ok = wait_or_abort(bar + kPVDone + s, ((j - kSBufs) / kSBufs) & 1, abort_flag))) break;
         if (!(ok = wait_or_abort(bar + kKVFull + j % kStages, (j / kStages) & 1, abort_flag))) break;
         tc_fence_after();
         const uint32_t k_base = smem_addr(sKV + (j % kStages) * Lay::kStageBytes);
@@ -276,11 +257,32 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_pair_kernel(const __grid_
                          smem_desc_sw128(k_base + koff, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
         }
         tc_commit_pair(bar + kSFull + s);
-        if (j >= 1 && !(ok = issue_pv(j - 1))) break;
       }
-      if (ok) issue_pv(ntiles - 1);
       tc_commit_pair(bar + kDrain);
       if (!wait_or_abort(bar + kDrain, 0, abort_flag) && a.status) atomicOr(a.status, PKV_DEV_TIMEOUT);
+    }
+    __syncwarp();
+  } else if (warp == 6) {
+    // ------------------------------------------------------------ PV issuer
+    if (rank == 0 && lane == 0) {
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(256, D, 0, 1);
+      for (int j = 0; j < ntiles; ++j) {
+        const int sp = j % kSBufs;
+        // P_j written by all eight softmax warps of the pair; V_j has landed (S_j used K_j of the same stage).
+        if (!wait_or_abort<true>(bar + kPReady + sp, (j / kSBufs) & 1, abort_flag)) break;
+        tc_fence_after();
+        const int valid = min(kKeysPerTile, kv_end - j * kKeysPerTile);
+        const int ksteps = (valid + kSubKeys - 1) / kSubKeys;
+        const uint32_t v_base = smem_addr(sKV + (j % kStages) * Lay::kStageBytes + Lay::kKBytes);
+        for (int ks = 0; ks < ksteps; ++ks) {
+          const uint64_t bdesc = smem_desc_sw128(v_base + ks * kSubKeys * 128, Lay::kVBytes, 1024);
+          tc_mma_ts_pair(tmem + kOCol, tmem + sp * 128 + ks * 8, bdesc, idesc_pv, (j > 0 || ks > 0) ? 1u : 0u);
+        }
+        tc_commit_pair(bar + kPVDone + sp);
+        tc_commit_pair(bar + kKVEmpty + j % kStages);
+      }
+      tc_commit_pair(bar + kDrainPV);
+      if (!wait_or_abort(bar + kDrainPV, 0, abort_flag) && a.status) atomicOr(a.status, PKV_DEV_TIMEOUT);
     }
     __syncwarp();
   } else {
@@ -295,9 +297,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_pair_kernel(const __grid_
     const uint32_t p_ready0 = cluster_addr(bar + kPReady, 0);
     float m_used = -INFINITY;  // log2 units
     bool ok = true;
+    float l_sum = 0.f;
     for (int j = 0; j < ntiles; ++j) {
-      const int s = j & 1;
-      if (!(ok = warp_wait_or_abort(bar + kSFull + s, (j >> 1) & 1, abort_flag))) break;
+      const int s = j % kSBufs;
+      if (!(ok = warp_wait_or_abort(bar + kSFull + s, (j / kSBufs) & 1, abort_flag))) break;
       tc_fence_after();
       uint32_t sv[4][32];
 #pragma unroll
@@ -322,11 +325,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_pair_kernel(const __grid_
       const bool need = j > 0 && m_new > m_used + kRescaleThreshold;
       if (j == 0) m_used = m_new;
       if (__any_sync(kFull, need)) {
-        // O and l must hold tile j-1's products before they are rescaled.
-        if (!(ok = warp_wait_or_abort(bar + kPVDone + ((j - 1) & 1), ((j - 1) >> 1) & 1, abort_flag))) break;
+        // O must hold tile j-1's products before it is rescaled.
+        if (!(ok = warp_wait_or_abort(bar + kPVDone + (j - 1) % kSBufs, ((j - 1) / kSBufs) & 1, abort_flag))) break;
         tc_fence_after();
         const float corr = need ? ex2_approx(m_used - m_new) : 1.f;
         if (need) m_used = m_new;
+        l_sum *= corr;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t ov[32];
@@ -336,21 +340,18 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_pair_kernel(const __grid_
           for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * corr);
           tmem_st32(tmem + lane_base + kOCol + c * 32, ov);
         }
-        uint32_t lv[32];
-        tmem_ld32(tmem + lane_base + kLCol, lv);
-        tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) lv[i] = __float_as_uint(__uint_as_float(lv[i]) * corr);
-        tmem_st32(tmem + lane_base + kLCol, lv);
       }
       const float nm = -m_used;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          pk[i] = pack_bf16x2(ex2_approx(fmaf(__uint_as_float(sv[c][2 * i]), sl2, nm)),
-                              ex2_approx(fmaf(__uint_as_float(sv[c][2 * i + 1]), sl2, nm)));
+        for (int i = 0; i < 16; ++i) {
+          const float p0 = ex2_approx(fmaf(__uint_as_float(sv[c][2 * i]), sl2, nm));
+          const float p1 = ex2_approx(fmaf(__uint_as_float(sv[c][2 * i + 1]), sl2, nm));
+          l_sum += p0 + p1;
+          pk[i] = pack_bf16x2(p0, p1);
+        }
         tmem_st16(tmem + lane_base + s * 128 + c * 16, pk);
       }
       if (j == ntiles - 1) {
@@ -369,14 +370,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_pair_kernel(const __grid_
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(p_ready0 + s * 8);
+      // Only the last tile also wrote shared memory (the V tail) for the MMA to read.
+      if (lane == 0) {
+        if (j == ntiles - 1)
+          mbar_arrive_cluster(p_ready0 + s * 8);
+        else
+          mbar_arrive_remote_cta_release(p_ready0 + s * 8);
+      }
     }
-    if (ok && warp_wait_or_abort(bar + kPVDone + ((ntiles - 1) & 1), ((ntiles - 1) >> 1) & 1, abort_flag)) {
+    if (ok && warp_wait_or_abort(bar + kPVDone + (ntiles - 1) % kSBufs, ((ntiles - 1) / kSBufs) & 1, abort_flag)) {
       tc_fence_after();
-      uint32_t lv[16];
-      tmem_ld16(tmem + lane_base + kLCol, lv);
-      tmem_wait_ld();
-      const float inv = 1.f / __uint_as_float(lv[0]);
+      const float inv = 1.f / l_sum;
       __nv_bfloat16 *orow = reinterpret_cast<__nv_bfloat16 *>(a.out) +
                             (static_cast<size_t>(row0 + pos0 + pos) * a.num_q_heads + g * G + hh) * D;
 #pragma unroll

@@ -88,6 +88,26 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// 2^x on the FMA pipe, to share the work of a softmax with the SFU.
+// Range reduction x = n + f with n = rint(x), taken from the low mantissa bits of
+// x + 1.5*2^23 (valid while |x| < 2^22), so f is in [-1/2, 1/2]; 2^f from the cubic
+// 1 + f(c1 + f(c2 + f c3)) whose coefficients were fitted to minimise the relative
+// error on that interval (max 1.02e-4, below bf16's 2^-9); 2^n is added straight
+// into the exponent field. x below -125 is clamped, giving 2^-125 (not 0).
+__device__ __forceinline__ float exp2_fma_poly(float x) {
+  x = fmaxf(x, -125.f);
+  const float t = x + 12582912.f;
+  const float f = x - (t - 12582912.f);
+  const float p = fmaf(f, fmaf(f, fmaf(f, 0.05500893f, 0.24221098f), 0.69328290f), 1.f);
+  return __uint_as_float(__float_as_uint(p) + (__float_as_uint(t) << 23));
+}
+
+// Two floats to bf16x2 by truncation (upper halves of the bit patterns; lo in
+// the low half). One byte permute on the integer pipe instead of a conversion.
+__device__ __forceinline__ uint32_t pack_bf16x2_trunc(float lo, float hi) {
+  return __byte_perm(__float_as_uint(lo), __float_as_uint(hi), 0x7632);
+}
+
 // Order this thread's generic-proxy shared-memory accesses before later
 // async-proxy (TMA, tcgen05.mma) accesses of the same memory.
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -321,15 +341,23 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster_addr) : "memory");
 }
 
+// Arrive on a barrier of either CTA of the pair with CTA-scope release: no
+// cluster-wide memory barrier. For signals that order only tcgen05 work that
+// the signalling thread has already waited for (tcgen05.wait::st followed by
+// tcgen05.fence::before_thread_sync), not generic memory writes.
+__device__ __forceinline__ void mbar_arrive_remote_cta_release(uint32_t bar_cluster_addr) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster_addr) : "memory");
+}
+
 // try_wait with cluster-scope acquire: for barriers the other CTA of the pair arrives on.
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity, uint32_t hint_ns) {
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity) {
   uint32_t done;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(done)
-      : "r"(smem_addr(bar)), "r"(parity), "r"(hint_ns)
+      : "r"(smem_addr(bar)), "r"(parity)
       : "memory");
   return done != 0;
 }
