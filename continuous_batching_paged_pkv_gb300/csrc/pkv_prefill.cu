@@ -196,11 +196,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     const uint8_t *kp = static_cast<const uint8_t *>(a.k_pool);
     const uint8_t *vp = static_cast<const uint8_t *>(a.v_pool);
     const int64_t row_bytes = static_cast<int64_t>(D) * 2;
-    // Lane u < 8 of each producer warp holds the pool row of sub-tile u of a
-    // tile (-1: the block ID is outside the pool), loaded one tile ahead.
-    auto tile_row = [&](int j) -> int {
-      const int key = j * kKeysPerTile + lane * kSubKeys;
-      if (lane >= kSubPerTile || key >= kv_end) return 0;
+    // Pool rows of the 16-key sub-tiles, four tiles per warp-wide load: lane l
+    // holds sub-tile l % 8 of tile t0 + l / 8 (0 for keys past the context;
+    // -1 when the block ID is outside the pool). The next group of four is
+    // loaded while the current one is in use.
+    auto group_rows = [&](int t0) -> int {
+      const int key = (t0 + (lane >> 3)) * kKeysPerTile + (lane & 7) * kSubKeys;
+      if (key >= kv_end) return 0;
       const int blk = __ldg(bt_row + key / a.block_size);
       if (blk < 0 || blk >= a.num_blocks) {
         if (a.status && warp == 0) atomicOr(a.status, PKV_DEV_BAD_BLOCK);
@@ -208,7 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       }
       return (blk * a.num_kv_heads + g) * a.block_size + key % a.block_size;
     };
-    int row_next = tile_row(0);
+    int rows_cur = group_rows(0), rows_next = group_rows(4);
     if (threadIdx.x == 0) {
       prefetch_tensormap(&tmap_q);
       mbar_arrive_expect_tx(bar + kQFull, H * G * P * 128);
@@ -221,8 +223,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       const int s = j % kStages;
       if (j >= kStages && !(ok = warp_wait_or_abort(bar + kKVEmpty + s, ((j - kStages) / kStages) & 1, abort_flag)))
         break;
-      const int row_cur = row_next;
-      if (j + 1 < ntiles) row_next = tile_row(j + 1);
+      if (j > 0 && (j & 3) == 0) {
+        rows_cur = rows_next;
+        rows_next = group_rows(j + 4);
+      }
       const int kt0 = j * kKeysPerTile;
       const uint32_t sK = smem_addr(sKV + s * Lay::kStageBytes);
       const uint32_t sV = sK + Lay::kKVBytes;
@@ -230,7 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       for (int k = 0; k < 64; ++k) {
         const int t = k >> 5, h = (k >> 4) & 1, u = (k >> 1) & 7;
         const int r = ((k & 1) << 3) + (p >> 3);
-        const int urow = __shfl_sync(kFull, row_cur, u);
+        const int urow = __shfl_sync(kFull, rows_cur, (j & 3) * 8 + u);
         if (h < H) {
           const bool valid = kt0 + u * kSubKeys + r < kv_end && urow >= 0;
           const int64_t off = (static_cast<int64_t>(valid ? urow : 0) + (valid ? r : 0)) * row_bytes + h * 128 + c * 16;

@@ -192,12 +192,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_pair_kernel(const __grid_
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    // Lane u < 8 holds the pool row of sub-tile u of a tile (0 when the block
-    // ID is outside the pool: the load stays in bounds, the status word
-    // reports it), loaded one tile ahead.
-    auto tile_row = [&](int j) -> int {
-      const int key = j * kKeysPerTile + lane * kSubKeys;
-      if (lane >= kSubPerTile || key >= kv_end) return 0;
+    // Pool rows of the 16-key sub-tiles, four tiles per warp-wide load: lane l
+    // holds sub-tile l % 8 of tile t0 + l / 8 (0 when the block ID is outside
+    // the pool: the load stays in bounds, the status word reports it). The
+    // next group of four is loaded while the current one is in use, so the
+    // block-table latency is not paid tile by tile.
+    auto group_rows = [&](int t0) -> int {
+      const int key = (t0 + (lane >> 3)) * kKeysPerTile + (lane & 7) * kSubKeys;
+      if (key >= kv_end) return 0;
       const int blk = __ldg(bt_row + key / a.block_size);
       if (blk < 0 || blk >= a.num_blocks) {
         if (a.status) atomicOr(a.status, PKV_DEV_BAD_BLOCK);
@@ -205,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_pair_kernel(const __grid_
       }
       return (blk * a.num_kv_heads + g) * a.block_size + key % a.block_size;
     };
-    int row_next = tile_row(0);
+    int rows_cur = group_rows(0), rows_next = group_rows(4);
     const uint32_t q_full = cluster_addr(bar + kQFull, 0);
     if (lane == 0) {
       prefetch_tensormap(&tmap_q);
@@ -225,14 +227,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_pair_kernel(const __grid_
     for (int j = 0; j < ntiles; ++j) {
       const int s = j % kStages;
       if (j >= kStages && !warp_wait_or_abort(bar + kKVEmpty + s, ((j - kStages) / kStages) & 1, abort_flag)) break;
-      const int row_cur = row_next;
-      if (j + 1 < ntiles) row_next = tile_row(j + 1);
+      if (j > 0 && (j & 3) == 0) {
+        rows_cur = rows_next;
+        rows_next = group_rows(j + 4);
+      }
       const int kt0 = j * kKeysPerTile;
       const int vs = min(kSubPerTile, (kv_end - kt0 + kSubKeys - 1) / kSubKeys);  // sub-tiles with a visible key
       const uint32_t kv_full = cluster_addr(bar + kKVFull + s, 0);
       // The pair loads 4 boxes per visible sub-tile: two K halves (one CTA) and two V halves (one each).
       if (rank == 0 && lane == 0) mbar_arrive_expect_tx(bar + kKVFull + s, vs * 4 * 2048);
-      const int urow = __shfl_sync(kFull, row_cur, u & 7);
+      const int urow = __shfl_sync(kFull, rows_cur, (j & 3) * 8 + (u & 7));
       if (lane < 16 && u < vs)
         tma_load_2d_pair(sKV + s * Lay::kStageBytes + dst_off, is_k ? &tmap_k : &tmap_v, x, urow, kv_full);
     }
