@@ -48,7 +48,6 @@ namespace pkv {
 namespace {
 
 constexpr int kKeysPerTile = 128;
-constexpr int kSubPerTile = kKeysPerTile / kSubKeys;  // 8
 constexpr int kTmemCols = 512;
 constexpr int kOCol = 256;                 // O accumulator; l follows at kOCol + D
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when the max grows by > 256x
