@@ -129,6 +129,22 @@ def run_attention(ds: DeviceStep, stream=None) -> None:
                     device_status=ds.status, stream=stream)
 
 
+def chunk_only(ds: DeviceStep):
+    """(work, info) holding only the step's prompt-chunk items: an attention call
+    with them launches the chunk kernel alone, on the same inputs and outputs."""
+    info = B.WorkInfo()
+    info.num_prefill_items = ds.info.num_prefill_items
+    info.work_words = ds.info.num_prefill_items * B.PKV_WORK_WORDS_PER_ITEM
+    off = ds.info.num_decode_items * B.PKV_WORK_WORDS_PER_ITEM
+    return ds.work[off: off + info.work_words].contiguous(), info
+
+
+def run_chunk_only(ds: DeviceStep, work_info, stream=None) -> None:
+    work, info = work_info
+    B.pkv_attention(ds.q, ds.cu_seqlens_q, ds.seq_slot, ds.context_lens, ds.block_tables, ds.k_pool,
+                    ds.v_pool, work, info, ds.out, None, scale=ds.scale, device_status=ds.status, stream=stream)
+
+
 def run_step(ds: DeviceStep, stream=None) -> None:
     run_cache_write(ds, stream)
     run_attention(ds, stream)
