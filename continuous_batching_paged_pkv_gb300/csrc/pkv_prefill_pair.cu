@@ -55,7 +55,7 @@ namespace {
 constexpr int D = 128;
 constexpr int kKeysPerTile = 128;
 constexpr int kSubPerTile = kKeysPerTile / kSubKeys;  // 8 sub-tiles of 16 keys
-constexpr int kStages = 4;
+constexpr int kStages = 6;  // K/V tiles in flight: the producer runs well ahead of the MMAs
 constexpr int kTmemCols = 512;
 constexpr int kSBufs = 3;      // S/P buffers in TMEM
 constexpr int kOCol = 384;
@@ -74,18 +74,20 @@ struct Layout {
   static constexpr int kBarOffset = kQBytes + kStages * kStageBytes;
   static constexpr int kSmem = kBarOffset + 256 + 1024;    // barriers/flags + alignment slack
 };
+static_assert(Layout::kSmem <= 232448, "dynamic shared memory per CTA");
 
 enum Bar : int {
-  kQFull = 0,      // even CTA: both Q tiles
-  kKVFull = 1,     // +stage; even CTA: both CTAs' halves of a K/V tile
-  kKVEmpty = 5,    // +stage; both CTAs
-  kSFull = 9,      // +buffer (3); both CTAs
-  kPReady = 12,    // +buffer (3); even CTA: one arrival per softmax warp of the pair
-  kPVDone = 15,    // +buffer (3); both CTAs
-  kDrain = 18,     // QK issuer's MMAs complete
-  kDrainPV = 19,   // PV issuer's MMAs complete
-  kNumBars = 20
+  kQFull = 0,                     // even CTA: both Q tiles
+  kKVFull = 1,                    // +stage; even CTA: both CTAs' halves of a K/V tile
+  kKVEmpty = kKVFull + kStages,   // +stage; both CTAs
+  kSFull = kKVEmpty + kStages,    // +buffer (3); both CTAs
+  kPReady = kSFull + kSBufs,      // +buffer (3); even CTA: one arrival per softmax warp of the pair
+  kPVDone = kPReady + kSBufs,     // +buffer (3); both CTAs
+  kDrain = kPVDone + kSBufs,      // QK issuer's MMAs complete
+  kDrainPV = kDrain + 1,          // PV issuer's MMAs complete
+  kNumBars = kDrainPV + 1
 };
+static_assert(kNumBars * 8 + 8 <= 256, "barriers, TMEM address and abort flag fit their 256 bytes");
 
 __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
   return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
