@@ -195,21 +195,24 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_pair_kernel(const __grid_
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     // Pool rows of the 16-key sub-tiles, four tiles per warp-wide load: lane l
-    // holds sub-tile l % 8 of tile t0 + l / 8 (0 when the block ID is outside
-    // the pool: the load stays in bounds, the status word reports it). The
-    // next group of four is loaded while the current one is in use, so the
-    // block-table latency is not paid tile by tile.
-    auto group_rows = [&](int t0) -> int {
+    // covers sub-tile l % 8 of tile t0 + l / 8. The block IDs of the next group
+    // are loaded raw one group ahead and turned into rows (checked against the
+    // pool: 0 when outside it, the status word reports it) only when that
+    // group comes into use, so no block-table latency is ever waited on.
+    auto group_ids = [&](int t0) -> int {
+      const int key = (t0 + (lane >> 3)) * kKeysPerTile + (lane & 7) * kSubKeys;
+      return key < kv_end ? __ldg(bt_row + key / a.block_size) : 0;
+    };
+    auto group_rows = [&](int t0, int blk) -> int {
       const int key = (t0 + (lane >> 3)) * kKeysPerTile + (lane & 7) * kSubKeys;
       if (key >= kv_end) return 0;
-      const int blk = __ldg(bt_row + key / a.block_size);
       if (blk < 0 || blk >= a.num_blocks) {
         if (a.status) atomicOr(a.status, PKV_DEV_BAD_BLOCK);
         return 0;
       }
       return (blk * a.num_kv_heads + g) * a.block_size + key % a.block_size;
     };
-    int rows_cur = group_rows(0), rows_next = group_rows(4);
+    int rows_cur = group_rows(0, group_ids(0)), ids_next = group_ids(4);
     const uint32_t q_full = cluster_addr(bar + kQFull, 0);
     if (lane == 0) {
       prefetch_tensormap(&tmap_q);
@@ -230,8 +233,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_pair_kernel(const __grid_
       const int s = j % kStages;
       if (j >= kStages && !warp_wait_or_abort(bar + kKVEmpty + s, ((j - kStages) / kStages) & 1, abort_flag)) break;
       if (j > 0 && (j & 3) == 0) {
-        rows_cur = rows_next;
-        rows_next = group_rows(j + 4);
+        rows_cur = group_rows(j, ids_next);
+        ids_next = group_ids(j + 4);
       }
       const int kt0 = j * kKeysPerTile;
       const int vs = min(kSubPerTile, (kv_end - kt0 + kSubKeys - 1) / kSubKeys);  // sub-tiles with a visible key
