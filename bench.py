@@ -68,6 +68,10 @@ WORKLOAD_TEXT = {
     "decode256": "decode step, 256 slots x 1 row, 64 q / 8 kv heads, head_dim 128, block 16, "
                  "lognormal contexts (median 2048, clip [16, 32768]), fragmented 131,072-block pool",
     "tiny": "tiny mixed step, 4 q / 2 kv heads, head_dim 64, block 16, 32 blocks",
+    "churn": "continuous-batching trace: Poisson(2) arrivals per step, prompts U[128, 8192], outputs "
+             "geometric (mean 256, max 4096), 64 slots, chunks of 512 (2048 while nothing decodes), "
+             "32 q / 8 kv heads, head_dim 128, block 16, 131,072-block pool; each step planned by the "
+             "library's scheduler, pool and lowering",
 }
 
 
@@ -264,6 +268,8 @@ def run_reference(args, rank, world):
     import oracle
 
     oracle.build()
+    if args.workload == "churn":
+        return run_reference_churn(args)
     w = W.make_step(args.workload, args.seed)
     st = oracle.prepare_step(w)
     cores = oracle.default_threads()
@@ -293,6 +299,36 @@ def run_reference(args, rank, world):
             "cpu_baseline": {"value": val, "unit": "GB/s", "cores": cores, "kind": "oracle",
                              "sample": f"{args.steps} steps of one segment each, fp64, {cores} threads"},
             "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def run_reference_churn(args):
+    """The churn trace as the oracle replays it (its own admission rules, no
+    library code); each timed step's rows sampled as in the churn arm."""
+    import numpy as np
+
+    from oracle import churn
+    from continuous_batching_paged_pkv_gb300 import workloads as W
+
+    spec = W.ChurnSpec()
+    reqs = W.churn_trace(args.seed, spec)
+    ref = churn.ChurnReplay(reqs, max_slots=spec.max_slots, num_blocks=spec.num_blocks, block_size=spec.block_size)
+    toks = W.TokenSource(args.seed, spec.num_q_heads, spec.num_kv_heads, spec.head_dim)
+    warm = max(args.warmup, 3)
+    samples = []
+    for step in range(warm + max(1, min(args.steps, spec.num_steps - warm))):
+        rows = ref.plan()
+        if step >= warm:
+            for r in rows:
+                samples.append((r.rid, r.begin + r.n, toks.rows(r.rid, r.begin + r.n - 1, r.begin + r.n)[2]))
+        ref.commit(rows)
+    cb = churn_oracle_rows(samples, toks, spec.num_kv_heads, spec.num_q_heads, spec.head_dim,
+                           1.0 / np.sqrt(spec.head_dim), args.cpu_seconds)
+    return {"metric": METRIC, "value": cb["value"], "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"churn: {WORKLOAD_TEXT['churn']}", "sample": cb["sample"]},
+            "impl": "reference", "cpu_baseline": cb,
+            "e2e": {"value": cb["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
 def run_ours(args, rank, world, local_rank):
@@ -492,6 +528,172 @@ def run_e2e(args, w, ds, dev, flush):
     return {"ms_total": sum(times), "steps": len(times), "h2d": h2d, "d2h": d2h}
 
 
+def run_churn(args, rank, world, local_rank):
+    """The churn trace replayed through the library: host planning per step
+    outside the events, cache write + attention inside (L2 flushed first)."""
+    import numpy as np
+    import torch
+
+    from continuous_batching_paged_pkv_gb300 import binding as B
+    from continuous_batching_paged_pkv_gb300 import build as libbuild
+    from continuous_batching_paged_pkv_gb300 import runtime as R
+    from continuous_batching_paged_pkv_gb300 import scheduler as S
+    from continuous_batching_paged_pkv_gb300 import workloads as W
+
+    libbuild.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    spec = W.ChurnSpec()
+    reqs = W.churn_trace(args.seed, spec)
+    bs, hq, hkv, d = spec.block_size, spec.num_q_heads, spec.num_kv_heads, spec.head_dim
+    mbps = -(-(spec.prompt_max + spec.output_max + 1) // bs) + 1
+    pool = B.Pool(spec.num_blocks, bs, spec.max_slots, mbps, free_order=W.churn_free_order(args.seed, spec.num_blocks))
+    sch = S.ChurnScheduler(reqs, pool)
+    toks = W.TokenSource(args.seed, hq, hkv, d)
+    k_pool, v_pool = R.empty_pool(spec.num_blocks, hkv, bs, d, dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = L2Flush(dev)
+    stream = torch.cuda.current_stream()
+    scale = 1.0 / np.sqrt(d)
+    warm = max(args.warmup, 3)
+    timed = max(1, min(args.steps, spec.num_steps - warm))
+    sample_cpu = not args.no_cpu_baseline and rank == 0 and world == 1
+    cpu_rows = []  # (request, length, last q row) of timed segments, for the oracle baseline
+
+    step_ms, e2e_ms, step_bytes, step_rows, prefill_steps = [], [], [], [], 0
+    launches = h2d_tot = d2h_tot = 0
+    clocks = None
+    for step in range(warm + timed):
+        rows = sch.plan()
+        if not rows:
+            sch.commit(rows)
+            continue
+        low = pool.lower([(r.slot, r.n) for r in rows])
+        parts = [toks.rows(r.rid, r.begin, r.begin + r.n) for r in rows]
+        host = {"k": np.concatenate([p[0] for p in parts]), "v": np.concatenate([p[1] for p in parts]),
+                "q": np.concatenate([p[2] for p in parts])}
+        pin = {k: torch.from_numpy(v.view(np.int16)).pin_memory() for k, v in host.items()}
+        meta = {"sm": low.slot_mapping.astype(np.int64), "cu": low.cu_seqlens_q, "ss": low.seq_slot,
+                "cl": low.context_lens, "bt": pool.block_tables()}
+        pin.update({k: torch.from_numpy(np.ascontiguousarray(v)).pin_memory() for k, v in meta.items()})
+        dv = {k: torch.empty_like(v, device=dev) for k, v in pin.items()}
+        out = torch.empty((len(host["q"]), hq, d), dtype=torch.bfloat16, device=dev)
+        out_host = torch.empty(out.shape, dtype=torch.bfloat16).pin_memory()
+        T = len(host["q"])
+        ctx = sum(int(low.context_lens[r.slot]) for r in rows)
+        nbytes = ctx * hkv * d * 4 + T * hq * d * 4
+        is_timed = step >= warm
+        if is_timed and clocks is None:
+            props = torch.cuda.get_device_properties(dev)
+            uuid = str(getattr(props, "uuid", "")) or None
+            clocks = ClockSampler(("GPU-" + uuid) if uuid and not uuid.startswith("GPU-") else uuid)
+            clocks.start()
+
+        # end to end: work list on the host, H2D, both calls, D2H, synchronised
+        flush()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        work, info = B.pkv_plan_work(low.cu_seqlens_q, low.seq_slot, low.context_lens, max_slots=spec.max_slots,
+                                     max_blocks_per_slot=mbps, block_size=bs, num_q_heads=hq, num_kv_heads=hkv,
+                                     head_dim=d)
+        work_h = torch.from_numpy(work)
+        work_d = torch.empty_like(work_h, device=dev)
+        for k in dv:
+            dv[k].copy_(pin[k], non_blocking=True)
+        work_d.copy_(work_h, non_blocking=True)
+        ws = torch.empty(max(int(info.workspace_bytes), 1), dtype=torch.uint8, device=dev)
+        B.pkv_cache_write(dv["k"].view(torch.bfloat16), dv["v"].view(torch.bfloat16), dv["sm"], k_pool, v_pool,
+                          device_status=status)
+        B.pkv_attention(dv["q"].view(torch.bfloat16), dv["cu"], dv["ss"], dv["cl"], dv["bt"], k_pool, v_pool,
+                        work_d, info, out, ws, scale=scale, device_status=status)
+        out_host.copy_(out, non_blocking=True)
+        stream.synchronize()
+        e2e = (time.perf_counter() - t0) * 1e3
+
+        # device time of the step alone (inputs resident), same calls again
+        flush()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        B.pkv_cache_write(dv["k"].view(torch.bfloat16), dv["v"].view(torch.bfloat16), dv["sm"], k_pool, v_pool,
+                          device_status=status)
+        B.pkv_attention(dv["q"].view(torch.bfloat16), dv["cu"], dv["ss"], dv["cl"], dv["bt"], k_pool, v_pool,
+                        work_d, info, out, ws, scale=scale, device_status=status)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if B.pkv_check_device_status(status) != 0:
+            raise RuntimeError(f"device status reported an error at churn step {step}")
+        if is_timed:
+            step_ms.append(e0.elapsed_time(e1))
+            e2e_ms.append(e2e)
+            step_bytes.append(nbytes)
+            step_rows.append(T)
+            prefill_steps += int(any(r.prefill for r in rows))
+            launches += 1 + int(info.num_decode_items > 0) + int(info.num_prefill_items > 0) + \
+                int(info.num_combine_items > 0)
+            h2d_tot += sum(t.numel() * t.element_size() for t in pin.values()) + work_h.numel() * 4
+            d2h_tot += out_host.numel() * 2
+        if sample_cpu and is_timed:
+            cpu_rows.extend((r.rid, r.begin + r.n, p[2][-1:]) for r, p in zip(rows, parts))
+        sch.commit(rows)
+    clk = clocks.stop() if clocks is not None else {}
+
+    n = len(step_ms)
+    tot_ms, tot_bytes = aggregate(sum(step_ms), sum(step_bytes), world)
+    hbm, _, peak_src = peaks()
+    value = tot_bytes / (tot_ms / 1e3) / 1e9
+    e_ms, _ = aggregate(sum(e2e_ms), sum(step_bytes), world)
+    res = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": n, "warmup": warm,
+        "ms_per_step": tot_ms / n, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"churn: {WORKLOAD_TEXT['churn']}",
+                   "trace_steps": f"{warm} untimed, then {n} timed, of {spec.num_steps}",
+                   "steps_with_prompt_chunks": prefill_steps, "rows_per_step_mean": sum(step_rows) / n,
+                   "step_ms_p50": statistics.median(step_ms), "step_ms_p90": sorted(step_ms)[int(0.9 * (n - 1))],
+                   "step_ms_max": max(step_ms),
+                   "l2": "flushed before every step (256 MiB written, then 256 MiB read), outside the events",
+                   "parallelism": f"replicas x{world} (no exchange between GPUs)", "seed": args.seed,
+                   "pool_blocks": spec.num_blocks},
+        "pct_hbm_peak": 100.0 * value / world / hbm,
+        "rows_per_s": world * sum(step_rows) / (tot_ms / 1e3),
+        "roofline": {"bound": "hbm", "kernel": "whole step (cache write + attention call), summed over the trace",
+                     "achieved": value / world, "peak": hbm, "unit": "GB/s", "frac": value / world / hbm,
+                     "traffic": None, "algorithmic_bytes_per_launch": sum(step_bytes) / n,
+                     "mean_launch_ms": sum(step_ms) / n, "peak_source": f"{peak_src} HBM copy bandwidth"},
+        "gpu_launches": launches, "clocks": clk,
+        "e2e": {"value": tot_bytes / (e_ms / 1e3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d_tot // n,
+                "d2h_bytes_per_step": d2h_tot // n, "steps": n, "ms_per_step": e_ms / n,
+                "timed": "wall clock per step: work list on the host, H2D copies, cache write, attention, "
+                         "D2H of the output, stream synchronised (K/V/q generation and planning outside)"},
+        "impl": "ours",
+    }
+    if cpu_rows:
+        res["cpu_baseline"] = churn_oracle_rows(cpu_rows, toks, hkv, hq, d, scale, args.cpu_seconds)
+    return res
+
+
+def churn_oracle_rows(samples, toks, hkv, hq, d, scale, seconds):
+    """The oracle's dense attention on sampled churn rows (a segment's last row
+    over its whole history), spread evenly over the samples, ~`seconds` of work."""
+    import oracle
+
+    oracle.build()
+    stride = max(1, len(samples) // 400)
+    done_b, runs, el = 0, 0, 0.0
+    for rid, L, qrow in samples[::stride]:
+        k, v, _ = toks.rows(rid, 0, L)  # the history, generated outside the clock
+        t0 = time.perf_counter()
+        oracle.attention_dense(qrow, k, v, scale)
+        el += time.perf_counter() - t0
+        done_b += L * hkv * d * 4 + hq * d * 4
+        runs += 1
+        if el >= seconds:
+            break
+    return {"value": done_b / el / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{runs} sampled rows of the timed trace steps (the last row of a segment, over its "
+                      f"whole history), fp64, one thread, {el:.1f} s of oracle time"}
+
+
 def main(argv=None):
     args = parse_args(argv)
     rank, world, local_rank = dist_env()
@@ -505,6 +707,8 @@ def main(argv=None):
         dist.init_process_group(backend=backend)
     if args.impl == "reference":
         res = run_reference(args, rank, world)
+    elif args.workload == "churn":
+        res = run_churn(args, rank, world, local_rank)
     else:
         res = run_ours(args, rank, world, local_rank)
     if rank == 0 and res is not None:
