@@ -1,5 +1,7 @@
 // C-ABI entry points of libpkv that touch the GPU: argument validation on the
-// host, TMA tensor-map encoding, kernel launches on the caller's stream, and
+// host, TMA tensor-map encoding, kernel launches on the caller's stream (plus
+// one library-owned stream per device, forked from and joined back to the
+// caller's stream, when a step has both prompt chunks and decode rows), and
 // the one synchronising call that reads the device status word.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -31,6 +33,33 @@ EncodeFn encoder() {
 }
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// A side stream per device for the decode kernels of a step that also has
+// prompt chunks: the chunk kernel (tensor-bound) leaves SMs idle and frees
+// more as its tiles finish, and the decode kernel (HBM-bound) only needs the
+// cache write that precedes the call. The fork and join are events; the mutex
+// keeps each call's record/wait pairs together when calls come from several
+// host threads.
+struct SideStream {
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  std::mutex mu;
+  bool ok = false;
+};
+
+SideStream *side_stream() {
+  static SideStream sides[64];
+  static std::once_flag once[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  SideStream *s = &sides[dev];
+  std::call_once(once[dev], [s] {
+    s->ok = cudaStreamCreateWithFlags(&s->stream, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaEventCreateWithFlags(&s->fork, cudaEventDisableTiming) == cudaSuccess &&
+            cudaEventCreateWithFlags(&s->join, cudaEventDisableTiming) == cudaSuccess;
+  });
+  return s->ok ? s : nullptr;
+}
 
 bool supported_shape(int32_t block_size, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim) {
   if (num_kv_heads <= 0 || num_q_heads <= 0 || num_q_heads % num_kv_heads != 0) return false;
@@ -155,10 +184,27 @@ pkv_status pkv_attention(const void *q, const int32_t *cu_seqlens_q, int32_t num
   const int32_t *dec = work;
   const int32_t *pre = dec + static_cast<int64_t>(info->num_decode_items) * PKV_WORK_WORDS_PER_ITEM;
   const int32_t *comb = pre + static_cast<int64_t>(info->num_prefill_items) * PKV_WORK_WORDS_PER_ITEM;
-  cudaError_t e = head_dim == 128 ? pkv::launch_prefill_pair(a, tq, tk, tv, rpt, info->num_prefill_items, pre, st)
-                                  : pkv::launch_prefill(a, tq, rpt, info->num_prefill_items, pre, st);
-  if (e == cudaSuccess) e = pkv::launch_decode(a, tk, tv, info->num_decode_items, dec, st);
-  if (e == cudaSuccess) e = pkv::launch_merge(a, info->num_combine_items, comb, st);
+  // Both kinds of rows: the chunk kernel goes first on the caller's stream (its
+  // CTAs take their SMs first), the decode and merge kernels run beside it on
+  // the side stream from the same starting point, and the caller's stream
+  // waits for them before anything it enqueues next.
+  SideStream *side = (info->num_prefill_items > 0 && info->num_decode_items > 0) ? side_stream() : nullptr;
+  std::unique_lock<std::mutex> lock;
+  if (side) lock = std::unique_lock<std::mutex>(side->mu);
+  cudaError_t e = side ? cudaEventRecord(side->fork, st) : cudaSuccess;
+  if (e == cudaSuccess)
+    e = head_dim == 128 ? pkv::launch_prefill_pair(a, tq, tk, tv, rpt, info->num_prefill_items, pre, st)
+                        : pkv::launch_prefill(a, tq, rpt, info->num_prefill_items, pre, st);
+  cudaStream_t dst = side ? side->stream : st;
+  if (e == cudaSuccess && side) e = cudaStreamWaitEvent(side->stream, side->fork, 0);
+  if (e == cudaSuccess) e = pkv::launch_decode(a, tk, tv, info->num_decode_items, dec, dst);
+  if (e == cudaSuccess) e = pkv::launch_merge(a, info->num_combine_items, comb, dst);
+  if (side) {
+    // join even after a failed launch, so the caller's stream never runs ahead of queued work
+    const cudaError_t j = cudaEventRecord(side->join, side->stream);
+    const cudaError_t w = j == cudaSuccess ? cudaStreamWaitEvent(st, side->join, 0) : j;
+    if (e == cudaSuccess) e = w;
+  }
   return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 

@@ -284,7 +284,11 @@ pkv_status pkv_cache_write(const void *k_new, const void *v_new, const int64_t *
  * on the GPU. The pool must already hold this step's rows (pkv_cache_write
  * first, same stream). The kernels are launched with programmatic dependent
  * launch, so they may start while the previous kernel in the stream drains;
- * each waits for it before reading any argument.
+ * each waits for it before reading any argument. When a step has both prompt
+ * chunks and decode rows, the decode kernels run on a stream the library owns
+ * (one per device), forked from `stream` at the call and joined back into it
+ * before the call returns: work enqueued on `stream` afterwards still starts
+ * only after all of this call's kernels.
  */
 pkv_status pkv_attention(const void *q, const int32_t *cu_seqlens_q, int32_t num_seqs,
                          int64_t total_q, const int32_t *seq_slot, const int32_t *context_lens,
