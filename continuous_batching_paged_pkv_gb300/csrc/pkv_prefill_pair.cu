@@ -306,7 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_pair_kernel(const __grid_
     const uint32_t p_ready0 = cluster_addr(bar + kPReady, 0);
     float m_used = -INFINITY;  // log2 units
     bool ok = true;
-    float l_sum = 0.f;
+    float l_sum = 0.f, l_odd = 0.f;  // row sum, as even and odd columns (packed adds)
     for (int j = 0; j < ntiles; ++j) {
       const int s = j % kSBufs;
       if (!(ok = warp_wait_or_abort(bar + kSFull + s, (j / kSBufs) & 1, abort_flag))) break;
@@ -324,11 +324,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_pair_kernel(const __grid_
           for (int i = 0; i < 32; ++i)
             if (c * 32 + i > lim) sv[c][i] = kNegInfBits;
       }
+      // Row max: three-input max, four independent chains.
       float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
       for (int c = 0; c < 4; ++c)
 #pragma unroll
-        for (int i = 0; i < 32; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], __uint_as_float(sv[c][i]));
+        for (int i = 0; i < 32; i += 2)
+          mx4[(i >> 1) & 3] = max3(mx4[(i >> 1) & 3], __uint_as_float(sv[c][i]), __uint_as_float(sv[c][i + 1]));
       const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * sl2;
       const float m_new = fmaxf(m_used, mx);
       const bool need = j > 0 && m_new > m_used + kRescaleThreshold;
@@ -340,6 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_pair_kernel(const __grid_
         const float corr = need ? ex2_approx(m_used - m_new) : 1.f;
         if (need) m_used = m_new;
         l_sum *= corr;
+        l_odd *= corr;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t ov[32];
@@ -356,9 +359,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_pair_kernel(const __grid_
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float p0 = ex2_approx(fmaf(__uint_as_float(sv[c][2 * i]), sl2, nm));
-          const float p1 = ex2_approx(fmaf(__uint_as_float(sv[c][2 * i + 1]), sl2, nm));
-          l_sum += p0 + p1;
+          float x0, x1;
+          fma2(x0, x1, __uint_as_float(sv[c][2 * i]), __uint_as_float(sv[c][2 * i + 1]), sl2, sl2, nm, nm);
+          const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+          add2(l_sum, l_odd, p0, p1);
           pk[i] = pack_bf16x2(p0, p1);
         }
         tmem_st16(tmem + lane_base + s * 128 + c * 16, pk);
@@ -389,7 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_pair_kernel(const __grid_
     }
     if (ok && warp_wait_or_abort(bar + kPVDone + (ntiles - 1) % kSBufs, ((ntiles - 1) / kSBufs) & 1, abort_flag)) {
       tc_fence_after();
-      const float inv = 1.f / l_sum;
+      const float inv = 1.f / (l_sum + l_odd);
       __nv_bfloat16 *orow = reinterpret_cast<__nv_bfloat16 *>(a.out) +
                             (static_cast<size_t>(row0 + pos0 + pos) * a.num_q_heads + g * G + hh) * D;
 #pragma unroll
