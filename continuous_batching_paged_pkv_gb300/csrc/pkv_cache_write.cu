@@ -22,8 +22,11 @@ __global__ void __launch_bounds__(256) cache_write_kernel(
     const int64_t *__restrict__ slot_mapping, int64_t num_tokens, uint4 *__restrict__ k_pool,
     uint4 *__restrict__ v_pool, int64_t pool_rows, int32_t block_size, int32_t num_kv_heads,
     int32_t vec_per_row, uint32_t *__restrict__ status) {
-  launch_dependents();
   grid_dependency_wait();  // k_new / v_new / slot_mapping may come from the previous kernel
+  // The attention call may start now: everything before this kernel has
+  // finished, so it can read its step metadata and q at once and wait for
+  // this kernel only before it reads the rows written here.
+  launch_dependents();
   // Vector index over [2 (k, v)][num_tokens][num_kv_heads][vec_per_row].
   const int64_t per_tensor = num_tokens * num_kv_heads * vec_per_row;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;

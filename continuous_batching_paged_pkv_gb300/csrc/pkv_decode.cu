@@ -75,6 +75,7 @@ struct Task {
   int bid;  // per lane: block of sub-tile `lane`
   int row;  // per lane: tensor-map row of sub-tile `lane`, -1 if its block ID is outside the pool
   bool raw_ok, finalized, ok;
+  bool reads_new;  // the span reaches this step's rows (written by the kernel before in the stream)
 };
 
 __device__ __forceinline__ int4 load_item(const int32_t *items, int t, int hkv) {
@@ -86,6 +87,7 @@ __device__ __forceinline__ void expand(Task &T, int t, int4 raw, const StepArgs 
   T.t = t;
   T.finalized = false;
   T.ok = false;
+  T.reads_new = true;
   T.units = 0;
   T.bid = 0;
   T.row = -1;
@@ -121,6 +123,7 @@ __device__ __forceinline__ void finalize(Task &T, const StepArgs &a, int lane) {
   }
   T.key1 = min(T.L, T.key0 + PKV_SPLIT_KEYS);
   T.units = (T.key1 - T.key0 + kSubKeys - 1) / kSubKeys;
+  T.reads_new = T.key1 > T.L - (T.row1 - T.row0);
   const bool in_pool = T.bid >= 0 && T.bid < a.num_blocks;
   T.row = in_pool ? (T.bid * a.num_kv_heads + T.g) * a.block_size + (T.key0 + lane * kSubKeys) % a.block_size : -1;
   if (lane < T.units && !in_pool && a.status) atomicOr(a.status, PKV_DEV_BAD_BLOCK);
@@ -171,8 +174,11 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     prefetch_tensormap(&tmap_v);
   }
   __syncwarp();
-  // Every input may come from the kernel before this one in the stream.
-  grid_dependency_wait();
+  // Metadata, q and the history rows are final when this grid starts (the
+  // kernel before it in the stream signals dependents only after its own
+  // wait); the rows written by that kernel itself (this step's K/V, the last
+  // span of each row) are read only after waiting for it, in issue().
+  bool waited = false;
 
   Task A, B;
   int4 rawC = make_int4(0, 0, 0, 0);
@@ -191,6 +197,10 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
   int P = 0, C = 0, pa = 0, pb = 0;
   int pstage = 0;  // P % NST
   auto issue = [&](const Task &T, int u) {
+    if (T.reads_new && !waited) {
+      grid_dependency_wait();
+      waited = true;
+    }
     const int row = __shfl_sync(kFull, T.row, u);
     if (lane == 0) {
       uint64_t *bar = full + pstage;
