@@ -472,8 +472,9 @@ __global__ void __launch_bounds__(128) merge_kernel(const StepArgs a, const int3
   constexpr int kChunk = 8;
   __shared__ float4 s_acc[U][F];
   __shared__ float s_m[U], s_l[U];
-  grid_dependency_wait();  // partials come from the decode kernel
-
+  // The work item and step metadata are final when this grid starts (the
+  // decode kernel starts only after everything before the cache write has
+  // finished); only the partials need the decode grid to finish (the wait below).
   const int4 it = __ldg(reinterpret_cast<const int4 *>(items) + blockIdx.x);
   const int seg = it.x, slot = it.y, spans = it.z, pbase = it.w;
   const int h = blockIdx.y;
@@ -486,6 +487,7 @@ __global__ void __launch_bounds__(128) merge_kernel(const StepArgs a, const int3
     bad = __ldg(a.seq_slot + seg) != slot || __ldg(a.cu_seqlens_q + seg + 1) - row0 != 1 ||
           (L + PKV_SPLIT_KEYS - 1) / PKV_SPLIT_KEYS != spans || row0 < 0 || row0 >= a.total_q;
   }
+  grid_dependency_wait();  // partials come from the decode kernel
   if (bad) {
     if (threadIdx.x == 0 && a.status) atomicOr(a.status, PKV_DEV_BAD_SEGMENT);
     return;
