@@ -43,7 +43,8 @@ class PkvError(RuntimeError):
 class WorkInfo(ctypes.Structure):
     _fields_ = [("num_decode_items", ctypes.c_int32), ("num_prefill_items", ctypes.c_int32),
                 ("num_combine_items", ctypes.c_int32), ("num_partials", ctypes.c_int32),
-                ("work_words", ctypes.c_int64), ("workspace_bytes", ctypes.c_uint64)]
+                ("work_words", ctypes.c_int64), ("workspace_bytes", ctypes.c_uint64),
+                ("decode_rows_max", ctypes.c_int32)]
 
 
 class PoolStats(ctypes.Structure):

@@ -146,6 +146,10 @@ pkv_status pkv_attention(const void *q, const int32_t *cu_seqlens_q, int32_t num
   if (need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 256)))
     return PKV_ERR_WORKSPACE_TOO_SMALL;
   if ((info->num_combine_items > 0) != (info->num_partials > 0)) return PKV_ERR_INVALID_ARG;
+  // a decode-path segment's (row, q head) columns fit one 16-column tile
+  if (info->decode_rows_max < 0 ||
+      (info->num_decode_items > 0 && info->decode_rows_max * (num_q_heads / num_kv_heads) > 16))
+    return PKV_ERR_INVALID_ARG;
 
   pkv::StepArgs a{};
   a.q = q;
@@ -165,6 +169,7 @@ pkv_status pkv_attention(const void *q, const int32_t *cu_seqlens_q, int32_t num
   a.num_kv_heads = num_kv_heads;
   a.group = num_q_heads / num_kv_heads;
   a.head_dim = head_dim;
+  a.decode_rows_max = info->decode_rows_max;
   const float s = scale > 0.f ? scale : 1.0f / std::sqrt(static_cast<float>(head_dim));
   a.scale_log2 = s * 1.4426950408889634f;
   a.work = work;

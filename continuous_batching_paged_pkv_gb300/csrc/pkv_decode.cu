@@ -26,6 +26,13 @@
 // MMA's B operand through an in-register 8x8 transpose (movmatrix). The
 // running output is rescaled only when a head's max grows by more than 2^8.
 //
+// A segment may also be a short run of causal rows (n rows with n x group <=
+// 16, e.g. draft tokens being verified): the MMA columns are then the (row,
+// q head) pairs, all rows share every K/V sub-tile the warp loads, and row i
+// masks the keys past L - n + i. Such a run can leave a row with no visible
+// key in the last span; its partial is (max -inf, sum 0) and the merge gives
+// it weight 0.
+//
 // A single-span segment's result goes straight to the output; otherwise each
 // span writes a partial (unnormalised sum, reference max, denominator) and the
 // merge kernel, launched right behind the decode kernel (programmatic
@@ -71,6 +78,7 @@ struct Task {
   int t;  // task index, -1 if none
   int seg, slot, span, pbase, g;
   int row0, row1, L, sslot;
+  int nrows;  // rows of the segment (1, or a short run of causal rows)
   int key0, key1, units;
   int bid;  // per lane: block of sub-tile `lane`
   int row;  // per lane: tensor-map row of sub-tile `lane`, -1 if its block ID is outside the pool
@@ -110,50 +118,58 @@ __device__ __forceinline__ void expand(Task &T, int t, int4 raw, const StepArgs 
 }
 
 // Check the metadata against the work item and derive the key range.
-__device__ __forceinline__ void finalize(Task &T, const StepArgs &a, int lane) {
+__device__ __forceinline__ void finalize(Task &T, const StepArgs &a, int lane, int max_cols, int max_rows) {
   if (T.finalized) return;
   T.finalized = true;
   if (T.t < 0) return;
-  T.ok = T.raw_ok && T.sslot == T.slot && T.row1 - T.row0 == 1 && T.L >= 1 &&
+  T.nrows = T.row1 - T.row0;
+  T.ok = T.raw_ok && T.sslot == T.slot && T.nrows >= 1 && T.nrows <= max_rows && T.nrows * a.group <= max_cols && T.nrows <= T.L &&
+         T.L >= 1 &&
          static_cast<int64_t>(T.L) <= static_cast<int64_t>(a.max_blocks_per_slot) * a.block_size &&
-         T.key0 < T.L && T.row0 >= 0 && T.row0 < a.total_q;
+         T.key0 < T.L && T.row0 >= 0 && static_cast<int64_t>(T.row0) + T.nrows <= a.total_q;
   if (!T.ok) {
     if (lane == 0 && a.status) atomicOr(a.status, PKV_DEV_BAD_SEGMENT);
     return;
   }
   T.key1 = min(T.L, T.key0 + PKV_SPLIT_KEYS);
   T.units = (T.key1 - T.key0 + kSubKeys - 1) / kSubKeys;
-  T.reads_new = T.key1 > T.L - (T.row1 - T.row0);
+  T.reads_new = T.key1 > T.L - T.nrows;
   const bool in_pool = T.bid >= 0 && T.bid < a.num_blocks;
   T.row = in_pool ? (T.bid * a.num_kv_heads + T.g) * a.block_size + (T.key0 + lane * kSubKeys) % a.block_size : -1;
   if (lane < T.units && !in_pool && a.status) atomicOr(a.status, PKV_DEV_BAD_BLOCK);
 }
 
-// Q^T fragments (B operand): head = nt*8 + lane/4, d = kk*16 + (lane%4)*2 (+8).
-template <int D, int NT>
+// Q^T fragments (B operand): column c = nt*8 + lane/4 is (row c / G, head
+// c % G) of the segment; d = kk*16 + (lane%4)*2 (+8). Columns past rows x G are zero.
+template <int D, int NT, bool MULTI>
 __device__ __forceinline__ void load_q(uint32_t (&qf)[NT][D / 16][2], const Task &T, const StepArgs &a,
                                        int lane) {
-  const uint16_t *qrow = static_cast<const uint16_t *>(a.q) +
-                         (static_cast<size_t>(T.row0) * a.num_q_heads + T.g * a.group) * D;
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
-    const int head = nt * 8 + (lane >> 2);
-    const uint32_t *qp = reinterpret_cast<const uint32_t *>(qrow + head * D) + (lane & 3);
+    const int col = nt * 8 + (lane >> 2);
+    const bool valid = col < (MULTI ? T.nrows : 1) * a.group;
+    const int i = MULTI && valid ? col / a.group : 0, h = !MULTI ? col : valid ? col % a.group : 0;
+    const uint16_t *qrow = static_cast<const uint16_t *>(a.q) +
+                           ((static_cast<size_t>(T.row0) + i) * a.num_q_heads + T.g * a.group + h) * D;
+    const uint32_t *qp = reinterpret_cast<const uint32_t *>(qrow) + (lane & 3);
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
-      qf[nt][kk][0] = head < a.group ? __ldg(qp + kk * 8) : 0u;
-      qf[nt][kk][1] = head < a.group ? __ldg(qp + kk * 8 + 4) : 0u;
+      qf[nt][kk][0] = valid ? __ldg(qp + kk * 8) : 0u;
+      qf[nt][kk][1] = valid ? __ldg(qp + kk * 8 + 4) : 0u;
     }
   }
 }
 
-template <int D, int NT>
+// NT: 8-column MMA tiles of (row, q head) columns; MULTI: segments may hold
+// more than one row (otherwise every segment is a single decode row).
+template <int D, int NT, bool MULTI>
 __global__ void __launch_bounds__(kWarps * 32, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                   const StepArgs a, const int32_t *__restrict__ items, int num_items) {
   using Cfg = DecodeCfg<D>;
   constexpr int KT = D / 16;  // k-steps of QK^T, m-tiles of PV
   constexpr int NST = Cfg::kStages;
+  constexpr int kMaxRows = MULTI ? 16 : 1;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = align1024(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -189,9 +205,9 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     const int t2 = t1 + stride;
     if (t2 < num_tasks) rawC = load_item(items, t2, hkv);
   }
-  finalize(A, a, lane);
+  finalize(A, a, lane, 8 * NT, kMaxRows);
   uint32_t qA[NT][KT][2], qB[NT][KT][2];
-  if (A.ok) load_q<D, NT>(qA, A, a, lane);
+  if (A.ok) load_q<D, NT, MULTI>(qA, A, a, lane);
   bool qB_loaded = false;
 
   int P = 0, C = 0, pa = 0, pb = 0;
@@ -226,9 +242,9 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     }
     if (B.t >= 0) {
       if (!B.finalized) {
-        finalize(B, a, lane);
+        finalize(B, a, lane, 8 * NT, kMaxRows);
         if (B.ok) {
-          load_q<D, NT>(qB, B, a, lane);
+          load_q<D, NT, MULTI>(qB, B, a, lane);
           qB_loaded = true;
         }
       }
@@ -275,6 +291,22 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
       for (int mt = 0; mt < KT; ++mt) acc[nt][mt][0] = acc[nt][mt][1] = acc[nt][mt][2] = acc[nt][mt][3] = 0.f;
     }
 
+    // Row i of the segment sees keys up to L - rows + i. Byte nt*2 + c holds
+    // the row of this thread's column (nt, c); padding columns take the last
+    // row and so see every key.
+    const int nrows = MULTI ? A.nrows : 1;
+    uint32_t colrow = 0;
+    if (MULTI) {
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const int col = nt * 8 + (lane & 3) * 2 + c;
+          const int i = col < nrows * G ? col / G : nrows - 1;
+          colrow |= static_cast<uint32_t>(i & 0xFF) << (8 * (nt * 2 + c));
+        }
+    }
+
     for (int u = 0; u < A.units; ++u) {
       const int stage = cstage;
       if (!mbar_wait(full + stage, cphase)) {
@@ -285,6 +317,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
       const int kbase = A.key0 + u * kSubKeys;
       // keys of the sub-tile that take part (0 for a block ID outside the pool)
       const int v = row >= 0 ? min(kSubKeys, A.key1 - kbase) : 0;
+      const int vis0 = A.L - nrows - kbase + 1;  // keys of the sub-tile row 0 sees
       const uint32_t kaddr = ring_addr + stage * Cfg::kStageBytes;
 
       // S^T = K Q^T, split over two accumulators to halve the MMA chain.
@@ -309,8 +342,10 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-          x[nt][c][0] = ka < v ? (s0[nt][c] + s1[nt][c]) * sl2 : -INFINITY;
-          x[nt][c][1] = kb < v ? (s0[nt][c + 2] + s1[nt][c + 2]) * sl2 : -INFINITY;
+          // causal limit of this column's row (a single row sees the whole span)
+          const int vis = MULTI ? min(v, vis0 + static_cast<int>((colrow >> (8 * (nt * 2 + c))) & 0xFF)) : v;
+          x[nt][c][0] = ka < vis ? (s0[nt][c] + s1[nt][c]) * sl2 : -INFINITY;
+          x[nt][c][1] = kb < vis ? (s0[nt][c + 2] + s1[nt][c + 2]) * sl2 : -INFINITY;
           float t = fmaxf(x[nt][c][0], x[nt][c][1]);
           t = fmaxf(t, __shfl_xor_sync(kFull, t, 4));
           t = fmaxf(t, __shfl_xor_sync(kFull, t, 8));
@@ -393,14 +428,15 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
         }
       const int hbase = A.g * G;
       if (A.pbase < 0) {
-        __nv_bfloat16 *out = reinterpret_cast<__nv_bfloat16 *>(a.out) +
-                             (static_cast<size_t>(A.row0) * a.num_q_heads + hbase) * D + (lane >> 2);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
-            const int hh = nt * 8 + (lane & 3) * 2 + c;
-            if (hh < G) {
+            const int col = nt * 8 + (lane & 3) * 2 + c;
+            if (col < nrows * G) {
+              const int i = MULTI ? col / G : 0, hh = MULTI ? col % G : col;
+              __nv_bfloat16 *out = reinterpret_cast<__nv_bfloat16 *>(a.out) +
+                                   ((static_cast<size_t>(A.row0) + i) * a.num_q_heads + hbase) * D + (lane >> 2);
               const float inv = 1.f / l[nt][c];
 #pragma unroll
               for (int mt = 0; mt < KT; ++mt) {
@@ -410,13 +446,15 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
             }
           }
       } else {
-        const size_t pi = static_cast<size_t>(A.pbase + A.span) * a.num_q_heads + hbase;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
-            const int hh = nt * 8 + (lane & 3) * 2 + c;
-            if (hh < G) {
+            const int col = nt * 8 + (lane & 3) * 2 + c;
+            if (col < nrows * G) {
+              // partial entry of (span, row i)
+              const int i = MULTI ? col / G : 0, hh = MULTI ? col % G : col;
+              const size_t pi = static_cast<size_t>(A.pbase + A.span * nrows + i) * a.num_q_heads + hbase;
               float *pacc = a.partial_acc + (pi + hh) * D + (lane >> 2);
 #pragma unroll
               for (int mt = 0; mt < KT; ++mt) {
@@ -438,7 +476,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     pa = pb;
     pb = 0;
     if (A.t >= 0) {
-      if (!A.finalized) finalize(A, a, lane);
+      if (!A.finalized) finalize(A, a, lane, 8 * NT, kMaxRows);
       if (qB_loaded) {
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
@@ -448,7 +486,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
             qA[nt][kk][1] = qB[nt][kk][1];
           }
       } else if (A.ok) {
-        load_q<D, NT>(qA, A, a, lane);
+        load_q<D, NT, MULTI>(qA, A, a, lane);
       }
     }
     qB_loaded = false;
@@ -459,7 +497,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
   }
 }
 
-// Span merge: one CTA of four warps per (multi-span segment, q head). Worker
+// Span merge: one CTA of four warps per (row of a multi-span segment, q head). Worker
 // u of the CTA takes spans u, u + U, ... and columns (float4) lane % F. Each
 // worker loads up to kChunk spans at once and folds them into a running
 // (max, denominator, sum); the workers are then folded together in worker
@@ -476,16 +514,22 @@ __global__ void __launch_bounds__(128) merge_kernel(const StepArgs a, const int3
   // decode kernel starts only after everything before the cache write has
   // finished); only the partials need the decode grid to finish (the wait below).
   const int4 it = __ldg(reinterpret_cast<const int4 *>(items) + blockIdx.x);
-  const int seg = it.x, slot = it.y, spans = it.z, pbase = it.w;
+  // word 2: spans | row index << 16 | (rows - 1) << 24; word 3: the partial
+  // entry of (span 0, this row); span s of the row is entry word3 + s * rows.
+  const int seg = it.x, slot = it.y, pbase = it.w;
+  const int spans = it.z & 0xFFFF, ri = (it.z >> 16) & 0xFF, nrows = ((it.z >> 24) & 0xFF) + 1;
   const int h = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  bool bad = seg < 0 || seg >= a.num_seqs || slot < 0 || slot >= a.max_slots || spans < 2 || pbase < 0;
-  int row0 = 0;
+  bool bad = seg < 0 || seg >= a.num_seqs || slot < 0 || slot >= a.max_slots || spans < 2 || pbase < 0 ||
+             ri >= nrows;
+  int row = 0;
   if (!bad) {
-    row0 = __ldg(a.cu_seqlens_q + seg);
+    const int row0 = __ldg(a.cu_seqlens_q + seg);
     const int L = __ldg(a.context_lens + slot);
-    bad = __ldg(a.seq_slot + seg) != slot || __ldg(a.cu_seqlens_q + seg + 1) - row0 != 1 ||
-          (L + PKV_SPLIT_KEYS - 1) / PKV_SPLIT_KEYS != spans || row0 < 0 || row0 >= a.total_q;
+    row = row0 + ri;
+    bad = __ldg(a.seq_slot + seg) != slot || __ldg(a.cu_seqlens_q + seg + 1) - row0 != nrows ||
+          (L + PKV_SPLIT_KEYS - 1) / PKV_SPLIT_KEYS != spans || row0 < 0 || row0 + nrows > a.total_q ||
+          nrows > L;
   }
   grid_dependency_wait();  // partials come from the decode kernel
   if (bad) {
@@ -495,6 +539,7 @@ __global__ void __launch_bounds__(128) merge_kernel(const StepArgs a, const int3
   const int u = warp * PER_WARP + lane / F, d4 = lane % F;
   const size_t hq = static_cast<size_t>(a.num_q_heads);
   const size_t base = static_cast<size_t>(pbase) * hq + h;
+  const size_t span_stride = static_cast<size_t>(nrows) * hq;
 
   float M = -INFINITY, lsum = 0.f;
   float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -508,7 +553,7 @@ __global__ void __launch_bounds__(128) merge_kernel(const StepArgs a, const int3
       li[k] = 0.f;
       ai[k] = make_float4(0.f, 0.f, 0.f, 0.f);
       if (i < spans) {
-        const size_t p = base + static_cast<size_t>(i) * hq;
+        const size_t p = base + static_cast<size_t>(i) * span_stride;
         mi[k] = __ldg(a.partial_ml + p * 2);
         li[k] = __ldg(a.partial_ml + p * 2 + 1);
         ai[k] = __ldg(reinterpret_cast<const float4 *>(a.partial_acc + p * D) + d4);
@@ -560,7 +605,7 @@ __global__ void __launch_bounds__(128) merge_kernel(const StepArgs a, const int3
     uint2 packed;
     packed.x = pack_bf16x2(r.x * inv, r.y * inv);
     packed.y = pack_bf16x2(r.z * inv, r.w * inv);
-    *reinterpret_cast<uint2 *>(reinterpret_cast<__nv_bfloat16 *>(a.out) + (static_cast<size_t>(row0) * hq + h) * D +
+    *reinterpret_cast<uint2 *>(reinterpret_cast<__nv_bfloat16 *>(a.out) + (static_cast<size_t>(row) * hq + h) * D +
                                4 * threadIdx.x) = packed;
   }
 }
@@ -578,7 +623,7 @@ int sm_count() {
   return count[dev];
 }
 
-template <int D, int NT>
+template <int D, int NT, bool MULTI>
 cudaError_t launch_decode_t(const StepArgs &a, const CUtensorMap &tk, const CUtensorMap &tv, int32_t num_items,
                             const int32_t *items, cudaStream_t stream) {
   constexpr int smem = DecodeCfg<D>::kSmem;
@@ -587,13 +632,13 @@ cudaError_t launch_decode_t(const StepArgs &a, const CUtensorMap &tk, const CUte
   cudaGetDevice(&dev);
   const uint64_t bit = 1ull << (dev & 63);
   if (!(configured & bit)) {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, NT, MULTI>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     configured |= bit;
   }
   const int64_t tasks = static_cast<int64_t>(num_items) * a.num_kv_heads;
   const int grid = static_cast<int>(tasks < sm_count() ? tasks : sm_count());
-  return launch_pdl(decode_kernel<D, NT>, dim3(grid), dim3(kWarps * 32), smem, stream, tk, tv, a, items, num_items);
+  return launch_pdl(decode_kernel<D, NT, MULTI>, dim3(grid), dim3(kWarps * 32), smem, stream, tk, tv, a, items, num_items);
 }
 
 }  // namespace
@@ -601,12 +646,20 @@ cudaError_t launch_decode_t(const StepArgs &a, const CUtensorMap &tk, const CUte
 cudaError_t launch_decode(const StepArgs &a, const CUtensorMap &tk, const CUtensorMap &tv, int32_t num_items,
                           const int32_t *items, cudaStream_t stream) {
   if (num_items <= 0) return cudaSuccess;
-  const bool wide = a.group > 8;
-  if (a.head_dim == 128)
-    return wide ? launch_decode_t<128, 2>(a, tk, tv, num_items, items, stream)
-                : launch_decode_t<128, 1>(a, tk, tv, num_items, items, stream);
-  return wide ? launch_decode_t<64, 2>(a, tk, tv, num_items, items, stream)
-              : launch_decode_t<64, 1>(a, tk, tv, num_items, items, stream);
+  // one column per (row, q head) of a segment: 8 columns per tile, 16 at most
+  const bool multi = a.decode_rows_max > 1;
+  const bool wide = a.group * (multi ? a.decode_rows_max : 1) > 8;
+  const int v = (a.head_dim == 128 ? 4 : 0) + (wide ? 2 : 0) + (multi ? 1 : 0);
+  switch (v) {
+    case 0: return launch_decode_t<64, 1, false>(a, tk, tv, num_items, items, stream);
+    case 1: return launch_decode_t<64, 1, true>(a, tk, tv, num_items, items, stream);
+    case 2: return launch_decode_t<64, 2, false>(a, tk, tv, num_items, items, stream);
+    case 3: return launch_decode_t<64, 2, true>(a, tk, tv, num_items, items, stream);
+    case 4: return launch_decode_t<128, 1, false>(a, tk, tv, num_items, items, stream);
+    case 5: return launch_decode_t<128, 1, true>(a, tk, tv, num_items, items, stream);
+    case 6: return launch_decode_t<128, 2, false>(a, tk, tv, num_items, items, stream);
+    default: return launch_decode_t<128, 2, true>(a, tk, tv, num_items, items, stream);
+  }
 }
 
 cudaError_t launch_merge(const StepArgs &a, int32_t num_items, const int32_t *items, cudaStream_t stream) {

@@ -284,7 +284,10 @@ pkv_status pkv_plan_work(const int32_t *cu, int32_t num_seqs, const int32_t *seq
   std::vector<Item> dec, pre, comb;
   std::vector<uint8_t> used(static_cast<size_t>(max_slots), 0);
   const int32_t rows_per_tile = 128 / group;
-  int32_t partials = 0;
+  // Segments of up to 16 / group rows (decode rows and short verify runs) take
+  // the split-KV decode path: rows x grouped heads fit its 16 MMA columns.
+  const int32_t decode_rows = std::max<int32_t>(1, 16 / group);
+  int32_t partials = 0, rows_max = 0;
   for (int32_t s = 0; s < num_seqs; ++s) {
     const int32_t n = cu[s + 1] - cu[s];
     if (n < 0) return PKV_ERR_INVALID_ARG;
@@ -297,17 +300,22 @@ pkv_status pkv_plan_work(const int32_t *cu, int32_t num_seqs, const int32_t *seq
     if (static_cast<int64_t>(L) > static_cast<int64_t>(max_blocks_per_slot) * block_size)
       return PKV_ERR_OUT_OF_RANGE;
     if (n == 0) continue;
-    if (n == 1) {
+    if (n <= decode_rows) {
+      // Partial entry of (span sp, row i): base + sp * n + i. One merge item per
+      // row: spans | row << 16 | (n - 1) << 24, and that row's first entry.
       const int32_t spans = static_cast<int32_t>(ceil_div(L, PKV_SPLIT_KEYS));
+      if (spans >= (1 << 16)) return PKV_ERR_UNSUPPORTED;
       const int32_t base = spans > 1 ? partials : -1;
       for (int32_t sp = 0; sp < spans; ++sp) {
         const int64_t keys = std::min<int64_t>(PKV_SPLIT_KEYS, L - static_cast<int64_t>(sp) * PKV_SPLIT_KEYS);
         dec.push_back({{s, slot, sp, base}, keys});
       }
       if (spans > 1) {
-        comb.push_back({{s, slot, spans, base}, spans});
-        partials += spans;
+        for (int32_t i = 0; i < n; ++i)
+          comb.push_back({{s, slot, spans | (i << 16) | ((n - 1) << 24), base + i}, spans});
+        partials += spans * n;
       }
+      rows_max = std::max(rows_max, n);
     } else {
       // head_dim 128 runs tiles in pairs on two SMs (the second may be past the segment's end).
       const int32_t tiles = static_cast<int32_t>(ceil_div(n, rows_per_tile));
@@ -329,6 +337,7 @@ pkv_status pkv_plan_work(const int32_t *cu, int32_t num_seqs, const int32_t *seq
   info->num_prefill_items = static_cast<int32_t>(pre.size());
   info->num_combine_items = static_cast<int32_t>(comb.size());
   info->num_partials = partials;
+  info->decode_rows_max = rows_max;
   const int64_t items = static_cast<int64_t>(dec.size() + pre.size() + comb.size());
   info->work_words = items * PKV_WORK_WORDS_PER_ITEM;
   auto align256 = [](uint64_t x) { return (x + 255) & ~uint64_t(255); };

@@ -24,6 +24,7 @@ struct StepArgs {
   int32_t num_seqs, max_slots, max_blocks_per_slot, block_size;
   int64_t num_blocks, total_q;
   int32_t num_q_heads, num_kv_heads, group, head_dim;
+  int32_t decode_rows_max;  // most rows of a segment on the decode path (1 for plain decode)
   float scale_log2;  // softmax scale times log2(e)
   const int32_t *work;
   void *out;
@@ -40,7 +41,7 @@ cudaError_t launch_cache_write(const void *k_new, const void *v_new, const int64
 cudaError_t launch_decode(const StepArgs &a, const CUtensorMap &tmap_k, const CUtensorMap &tmap_v,
                           int32_t num_items, const int32_t *items, cudaStream_t stream);
 
-// One CTA per (multi-span segment, q head): merges the segment's span partials.
+// One CTA per (row of a multi-span segment, q head): merges that row's span partials.
 cudaError_t launch_merge(const StepArgs &a, int32_t num_items, const int32_t *items, cudaStream_t stream);
 
 cudaError_t launch_prefill(const StepArgs &a, const CUtensorMap &tmap_q, int32_t rows_per_tile,

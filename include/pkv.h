@@ -185,18 +185,22 @@ pkv_status pkv_plan_lower(pkv_pool *pool, const pkv_segment *plan, int32_t num_s
 
 /* ------------------------------------------------------------------------
  * Attention work list (host side).
- * Rows of a segment with one row go to the split-KV decode kernel: the
- * segment's keys are cut into fixed spans of PKV_SPLIT_KEYS (the cut depends
- * only on that segment's context, so a row's result does not depend on what
- * else is in the batch); a merge kernel combines a segment's spans in order.
+ * Segments of up to 16 / (num_q_heads / num_kv_heads) rows — decode rows,
+ * and short runs of causal rows such as speculative-verification rows — go to
+ * the split-KV decode kernel: the segment's keys are cut into fixed spans of
+ * PKV_SPLIT_KEYS (the cut depends only on that segment's context, so a row's
+ * result does not depend on what else is in the batch); a merge kernel
+ * combines each row's spans in order.
  * Segments with several rows (prompt chunks) go to the tensor-core chunk
  * kernel, in tiles of 128 / (num_q_heads / num_kv_heads) query rows; with
  * head_dim 128 one item is a pair of consecutive tiles run by two SMs
  * together. The pages leave this split open; it is this library's design.
  *
- * Item words: decode (segment, slot, key span, first partial or -1);
- * prefill (segment, slot, first query tile, tiles in the item: 1 or 2);
- * merge (segment, slot, spans, first partial).
+ * Item words: decode (segment, slot, key span, first partial or -1; the
+ * partial of span s, row i is first + s * rows + i); prefill (segment, slot,
+ * first query tile, tiles in the item: 1 or 2); merge, one per row of a
+ * multi-span segment (segment, slot, spans | row << 16 | (rows - 1) << 24,
+ * first partial of the row).
  * ---------------------------------------------------------------------- */
 #define PKV_SPLIT_KEYS 256
 #define PKV_WORK_WORDS_PER_ITEM 4
@@ -204,10 +208,11 @@ pkv_status pkv_plan_lower(pkv_pool *pool, const pkv_segment *plan, int32_t num_s
 typedef struct pkv_work_info {
     int32_t num_decode_items;  /* (segment, key span) items */
     int32_t num_prefill_items; /* (segment, query tile or tile pair) items */
-    int32_t num_combine_items; /* (segment) merge items: decode segments with more than one span */
+    int32_t num_combine_items; /* (segment row) merge items: rows of decode segments with more than one span */
     int32_t num_partials;      /* span results kept in the workspace */
     int64_t work_words;        /* int32 words of the item array: decode, prefill, then merge items */
     uint64_t workspace_bytes;  /* device workspace pkv_attention needs (may be 0) */
+    int32_t decode_rows_max;   /* most rows in a segment of the decode path (0: none) */
 } pkv_work_info;
 
 /*

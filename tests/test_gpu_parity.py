@@ -98,6 +98,9 @@ EDGE_SHAPES = {
     "span boundaries": [(1, 511), (1, 512), (1, 513), (1, 1024), (1, 1025), (1, 1536)],
     "chunks with ragged tails": [(2, 2), (31, 40), (32, 32), (33, 100), (129, 300), (7, 7)],
     "whole prompt as one chunk": [(200, 200), (128, 128), (1, 300)],
+    # short causal runs (verify rows); at small groups they take the decode path,
+    # and a run across a span boundary leaves its first rows with an empty last span
+    "verify runs": [(2, 257), (3, 258), (4, 257), (4, 513), (8, 520), (16, 777), (5, 5), (2, 2)],
 }
 
 

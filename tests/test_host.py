@@ -225,6 +225,29 @@ def test_work_list_tile_pairs():
     assert info64.num_prefill_items == 6 and (work64.reshape(-1, 4)[:, 3] == 1).all()
 
 
+def test_work_list_verify_rows():
+    """Segments of up to 16 / group rows take the decode path; the merge runs one item per row."""
+    S = B.PKV_SPLIT_KEYS
+    ctx = np.zeros(8, np.int32)
+    ctx[[2, 5, 7]] = [2 * S + 88, 100, 40]
+    # group 4: 3 rows over 3 spans, 4 rows in one span, 5 rows (a chunk)
+    work, info = _work([0, 3, 7, 12], [2, 5, 7], ctx)
+    assert (info.num_decode_items, info.num_prefill_items, info.num_combine_items) == (4, 1, 3)
+    assert info.decode_rows_max == 4 and info.num_partials == 9
+    items = work.reshape(-1, 4)
+    dec, pre, comb = items[:4], items[4:5], items[5:]
+    assert sorted(map(tuple, dec.tolist())) == [(0, 2, 0, 0), (0, 2, 1, 0), (0, 2, 2, 0), (1, 5, 0, -1)]
+    assert pre.tolist() == [[2, 7, 0, 1]]
+    # spans | row << 16 | (rows - 1) << 24, and the row's entry for span 0 (span s: + s * rows)
+    assert comb.tolist() == [[0, 2, 3 | (i << 16) | (2 << 24), i] for i in range(3)]
+    # group 1: 16 rows still fit; 17 do not. group 16: every multi-row segment is a chunk.
+    ctx[[0, 1]] = [600, 600]
+    _, i1 = _work([0, 16, 33], [0, 1], ctx, num_q_heads=8, num_kv_heads=8)
+    assert (i1.num_prefill_items, i1.decode_rows_max, i1.num_partials) == (1, 16, 48)
+    _, i16 = _work([0, 1, 3], [0, 1], ctx, num_q_heads=16, num_kv_heads=1)
+    assert (i16.num_prefill_items, i16.decode_rows_max, i16.num_partials) == (1, 1, 3)
+
+
 def test_work_list_unsupported_shapes():
     ctx = np.array([5] + [0] * 7, np.int32)
     for kw in (dict(head_dim=96), dict(block_size=8), dict(num_q_heads=34 * 8, num_kv_heads=8)):
