@@ -471,8 +471,9 @@ def run_ours(args, rank, world, local_rank):
         res["e2e"] = {"value": e_units / (e_ms / 1e3) / 1e9, "unit": "GB/s",
                       "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
                       "steps": e2e["steps"], "ms_per_step": e_ms / e2e["steps"],
-                      "timed": "wall clock per step: work list on the host, H2D copies, cache write, "
-                               "attention, D2H of the output, stream synchronised"}
+                      "timed": "wall clock per step: one pkv_step call (work list planned on the host, "
+                               "one H2D copy of the staged inputs, cache write, attention, one D2H copy of "
+                               "the output) and the stream synchronised"}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
     res["impl"] = "ours"
@@ -480,29 +481,26 @@ def run_ours(args, rank, world, local_rank):
 
 
 def run_e2e(args, w, ds, dev, flush):
-    import numpy as np
+    """The step through the one-call host path: the inputs sit in a page-locked
+    staging buffer; the timed region is ``pkv_step`` (work list planned on the
+    host, one H2D copy, cache write, attention, one D2H copy of the output) and
+    the stream synchronisation."""
     import torch
 
     from continuous_batching_paged_pkv_gb300 import binding as B
+    from continuous_batching_paged_pkv_gb300 import runtime as R
 
     if args.e2e_steps <= 0:
         return None
     low = ds.lowered
-    bt = ds.pool.block_tables()
-
-    def pinned(a, dtype):
-        t = torch.from_numpy(np.ascontiguousarray(a).view(dtype)).pin_memory()
-        return t
-
-    h = {
-        "q": pinned(w.q, np.int16), "k": pinned(w.new_k(), np.int16), "v": pinned(w.new_v(), np.int16),
-        "sm": pinned(low.slot_mapping.astype(np.int64), np.int64), "cu": pinned(low.cu_seqlens_q, np.int32),
-        "ss": pinned(low.seq_slot, np.int32), "cl": pinned(low.context_lens, np.int32), "bt": pinned(bt, np.int32),
-    }
-    d = {k: torch.empty_like(v, device=dev) for k, v in h.items()}
-    work_dev = torch.empty_like(ds.work)
-    out_host = torch.empty(ds.out.shape, dtype=torch.bfloat16).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in h.values()) + ds.work.numel() * 4
+    lay = B.pkv_stage_layout_init(w.total_q, len(w.segments), w.max_slots, w.max_blocks_per_slot, w.num_q_heads,
+                                  w.num_kv_heads, w.head_dim)
+    stage = R.HostStage(lay.work + 4 * int(ds.info.work_words), dev)
+    stage.fill(lay, q=w.q, k_new=w.new_k(), v_new=w.new_v(), slot_mapping=low.slot_mapping,
+               cu_seqlens_q=low.cu_seqlens_q, seq_slot=low.seq_slot, context_lens=low.context_lens,
+               block_tables=ds.pool.block_tables())
+    out_host = torch.empty(ds.out.shape, dtype=torch.bfloat16, pin_memory=True)
+    h2d = lay.work + 4 * int(ds.info.work_words)
     d2h = out_host.numel() * 2
     stream = torch.cuda.current_stream()
     times = []
@@ -510,21 +508,13 @@ def run_e2e(args, w, ds, dev, flush):
         flush()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        work, info = B.pkv_plan_work(low.cu_seqlens_q, low.seq_slot, low.context_lens, max_slots=w.max_slots,
-                                     max_blocks_per_slot=w.max_blocks_per_slot, block_size=w.block_size,
-                                     num_q_heads=w.num_q_heads, num_kv_heads=w.num_kv_heads, head_dim=w.head_dim)
-        wh = torch.from_numpy(work)
-        for k in h:
-            d[k].copy_(h[k], non_blocking=True)
-        work_dev.copy_(wh, non_blocking=True)
-        B.pkv_cache_write(d["k"].view(torch.bfloat16), d["v"].view(torch.bfloat16), d["sm"], ds.k_pool, ds.v_pool,
-                          device_status=ds.status)
-        B.pkv_attention(d["q"].view(torch.bfloat16), d["cu"], d["ss"], d["cl"], d["bt"], ds.k_pool, ds.v_pool,
-                        work_dev, info, ds.out, ds.workspace, scale=w.scale, device_status=ds.status)
-        out_host.copy_(ds.out, non_blocking=True)
+        B.pkv_step(lay, stage.host, stage.device, ds.k_pool, ds.v_pool, ds.out, ds.workspace, out_host=out_host,
+                   scale=w.scale, device_status=ds.status, stream=stream)
         stream.synchronize()
         if i >= 5:
             times.append((time.perf_counter() - t0) * 1e3)
+    if B.pkv_check_device_status(ds.status) != 0:
+        raise RuntimeError("device status reported an error in the end-to-end steps")
     return {"ms_total": sum(times), "steps": len(times), "h2d": h2d, "d2h": d2h}
 
 
@@ -562,7 +552,7 @@ def run_churn(args, rank, world, local_rank):
 
     step_ms, e2e_ms, step_bytes, step_rows, prefill_steps = [], [], [], [], 0
     launches = h2d_tot = d2h_tot = 0
-    clocks = None
+    clocks = stage = ws = None
     for step in range(warm + timed):
         rows = sch.plan()
         if not rows:
@@ -572,14 +562,22 @@ def run_churn(args, rank, world, local_rank):
         parts = [toks.rows(r.rid, r.begin, r.begin + r.n) for r in rows]
         host = {"k": np.concatenate([p[0] for p in parts]), "v": np.concatenate([p[1] for p in parts]),
                 "q": np.concatenate([p[2] for p in parts])}
-        pin = {k: torch.from_numpy(v.view(np.int16)).pin_memory() for k, v in host.items()}
-        meta = {"sm": low.slot_mapping.astype(np.int64), "cu": low.cu_seqlens_q, "ss": low.seq_slot,
-                "cl": low.context_lens, "bt": pool.block_tables()}
-        pin.update({k: torch.from_numpy(np.ascontiguousarray(v)).pin_memory() for k, v in meta.items()})
-        dv = {k: torch.empty_like(v, device=dev) for k, v in pin.items()}
-        out = torch.empty((len(host["q"]), hq, d), dtype=torch.bfloat16, device=dev)
-        out_host = torch.empty(out.shape, dtype=torch.bfloat16).pin_memory()
         T = len(host["q"])
+        lay = B.pkv_stage_layout_init(T, len(rows), spec.max_slots, mbps, hq, hkv, d)
+        # sizing only (outside the timed region): the step plans its own work list again inside
+        _, info0 = B.pkv_plan_work(low.cu_seqlens_q, low.seq_slot, low.context_lens, max_slots=spec.max_slots,
+                                   max_blocks_per_slot=mbps, block_size=bs, num_q_heads=hq, num_kv_heads=hkv,
+                                   head_dim=d)
+        need = lay.work + 4 * int(info0.work_words)
+        if stage is None or stage.nbytes < need:
+            stage = R.HostStage(max(need, 32 << 20), dev)
+        if ws is None or ws.numel() < int(info0.workspace_bytes):
+            ws = torch.empty(max(int(info0.workspace_bytes), 64 << 20), dtype=torch.uint8, device=dev)
+        stage.fill(lay, q=host["q"], k_new=host["k"], v_new=host["v"], slot_mapping=low.slot_mapping,
+                   cu_seqlens_q=low.cu_seqlens_q, seq_slot=low.seq_slot, context_lens=low.context_lens,
+                   block_tables=pool.block_tables())
+        out = torch.empty((T, hq, d), dtype=torch.bfloat16, device=dev)
+        out_host = torch.empty(out.shape, dtype=torch.bfloat16, pin_memory=True)
         ctx = sum(int(low.context_lens[r.slot]) for r in rows)
         nbytes = ctx * hkv * d * 4 + T * hq * d * 4
         is_timed = step >= warm
@@ -589,35 +587,23 @@ def run_churn(args, rank, world, local_rank):
             clocks = ClockSampler(("GPU-" + uuid) if uuid and not uuid.startswith("GPU-") else uuid)
             clocks.start()
 
-        # end to end: work list on the host, H2D, both calls, D2H, synchronised
+        # end to end: one pkv_step call (work list, H2D, both calls, D2H), synchronised
         flush()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        work, info = B.pkv_plan_work(low.cu_seqlens_q, low.seq_slot, low.context_lens, max_slots=spec.max_slots,
-                                     max_blocks_per_slot=mbps, block_size=bs, num_q_heads=hq, num_kv_heads=hkv,
-                                     head_dim=d)
-        work_h = torch.from_numpy(work)
-        work_d = torch.empty_like(work_h, device=dev)
-        for k in dv:
-            dv[k].copy_(pin[k], non_blocking=True)
-        work_d.copy_(work_h, non_blocking=True)
-        ws = torch.empty(max(int(info.workspace_bytes), 1), dtype=torch.uint8, device=dev)
-        B.pkv_cache_write(dv["k"].view(torch.bfloat16), dv["v"].view(torch.bfloat16), dv["sm"], k_pool, v_pool,
-                          device_status=status)
-        B.pkv_attention(dv["q"].view(torch.bfloat16), dv["cu"], dv["ss"], dv["cl"], dv["bt"], k_pool, v_pool,
-                        work_d, info, out, ws, scale=scale, device_status=status)
-        out_host.copy_(out, non_blocking=True)
+        info = B.pkv_step(lay, stage.host, stage.device, k_pool, v_pool, out, ws, out_host=out_host, scale=scale,
+                          device_status=status, stream=stream)
         stream.synchronize()
         e2e = (time.perf_counter() - t0) * 1e3
 
-        # device time of the step alone (inputs resident), same calls again
+        # device time of the step alone (inputs resident in the device stage), same calls again
+        v = stage.device_views(lay, info)
         flush()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        B.pkv_cache_write(dv["k"].view(torch.bfloat16), dv["v"].view(torch.bfloat16), dv["sm"], k_pool, v_pool,
-                          device_status=status)
-        B.pkv_attention(dv["q"].view(torch.bfloat16), dv["cu"], dv["ss"], dv["cl"], dv["bt"], k_pool, v_pool,
-                        work_d, info, out, ws, scale=scale, device_status=status)
+        B.pkv_cache_write(v["k_new"], v["v_new"], v["slot_mapping"], k_pool, v_pool, device_status=status)
+        B.pkv_attention(v["q"], v["cu_seqlens_q"], v["seq_slot"], v["context_lens"], v["block_tables"], k_pool,
+                        v_pool, v["work"], info, out, ws, scale=scale, device_status=status)
         e1.record(stream)
         torch.cuda.synchronize()
         if B.pkv_check_device_status(status) != 0:
@@ -630,7 +616,7 @@ def run_churn(args, rank, world, local_rank):
             prefill_steps += int(any(r.prefill for r in rows))
             launches += 1 + int(info.num_decode_items > 0) + int(info.num_prefill_items > 0) + \
                 int(info.num_combine_items > 0)
-            h2d_tot += sum(t.numel() * t.element_size() for t in pin.values()) + work_h.numel() * 4
+            h2d_tot += lay.work + 4 * int(info.work_words)
             d2h_tot += out_host.numel() * 2
         if sample_cpu and is_timed:
             cpu_rows.extend((r.rid, r.begin + r.n, p[2][-1:]) for r, p in zip(rows, parts))
@@ -663,8 +649,9 @@ def run_churn(args, rank, world, local_rank):
         "gpu_launches": launches, "clocks": clk,
         "e2e": {"value": tot_bytes / (e_ms / 1e3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d_tot // n,
                 "d2h_bytes_per_step": d2h_tot // n, "steps": n, "ms_per_step": e_ms / n,
-                "timed": "wall clock per step: work list on the host, H2D copies, cache write, attention, "
-                         "D2H of the output, stream synchronised (K/V/q generation and planning outside)"},
+                "timed": "wall clock per step: one pkv_step call (work list planned on the host, one H2D "
+                         "copy of the staged inputs, cache write, attention, one D2H copy of the output) and "
+                         "the stream synchronised (K/V/q generation, scheduling and staging outside)"},
         "impl": "ours",
     }
     if cpu_rows:

@@ -47,6 +47,14 @@ class WorkInfo(ctypes.Structure):
                 ("decode_rows_max", ctypes.c_int32)]
 
 
+class StageLayout(ctypes.Structure):
+    _fields_ = [("total_q", ctypes.c_int64), ("num_seqs", ctypes.c_int32), ("max_slots", ctypes.c_int32),
+                ("max_blocks_per_slot", ctypes.c_int32), ("num_q_heads", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32)] + \
+              [(n, ctypes.c_uint64) for n in ("q", "k_new", "v_new", "slot_mapping", "cu_seqlens_q", "seq_slot",
+                                              "context_lens", "block_tables", "work")]
+
+
 class PoolStats(ctypes.Structure):
     _fields_ = [("num_blocks", ctypes.c_int64), ("block_size", ctypes.c_int32),
                 ("max_slots", ctypes.c_int32), ("free_blocks", ctypes.c_int64),
@@ -90,6 +98,9 @@ def _lib():
             "pkv_check_device_status": ([p, p, ctypes.POINTER(ctypes.c_uint32)], ctypes.c_int),
             "pkv_attention_no_alloc": ([p, p, i32, i64, p, p, p, i32, i32, i32, p, p, i64, i32, i32, i32, f32, p,
                                         ctypes.POINTER(WorkInfo), p, p, p], ctypes.c_int),
+            "pkv_stage_layout_init": ([ctypes.POINTER(StageLayout), i64, i32, i32, i32, i32, i32, i32], ctypes.c_int),
+            "pkv_step": ([ctypes.POINTER(StageLayout), p, u64, p, u64, p, p, i64, i32, f32, p, u64, p, p, p, p,
+                          ctypes.POINTER(WorkInfo)], ctypes.c_int),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -296,3 +307,44 @@ def pkv_check_device_status(device_status, stream=None) -> int:
     if rc not in (PKV_OK, 6, 8):
         _check(rc, "pkv_check_device_status")
     return bits.value
+
+
+def pkv_stage_layout_init(total_q: int, num_seqs: int, max_slots: int, max_blocks_per_slot: int,
+                          num_q_heads: int, num_kv_heads: int, head_dim: int) -> StageLayout:
+    layout = StageLayout()
+    _check(_lib().pkv_stage_layout_init(ctypes.byref(layout), total_q, num_seqs, max_slots, max_blocks_per_slot,
+                                        num_q_heads, num_kv_heads, head_dim), "pkv_stage_layout_init")
+    return layout
+
+
+def _buf(b):
+    """(pointer, bytes) of a torch tensor or numpy array used as a raw byte buffer."""
+    if b is None:
+        return None, 0
+    if isinstance(b, np.ndarray):
+        return ctypes.c_void_p(b.ctypes.data), b.nbytes
+    return ctypes.c_void_p(b.data_ptr()), b.numel() * b.element_size()
+
+
+def pkv_step(layout: StageLayout, host_stage, device_stage, k_pool, v_pool, out, workspace=None, *,
+             out_host=None, scale: float = 0.0, device_status=None, stream=None) -> WorkInfo:
+    """One step from the host staging buffer (see ``include/pkv.h``). Returns the step's work info.
+
+    On an error the raised PkvError carries ``info`` (filled where the library got that far).
+    """
+    _need(out, "torch.bfloat16", "out")
+    _need(k_pool, "torch.bfloat16", "k_pool")
+    _need(v_pool, "torch.bfloat16", "v_pool")
+    nb, hkv, bs, d = k_pool.shape
+    hp, hn = _buf(host_stage)
+    dp, dn = _buf(device_stage)
+    wp, wn = _buf(workspace)
+    info = WorkInfo()
+    rc = _lib().pkv_step(ctypes.byref(layout), hp, hn, dp, dn, _t_ptr(k_pool), _t_ptr(v_pool), nb, bs, float(scale),
+                         wp, wn, _t_ptr(out), _buf(out_host)[0], _t_ptr(device_status), _stream(stream),
+                         ctypes.byref(info))
+    if rc != PKV_OK:
+        err = PkvError(rc, "pkv_step")
+        err.info = info
+        raise err
+    return info

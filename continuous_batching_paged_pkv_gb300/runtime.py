@@ -11,7 +11,9 @@ histories, and the packed query rows), this module:
    uploads the step's metadata, queries and new keys/values.
 
 ``run_cache_write`` and ``run_attention`` then issue the step's two device
-calls. Nothing here computes attention; it only moves arguments.
+calls. ``HostStage`` holds the page-locked staging buffers of the one-call
+host path (``pkv_step``). Nothing here computes attention; it only moves
+arguments.
 """
 
 from __future__ import annotations
@@ -161,3 +163,61 @@ def pool_bits(ds: DeviceStep):
 
     return (ds.k_pool.view(torch.int16).cpu().numpy().view(np.uint16),
             ds.v_pool.view(torch.int16).cpu().numpy().view(np.uint16))
+
+
+class HostStage:
+    """Page-locked host staging buffer for ``pkv_step`` and its device twin.
+
+    One buffer of ``nbytes`` on each side; ``fill`` writes a step's inputs at
+    the offsets of its ``pkv_stage_layout`` (the rest of the buffer is the
+    work list's room). Reusable across steps of different shapes.
+    """
+
+    def __init__(self, nbytes: int, device):
+        import torch
+
+        self.nbytes = int(nbytes)
+        self.host = torch.empty(self.nbytes, dtype=torch.uint8, pin_memory=True)
+        self.device = torch.empty(self.nbytes, dtype=torch.uint8, device=device)
+        self._np = self.host.numpy()
+
+    def _fields(self, layout):
+        T, S, ms, mb = layout.total_q, layout.num_seqs, layout.max_slots, layout.max_blocks_per_slot
+        hq, hkv, d = layout.num_q_heads, layout.num_kv_heads, layout.head_dim
+        return {"q": (np.uint16, (T, hq, d)), "k_new": (np.uint16, (T, hkv, d)), "v_new": (np.uint16, (T, hkv, d)),
+                "slot_mapping": (np.int64, (T,)), "cu_seqlens_q": (np.int32, (S + 1,)),
+                "seq_slot": (np.int32, (S,)), "context_lens": (np.int32, (ms,)),
+                "block_tables": (np.int32, (ms, mb))}
+
+    def fill(self, layout, **arrays) -> None:
+        """Write every field of ``layout`` (bf16 tensors as uint16 bit patterns)."""
+        if layout.work > self.nbytes:
+            raise ValueError(f"staging buffer of {self.nbytes} B is smaller than the layout ({layout.work} B)")
+        fields = self._fields(layout)
+        if set(arrays) != set(fields):
+            raise ValueError(f"fill needs exactly {sorted(fields)}")
+        for name, (dtype, shape) in fields.items():
+            a = np.asarray(arrays[name])
+            if a.dtype != dtype and not (dtype == np.uint16 and a.dtype == np.int16):
+                a = a.astype(dtype)
+            a = np.ascontiguousarray(a)
+            if a.shape != shape:
+                raise ValueError(f"{name}: shape {a.shape}, expected {shape}")
+            off = getattr(layout, name)
+            self._np[off:off + a.nbytes] = a.reshape(-1).view(np.uint8)
+
+    def device_views(self, layout, info):
+        """Torch views of the staged inputs and work list in the device buffer (after a ``pkv_step``)."""
+        import torch
+
+        tdt = {np.uint16: torch.bfloat16, np.int64: torch.int64, np.int32: torch.int32}
+        views = {}
+        for name, (dtype, shape) in self._fields(layout).items():
+            n = int(np.prod(shape)) * np.dtype(dtype).itemsize
+            off = getattr(layout, name)
+            raw = self.device[off:off + n]
+            views[name] = (raw.view(torch.int16).view(torch.bfloat16) if dtype is np.uint16
+                           else raw.view(tdt[dtype])).view(shape)
+        nw = int(info.work_words)
+        views["work"] = self.device[layout.work:layout.work + 4 * nw].view(torch.int32)
+        return views

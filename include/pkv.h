@@ -340,6 +340,67 @@ pkv_status pkv_attention_no_alloc(const void *q, const int32_t *cu_seqlens_q, in
                                   float scale, const int32_t *work, const pkv_work_info *info,
                                   void *out, uint32_t *device_status, pkv_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * Host-staged step: a whole step from host memory in one call.
+ * [LB] §One scheduler, model-specific execution: the engine hands the lowered
+ * step to its backend in one go. The pages give no host/device protocol; this
+ * one is the library's design: every per-step input sits in one caller-owned
+ * host staging buffer at offsets fixed by pkv_stage_layout_init, so a step is
+ * one host-to-device copy, the cache write, the attention call and one
+ * device-to-host copy of the output, all on `stream`.
+ * ---------------------------------------------------------------------- */
+typedef struct pkv_stage_layout {
+    /* shapes the layout was made for */
+    int64_t total_q;
+    int32_t num_seqs, max_slots, max_blocks_per_slot, num_q_heads, num_kv_heads, head_dim;
+    /* byte offsets into the staging buffers (each a multiple of 256) */
+    uint64_t q;            /* bf16 [total_q][num_q_heads][head_dim] */
+    uint64_t k_new;        /* bf16 [total_q][num_kv_heads][head_dim] */
+    uint64_t v_new;        /* bf16 [total_q][num_kv_heads][head_dim] */
+    uint64_t slot_mapping; /* int64 [total_q] */
+    uint64_t cu_seqlens_q; /* int32 [num_seqs + 1] */
+    uint64_t seq_slot;     /* int32 [num_seqs] */
+    uint64_t context_lens; /* int32 [max_slots] */
+    uint64_t block_tables; /* int32 [max_slots][max_blocks_per_slot] */
+    uint64_t work;         /* int32 work list, written by pkv_step; runs to the end of the buffer */
+} pkv_stage_layout;
+
+/*
+ * Fill `layout` for a step of these shapes. The caller writes the step's
+ * inputs (as pkv_plan_lower and its own model produce them) at the offsets;
+ * a staging buffer needs `layout->work` bytes plus room for the work list.
+ * PKV_ERR_INVALID_ARG for a negative or zero shape or a size overflow.
+ */
+pkv_status pkv_stage_layout_init(pkv_stage_layout *layout, int64_t total_q, int32_t num_seqs,
+                                 int32_t max_slots, int32_t max_blocks_per_slot,
+                                 int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim);
+
+/*
+ * Run one step from the host staging buffer `host_stage` (host memory laid
+ * out by `layout`; page-locked for the copies to be asynchronous):
+ *   1. plan the work list on the host from the staged cu_seqlens_q, seq_slot
+ *      and context_lens, writing it into host_stage at layout->work (the
+ *      room left there, (host_stage_bytes - layout->work) / 4 words, bounds it);
+ *   2. one cudaMemcpyAsync of host_stage[0, layout->work + work bytes) to
+ *      `device_stage` (device, 256-byte aligned, at least that many bytes);
+ *   3. pkv_cache_write of the staged k_new / v_new / slot_mapping;
+ *   4. pkv_attention over the staged q and metadata into `out` (device,
+ *      bf16 [total_q][num_q_heads][head_dim]), with `workspace` as there;
+ *   5. if `out_host` is not NULL, one cudaMemcpyAsync of `out` to it.
+ * Nothing synchronises: the caller waits on `stream` before reading
+ * out_host or writing host_stage again. `info_out` (nullable) receives the
+ * step's work info, also on PKV_ERR_WORKSPACE_TOO_SMALL, so a caller can grow
+ * `workspace` or the staging buffers and call again. The staged
+ * cu_seqlens_q must end at layout->total_q. Any error from steps 1-2 returns
+ * before anything is enqueued; an error from steps 3-5 is returned as
+ * soon as it happens, with the earlier steps already enqueued.
+ */
+pkv_status pkv_step(const pkv_stage_layout *layout, void *host_stage, uint64_t host_stage_bytes,
+                    void *device_stage, uint64_t device_stage_bytes, void *k_pool, void *v_pool,
+                    int64_t num_blocks, int32_t block_size, float scale, void *workspace,
+                    uint64_t workspace_bytes, void *out, void *out_host, uint32_t *device_status,
+                    pkv_stream_t stream, pkv_work_info *info_out);
+
 /*
  * Synchronise `stream`, read *device_status (device memory), clear it, and
  * map it to a status: PKV_OK if zero; PKV_ERR_DEVICE_TIMEOUT if the timeout

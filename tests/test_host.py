@@ -255,6 +255,68 @@ def test_work_list_unsupported_shapes():
             _work([0, 1], [0], ctx, **kw)
 
 
+# ---- host-staged step ------------------------------------------------------------
+
+def test_stage_layout_offsets():
+    T, S, ms, mb, hq, hkv, d = 516, 5, 8, 200, 32, 8, 128
+    lay = B.pkv_stage_layout_init(T, S, ms, mb, hq, hkv, d)
+    sizes = {"q": T * hq * d * 2, "k_new": T * hkv * d * 2, "v_new": T * hkv * d * 2, "slot_mapping": T * 8,
+             "cu_seqlens_q": (S + 1) * 4, "seq_slot": S * 4, "context_lens": ms * 4, "block_tables": ms * mb * 4}
+    order = list(sizes)
+    offs = [getattr(lay, n) for n in order] + [lay.work]
+    assert all(o % 256 == 0 for o in offs)
+    for i, n in enumerate(order):  # in order, each field fits before the next
+        assert offs[i] + sizes[n] <= offs[i + 1] < offs[i] + sizes[n] + 256
+    assert (lay.total_q, lay.num_seqs, lay.max_slots, lay.max_blocks_per_slot) == (T, S, ms, mb)
+    with pytest.raises(B.PkvError, match="INVALID_ARG"):
+        B.pkv_stage_layout_init(-1, S, ms, mb, hq, hkv, d)
+
+
+def _aligned_bytes(n):
+    raw = np.zeros(n + 256, np.uint8)
+    off = (-raw.ctypes.data) % 256
+    return raw[off:off + n]
+
+
+def test_step_rejects_bad_staging_before_any_device_work():
+    """Every check here fails on the host, before pkv_step enqueues anything (no GPU needed)."""
+    ctx = np.zeros(8, np.int32)
+    ctx[[0, 1]] = [600, 40]
+    lay = B.pkv_stage_layout_init(2, 2, 8, 64, 32, 8, 128)
+    host = _aligned_bytes(lay.work + 4096)
+    def put(name, a):
+        a = np.ascontiguousarray(a)
+        host[getattr(lay, name):getattr(lay, name) + a.nbytes] = a.reshape(-1).view(np.uint8)
+    put("cu_seqlens_q", np.array([0, 1, 2], np.int32))
+    put("seq_slot", np.array([0, 1], np.int32))
+    put("context_lens", ctx)
+    # host stand-ins for the device pointers: pkv_step must return before using any of them
+    pools = _aligned_bytes(4 * 8 * 16 * 128 * 2)
+    out = _aligned_bytes(2 * 32 * 128 * 2)
+    dev = _aligned_bytes(lay.work + 4096)
+    p = lambda a: ctypes.c_void_p(a.ctypes.data)
+
+    def call(h, d_, ws=None):
+        info = B.WorkInfo()
+        rc = B._lib().pkv_step(ctypes.byref(lay), p(h), h.nbytes, p(d_), d_.nbytes, p(pools), p(pools), 4, 16,
+                               0.0, None if ws is None else p(ws), 0 if ws is None else ws.nbytes, p(out), None,
+                               None, None, ctypes.byref(info))
+        return B.STATUS_NAMES[rc], info
+
+    # workspace missing: slot 0 has 3 spans, so partials are needed
+    rc, info = call(host, dev)
+    assert rc == "PKV_ERR_WORKSPACE_TOO_SMALL" and info.num_partials == 3 and info.workspace_bytes > 0
+    # no room for the work list in the host buffer
+    rc, info = call(host[:lay.work + 8], dev)
+    assert rc == "PKV_ERR_WORKSPACE_TOO_SMALL" and info.work_words == 4 * (3 + 1 + 1)  # 3 + 1 spans, 1 merge row
+    # device stage too small for the staged bytes
+    assert call(host, dev[:lay.work], _aligned_bytes(1 << 20))[0] == "PKV_ERR_WORKSPACE_TOO_SMALL"
+    # device stage not 256-byte aligned; cu_seqlens_q not ending at total_q
+    assert call(host, dev[1:])[0] == "PKV_ERR_INVALID_ARG"
+    put("cu_seqlens_q", np.array([0, 1, 3], np.int32))
+    assert call(host, dev)[0] == "PKV_ERR_INVALID_ARG"
+
+
 # ---- scheduler vs the oracle's replay -------------------------------------------
 
 def _compare_trace(reqs, spec_steps, num_blocks, max_slots, bs=16):
