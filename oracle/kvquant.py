@@ -1,0 +1,131 @@
+"""Oracle for the 8-bit block-scaled KV pool -- TEST INFRASTRUCTURE.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline
+leg may import this module; the CUDA library never calls it and shares no code
+with it.
+
+The pages run their KV caches quantised (Lucebox, "Continuous batching ...",
+§DeepSeek V4 Flash on Strix Halo and two GPUs: 4-bit KV; §Qwen3.8-27B DFlash2
+on the R9700 (vs llama.cpp): 8-bit KV) but do not define the formats. The
+reading taken here is the plainest 8-bit block-scaled one:
+
+* each pool row (one token, one kv head, head_dim values) is cut into groups
+  of 32 consecutive values;
+* a group stores one bfloat16 scale ``d`` and 32 signed 8-bit codes in
+  [-127, 127]; the value a code stands for is ``code * d``;
+* quantising a group of bfloat16 values ``x`` (all steps in float32, the
+  precision the codes are decided in):
+    amax = max |x|;  d = amax / 127 rounded to bfloat16 (nearest even);
+    code = clamp(round_half_even(x / d), -127, 127), or 0 when d is 0.
+  A bfloat16 scale has float32's range, so every finite bfloat16 group
+  quantises with the same relative precision.
+
+Attention over such a pool is ordinary causal grouped-query attention over the
+dequantised values ``code * d`` (exact in double), computed here in float64
+with a plain per-segment gather through the block table.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+GROUP = 32  # values per scale
+CODE_MAX = 127
+
+
+def _widen(bits) -> np.ndarray:
+    b = np.ascontiguousarray(bits, dtype=np.uint16)
+    return (b.astype(np.uint32) << 16).view(np.float32)
+
+
+def _round_bf16(x) -> np.ndarray:
+    """float32 -> bfloat16 bits, round to nearest even (finite inputs)."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    return ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+
+
+def quantize(x_bits):
+    """bf16 bits ``[..., D]`` -> (codes int8 ``[..., D]``, scale bits uint16 ``[..., D / 32]``)."""
+    x = _widen(x_bits)
+    d_len = x.shape[-1]
+    if d_len % GROUP:
+        raise ValueError(f"head_dim {d_len} is not a multiple of {GROUP}")
+    g = x.reshape(*x.shape[:-1], d_len // GROUP, GROUP)
+    amax = np.abs(g).max(axis=-1)
+    d_bits = _round_bf16((amax / np.float32(CODE_MAX)).astype(np.float32))
+    df = _widen(d_bits)[..., None]
+    safe = np.where(df > 0, df, np.float32(1))
+    r = np.where(df > 0, g / safe, np.float32(0)).astype(np.float32)
+    codes = np.clip(np.rint(r), -CODE_MAX, CODE_MAX).astype(np.int8)
+    return codes.reshape(x.shape), d_bits
+
+
+def dequantize(codes, scale_bits) -> np.ndarray:
+    """The values codes stand for, in float64 (exact)."""
+    c = np.asarray(codes, dtype=np.int8)
+    s = _widen(scale_bits).astype(np.float64)
+    g = c.reshape(*c.shape[:-1], c.shape[-1] // GROUP, GROUP).astype(np.float64)
+    return (g * s[..., None]).reshape(c.shape)
+
+
+def empty_pool(num_blocks, num_kv_heads, block_size, head_dim):
+    """(codes, scales) pools filled with a recognisable pattern for rows never written."""
+    codes = np.full((num_blocks, num_kv_heads, block_size, head_dim), -128, np.int8)
+    scales = np.full((num_blocks, num_kv_heads, block_size, head_dim // GROUP), 0x7FC1, np.uint16)  # NaN
+    return codes, scales
+
+
+def cache_write(k_codes, k_scales, v_codes, v_scales, k_new, v_new, mapping) -> None:
+    """Quantise new rows ``[T, Hkv, D]`` (bf16 bits) into the pools at pool rows ``mapping`` (< 0: skip)."""
+    nb, hkv, bs, d = k_codes.shape
+    mapping = np.asarray(mapping, dtype=np.int64)
+    if np.any(mapping >= nb * bs):
+        raise ValueError("slot mapping past the pool")
+    kq, ks = quantize(k_new)
+    vq, vs = quantize(v_new)
+    for t, s in enumerate(mapping):
+        if s < 0:
+            continue
+        blk, row = divmod(int(s), bs)
+        k_codes[blk, :, row, :] = kq[t]
+        k_scales[blk, :, row, :] = ks[t]
+        v_codes[blk, :, row, :] = vq[t]
+        v_scales[blk, :, row, :] = vs[t]
+
+
+def attention_paged(q, cu_seqlens_q, seq_slot, context_lens, block_tables, k_codes, k_scales, v_codes,
+                    v_scales, scale: float, *, num_q_heads: int, rows=None) -> np.ndarray:
+    """float64 ``[T, Hq, D]``; rows outside ``rows`` (if given) are NaN.
+
+    Segment s (slot c, n rows, L = context_lens[c]): row i sits at position
+    L - n + i and attends keys 0..L-n+i of slot c, gathered block by block in
+    logical order; q head h reads kv head h // (Hq / Hkv).
+    """
+    nb, hkv, bs, d = k_codes.shape
+    qf = _widen(q).astype(np.float64)
+    T = qf.shape[0]
+    out = np.full((T, num_q_heads, d), np.nan)
+    keep = None if rows is None else set(int(r) for r in rows)
+    G = num_q_heads // hkv
+    cu = np.asarray(cu_seqlens_q)
+    for s, slot in enumerate(np.asarray(seq_slot)):
+        r0, r1 = int(cu[s]), int(cu[s + 1])
+        n, L = r1 - r0, int(context_lens[slot])
+        if n == 0:
+            continue
+        blocks = np.asarray(block_tables[slot][: -(-L // bs)], dtype=np.int64)
+        if np.any(blocks < 0) or np.any(blocks >= nb):
+            raise ValueError(f"segment {s}: block id outside the pool")
+        # [nblk, Hkv, bs, D] -> [nblk * bs, Hkv, D], first L positions
+        k = dequantize(k_codes[blocks], k_scales[blocks]).transpose(0, 2, 1, 3).reshape(-1, hkv, d)[:L]
+        v = dequantize(v_codes[blocks], v_scales[blocks]).transpose(0, 2, 1, 3).reshape(-1, hkv, d)[:L]
+        for i in range(n):
+            row = r0 + i
+            if keep is not None and row not in keep:
+                continue
+            p = L - n + i
+            for h in range(num_q_heads):
+                sc = scale * (k[: p + 1, h // G, :] @ qf[row, h, :])
+                w = np.exp(sc - sc.max())
+                out[row, h, :] = (w @ v[: p + 1, h // G, :]) / w.sum()
+    return out
