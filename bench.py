@@ -86,6 +86,8 @@ def parse_args(argv=None):
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle CPU-baseline budget")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=300)
+    p.add_argument("--kv", choices=["bf16", "q8"], default="bf16",
+                   help="pool format: bf16, or the 8-bit block-scaled pool (no end-to-end leg)")
     p.add_argument("--pool-blocks", type=int, default=None,
                    help="smaller synthetic pool (same contexts) for profiling captures")
     return p.parse_args(argv)
@@ -95,10 +97,14 @@ def parse_args(argv=None):
 # Work accounting (from the workload's shapes only).
 # ---------------------------------------------------------------------------
 
-def kv_bytes(w) -> int:
-    """Algorithmic bytes of the attention: K and V of every visible key once per kv head, Q in, O out."""
-    kv = sum(s.ctx for s in w.segments) * w.num_kv_heads * w.head_dim * 2 * 2
-    return kv + w.total_q * w.num_q_heads * w.head_dim * 2 * 2
+def kv_bytes(w, kv: str = "bf16") -> int:
+    """Algorithmic bytes of the attention: K and V of every visible key once per kv head, Q in, O out.
+
+    A key's row costs 2 * head_dim bytes in a bf16 pool, head_dim codes plus
+    head_dim / 32 bf16 scales in the 8-bit pool."""
+    row = w.head_dim * 2 if kv == "bf16" else w.head_dim + w.head_dim // 16
+    kvb = sum(s.ctx for s in w.segments) * w.num_kv_heads * row * 2
+    return kvb + w.total_q * w.num_q_heads * w.head_dim * 2 * 2
 
 
 def write_bytes(w) -> int:
@@ -344,8 +350,9 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     w = W.make_step(args.workload, args.seed, pool_blocks=args.pool_blocks)
-    ds = R.prepare(w, dev)
+    ds = R.prepare(w, dev, kv=args.kv)
     stream = torch.cuda.current_stream()
+    kvb = kv_bytes(w, args.kv)
     flush = L2Flush(dev)
     launches_per_step = (int(w.total_q > 0) + int(ds.info.num_decode_items > 0) + int(ds.info.num_prefill_items > 0)
                          + int(ds.info.num_combine_items > 0))
@@ -402,7 +409,7 @@ def run_ours(args, rank, world, local_rank):
     # work list launches the tensor-core chunk kernel alone (same inputs and
     # output rows), so its own duration is measured on the launching stream.
     chunk_ms = []
-    if ds.info.num_prefill_items:
+    if ds.info.num_prefill_items and args.kv == "bf16":
         wi = R.chunk_only(ds)
         ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(max(args.steps // 4, 20))]
         for e0, e1 in ev:
@@ -415,17 +422,17 @@ def run_ours(args, rank, world, local_rank):
     if B.pkv_check_device_status(ds.status) != 0:
         raise RuntimeError("device status reported an error during the timed steps")
 
-    total_ms, total_bytes = aggregate(sum(step_ms), kv_bytes(w) * args.steps, world)
+    total_ms, total_bytes = aggregate(sum(step_ms), kvb * args.steps, world)
     hbm, tflops, peak_src = peaks()
     value = total_bytes / (total_ms / 1e3) / 1e9
     attn_mean = sum(attn_ms) / len(attn_ms)
-    achieved = kv_bytes(w) / (attn_mean / 1e3) / 1e9
+    achieved = kvb / (attn_mean / 1e3) / 1e9
     res = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": f"{args.workload}: {WORKLOAD_TEXT[args.workload]}",
-                   "rows_per_step": w.total_q, "kv_bytes_per_step": kv_bytes(w),
+                   "rows_per_step": w.total_q, "kv_bytes_per_step": kvb, "kv_format": args.kv,
                    "l2": "flushed before every step: 256 MiB written, then 256 MiB read so L2 holds clean lines; "
                          "both outside the timed events",
                    "parallelism": f"replicas x{world} (no exchange between GPUs)", "seed": args.seed,
@@ -436,13 +443,16 @@ def run_ours(args, rank, world, local_rank):
                               "step": statistics.median(step_ms)},
     }
     chunk_kernel = "prefill_pair_kernel" if w.head_dim == 128 else "prefill_kernel"
-    if ds.info.num_prefill_items:
+    dec_kernel = "decode_q8_kernel" if args.kv == "q8" else "decode_kernel"
+    if ds.info.num_prefill_items and args.kv == "bf16":
         # the chunk kernel dominates the library's time on steps that carry a prompt chunk
         bound, unit, kernel = "tensor", "TFLOP/s", chunk_kernel
+    elif ds.info.num_prefill_items:
+        bound, unit, kernel = "hbm", "GB/s", "attention call: widen_q8 + chunk + decode_q8 + merge kernels"
     elif ds.info.num_combine_items:
-        bound, unit, kernel = "hbm", "GB/s", "attention call: decode_kernel + merge_kernel"
+        bound, unit, kernel = "hbm", "GB/s", f"attention call: {dec_kernel} + merge_kernel"
     else:
-        bound, unit, kernel = "hbm", "GB/s", "decode_kernel"
+        bound, unit, kernel = "hbm", "GB/s", dec_kernel
     if bound == "tensor":
         chunk_mean = sum(chunk_ms) / len(chunk_ms)
         ach = chunk_flops(w) / (chunk_mean / 1e3) / 1e12
@@ -454,10 +464,11 @@ def run_ours(args, rank, world, local_rank):
         res["attention_call"] = {"kv_gbs": achieved, "pct_hbm_peak": 100.0 * achieved / hbm, "mean_ms": attn_mean,
                                  "kernels": "chunk + decode + span merge"}
     else:
-        traffic = profiled_traffic("pkv_decode.cu", args.workload) if kernel.startswith("attention call: decode") or kernel == "decode_kernel" else None
+        src = "pkv_kvq8.cu" if args.kv == "q8" else "pkv_decode.cu"
+        traffic = profiled_traffic(src, args.workload) if dec_kernel in kernel else None
         res["roofline"] = {"bound": "hbm", "kernel": kernel, "achieved": achieved, "peak": hbm, "unit": "GB/s",
                            "frac": achieved / hbm, "traffic": traffic,
-                           "algorithmic_bytes_per_launch": kv_bytes(w), "mean_launch_ms": attn_mean,
+                           "algorithmic_bytes_per_launch": kvb, "mean_launch_ms": attn_mean,
                            "peak_source": f"{peak_src} HBM copy bandwidth"}
     if chunk_ms:
         res["chunk_kernel_ms"] = statistics.median(chunk_ms)
@@ -465,9 +476,9 @@ def run_ours(args, rank, world, local_rank):
     res["clocks"] = clk
 
     # ---- end to end through the C ABI, inputs from pinned host memory ----
-    e2e = run_e2e(args, w, ds, dev, flush)
+    e2e = run_e2e(args, w, ds, dev, flush) if args.kv == "bf16" else None
     if e2e:
-        e_ms, e_units = aggregate(e2e["ms_total"], kv_bytes(w) * e2e["steps"], world)
+        e_ms, e_units = aggregate(e2e["ms_total"], kvb * e2e["steps"], world)
         res["e2e"] = {"value": e_units / (e_ms / 1e3) / 1e9, "unit": "GB/s",
                       "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
                       "steps": e2e["steps"], "ms_per_step": e_ms / e2e["steps"],

@@ -81,6 +81,20 @@ bool encode_pool(CUtensorMap *m, const void *pool, int64_t rows, int32_t head_di
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 8-bit codes [rows][D] -> boxes of 16 whole rows; 128-byte swizzle for
+// 128-byte rows (D = 128), 64-byte swizzle for 64-byte rows (D = 64).
+bool encode_codes(CUtensorMap *m, const void *codes, int64_t rows, int32_t head_dim) {
+  EncodeFn enc = encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(head_dim)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(head_dim), static_cast<cuuint32_t>(pkv::kSubKeys)};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(codes), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, head_dim == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // q [T][Hq][D] -> boxes of (64 columns, G heads, P positions), 128B swizzle.
 bool encode_q(CUtensorMap *m, const void *q, int64_t total_q, int32_t hq, int32_t d, int32_t g, int32_t p) {
   EncodeFn enc = encoder();
@@ -130,9 +144,10 @@ pkv_status pkv_attention(const void *q, const int32_t *cu_seqlens_q, int32_t num
   const int64_t rows = num_blocks * num_kv_heads * block_size;
   if (rows > INT32_MAX || total_q > INT32_MAX) return PKV_ERR_UNSUPPORTED;
   const int64_t items = static_cast<int64_t>(info->num_decode_items) + info->num_prefill_items +
-                        info->num_combine_items;
+                        info->num_combine_items + info->num_scratch_items;
   if (info->num_decode_items < 0 || info->num_prefill_items < 0 || info->num_combine_items < 0 ||
-      info->num_partials < 0 || info->work_words != items * PKV_WORK_WORDS_PER_ITEM)
+      info->num_scratch_items < 0 || info->num_partials < 0 ||
+      info->work_words != items * PKV_WORK_WORDS_PER_ITEM)
     return PKV_ERR_INVALID_ARG;
   if (items == 0 || total_q == 0) return PKV_OK;
   if (!q || !cu_seqlens_q || !seq_slot || !context_lens || !block_tables || !k_pool || !v_pool || !work || !out)
@@ -206,6 +221,150 @@ pkv_status pkv_attention(const void *q, const int32_t *cu_seqlens_q, int32_t num
   if (e == cudaSuccess) e = pkv::launch_merge(a, info->num_combine_items, comb, dst);
   if (side) {
     // join even after a failed launch, so the caller's stream never runs ahead of queued work
+    const cudaError_t j = cudaEventRecord(side->join, side->stream);
+    const cudaError_t w = j == cudaSuccess ? cudaStreamWaitEvent(st, side->join, 0) : j;
+    if (e == cudaSuccess) e = w;
+  }
+  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+pkv_status pkv_cache_write_q8(const void *k_new, const void *v_new, const int64_t *slot_mapping,
+                              int64_t num_tokens, int8_t *k_codes, void *k_scales, int8_t *v_codes, void *v_scales,
+                              int64_t num_blocks, int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
+                              uint32_t *device_status, pkv_stream_t stream) {
+  if (num_tokens < 0 || num_blocks <= 0 || block_size <= 0 || num_kv_heads <= 0) return PKV_ERR_INVALID_ARG;
+  if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return PKV_OK;
+  if (!k_new || !v_new || !slot_mapping || !k_codes || !v_codes || !k_scales || !v_scales)
+    return PKV_ERR_INVALID_ARG;
+  if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_codes, 16) || !aligned(v_codes, 16) ||
+      !aligned(k_scales, 16) || !aligned(v_scales, 16) || !aligned(slot_mapping, 8))
+    return PKV_ERR_INVALID_ARG;
+  cudaError_t e = pkv::launch_cache_write_q8(k_new, v_new, slot_mapping, num_tokens, k_codes, k_scales, v_codes,
+                                             v_scales, num_blocks, block_size, num_kv_heads, head_dim, device_status,
+                                             reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+pkv_status pkv_attention_q8(const void *q, const int32_t *cu_seqlens_q, int32_t num_seqs, int64_t total_q,
+                            const int32_t *seq_slot, const int32_t *context_lens, const int32_t *block_tables,
+                            int32_t max_slots, int32_t max_blocks_per_slot, int32_t block_size,
+                            const int8_t *k_codes, const void *k_scales, const int8_t *v_codes, const void *v_scales,
+                            int64_t num_blocks, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                            float scale, const int32_t *work, const pkv_work_info *info, void *out, void *workspace,
+                            uint64_t workspace_bytes, uint32_t *device_status, pkv_stream_t stream) {
+  if (!info || num_seqs < 0 || total_q < 0 || max_slots <= 0 || max_blocks_per_slot <= 0 || num_blocks <= 0)
+    return PKV_ERR_INVALID_ARG;
+  if (!supported_shape(block_size, num_q_heads, num_kv_heads, head_dim)) return PKV_ERR_UNSUPPORTED;
+  const int64_t rows = num_blocks * num_kv_heads * block_size;
+  if (rows > INT32_MAX || total_q > INT32_MAX) return PKV_ERR_UNSUPPORTED;
+  const int64_t items = static_cast<int64_t>(info->num_decode_items) + info->num_prefill_items +
+                        info->num_combine_items + info->num_scratch_items;
+  if (info->num_decode_items < 0 || info->num_prefill_items < 0 || info->num_combine_items < 0 ||
+      info->num_scratch_items < 0 || info->num_partials < 0 || info->scratch_blocks < 0 ||
+      info->work_words != items * PKV_WORK_WORDS_PER_ITEM ||
+      (info->num_prefill_items > 0) != (info->num_scratch_items > 0))
+    return PKV_ERR_INVALID_ARG;
+  if (items == 0 || total_q == 0) return PKV_OK;
+  if (!q || !cu_seqlens_q || !seq_slot || !context_lens || !block_tables || !k_codes || !v_codes || !k_scales ||
+      !v_scales || !work || !out)
+    return PKV_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k_codes, 16) || !aligned(v_codes, 16) || !aligned(k_scales, 16) ||
+      !aligned(v_scales, 16) || !aligned(out, 16) || !aligned(work, 16))
+    return PKV_ERR_INVALID_ARG;
+  const uint64_t acc_bytes = align256(uint64_t(info->num_partials) * num_q_heads * head_dim * 4);
+  const uint64_t ml_bytes = align256(uint64_t(info->num_partials) * num_q_heads * 8);
+  const uint64_t part_bytes = info->num_partials == 0 ? 0 : acc_bytes + ml_bytes;
+  const uint64_t sb = static_cast<uint64_t>(info->scratch_blocks);
+  const uint64_t scratch_pool = align256(sb * num_kv_heads * block_size * head_dim * 2);
+  const uint64_t table_bytes = align256(uint64_t(max_slots) * max_blocks_per_slot * 4);
+  const uint64_t need = part_bytes + (sb ? 2 * scratch_pool + table_bytes : 0);
+  if (need != info->workspace_bytes_q8) return PKV_ERR_INVALID_ARG;  // info from another shape
+  if (need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 256)))
+    return PKV_ERR_WORKSPACE_TOO_SMALL;
+  if ((info->num_combine_items > 0) != (info->num_partials > 0)) return PKV_ERR_INVALID_ARG;
+  if (info->decode_rows_max < 0 ||
+      (info->num_decode_items > 0 && info->decode_rows_max * (num_q_heads / num_kv_heads) > 16))
+    return PKV_ERR_INVALID_ARG;
+  if (sb && sb * num_kv_heads * block_size > INT32_MAX) return PKV_ERR_UNSUPPORTED;
+
+  pkv::StepArgs a{};
+  a.q = q;
+  a.k_pool = k_codes;
+  a.v_pool = v_codes;
+  a.cu_seqlens_q = cu_seqlens_q;
+  a.seq_slot = seq_slot;
+  a.context_lens = context_lens;
+  a.block_tables = block_tables;
+  a.num_seqs = num_seqs;
+  a.max_slots = max_slots;
+  a.max_blocks_per_slot = max_blocks_per_slot;
+  a.block_size = block_size;
+  a.num_blocks = num_blocks;
+  a.total_q = total_q;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.group = num_q_heads / num_kv_heads;
+  a.head_dim = head_dim;
+  a.decode_rows_max = info->decode_rows_max;
+  const float s = scale > 0.f ? scale : 1.0f / std::sqrt(static_cast<float>(head_dim));
+  a.scale_log2 = s * 1.4426950408889634f;
+  a.work = work;
+  a.out = out;
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  a.partial_acc = info->num_partials ? reinterpret_cast<float *>(ws) : nullptr;
+  a.partial_ml = info->num_partials ? reinterpret_cast<float *>(ws + acc_bytes) : nullptr;
+  a.status = device_status;
+
+  // The chunk kernel reads a bf16 scratch pool: the chunk segments' histories,
+  // widened block by block, with a scratch block table in the same shape.
+  pkv::StepArgs c = a;
+  void *scratch_k = nullptr, *scratch_v = nullptr;
+  int32_t *scratch_table = nullptr;
+  if (sb) {
+    scratch_k = ws + part_bytes;
+    scratch_v = ws + part_bytes + scratch_pool;
+    scratch_table = reinterpret_cast<int32_t *>(ws + part_bytes + 2 * scratch_pool);
+    c.k_pool = scratch_k;
+    c.v_pool = scratch_v;
+    c.block_tables = scratch_table;
+    c.num_blocks = static_cast<int64_t>(sb);
+  }
+
+  CUtensorMap tkc, tvc, tq, tk, tv;
+  if (info->num_decode_items > 0 &&
+      (!encode_codes(&tkc, k_codes, rows, head_dim) || !encode_codes(&tvc, v_codes, rows, head_dim)))
+    return PKV_ERR_CUDA;
+  const int32_t rpt = pkv::prefill_rows_per_tile(a.group);
+  if (info->num_prefill_items > 0) {
+    const int64_t srows = static_cast<int64_t>(sb) * num_kv_heads * block_size;
+    if (!encode_q(&tq, q, total_q, num_q_heads, head_dim, a.group, rpt) ||
+        !encode_pool(&tk, scratch_k, srows, head_dim) || !encode_pool(&tv, scratch_v, srows, head_dim))
+      return PKV_ERR_CUDA;
+  }
+
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int32_t *dec = work;
+  const int32_t *pre = dec + static_cast<int64_t>(info->num_decode_items) * PKV_WORK_WORDS_PER_ITEM;
+  const int32_t *comb = pre + static_cast<int64_t>(info->num_prefill_items) * PKV_WORK_WORDS_PER_ITEM;
+  const int32_t *scr = comb + static_cast<int64_t>(info->num_combine_items) * PKV_WORK_WORDS_PER_ITEM;
+  SideStream *side = (info->num_prefill_items > 0 && info->num_decode_items > 0) ? side_stream() : nullptr;
+  std::unique_lock<std::mutex> lock;
+  if (side) lock = std::unique_lock<std::mutex>(side->mu);
+  cudaError_t e = side ? cudaEventRecord(side->fork, st) : cudaSuccess;
+  if (e == cudaSuccess && info->num_prefill_items > 0) {
+    e = pkv::launch_widen_q8(a, k_codes, k_scales, v_codes, v_scales, scratch_k, scratch_v, scratch_table,
+                             static_cast<int64_t>(sb), info->num_scratch_items, scr, st);
+    if (e == cudaSuccess)
+      e = head_dim == 128 ? pkv::launch_prefill_pair(c, tq, tk, tv, rpt, info->num_prefill_items, pre, st)
+                          : pkv::launch_prefill(c, tq, rpt, info->num_prefill_items, pre, st);
+  }
+  cudaStream_t dst = side ? side->stream : st;
+  if (e == cudaSuccess && side) e = cudaStreamWaitEvent(side->stream, side->fork, 0);
+  if (e == cudaSuccess)
+    e = pkv::launch_decode_q8(a, tkc, tvc, k_scales, v_scales, info->num_decode_items, dec, dst);
+  if (e == cudaSuccess) e = pkv::launch_merge(a, info->num_combine_items, comb, dst);
+  if (side) {
     const cudaError_t j = cudaEventRecord(side->join, side->stream);
     const cudaError_t w = j == cudaSuccess ? cudaStreamWaitEvent(st, side->join, 0) : j;
     if (e == cudaSuccess) e = w;

@@ -281,7 +281,8 @@ pkv_status pkv_plan_work(const int32_t *cu, int32_t num_seqs, const int32_t *seq
     int32_t w[4];
     int64_t cost;
   };
-  std::vector<Item> dec, pre, comb;
+  std::vector<Item> dec, pre, comb, scr;
+  int64_t scratch_blocks = 0;
   std::vector<uint8_t> used(static_cast<size_t>(max_slots), 0);
   const int32_t rows_per_tile = 128 / group;
   // Segments of up to 16 / group rows (decode rows and short verify runs) take
@@ -317,6 +318,12 @@ pkv_status pkv_plan_work(const int32_t *cu, int32_t num_seqs, const int32_t *seq
       }
       rows_max = std::max(rows_max, n);
     } else {
+      // The 8-bit pool's chunk path first widens the segment's whole history
+      // into scratch blocks [first, first + blocks) of a bf16 scratch pool.
+      const int64_t nblk = ceil_div(L, block_size);
+      scr.push_back({{s, slot, static_cast<int32_t>(scratch_blocks), static_cast<int32_t>(nblk)}, 0});
+      scratch_blocks += nblk;
+      if (scratch_blocks > INT32_MAX) return PKV_ERR_UNSUPPORTED;
       // head_dim 128 runs tiles in pairs on two SMs (the second may be past the segment's end).
       const int32_t tiles = static_cast<int32_t>(ceil_div(n, rows_per_tile));
       const int32_t step = head_dim == 128 ? 2 : 1;
@@ -338,16 +345,23 @@ pkv_status pkv_plan_work(const int32_t *cu, int32_t num_seqs, const int32_t *seq
   info->num_combine_items = static_cast<int32_t>(comb.size());
   info->num_partials = partials;
   info->decode_rows_max = rows_max;
-  const int64_t items = static_cast<int64_t>(dec.size() + pre.size() + comb.size());
+  info->num_scratch_items = static_cast<int32_t>(scr.size());
+  info->scratch_blocks = scratch_blocks;
+  const int64_t items = static_cast<int64_t>(dec.size() + pre.size() + comb.size() + scr.size());
   info->work_words = items * PKV_WORK_WORDS_PER_ITEM;
   auto align256 = [](uint64_t x) { return (x + 255) & ~uint64_t(255); };
   info->workspace_bytes =
       partials == 0 ? 0
                     : align256(uint64_t(partials) * num_q_heads * head_dim * 4) +
                           align256(uint64_t(partials) * num_q_heads * 2 * 4);
+  info->workspace_bytes_q8 =
+      info->workspace_bytes +
+      (scratch_blocks == 0 ? 0
+                           : 2 * align256(uint64_t(scratch_blocks) * num_kv_heads * block_size * head_dim * 2) +
+                                 align256(uint64_t(max_slots) * max_blocks_per_slot * 4));
   if (!work || work_capacity < info->work_words) return PKV_ERR_WORKSPACE_TOO_SMALL;
   int32_t *w = work;
-  for (const auto *v : {&dec, &pre, &comb})
+  for (const auto *v : {&dec, &pre, &comb, &scr})
     for (const Item &it : *v) {
       std::memcpy(w, it.w, sizeof(it.w));
       w += PKV_WORK_WORDS_PER_ITEM;

@@ -1,0 +1,724 @@
+// 8-bit block-scaled KV pool: the quantising cache write, split-KV decode
+// attention straight from the 8-bit codes, and the widening of prompt-chunk
+// histories into a bf16 scratch pool for the tensor-core chunk kernel.
+//
+// Lucebox, "Continuous batching: Qwen3.8-27B at 301 tok/s across five
+// clients, up to 1.97x llama.cpp", §Qwen3.8-27B DFlash2 on the R9700 (vs
+// llama.cpp) and §DeepSeek V4 Flash on Strix Halo and two GPUs: the pages
+// serve from 8-bit and 4-bit KV caches without defining the formats. This
+// library's 8-bit format: every pool row (token, kv head) is cut into groups
+// of 32 values; a group keeps one power-of-two scale d, the smallest at or
+// above amax / 127 (at least 2^-126), stored as a bfloat16 (exact), and 32
+// int8 codes round_half_even(x / d) clamped to [-127, 127] -- the
+// shared-exponent choice of the OCP microscaling formats. x / d is exact and
+// every code * d is a bfloat16 number, so widening codes to bf16 loses
+// nothing. Codes live in [num_blocks][Hkv][bs][D] int8, scales in
+// [num_blocks][Hkv][bs][D / 32] bf16: a row costs D + D / 16 bytes instead of
+// 2 D, so decode reads 53% of the bf16 pool's bytes.
+//
+// Decode kernel (same task pipeline as the bf16 decode kernel: persistent
+// warps, a TMA ring per warp, work sorted longest first). Per 16-key sub-tile
+// a stage holds the K and V codes (TMA, swizzled like the bf16 tiles) and
+// their scales (one bulk copy each). Math, per warp:
+//   S^T = K Q^T as fp16 MMAs over the integer codes (exact in fp16), one
+//   accumulator per scale group; the group scales multiply the four partial
+//   sums in fp32. Q is widened to fp16 after a power-of-two rescale per
+//   column (max |q'| < 2^15), undone in the softmax scale, so fp16's range
+//   never clips a query.
+//   O^T += V^T P^T as bf16 MMAs over the integer codes (exact in bf16), with
+//   each V scale folded into P: the m-tiles of one scale group share one
+//   scaled copy of P^T. head_dim is permuted inside each tile so that every
+//   thread reads whole 4-byte words of codes; the permutation is undone in the
+//   output address.
+// Codes become floats without conversion instructions: a byte b (offset by
+// 128) placed under the exponent of 1024.0 (fp16) or 2^23 (fp32) is that
+// power plus b, one subtraction away from the code.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+
+#include "pkv_decode_task.cuh"
+#include "pkv_internal.h"
+#include "pkv_ptx.cuh"
+
+namespace pkv {
+namespace {
+
+constexpr int kWarpsQ8 = 8;
+constexpr uint32_t kAll = 0xffffffffu;
+constexpr float kRescaleQ8 = 8.0f;  // log2 units, as in the bf16 decode kernel
+
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
+
+// ---- quantising cache write ---------------------------------------------------
+
+// One warp per (k or v, token, kv head) row; lane l holds D/32 consecutive
+// values, so one scale group spans 1024/D lanes.
+template <int D>
+__global__ void __launch_bounds__(256) cache_write_q8_kernel(
+    const __nv_bfloat16 *__restrict__ k_new, const __nv_bfloat16 *__restrict__ v_new,
+    const int64_t *__restrict__ slot_mapping, int64_t num_tokens, int8_t *__restrict__ k_codes,
+    __nv_bfloat16 *__restrict__ k_scales, int8_t *__restrict__ v_codes, __nv_bfloat16 *__restrict__ v_scales,
+    int64_t pool_rows, int32_t block_size, int32_t num_kv_heads, uint32_t *__restrict__ status) {
+  grid_dependency_wait();
+  launch_dependents();  // as the bf16 cache write: everything before this kernel has finished
+  constexpr int VPL = D / 32;       // values per lane
+  constexpr int LPG = 32 / VPL;     // lanes per scale group
+  const int lane = threadIdx.x & 31;
+  const int64_t per_tensor = num_tokens * num_kv_heads;
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x / 32);
+  for (int64_t w = static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32; w < 2 * per_tensor;
+       w += warps) {
+    const bool is_v = w >= per_tensor;
+    const int64_t th = is_v ? w - per_tensor : w;
+    const int64_t t = th / num_kv_heads, h = th % num_kv_heads;
+    const int64_t s = __ldg(slot_mapping + t);
+    if (s < 0) continue;
+    if (s >= pool_rows) {
+      if (status && lane == 0 && h == 0 && !is_v) atomicOr(status, PKV_DEV_BAD_SLOT_MAPPING);
+      continue;
+    }
+    const __nv_bfloat16 *src = (is_v ? v_new : k_new) + th * D + lane * VPL;
+    float x[VPL];
+    if constexpr (VPL == 4) {
+      const uint2 raw = __ldg(reinterpret_cast<const uint2 *>(src));
+      x[0] = bf16_bits_to_float(raw.x & 0xFFFFu);
+      x[1] = bf16_bits_to_float(raw.x >> 16);
+      x[2] = bf16_bits_to_float(raw.y & 0xFFFFu);
+      x[3] = bf16_bits_to_float(raw.y >> 16);
+    } else {
+      const uint32_t raw = __ldg(reinterpret_cast<const uint32_t *>(src));
+      x[0] = bf16_bits_to_float(raw & 0xFFFFu);
+      x[1] = bf16_bits_to_float(raw >> 16);
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) amax = fmaxf(amax, fabsf(x[i]));
+#pragma unroll
+    for (int o = 1; o < LPG; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(kAll, amax, o));
+    // d: the smallest power of two >= amax / 127 (float32 quotient), at least 2^-126
+    const uint32_t tb = __float_as_uint(__fdiv_rn(amax, 127.f));
+    const uint32_t te = tb & 0x7F800000u;
+    uint32_t db = (tb & 0x007FFFFFu) == 0 ? tb : te + 0x00800000u;
+    if (te == 0) db = 0x00800000u;
+    if (tb == 0) db = 0;
+    const float d = __uint_as_float(db);
+    const __nv_bfloat16 dq = __ushort_as_bfloat16(static_cast<unsigned short>(db >> 16));
+    uint32_t packed = 0;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      float c = d > 0.f ? rintf(__fdiv_rn(x[i], d)) : 0.f;
+      c = fminf(fmaxf(c, -127.f), 127.f);
+      packed |= (static_cast<uint32_t>(static_cast<int32_t>(c)) & 0xFFu) << (8 * i);
+    }
+    const int64_t blk = s / block_size, row = s % block_size;
+    const int64_t prow = (blk * num_kv_heads + h) * block_size + row;
+    int8_t *dst = (is_v ? v_codes : k_codes) + prow * D + lane * VPL;
+    if constexpr (VPL == 4)
+      *reinterpret_cast<uint32_t *>(dst) = packed;
+    else
+      *reinterpret_cast<uint16_t *>(dst) = static_cast<uint16_t>(packed);
+    if (lane % LPG == 0) (is_v ? v_scales : k_scales)[prow * (D / 32) + lane / LPG] = dq;
+  }
+}
+
+// ---- prompt-chunk histories widened into a bf16 scratch pool ------------------
+
+// Item (segment, slot, first scratch block, blocks). CTA (item, y) widens the
+// item's logical blocks y, y + gridDim.y, ... : block j of the slot becomes
+// scratch block first + j, and the scratch table row of the slot points there.
+template <int D>
+__global__ void __launch_bounds__(256) widen_q8_kernel(const StepArgs a, const int32_t *__restrict__ items,
+                                                       const int8_t *__restrict__ k_codes,
+                                                       const __nv_bfloat16 *__restrict__ k_scales,
+                                                       const int8_t *__restrict__ v_codes,
+                                                       const __nv_bfloat16 *__restrict__ v_scales,
+                                                       __nv_bfloat16 *__restrict__ k_out,
+                                                       __nv_bfloat16 *__restrict__ v_out,
+                                                       int32_t *__restrict__ scratch_table, int64_t scratch_blocks) {
+  const int4 it = __ldg(reinterpret_cast<const int4 *>(items) + blockIdx.x);
+  const int seg = it.x, slot = it.y, first = it.z, nblk = it.w;
+  bool ok = seg >= 0 && seg < a.num_seqs && slot >= 0 && slot < a.max_slots && first >= 0 && nblk >= 1 &&
+            static_cast<int64_t>(first) + nblk <= scratch_blocks && nblk <= a.max_blocks_per_slot;
+  if (ok) {
+    const int L = __ldg(a.context_lens + slot);
+    ok = __ldg(a.seq_slot + seg) == slot && (L + a.block_size - 1) / a.block_size == nblk;
+  }
+  grid_dependency_wait();  // the codes come from the cache write before this kernel
+  launch_dependents();
+  if (!ok) {
+    if (threadIdx.x == 0 && blockIdx.y == 0 && a.status) atomicOr(a.status, PKV_DEV_BAD_SEGMENT);
+    return;
+  }
+  constexpr int NG = D / 32;
+  const int64_t rows = static_cast<int64_t>(a.num_kv_heads) * a.block_size;  // rows of one block
+  const int64_t vecs = rows * (D / 8);                                      // 8 values per vector
+  for (int j = blockIdx.y; j < nblk; j += gridDim.y) {
+    const int bid = __ldg(a.block_tables + static_cast<int64_t>(slot) * a.max_blocks_per_slot + j);
+    const bool in_pool = bid >= 0 && bid < a.num_blocks;
+    if (!in_pool && threadIdx.x == 0 && a.status) atomicOr(a.status, PKV_DEV_BAD_BLOCK);
+    if (threadIdx.x == 0) scratch_table[static_cast<int64_t>(slot) * a.max_blocks_per_slot + j] = first + j;
+    const int64_t src_row0 = static_cast<int64_t>(in_pool ? bid : 0) * rows;
+    const int64_t dst_row0 = static_cast<int64_t>(first + j) * rows;
+    for (int64_t i = threadIdx.x; i < 2 * vecs; i += blockDim.x) {
+      const bool is_v = i >= vecs;
+      const int64_t e = is_v ? i - vecs : i;
+      const int64_t r = e / (D / 8), c8 = e % (D / 8);
+      uint4 outv = make_uint4(0, 0, 0, 0);
+      if (in_pool) {
+        const int8_t *codes = (is_v ? v_codes : k_codes) + (src_row0 + r) * D + c8 * 8;
+        const __nv_bfloat16 *sc = (is_v ? v_scales : k_scales) + (src_row0 + r) * NG + (c8 * 8) / 32;
+        const uint2 raw = __ldg(reinterpret_cast<const uint2 *>(codes));
+        const float d = __bfloat162float(*sc);
+        uint32_t w[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t word = q < 2 ? raw.x : raw.y;
+          const int b0 = (q & 1) * 2;
+          const float lo = static_cast<float>(static_cast<int8_t>((word >> (8 * b0)) & 0xFF)) * d;
+          const float hi = static_cast<float>(static_cast<int8_t>((word >> (8 * (b0 + 1))) & 0xFF)) * d;
+          w[q] = pack_bf16x2(lo, hi);
+        }
+        outv = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+      *reinterpret_cast<uint4 *>((is_v ? v_out : k_out) + (dst_row0 + r) * D + c8 * 8) = outv;
+    }
+  }
+}
+
+// ---- split-KV decode over the codes ---------------------------------------------
+
+template <int D>
+struct Q8Cfg {
+  static constexpr int kGroups = D / 32;
+  static constexpr int kCodeBytes = kSubKeys * D;              // K (or V) codes of one sub-tile
+  static constexpr int kScaleBytes = kSubKeys * kGroups * 2;   // their scales
+  static constexpr int kStages = D == 128 ? 6 : 12;
+  static constexpr int kVc = kStages * kCodeBytes;             // offsets inside a warp's ring
+  static constexpr int kKs = 2 * kStages * kCodeBytes;
+  static constexpr int kVs = kKs + kStages * kScaleBytes;
+  static constexpr int kWarpRing = ((kVs + kStages * kScaleBytes) + 1023) / 1024 * 1024;
+  static constexpr int kStageTx = 2 * kCodeBytes + 2 * kScaleBytes;
+  static constexpr int kSmem = kWarpsQ8 * kWarpRing + kWarpsQ8 * kStages * 8 + 1024;
+  static_assert(kSmem <= 232448, "decode ring exceeds shared memory");
+};
+
+// Byte (row, col) of a swizzled sub-tile of codes: 128-byte rows with the
+// 128-byte swizzle (D = 128) or 64-byte rows with the 64-byte swizzle (D = 64).
+template <int D>
+__device__ __forceinline__ uint32_t code_off(int row, int col) {
+  if constexpr (D == 128)
+    return row * 128 + ((((col >> 4) ^ (row & 7))) << 4) + (col & 15);
+  else
+    return row * 64 + ((((col >> 4) ^ ((row >> 1) & 3))) << 4) + (col & 15);
+}
+
+// Four codes (a word, two's complement) -> two fp16 pairs of the integer values.
+__device__ __forceinline__ void codes_to_f16(uint32_t w, uint32_t &lo, uint32_t &hi) {
+  const uint32_t u = w ^ 0x80808080u;                  // offset by 128
+  const uint32_t m = 0x64806480u;                      // 1152 = 1024 + 128 in both halves
+  const uint32_t a = prmt(u, 0x64646464u, 0x4140u);    // 1024 + u0, 1024 + u1
+  const uint32_t b = prmt(u, 0x64646464u, 0x4342u);    // 1024 + u2, 1024 + u3
+  __half2 ha = __hsub2(*reinterpret_cast<const __half2 *>(&a), *reinterpret_cast<const __half2 *>(&m));
+  __half2 hb = __hsub2(*reinterpret_cast<const __half2 *>(&b), *reinterpret_cast<const __half2 *>(&m));
+  lo = *reinterpret_cast<uint32_t *>(&ha);
+  hi = *reinterpret_cast<uint32_t *>(&hb);
+}
+
+// Code byte `sel` of word x and of word y -> one bf16 pair (x's in the low half).
+__device__ __forceinline__ uint32_t codes_to_bf16_pair(uint32_t ux, uint32_t uy, uint32_t sel) {
+  const float fx = __uint_as_float(prmt(ux, 0x4B000000u, 0x7540u | sel)) - 8388736.f;  // 2^23 + 128
+  const float fy = __uint_as_float(prmt(uy, 0x4B000000u, 0x7540u | sel)) - 8388736.f;
+  return prmt(__float_as_uint(fx), __float_as_uint(fy), 0x7632u);  // upper halves: exact for integers
+}
+
+// Q'^T fragments (B operand, fp16) for k-step kk = 2 g + h: thread (column
+// lane/4, j = lane%4) holds q[column][32 g + 16 h + 4 j + 0..3], scaled by
+// 2^sh (per column) so that max |q'| < 2^15; `inv` receives 2^-sh.
+template <int D, int NT, bool MULTI>
+__device__ __forceinline__ void load_q_q8(uint32_t (&qf)[NT][D / 16][2], float (&inv)[NT], const Task &T,
+                                          const StepArgs &a, int lane) {
+  constexpr int KT = D / 16;
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int col = nt * 8 + (lane >> 2);
+    const bool valid = col < (MULTI ? T.nrows : 1) * a.group;
+    const int i = MULTI && valid ? col / a.group : 0, h = !MULTI ? col : valid ? col % a.group : 0;
+    const __nv_bfloat16 *qrow = static_cast<const __nv_bfloat16 *>(a.q) +
+                                ((static_cast<size_t>(T.row0) + i) * a.num_q_heads + T.g * a.group + h) * D;
+    const int j = lane & 3;
+    uint2 raw[KT];
+    float mx = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < KT; ++kk) {
+      raw[kk] = valid ? __ldg(reinterpret_cast<const uint2 *>(qrow + 32 * (kk >> 1) + 16 * (kk & 1) + 4 * j))
+                      : make_uint2(0, 0);
+      mx = fmaxf(mx, fmaxf(fmaxf(fabsf(bf16_bits_to_float(raw[kk].x & 0xFFFFu)),
+                                 fabsf(bf16_bits_to_float(raw[kk].x >> 16))),
+                           fmaxf(fabsf(bf16_bits_to_float(raw[kk].y & 0xFFFFu)),
+                                 fabsf(bf16_bits_to_float(raw[kk].y >> 16)))));
+    }
+    mx = fmaxf(mx, __shfl_xor_sync(kAll, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(kAll, mx, 2));
+    // exponent of mx (its float bits; 0 and subnormals read as -127)
+    const int e = static_cast<int>((__float_as_uint(mx) >> 23) & 0xFF) - 127;
+    const int sh = mx > 0.f ? min(126, max(-126, 14 - e)) : 0;
+    const float f = __uint_as_float(static_cast<uint32_t>(sh + 127) << 23);
+    inv[nt] = __uint_as_float(static_cast<uint32_t>(127 - sh) << 23);
+#pragma unroll
+    for (int kk = 0; kk < KT; ++kk) {
+      __half2 lo = __floats2half2_rn(bf16_bits_to_float(raw[kk].x & 0xFFFFu) * f,
+                                     bf16_bits_to_float(raw[kk].x >> 16) * f);
+      __half2 hi = __floats2half2_rn(bf16_bits_to_float(raw[kk].y & 0xFFFFu) * f,
+                                     bf16_bits_to_float(raw[kk].y >> 16) * f);
+      qf[nt][kk][0] = *reinterpret_cast<uint32_t *>(&lo);
+      qf[nt][kk][1] = *reinterpret_cast<uint32_t *>(&hi);
+    }
+  }
+}
+
+template <int D, int NT, bool MULTI>
+__global__ void __launch_bounds__(kWarpsQ8 * 32, 1)
+    decode_q8_kernel(const __grid_constant__ CUtensorMap tmap_kc, const __grid_constant__ CUtensorMap tmap_vc,
+                     const StepArgs a, const __nv_bfloat16 *__restrict__ k_scales,
+                     const __nv_bfloat16 *__restrict__ v_scales, const int32_t *__restrict__ items, int num_items) {
+  using Cfg = Q8Cfg<D>;
+  constexpr int KT = D / 16;  // k-steps of QK^T, m-tiles of PV
+  constexpr int NG = Cfg::kGroups;
+  constexpr int NST = Cfg::kStages;
+  constexpr int kMaxRows = MULTI ? 16 : 1;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint8_t *ring = smem + warp * Cfg::kWarpRing;
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + kWarpsQ8 * Cfg::kWarpRing) + warp * NST;
+
+  launch_dependents();  // the span merge may launch now; it waits for this grid before reading
+  const int hkv = a.num_kv_heads;
+  const int num_tasks = num_items * hkv;
+  const int stride = gridDim.x * kWarpsQ8;
+  const int t0 = warp * gridDim.x + blockIdx.x;
+  if (t0 >= num_tasks) return;
+  if (lane == 0) {
+    for (int s = 0; s < NST; ++s) mbar_init(full + s, 1);
+    fence_barrier_init();
+    prefetch_tensormap(&tmap_kc);
+    prefetch_tensormap(&tmap_vc);
+  }
+  __syncwarp();
+  bool waited = false;  // rows written by the kernel before (this step's) are read after its wait
+
+  Task A, B;
+  int4 rawC = make_int4(0, 0, 0, 0);
+  expand(A, t0, load_item(items, t0, hkv), a, lane);
+  {
+    const int t1 = t0 + stride;
+    expand(B, t1 < num_tasks ? t1 : -1, t1 < num_tasks ? load_item(items, t1, hkv) : rawC, a, lane);
+    const int t2 = t1 + stride;
+    if (t2 < num_tasks) rawC = load_item(items, t2, hkv);
+  }
+  finalize(A, a, lane, 8 * NT, kMaxRows);
+  uint32_t qA[NT][KT][2], qB[NT][KT][2];
+  float invA[NT], invB[NT];
+  if (A.ok) load_q_q8<D, NT, MULTI>(qA, invA, A, a, lane);
+  bool qB_loaded = false;
+
+  int P = 0, C = 0, pa = 0, pb = 0;
+  int pstage = 0;
+  auto issue = [&](const Task &T, int u) {
+    if (T.reads_new && !waited) {
+      grid_dependency_wait();
+      waited = true;
+    }
+    const int row = __shfl_sync(kAll, T.row, u);
+    if (lane == 0) {
+      uint64_t *bar = full + pstage;
+      if (row >= 0) {
+        mbar_arrive_expect_tx(bar, Cfg::kStageTx);
+        tma_load_2d(ring + pstage * Cfg::kCodeBytes, &tmap_kc, 0, row, bar);
+        tma_load_2d(ring + Cfg::kVc + pstage * Cfg::kCodeBytes, &tmap_vc, 0, row, bar);
+        bulk_load(ring + Cfg::kKs + pstage * Cfg::kScaleBytes, k_scales + static_cast<int64_t>(row) * NG,
+                  Cfg::kScaleBytes, bar);
+        bulk_load(ring + Cfg::kVs + pstage * Cfg::kScaleBytes, v_scales + static_cast<int64_t>(row) * NG,
+                  Cfg::kScaleBytes, bar);
+      } else {
+        mbar_arrive(bar);  // nothing loaded; the consumer masks this sub-tile out
+      }
+    }
+    ++P;
+    pstage = pstage + 1 == NST ? 0 : pstage + 1;
+  };
+  auto issue_next = [&]() -> bool {
+    if (pa < A.units) {
+      issue(A, pa++);
+      return true;
+    }
+    if (B.t >= 0) {
+      if (!B.finalized) {
+        finalize(B, a, lane, 8 * NT, kMaxRows);
+        if (B.ok) {
+          load_q_q8<D, NT, MULTI>(qB, invB, B, a, lane);
+          qB_loaded = true;
+        }
+      }
+      if (pb < B.units) {
+        issue(B, pb++);
+        return true;
+      }
+    }
+    return false;
+  };
+  while (P - C < NST && issue_next()) {
+  }
+
+  const uint32_t ring_addr = smem_addr(ring);
+  const float sl2 = a.scale_log2;
+  const int G = a.group;
+  const int ka = lane >> 2, kb = ka + 8, jq = lane & 3, k0 = jq * 2, r = lane >> 2;
+  // per-thread code offsets inside a sub-tile (rows kb = ka + 8 and k0 + 8 share the swizzle phase)
+  const uint32_t koff = code_off<D>(ka, 4 * jq);  // + group/half chunk below
+  int cstage = 0;
+  uint32_t cphase = 0;
+
+  while (A.t >= 0) {
+    float m[NT][2], l[NT][2], acc[NT][KT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      m[nt][0] = m[nt][1] = -INFINITY;
+      l[nt][0] = l[nt][1] = 0.f;
+#pragma unroll
+      for (int mt = 0; mt < KT; ++mt) acc[nt][mt][0] = acc[nt][mt][1] = acc[nt][mt][2] = acc[nt][mt][3] = 0.f;
+    }
+    const int nrows = MULTI ? A.nrows : 1;
+    uint32_t colrow = 0;
+    if (MULTI) {
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const int col = nt * 8 + jq * 2 + c;
+          const int i = col < nrows * G ? col / G : nrows - 1;
+          colrow |= static_cast<uint32_t>(i & 0xFF) << (8 * (nt * 2 + c));
+        }
+    }
+    // softmax scale of this thread's columns (2 jq + c): scale * log2(e) / 2^sh of the column
+    float sl2c[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int c = 0; c < 2; ++c) sl2c[nt][c] = sl2 * __shfl_sync(kAll, invA[nt], (jq * 2 + c) * 4);
+
+    for (int u = 0; u < A.units; ++u) {
+      const int stage = cstage;
+      if (!mbar_wait(full + stage, cphase)) {
+        if (lane == 0 && a.status) atomicOr(a.status, PKV_DEV_TIMEOUT);
+        return;
+      }
+      const int row = __shfl_sync(kAll, A.row, u);
+      const int kbase = A.key0 + u * kSubKeys;
+      const int v = row >= 0 ? min(kSubKeys, A.key1 - kbase) : 0;
+      const int vis0 = A.L - nrows - kbase + 1;
+      const uint32_t kc = ring_addr + stage * Cfg::kCodeBytes;
+      const uint32_t vc = ring_addr + Cfg::kVc + stage * Cfg::kCodeBytes;
+      const uint32_t ks = ring_addr + Cfg::kKs + stage * Cfg::kScaleBytes;
+      const uint32_t vs = ring_addr + Cfg::kVs + stage * Cfg::kScaleBytes;
+
+      // S^T = K Q^T per scale group (integer codes, fp16 MMA)
+      float sg[NG][NT][4];
+#pragma unroll
+      for (int g = 0; g < NG; ++g)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) sg[g][nt][0] = sg[g][nt][1] = sg[g][nt][2] = sg[g][nt][3] = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < KT; ++kk) {
+        // chunk 2g + h of rows ka / kb: the swizzle XORs the chunk index
+        const uint32_t off = koff ^ (static_cast<uint32_t>(kk) << 4);
+        const uint32_t wa = lds32(kc + off);
+        const uint32_t wb = lds32(kc + off + 8 * (D == 128 ? 128 : 64));
+        uint32_t af[4];
+        codes_to_f16(wa, af[0], af[2]);
+        codes_to_f16(wb, af[1], af[3]);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) mma_f16_16816(sg[kk >> 1][nt], af, qA[nt][kk][0], qA[nt][kk][1]);
+      }
+      // group scales of keys ka and kb; V scales of the same keys, zero past the sub-tile's keys
+      float dka[NG], dkb[NG], dva[NG], dvb[NG];
+      {
+        uint32_t w[4];
+        if constexpr (NG == 4) {
+          const uint2 x0 = lds64(ks + ka * 8), x1 = lds64(ks + kb * 8);
+          const uint2 y0 = lds64(vs + ka * 8), y1 = lds64(vs + kb * 8);
+          w[0] = x0.x; w[1] = x0.y; w[2] = x1.x; w[3] = x1.y;
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            dka[g] = bf16_bits_to_float((w[g >> 1] >> (16 * (g & 1))) & 0xFFFFu);
+            dkb[g] = bf16_bits_to_float((w[2 + (g >> 1)] >> (16 * (g & 1))) & 0xFFFFu);
+          }
+          w[0] = y0.x; w[1] = y0.y; w[2] = y1.x; w[3] = y1.y;
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            dva[g] = ka < v ? bf16_bits_to_float((w[g >> 1] >> (16 * (g & 1))) & 0xFFFFu) : 0.f;
+            dvb[g] = kb < v ? bf16_bits_to_float((w[2 + (g >> 1)] >> (16 * (g & 1))) & 0xFFFFu) : 0.f;
+          }
+        } else {
+          const uint32_t x0 = lds32(ks + ka * 4), x1 = lds32(ks + kb * 4);
+          const uint32_t y0 = lds32(vs + ka * 4), y1 = lds32(vs + kb * 4);
+#pragma unroll
+          for (int g = 0; g < 2; ++g) {
+            dka[g] = bf16_bits_to_float((x0 >> (16 * g)) & 0xFFFFu);
+            dkb[g] = bf16_bits_to_float((x1 >> (16 * g)) & 0xFFFFu);
+            dva[g] = ka < v ? bf16_bits_to_float((y0 >> (16 * g)) & 0xFFFFu) : 0.f;
+            dvb[g] = kb < v ? bf16_bits_to_float((y1 >> (16 * g)) & 0xFFFFu) : 0.f;
+          }
+        }
+      }
+
+      // online softmax (keys ka, kb of columns 2 jq + c)
+      float x[NT][2][2], mx[NT][2];
+      bool need = false;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          float sa = 0.f, sb = 0.f;
+#pragma unroll
+          for (int g = 0; g < NG; ++g) {
+            sa = fmaf(dka[g], sg[g][nt][c], sa);
+            sb = fmaf(dkb[g], sg[g][nt][c + 2], sb);
+          }
+          const int vis = MULTI ? min(v, vis0 + static_cast<int>((colrow >> (8 * (nt * 2 + c))) & 0xFF)) : v;
+          x[nt][c][0] = ka < vis ? sa * sl2c[nt][c] : -INFINITY;
+          x[nt][c][1] = kb < vis ? sb * sl2c[nt][c] : -INFINITY;
+          float t = fmaxf(x[nt][c][0], x[nt][c][1]);
+          t = fmaxf(t, __shfl_xor_sync(kAll, t, 4));
+          t = fmaxf(t, __shfl_xor_sync(kAll, t, 8));
+          t = fmaxf(t, __shfl_xor_sync(kAll, t, 16));
+          mx[nt][c] = t;
+          need |= t > m[nt][c] + kRescaleQ8;
+        }
+      if (__any_sync(kAll, need)) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int c = 0; c < 2; ++c)
+            if (mx[nt][c] > m[nt][c] + kRescaleQ8) {
+              const float corr = exp2f(m[nt][c] - mx[nt][c]);
+              m[nt][c] = mx[nt][c];
+              l[nt][c] *= corr;
+#pragma unroll
+              for (int mt = 0; mt < KT; ++mt) {
+                acc[nt][mt][c] *= corr;
+                acc[nt][mt][c + 2] *= corr;
+              }
+            }
+      }
+      // P (fp32), then one scaled bf16 copy of P^T per V scale group
+      uint32_t pf[NG][NT][2];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const float m0 = m[nt][0] == -INFINITY ? 0.f : m[nt][0];
+        const float m1 = m[nt][1] == -INFINITY ? 0.f : m[nt][1];
+        const float p00 = exp2f(x[nt][0][0] - m0), p01 = exp2f(x[nt][0][1] - m0);  // column c=0: keys ka, kb
+        const float p10 = exp2f(x[nt][1][0] - m1), p11 = exp2f(x[nt][1][1] - m1);  // column c=1
+        l[nt][0] += p00 + p01;
+        l[nt][1] += p10 + p11;
+#pragma unroll
+        for (int g = 0; g < NG; ++g) {
+          pf[g][nt][0] = movmatrix_trans(pack_bf16x2(p00 * dva[g], p10 * dva[g]));
+          pf[g][nt][1] = movmatrix_trans(pack_bf16x2(p01 * dvb[g], p11 * dvb[g]));
+        }
+      }
+
+      // O^T += V^T P'^T (integer codes, bf16 MMA). m-tile 2g + h, rows r / r + 8:
+      // head_dim 32 g + 4 r + 2 h (+ 1); keys k0, k0 + 1 (+ 8).
+#pragma unroll
+      for (int g = 0; g < NG; ++g) {
+        const int col = 32 * g + 4 * r;
+        const uint32_t u0 = lds32(vc + code_off<D>(k0, col)) ^ 0x80808080u;
+        const uint32_t u1 = lds32(vc + code_off<D>(k0 + 1, col)) ^ 0x80808080u;
+        const uint32_t u8 = lds32(vc + code_off<D>(k0 + 8, col)) ^ 0x80808080u;
+        const uint32_t u9 = lds32(vc + code_off<D>(k0 + 9, col)) ^ 0x80808080u;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t af[4];
+          af[0] = codes_to_bf16_pair(u0, u1, 2 * h);
+          af[1] = codes_to_bf16_pair(u0, u1, 2 * h + 1);
+          af[2] = codes_to_bf16_pair(u8, u9, 2 * h);
+          af[3] = codes_to_bf16_pair(u8, u9, 2 * h + 1);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(acc[nt][2 * g + h], af, pf[g][nt][0], pf[g][nt][1]);
+        }
+      }
+      __syncwarp();  // every read of this stage is consumed before the ring refills it
+      ++C;
+      if (++cstage == NST) {
+        cstage = 0;
+        cphase ^= 1u;
+      }
+      issue_next();
+    }
+
+    // ---- finish task A: the output row, or this span's partial ----
+    if (A.ok) {
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          float t = l[nt][c];
+          t += __shfl_xor_sync(kAll, t, 4);
+          t += __shfl_xor_sync(kAll, t, 8);
+          t += __shfl_xor_sync(kAll, t, 16);
+          l[nt][c] = t;
+        }
+      const int hbase = A.g * G;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const int col = nt * 8 + jq * 2 + c;
+          if (col < nrows * G) {
+            const int i = MULTI ? col / G : 0, hh = MULTI ? col % G : col;
+            if (A.pbase < 0) {
+              __nv_bfloat16 *out = reinterpret_cast<__nv_bfloat16 *>(a.out) +
+                                   ((static_cast<size_t>(A.row0) + i) * a.num_q_heads + hbase + hh) * D + 4 * r;
+              const float inv = 1.f / l[nt][c];
+#pragma unroll
+              for (int g = 0; g < NG; ++g) {
+                uint2 pk;
+                pk.x = pack_bf16x2(acc[nt][2 * g][c] * inv, acc[nt][2 * g][c + 2] * inv);
+                pk.y = pack_bf16x2(acc[nt][2 * g + 1][c] * inv, acc[nt][2 * g + 1][c + 2] * inv);
+                *reinterpret_cast<uint2 *>(out + 32 * g) = pk;
+              }
+            } else {
+              const size_t pi = (static_cast<size_t>(A.pbase + A.span * nrows + i) * a.num_q_heads + hbase + hh);
+              float *pacc = a.partial_acc + pi * D + 4 * r;
+#pragma unroll
+              for (int g = 0; g < NG; ++g)
+                *reinterpret_cast<float4 *>(pacc + 32 * g) =
+                    make_float4(acc[nt][2 * g][c], acc[nt][2 * g][c + 2], acc[nt][2 * g + 1][c],
+                                acc[nt][2 * g + 1][c + 2]);
+              if (r == 0) {
+                a.partial_ml[pi * 2] = m[nt][c];
+                a.partial_ml[pi * 2 + 1] = l[nt][c];
+              }
+            }
+          }
+        }
+    }
+
+    // ---- advance: B becomes current, the task after it is expanded ----
+    const int next_t = B.t >= 0 ? B.t + stride : num_tasks;
+    A = B;
+    pa = pb;
+    pb = 0;
+    if (A.t >= 0) {
+      if (!A.finalized) finalize(A, a, lane, 8 * NT, kMaxRows);
+      if (qB_loaded) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          invA[nt] = invB[nt];
+#pragma unroll
+          for (int kk = 0; kk < KT; ++kk) {
+            qA[nt][kk][0] = qB[nt][kk][0];
+            qA[nt][kk][1] = qB[nt][kk][1];
+          }
+        }
+      } else if (A.ok) {
+        load_q_q8<D, NT, MULTI>(qA, invA, A, a, lane);
+      }
+    }
+    qB_loaded = false;
+    expand(B, next_t < num_tasks ? next_t : -1, rawC, a, lane);
+    if (next_t + stride < num_tasks) rawC = load_item(items, next_t + stride, hkv);
+    while (P - C < NST && issue_next()) {
+    }
+  }
+}
+
+template <int D, int NT, bool MULTI>
+cudaError_t launch_decode_q8_t(const StepArgs &a, const CUtensorMap &tk, const CUtensorMap &tv,
+                               const void *k_scales, const void *v_scales, int32_t num_items, const int32_t *items,
+                               cudaStream_t stream) {
+  constexpr int smem = Q8Cfg<D>::kSmem;
+  static uint64_t configured = 0;  // one bit per device
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(configured & bit)) {
+    cudaError_t e =
+        cudaFuncSetAttribute(decode_q8_kernel<D, NT, MULTI>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    configured |= bit;
+  }
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = 148;
+  const int64_t tasks = static_cast<int64_t>(num_items) * a.num_kv_heads;
+  const int grid = static_cast<int>(tasks < sms ? tasks : sms);
+  return launch_pdl(decode_q8_kernel<D, NT, MULTI>, dim3(grid), dim3(kWarpsQ8 * 32), smem, stream, tk, tv, a,
+                    static_cast<const __nv_bfloat16 *>(k_scales), static_cast<const __nv_bfloat16 *>(v_scales),
+                    items, num_items);
+}
+
+}  // namespace
+
+cudaError_t launch_cache_write_q8(const void *k_new, const void *v_new, const int64_t *slot_mapping,
+                                  int64_t num_tokens, void *k_codes, void *k_scales, void *v_codes, void *v_scales,
+                                  int64_t num_blocks, int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
+                                  uint32_t *status, cudaStream_t stream) {
+  const int64_t rows = 2 * num_tokens * num_kv_heads;
+  int64_t blocks = (rows + 7) / 8;  // 8 warps per CTA, one row each
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  const dim3 grid(static_cast<unsigned>(blocks));
+  auto *kn = static_cast<const __nv_bfloat16 *>(k_new);
+  auto *vn = static_cast<const __nv_bfloat16 *>(v_new);
+  auto *kc = static_cast<int8_t *>(k_codes);
+  auto *vc = static_cast<int8_t *>(v_codes);
+  auto *ksc = static_cast<__nv_bfloat16 *>(k_scales);
+  auto *vsc = static_cast<__nv_bfloat16 *>(v_scales);
+  if (head_dim == 128)
+    return launch_pdl(cache_write_q8_kernel<128>, grid, dim3(256), 0, stream, kn, vn, slot_mapping, num_tokens, kc,
+                      ksc, vc, vsc, num_blocks * block_size, block_size, num_kv_heads, status);
+  return launch_pdl(cache_write_q8_kernel<64>, grid, dim3(256), 0, stream, kn, vn, slot_mapping, num_tokens, kc, ksc,
+                    vc, vsc, num_blocks * block_size, block_size, num_kv_heads, status);
+}
+
+cudaError_t launch_widen_q8(const StepArgs &a, const void *k_codes, const void *k_scales, const void *v_codes,
+                            const void *v_scales, void *k_out, void *v_out, int32_t *scratch_table,
+                            int64_t scratch_blocks, int32_t num_items, const int32_t *items, cudaStream_t stream) {
+  if (num_items <= 0) return cudaSuccess;
+  // about four CTAs per SM over all items; a CTA whose first block is past its item's end exits
+  const int per_item = (4 * 152 + num_items - 1) / num_items;
+  const dim3 grid(static_cast<unsigned>(num_items), static_cast<unsigned>(per_item < 1 ? 1 : per_item > 512 ? 512 : per_item));
+  auto *kc = static_cast<const int8_t *>(k_codes);
+  auto *vc = static_cast<const int8_t *>(v_codes);
+  auto *ksc = static_cast<const __nv_bfloat16 *>(k_scales);
+  auto *vsc = static_cast<const __nv_bfloat16 *>(v_scales);
+  auto *ko = static_cast<__nv_bfloat16 *>(k_out);
+  auto *vo = static_cast<__nv_bfloat16 *>(v_out);
+  if (a.head_dim == 128)
+    return launch_pdl(widen_q8_kernel<128>, grid, dim3(256), 0, stream, a, items, kc, ksc, vc, vsc, ko, vo,
+                      scratch_table, scratch_blocks);
+  return launch_pdl(widen_q8_kernel<64>, grid, dim3(256), 0, stream, a, items, kc, ksc, vc, vsc, ko, vo,
+                    scratch_table, scratch_blocks);
+}
+
+cudaError_t launch_decode_q8(const StepArgs &a, const CUtensorMap &tk, const CUtensorMap &tv, const void *k_scales,
+                             const void *v_scales, int32_t num_items, const int32_t *items, cudaStream_t stream) {
+  if (num_items <= 0) return cudaSuccess;
+  const bool multi = a.decode_rows_max > 1;
+  const bool wide = a.group * (multi ? a.decode_rows_max : 1) > 8;
+  const int v = (a.head_dim == 128 ? 4 : 0) + (wide ? 2 : 0) + (multi ? 1 : 0);
+  switch (v) {
+    case 0: return launch_decode_q8_t<64, 1, false>(a, tk, tv, k_scales, v_scales, num_items, items, stream);
+    case 1: return launch_decode_q8_t<64, 1, true>(a, tk, tv, k_scales, v_scales, num_items, items, stream);
+    case 2: return launch_decode_q8_t<64, 2, false>(a, tk, tv, k_scales, v_scales, num_items, items, stream);
+    case 3: return launch_decode_q8_t<64, 2, true>(a, tk, tv, k_scales, v_scales, num_items, items, stream);
+    case 4: return launch_decode_q8_t<128, 1, false>(a, tk, tv, k_scales, v_scales, num_items, items, stream);
+    case 5: return launch_decode_q8_t<128, 1, true>(a, tk, tv, k_scales, v_scales, num_items, items, stream);
+    case 6: return launch_decode_q8_t<128, 2, false>(a, tk, tv, k_scales, v_scales, num_items, items, stream);
+    default: return launch_decode_q8_t<128, 2, true>(a, tk, tv, k_scales, v_scales, num_items, items, stream);
+  }
+}
+
+}  // namespace pkv

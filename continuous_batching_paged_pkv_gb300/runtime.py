@@ -56,6 +56,19 @@ def empty_pool(num_blocks, num_kv_heads, block_size, head_dim, device):
     return k, v
 
 
+def empty_pool_q8(num_blocks, num_kv_heads, block_size, head_dim, device):
+    """(k_codes, k_scales, v_codes, v_scales) of an 8-bit pool; scales of rows never written are NaN."""
+    import torch
+
+    codes = [torch.full((num_blocks, num_kv_heads, block_size, head_dim), -128, dtype=torch.int8, device=device)
+             for _ in range(2)]
+    scales = [torch.empty((num_blocks, num_kv_heads, block_size, head_dim // 32), dtype=torch.bfloat16,
+                          device=device) for _ in range(2)]
+    for t in scales:
+        t.view(torch.int16).fill_(SENTINEL_BITS)
+    return codes[0], scales[0], codes[1], scales[1]
+
+
 @dataclass
 class DeviceStep:
     w: object                 # the step description (workloads.StepInputs)
@@ -76,21 +89,34 @@ class DeviceStep:
     workspace: object
     out: object
     status: object
+    kv: str = "bf16"          # pool format: "bf16", or "q8" (k_pool/v_pool hold the codes)
+    k_scales: object = None
+    v_scales: object = None
 
     @property
     def scale(self) -> float:
         return self.w.scale
 
 
-def prepare(w, device="cuda", *, pools=None) -> DeviceStep:
-    """Build the pool state before the step and upload the step's inputs."""
+def prepare(w, device="cuda", *, pools=None, kv: str = "bf16") -> DeviceStep:
+    """Build the pool state before the step and upload the step's inputs.
+
+    ``kv="q8"`` keeps the pool in the 8-bit block-scaled format (history
+    written through ``pkv_cache_write_q8``)."""
     import torch
 
     pool = B.Pool(w.num_blocks, w.block_size, w.max_slots, w.max_blocks_per_slot)
     for slot in sorted(w.blocks):
         pool.admit_blocks(slot, w.blocks[slot])
-    k_pool, v_pool = pools if pools is not None else empty_pool(
-        w.num_blocks, w.num_kv_heads, w.block_size, w.head_dim, device)
+    k_scales = v_scales = None
+    if kv == "q8":
+        k_pool, k_scales, v_pool, v_scales = pools if pools is not None else empty_pool_q8(
+            w.num_blocks, w.num_kv_heads, w.block_size, w.head_dim, device)
+    elif kv == "bf16":
+        k_pool, v_pool = pools if pools is not None else empty_pool(
+            w.num_blocks, w.num_kv_heads, w.block_size, w.head_dim, device)
+    else:
+        raise ValueError(f"unknown pool format {kv!r}")
     status = torch.zeros(1, dtype=torch.int32, device=device)
 
     # Cached history: every segment's positions before this step's rows.
@@ -99,16 +125,21 @@ def prepare(w, device="cuda", *, pools=None) -> DeviceStep:
     if len(hist.slot_mapping):
         hk = np.concatenate([w.hist_k[s.slot][: s.ctx - s.q_len] for s in w.segments])
         hv = np.concatenate([w.hist_v[s.slot][: s.ctx - s.q_len] for s in w.segments])
-        B.pkv_cache_write(_bf16_tensor(hk, device), _bf16_tensor(hv, device), _i64(hist.slot_mapping, device),
-                          k_pool, v_pool, device_status=status)
+        if kv == "q8":
+            B.pkv_cache_write_q8(_bf16_tensor(hk, device), _bf16_tensor(hv, device), _i64(hist.slot_mapping, device),
+                                 k_pool, k_scales, v_pool, v_scales, device_status=status)
+        else:
+            B.pkv_cache_write(_bf16_tensor(hk, device), _bf16_tensor(hv, device), _i64(hist.slot_mapping, device),
+                              k_pool, v_pool, device_status=status)
 
     low = pool.lower([(s.slot, s.q_len) for s in w.segments])
     work, info = B.pkv_plan_work(low.cu_seqlens_q, low.seq_slot, low.context_lens, max_slots=w.max_slots,
                                  max_blocks_per_slot=w.max_blocks_per_slot, block_size=w.block_size,
                                  num_q_heads=w.num_q_heads, num_kv_heads=w.num_kv_heads, head_dim=w.head_dim)
     ws = None
-    if info.workspace_bytes:
-        ws = torch.empty(int(info.workspace_bytes), dtype=torch.uint8, device=device)
+    ws_bytes = int(info.workspace_bytes_q8 if kv == "q8" else info.workspace_bytes)
+    if ws_bytes:
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device=device)
     out = torch.empty((w.total_q, w.num_q_heads, w.head_dim), dtype=torch.bfloat16, device=device)
     out.view(torch.int16).fill_(SENTINEL_BITS)
     return DeviceStep(
@@ -117,18 +148,27 @@ def prepare(w, device="cuda", *, pools=None) -> DeviceStep:
         slot_mapping=_i64(low.slot_mapping, device), cu_seqlens_q=_i32(low.cu_seqlens_q, device),
         seq_slot=_i32(low.seq_slot, device), context_lens=_i32(low.context_lens, device),
         block_tables=_i32(pool.block_tables(), device), work=_i32(work, device), info=info, workspace=ws,
-        out=out, status=status)
+        out=out, status=status, kv=kv, k_scales=k_scales, v_scales=v_scales)
 
 
 def run_cache_write(ds: DeviceStep, stream=None) -> None:
-    B.pkv_cache_write(ds.k_new, ds.v_new, ds.slot_mapping, ds.k_pool, ds.v_pool,
-                      device_status=ds.status, stream=stream)
+    if ds.kv == "q8":
+        B.pkv_cache_write_q8(ds.k_new, ds.v_new, ds.slot_mapping, ds.k_pool, ds.k_scales, ds.v_pool, ds.v_scales,
+                             device_status=ds.status, stream=stream)
+    else:
+        B.pkv_cache_write(ds.k_new, ds.v_new, ds.slot_mapping, ds.k_pool, ds.v_pool,
+                          device_status=ds.status, stream=stream)
 
 
 def run_attention(ds: DeviceStep, stream=None) -> None:
-    B.pkv_attention(ds.q, ds.cu_seqlens_q, ds.seq_slot, ds.context_lens, ds.block_tables, ds.k_pool,
-                    ds.v_pool, ds.work, ds.info, ds.out, ds.workspace, scale=ds.scale,
-                    device_status=ds.status, stream=stream)
+    if ds.kv == "q8":
+        B.pkv_attention_q8(ds.q, ds.cu_seqlens_q, ds.seq_slot, ds.context_lens, ds.block_tables, ds.k_pool,
+                           ds.k_scales, ds.v_pool, ds.v_scales, ds.work, ds.info, ds.out, ds.workspace,
+                           scale=ds.scale, device_status=ds.status, stream=stream)
+    else:
+        B.pkv_attention(ds.q, ds.cu_seqlens_q, ds.seq_slot, ds.context_lens, ds.block_tables, ds.k_pool,
+                        ds.v_pool, ds.work, ds.info, ds.out, ds.workspace, scale=ds.scale,
+                        device_status=ds.status, stream=stream)
 
 
 def chunk_only(ds: DeviceStep):

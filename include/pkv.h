@@ -200,7 +200,9 @@ pkv_status pkv_plan_lower(pkv_pool *pool, const pkv_segment *plan, int32_t num_s
  * partial of span s, row i is first + s * rows + i); prefill (segment, slot,
  * first query tile, tiles in the item: 1 or 2); merge, one per row of a
  * multi-span segment (segment, slot, spans | row << 16 | (rows - 1) << 24,
- * first partial of the row).
+ * first partial of the row); scratch, one per prompt-chunk segment
+ * (segment, slot, first scratch block, blocks = ceil(context / block_size)),
+ * used only by pkv_attention_q8.
  * ---------------------------------------------------------------------- */
 #define PKV_SPLIT_KEYS 256
 #define PKV_WORK_WORDS_PER_ITEM 4
@@ -213,6 +215,9 @@ typedef struct pkv_work_info {
     int64_t work_words;        /* int32 words of the item array: decode, prefill, then merge items */
     uint64_t workspace_bytes;  /* device workspace pkv_attention needs (may be 0) */
     int32_t decode_rows_max;   /* most rows in a segment of the decode path (0: none) */
+    int32_t num_scratch_items; /* (segment) items of the 8-bit pool's chunk path, one per chunk segment */
+    int64_t scratch_blocks;    /* bf16 scratch blocks those items widen the chunks' histories into */
+    uint64_t workspace_bytes_q8; /* device workspace pkv_attention_q8 needs (may be 0) */
 } pkv_work_info;
 
 /*
@@ -339,6 +344,61 @@ pkv_status pkv_attention_no_alloc(const void *q, const int32_t *cu_seqlens_q, in
                                   int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                                   float scale, const int32_t *work, const pkv_work_info *info,
                                   void *out, uint32_t *device_status, pkv_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * 8-bit block-scaled KV pool.
+ * [LB] §Qwen3.8-27B DFlash2 on the R9700 (vs llama.cpp) and §DeepSeek V4
+ * Flash on Strix Halo and two GPUs: the pages serve from 8-bit and 4-bit KV
+ * caches but do not define the formats. This library's 8-bit format: each
+ * pool row (token, kv head) is cut into groups of 32 consecutive values; a
+ * group keeps one power-of-two scale d -- the smallest power of two at or
+ * above amax / 127 (amax = max |x| over the group, the quotient in float32),
+ * at least 2^-126, 0 when amax is 0 -- stored as a bfloat16 (exact), and 32
+ * int8 codes round_half_even(x / d) clamped to [-127, 127]. A code stands
+ * for code * d, which is always a bfloat16 number.
+ *
+ *   k_codes, v_codes   int8 [num_blocks][num_kv_heads][block_size][head_dim]
+ *   k_scales, v_scales bf16 [num_blocks][num_kv_heads][block_size][head_dim / 32]
+ * A row costs head_dim + head_dim / 16 bytes instead of 2 * head_dim.
+ * ---------------------------------------------------------------------- */
+
+/*
+ * pkv_cache_write for an 8-bit pool: quantise each new row's key and value
+ * (bf16 [num_tokens][num_kv_heads][head_dim], device) into the pool row
+ * slot_mapping[t] (< 0: skip). Bit-exact with the format's definition. Same
+ * validation, device-status bits and stream behaviour as pkv_cache_write;
+ * all pool pointers 16-byte aligned.
+ */
+pkv_status pkv_cache_write_q8(const void *k_new, const void *v_new, const int64_t *slot_mapping,
+                              int64_t num_tokens, int8_t *k_codes, void *k_scales, int8_t *v_codes,
+                              void *v_scales, int64_t num_blocks, int32_t block_size,
+                              int32_t num_kv_heads, int32_t head_dim, uint32_t *device_status,
+                              pkv_stream_t stream);
+
+/*
+ * pkv_attention over an 8-bit pool: attention over the values the codes
+ * stand for (code * scale), with the same arguments, results and ordering
+ * rules as pkv_attention, except:
+ *   - the pool is the four arrays above;
+ *   - `workspace` must hold info->workspace_bytes_q8 bytes (256-byte
+ *     aligned): the span partials, then, when the step has prompt chunks, a
+ *     bf16 scratch pool of info->scratch_blocks blocks for K and for V and a
+ *     scratch block table [max_slots][max_blocks_per_slot]. The chunk
+ *     segments' histories are widened there (code * scale rounded to bf16)
+ *     before the tensor-core chunk kernel reads them; decode rows read the
+ *     codes directly.
+ * `info` must come from pkv_plan_work for the same shapes (its
+ * workspace_bytes_q8 is checked against them: PKV_ERR_INVALID_ARG otherwise).
+ */
+pkv_status pkv_attention_q8(const void *q, const int32_t *cu_seqlens_q, int32_t num_seqs,
+                            int64_t total_q, const int32_t *seq_slot, const int32_t *context_lens,
+                            const int32_t *block_tables, int32_t max_slots,
+                            int32_t max_blocks_per_slot, int32_t block_size, const int8_t *k_codes,
+                            const void *k_scales, const int8_t *v_codes, const void *v_scales,
+                            int64_t num_blocks, int32_t num_q_heads, int32_t num_kv_heads,
+                            int32_t head_dim, float scale, const int32_t *work,
+                            const pkv_work_info *info, void *out, void *workspace,
+                            uint64_t workspace_bytes, uint32_t *device_status, pkv_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * Host-staged step: a whole step from host memory in one call.

@@ -11,14 +11,18 @@ reading taken here is the plainest 8-bit block-scaled one:
 
 * each pool row (one token, one kv head, head_dim values) is cut into groups
   of 32 consecutive values;
-* a group stores one bfloat16 scale ``d`` and 32 signed 8-bit codes in
-  [-127, 127]; the value a code stands for is ``code * d``;
+* a group stores one power-of-two scale ``d`` (kept as a bfloat16, which
+  holds it exactly) and 32 signed 8-bit codes in [-127, 127]; the value a
+  code stands for is ``code * d``;
 * quantising a group of bfloat16 values ``x`` (all steps in float32, the
   precision the codes are decided in):
-    amax = max |x|;  d = amax / 127 rounded to bfloat16 (nearest even);
+    amax = max |x|;  t = amax / 127;  d = the smallest power of two >= t
+    (at least 2^-126; 0 when amax is 0);
     code = clamp(round_half_even(x / d), -127, 127), or 0 when d is 0.
-  A bfloat16 scale has float32's range, so every finite bfloat16 group
-  quantises with the same relative precision.
+  A power-of-two scale is the shared-exponent choice of the OCP microscaling
+  formats: x / d is exact, |x - code * d| <= d / 2, and every value a code
+  stands for is exactly a bfloat16 number (7 significant bits times a power
+  of two), so attention may widen codes to bfloat16 without rounding.
 
 Attention over such a pool is ordinary causal grouped-query attention over the
 dequantised values ``code * d`` (exact in double), computed here in float64
@@ -38,10 +42,13 @@ def _widen(bits) -> np.ndarray:
     return (b.astype(np.uint32) << 16).view(np.float32)
 
 
-def _round_bf16(x) -> np.ndarray:
-    """float32 -> bfloat16 bits, round to nearest even (finite inputs)."""
-    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
-    return ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+def _pow2_ceil(t) -> np.ndarray:
+    """Smallest power of two >= t (float32 t >= 0), at least 2^-126; 0 for t == 0. Float32 bits."""
+    b = np.ascontiguousarray(t, dtype=np.float32).view(np.uint32)
+    exp_bits = b & np.uint32(0x7F800000)
+    up = np.where((b & np.uint32(0x007FFFFF)) == 0, b, exp_bits + np.uint32(0x00800000))
+    up = np.where(exp_bits == 0, np.uint32(0x00800000), up)  # below 2^-126
+    return np.where(b == 0, np.uint32(0), up).astype(np.uint32)
 
 
 def quantize(x_bits):
@@ -52,7 +59,8 @@ def quantize(x_bits):
         raise ValueError(f"head_dim {d_len} is not a multiple of {GROUP}")
     g = x.reshape(*x.shape[:-1], d_len // GROUP, GROUP)
     amax = np.abs(g).max(axis=-1)
-    d_bits = _round_bf16((amax / np.float32(CODE_MAX)).astype(np.float32))
+    d32 = _pow2_ceil((amax / np.float32(CODE_MAX)).astype(np.float32))
+    d_bits = (d32 >> 16).astype(np.uint16)  # a power of two: its bfloat16 is exact
     df = _widen(d_bits)[..., None]
     safe = np.where(df > 0, df, np.float32(1))
     r = np.where(df > 0, g / safe, np.float32(0)).astype(np.float32)

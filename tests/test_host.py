@@ -174,8 +174,10 @@ def test_work_list_items():
     # run as 8 pairs at head_dim 128
     assert (info.num_decode_items, info.num_prefill_items, info.num_combine_items) == (6, 8, 2)
     items = work.reshape(-1, 4)
-    assert len(items) == 16
-    dec, pre, comb = items[:6], items[6:14], items[14:]
+    assert len(items) == 17 and info.num_scratch_items == 1
+    dec, pre, comb, scr = items[:6], items[6:14], items[14:16], items[16:]
+    # the chunk's history (1536 keys) as 96 scratch blocks for the 8-bit pool's chunk path
+    assert scr.tolist() == [[0, 3, 0, 96]] and info.scratch_blocks == 96
     assert [list(c) for c in comb] == [[1, 1, 3, 0], [2, 6, 2, 3]]  # (seg, slot, spans, partial base)
     assert sorted(map(tuple, dec[:, :3].tolist())) == [(1, 1, 0), (1, 1, 1), (1, 1, 2), (2, 6, 0), (2, 6, 1),
                                                         (3, 2, 0)]
@@ -191,6 +193,7 @@ def test_work_list_items():
     assert pre[0, 2] == 14  # the pair that sees the most keys first
     a256 = lambda x: (x + 255) // 256 * 256
     assert info.workspace_bytes == a256(5 * 32 * 128 * 4) + a256(5 * 32 * 2 * 4)
+    assert info.workspace_bytes_q8 == info.workspace_bytes + 2 * a256(96 * 8 * 16 * 128 * 2) + a256(8 * 128 * 4)
 
 
 @pytest.mark.parametrize("cu,slots,ctx_pairs,err", [
@@ -214,15 +217,15 @@ def test_work_list_tile_pairs():
     ctx[[0, 1]] = [100, 90]
     # group 4: 32 rows per tile; 80 and 70 rows are 3 tiles each: a pair and a single
     work, info = _work([0, 80, 150], [0, 1], ctx)
-    pre = work.reshape(-1, 4)
-    assert info.num_prefill_items == 4
+    pre = work.reshape(-1, 4)[:info.num_prefill_items]
+    assert info.num_prefill_items == 4 and info.num_scratch_items == 2 and info.scratch_blocks == 7 + 6
     by_seg = {}
     for seg, slot, t, c in pre.tolist():
         by_seg.setdefault(seg, []).append((t, c))
     assert sorted(by_seg[0]) == [(0, 2), (2, 1)]          # 80 rows: 3 tiles
     assert sorted(by_seg[1]) == [(0, 2), (2, 1)]          # 70 rows: 3 tiles
     work64, info64 = _work([0, 80, 150], [0, 1], ctx, head_dim=64)
-    assert info64.num_prefill_items == 6 and (work64.reshape(-1, 4)[:, 3] == 1).all()
+    assert info64.num_prefill_items == 6 and (work64.reshape(-1, 4)[:6, 3] == 1).all()
 
 
 def test_work_list_verify_rows():
@@ -233,9 +236,10 @@ def test_work_list_verify_rows():
     # group 4: 3 rows over 3 spans, 4 rows in one span, 5 rows (a chunk)
     work, info = _work([0, 3, 7, 12], [2, 5, 7], ctx)
     assert (info.num_decode_items, info.num_prefill_items, info.num_combine_items) == (4, 1, 3)
-    assert info.decode_rows_max == 4 and info.num_partials == 9
+    assert info.decode_rows_max == 4 and info.num_partials == 9 and info.num_scratch_items == 1
     items = work.reshape(-1, 4)
-    dec, pre, comb = items[:4], items[4:5], items[5:]
+    dec, pre, comb = items[:4], items[4:5], items[5:8]
+    assert items[8:].tolist() == [[2, 7, 0, 3]]
     assert sorted(map(tuple, dec.tolist())) == [(0, 2, 0, 0), (0, 2, 1, 0), (0, 2, 2, 0), (1, 5, 0, -1)]
     assert pre.tolist() == [[2, 7, 0, 1]]
     # spans | row << 16 | (rows - 1) << 24, and the row's entry for span 0 (span s: + s * rows)

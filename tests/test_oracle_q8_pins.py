@@ -1,11 +1,13 @@
 """Pins for the 8-bit block-scaled KV oracle (``oracle.kvquant``).
 
 The format is this library's reading (the pages run 8-bit and 4-bit KV caches
-without defining them): groups of 32 values, one bfloat16 scale amax / 127,
-codes rounded half to even into [-127, 127]. The pins tie the oracle to facts that
-hold independently of its code:
+without defining them): groups of 32 values, one power-of-two scale (the
+smallest at or above amax / 127), codes rounded half to even into [-127, 127].
+The pins tie the oracle to facts that hold independently of its code:
 
-* the error bound of round-to-nearest: |x - code * d| <= d / 2;
+* the error bound of round-to-nearest: |x - code * d| <= d / 2, with d a power
+  of two in [amax / 127, 2 amax / 127);
+* every dequantised value is exactly a bfloat16 number;
 * exact reconstruction of groups that are integer multiples of a power of two
   with one value at +-127 of them;
 * the half-way cases, which must round to even;
@@ -38,9 +40,16 @@ def test_error_bound_and_code_range():
     assert codes.dtype == np.int8 and sb.shape == (64, 4, 4)
     assert codes.min() >= -127 and codes.max() <= 127
     err = np.abs(xf.reshape(64, 4, 4, 32) - codes.reshape(64, 4, 4, 32) * d[..., None])
-    assert np.all(err <= d[..., None] * (0.5 + 1e-5))
-    # the largest magnitude of every group lands on +-127
-    assert np.all(np.abs(codes.reshape(64, 4, 4, 32)).max(axis=-1) == 127)
+    assert np.all(err <= d[..., None] / 2)
+    # d is a power of two between amax / 127 and twice that, so the largest code is in [64, 127]
+    amax = np.abs(xf.reshape(64, 4, 4, 32)).max(axis=-1)
+    assert np.all(np.frexp(d)[0] == 0.5)
+    assert np.all((d >= amax / 127) & (d < 2 * amax / 127 * (1 + 1e-6)))
+    top = np.abs(codes.reshape(64, 4, 4, 32)).max(axis=-1)
+    assert np.all((top >= 64) & (top <= 127))
+    # each dequantised value is a bfloat16 number: widening to bf16 loses nothing
+    deq = KQ.dequantize(codes, sb).astype(np.float32)
+    assert np.array_equal(W.bf16_bits_to_f32(W.f32_to_bf16_bits(deq)), deq)
 
 
 @pytest.mark.parametrize("e", [-120, -24, -7, 0, 5, 100])
@@ -75,9 +84,10 @@ def test_zero_group_and_range_ends():
     for r in (1, 2, 3):
         xf = W.bf16_bits_to_f32(_bits(x[r, :32])).astype(np.float64)
         d = float(W.bf16_bits_to_f32(sb[r, :1])[0])
+        assert np.frexp(d)[0] == 0.5 and d >= 2.0 ** -126
         if r < 3:
-            assert codes[r, 0] == -127 and codes[r, 31] == 127
-        assert np.all(np.abs(xf - codes[r, :32] * d) <= d * (0.5 + 1e-5))
+            assert codes[r, 0] == -codes[r, 31] and 64 <= codes[r, 31] <= 127
+        assert np.all(np.abs(xf - codes[r, :32] * d) <= d / 2)
 
 
 def _exact_step(rng, shapes, hq, hkv, d, e=-6):
