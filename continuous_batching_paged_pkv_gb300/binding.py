@@ -60,7 +60,7 @@ class PoolStats(ctypes.Structure):
     _fields_ = [("num_blocks", ctypes.c_int64), ("block_size", ctypes.c_int32),
                 ("max_slots", ctypes.c_int32), ("free_blocks", ctypes.c_int64),
                 ("owned_blocks", ctypes.c_int64), ("live_slots", ctypes.c_int32),
-                ("live_tokens", ctypes.c_int64)]
+                ("live_tokens", ctypes.c_int64), ("shared_blocks", ctypes.c_int64)]
 
 
 class Segment(ctypes.Structure):
@@ -90,6 +90,11 @@ def _lib():
             "pkv_pool_slot_blocks": ([p, i32], i32),
             "pkv_pool_get_stats": ([p, ctypes.POINTER(PoolStats)], ctypes.c_int),
             "pkv_pool_copy_block_tables": ([p, p, i64], ctypes.c_int),
+            "pkv_pool_adopt": ([p, i32, i32, i64, i64], ctypes.c_int),
+            "pkv_pool_block_refs": ([p, i32], i32),
+            "pkv_pool_take_copies": ([p, p, i64, ctypes.POINTER(ctypes.c_int64)], ctypes.c_int),
+            "pkv_copy_blocks": ([p, i64, ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(ctypes.c_int64), i32, i64,
+                                 p, p], ctypes.c_int),
             "pkv_plan_lower": ([p, p, i32, p, p, p, p, i64, ctypes.POINTER(ctypes.c_int64)], ctypes.c_int),
             "pkv_plan_work": ([p, i32, p, p, i32, i32, i32, i32, i32, i32, p, i64, ctypes.POINTER(WorkInfo)],
                               ctypes.c_int),
@@ -190,6 +195,23 @@ class Pool:
 
     def release(self, slot: int) -> None:
         _check(_lib().pkv_pool_release(self._h, slot), "pkv_pool_release")
+
+    def adopt(self, slot: int, donor_slot: int, num_tokens: int, reserve_tokens: int = 0) -> int:
+        """``pkv_pool_adopt``; returns the status code (PKV_ERR_NO_BLOCKS is an answer, not an error)."""
+        return _lib().pkv_pool_adopt(self._h, slot, donor_slot, num_tokens, reserve_tokens)
+
+    def block_refs(self, block: int) -> int:
+        return _lib().pkv_pool_block_refs(self._h, block)
+
+    def take_copies(self) -> np.ndarray:
+        """Pending copy-on-write copies as an int32 ``[n, 2]`` array of (source, destination) blocks."""
+        n = ctypes.c_int64(0)
+        rc = _lib().pkv_pool_take_copies(self._h, None, 0, ctypes.byref(n))
+        if rc == PKV_OK and n.value == 0:
+            return np.zeros((0, 2), np.int32)
+        out = np.empty((n.value, 2), np.int32)
+        _check(_lib().pkv_pool_take_copies(self._h, _np_ptr(out), n.value, ctypes.byref(n)), "pkv_pool_take_copies")
+        return out
 
     def slot_length(self, slot: int) -> int:
         return _lib().pkv_pool_slot_length(self._h, slot)
@@ -344,6 +366,25 @@ def pkv_attention_q8(q, cu_seqlens_q, seq_slot, context_lens, block_tables, k_co
                                    q.shape[1], hkv, d, float(scale), _t_ptr(work), ctypes.byref(info), _t_ptr(out),
                                    _t_ptr(workspace), ws_bytes, _t_ptr(device_status), _stream(stream)),
            "pkv_attention_q8")
+
+
+def pkv_copy_blocks(pairs, arrays, *, device_status=None, stream=None) -> None:
+    """Copy whole blocks (source, destination) in every pool array of ``arrays``.
+
+    ``pairs``: int32 device tensor ``[n, 2]``; ``arrays``: device tensors whose
+    first dimension is the block (``[num_blocks, ...]``), all with the same
+    number of blocks (a bf16 pool's K and V, or an 8-bit pool's four arrays)."""
+    _need(pairs, "torch.int32", "pairs")
+    if not arrays or len(arrays) > 4:
+        raise ValueError("pkv_copy_blocks takes one to four pool arrays")
+    nb = arrays[0].shape[0]
+    for t in arrays:
+        if not t.is_cuda or not t.is_contiguous() or t.shape[0] != nb:
+            raise ValueError("pool arrays must be contiguous CUDA tensors with the same number of blocks")
+    ptrs = (ctypes.c_void_p * len(arrays))(*[t.data_ptr() for t in arrays])
+    sizes = (ctypes.c_int64 * len(arrays))(*[t[0].numel() * t.element_size() for t in arrays])
+    _check(_lib().pkv_copy_blocks(_t_ptr(pairs), pairs.shape[0], ptrs, sizes, len(arrays), nb,
+                                  _t_ptr(device_status), _stream(stream)), "pkv_copy_blocks")
 
 
 def pkv_check_device_status(device_status, stream=None) -> int:

@@ -228,6 +228,21 @@ pkv_status pkv_attention(const void *q, const int32_t *cu_seqlens_q, int32_t num
   return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
+pkv_status pkv_copy_blocks(const int32_t *pairs, int64_t num_pairs, void *const *arrays,
+                           const int64_t *block_bytes, int32_t num_arrays, int64_t num_blocks,
+                           uint32_t *device_status, pkv_stream_t stream) {
+  if (num_pairs < 0 || num_arrays < 1 || num_arrays > 4 || num_blocks <= 0 || !arrays || !block_bytes)
+    return PKV_ERR_INVALID_ARG;
+  if (num_pairs == 0) return PKV_OK;
+  if (!pairs || !aligned(pairs, 8)) return PKV_ERR_INVALID_ARG;
+  for (int32_t a = 0; a < num_arrays; ++a)
+    if (!arrays[a] || !aligned(arrays[a], 16) || block_bytes[a] <= 0 || block_bytes[a] % 16 != 0)
+      return PKV_ERR_INVALID_ARG;
+  cudaError_t e = pkv::launch_copy_blocks(pairs, num_pairs, arrays, block_bytes, num_arrays, num_blocks,
+                                          device_status, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
 pkv_status pkv_cache_write_q8(const void *k_new, const void *v_new, const int64_t *slot_mapping,
                               int64_t num_tokens, int8_t *k_codes, void *k_scales, int8_t *v_codes, void *v_scales,
                               int64_t num_blocks, int32_t block_size, int32_t num_kv_heads, int32_t head_dim,

@@ -53,7 +53,57 @@ __global__ void __launch_bounds__(256) cache_write_kernel(
   }
 }
 
+// Copy-on-write: whole blocks, source -> destination, in up to four pool
+// arrays at once (mlxcel manual, "Continuous batching", §Paged KV cache and
+// prefix sharing: a shared block branches by copy when a sequence's contents
+// diverge from it). A block is contiguous in every pool array ([block][...]),
+// so one block is block_bytes[a] / 16 consecutive 16-byte vectors.
+struct CopyArrays {
+  uint4 *base[4];
+  int64_t vecs[4];  // 16-byte vectors per block
+  int32_t count;
+};
+
+__global__ void __launch_bounds__(256) copy_blocks_kernel(const int32_t *__restrict__ pairs, int64_t num_pairs,
+                                                          const CopyArrays arrays, int64_t num_blocks,
+                                                          uint32_t *__restrict__ status) {
+  grid_dependency_wait();  // the pairs and the source blocks come from earlier work
+  launch_dependents();
+  for (int64_t pi = blockIdx.y; pi < num_pairs; pi += gridDim.y) {
+    const int32_t src = __ldg(pairs + 2 * pi), dst = __ldg(pairs + 2 * pi + 1);
+    if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks || src == dst) {
+      if (status && threadIdx.x == 0 && blockIdx.x == 0) atomicOr(status, PKV_DEV_BAD_BLOCK);
+      continue;
+    }
+    for (int a = 0; a < arrays.count; ++a) {
+      const int64_t n = arrays.vecs[a];
+      const uint4 *s = arrays.base[a] + src * n;
+      uint4 *d = arrays.base[a] + dst * n;
+      for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+           i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+        d[i] = __ldg(s + i);
+    }
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_copy_blocks(const int32_t *pairs, int64_t num_pairs, void *const *arrays,
+                               const int64_t *block_bytes, int32_t num_arrays, int64_t num_blocks, uint32_t *status,
+                               cudaStream_t stream) {
+  CopyArrays ca{};
+  ca.count = num_arrays;
+  int64_t most = 0;
+  for (int a = 0; a < num_arrays; ++a) {
+    ca.base[a] = static_cast<uint4 *>(arrays[a]);
+    ca.vecs[a] = block_bytes[a] / 16;
+    most = ca.vecs[a] > most ? ca.vecs[a] : most;
+  }
+  const int64_t x = (most + 255) / 256;
+  const int64_t y = num_pairs < 4096 ? num_pairs : 4096;
+  return launch_pdl(copy_blocks_kernel, dim3(static_cast<unsigned>(x > 0 ? x : 1), static_cast<unsigned>(y)),
+                    dim3(256), 0, stream, pairs, num_pairs, ca, num_blocks, status);
+}
 
 cudaError_t launch_cache_write(const void *k_new, const void *v_new, const int64_t *slot_mapping,
                                int64_t num_tokens, void *k_pool, void *v_pool, int64_t num_blocks,

@@ -11,6 +11,11 @@
 //   §Packing unequal prompt chunks together -- one packed token axis with
 //     segment metadata;
 //   §Keeping track of each request -- stable slots and a row-to-slot map.
+// mlxcel manual, "Continuous batching", §Paged KV cache and prefix sharing --
+//   one refcounted, copy-on-write block pool: a request that shares a prompt
+//   prefix adopts the donor's blocks by reference instead of prefilling them,
+//   and a shared block is copied only when a sequence's contents diverge
+//   from it (its first append into that block).
 #include <algorithm>
 #include <cstring>
 #include <new>
@@ -33,6 +38,8 @@ struct pkv_pool {
   int32_t block_size = 0, max_slots = 0, max_blocks_per_slot = 0;
   std::vector<int32_t> free_stack;  // top = back()
   std::vector<uint8_t> on_free;     // per block: 1 while on the free stack
+  std::vector<int32_t> refs;        // per block: block tables holding it (0 while free)
+  std::vector<int32_t> copies;      // pending copy-on-write pairs (source, destination)
   struct Slot {
     bool live = false;
     int64_t length = 0;
@@ -74,6 +81,7 @@ pkv_pool *pkv_pool_create(int64_t num_blocks, int32_t block_size, int32_t max_sl
     p->max_slots = max_slots;
     p->max_blocks_per_slot = max_blocks_per_slot;
     p->on_free.assign(static_cast<size_t>(num_blocks), 0);
+    p->refs.assign(static_cast<size_t>(num_blocks), 0);
     p->slots.resize(static_cast<size_t>(max_slots));
     if (free_order) {
       if (free_order_len < 0 || free_order_len > num_blocks) {
@@ -120,6 +128,7 @@ pkv_status pkv_pool_admit(pkv_pool *p, int32_t slot, int64_t reserve_tokens) {
     int32_t b = p->free_stack.back();
     p->free_stack.pop_back();
     p->on_free[b] = 0;
+    p->refs[b] = 1;
     s.blocks.push_back(b);
   }
   s.live = true;
@@ -150,7 +159,10 @@ pkv_status pkv_pool_admit_blocks(pkv_pool *p, int32_t slot, const int32_t *block
     if (!take[b]) kept.push_back(b);
   p->free_stack.swap(kept);
   s.blocks.assign(blocks, blocks + num);
-  for (int32_t i = 0; i < num; ++i) p->on_free[blocks[i]] = 0;
+  for (int32_t i = 0; i < num; ++i) {
+    p->on_free[blocks[i]] = 0;
+    p->refs[blocks[i]] = 1;
+  }
   s.live = true;
   s.length = 0;
   return PKV_OK;
@@ -162,12 +174,55 @@ pkv_status pkv_pool_release(pkv_pool *p, int32_t slot) {
   pkv_pool::Slot &s = p->slots[slot];
   if (!s.live) return PKV_ERR_INVALID_ARG;
   for (auto it = s.blocks.rbegin(); it != s.blocks.rend(); ++it) {
+    if (--p->refs[*it] > 0) continue;  // still in another table
     p->free_stack.push_back(*it);
     p->on_free[*it] = 1;
   }
   s.blocks.clear();
   s.live = false;
   s.length = 0;
+  return PKV_OK;
+}
+
+pkv_status pkv_pool_adopt(pkv_pool *p, int32_t slot, int32_t donor_slot, int64_t num_tokens,
+                          int64_t reserve_tokens) {
+  if (!p || num_tokens < 0 || reserve_tokens < 0) return PKV_ERR_INVALID_ARG;
+  if (slot < 0 || slot >= p->max_slots || donor_slot < 0 || donor_slot >= p->max_slots) return PKV_ERR_OUT_OF_RANGE;
+  pkv_pool::Slot &s = p->slots[slot];
+  const pkv_pool::Slot &d = p->slots[donor_slot];
+  if (s.live || !d.live || slot == donor_slot || num_tokens > d.length) return PKV_ERR_INVALID_ARG;
+  const int64_t shared = ceil_div(num_tokens, p->block_size);
+  const int64_t total = std::max(shared, ceil_div(reserve_tokens, p->block_size));
+  if (total > p->max_blocks_per_slot) return PKV_ERR_OUT_OF_RANGE;
+  if (total - shared > static_cast<int64_t>(p->free_stack.size())) return PKV_ERR_NO_BLOCKS;
+  s.blocks.assign(d.blocks.begin(), d.blocks.begin() + shared);
+  s.blocks.reserve(static_cast<size_t>(p->max_blocks_per_slot));
+  for (int64_t i = 0; i < shared; ++i) ++p->refs[s.blocks[i]];
+  for (int64_t i = shared; i < total; ++i) {
+    int32_t b = p->free_stack.back();
+    p->free_stack.pop_back();
+    p->on_free[b] = 0;
+    p->refs[b] = 1;
+    s.blocks.push_back(b);
+  }
+  s.live = true;
+  s.length = num_tokens;
+  return PKV_OK;
+}
+
+int32_t pkv_pool_block_refs(const pkv_pool *p, int32_t block) {
+  if (!p || block < 0 || block >= p->num_blocks) return -1;
+  return p->refs[block];
+}
+
+pkv_status pkv_pool_take_copies(pkv_pool *p, int32_t *pairs, int64_t capacity, int64_t *num_pairs) {
+  if (!p || !num_pairs) return PKV_ERR_INVALID_ARG;
+  const int64_t n = static_cast<int64_t>(p->copies.size()) / 2;
+  *num_pairs = n;
+  if (n == 0) return PKV_OK;
+  if (!pairs || capacity < n) return PKV_ERR_WORKSPACE_TOO_SMALL;
+  std::copy(p->copies.begin(), p->copies.end(), pairs);
+  p->copies.clear();
   return PKV_OK;
 }
 
@@ -191,8 +246,11 @@ pkv_status pkv_pool_get_stats(const pkv_pool *p, pkv_pool_stats *st) {
   for (const auto &s : p->slots) {
     if (!s.live) continue;
     st->live_slots += 1;
-    st->owned_blocks += static_cast<int64_t>(s.blocks.size());
     st->live_tokens += s.length;
+  }
+  for (int32_t r : p->refs) {
+    st->owned_blocks += r > 0;
+    st->shared_blocks += r > 1;
   }
   return PKV_OK;
 }
@@ -224,10 +282,16 @@ pkv_status pkv_plan_lower(pkv_pool *p, const pkv_segment *plan, int32_t num_segm
     if (slot < 0 || slot >= p->max_slots) return PKV_ERR_OUT_OF_RANGE;
     if (n < 0 || !p->slots[slot].live || used[slot]) return PKV_ERR_INVALID_ARG;
     used[slot] = 1;
-    const int64_t len = p->slots[slot].length + n;
+    const pkv_pool::Slot &sl = p->slots[slot];
+    const int64_t len = sl.length + n;
     const int64_t blocks = ceil_div(len, p->block_size);
     if (blocks > p->max_blocks_per_slot || len > INT32_MAX) return PKV_ERR_OUT_OF_RANGE;
-    new_blocks += std::max<int64_t>(0, blocks - static_cast<int64_t>(p->slots[slot].blocks.size()));
+    new_blocks += std::max<int64_t>(0, blocks - static_cast<int64_t>(sl.blocks.size()));
+    // The first append lands in block length / block_size; if another table
+    // holds that block too, it is copied first (only that block can be shared:
+    // adoption shares whole blocks up to the adopted length).
+    const int64_t lb0 = sl.length / p->block_size;
+    if (n > 0 && lb0 < static_cast<int64_t>(sl.blocks.size()) && p->refs[sl.blocks[lb0]] > 1) ++new_blocks;
     rows += n;
   }
   if (rows > INT32_MAX) return PKV_ERR_OUT_OF_RANGE;
@@ -240,6 +304,18 @@ pkv_status pkv_plan_lower(pkv_pool *p, const pkv_segment *plan, int32_t num_segm
   for (int32_t i = 0; i < num_segments; ++i) {
     pkv_pool::Slot &s = p->slots[plan[i].slot];
     const int32_t n = plan[i].num_tokens;
+    const int64_t lb0 = s.length / p->block_size;
+    if (n > 0 && lb0 < static_cast<int64_t>(s.blocks.size()) && p->refs[s.blocks[lb0]] > 1) {
+      const int32_t old = s.blocks[lb0];
+      const int32_t b = p->free_stack.back();
+      p->free_stack.pop_back();
+      p->on_free[b] = 0;
+      p->refs[b] = 1;
+      --p->refs[old];
+      s.blocks[lb0] = b;
+      p->copies.push_back(old);
+      p->copies.push_back(b);
+    }
     for (int32_t j = 0; j < n; ++j) {
       const int64_t pos = s.length + j;
       const int64_t lb = pos / p->block_size;
@@ -247,6 +323,7 @@ pkv_status pkv_plan_lower(pkv_pool *p, const pkv_segment *plan, int32_t num_segm
         int32_t b = p->free_stack.back();
         p->free_stack.pop_back();
         p->on_free[b] = 0;
+        p->refs[b] = 1;
         s.blocks.push_back(b);
       }
       slot_mapping[t++] = static_cast<int64_t>(s.blocks[lb]) * p->block_size + pos % p->block_size;

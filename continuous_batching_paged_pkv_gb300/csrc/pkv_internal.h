@@ -38,6 +38,10 @@ cudaError_t launch_cache_write(const void *k_new, const void *v_new, const int64
                                int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
                                uint32_t *status, cudaStream_t stream);
 
+cudaError_t launch_copy_blocks(const int32_t *pairs, int64_t num_pairs, void *const *arrays,
+                               const int64_t *block_bytes, int32_t num_arrays, int64_t num_blocks, uint32_t *status,
+                               cudaStream_t stream);
+
 cudaError_t launch_decode(const StepArgs &a, const CUtensorMap &tmap_k, const CUtensorMap &tmap_v,
                           int32_t num_items, const int32_t *items, cudaStream_t stream);
 

@@ -82,6 +82,16 @@ int32_t pkv_version(void);
  *
  * The free list is a stack: released blocks go on top and are handed out
  * first. All calls are host-only, not thread-safe, and never touch a GPU.
+ *
+ * Blocks are reference counted ([MX] §Paged KV cache and prefix sharing: one
+ * refcount + copy-on-write block pool). A request whose prompt starts with
+ * another sequence's tokens adopts that sequence's blocks by reference
+ * (pkv_pool_adopt) instead of prefilling them; a block held by several
+ * tables is copied only when one of them first appends into it
+ * (pkv_plan_lower records the copy; pkv_pool_take_copies hands it to the
+ * caller, who runs pkv_copy_blocks before the step's cache write). A prompt
+ * prefix cache is a slot that adopts a finished request's prefix and is
+ * released to evict it.
  * ---------------------------------------------------------------------- */
 typedef struct pkv_pool pkv_pool;
 
@@ -90,9 +100,10 @@ typedef struct pkv_pool_stats {
     int32_t block_size;     /* tokens per block */
     int32_t max_slots;      /* sequence slots */
     int64_t free_blocks;    /* on the free stack */
-    int64_t owned_blocks;   /* held by live slots */
+    int64_t owned_blocks;   /* distinct blocks held by live slots (free + owned = available) */
     int32_t live_slots;     /* slots currently admitted */
     int64_t live_tokens;    /* sum of live slots' lengths */
+    int64_t shared_blocks;  /* blocks held by more than one slot */
 } pkv_pool_stats;
 
 /*
@@ -126,11 +137,40 @@ pkv_status pkv_pool_admit_blocks(pkv_pool *pool, int32_t slot, const int32_t *bl
                                  int32_t num);
 
 /*
- * Retire `slot`: its blocks go back on the free stack with the slot's first
- * block on top, and the slot becomes free. Other slots are untouched.
+ * Retire `slot`: each of its blocks loses one reference; blocks no other
+ * table holds go back on the free stack (the slot's first such block on
+ * top), and the slot becomes free. Other slots are untouched.
  * Errors: PKV_ERR_OUT_OF_RANGE, PKV_ERR_INVALID_ARG (slot not live).
  */
 pkv_status pkv_pool_release(pkv_pool *pool, int32_t slot);
+
+/*
+ * Admit `slot` by adopting the first `num_tokens` tokens of live slot
+ * `donor_slot`: the slot's table starts with the donor's first
+ * ceil(num_tokens / block_size) blocks (one more reference each) and its
+ * length is num_tokens, so those positions are never prefilled again. Fresh
+ * blocks are reserved after them, all or nothing, up to
+ * ceil(reserve_tokens / block_size) blocks in all. A partly filled last
+ * shared block is copied on the slot's first append (pkv_plan_lower).
+ * Errors: PKV_ERR_OUT_OF_RANGE, PKV_ERR_INVALID_ARG (slot live, donor not
+ * live, same slot, num_tokens beyond the donor's length), PKV_ERR_NO_BLOCKS.
+ */
+pkv_status pkv_pool_adopt(pkv_pool *pool, int32_t slot, int32_t donor_slot, int64_t num_tokens,
+                          int64_t reserve_tokens);
+
+/* Tables currently holding `block` (0 if free), or -1 for a bad block ID. */
+int32_t pkv_pool_block_refs(const pkv_pool *pool, int32_t block);
+
+/*
+ * Hand over the copy-on-write copies recorded by pkv_plan_lower since the
+ * last call: `pairs` receives 2 * num_pairs int32 (source block, destination
+ * block); the list is then cleared. With too little `capacity` (in pairs)
+ * nothing is cleared and *num_pairs says how many there are
+ * (PKV_ERR_WORKSPACE_TOO_SMALL). The copies must run (pkv_copy_blocks, same
+ * stream) before the step's cache write.
+ */
+pkv_status pkv_pool_take_copies(pkv_pool *pool, int32_t *pairs, int64_t capacity,
+                                int64_t *num_pairs);
 
 /* Current length (tokens appended) of a live slot, or -1. */
 int64_t pkv_pool_slot_length(const pkv_pool *pool, int32_t slot);
@@ -166,7 +206,9 @@ typedef struct pkv_segment {
  * in slot c of current length len: rows take positions len .. len+n-1, the
  * slot's length becomes len+n, and blocks are taken off the free stack when
  * a position opens a block the table does not have yet (all or nothing for
- * the whole plan). Host outputs:
+ * the whole plan). A segment whose first append falls in a block that
+ * another table also holds gets a fresh copy of that block first (recorded
+ * for pkv_pool_take_copies). Host outputs:
  *   cu_seqlens_q  int32 [num_segments+1]  row offsets of each segment
  *   seq_slot      int32 [num_segments]    row-to-slot map
  *   context_lens  int32 [max_slots]       every slot's length after the step (0 if free)
@@ -374,6 +416,21 @@ pkv_status pkv_cache_write_q8(const void *k_new, const void *v_new, const int64_
                               void *v_scales, int64_t num_blocks, int32_t block_size,
                               int32_t num_kv_heads, int32_t head_dim, uint32_t *device_status,
                               pkv_stream_t stream);
+
+/*
+ * Copy-on-write copies ([MX] §Paged KV cache and prefix sharing): for each
+ * (source, destination) pair of `pairs` (device, int32 [num_pairs][2], from
+ * pkv_pool_take_copies), copy the whole source block over the destination
+ * block in each of the `num_arrays` (1 to 4) pool arrays: arrays[a] (device,
+ * 16-byte aligned) holds num_blocks blocks of block_bytes[a] bytes (a
+ * multiple of 16) each -- a bf16 pool's K and V, or an 8-bit pool's codes
+ * and scales. `arrays` and `block_bytes` are host arrays. A pair naming a
+ * block outside the pool (or the same block twice) is skipped and sets
+ * PKV_DEV_BAD_BLOCK. Run before the step's cache write, on its stream.
+ */
+pkv_status pkv_copy_blocks(const int32_t *pairs, int64_t num_pairs, void *const *arrays,
+                           const int64_t *block_bytes, int32_t num_arrays, int64_t num_blocks,
+                           uint32_t *device_status, pkv_stream_t stream);
 
 /*
  * pkv_attention over an 8-bit pool: attention over the values the codes

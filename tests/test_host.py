@@ -92,6 +92,106 @@ def test_pool_each_block_owned_once():
         assert st.free_blocks + st.owned_blocks == 200
 
 
+# ---- prefix adoption and copy-on-write -------------------------------------------
+
+def _check_accounting(pool, total):
+    st = pool.stats()
+    assert st.free_blocks + st.owned_blocks == total
+    bt = pool.block_tables()
+    used = bt[bt >= 0]
+    for b in np.unique(used):
+        assert pool.block_refs(int(b)) == int((used == b).sum())
+
+
+def test_adopt_shares_blocks_and_copies_on_first_append():
+    """mlxcel manual, §Paged KV cache and prefix sharing: adopt by reference, copy on divergence."""
+    pool = B.Pool(64, 16, 4, 16)
+    assert pool.admit(0, 100) == B.PKV_OK
+    pool.lower([(0, 100)])
+    a_blocks = pool.block_tables()[0, :7].copy()
+    free0 = pool.stats().free_blocks
+    # B adopts 70 tokens (blocks 0..4, the last one partly filled) and reserves room for 90
+    assert pool.adopt(1, 0, 70, 90) == B.PKV_OK
+    assert pool.slot_length(1) == 70 and pool.slot_blocks(1) == 6
+    assert list(pool.block_tables()[1, :5]) == list(a_blocks[:5])
+    assert pool.stats().free_blocks == free0 - 1 and pool.stats().shared_blocks == 5
+    assert [pool.block_refs(int(b)) for b in a_blocks[:6]] == [2, 2, 2, 2, 2, 1]
+    _check_accounting(pool, 64)
+    # B's first append lands in shared block 4: it gets a copy, A keeps the original
+    low = pool.lower([(1, 20)])
+    cp = pool.take_copies()
+    b_blocks = pool.block_tables()[1]
+    assert cp.shape == (1, 2) and cp[0, 0] == a_blocks[4] and cp[0, 1] == b_blocks[4] != a_blocks[4]
+    assert pool.block_refs(int(a_blocks[4])) == 1 and pool.block_refs(int(b_blocks[4])) == 1
+    pos = np.arange(70, 90)
+    assert np.array_equal(low.slot_mapping, b_blocks[pos // 16].astype(np.int64) * 16 + pos % 16)
+    assert pool.take_copies().shape == (0, 2)  # handed over once
+    # later appends into B's own blocks copy nothing; A's appends never touch B's blocks
+    pool.lower([(1, 1), (0, 1)])
+    assert pool.take_copies().shape == (0, 2)
+    assert list(pool.block_tables()[0, :7]) == list(a_blocks)
+    _check_accounting(pool, 64)
+
+
+def test_adopt_on_a_block_boundary_never_copies():
+    pool = B.Pool(64, 16, 4, 16)
+    assert pool.admit(0, 100) == B.PKV_OK
+    pool.lower([(0, 100)])
+    assert pool.adopt(2, 0, 64, 0) == B.PKV_OK  # four full blocks, no reserve: the next block is grown
+    pool.lower([(2, 3)])
+    assert pool.take_copies().shape == (0, 2) and pool.slot_blocks(2) == 5
+    _check_accounting(pool, 64)
+
+
+def test_donor_append_into_a_shared_block_copies_for_the_donor():
+    pool = B.Pool(64, 16, 4, 16)
+    assert pool.admit(0, 100) == B.PKV_OK
+    pool.lower([(0, 100)])
+    a6 = int(pool.block_tables()[0, 6])
+    assert pool.adopt(1, 0, 100, 0) == B.PKV_OK  # shares all seven blocks, the last partly filled
+    pool.lower([(0, 1)])
+    cp = pool.take_copies()
+    assert cp.tolist() == [[a6, int(pool.block_tables()[0, 6])]] and pool.block_tables()[1, 6] == a6
+    _check_accounting(pool, 64)
+
+
+def test_release_keeps_shared_blocks_until_the_last_holder():
+    pool = B.Pool(32, 16, 4, 8)
+    assert pool.admit(0, 64) == B.PKV_OK
+    pool.lower([(0, 64)])
+    assert pool.adopt(1, 0, 64, 64) == B.PKV_OK  # a prefix-cache slot holding A's four blocks
+    shared = pool.block_tables()[0, :4].copy()
+    pool.release(0)
+    assert pool.stats().free_blocks == 28 and all(pool.block_refs(int(b)) == 1 for b in shared)
+    # a new request adopts from the cache slot, then the cache entry is evicted
+    assert pool.adopt(2, 1, 40, 80) == B.PKV_OK
+    pool.release(1)
+    assert pool.stats().free_blocks == 32 - 5  # slot 2: prefix blocks 0..2 and two fresh blocks
+    assert [pool.block_refs(int(b)) for b in shared] == [1, 1, 1, 0]
+    pool.release(2)
+    assert pool.stats().free_blocks == 32 and pool.stats().shared_blocks == 0
+    _check_accounting(pool, 32)
+
+
+def test_adopt_is_all_or_nothing_and_validated():
+    pool = B.Pool(8, 16, 4, 8)
+    assert pool.admit(0, 64) == B.PKV_OK
+    pool.lower([(0, 40)])
+    before = pool.block_tables().copy()
+    assert pool.adopt(1, 0, 40, 16 * 8) == B.PKV_ERR_NO_BLOCKS  # needs 5 fresh, 4 free
+    assert np.array_equal(pool.block_tables(), before) and pool.slot_length(1) == -1
+    assert [pool.block_refs(int(b)) for b in before[0, :4]] == [1, 1, 1, 1]
+    for args in ((1, 0, 41, 0), (1, 3, 10, 0), (0, 0, 10, 0)):  # past the donor, donor not live, slot live
+        assert pool.adopt(*args) != B.PKV_OK
+    # a lowering that needs a copy counts the copy's block: all or nothing
+    assert pool.adopt(1, 0, 40, 0) == B.PKV_OK
+    assert pool.admit(2, 64) == B.PKV_OK  # takes the last four free blocks
+    with pytest.raises(B.PkvError):
+        pool.lower([(1, 1)])
+    assert pool.slot_length(1) == 40 and pool.take_copies().shape == (0, 2)
+    _check_accounting(pool, 8)
+
+
 # ---- lowering ----------------------------------------------------------------
 
 def test_lowering_packing_example_from_the_page():
