@@ -20,12 +20,38 @@ chunked prompts, decode rows and retirements. Policy, from the pages:
   step that produced its last token and its slot and blocks return at once
   (Lucebox §One scheduler, model-specific execution).
 
+Budget policies (mlxcel manual, "Continuous batching", §Preemptive eviction,
+§Paged KV cache and prefix sharing, §Decode headroom under a tight budget),
+all off by default:
+
+* Admission watermark F (0 <= F <= 0.5): while a decode batch runs, a request
+  is admitted only if the free blocks minus F times the pool's blocks still
+  cover its reservation.
+* Priority preemption ("longest-first" or "lowest-priority"): when the head
+  of the queue does not fit (no free slot or not enough blocks), it may evict
+  an admitted request of strictly lower priority -- the one that generated
+  the most tokens, or the lowest priority with most tokens breaking ties --
+  and try again.
+* Decode headroom: decode rows reserve the blocks they open before the step;
+  if the pool cannot cover them, the eviction ladder runs: cached prompt
+  prefixes first and prefixes adopted by waiting requests next (this
+  scheduler keeps neither, so those rungs are empty), then the admitted
+  request with the least progress is preempted, until the rows fit.
+  Reading of "least progress": fewest generated tokens, then fewest rows in
+  the cache, then the latest admitted.
+* A preempted request's generated tokens are kept and its KV freed; it goes
+  back into the deferred queue in arrival order and, when admitted again,
+  re-prefills its prompt and the tokens it had generated (the last re-prefill
+  chunk yields its next token), then decodes on. Ties between victims by
+  generated tokens fall to the latest admitted.
+
 Slots are handed out lowest-free-first. Decode rows take new blocks inside
 ``pkv_plan_lower`` when their position opens one.
 """
 
 from __future__ import annotations
 
+import bisect
 import heapq
 from collections import deque
 from dataclasses import dataclass
@@ -37,8 +63,12 @@ from . import binding as B
 class _Live:
     rid: int
     slot: int
-    prompt: int
+    prompt: int   # rows to prefill: the prompt, or prompt + generated tokens after a preemption
+    base: int     # the request's own prompt length
     output: int
+    arrival: int
+    priority: int
+    order: int    # admission counter (later admitted = larger)
     pos: int = 0
     decoding: bool = False
     generated: int = 0
@@ -53,32 +83,108 @@ class PlannedRow:
     prefill: bool
 
 
+@dataclass
+class _Waiting:
+    key: tuple      # (arrival step, rid): the deferred queue's order
+    rid: int
+    prompt: int     # rows to prefill on admission
+    base: int       # the request's own prompt length
+    output: int
+    priority: int
+    generated: int  # tokens generated before a preemption (0 for a new request)
+
+    def __lt__(self, other):
+        return self.key < other.key
+
+
 class ChurnScheduler:
-    def __init__(self, requests, pool: B.Pool, *, chunk_idle: int = 2048, chunk_busy: int = 512):
+    def __init__(self, requests, pool: B.Pool, *, chunk_idle: int = 2048, chunk_busy: int = 512,
+                 watermark: float = 0.0, preemption: str | None = None):
+        if not 0.0 <= watermark <= 0.5:
+            raise ValueError("watermark must be in [0, 0.5]")
+        if preemption not in (None, "longest-first", "lowest-priority"):
+            raise ValueError(f"unknown preemption policy {preemption!r}")
         self.pool = pool
         self.pending = deque(sorted(requests, key=lambda r: (r.arrival_step, r.rid)))
-        self.queue: deque = deque()
+        self.queue: list[_Waiting] = []  # sorted by key
         self.live: list[_Live] = []
         self.free_slots = list(range(pool.max_slots))
         heapq.heapify(self.free_slots)
         self.chunk_idle, self.chunk_busy = chunk_idle, chunk_busy
+        self.watermark, self.preemption = watermark, preemption
         self.step_index = 0
+        self.admitted = 0
+        self.preempted: list[int] = []  # request IDs, in preemption order
+        self.preempt_reasons: list[str] = []  # "priority" or "headroom", one per preemption
 
+    # ---- helpers ------------------------------------------------------------
+    def _free_blocks(self) -> int:
+        return self.pool.stats().free_blocks
+
+    def _preempt(self, r: _Live, reason: str, hold: list | None = None) -> None:
+        """Release r; it waits again in arrival order (in ``hold`` until the request that evicted it is in)."""
+        self.pool.release(r.slot)
+        heapq.heappush(self.free_slots, r.slot)
+        self.live.remove(r)
+        # re-prefill the prompt and every generated token; keep the count of generated tokens
+        w = _Waiting((r.arrival, r.rid), r.rid, r.base + r.generated, r.base, r.output, r.priority, r.generated)
+        if hold is None:
+            bisect.insort(self.queue, w)
+        else:
+            hold.append(w)
+        self.preempted.append(r.rid)
+        self.preempt_reasons.append(reason)
+
+    def _priority_victim(self, priority: int):
+        cands = [r for r in self.live if r.priority < priority]
+        if not cands:
+            return None
+        if self.preemption == "lowest-priority":
+            return min(cands, key=lambda r: (r.priority, -r.generated, -r.order))
+        return max(cands, key=lambda r: (r.generated, r.order))
+
+    def _decode_blocks_needed(self) -> int:
+        bs = self.pool.block_size
+        return sum(1 for r in self.live if r.decoding and r.pos // bs >= self.pool.slot_blocks(r.slot))
+
+    # ---- one step -------------------------------------------------------------
     def plan(self) -> list[PlannedRow]:
         s = self.step_index
+        bs = self.pool.block_size
         while self.pending and self.pending[0].arrival_step <= s:
-            self.queue.append(self.pending.popleft())
-        while self.queue and self.free_slots:
+            q = self.pending.popleft()
+            bisect.insort(self.queue, _Waiting((q.arrival_step, q.rid), q.rid, q.prompt_len, q.prompt_len,
+                                               q.output_len, q.priority, 0))
+        hold: list[_Waiting] = []  # evicted for the current head: they queue up behind it
+        while self.queue:
             head = self.queue[0]
+            need = -(-(head.prompt + 1) // bs)
+            mark = self.watermark * self.pool.num_blocks if any(r.decoding for r in self.live) else 0.0
+            if not self.free_slots or self._free_blocks() - need < mark:
+                victim = self._priority_victim(head.priority) if self.preemption else None
+                if victim is None:
+                    break  # strict FIFO: the head waits, nobody behind it jumps ahead
+                self._preempt(victim, "priority", hold)
+                continue
             slot = self.free_slots[0]
-            rc = self.pool.admit(slot, head.prompt_len + 1)
-            if rc == B.PKV_ERR_NO_BLOCKS:
-                break  # strict FIFO
+            rc = self.pool.admit(slot, head.prompt + 1)
             if rc != B.PKV_OK:
                 raise B.PkvError(rc, "pkv_pool_admit")
             heapq.heappop(self.free_slots)
-            self.queue.popleft()
-            self.live.append(_Live(head.rid, slot, head.prompt_len, head.output_len))
+            self.queue.pop(0)
+            for w in hold:
+                bisect.insort(self.queue, w)
+            hold.clear()
+            r = _Live(head.rid, slot, head.prompt, head.base, head.output, head.key[0], head.priority, self.admitted)
+            r.generated = head.generated
+            self.admitted += 1
+            self.live.append(r)
+        for w in hold:  # the head did not fit even after every eviction it could make
+            bisect.insort(self.queue, w)
+        # decode headroom: blocks the decode rows open must be free before the step
+        while self._decode_blocks_needed() > self._free_blocks():
+            victim = min(self.live, key=lambda r: (r.generated, r.pos, -r.order))
+            self._preempt(victim, "headroom")
         budget = self.chunk_busy if any(r.decoding for r in self.live) else self.chunk_idle
         rows: list[PlannedRow] = []
         for r in self.live:
@@ -100,7 +206,7 @@ class ChurnScheduler:
             if row.prefill:
                 if r.pos == r.prompt:
                     r.decoding = True
-                    r.generated = 1
+                    r.generated += 1
             else:
                 r.generated += 1
             if r.pos >= r.prompt and r.generated >= r.output:

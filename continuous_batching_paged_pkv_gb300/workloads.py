@@ -280,6 +280,7 @@ class Request:
     arrival_step: int
     prompt_len: int
     output_len: int
+    priority: int = 0  # higher is more urgent
 
 
 @dataclass(frozen=True)
@@ -296,17 +297,22 @@ class ChurnSpec:
     block_size: int = 16
     num_blocks: int = 131072
     max_slots: int = 64
+    high_priority: float = 0.0  # fraction of requests with priority 1 (the rest 0)
 
 
 def churn_trace(seed: int = 0, spec: ChurnSpec = ChurnSpec()) -> list[Request]:
-    """Arrivals Poisson(rate) per step; prompt ~ U[min, max]; output ~ Geometric(1/mean), clipped."""
+    """Arrivals Poisson(rate) per step; prompt ~ U[min, max]; output ~ Geometric(1/mean), clipped.
+
+    Priorities come from a stream of their own, so the trace without them is unchanged."""
     (r,) = _rngs(seed, 1, 4)
+    (rp,) = _rngs(seed, 1, 7)
     reqs = []
     for step in range(spec.num_steps):
         for _ in range(int(r.poisson(spec.arrival_rate))):
             p = int(r.integers(spec.prompt_min, spec.prompt_max + 1))
             o = int(min(r.geometric(1.0 / spec.output_mean), spec.output_max))
-            reqs.append(Request(len(reqs), step, p, o))
+            prio = int(rp.random() < spec.high_priority) if spec.high_priority > 0 else 0
+            reqs.append(Request(len(reqs), step, p, o, prio))
     return reqs
 
 

@@ -30,6 +30,28 @@ oracle's plain reading where the pages leave a value open):
   Lifecycle; Lucebox §One scheduler, model-specific execution.)
 * Decode rows take one more block when their position crosses into a block
   the reservation did not cover.
+
+Budget rules (mlxcel manual, "Continuous batching", §Preemptive eviction,
+§Paged KV cache and prefix sharing, and the section on decode headroom under a
+tight budget), used only when switched on:
+
+* Watermark F: while some request decodes, the queue head is admitted only if
+  free blocks - F * (pool blocks) >= its reservation.
+* Preemption for priority: if the head does not fit (slot or blocks) and some
+  admitted request has a strictly lower priority, one of those is evicted --
+  policy "longest-first": the one with the most generated tokens;
+  "lowest-priority": the lowest priority, most generated tokens on ties --
+  and admission is tried again. Reading: remaining ties go to the latest
+  admitted.
+* Decode headroom: before the step, the blocks that decode rows open must be
+  free; otherwise admitted requests are preempted, least progress first
+  (reading: fewest generated tokens, then fewest cached rows, then latest
+  admitted), until they are. (The pages' earlier rungs, cold cached prefixes
+  and prefixes adopted by waiting requests, do not exist in this replay.)
+* A preempted request frees its slot and blocks, keeps its generated-token
+  count, and waits again in arrival order; once admitted it prefills its
+  prompt plus the tokens it had generated, the last chunk yielding one more
+  token, then decodes.
 """
 
 from __future__ import annotations
@@ -51,6 +73,10 @@ class _Live:
     decoding: bool = False
     generated: int = 0
     blocks: int = 0
+    own_prompt: int = 0
+    arrival: int = 0
+    priority: int = 0
+    admitted_as: int = 0
 
 
 @dataclass(frozen=True)
@@ -69,31 +95,80 @@ def _ceil_div(a: int, b: int) -> int:
 
 class ChurnReplay:
     def __init__(self, requests, *, max_slots: int, num_blocks: int, block_size: int,
-                 chunk_idle: int = 2048, chunk_busy: int = 512):
+                 chunk_idle: int = 2048, chunk_busy: int = 512, watermark: float = 0.0,
+                 preemption: str | None = None):
         self.pending = deque(sorted(requests, key=lambda r: (r.arrival_step, r.rid)))
-        self.queue: deque = deque()
+        # waiting requests: (arrival, rid, rows to prefill, own prompt, output, priority, generated)
+        self.queue: list[tuple] = []
         self.live: list[_Live] = []  # admission order
         self.free_slots = max_slots
         self.free_blocks = num_blocks
+        self.num_blocks = num_blocks
         self.bs = block_size
         self.chunk_idle, self.chunk_busy = chunk_idle, chunk_busy
+        self.watermark, self.preemption = watermark, preemption
         self.step_index = 0
         self.finished: list[int] = []
+        self.preempted: list[int] = []
+        self.preempt_reasons: list[str] = []  # "priority" or "headroom"
+        self._admissions = 0
+
+    def _evict(self, r: _Live, reason: str, held=None) -> None:
+        """Free r's slot and blocks; it waits again (in `held` until the request that evicted it is in)."""
+        self.live.remove(r)
+        self.free_slots += 1
+        self.free_blocks += r.blocks
+        entry = (r.arrival, r.rid, r.own_prompt + r.generated, r.own_prompt, r.output, r.priority, r.generated)
+        if held is None:
+            self.queue.append(entry)
+            self.queue.sort()
+        else:
+            held.append(entry)
+        self.preempted.append(r.rid)
+        self.preempt_reasons.append(reason)
 
     def plan(self) -> list[Row]:
         """Advance admission for the current step and return its rows (packed order)."""
         s = self.step_index
         while self.pending and self.pending[0].arrival_step <= s:
-            self.queue.append(self.pending.popleft())
-        while self.queue and self.free_slots > 0:
-            head = self.queue[0]
-            need = _ceil_div(head.prompt_len + 1, self.bs)
-            if need > self.free_blocks:
-                break  # strict FIFO: nobody jumps ahead
-            self.queue.popleft()
+            q = self.pending.popleft()
+            self.queue.append((q.arrival_step, q.rid, q.prompt_len, q.prompt_len, q.output_len,
+                               getattr(q, "priority", 0), 0))
+            self.queue.sort()
+        held: list[tuple] = []  # evicted for the current head; they wait behind it
+        while self.queue:
+            arrival, rid, rows_to_fill, own, output, prio, gen = self.queue[0]
+            need = _ceil_div(rows_to_fill + 1, self.bs)
+            floor = self.watermark * self.num_blocks if any(r.decoding for r in self.live) else 0.0
+            if self.free_slots == 0 or self.free_blocks - need < floor:
+                lower = [r for r in self.live if r.priority < prio] if self.preemption else []
+                if not lower:
+                    break  # strict FIFO: nobody jumps ahead
+                if self.preemption == "lowest-priority":
+                    lower.sort(key=lambda r: (r.priority, -r.generated, -r.admitted_as))
+                else:  # longest-first
+                    lower.sort(key=lambda r: (-r.generated, -r.admitted_as))
+                self._evict(lower[0], "priority", held)
+                continue
+            self.queue.pop(0)
+            if held:
+                self.queue.extend(held)
+                self.queue.sort()
+                held.clear()
             self.free_slots -= 1
             self.free_blocks -= need
-            self.live.append(_Live(head.rid, head.prompt_len, head.output_len, blocks=need))
+            self.live.append(_Live(rid, rows_to_fill, output, generated=gen, blocks=need, own_prompt=own,
+                                   arrival=arrival, priority=prio, admitted_as=self._admissions))
+            self._admissions += 1
+        if held:  # the head still did not fit after every eviction it could make
+            self.queue.extend(held)
+            self.queue.sort()
+        # decode headroom
+        while True:
+            opening = sum(1 for r in self.live if r.decoding and r.pos // self.bs >= r.blocks)
+            if opening <= self.free_blocks:
+                break
+            self._evict(sorted(self.live, key=lambda r: (r.generated, r.pos, -r.admitted_as))[0], "headroom")
         budget = self.chunk_busy if any(r.decoding for r in self.live) else self.chunk_idle
         rows: list[Row] = []
         for r in self.live:
@@ -123,7 +198,7 @@ class ChurnReplay:
             if row.prefill:
                 if r.pos == r.prompt:
                     r.decoding = True
-                    r.generated = 1
+                    r.generated += 1
             else:
                 r.generated += 1
             if r.pos >= r.prompt and r.generated >= r.output:

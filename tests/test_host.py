@@ -423,20 +423,48 @@ def test_step_rejects_bad_staging_before_any_device_work():
 
 # ---- scheduler vs the oracle's replay -------------------------------------------
 
-def _compare_trace(reqs, spec_steps, num_blocks, max_slots, bs=16):
+def _compare_trace(reqs, spec_steps, num_blocks, max_slots, bs=16, **policy):
     pool = B.Pool(num_blocks, bs, max_slots, 1024, free_order=W.churn_free_order(0, num_blocks))
-    sch = S.ChurnScheduler(reqs, pool)
-    ref = churn.ChurnReplay(reqs, max_slots=max_slots, num_blocks=num_blocks, block_size=bs)
+    sch = S.ChurnScheduler(reqs, pool, **policy)
+    ref = churn.ChurnReplay(reqs, max_slots=max_slots, num_blocks=num_blocks, block_size=bs, **policy)
     for step in range(spec_steps):
         rows = sch.plan()
         want = ref.plan()
         assert [(r.rid, r.begin, r.n, r.prefill) for r in rows] == \
                [(r.rid, r.begin, r.n, r.prefill) for r in want], f"step {step}"
+        assert sch.preempted == ref.preempted, f"step {step}: preemptions differ"
+        assert sch.preempt_reasons == ref.preempt_reasons, f"step {step}: preemption reasons differ"
         low = pool.lower([(r.slot, r.n) for r in rows])
         assert len(low.slot_mapping) == sum(r.n for r in rows)
         assert sch.commit(rows) == ref.commit(want)
         assert pool.stats().free_blocks == ref.free_blocks
     return sch
+
+
+# 300 blocks (4800 tokens) and 16 slots for ~100 requests of 64-1024 prompt tokens: the pool, not the
+# slots, limits admission, decode rows run out of blocks, and 30% of requests carry priority 1.
+PRESSURE = W.ChurnSpec(num_steps=200, arrival_rate=0.5, prompt_min=64, prompt_max=1024, output_mean=96.0,
+                       output_max=400, high_priority=0.3)
+
+
+@pytest.mark.parametrize("policy", [dict(), dict(watermark=0.01), dict(watermark=0.01, preemption="longest-first"),
+                                    dict(watermark=0.01, preemption="lowest-priority")])
+def test_budgeted_scheduler_matches_oracle_under_pool_pressure(policy):
+    """Small pool: watermark admission, priority preemption and decode-headroom preemption all fire."""
+    reqs = W.churn_trace(5, PRESSURE)
+    sch = _compare_trace(reqs, PRESSURE.num_steps, 300, 16, **policy)
+    assert len(sch.preempted) > 0  # the budget rules were exercised, not just the happy path
+    if policy.get("preemption"):
+        assert "priority" in sch.preempt_reasons and "headroom" in sch.preempt_reasons
+    else:
+        assert set(sch.preempt_reasons) == {"headroom"}
+
+
+def test_watermark_reduces_decode_preemptions():
+    """The pages' reason for the watermark: keeping free blocks at admission leaves decode headroom."""
+    reqs = W.churn_trace(5, PRESSURE)
+    counts = [len(_compare_trace(reqs, PRESSURE.num_steps, 300, 16, watermark=f).preempted) for f in (0.0, 0.05)]
+    assert counts[1] < counts[0]
 
 
 def test_scheduler_matches_oracle_replay_on_churn_trace():

@@ -317,9 +317,96 @@ def test_thread_count_does_not_change_results(oracle_lib):
 # ---- the churn replay's scheduling rules ------------------------------------
 
 class _Req:
-    def __init__(self, rid, arrival_step, prompt_len, output_len):
+    def __init__(self, rid, arrival_step, prompt_len, output_len, priority=0):
         self.rid, self.arrival_step = rid, arrival_step
         self.prompt_len, self.output_len = prompt_len, output_len
+        self.priority = priority
+
+
+def _run_steps(r, n):
+    out = []
+    for _ in range(n):
+        rows = r.plan()
+        out.append(rows)
+        r.commit(rows)
+    return out
+
+
+# ---- budget rules (mlxcel manual, §Preemptive eviction and the decode-headroom
+# section), hand-worked scenarios ---------------------------------------------
+
+def test_watermark_holds_back_admission_only_while_decoding():
+    # A (prompt 15: one block with its first decode row) decodes from step 1; B arrives at step 1.
+    # 100 blocks, F = 0.10: B is admitted only if 99 free - its blocks >= 10.
+    def live_after(b_blocks, watermark=0.10, with_a=True):
+        reqs = ([_Req(0, 0, 15, 50)] if with_a else []) + [_Req(1, 1 if with_a else 0, b_blocks * 16 - 1, 1)]
+        r = churn.ChurnReplay(reqs, max_slots=4, num_blocks=100, block_size=16, watermark=watermark)
+        _run_steps(r, 1 if not with_a else 1)
+        r.plan()
+        return [x.rid for x in r.live], [q[1] for q in r.queue]
+
+    assert live_after(85) == ([0, 1], [])   # 99 - 85 = 14 >= 10
+    assert live_after(89) == ([0, 1], [])   # 99 - 89 = 10 >= 10: exactly at the floor
+    assert live_after(90) == ([0], [1])     # 99 - 90 = 9 < 10: waits
+    assert live_after(90, watermark=0.0) == ([0, 1], [])
+    # with nothing decoding the watermark does not apply
+    r = churn.ChurnReplay([_Req(1, 0, 99 * 16 - 1, 1)], max_slots=4, num_blocks=100, block_size=16,
+                          watermark=0.10)
+    r.plan()
+    assert [x.rid for x in r.live] == [1]
+
+
+@pytest.mark.parametrize("policy,victim", [("longest-first", 1), ("lowest-priority", 0)])
+def test_priority_preemption_picks_the_policy_victim(policy, victim):
+    # two slots; X (prio 0) and Y (prio 0 / 1) decode; Z (prio 2) arrives and finds no slot
+    reqs = [_Req(0, 0, 15, 100, 0), _Req(1, 0, 15, 100, 1 if policy == "lowest-priority" else 0),
+            _Req(2, 6, 15, 100, 2)]
+    r = churn.ChurnReplay(reqs, max_slots=2, num_blocks=64, block_size=16, preemption=policy)
+    # X generates one token fewer than Y: Y gets its first token one step earlier
+    r.live[0:0] = []
+    _run_steps(r, 6)
+    by = {x.rid: x for x in r.live}
+    gen = {k: v.generated for k, v in by.items()}
+    if policy == "longest-first":  # equal priority 0: the most generated tokens, ties to the latest admitted
+        assert gen[0] == gen[1]
+    rows = r.plan()
+    assert r.preempted == [victim] and sorted(x.rid for x in r.live) == sorted({0, 1, 2} - {victim})
+    # the victim waits with its prompt plus the tokens it generated, in arrival order
+    assert r.queue[0][1] == victim and r.queue[0][2] == 15 + gen[victim] and r.queue[0][6] == gen[victim]
+    assert any(x.rid == 2 and x.prefill for x in rows)
+
+
+def test_decode_headroom_preempts_the_least_progress():
+    # 4 blocks in all: A and B each reserve 1 (prompt 14 + 1 row) and decode into block 2 at position 16
+    reqs = [_Req(0, 0, 14, 50), _Req(1, 0, 14, 50), _Req(2, 1, 14, 50)]
+    r = churn.ChurnReplay(reqs, max_slots=4, num_blocks=4, block_size=16)
+    _run_steps(r, 1)          # A, B prefill (generated 1 each); C not yet arrived
+    _run_steps(r, 1)          # C admitted (1 block, free 1) and prefills; A, B decode at 14
+    rows = r.plan()           # A, B at 15: still in block 1
+    r.commit(rows)
+    rows = r.plan()           # A, B open block 2 (two blocks, one free): C has the least progress
+    assert r.preempted == [2] and {x.rid for x in rows} == {0, 1}
+    assert r.free_blocks == 0 and r.queue[0][1] == 2
+
+
+def test_re_prefill_resumes_where_the_request_stopped():
+    reqs = [_Req(0, 0, 14, 6), _Req(1, 0, 14, 50), _Req(2, 1, 14, 50)]
+    r = churn.ChurnReplay(reqs, max_slots=4, num_blocks=4, block_size=16)
+    seen_gen, refill = {}, None
+    for _ in range(12):  # C: prefill, one decode, preempted at its first block crossing, back at step 6
+        rows = r.plan()
+        if r.preempted and 2 not in seen_gen:
+            seen_gen[2] = r.queue[0][6]  # generated tokens kept while it waits
+        for x in rows:
+            if x.rid == 2 and 2 in seen_gen and refill is None:
+                refill = x
+        r.commit(rows)
+    assert r.preempted[0] == 2 and 0 in r.finished
+    # once back, C prefills its prompt plus the tokens it had generated, from position 0
+    g = seen_gen[2]
+    assert g >= 1 and refill.prefill and refill.begin == 0 and refill.n == 14 + g
+    c = next(x for x in r.live if x.rid == 2)
+    assert c.decoding and c.generated == g + 1 + (c.pos - (14 + g))
 
 
 def test_chunk_schedule_example_from_the_page():
@@ -354,7 +441,7 @@ def test_fifo_admission_example_from_the_page():
     reqs = [_Req(0, 0, d_tokens, 1), _Req(1, 0, e_tokens, 1)]
     r = churn.ChurnReplay(reqs, max_slots=8, num_blocks=g["free_blocks"], block_size=bs)
     assert r.plan() == []
-    assert [q.rid for q in r.queue] == [0, 1] and r.free_blocks == g["free_blocks"]
+    assert [q[1] for q in r.queue] == [0, 1] and r.free_blocks == g["free_blocks"]  # (arrival, rid, ...)
 
 
 def test_chunk_size_rule_from_the_page():
