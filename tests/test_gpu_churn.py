@@ -28,35 +28,41 @@ MAX_ABS = 2e-2
 MAX_REL_L2 = 1e-2
 
 
-def test_churn_trace_matches_contiguous_oracle():
+def _replay(spec, seed, num_blocks, max_slots, **policy):
+    """Run the trace through the library and the oracle side by side; returns what it saw."""
     torch = pytest.importorskip("torch")
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     libbuild.build()
     oracle.build()
 
-    spec = W.ChurnSpec()
-    reqs = W.churn_trace(0, spec)
+    reqs = W.churn_trace(seed, spec)
     bs, hq, hkv, d = spec.block_size, spec.num_q_heads, spec.num_kv_heads, spec.head_dim
-    mbps = -(-(spec.prompt_max + spec.output_max + 1) // bs) + 1
-    pool = B.Pool(spec.num_blocks, bs, spec.max_slots, mbps, free_order=W.churn_free_order(0, spec.num_blocks))
-    sch = S.ChurnScheduler(reqs, pool)
-    ref = churn.ChurnReplay(reqs, max_slots=spec.max_slots, num_blocks=spec.num_blocks, block_size=bs)
+    mbps = -(-(spec.prompt_max + 2 * spec.output_max + 1) // bs) + 1  # re-prefill covers generated tokens too
+    pool = B.Pool(num_blocks, bs, max_slots, mbps, free_order=W.churn_free_order(seed, num_blocks))
+    sch = S.ChurnScheduler(reqs, pool, **policy)
+    ref = churn.ChurnReplay(reqs, max_slots=max_slots, num_blocks=num_blocks, block_size=bs, **policy)
     hist = churn.ContiguousHistory()
     toks = W.TokenSource(0, hq, hkv, d)
     scale = 1.0 / np.sqrt(d)
     dev = "cuda"
-    k_pool, v_pool = R.empty_pool(spec.num_blocks, hkv, bs, d, dev)
+    k_pool, v_pool = R.empty_pool(num_blocks, hkv, bs, d, dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     pick = np.random.default_rng(7)
 
     checked_rows = steps_with_rows = max_ctx = 0
     saw_prefill_and_decode = saw_retire = False
+    refilled = set()
     for step in range(spec.num_steps):
+        n_pre = len(sch.preempted)
         rows = sch.plan()
         want = ref.plan()
         assert [(r.rid, r.begin, r.n, r.prefill) for r in rows] == \
                [(r.rid, r.begin, r.n, r.prefill) for r in want], f"step {step}: plans differ"
+        assert sch.preempted == ref.preempted, f"step {step}: preemptions differ"
+        for rid in sch.preempted[n_pre:]:
+            hist.drop(rid)  # its KV is gone; it re-prefills from position 0 when admitted again
+        refilled |= {r.rid for r in rows if r.prefill and r.rid in sch.preempted}
         if rows:
             steps_with_rows += 1
             low = pool.lower([(r.slot, r.n) for r in rows])
@@ -65,7 +71,7 @@ def test_churn_trace_matches_contiguous_oracle():
             v_new = np.concatenate([p[1] for p in parts])
             q = np.concatenate([p[2] for p in parts])
             work, info = B.pkv_plan_work(low.cu_seqlens_q, low.seq_slot, low.context_lens,
-                                         max_slots=spec.max_slots, max_blocks_per_slot=mbps, block_size=bs,
+                                         max_slots=max_slots, max_blocks_per_slot=mbps, block_size=bs,
                                          num_q_heads=hq, num_kv_heads=hkv, head_dim=d)
             t_k, t_v, t_q = (R._bf16_tensor(x, dev) for x in (k_new, v_new, q))
             t_sm = R._i64(low.slot_mapping, dev)
@@ -117,6 +123,29 @@ def test_churn_trace_matches_contiguous_oracle():
             hist.drop(rid)
         assert pool.stats().free_blocks == ref.free_blocks, f"step {step}: free blocks"
 
+    return dict(steps_with_rows=steps_with_rows, checked_rows=checked_rows, max_ctx=max_ctx,
+                saw_prefill_and_decode=saw_prefill_and_decode, saw_retire=saw_retire,
+                preempted=list(sch.preempted), reasons=list(sch.preempt_reasons), refilled=refilled)
+
+
+def test_churn_trace_matches_contiguous_oracle():
+    spec = W.ChurnSpec()
+    seen = _replay(spec, 0, spec.num_blocks, spec.max_slots)
     # the trace exercised what it is for
-    assert steps_with_rows >= spec.num_steps - 5 and checked_rows > 300
-    assert saw_prefill_and_decode and saw_retire and max_ctx > 2048
+    assert seen["steps_with_rows"] >= spec.num_steps - 5 and seen["checked_rows"] > 300
+    assert seen["saw_prefill_and_decode"] and seen["saw_retire"] and seen["max_ctx"] > 2048
+    assert not seen["preempted"]
+
+
+# 300 blocks (4,800 tokens) and 16 slots for ~100 requests of 64-1024 prompt tokens, 30% at priority 1
+PRESSURE = W.ChurnSpec(num_steps=200, arrival_rate=0.5, prompt_min=64, prompt_max=1024, output_mean=96.0,
+                       output_max=400, high_priority=0.3)
+
+
+def test_churn_under_pool_pressure_with_preemption_matches_oracle():
+    """Watermark admission, priority and decode-headroom preemption, and re-prefill of preempted requests:
+    the re-prefilled K/V rows land in new blocks and the outputs still match the contiguous replay."""
+    seen = _replay(PRESSURE, 5, 300, 16, watermark=0.01, preemption="lowest-priority")
+    assert seen["preempted"] and {"priority", "headroom"} <= set(seen["reasons"])
+    assert seen["refilled"]  # some preempted request came back and re-prefilled on the GPU
+    assert seen["saw_retire"] and seen["checked_rows"] > 100
