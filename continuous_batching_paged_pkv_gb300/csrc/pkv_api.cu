@@ -157,7 +157,7 @@ pkv_status pkv_attention(const void *q, const int32_t *cu_seqlens_q, int32_t num
     return PKV_ERR_INVALID_ARG;
   const uint64_t acc_bytes = align256(uint64_t(info->num_partials) * num_q_heads * head_dim * 4);
   const uint64_t ml_bytes = align256(uint64_t(info->num_partials) * num_q_heads * 8);
-  const uint64_t need = info->num_partials == 0 ? 0 : acc_bytes + ml_bytes;
+  const uint64_t need = info->num_partials == 0 ? 0 : acc_bytes + ml_bytes + pkv::kCounterBytes;
   if (need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 256)))
     return PKV_ERR_WORKSPACE_TOO_SMALL;
   if ((info->num_combine_items > 0) != (info->num_partials > 0)) return PKV_ERR_INVALID_ARG;
@@ -192,6 +192,8 @@ pkv_status pkv_attention(const void *q, const int32_t *cu_seqlens_q, int32_t num
   a.partial_acc = static_cast<float *>(workspace);
   a.partial_ml = need ? reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + acc_bytes) : nullptr;
   a.status = device_status;
+  a.task_counter =
+      need ? reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(workspace) + acc_bytes + ml_bytes) : nullptr;
 
   CUtensorMap tk, tv, tq;
   if (!encode_pool(&tk, k_pool, rows, head_dim) || !encode_pool(&tv, v_pool, rows, head_dim))
@@ -289,7 +291,7 @@ pkv_status pkv_attention_q8(const void *q, const int32_t *cu_seqlens_q, int32_t 
     return PKV_ERR_INVALID_ARG;
   const uint64_t acc_bytes = align256(uint64_t(info->num_partials) * num_q_heads * head_dim * 4);
   const uint64_t ml_bytes = align256(uint64_t(info->num_partials) * num_q_heads * 8);
-  const uint64_t part_bytes = info->num_partials == 0 ? 0 : acc_bytes + ml_bytes;
+  const uint64_t part_bytes = info->num_partials == 0 ? 0 : acc_bytes + ml_bytes + pkv::kCounterBytes;
   const uint64_t sb = static_cast<uint64_t>(info->scratch_blocks);
   const uint64_t scratch_pool = align256(sb * num_kv_heads * block_size * head_dim * 2);
   const uint64_t table_bytes = align256(uint64_t(max_slots) * max_blocks_per_slot * 4);

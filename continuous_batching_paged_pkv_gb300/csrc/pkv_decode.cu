@@ -8,16 +8,21 @@
 // of rebuilding a contiguous window every step.
 //
 // Decode kernel. A task is one (decode segment, key span of PKV_SPLIT_KEYS
-// keys, kv head). The grid is one CTA per SM with eight warps; every warp is
-// an independent worker taking tasks t = w, w + W, w + 2W, ... (W = all warps;
-// the work list is sorted longest first and consecutive tasks go to different
-// SMs). A warp streams its tasks' 16-key K/V sub-tiles through its own
-// three-stage ring in shared memory with TMA (64-column x 16-row boxes,
+// keys, kv head). The grid is one CTA per SM with eight warps (four to six,
+// with deeper rings, on steps with few tasks); every warp is
+// an independent worker taking tasks t = w, w + W, w + 2W (W = all warps; the
+// work list is sorted longest first and consecutive tasks go to different
+// SMs), then, on steps with more tasks, the next unclaimed task from a counter
+// in the workspace: some SMs stream faster than others, and claiming keeps
+// them all busy to the end. A warp streams its tasks' 16-key K/V sub-tiles
+// through its own three-stage ring in shared memory with TMA (64-column x 16-row boxes,
 // 128-byte swizzle) straight from the pool rows the block table names. The
 // ring keeps flowing across task boundaries: the next task's metadata and
 // block IDs load while the current task computes, and its first sub-tiles are
 // requested before the current task ends. Eight warps x three 8 KiB stages
-// keep ~192 KiB of K/V in flight per SM, enough to cover HBM latency.
+// keep ~192 KiB of K/V in flight per SM, enough to cover HBM latency; a step
+// with four to six tasks per SM runs four to six warps with six to four
+// stages, so its busy warps keep about as much in flight.
 //
 // Math per sub-tile: warp-level bf16 MMA (m16n8k16), fp32 accumulation,
 //   S^T[16 keys][8 heads] = K[16 keys][D] * Q^T[D][8 heads]   (GQA group on N)
@@ -54,19 +59,21 @@
 namespace pkv {
 namespace {
 
-constexpr int kWarps = 8;  // independent workers per CTA
+constexpr int kWarps = 8;  // independent workers per CTA on steps that fill every warp
 constexpr uint32_t kFull = 0xffffffffu;
 constexpr float kRescale = 8.0f;  // log2 units
 
-template <int D>
+// NW warps per CTA, each with a ring of NST stages (0: 24 KiB per warp).
+template <int D, int NW = kWarps, int NST = 0>
 struct DecodeCfg {
   static constexpr int kHalves = D / 64;
   static constexpr int kHalfBytes = kSubKeys * 128;        // 16 rows x 128 B
   static constexpr int kTileBytes = kHalves * kHalfBytes;  // one K (or V) sub-tile
   static constexpr int kStageBytes = 2 * kTileBytes;       // K then V
-  static constexpr int kStages = (24 * 1024) / kStageBytes;  // 3 (D=128) or 6 (D=64)
+  static constexpr int kStages = NST > 0 ? NST : (24 * 1024) / kStageBytes;  // default 3 (D=128) or 6 (D=64)
   static constexpr int kWarpRing = kStages * kStageBytes;
-  static constexpr int kSmem = kWarps * kWarpRing + kWarps * kStages * 8 + 1024;
+  static constexpr int kSmem = NW * kWarpRing + NW * kStages * 8 + 1024;
+  static_assert(kSmem <= 227 * 1024, "ring does not fit in shared memory");
 };
 
 __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
@@ -96,11 +103,15 @@ __device__ __forceinline__ void load_q(uint32_t (&qf)[NT][D / 16][2], const Task
 
 // NT: 8-column MMA tiles of (row, q head) columns; MULTI: segments may hold
 // more than one row (otherwise every segment is a single decode row).
-template <int D, int NT, bool MULTI>
-__global__ void __launch_bounds__(kWarps * 32, 1)
+// NW, NS: warps per CTA and stages per warp ring. A warp's stream of
+// sub-tiles is latency-bound (its ring's bytes per HBM round trip), so steps
+// with fewer tasks than warps run fewer warps with deeper rings; the math of
+// a task does not depend on them.
+template <int D, int NT, bool MULTI, int NW, int NS>
+__global__ void __launch_bounds__(NW * 32, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                   const StepArgs a, const int32_t *__restrict__ items, int num_items) {
-  using Cfg = DecodeCfg<D>;
+  using Cfg = DecodeCfg<D, NW, NS>;
   constexpr int KT = D / 16;  // k-steps of QK^T, m-tiles of PV
   constexpr int NST = Cfg::kStages;
   constexpr int kMaxRows = MULTI ? 16 : 1;
@@ -108,13 +119,13 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
   uint8_t *smem = align1024(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint8_t *ring = smem + warp * Cfg::kWarpRing;
-  uint64_t *full = reinterpret_cast<uint64_t *>(smem + kWarps * Cfg::kWarpRing) + warp * NST;
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + NW * Cfg::kWarpRing) + warp * NST;
 
   // The span merge may launch now; it waits for this grid before reading.
   launch_dependents();
   const int hkv = a.num_kv_heads;
   const int num_tasks = num_items * hkv;
-  const int stride = gridDim.x * kWarps;
+  const int stride = gridDim.x * NW;
   const int t0 = warp * gridDim.x + blockIdx.x;
   if (t0 >= num_tasks) return;
   if (lane == 0) {
@@ -130,14 +141,19 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
   // span of each row) are read only after waiting for it, in issue().
   bool waited = false;
 
+  // A warp's tasks: t0, t0 + stride, t0 + 2 stride, then (with a task
+  // counter) 3 stride + the counter's next value, else t0 + 3 stride, ...
+  // A is current, B expanded, tC the task whose work item is in rawC.
+  uint32_t *const counter = a.task_counter;
   Task A, B;
   int4 rawC = make_int4(0, 0, 0, 0);
   expand(A, t0, load_item(items, t0, hkv), a, lane);
+  int tC;
   {
     const int t1 = t0 + stride;
     expand(B, t1 < num_tasks ? t1 : -1, t1 < num_tasks ? load_item(items, t1, hkv) : rawC, a, lane);
-    const int t2 = t1 + stride;
-    if (t2 < num_tasks) rawC = load_item(items, t2, hkv);
+    tC = t1 + stride;
+    if (tC < num_tasks) rawC = load_item(items, tC, hkv);
   }
   finalize(A, a, lane, 8 * NT, kMaxRows);
   uint32_t qA[NT][KT][2], qB[NT][KT][2];
@@ -147,7 +163,8 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
   int P = 0, C = 0, pa = 0, pb = 0;
   int pstage = 0;  // P % NST
   auto issue = [&](const Task &T, int u) {
-    if (T.reads_new && !waited) {
+    // only the sub-tiles holding this step's rows wait for the cache write
+    if (!waited && T.reads_new && T.key0 + (u + 1) * kSubKeys > T.L - T.nrows) {
       grid_dependency_wait();
       waited = true;
     }
@@ -213,6 +230,9 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
   uint32_t cphase = 0;  // (C / NST) & 1
 
   while (A.t >= 0) {
+    // Claim the task after tC now; the answer is needed only when A is done.
+    uint32_t claim = 0;
+    if (counter && tC < num_tasks && lane == 0) claim = atomicAdd(counter, 1u);
     // m: the reference max each head's sums are scaled to (log2 units); it is
     // only raised when a head's running max exceeds it by more than 2^8, so
     // exp2(x - m) <= 256 and the sums stay exact up to rounding.
@@ -405,7 +425,17 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     }
 
     // ---- advance: B becomes current, the task after it is expanded ----
-    const int next_t = B.t >= 0 ? B.t + stride : num_tasks;
+    const int next_t = tC < num_tasks ? tC : num_tasks;
+    int after = num_tasks;
+    if (next_t < num_tasks) {
+      if (counter) {
+        const uint32_t c = __shfl_sync(kFull, claim, 0);
+        after = c < static_cast<uint32_t>(num_tasks) ? 3 * stride + static_cast<int>(c) : num_tasks;
+        if (after > num_tasks) after = num_tasks;
+      } else {
+        after = next_t + stride;
+      }
+    }
     A = B;
     pa = pb;
     pb = 0;
@@ -425,123 +455,243 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     }
     qB_loaded = false;
     expand(B, next_t < num_tasks ? next_t : -1, rawC, a, lane);
-    if (next_t + stride < num_tasks) rawC = load_item(items, next_t + stride, hkv);
+    tC = after;
+    if (tC < num_tasks) rawC = load_item(items, tC, hkv);
     while (P - C < NST && issue_next()) {
     }
   }
 }
 
-// Span merge: one CTA of four warps per (row of a multi-span segment, q head). Worker
-// u of the CTA takes spans u, u + U, ... and columns (float4) lane % F. Each
-// worker loads up to kChunk spans at once and folds them into a running
-// (max, denominator, sum); the workers are then folded together in worker
-// order. The order of every addition is fixed, so the result is deterministic.
-template <int D>
-__global__ void __launch_bounds__(128) merge_kernel(const StepArgs a, const int32_t *__restrict__ items) {
-  constexpr int F = D / 4;          // float4 per output row
-  constexpr int PER_WARP = 32 / F;  // workers per warp
-  constexpr int U = 4 * PER_WARP;   // workers per CTA
-  constexpr int kChunk = 8;
-  __shared__ float4 s_acc[U][F];
-  __shared__ float s_m[U], s_l[U];
-  // The work item and step metadata are final when this grid starts (the
-  // decode kernel starts only after everything before the cache write has
-  // finished); only the partials need the decode grid to finish (the wait below).
+// Span merge. A row's result is fixed by its spans alone, whichever kernel
+// below merges it, so it never depends on the step around it:
+//   M   = the largest span max (exact), w_i = 2^(m_i - M) (0 for an empty span);
+//   per group g of 8 consecutive spans, from zero and in span order,
+//         L_g = sum l_i * w_i and A_g = sum acc_i * w_i (fused multiply-adds);
+//   L = sum_g L_g and A = sum_g A_g, added in group order from zero;
+//   out = bf16(A * (1 / L)).
+// merge_small_kernel spreads a row's groups over four adjacent lanes per
+// column (for the short steps, where merge latency is on the critical path);
+// merge_wide_kernel gives each thread all groups of its columns and stages
+// the spans' (max, denominator) pairs in shared memory (for steps with
+// thousands of merges). Both take one float4 of columns per thread.
+constexpr int kMergeThreads = 128;
+constexpr int kGroup = 8;   // spans per group
+constexpr int kPiece = 64;  // spans staged in shared memory at a time (a multiple of kGroup)
+
+struct MergeRow {
+  int row, spans, pbase, nrows;
+  bool bad;
+};
+
+// Decode a merge item and check it against the step metadata.
+__device__ __forceinline__ MergeRow merge_row(const StepArgs &a, const int32_t *items) {
   const int4 it = __ldg(reinterpret_cast<const int4 *>(items) + blockIdx.x);
   // word 2: spans | row index << 16 | (rows - 1) << 24; word 3: the partial
   // entry of (span 0, this row); span s of the row is entry word3 + s * rows.
-  const int seg = it.x, slot = it.y, pbase = it.w;
-  const int spans = it.z & 0xFFFF, ri = (it.z >> 16) & 0xFF, nrows = ((it.z >> 24) & 0xFF) + 1;
-  const int h = blockIdx.y;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  bool bad = seg < 0 || seg >= a.num_seqs || slot < 0 || slot >= a.max_slots || spans < 2 || pbase < 0 ||
-             ri >= nrows;
-  int row = 0;
-  if (!bad) {
+  MergeRow r;
+  const int seg = it.x, slot = it.y;
+  r.pbase = it.w;
+  r.spans = it.z & 0xFFFF;
+  const int ri = (it.z >> 16) & 0xFF;
+  r.nrows = ((it.z >> 24) & 0xFF) + 1;
+  r.row = 0;
+  r.bad = seg < 0 || seg >= a.num_seqs || slot < 0 || slot >= a.max_slots || r.spans < 2 || r.pbase < 0 ||
+          ri >= r.nrows;
+  if (!r.bad) {
     const int row0 = __ldg(a.cu_seqlens_q + seg);
     const int L = __ldg(a.context_lens + slot);
-    row = row0 + ri;
-    bad = __ldg(a.seq_slot + seg) != slot || __ldg(a.cu_seqlens_q + seg + 1) - row0 != nrows ||
-          (L + PKV_SPLIT_KEYS - 1) / PKV_SPLIT_KEYS != spans || row0 < 0 || row0 + nrows > a.total_q ||
-          nrows > L;
+    r.row = row0 + ri;
+    r.bad = __ldg(a.seq_slot + seg) != slot || __ldg(a.cu_seqlens_q + seg + 1) - row0 != r.nrows ||
+            (L + PKV_SPLIT_KEYS - 1) / PKV_SPLIT_KEYS != r.spans || row0 < 0 || row0 + r.nrows > a.total_q ||
+            r.nrows > L;
   }
+  return r;
+}
+
+__device__ __forceinline__ float span_weight(float m, float M) { return m == -INFINITY ? 0.f : exp2f(m - M); }
+
+__device__ __forceinline__ void fold_span(float &lg, float4 &ag, float l, const float4 &acc, float w) {
+  lg = __fmaf_rn(l, w, lg);
+  ag.x = __fmaf_rn(acc.x, w, ag.x);
+  ag.y = __fmaf_rn(acc.y, w, ag.y);
+  ag.z = __fmaf_rn(acc.z, w, ag.z);
+  ag.w = __fmaf_rn(acc.w, w, ag.w);
+}
+
+__device__ __forceinline__ void add_group(float &lt, float4 &at, float lg, const float4 &ag) {
+  lt = __fadd_rn(lt, lg);
+  at.x = __fadd_rn(at.x, ag.x);
+  at.y = __fadd_rn(at.y, ag.y);
+  at.z = __fadd_rn(at.z, ag.z);
+  at.w = __fadd_rn(at.w, ag.w);
+}
+
+template <int D>
+__device__ __forceinline__ void store_merged(const StepArgs &a, int row, int h, int col, float lt, const float4 &at) {
+  const float inv = 1.f / lt;
+  uint2 packed;
+  packed.x = pack_bf16x2(__fmul_rn(at.x, inv), __fmul_rn(at.y, inv));
+  packed.y = pack_bf16x2(__fmul_rn(at.z, inv), __fmul_rn(at.w, inv));
+  *reinterpret_cast<uint2 *>(reinterpret_cast<__nv_bfloat16 *>(a.out) +
+                             (static_cast<size_t>(row) * a.num_q_heads + h) * D + 4 * col) = packed;
+}
+
+// Four lanes per float4 column: lane w of a column folds groups w, w + 4,
+// ...; the column's maximum and its ordered group sums go across the four
+// lanes by shuffles. 128 threads hold D / 4 columns x 4 lanes of 128 / D q heads.
+template <int D>
+__global__ void __launch_bounds__(kMergeThreads) merge_small_kernel(const StepArgs a,
+                                                                    const int32_t *__restrict__ items) {
+  constexpr int F = D / 4;             // float4 columns per q head
+  constexpr int WPH = F / 8;           // warps per q head (8 columns per warp)
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = blockIdx.y * (kMergeThreads / (4 * F)) + warp / WPH;
+  const int col = (warp % WPH) * 8 + (lane >> 2), w = lane & 3;
+  // The work item and step metadata are final when this grid starts (the
+  // decode kernel starts only after everything before the cache write has
+  // finished); only the partials need the decode grid to finish (the wait below).
+  const MergeRow r = merge_row(a, items);
   grid_dependency_wait();  // partials come from the decode kernel
-  if (bad) {
+  if (r.bad) {
     if (threadIdx.x == 0 && a.status) atomicOr(a.status, PKV_DEV_BAD_SEGMENT);
     return;
   }
-  const int u = warp * PER_WARP + lane / F, d4 = lane % F;
-  const size_t hq = static_cast<size_t>(a.num_q_heads);
-  const size_t base = static_cast<size_t>(pbase) * hq + h;
-  const size_t span_stride = static_cast<size_t>(nrows) * hq;
+  if (h >= a.num_q_heads) return;  // whole warps
+  const int hq = a.num_q_heads;
+  const uint32_t stride = static_cast<uint32_t>(r.nrows) * hq;  // entries between spans
+  const size_t e0 = static_cast<size_t>(r.pbase) * hq + h;
+  const float2 *ml = reinterpret_cast<const float2 *>(a.partial_ml) + e0;
+  const float4 *acc = reinterpret_cast<const float4 *>(a.partial_acc + e0 * D) + col;
+  const int groups = (r.spans + kGroup - 1) / kGroup, rounds = (groups + 3) / 4;
 
-  float M = -INFINITY, lsum = 0.f;
-  float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int c0 = u; c0 < spans; c0 += U * kChunk) {
-    float mi[kChunk], li[kChunk];
-    float4 ai[kChunk];
+  float mi[kGroup], li[kGroup];
+  float4 ai[kGroup];
+  auto load_group = [&](int g) {
 #pragma unroll
-    for (int k = 0; k < kChunk; ++k) {
-      const int i = c0 + k * U;
+    for (int k = 0; k < kGroup; ++k) {
+      const int i = g * kGroup + k;
       mi[k] = -INFINITY;
       li[k] = 0.f;
-      ai[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (i < spans) {
-        const size_t p = base + static_cast<size_t>(i) * span_stride;
-        mi[k] = __ldg(a.partial_ml + p * 2);
-        li[k] = __ldg(a.partial_ml + p * 2 + 1);
-        ai[k] = __ldg(reinterpret_cast<const float4 *>(a.partial_acc + p * D) + d4);
+      if (i < r.spans) {
+        const float2 v = __ldg(ml + static_cast<size_t>(static_cast<uint32_t>(i) * stride));
+        mi[k] = v.x;
+        li[k] = v.y;
+        ai[k] = __ldg(acc + static_cast<size_t>(static_cast<uint32_t>(i) * stride) * F);
       }
     }
-    float cm = M;
+  };
+  float M = -INFINITY;
+  if (rounds == 1) {
+    load_group(w);
 #pragma unroll
-    for (int k = 0; k < kChunk; ++k) cm = fmaxf(cm, mi[k]);
-    const float corr = M == -INFINITY ? 0.f : exp2f(M - cm);
-    lsum *= corr;
-    o.x *= corr;
-    o.y *= corr;
-    o.z *= corr;
-    o.w *= corr;
-    M = cm;
+    for (int k = 0; k < kGroup; ++k) M = fmaxf(M, mi[k]);
+  } else {
+    for (int g = w; g < groups; g += 4)
 #pragma unroll
-    for (int k = 0; k < kChunk; ++k) {
-      const float w = mi[k] == -INFINITY ? 0.f : exp2f(mi[k] - M);
-      lsum += li[k] * w;
-      o.x += ai[k].x * w;
-      o.y += ai[k].y * w;
-      o.z += ai[k].z * w;
-      o.w += ai[k].w * w;
+      for (int k = 0; k < kGroup; ++k) {
+        const int i = g * kGroup + k;
+        if (i < r.spans) M = fmaxf(M, __ldg(ml + static_cast<size_t>(static_cast<uint32_t>(i) * stride)).x);
+      }
+  }
+  M = fmaxf(M, __shfl_xor_sync(kFull, M, 1));
+  M = fmaxf(M, __shfl_xor_sync(kFull, M, 2));
+
+  float lt = 0.f;
+  float4 at = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int rd = 0; rd < rounds; ++rd) {
+    const int g = rd * 4 + w;
+    if (rounds > 1) load_group(g);
+    float lg = 0.f;
+    float4 ag = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < kGroup; ++k)
+      if (g * kGroup + k < r.spans) fold_span(lg, ag, li[k], ai[k], span_weight(mi[k], M));
+    // groups 4 rd .. 4 rd + 3 in order, from the four lanes of this column
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int src = (lane & ~3) | j;
+      const float lj = __shfl_sync(kFull, lg, src);
+      float4 aj;
+      aj.x = __shfl_sync(kFull, ag.x, src);
+      aj.y = __shfl_sync(kFull, ag.y, src);
+      aj.z = __shfl_sync(kFull, ag.z, src);
+      aj.w = __shfl_sync(kFull, ag.w, src);
+      if (rd * 4 + j < groups) add_group(lt, at, lj, aj);
     }
   }
-  s_acc[u][d4] = o;
-  if (d4 == 0) {
-    s_m[u] = M;
-    s_l[u] = lsum;
+  if (w == 0) store_merged<D>(a, r.row, h, col, lt, at);
+}
+
+// One thread per float4 column; 128 threads hold 128 / (D / 4) q heads. The
+// CTA stages its heads' (max, denominator) pairs kPiece spans at a time in
+// shared memory; each thread reads the maxima from there, then folds its
+// groups in order, each group's eight sums loaded at once.
+template <int D>
+__global__ void __launch_bounds__(kMergeThreads) merge_wide_kernel(const StepArgs a,
+                                                                   const int32_t *__restrict__ items) {
+  constexpr int F = D / 4;                // float4 columns per q head
+  constexpr int HPC = kMergeThreads / F;  // q heads per CTA
+  __shared__ float s_m[HPC][kPiece], s_l[HPC][kPiece];
+  const int hl = static_cast<int>(threadIdx.x) / F, col = threadIdx.x % F;
+  const int h0 = blockIdx.y * HPC, h = h0 + hl;
+  const MergeRow r = merge_row(a, items);
+  grid_dependency_wait();  // partials come from the decode kernel
+  if (r.bad) {  // uniform over the CTA
+    if (threadIdx.x == 0 && a.status) atomicOr(a.status, PKV_DEV_BAD_SEGMENT);
+    return;
   }
-  __syncthreads();
-  if (threadIdx.x < F) {
-    float Mx = -INFINITY;
+  const int hq = a.num_q_heads;
+  const bool live = h < hq;
+  const uint32_t stride = static_cast<uint32_t>(r.nrows) * hq;
+  const float2 *ml = reinterpret_cast<const float2 *>(a.partial_ml) + static_cast<size_t>(r.pbase) * hq;
+  const float4 *acc =
+      reinterpret_cast<const float4 *>(a.partial_acc + (static_cast<size_t>(r.pbase) * hq + (live ? h : 0)) * D) +
+      col;
+  const int spans = r.spans;
+
+  float4 ai[kGroup];
+  auto load_sums = [&](int g) {
 #pragma unroll
-    for (int k = 0; k < U; ++k) Mx = fmaxf(Mx, s_m[k]);
-    float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
-    float L = 0.f;
-#pragma unroll
-    for (int k = 0; k < U; ++k) {
-      const float w = s_m[k] == -INFINITY ? 0.f : exp2f(s_m[k] - Mx);
-      const float4 t = s_acc[k][threadIdx.x];
-      r.x += t.x * w;
-      r.y += t.y * w;
-      r.z += t.z * w;
-      r.w += t.w * w;
-      L += s_l[k] * w;
+    for (int k = 0; k < kGroup; ++k) {
+      const int i = g * kGroup + k;
+      if (live && i < spans) ai[k] = __ldg(acc + static_cast<size_t>(static_cast<uint32_t>(i) * stride) * F);
     }
-    const float inv = 1.f / L;
-    uint2 packed;
-    packed.x = pack_bf16x2(r.x * inv, r.y * inv);
-    packed.y = pack_bf16x2(r.z * inv, r.w * inv);
-    *reinterpret_cast<uint2 *>(reinterpret_cast<__nv_bfloat16 *>(a.out) + (static_cast<size_t>(row) * hq + h) * D +
-                               4 * threadIdx.x) = packed;
+  };
+  auto stage = [&](int p0, int n) {  // (max, denominator) of spans p0 .. p0 + n - 1 of the CTA's heads
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < HPC * n; idx += kMergeThreads) {
+      const int hh = idx / n, i = idx % n;
+      float2 v = make_float2(-INFINITY, 0.f);
+      if (h0 + hh < hq) v = __ldg(ml + static_cast<size_t>(static_cast<uint32_t>(p0 + i) * stride) + h0 + hh);
+      s_m[hh][i] = v.x;
+      s_l[hh][i] = v.y;
+    }
+    __syncthreads();
+  };
+  load_sums(0);  // the first group's sums do not depend on the maxima
+  float M = -INFINITY;
+  for (int p0 = 0; p0 < spans; p0 += kPiece) {
+    const int n = min(kPiece, spans - p0);
+    stage(p0, n);
+    for (int i = 0; i < n; ++i) M = fmaxf(M, s_m[hl][i]);
   }
+  float lt = 0.f;
+  float4 at = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int p0 = 0; p0 < spans; p0 += kPiece) {
+    const int n = min(kPiece, spans - p0);
+    if (spans > kPiece) stage(p0, n);  // otherwise still staged from the max pass
+    for (int c0 = 0; c0 < n; c0 += kGroup) {
+      const int g = (p0 + c0) / kGroup;
+      if (g > 0) load_sums(g);
+      float lg = 0.f;
+      float4 ag = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int k = 0; k < kGroup; ++k)
+        if (c0 + k < n) fold_span(lg, ag, s_l[hl][c0 + k], ai[k], span_weight(s_m[hl][c0 + k], M));
+      add_group(lt, at, lg, ag);
+    }
+  }
+  if (live) store_merged<D>(a, r.row, h, col, lt, at);
 }
 
 int sm_count() {
@@ -557,22 +707,47 @@ int sm_count() {
   return count[dev];
 }
 
-template <int D, int NT, bool MULTI>
+template <int D, int NT, bool MULTI, int NW = kWarps, int NS = 0>
 cudaError_t launch_decode_t(const StepArgs &a, const CUtensorMap &tk, const CUtensorMap &tv, int32_t num_items,
                             const int32_t *items, cudaStream_t stream) {
-  constexpr int smem = DecodeCfg<D>::kSmem;
+  constexpr int smem = DecodeCfg<D, NW, NS>::kSmem;
   static uint64_t configured = 0;  // one bit per device
   int dev = 0;
   cudaGetDevice(&dev);
   const uint64_t bit = 1ull << (dev & 63);
   if (!(configured & bit)) {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, NT, MULTI>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e =
+        cudaFuncSetAttribute(decode_kernel<D, NT, MULTI, NW, NS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     configured |= bit;
   }
   const int64_t tasks = static_cast<int64_t>(num_items) * a.num_kv_heads;
   const int grid = static_cast<int>(tasks < sm_count() ? tasks : sm_count());
-  return launch_pdl(decode_kernel<D, NT, MULTI>, dim3(grid), dim3(kWarps * 32), smem, stream, tk, tv, a, items, num_items);
+  // Past three static rounds, warps take tasks from the workspace counter, so
+  // SMs that stream faster take more and all finish together.
+  StepArgs b = a;
+  if (b.task_counter && tasks > 3ll * grid * NW) {
+    const cudaError_t e = cudaMemsetAsync(b.task_counter, 0, sizeof(uint32_t), stream);
+    if (e != cudaSuccess) return e;
+  } else {
+    b.task_counter = nullptr;
+  }
+  return launch_pdl(decode_kernel<D, NT, MULTI, NW, NS>, dim3(grid), dim3(NW * 32), smem, stream, tk, tv, b, items,
+                    num_items);
+}
+
+// Single-row decode at head_dim 128: with at most 4, 5 or 6 tasks per SM,
+// 4 warps x 6 stages, 5 x 5 or 6 x 4 (192-200 KiB of rings) keep more bytes
+// in flight per busy warp than 8 x 3.
+template <int NT>
+cudaError_t launch_decode_128(const StepArgs &a, const CUtensorMap &tk, const CUtensorMap &tv, int32_t num_items,
+                              const int32_t *items, cudaStream_t stream) {
+  const int64_t tasks = static_cast<int64_t>(num_items) * a.num_kv_heads;
+  const int64_t per_sm = (tasks + sm_count() - 1) / sm_count();
+  if (per_sm <= 4) return launch_decode_t<128, NT, false, 4, 6>(a, tk, tv, num_items, items, stream);
+  if (per_sm == 5) return launch_decode_t<128, NT, false, 5, 5>(a, tk, tv, num_items, items, stream);
+  if (per_sm == 6) return launch_decode_t<128, NT, false, 6, 4>(a, tk, tv, num_items, items, stream);
+  return launch_decode_t<128, NT, false>(a, tk, tv, num_items, items, stream);
 }
 
 }  // namespace
@@ -589,18 +764,29 @@ cudaError_t launch_decode(const StepArgs &a, const CUtensorMap &tk, const CUtens
     case 1: return launch_decode_t<64, 1, true>(a, tk, tv, num_items, items, stream);
     case 2: return launch_decode_t<64, 2, false>(a, tk, tv, num_items, items, stream);
     case 3: return launch_decode_t<64, 2, true>(a, tk, tv, num_items, items, stream);
-    case 4: return launch_decode_t<128, 1, false>(a, tk, tv, num_items, items, stream);
+    case 4: return launch_decode_128<1>(a, tk, tv, num_items, items, stream);
     case 5: return launch_decode_t<128, 1, true>(a, tk, tv, num_items, items, stream);
-    case 6: return launch_decode_t<128, 2, false>(a, tk, tv, num_items, items, stream);
+    case 6: return launch_decode_128<2>(a, tk, tv, num_items, items, stream);
     default: return launch_decode_t<128, 2, true>(a, tk, tv, num_items, items, stream);
   }
 }
 
 cudaError_t launch_merge(const StepArgs &a, int32_t num_items, const int32_t *items, cudaStream_t stream) {
   if (num_items <= 0) return cudaSuccess;
-  const dim3 grid(static_cast<unsigned>(num_items), static_cast<unsigned>(a.num_q_heads));
-  if (a.head_dim == 128) return launch_pdl(merge_kernel<128>, grid, dim3(128), 0, stream, a, items);
-  return launch_pdl(merge_kernel<64>, grid, dim3(128), 0, stream, a, items);
+  const int f = a.head_dim / 4;  // float4 columns per q head
+  const dim3 block(kMergeThreads);
+  // Four lanes per column while that fits about one wave of CTAs, else one.
+  const int64_t small_ctas = static_cast<int64_t>(num_items) * ((a.num_q_heads * 4 * f + kMergeThreads - 1) / kMergeThreads);
+  if (small_ctas <= 2ll * sm_count()) {
+    const int hpc = kMergeThreads / (4 * f);
+    const dim3 grid(static_cast<unsigned>(num_items), static_cast<unsigned>((a.num_q_heads + hpc - 1) / hpc));
+    if (a.head_dim == 128) return launch_pdl(merge_small_kernel<128>, grid, block, 0, stream, a, items);
+    return launch_pdl(merge_small_kernel<64>, grid, block, 0, stream, a, items);
+  }
+  const int hpc = kMergeThreads / f;
+  const dim3 grid(static_cast<unsigned>(num_items), static_cast<unsigned>((a.num_q_heads + hpc - 1) / hpc));
+  if (a.head_dim == 128) return launch_pdl(merge_wide_kernel<128>, grid, block, 0, stream, a, items);
+  return launch_pdl(merge_wide_kernel<64>, grid, block, 0, stream, a, items);
 }
 
 }  // namespace pkv

@@ -22,6 +22,7 @@
 #include <vector>
 
 #include "pkv.h"
+#include "pkv_internal.h"
 
 namespace {
 
@@ -416,6 +417,7 @@ pkv_status pkv_plan_work(const int32_t *cu, int32_t num_seqs, const int32_t *seq
   auto by_cost = [](const Item &a, const Item &b) { return a.cost > b.cost; };
   std::stable_sort(dec.begin(), dec.end(), by_cost);
   std::stable_sort(pre.begin(), pre.end(), by_cost);
+  std::stable_sort(comb.begin(), comb.end(), by_cost);  // long merges start first
 
   info->num_decode_items = static_cast<int32_t>(dec.size());
   info->num_prefill_items = static_cast<int32_t>(pre.size());
@@ -427,10 +429,11 @@ pkv_status pkv_plan_work(const int32_t *cu, int32_t num_seqs, const int32_t *seq
   const int64_t items = static_cast<int64_t>(dec.size() + pre.size() + comb.size() + scr.size());
   info->work_words = items * PKV_WORK_WORDS_PER_ITEM;
   auto align256 = [](uint64_t x) { return (x + 255) & ~uint64_t(255); };
+  // span partials (sums, then max and denominator), then the decode kernel's task counter
   info->workspace_bytes =
       partials == 0 ? 0
                     : align256(uint64_t(partials) * num_q_heads * head_dim * 4) +
-                          align256(uint64_t(partials) * num_q_heads * 2 * 4);
+                          align256(uint64_t(partials) * num_q_heads * 2 * 4) + pkv::kCounterBytes;
   info->workspace_bytes_q8 =
       info->workspace_bytes +
       (scratch_blocks == 0 ? 0

@@ -31,7 +31,14 @@ struct StepArgs {
   float *partial_acc;  // [num_partials][Hq][D]
   float *partial_ml;   // [num_partials][Hq][2]  (running max in log2 units, sum)
   uint32_t *status;
+  // Workspace word the decode kernel hands out tasks from past its first
+  // three static rounds (nullptr: every task is assigned statically). The
+  // launch zeroes it on the stream first.
+  uint32_t *task_counter;
 };
+
+// Bytes of workspace after the span partials: the decode kernel's task counter.
+constexpr uint64_t kCounterBytes = 256;
 
 cudaError_t launch_cache_write(const void *k_new, const void *v_new, const int64_t *slot_mapping,
                                int64_t num_tokens, void *k_pool, void *v_pool, int64_t num_blocks,
@@ -45,7 +52,7 @@ cudaError_t launch_copy_blocks(const int32_t *pairs, int64_t num_pairs, void *co
 cudaError_t launch_decode(const StepArgs &a, const CUtensorMap &tmap_k, const CUtensorMap &tmap_v,
                           int32_t num_items, const int32_t *items, cudaStream_t stream);
 
-// One CTA per (row of a multi-span segment, q head): merges that row's span partials.
+// One CTA per (row of a multi-span segment, group of q heads): merges that row's span partials.
 cudaError_t launch_merge(const StepArgs &a, int32_t num_items, const int32_t *items, cudaStream_t stream);
 
 // 8-bit block-scaled pool: quantising cache write, decode over the codes, and

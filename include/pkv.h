@@ -331,9 +331,11 @@ pkv_status pkv_cache_write(const void *k_new, const void *v_new, const int64_t *
  * output rounded to bf16 (nearest even). Results are deterministic and do
  * not depend on the other segments in the step or on their order.
  * `workspace` (device, >= info->workspace_bytes, 256-byte aligned) holds the
- * key-span partial results between the decode kernel and the merge kernel;
- * it needs no initialisation. Calls that share a workspace must not overlap
- * on the GPU. The pool must already hold this step's rows (pkv_cache_write
+ * key-span partial results between the decode kernel and the merge kernel,
+ * then the decode kernel's task counter (the last 256 bytes); it needs no
+ * initialisation: on steps with more decode tasks than three per warp the
+ * call zeroes the counter on `stream` (cudaMemsetAsync) before the decode
+ * kernel. Calls that share a workspace must not overlap on the GPU. The pool must already hold this step's rows (pkv_cache_write
  * first, same stream). The kernels are launched with programmatic dependent
  * launch, so they may start while the previous kernel in the stream drains.
  * The decode kernel reads the step metadata, q and the cached history at

@@ -194,6 +194,28 @@ def test_batch_of_one_equals_in_batch():
         np.testing.assert_array_equal(_gpu_out(one), full[seg.slot])
 
 
+@pytest.mark.parametrize("heads,d", [((16, 2), 64), ((8, 1), 128)])
+def test_merge_kernels_agree_bit_for_bit(heads, d):
+    """A step of many split rows is merged by the many-row kernel; the same rows in a step of their
+    own are merged by the few-row kernel. Both follow one fixed order of operations, so the rows
+    must come out bit-identical -- also for rows of more than 32 spans (several rounds per lane)
+    and of more than 64 spans (several shared-memory pieces)."""
+    hq, hkv = heads
+    ctxs = [int(c) for c in np.random.default_rng(31).integers(300, 2500, 44)] + [9000, 17000, 20001, 513]
+    shapes = [(1, c) for c in ctxs]
+    w = W.random_step(31, shapes, num_q_heads=hq, num_kv_heads=hkv, head_dim=d)
+    _, got_full, _ = run_and_check(w)
+    full = _out_rows(w, got_full)
+    pick = [44, 45, 46, 3]
+    sub = W.random_step(31, shapes, num_q_heads=hq, num_kv_heads=hkv, head_dim=d)
+    sub.segments = [w.segments[i] for i in pick]
+    sub.q = np.concatenate([w.q[i:i + 1] for i in pick])  # one row per segment, in packed order
+    got = _out_rows(sub, _gpu_out(sub))
+    for i in pick:
+        slot = w.segments[i].slot
+        np.testing.assert_array_equal(got[slot], full[slot])
+
+
 def test_slot_reuse_leaves_other_slots_bit_identical():
     """B retires; a new sequence D takes B's slot and blocks. A's and C's pool rows and outputs stay."""
     import torch

@@ -292,7 +292,7 @@ def test_work_list_items():
     assert (pre[:, 3] == 2).all()
     assert pre[0, 2] == 14  # the pair that sees the most keys first
     a256 = lambda x: (x + 255) // 256 * 256
-    assert info.workspace_bytes == a256(5 * 32 * 128 * 4) + a256(5 * 32 * 2 * 4)
+    assert info.workspace_bytes == a256(5 * 32 * 128 * 4) + a256(5 * 32 * 2 * 4) + 256  # + the task counter
     assert info.workspace_bytes_q8 == info.workspace_bytes + 2 * a256(96 * 8 * 16 * 128 * 2) + a256(8 * 128 * 4)
 
 
