@@ -332,6 +332,7 @@ pkv_status pkv_attention_q8(const void *q, const int32_t *cu_seqlens_q, int32_t 
   a.partial_acc = info->num_partials ? reinterpret_cast<float *>(ws) : nullptr;
   a.partial_ml = info->num_partials ? reinterpret_cast<float *>(ws + acc_bytes) : nullptr;
   a.status = device_status;
+  a.task_counter = info->num_partials ? reinterpret_cast<uint32_t *>(ws + acc_bytes + ml_bytes) : nullptr;
 
   // The chunk kernel reads a bf16 scratch pool: the chunk segments' histories,
   // widened block by block, with a scratch block table in the same shape.

@@ -309,14 +309,19 @@ __global__ void __launch_bounds__(kWarpsQ8 * 32, 1)
   __syncwarp();
   bool waited = false;  // rows written by the kernel before (this step's) are read after its wait
 
+  // Tasks as in the bf16 decode kernel: three static rounds, then (with a
+  // task counter) 3 stride + the counter's next value. A current, B
+  // expanded, tC the task whose work item is in rawC.
+  uint32_t *const counter = a.task_counter;
   Task A, B;
   int4 rawC = make_int4(0, 0, 0, 0);
   expand(A, t0, load_item(items, t0, hkv), a, lane);
+  int tC;
   {
     const int t1 = t0 + stride;
     expand(B, t1 < num_tasks ? t1 : -1, t1 < num_tasks ? load_item(items, t1, hkv) : rawC, a, lane);
-    const int t2 = t1 + stride;
-    if (t2 < num_tasks) rawC = load_item(items, t2, hkv);
+    tC = t1 + stride;
+    if (tC < num_tasks) rawC = load_item(items, tC, hkv);
   }
   finalize(A, a, lane, 8 * NT, kMaxRows);
   uint32_t qA[NT][KT][2], qB[NT][KT][2];
@@ -327,7 +332,8 @@ __global__ void __launch_bounds__(kWarpsQ8 * 32, 1)
   int P = 0, C = 0, pa = 0, pb = 0;
   int pstage = 0;
   auto issue = [&](const Task &T, int u) {
-    if (T.reads_new && !waited) {
+    // only the sub-tiles holding this step's rows wait for the cache write
+    if (!waited && T.reads_new && T.key0 + (u + 1) * kSubKeys > T.L - T.nrows) {
       grid_dependency_wait();
       waited = true;
     }
@@ -382,6 +388,9 @@ __global__ void __launch_bounds__(kWarpsQ8 * 32, 1)
   uint32_t cphase = 0;
 
   while (A.t >= 0) {
+    // Claim the task after tC now; the answer is needed only when A is done.
+    uint32_t claim = 0;
+    if (counter && tC < num_tasks && lane == 0) claim = atomicAdd(counter, 1u);
     float m[NT][2], l[NT][2], acc[NT][KT][4];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
@@ -608,7 +617,17 @@ __global__ void __launch_bounds__(kWarpsQ8 * 32, 1)
     }
 
     // ---- advance: B becomes current, the task after it is expanded ----
-    const int next_t = B.t >= 0 ? B.t + stride : num_tasks;
+    const int next_t = tC < num_tasks ? tC : num_tasks;
+    int after = num_tasks;
+    if (next_t < num_tasks) {
+      if (counter) {
+        const uint32_t c = __shfl_sync(kAll, claim, 0);
+        after = c < static_cast<uint32_t>(num_tasks) ? 3 * stride + static_cast<int>(c) : num_tasks;
+        if (after > num_tasks) after = num_tasks;
+      } else {
+        after = next_t + stride;
+      }
+    }
     A = B;
     pa = pb;
     pb = 0;
@@ -630,7 +649,8 @@ __global__ void __launch_bounds__(kWarpsQ8 * 32, 1)
     }
     qB_loaded = false;
     expand(B, next_t < num_tasks ? next_t : -1, rawC, a, lane);
-    if (next_t + stride < num_tasks) rawC = load_item(items, next_t + stride, hkv);
+    tC = after;
+    if (tC < num_tasks) rawC = load_item(items, tC, hkv);
     while (P - C < NST && issue_next()) {
     }
   }
@@ -655,7 +675,14 @@ cudaError_t launch_decode_q8_t(const StepArgs &a, const CUtensorMap &tk, const C
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = 148;
   const int64_t tasks = static_cast<int64_t>(num_items) * a.num_kv_heads;
   const int grid = static_cast<int>(tasks < sms ? tasks : sms);
-  return launch_pdl(decode_q8_kernel<D, NT, MULTI>, dim3(grid), dim3(kWarpsQ8 * 32), smem, stream, tk, tv, a,
+  StepArgs b = a;  // past three static rounds, tasks come from the workspace counter
+  if (b.task_counter && tasks > 3ll * grid * kWarpsQ8) {
+    const cudaError_t e = cudaMemsetAsync(b.task_counter, 0, sizeof(uint32_t), stream);
+    if (e != cudaSuccess) return e;
+  } else {
+    b.task_counter = nullptr;
+  }
+  return launch_pdl(decode_q8_kernel<D, NT, MULTI>, dim3(grid), dim3(kWarpsQ8 * 32), smem, stream, tk, tv, b,
                     static_cast<const __nv_bfloat16 *>(k_scales), static_cast<const __nv_bfloat16 *>(v_scales),
                     items, num_items);
 }
