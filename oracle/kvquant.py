@@ -1,4 +1,4 @@
-"""Oracle for the 8-bit block-scaled KV pool -- TEST INFRASTRUCTURE.
+"""Oracle for the 8-bit and 4-bit block-scaled KV pools -- TEST INFRASTRUCTURE.
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline
 leg may import this module; the CUDA library never calls it and shares no code
@@ -7,22 +7,26 @@ with it.
 The pages run their KV caches quantised (Lucebox, "Continuous batching ...",
 §DeepSeek V4 Flash on Strix Halo and two GPUs: 4-bit KV; §Qwen3.8-27B DFlash2
 on the R9700 (vs llama.cpp): 8-bit KV) but do not define the formats. The
-reading taken here is the plainest 8-bit block-scaled one:
+reading taken here is the plainest block-scaled one, with B bits per code and
+Q = 2^(B-1) - 1 (127 for 8 bits, 7 for 4 bits):
 
 * each pool row (one token, one kv head, head_dim values) is cut into groups
   of 32 consecutive values;
 * a group stores one power-of-two scale ``d`` (kept as a bfloat16, which
-  holds it exactly) and 32 signed 8-bit codes in [-127, 127]; the value a
-  code stands for is ``code * d``;
+  holds it exactly) and 32 signed codes in [-Q, Q]; the value a code stands
+  for is ``code * d``;
 * quantising a group of bfloat16 values ``x`` (all steps in float32, the
   precision the codes are decided in):
-    amax = max |x|;  t = amax / 127;  d = the smallest power of two >= t
+    amax = max |x|;  t = amax / Q;  d = the smallest power of two >= t
     (at least 2^-126; 0 when amax is 0);
-    code = clamp(round_half_even(x / d), -127, 127), or 0 when d is 0.
+    code = clamp(round_half_even(x / d), -Q, Q), or 0 when d is 0.
   A power-of-two scale is the shared-exponent choice of the OCP microscaling
   formats: x / d is exact, |x - code * d| <= d / 2, and every value a code
-  stands for is exactly a bfloat16 number (7 significant bits times a power
-  of two), so attention may widen codes to bfloat16 without rounding.
+  stands for is exactly a bfloat16 number (at most 7 significant bits times a
+  power of two), so attention may widen codes to bfloat16 without rounding.
+* storage: 8-bit codes one per byte; 4-bit codes two per byte, the code of
+  the even value in the low nibble, each a 4-bit two's complement number
+  (``pack_nibbles``). Scales are stored as in the 8-bit pool.
 
 Attention over such a pool is ordinary causal grouped-query attention over the
 dequantised values ``code * d`` (exact in double), computed here in float64
@@ -34,7 +38,13 @@ from __future__ import annotations
 import numpy as np
 
 GROUP = 32  # values per scale
-CODE_MAX = 127
+CODE_MAX = 127  # 8-bit codes
+
+
+def code_max(bits: int) -> int:
+    if bits not in (8, 4):
+        raise ValueError(f"{bits}-bit codes are not a format of this pool")
+    return (1 << (bits - 1)) - 1
 
 
 def _widen(bits) -> np.ndarray:
@@ -51,20 +61,21 @@ def _pow2_ceil(t) -> np.ndarray:
     return np.where(b == 0, np.uint32(0), up).astype(np.uint32)
 
 
-def quantize(x_bits):
-    """bf16 bits ``[..., D]`` -> (codes int8 ``[..., D]``, scale bits uint16 ``[..., D / 32]``)."""
+def quantize(x_bits, bits: int = 8):
+    """bf16 bits ``[..., D]`` -> (codes int8 ``[..., D]`` in [-Q, Q], scale bits uint16 ``[..., D / 32]``)."""
+    q = code_max(bits)
     x = _widen(x_bits)
     d_len = x.shape[-1]
     if d_len % GROUP:
         raise ValueError(f"head_dim {d_len} is not a multiple of {GROUP}")
     g = x.reshape(*x.shape[:-1], d_len // GROUP, GROUP)
     amax = np.abs(g).max(axis=-1)
-    d32 = _pow2_ceil((amax / np.float32(CODE_MAX)).astype(np.float32))
+    d32 = _pow2_ceil((amax / np.float32(q)).astype(np.float32))
     d_bits = (d32 >> 16).astype(np.uint16)  # a power of two: its bfloat16 is exact
     df = _widen(d_bits)[..., None]
     safe = np.where(df > 0, df, np.float32(1))
     r = np.where(df > 0, g / safe, np.float32(0)).astype(np.float32)
-    codes = np.clip(np.rint(r), -CODE_MAX, CODE_MAX).astype(np.int8)
+    codes = np.clip(np.rint(r), -q, q).astype(np.int8)
     return codes.reshape(x.shape), d_bits
 
 
@@ -76,21 +87,38 @@ def dequantize(codes, scale_bits) -> np.ndarray:
     return (g * s[..., None]).reshape(c.shape)
 
 
-def empty_pool(num_blocks, num_kv_heads, block_size, head_dim):
-    """(codes, scales) pools filled with a recognisable pattern for rows never written."""
-    codes = np.full((num_blocks, num_kv_heads, block_size, head_dim), -128, np.int8)
+def pack_nibbles(codes) -> np.ndarray:
+    """4-bit storage of codes in [-8, 7] ``[..., D]``: uint8 ``[..., D / 2]``, even value in the low nibble."""
+    c = np.asarray(codes, dtype=np.int8).astype(np.int16) & 0xF
+    return (c[..., 0::2] | (c[..., 1::2] << 4)).astype(np.uint8)
+
+
+def unpack_nibbles(packed) -> np.ndarray:
+    """Inverse of ``pack_nibbles``: int8 codes ``[..., 2 * D2]``."""
+    p = np.asarray(packed, dtype=np.uint8).astype(np.int16)
+    lo, hi = p & 0xF, p >> 4
+    out = np.empty(p.shape[:-1] + (2 * p.shape[-1],), np.int16)
+    out[..., 0::2], out[..., 1::2] = lo, hi
+    return np.where(out >= 8, out - 16, out).astype(np.int8)
+
+
+def empty_pool(num_blocks, num_kv_heads, block_size, head_dim, bits: int = 8):
+    """(codes, scales) pools filled with a recognisable pattern for rows never written.
+
+    Codes are kept one per int8 here; the unused code -2^(B-1) marks rows never written."""
+    codes = np.full((num_blocks, num_kv_heads, block_size, head_dim), -(code_max(bits) + 1), np.int8)
     scales = np.full((num_blocks, num_kv_heads, block_size, head_dim // GROUP), 0x7FC1, np.uint16)  # NaN
     return codes, scales
 
 
-def cache_write(k_codes, k_scales, v_codes, v_scales, k_new, v_new, mapping) -> None:
+def cache_write(k_codes, k_scales, v_codes, v_scales, k_new, v_new, mapping, bits: int = 8) -> None:
     """Quantise new rows ``[T, Hkv, D]`` (bf16 bits) into the pools at pool rows ``mapping`` (< 0: skip)."""
     nb, hkv, bs, d = k_codes.shape
     mapping = np.asarray(mapping, dtype=np.int64)
     if np.any(mapping >= nb * bs):
         raise ValueError("slot mapping past the pool")
-    kq, ks = quantize(k_new)
-    vq, vs = quantize(v_new)
+    kq, ks = quantize(k_new, bits)
+    vq, vs = quantize(v_new, bits)
     for t, s in enumerate(mapping):
         if s < 0:
             continue
