@@ -189,18 +189,19 @@ __global__ void __launch_bounds__(256) widen_q8_kernel(const StepArgs a, const i
 
 // ---- split-KV decode over the codes ---------------------------------------------
 
-template <int D>
+// NW warps per CTA (the ring depth follows from the shared memory they share).
+template <int D, int NW>
 struct Q8Cfg {
   static constexpr int kGroups = D / 32;
   static constexpr int kCodeBytes = kSubKeys * D;              // K (or V) codes of one sub-tile
   static constexpr int kScaleBytes = kSubKeys * kGroups * 2;   // their scales
-  static constexpr int kStages = D == 128 ? 6 : 12;
+  static constexpr int kStages = (D == 128 ? 48 : 96) / NW;  // 6 or 12 at eight warps
   static constexpr int kVc = kStages * kCodeBytes;             // offsets inside a warp's ring
   static constexpr int kKs = 2 * kStages * kCodeBytes;
   static constexpr int kVs = kKs + kStages * kScaleBytes;
   static constexpr int kWarpRing = ((kVs + kStages * kScaleBytes) + 1023) / 1024 * 1024;
   static constexpr int kStageTx = 2 * kCodeBytes + 2 * kScaleBytes;
-  static constexpr int kSmem = kWarpsQ8 * kWarpRing + kWarpsQ8 * kStages * 8 + 1024;
+  static constexpr int kSmem = NW * kWarpRing + NW * kStages * 8 + 1024;
   static_assert(kSmem <= 232448, "decode ring exceeds shared memory");
 };
 
@@ -278,12 +279,12 @@ __device__ __forceinline__ void load_q_q8(uint32_t (&qf)[NT][D / 16][2], float (
   }
 }
 
-template <int D, int NT, bool MULTI>
-__global__ void __launch_bounds__(kWarpsQ8 * 32, 1)
+template <int D, int NT, bool MULTI, int NW>
+__global__ void __launch_bounds__(NW * 32, 1)
     decode_q8_kernel(const __grid_constant__ CUtensorMap tmap_kc, const __grid_constant__ CUtensorMap tmap_vc,
                      const StepArgs a, const __nv_bfloat16 *__restrict__ k_scales,
                      const __nv_bfloat16 *__restrict__ v_scales, const int32_t *__restrict__ items, int num_items) {
-  using Cfg = Q8Cfg<D>;
+  using Cfg = Q8Cfg<D, NW>;
   constexpr int KT = D / 16;  // k-steps of QK^T, m-tiles of PV
   constexpr int NG = Cfg::kGroups;
   constexpr int NST = Cfg::kStages;
@@ -292,12 +293,12 @@ __global__ void __launch_bounds__(kWarpsQ8 * 32, 1)
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint8_t *ring = smem + warp * Cfg::kWarpRing;
-  uint64_t *full = reinterpret_cast<uint64_t *>(smem + kWarpsQ8 * Cfg::kWarpRing) + warp * NST;
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + NW * Cfg::kWarpRing) + warp * NST;
 
   launch_dependents();  // the span merge may launch now; it waits for this grid before reading
   const int hkv = a.num_kv_heads;
   const int num_tasks = num_items * hkv;
-  const int stride = gridDim.x * kWarpsQ8;
+  const int stride = gridDim.x * NW;
   const int t0 = warp * gridDim.x + blockIdx.x;
   if (t0 >= num_tasks) return;
   if (lane == 0) {
@@ -656,35 +657,53 @@ __global__ void __launch_bounds__(kWarpsQ8 * 32, 1)
   }
 }
 
-template <int D, int NT, bool MULTI>
-cudaError_t launch_decode_q8_t(const StepArgs &a, const CUtensorMap &tk, const CUtensorMap &tv,
+template <int D, int NT, bool MULTI, int NW>
+cudaError_t launch_decode_q8_w(const StepArgs &a, const CUtensorMap &tk, const CUtensorMap &tv,
                                const void *k_scales, const void *v_scales, int32_t num_items, const int32_t *items,
-                               cudaStream_t stream) {
-  constexpr int smem = Q8Cfg<D>::kSmem;
+                               int grid, cudaStream_t stream) {
+  constexpr int smem = Q8Cfg<D, NW>::kSmem;
   static uint64_t configured = 0;  // one bit per device
   int dev = 0;
   cudaGetDevice(&dev);
   const uint64_t bit = 1ull << (dev & 63);
   if (!(configured & bit)) {
     cudaError_t e =
-        cudaFuncSetAttribute(decode_q8_kernel<D, NT, MULTI>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        cudaFuncSetAttribute(decode_q8_kernel<D, NT, MULTI, NW>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     configured |= bit;
   }
-  int sms = 0;
-  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = 148;
   const int64_t tasks = static_cast<int64_t>(num_items) * a.num_kv_heads;
-  const int grid = static_cast<int>(tasks < sms ? tasks : sms);
   StepArgs b = a;  // past three static rounds, tasks come from the workspace counter
-  if (b.task_counter && tasks > 3ll * grid * kWarpsQ8) {
+  if (b.task_counter && tasks > 3ll * grid * NW) {
     const cudaError_t e = cudaMemsetAsync(b.task_counter, 0, sizeof(uint32_t), stream);
     if (e != cudaSuccess) return e;
   } else {
     b.task_counter = nullptr;
   }
-  return launch_pdl(decode_q8_kernel<D, NT, MULTI>, dim3(grid), dim3(kWarpsQ8 * 32), smem, stream, tk, tv, b,
+  return launch_pdl(decode_q8_kernel<D, NT, MULTI, NW>, dim3(grid), dim3(NW * 32), smem, stream, tk, tv, b,
                     static_cast<const __nv_bfloat16 *>(k_scales), static_cast<const __nv_bfloat16 *>(v_scales),
                     items, num_items);
+}
+
+// Eight warps x six stages (head_dim 128); single-row, single-tile steps with
+// more than three rounds of tasks run 12 warps x 4 stages instead: the code
+// conversions make a warp's sub-tile a long dependent chain, and more warps
+// per scheduler hide it once every warp has work (a small step's few busy
+// warps stream faster through deeper rings).
+template <int D, int NT, bool MULTI>
+cudaError_t launch_decode_q8_t(const StepArgs &a, const CUtensorMap &tk, const CUtensorMap &tv,
+                               const void *k_scales, const void *v_scales, int32_t num_items, const int32_t *items,
+                               cudaStream_t stream) {
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = 148;
+  const int64_t tasks = static_cast<int64_t>(num_items) * a.num_kv_heads;
+  const int grid = static_cast<int>(tasks < sms ? tasks : sms);
+  if constexpr (D == 128 && NT == 1 && !MULTI) {
+    if (tasks > 3ll * grid * 12)
+      return launch_decode_q8_w<D, NT, MULTI, 12>(a, tk, tv, k_scales, v_scales, num_items, items, grid, stream);
+  }
+  return launch_decode_q8_w<D, NT, MULTI, kWarpsQ8>(a, tk, tv, k_scales, v_scales, num_items, items, grid, stream);
 }
 
 }  // namespace

@@ -138,3 +138,11 @@ def test_mixed_step_q8():
     w = W.make_step("mixed", 0, pool_blocks=4096)
     rows = sorted({0, 1, 255, 256, 511, *range(512, w.total_q)})
     _run(w, rows=rows)
+
+
+def test_many_rows_q8():
+    """A step with more than three rounds of decode tasks per warp: the 12-warp kernel and the task counter."""
+    ctxs = [int(c) for c in np.random.default_rng(41).integers(1500, 2600, 360)]
+    w = W.random_step(41, [(1, c) for c in ctxs], num_q_heads=16, num_kv_heads=2, head_dim=128)
+    rows = sorted({0, 1, 2, 100, 200, 358, 359})
+    _run(w, rows=rows)
