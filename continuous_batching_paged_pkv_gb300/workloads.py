@@ -281,6 +281,8 @@ class Request:
     prompt_len: int
     output_len: int
     priority: int = 0  # higher is more urgent
+    prefix_id: int = -1  # requests with the same prefix_id share their first prefix_len prompt tokens
+    prefix_len: int = 0
 
 
 @dataclass(frozen=True)
@@ -298,21 +300,35 @@ class ChurnSpec:
     num_blocks: int = 131072
     max_slots: int = 64
     high_priority: float = 0.0  # fraction of requests with priority 1 (the rest 0)
+    prefix_groups: int = 0      # distinct shared prompt prefixes (0: none)
+    prefix_share: float = 0.0   # fraction of requests whose prompt starts with one of them
+    prefix_min: int = 64        # shared prefix lengths ~ U[min, max], each below its request's prompt
+    prefix_max: int = 512
 
 
 def churn_trace(seed: int = 0, spec: ChurnSpec = ChurnSpec()) -> list[Request]:
     """Arrivals Poisson(rate) per step; prompt ~ U[min, max]; output ~ Geometric(1/mean), clipped.
 
-    Priorities come from a stream of their own, so the trace without them is unchanged."""
+    Priorities and shared prefixes come from streams of their own, so the trace
+    without them is unchanged. A shared prefix (one of ``prefix_groups``, each
+    with a length drawn once) is given to a ``prefix_share`` fraction of the
+    requests whose prompt is longer than it."""
     (r,) = _rngs(seed, 1, 4)
     (rp,) = _rngs(seed, 1, 7)
+    (rx,) = _rngs(seed, 1, 9)
+    plens = [int(rx.integers(spec.prefix_min, spec.prefix_max + 1)) for _ in range(spec.prefix_groups)]
     reqs = []
     for step in range(spec.num_steps):
         for _ in range(int(r.poisson(spec.arrival_rate))):
             p = int(r.integers(spec.prompt_min, spec.prompt_max + 1))
             o = int(min(r.geometric(1.0 / spec.output_mean), spec.output_max))
             prio = int(rp.random() < spec.high_priority) if spec.high_priority > 0 else 0
-            reqs.append(Request(len(reqs), step, p, o, prio))
+            pid, plen = -1, 0
+            if spec.prefix_groups > 0 and rx.random() < spec.prefix_share:
+                g = int(rx.integers(spec.prefix_groups))
+                if plens[g] < p:
+                    pid, plen = g, plens[g]
+            reqs.append(Request(len(reqs), step, p, o, prio, pid, plen))
     return reqs
 
 
@@ -327,23 +343,26 @@ class TokenSource:
 
     Rows are drawn in pages of 256 positions from a stream keyed by
     (seed, request, page), so a row's value does not depend on how a scheduler
-    chunks the prompt.
+    chunks the prompt. The first ``prefix_len`` positions of a request with a
+    shared prefix come from a stream keyed by (seed, prefix, page) instead, so
+    every request sharing that prefix has the same rows there.
     """
 
     PAGE = 256
 
     def __init__(self, seed: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
-                 cache_pages: int = 512):
+                 cache_pages: int = 512, requests=()):
         self.seed, self.hq, self.hkv, self.d = seed, num_q_heads, num_kv_heads, head_dim
         self._cache: dict = {}
         self._cap = cache_pages
+        self._prefix = {r.rid: (r.prefix_id, r.prefix_len) for r in requests if r.prefix_id >= 0}
 
-    def _page(self, rid: int, page: int):
-        key = (rid, page)
+    def _page(self, rid: int, page: int, shared: bool = False):
+        key = ("p" if shared else "r", rid, page)
         hit = self._cache.get(key)
         if hit is not None:
             return hit
-        rk, rv, rq = _rngs(self.seed, 3, 6, rid, page)
+        rk, rv, rq = _rngs(self.seed, 3, 8 if shared else 6, rid, page)
         val = (_normal_bf16(rk, (self.PAGE, self.hkv, self.d)),
                _normal_bf16(rv, (self.PAGE, self.hkv, self.d)),
                _normal_bf16(rq, (self.PAGE, self.hq, self.d)))
@@ -356,10 +375,15 @@ class TokenSource:
         """(k, v, q) bf16 bits for positions [begin, end) of request ``rid``."""
         ks, vs, qs = [], [], []
         pos = begin
+        pid, plen = self._prefix.get(rid, (-1, 0))
         while pos < end:
             page, off = divmod(pos, self.PAGE)
             take = min(end - pos, self.PAGE - off)
-            k, v, q = self._page(rid, page)
+            if pos < plen:
+                take = min(take, plen - pos)
+                k, v, q = self._page(pid, page, shared=True)
+            else:
+                k, v, q = self._page(rid, page)
             ks.append(k[off:off + take])
             vs.append(v[off:off + take])
             qs.append(q[off:off + take])

@@ -44,14 +44,38 @@ tight budget), used only when switched on:
   and admission is tried again. Reading: remaining ties go to the latest
   admitted.
 * Decode headroom: before the step, the blocks that decode rows open must be
-  free; otherwise admitted requests are preempted, least progress first
-  (reading: fewest generated tokens, then fewest cached rows, then latest
-  admitted), until they are. (The pages' earlier rungs, cold cached prefixes
-  and prefixes adopted by waiting requests, do not exist in this replay.)
+  free; otherwise the eviction ladder runs: cold cached prefixes first (with a
+  prefix cache, below), then prefixes adopted by waiting requests (none here:
+  a waiting request holds no blocks), then admitted requests are preempted,
+  least progress first (reading: fewest generated tokens, then fewest cached
+  rows, then latest admitted), until they fit.
 * A preempted request frees its slot and blocks, keeps its generated-token
   count, and waits again in arrival order; once admitted it prefills its
   prompt plus the tokens it had generated, the last chunk yielding one more
   token, then decodes.
+
+Prompt-prefix cache (mlxcel manual, §Paged KV cache and prefix sharing:
+requests sharing a prompt prefix store its blocks once and adopt them by
+reference; an adopter is charged only for the blocks its suffix creates; under
+a budget, cold cached prefixes are evicted, least recently used first, before
+anyone is preempted), used only with a capacity C > 0. Readings:
+
+* The cached part of a request's shared prefix of length p is its whole
+  blocks, c = floor(p / block) * block tokens (nothing when c = 0), so no
+  block is ever shared partly filled and nobody appends into a shared block.
+* Donation, at the end of a step before that step's retirements: each request
+  (admission order) that prefilled its shared prefix itself and whose position
+  has reached c, and whose prefix is not cached, donates its first c / block
+  blocks to a new entry; with C entries already cached, the least recently
+  used is dropped first. An entry is used when created and when adopted.
+* Admission: a head whose prefix is cached adopts the entry's blocks and
+  starts prefilling at position c; it needs ceil((rows + 1) / block) - c /
+  block fresh blocks. When the head lacks blocks (not a slot), cold entries --
+  held by the cache alone, other than the head's own -- are evicted least
+  recently used first (ties: the earlier created), until it fits, before
+  priority preemption is tried.
+* A shared block returns to the free list when its last holder (the entry or
+  a request) lets go; an adopter whose entry was dropped keeps the blocks.
 """
 
 from __future__ import annotations
@@ -65,6 +89,17 @@ from . import attention_dense
 
 
 @dataclass
+class _Entry:
+    """A cached prompt prefix: ``nb`` shared blocks and the count of their holders."""
+
+    pid: int
+    nb: int
+    refs: int
+    last_used: int
+    order: int
+
+
+@dataclass
 class _Live:
     rid: int
     prompt: int
@@ -72,11 +107,18 @@ class _Live:
     pos: int = 0
     decoding: bool = False
     generated: int = 0
-    blocks: int = 0
+    blocks: int = 0  # blocks of its own (shared prefix blocks are counted once, in their entry)
     own_prompt: int = 0
     arrival: int = 0
     priority: int = 0
     admitted_as: int = 0
+    prefix_id: int = -1
+    cached_len: int = 0  # the whole-block part of its shared prefix
+    entry: _Entry | None = None  # the shared blocks it holds (adopted or donated)
+
+    @property
+    def all_blocks(self) -> int:
+        return self.blocks + (self.entry.nb if self.entry else 0)
 
 
 @dataclass(frozen=True)
@@ -96,7 +138,7 @@ def _ceil_div(a: int, b: int) -> int:
 class ChurnReplay:
     def __init__(self, requests, *, max_slots: int, num_blocks: int, block_size: int,
                  chunk_idle: int = 2048, chunk_busy: int = 512, watermark: float = 0.0,
-                 preemption: str | None = None):
+                 preemption: str | None = None, prefix_cache: int = 0):
         self.pending = deque(sorted(requests, key=lambda r: (r.arrival_step, r.rid)))
         # waiting requests: (arrival, rid, rows to prefill, own prompt, output, priority, generated)
         self.queue: list[tuple] = []
@@ -112,13 +154,43 @@ class ChurnReplay:
         self.preempted: list[int] = []
         self.preempt_reasons: list[str] = []  # "priority" or "headroom"
         self._admissions = 0
+        self.cache_capacity = prefix_cache
+        self.cache: dict[int, _Entry] = {}
+        self._entries_made = 0
+        # (step, event, prefix id): "donate", "adopt", "drop-capacity", "drop-admission", "drop-headroom"
+        self.cache_events: list[tuple] = []
+
+    # ---- blocks held by requests and cached prefixes --------------------------------
+    def _unref(self, e: _Entry) -> None:
+        e.refs -= 1
+        if e.refs == 0:
+            self.free_blocks += e.nb
+
+    def _release(self, r: _Live) -> None:
+        self.free_blocks += r.blocks
+        if r.entry is not None:
+            self._unref(r.entry)
+
+    def _drop(self, e: _Entry, why: str) -> None:
+        del self.cache[e.pid]
+        self.cache_events.append((self.step_index, "drop-" + why, e.pid))
+        self._unref(e)
+
+    def _cold(self, spare: int | None = None) -> list[_Entry]:
+        """Cached entries held by the cache alone, least recently used first."""
+        cold = [e for e in self.cache.values() if e.refs == 1 and e.pid != spare]
+        return sorted(cold, key=lambda e: (e.last_used, e.order))
+
+    def _cached_len(self, prefix_id: int, prefix_len: int) -> int:
+        return (prefix_len // self.bs) * self.bs if self.cache_capacity > 0 and prefix_id >= 0 else 0
 
     def _evict(self, r: _Live, reason: str, held=None) -> None:
         """Free r's slot and blocks; it waits again (in `held` until the request that evicted it is in)."""
         self.live.remove(r)
         self.free_slots += 1
-        self.free_blocks += r.blocks
-        entry = (r.arrival, r.rid, r.own_prompt + r.generated, r.own_prompt, r.output, r.priority, r.generated)
+        self._release(r)
+        entry = (r.arrival, r.rid, r.own_prompt + r.generated, r.own_prompt, r.output, r.priority, r.generated,
+                 r.prefix_id, r.cached_len)
         if held is None:
             self.queue.append(entry)
             self.queue.sort()
@@ -132,15 +204,22 @@ class ChurnReplay:
         s = self.step_index
         while self.pending and self.pending[0].arrival_step <= s:
             q = self.pending.popleft()
+            pid = getattr(q, "prefix_id", -1)
             self.queue.append((q.arrival_step, q.rid, q.prompt_len, q.prompt_len, q.output_len,
-                               getattr(q, "priority", 0), 0))
+                               getattr(q, "priority", 0), 0, pid,
+                               self._cached_len(pid, getattr(q, "prefix_len", 0))))
             self.queue.sort()
         held: list[tuple] = []  # evicted for the current head; they wait behind it
         while self.queue:
-            arrival, rid, rows_to_fill, own, output, prio, gen = self.queue[0]
-            need = _ceil_div(rows_to_fill + 1, self.bs)
+            arrival, rid, rows_to_fill, own, output, prio, gen, pid, clen = self.queue[0]
+            e = self.cache.get(pid) if clen > 0 else None
+            need = _ceil_div(rows_to_fill + 1, self.bs) - (e.nb if e else 0)
             floor = self.watermark * self.num_blocks if any(r.decoding for r in self.live) else 0.0
             if self.free_slots == 0 or self.free_blocks - need < floor:
+                cold = self._cold(spare=pid if e else None) if self.free_slots > 0 else []
+                if cold:  # first rung: a cold cached prefix
+                    self._drop(cold[0], "admission")
+                    continue
                 lower = [r for r in self.live if r.priority < prio] if self.preemption else []
                 if not lower:
                     break  # strict FIFO: nobody jumps ahead
@@ -157,17 +236,27 @@ class ChurnReplay:
                 held.clear()
             self.free_slots -= 1
             self.free_blocks -= need
-            self.live.append(_Live(rid, rows_to_fill, output, generated=gen, blocks=need, own_prompt=own,
-                                   arrival=arrival, priority=prio, admitted_as=self._admissions))
+            r = _Live(rid, rows_to_fill, output, generated=gen, blocks=need, own_prompt=own, arrival=arrival,
+                      priority=prio, admitted_as=self._admissions, prefix_id=pid, cached_len=clen)
+            if e is not None:  # adopt: start after the cached prefix
+                e.refs += 1
+                e.last_used = s
+                r.entry, r.pos = e, clen
+                self.cache_events.append((s, "adopt", pid))
+            self.live.append(r)
             self._admissions += 1
         if held:  # the head still did not fit after every eviction it could make
             self.queue.extend(held)
             self.queue.sort()
         # decode headroom
         while True:
-            opening = sum(1 for r in self.live if r.decoding and r.pos // self.bs >= r.blocks)
+            opening = sum(1 for r in self.live if r.decoding and r.pos // self.bs >= r.all_blocks)
             if opening <= self.free_blocks:
                 break
+            cold = self._cold()
+            if cold:
+                self._drop(cold[0], "headroom")
+                continue
             self._evict(sorted(self.live, key=lambda r: (r.generated, r.pos, -r.admitted_as))[0], "headroom")
         budget = self.chunk_busy if any(r.decoding for r in self.live) else self.chunk_idle
         rows: list[Row] = []
@@ -180,7 +269,7 @@ class ChurnReplay:
                 budget -= take
         for r in self.live:
             if r.decoding:
-                if r.pos // self.bs >= r.blocks:
+                if r.pos // self.bs >= r.all_blocks:
                     if self.free_blocks == 0:
                         raise RuntimeError("pool exhausted during decode")
                     self.free_blocks -= 1
@@ -203,11 +292,23 @@ class ChurnReplay:
                 r.generated += 1
             if r.pos >= r.prompt and r.generated >= r.output:
                 done.append(r.rid)
+        # donations, before this step's retirements
+        for r in self.live:
+            if (r.cached_len > 0 and r.entry is None and r.pos >= r.cached_len
+                    and r.prefix_id not in self.cache):
+                if len(self.cache) >= self.cache_capacity:
+                    self._drop(min(self.cache.values(), key=lambda e: (e.last_used, e.order)), "capacity")
+                e = _Entry(r.prefix_id, r.cached_len // self.bs, 2, self.step_index, self._entries_made)
+                self._entries_made += 1
+                self.cache[r.prefix_id] = e
+                r.blocks -= e.nb
+                r.entry = e
+                self.cache_events.append((self.step_index, "donate", r.prefix_id))
         for rid in done:
             r = by_rid[rid]
             self.live.remove(r)
             self.free_slots += 1
-            self.free_blocks += r.blocks
+            self._release(r)
         self.finished.extend(done)
         self.step_index += 1
         return done

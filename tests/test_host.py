@@ -424,7 +424,8 @@ def test_step_rejects_bad_staging_before_any_device_work():
 # ---- scheduler vs the oracle's replay -------------------------------------------
 
 def _compare_trace(reqs, spec_steps, num_blocks, max_slots, bs=16, **policy):
-    pool = B.Pool(num_blocks, bs, max_slots, 1024, free_order=W.churn_free_order(0, num_blocks))
+    pool = B.Pool(num_blocks, bs, max_slots + policy.get("prefix_cache", 0), 1024,
+                  free_order=W.churn_free_order(0, num_blocks))
     sch = S.ChurnScheduler(reqs, pool, **policy)
     ref = churn.ChurnReplay(reqs, max_slots=max_slots, num_blocks=num_blocks, block_size=bs, **policy)
     for step in range(spec_steps):
@@ -434,8 +435,10 @@ def _compare_trace(reqs, spec_steps, num_blocks, max_slots, bs=16, **policy):
                [(r.rid, r.begin, r.n, r.prefill) for r in want], f"step {step}"
         assert sch.preempted == ref.preempted, f"step {step}: preemptions differ"
         assert sch.preempt_reasons == ref.preempt_reasons, f"step {step}: preemption reasons differ"
+        assert sch.cache_events == ref.cache_events, f"step {step}: prefix cache events differ"
         low = pool.lower([(r.slot, r.n) for r in rows])
         assert len(low.slot_mapping) == sum(r.n for r in rows)
+        assert len(pool.take_copies()) == 0  # only whole blocks are ever shared: nothing to copy
         assert sch.commit(rows) == ref.commit(want)
         assert pool.stats().free_blocks == ref.free_blocks
     return sch
@@ -465,6 +468,30 @@ def test_watermark_reduces_decode_preemptions():
     reqs = W.churn_trace(5, PRESSURE)
     counts = [len(_compare_trace(reqs, PRESSURE.num_steps, 300, 16, watermark=f).preempted) for f in (0.0, 0.05)]
     assert counts[1] < counts[0]
+
+
+PREFIXED = W.ChurnSpec(num_steps=200, arrival_rate=0.5, prompt_min=64, prompt_max=1024, output_mean=96.0,
+                       output_max=400, high_priority=0.3, prefix_groups=5, prefix_share=0.6, prefix_min=100,
+                       prefix_max=600)
+
+
+def test_prefix_cache_scheduler_matches_oracle_under_pool_pressure():
+    """Shared prompt prefixes, a 4-entry prefix cache and a tight pool: donations, adoptions and every
+    kind of cache eviction happen, and the library (real refcounted pool) agrees with the replay."""
+    reqs = W.churn_trace(6, PREFIXED)
+    sch = _compare_trace(reqs, PREFIXED.num_steps, 300, 16, watermark=0.01, preemption="lowest-priority",
+                         prefix_cache=4)
+    kinds = {e[1] for e in sch.cache_events}
+    assert kinds == {"donate", "adopt", "drop-capacity", "drop-admission", "drop-headroom"}
+    assert sch.preempted
+    # an adopter's first prefill row starts after the cached prefix
+    assert sum(1 for e in sch.cache_events if e[1] == "adopt") >= 3
+
+
+def test_prefix_cache_off_leaves_plans_unchanged():
+    reqs = W.churn_trace(6, PREFIXED)
+    a = _compare_trace(reqs, 120, 300, 16, watermark=0.01, preemption="lowest-priority")
+    assert a.cache_events == []
 
 
 def test_scheduler_matches_oracle_replay_on_churn_trace():

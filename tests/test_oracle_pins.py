@@ -317,10 +317,11 @@ def test_thread_count_does_not_change_results(oracle_lib):
 # ---- the churn replay's scheduling rules ------------------------------------
 
 class _Req:
-    def __init__(self, rid, arrival_step, prompt_len, output_len, priority=0):
+    def __init__(self, rid, arrival_step, prompt_len, output_len, priority=0, prefix=(-1, 0)):
         self.rid, self.arrival_step = rid, arrival_step
         self.prompt_len, self.output_len = prompt_len, output_len
         self.priority = priority
+        self.prefix_id, self.prefix_len = prefix
 
 
 def _run_steps(r, n):
@@ -374,6 +375,58 @@ def test_priority_preemption_picks_the_policy_victim(policy, victim):
     # the victim waits with its prompt plus the tokens it generated, in arrival order
     assert r.queue[0][1] == victim and r.queue[0][2] == 15 + gen[victim] and r.queue[0][6] == gen[victim]
     assert any(x.rid == 2 and x.prefill for x in rows)
+
+
+# ---- prompt-prefix cache (mlxcel manual, §Paged KV cache and prefix sharing), by hand ----
+
+def test_prefix_donated_in_whole_blocks_and_adopter_charged_for_its_suffix():
+    # A's shared prefix is 40 tokens: its whole blocks, 32 tokens (2 blocks), are cached.
+    reqs = [_Req(0, 0, 60, 3, prefix=(0, 40)), _Req(1, 1, 50, 2, prefix=(0, 40))]
+    r = churn.ChurnReplay(reqs, max_slots=4, num_blocks=64, block_size=16, prefix_cache=2)
+    _run_steps(r, 1)                     # A: 4 blocks, prefills 60 rows, donates 2 of them
+    assert r.free_blocks == 60 and r.cache[0].nb == 2 and r.cache[0].refs == 2
+    rows = r.plan()                      # B adopts: ceil(51 / 16) - 2 = 2 fresh blocks, prefill from 32
+    assert r.free_blocks == 58 and r.cache[0].refs == 3
+    assert [(x.rid, x.begin, x.n, x.prefill) for x in rows] == [(1, 32, 18, True), (0, 60, 1, False)]
+    r.commit(rows)
+    _run_steps(r, 1)                     # both retire; the cached prefix keeps its 2 blocks
+    assert r.finished == [0, 1] and r.free_blocks == 62 and r.cache[0].refs == 1
+    assert r.cache_events == [(0, "donate", 0), (1, "adopt", 0)]
+
+
+def test_cold_prefix_is_evicted_before_anyone_is_preempted():
+    # 4 blocks. A caches 2 blocks and retires; D and E take the other two; D's decode then
+    # opens a block: the cold prefix goes, nobody is preempted.
+    reqs = [_Req(0, 0, 33, 2, prefix=(0, 32)), _Req(1, 1, 14, 50), _Req(2, 2, 14, 50)]
+    r = churn.ChurnReplay(reqs, max_slots=4, num_blocks=4, block_size=16, prefix_cache=2)
+    _run_steps(r, 4)
+    assert r.free_blocks == 0 and r.cache[0].refs == 1
+    r.plan()
+    assert r.cache_events[-1] == (4, "drop-headroom", 0) and r.preempted == [] and 0 not in r.cache
+    assert r.free_blocks == 1  # the 2 freed blocks, minus the one D's row opens
+
+
+def test_admission_evicts_cold_prefixes_but_spares_the_heads_own():
+    base = [_Req(0, 0, 33, 2, prefix=(0, 32))]
+    # a head with no prefix needing 3 blocks (2 free): the cold prefix goes
+    r = churn.ChurnReplay(base + [_Req(1, 2, 40, 2)], max_slots=4, num_blocks=4, block_size=16, prefix_cache=2)
+    _run_steps(r, 2)
+    r.plan()
+    assert r.cache_events[-1] == (2, "drop-admission", 0) and [x.rid for x in r.live] == [1]
+    # a head that would adopt that prefix (3 fresh blocks on top of it) waits instead
+    r = churn.ChurnReplay(base + [_Req(1, 2, 70, 2, prefix=(0, 32))], max_slots=4, num_blocks=4, block_size=16,
+                          prefix_cache=2)
+    _run_steps(r, 2)
+    r.plan()
+    assert 0 in r.cache and r.live == [] and [q[1] for q in r.queue] == [1]
+
+
+def test_full_prefix_cache_drops_the_least_recently_used():
+    reqs = [_Req(0, 0, 20, 1, prefix=(0, 16)), _Req(1, 1, 20, 1, prefix=(1, 16))]
+    r = churn.ChurnReplay(reqs, max_slots=4, num_blocks=8, block_size=16, prefix_cache=1)
+    _run_steps(r, 2)
+    assert r.cache_events == [(0, "donate", 0), (1, "drop-capacity", 0), (1, "donate", 1)]
+    assert list(r.cache) == [1] and r.free_blocks == 7
 
 
 def test_decode_headroom_preempts_the_least_progress():
