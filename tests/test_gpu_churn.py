@@ -39,18 +39,19 @@ def _replay(spec, seed, num_blocks, max_slots, **policy):
     reqs = W.churn_trace(seed, spec)
     bs, hq, hkv, d = spec.block_size, spec.num_q_heads, spec.num_kv_heads, spec.head_dim
     mbps = -(-(spec.prompt_max + 2 * spec.output_max + 1) // bs) + 1  # re-prefill covers generated tokens too
-    pool = B.Pool(num_blocks, bs, max_slots, mbps, free_order=W.churn_free_order(seed, num_blocks))
+    pool = B.Pool(num_blocks, bs, max_slots + policy.get("prefix_cache", 0), mbps,
+                  free_order=W.churn_free_order(seed, num_blocks))
     sch = S.ChurnScheduler(reqs, pool, **policy)
     ref = churn.ChurnReplay(reqs, max_slots=max_slots, num_blocks=num_blocks, block_size=bs, **policy)
     hist = churn.ContiguousHistory()
-    toks = W.TokenSource(0, hq, hkv, d)
+    toks = W.TokenSource(0, hq, hkv, d, requests=reqs)
     scale = 1.0 / np.sqrt(d)
     dev = "cuda"
     k_pool, v_pool = R.empty_pool(num_blocks, hkv, bs, d, dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     pick = np.random.default_rng(7)
 
-    checked_rows = steps_with_rows = max_ctx = 0
+    checked_rows = steps_with_rows = max_ctx = adopted_rows = 0
     saw_prefill_and_decode = saw_retire = False
     refilled = set()
     for step in range(spec.num_steps):
@@ -61,8 +62,13 @@ def _replay(spec, seed, num_blocks, max_slots, **policy):
                [(r.rid, r.begin, r.n, r.prefill) for r in want], f"step {step}: plans differ"
         assert sch.preempted == ref.preempted, f"step {step}: preemptions differ"
         for rid in sch.preempted[n_pre:]:
-            hist.drop(rid)  # its KV is gone; it re-prefills from position 0 when admitted again
+            hist.drop(rid)  # its KV is gone; it re-prefills when admitted again
         refilled |= {r.rid for r in rows if r.prefill and r.rid in sch.preempted}
+        for r in rows:  # an adopter starts after the cached prefix: its history holds the shared rows
+            if r.prefill and r.begin > 0 and hist.len.get(r.rid, 0) == 0:
+                pk, pv, _ = toks.rows(r.rid, 0, r.begin)
+                hist.append(r.rid, pk, pv)
+                adopted_rows += r.n
         if rows:
             steps_with_rows += 1
             low = pool.lower([(r.slot, r.n) for r in rows])
@@ -71,7 +77,7 @@ def _replay(spec, seed, num_blocks, max_slots, **policy):
             v_new = np.concatenate([p[1] for p in parts])
             q = np.concatenate([p[2] for p in parts])
             work, info = B.pkv_plan_work(low.cu_seqlens_q, low.seq_slot, low.context_lens,
-                                         max_slots=max_slots, max_blocks_per_slot=mbps, block_size=bs,
+                                         max_slots=pool.max_slots, max_blocks_per_slot=mbps, block_size=bs,
                                          num_q_heads=hq, num_kv_heads=hkv, head_dim=d)
             t_k, t_v, t_q = (R._bf16_tensor(x, dev) for x in (k_new, v_new, q))
             t_sm = R._i64(low.slot_mapping, dev)
@@ -125,7 +131,8 @@ def _replay(spec, seed, num_blocks, max_slots, **policy):
 
     return dict(steps_with_rows=steps_with_rows, checked_rows=checked_rows, max_ctx=max_ctx,
                 saw_prefill_and_decode=saw_prefill_and_decode, saw_retire=saw_retire,
-                preempted=list(sch.preempted), reasons=list(sch.preempt_reasons), refilled=refilled)
+                preempted=list(sch.preempted), reasons=list(sch.preempt_reasons), refilled=refilled,
+                cache_events=list(sch.cache_events), adopted_rows=adopted_rows)
 
 
 def test_churn_trace_matches_contiguous_oracle():
@@ -149,3 +156,17 @@ def test_churn_under_pool_pressure_with_preemption_matches_oracle():
     assert seen["preempted"] and {"priority", "headroom"} <= set(seen["reasons"])
     assert seen["refilled"]  # some preempted request came back and re-prefilled on the GPU
     assert seen["saw_retire"] and seen["checked_rows"] > 100
+
+
+PREFIXED = W.ChurnSpec(num_steps=200, arrival_rate=0.5, prompt_min=64, prompt_max=1024, output_mean=96.0,
+                       output_max=400, high_priority=0.3, prefix_groups=5, prefix_share=0.6, prefix_min=100,
+                       prefix_max=600)
+
+
+def test_churn_with_prefix_cache_matches_oracle():
+    """Shared prompt prefixes through a 4-entry prefix cache on a tight pool: adopters attend over
+    blocks another request wrote, whose rows the oracle has as part of the adopter's own history."""
+    seen = _replay(PREFIXED, 6, 300, 16, watermark=0.01, preemption="lowest-priority", prefix_cache=4)
+    kinds = {e[1] for e in seen["cache_events"]}
+    assert {"donate", "adopt", "drop-admission", "drop-headroom"} <= kinds
+    assert seen["adopted_rows"] > 0 and seen["checked_rows"] > 100 and seen["saw_retire"]
