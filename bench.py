@@ -86,8 +86,8 @@ def parse_args(argv=None):
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle CPU-baseline budget")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=300)
-    p.add_argument("--kv", choices=["bf16", "q8"], default="bf16",
-                   help="pool format: bf16, or the 8-bit block-scaled pool (no end-to-end leg)")
+    p.add_argument("--kv", choices=["bf16", "q8", "q4"], default="bf16",
+                   help="pool format: bf16, or the 8-bit / 4-bit block-scaled pool (no end-to-end leg)")
     p.add_argument("--pool-blocks", type=int, default=None,
                    help="smaller synthetic pool (same contexts) for profiling captures")
     return p.parse_args(argv)
@@ -100,9 +100,11 @@ def parse_args(argv=None):
 def kv_bytes(w, kv: str = "bf16") -> int:
     """Algorithmic bytes of the attention: K and V of every visible key once per kv head, Q in, O out.
 
-    A key's row costs 2 * head_dim bytes in a bf16 pool, head_dim codes plus
-    head_dim / 32 bf16 scales in the 8-bit pool."""
-    row = w.head_dim * 2 if kv == "bf16" else w.head_dim + w.head_dim // 16
+    A key's row costs 2 * head_dim bytes in a bf16 pool, head_dim (8-bit) or
+    head_dim / 2 (4-bit) bytes of codes plus head_dim / 32 bf16 scales in the
+    block-scaled pools."""
+    codes = {"bf16": 0, "q8": w.head_dim, "q4": w.head_dim // 2}[kv]
+    row = w.head_dim * 2 if kv == "bf16" else codes + w.head_dim // 16
     kvb = sum(s.ctx for s in w.segments) * w.num_kv_heads * row * 2
     return kvb + w.total_q * w.num_q_heads * w.head_dim * 2 * 2
 
@@ -443,14 +445,14 @@ def run_ours(args, rank, world, local_rank):
                               "step": statistics.median(step_ms)},
     }
     chunk_kernel = "prefill_pair_kernel" if w.head_dim == 128 else "prefill_kernel"
-    dec_kernel = "decode_q8_kernel" if args.kv == "q8" else "decode_kernel"
+    dec_kernel = "decode_q8_kernel" if args.kv in ("q8", "q4") else "decode_kernel"
     if ds.info.num_prefill_items and args.kv == "bf16":
         # the chunk kernel dominates the library's time on steps that carry a prompt chunk
         bound, unit, kernel = "tensor", "TFLOP/s", chunk_kernel
     elif ds.info.num_prefill_items:
-        bound, unit, kernel = "hbm", "GB/s", "attention call: widen_q8 + chunk + decode_q8 + merge kernels"
+        bound, unit, kernel = "hbm", "GB/s", "attention call: widen_q8 + chunk + decode_q8 + span merge kernels"
     elif ds.info.num_combine_items:
-        bound, unit, kernel = "hbm", "GB/s", f"attention call: {dec_kernel} + merge_kernel"
+        bound, unit, kernel = "hbm", "GB/s", f"attention call: {dec_kernel} + span merge (merge_small/merge_wide)"
     else:
         bound, unit, kernel = "hbm", "GB/s", dec_kernel
     if bound == "tensor":
@@ -464,7 +466,7 @@ def run_ours(args, rank, world, local_rank):
         res["attention_call"] = {"kv_gbs": achieved, "pct_hbm_peak": 100.0 * achieved / hbm, "mean_ms": attn_mean,
                                  "kernels": "chunk + decode + span merge"}
     else:
-        src = "pkv_kvq8.cu" if args.kv == "q8" else "pkv_decode.cu"
+        src = "pkv_kvq8.cu" if args.kv in ("q8", "q4") else "pkv_decode.cu"
         traffic = profiled_traffic(src, args.workload) if dec_kernel in kernel else None
         res["roofline"] = {"bound": "hbm", "kernel": kernel, "achieved": achieved, "peak": hbm, "unit": "GB/s",
                            "frac": achieved / hbm, "traffic": traffic,

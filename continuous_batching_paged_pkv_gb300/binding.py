@@ -107,6 +107,9 @@ def _lib():
             "pkv_cache_write_q8": ([p, p, p, i64, p, p, p, p, i64, i32, i32, i32, p, p], ctypes.c_int),
             "pkv_attention_q8": ([p, p, i32, i64, p, p, p, i32, i32, i32, p, p, p, p, i64, i32, i32, i32, f32, p,
                                   ctypes.POINTER(WorkInfo), p, p, u64, p, p], ctypes.c_int),
+            "pkv_cache_write_q4": ([p, p, p, i64, p, p, p, p, i64, i32, i32, i32, p, p], ctypes.c_int),
+            "pkv_attention_q4": ([p, p, i32, i64, p, p, p, i32, i32, i32, p, p, p, p, i64, i32, i32, i32, f32, p,
+                                  ctypes.POINTER(WorkInfo), p, p, u64, p, p], ctypes.c_int),
             "pkv_stage_layout_init": ([ctypes.POINTER(StageLayout), i64, i32, i32, i32, i32, i32, i32], ctypes.c_int),
             "pkv_step": ([ctypes.POINTER(StageLayout), p, u64, p, u64, p, p, i64, i32, f32, p, u64, p, p, p, p,
                           ctypes.POINTER(WorkInfo)], ctypes.c_int),
@@ -326,46 +329,73 @@ def pkv_attention_no_alloc(q, cu_seqlens_q, seq_slot, context_lens, block_tables
                                          _stream(stream)), "pkv_attention_no_alloc")
 
 
-def _need_q8_pool(k_codes, k_scales, v_codes, v_scales):
+def _need_quant_pool(k_codes, k_scales, v_codes, v_scales, bits: int):
+    """Shapes of a block-scaled pool: 8-bit codes int8 [blocks, Hkv, bs, D], 4-bit codes uint8
+    [blocks, Hkv, bs, D/2] (two per byte); scales bf16 [blocks, Hkv, bs, D/32]."""
     for t, nm in ((k_codes, "k_codes"), (v_codes, "v_codes")):
-        _need(t, "torch.int8", nm)
+        _need(t, "torch.int8" if bits == 8 else "torch.uint8", nm)
     for t, nm in ((k_scales, "k_scales"), (v_scales, "v_scales")):
         _need(t, "torch.bfloat16", nm)
-    nb, hkv, bs, d = k_codes.shape
-    if tuple(v_codes.shape) != (nb, hkv, bs, d) or tuple(k_scales.shape) != (nb, hkv, bs, d // 32) or \
+    nb, hkv, bs, w = k_codes.shape
+    d = w * 8 // bits
+    if tuple(v_codes.shape) != (nb, hkv, bs, w) or tuple(k_scales.shape) != (nb, hkv, bs, d // 32) or \
             tuple(v_scales.shape) != (nb, hkv, bs, d // 32):
-        raise ValueError("8-bit pool: codes [blocks, Hkv, bs, D] int8 and scales [blocks, Hkv, bs, D/32] bf16")
+        raise ValueError(f"{bits}-bit pool: codes [blocks, Hkv, bs, D*{bits}/8] and scales [blocks, Hkv, bs, D/32] bf16")
     return nb, hkv, bs, d
 
 
-def pkv_cache_write_q8(k_new, v_new, slot_mapping, k_codes, k_scales, v_codes, v_scales, *, device_status=None,
-                       stream=None) -> None:
+def _cache_write_quant(bits, k_new, v_new, slot_mapping, k_codes, k_scales, v_codes, v_scales, device_status,
+                       stream) -> None:
     _need(k_new, "torch.bfloat16", "k_new")
     _need(v_new, "torch.bfloat16", "v_new")
     _need(slot_mapping, "torch.int64", "slot_mapping")
-    nb, hkv, bs, d = _need_q8_pool(k_codes, k_scales, v_codes, v_scales)
-    _check(_lib().pkv_cache_write_q8(_t_ptr(k_new), _t_ptr(v_new), _t_ptr(slot_mapping), slot_mapping.numel(),
-                                     _t_ptr(k_codes), _t_ptr(k_scales), _t_ptr(v_codes), _t_ptr(v_scales), nb, bs,
-                                     hkv, d, _t_ptr(device_status), _stream(stream)), "pkv_cache_write_q8")
+    nb, hkv, bs, d = _need_quant_pool(k_codes, k_scales, v_codes, v_scales, bits)
+    name = f"pkv_cache_write_q{bits}"
+    _check(getattr(_lib(), name)(_t_ptr(k_new), _t_ptr(v_new), _t_ptr(slot_mapping), slot_mapping.numel(),
+                                 _t_ptr(k_codes), _t_ptr(k_scales), _t_ptr(v_codes), _t_ptr(v_scales), nb, bs, hkv, d,
+                                 _t_ptr(device_status), _stream(stream)), name)
 
 
-def pkv_attention_q8(q, cu_seqlens_q, seq_slot, context_lens, block_tables, k_codes, k_scales, v_codes, v_scales,
-                     work, info: WorkInfo, out, workspace=None, *, scale: float = 0.0, device_status=None,
-                     stream=None) -> None:
+def _attention_quant(bits, q, cu_seqlens_q, seq_slot, context_lens, block_tables, k_codes, k_scales, v_codes,
+                     v_scales, work, info, out, workspace, scale, device_status, stream) -> None:
     _need(q, "torch.bfloat16", "q")
     _need(out, "torch.bfloat16", "out")
     for t, nm in ((cu_seqlens_q, "cu_seqlens_q"), (seq_slot, "seq_slot"), (context_lens, "context_lens"),
                   (block_tables, "block_tables"), (work, "work")):
         _need(t, "torch.int32", nm)
-    nb, hkv, bs, d = _need_q8_pool(k_codes, k_scales, v_codes, v_scales)
+    nb, hkv, bs, d = _need_quant_pool(k_codes, k_scales, v_codes, v_scales, bits)
     ms, mbps = block_tables.shape
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _check(_lib().pkv_attention_q8(_t_ptr(q), _t_ptr(cu_seqlens_q), cu_seqlens_q.numel() - 1, q.shape[0],
-                                   _t_ptr(seq_slot), _t_ptr(context_lens), _t_ptr(block_tables), ms, mbps, bs,
-                                   _t_ptr(k_codes), _t_ptr(k_scales), _t_ptr(v_codes), _t_ptr(v_scales), nb,
-                                   q.shape[1], hkv, d, float(scale), _t_ptr(work), ctypes.byref(info), _t_ptr(out),
-                                   _t_ptr(workspace), ws_bytes, _t_ptr(device_status), _stream(stream)),
-           "pkv_attention_q8")
+    name = f"pkv_attention_q{bits}"
+    _check(getattr(_lib(), name)(_t_ptr(q), _t_ptr(cu_seqlens_q), cu_seqlens_q.numel() - 1, q.shape[0],
+                                 _t_ptr(seq_slot), _t_ptr(context_lens), _t_ptr(block_tables), ms, mbps, bs,
+                                 _t_ptr(k_codes), _t_ptr(k_scales), _t_ptr(v_codes), _t_ptr(v_scales), nb,
+                                 q.shape[1], hkv, d, float(scale), _t_ptr(work), ctypes.byref(info), _t_ptr(out),
+                                 _t_ptr(workspace), ws_bytes, _t_ptr(device_status), _stream(stream)), name)
+
+
+def pkv_cache_write_q8(k_new, v_new, slot_mapping, k_codes, k_scales, v_codes, v_scales, *, device_status=None,
+                       stream=None) -> None:
+    _cache_write_quant(8, k_new, v_new, slot_mapping, k_codes, k_scales, v_codes, v_scales, device_status, stream)
+
+
+def pkv_cache_write_q4(k_new, v_new, slot_mapping, k_codes, k_scales, v_codes, v_scales, *, device_status=None,
+                       stream=None) -> None:
+    _cache_write_quant(4, k_new, v_new, slot_mapping, k_codes, k_scales, v_codes, v_scales, device_status, stream)
+
+
+def pkv_attention_q8(q, cu_seqlens_q, seq_slot, context_lens, block_tables, k_codes, k_scales, v_codes, v_scales,
+                     work, info: WorkInfo, out, workspace=None, *, scale: float = 0.0, device_status=None,
+                     stream=None) -> None:
+    _attention_quant(8, q, cu_seqlens_q, seq_slot, context_lens, block_tables, k_codes, k_scales, v_codes, v_scales,
+                     work, info, out, workspace, scale, device_status, stream)
+
+
+def pkv_attention_q4(q, cu_seqlens_q, seq_slot, context_lens, block_tables, k_codes, k_scales, v_codes, v_scales,
+                     work, info: WorkInfo, out, workspace=None, *, scale: float = 0.0, device_status=None,
+                     stream=None) -> None:
+    _attention_quant(4, q, cu_seqlens_q, seq_slot, context_lens, block_tables, k_codes, k_scales, v_codes, v_scales,
+                     work, info, out, workspace, scale, device_status, stream)
 
 
 def pkv_copy_blocks(pairs, arrays, *, device_status=None, stream=None) -> None:

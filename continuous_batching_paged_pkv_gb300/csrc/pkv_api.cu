@@ -83,15 +83,18 @@ bool encode_pool(CUtensorMap *m, const void *pool, int64_t rows, int32_t head_di
 
 // 8-bit codes [rows][D] -> boxes of 16 whole rows; 128-byte swizzle for
 // 128-byte rows (D = 128), 64-byte swizzle for 64-byte rows (D = 64).
-bool encode_codes(CUtensorMap *m, const void *codes, int64_t rows, int32_t head_dim) {
+// Code rows of head_dim * bits / 8 bytes (128 or 64), 16-row boxes with the
+// matching swizzle (128B or 64B).
+bool encode_codes(CUtensorMap *m, const void *codes, int64_t rows, int32_t head_dim, int32_t bits) {
   EncodeFn enc = encoder();
   if (!enc) return false;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(head_dim)};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(head_dim), static_cast<cuuint32_t>(pkv::kSubKeys)};
+  const int32_t row_bytes = head_dim * bits / 8;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(row_bytes), static_cast<cuuint32_t>(pkv::kSubKeys)};
   cuuint32_t estr[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(codes), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, head_dim == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, row_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -245,12 +248,14 @@ pkv_status pkv_copy_blocks(const int32_t *pairs, int64_t num_pairs, void *const 
   return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
-pkv_status pkv_cache_write_q8(const void *k_new, const void *v_new, const int64_t *slot_mapping,
-                              int64_t num_tokens, int8_t *k_codes, void *k_scales, int8_t *v_codes, void *v_scales,
-                              int64_t num_blocks, int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
-                              uint32_t *device_status, pkv_stream_t stream) {
+// The block-scaled pools' entry points share these bodies; `bits` is 8, or 4
+// (head_dim 128 only).
+static pkv_status cache_write_quant(int32_t bits, const void *k_new, const void *v_new, const int64_t *slot_mapping,
+                                    int64_t num_tokens, int8_t *k_codes, void *k_scales, int8_t *v_codes,
+                                    void *v_scales, int64_t num_blocks, int32_t block_size, int32_t num_kv_heads,
+                                    int32_t head_dim, uint32_t *device_status, pkv_stream_t stream) {
   if (num_tokens < 0 || num_blocks <= 0 || block_size <= 0 || num_kv_heads <= 0) return PKV_ERR_INVALID_ARG;
-  if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
+  if ((head_dim != 64 && head_dim != 128) || (bits == 4 && head_dim != 128)) return PKV_ERR_UNSUPPORTED;
   if (num_tokens == 0) return PKV_OK;
   if (!k_new || !v_new || !slot_mapping || !k_codes || !v_codes || !k_scales || !v_scales)
     return PKV_ERR_INVALID_ARG;
@@ -258,21 +263,40 @@ pkv_status pkv_cache_write_q8(const void *k_new, const void *v_new, const int64_
       !aligned(k_scales, 16) || !aligned(v_scales, 16) || !aligned(slot_mapping, 8))
     return PKV_ERR_INVALID_ARG;
   cudaError_t e = pkv::launch_cache_write_q8(k_new, v_new, slot_mapping, num_tokens, k_codes, k_scales, v_codes,
-                                             v_scales, num_blocks, block_size, num_kv_heads, head_dim, device_status,
-                                             reinterpret_cast<cudaStream_t>(stream));
+                                             v_scales, num_blocks, block_size, num_kv_heads, head_dim, bits,
+                                             device_status, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
-pkv_status pkv_attention_q8(const void *q, const int32_t *cu_seqlens_q, int32_t num_seqs, int64_t total_q,
-                            const int32_t *seq_slot, const int32_t *context_lens, const int32_t *block_tables,
-                            int32_t max_slots, int32_t max_blocks_per_slot, int32_t block_size,
-                            const int8_t *k_codes, const void *k_scales, const int8_t *v_codes, const void *v_scales,
-                            int64_t num_blocks, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
-                            float scale, const int32_t *work, const pkv_work_info *info, void *out, void *workspace,
-                            uint64_t workspace_bytes, uint32_t *device_status, pkv_stream_t stream) {
+pkv_status pkv_cache_write_q8(const void *k_new, const void *v_new, const int64_t *slot_mapping,
+                              int64_t num_tokens, int8_t *k_codes, void *k_scales, int8_t *v_codes, void *v_scales,
+                              int64_t num_blocks, int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
+                              uint32_t *device_status, pkv_stream_t stream) {
+  return cache_write_quant(8, k_new, v_new, slot_mapping, num_tokens, k_codes, k_scales, v_codes, v_scales,
+                           num_blocks, block_size, num_kv_heads, head_dim, device_status, stream);
+}
+
+pkv_status pkv_cache_write_q4(const void *k_new, const void *v_new, const int64_t *slot_mapping,
+                              int64_t num_tokens, uint8_t *k_codes, void *k_scales, uint8_t *v_codes, void *v_scales,
+                              int64_t num_blocks, int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
+                              uint32_t *device_status, pkv_stream_t stream) {
+  return cache_write_quant(4, k_new, v_new, slot_mapping, num_tokens, reinterpret_cast<int8_t *>(k_codes), k_scales,
+                           reinterpret_cast<int8_t *>(v_codes), v_scales, num_blocks, block_size, num_kv_heads,
+                           head_dim, device_status, stream);
+}
+
+static pkv_status attention_quant(int32_t bits, const void *q, const int32_t *cu_seqlens_q, int32_t num_seqs,
+                                  int64_t total_q, const int32_t *seq_slot, const int32_t *context_lens,
+                                  const int32_t *block_tables, int32_t max_slots, int32_t max_blocks_per_slot,
+                                  int32_t block_size, const int8_t *k_codes, const void *k_scales,
+                                  const int8_t *v_codes, const void *v_scales, int64_t num_blocks,
+                                  int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, float scale,
+                                  const int32_t *work, const pkv_work_info *info, void *out, void *workspace,
+                                  uint64_t workspace_bytes, uint32_t *device_status, pkv_stream_t stream) {
   if (!info || num_seqs < 0 || total_q < 0 || max_slots <= 0 || max_blocks_per_slot <= 0 || num_blocks <= 0)
     return PKV_ERR_INVALID_ARG;
-  if (!supported_shape(block_size, num_q_heads, num_kv_heads, head_dim)) return PKV_ERR_UNSUPPORTED;
+  if (!supported_shape(block_size, num_q_heads, num_kv_heads, head_dim) || (bits == 4 && head_dim != 128))
+    return PKV_ERR_UNSUPPORTED;
   const int64_t rows = num_blocks * num_kv_heads * block_size;
   if (rows > INT32_MAX || total_q > INT32_MAX) return PKV_ERR_UNSUPPORTED;
   const int64_t items = static_cast<int64_t>(info->num_decode_items) + info->num_prefill_items +
@@ -351,7 +375,7 @@ pkv_status pkv_attention_q8(const void *q, const int32_t *cu_seqlens_q, int32_t 
 
   CUtensorMap tkc, tvc, tq, tk, tv;
   if (info->num_decode_items > 0 &&
-      (!encode_codes(&tkc, k_codes, rows, head_dim) || !encode_codes(&tvc, v_codes, rows, head_dim)))
+      (!encode_codes(&tkc, k_codes, rows, head_dim, bits) || !encode_codes(&tvc, v_codes, rows, head_dim, bits)))
     return PKV_ERR_CUDA;
   const int32_t rpt = pkv::prefill_rows_per_tile(a.group);
   if (info->num_prefill_items > 0) {
@@ -372,7 +396,7 @@ pkv_status pkv_attention_q8(const void *q, const int32_t *cu_seqlens_q, int32_t 
   cudaError_t e = side ? cudaEventRecord(side->fork, st) : cudaSuccess;
   if (e == cudaSuccess && info->num_prefill_items > 0) {
     e = pkv::launch_widen_q8(a, k_codes, k_scales, v_codes, v_scales, scratch_k, scratch_v, scratch_table,
-                             static_cast<int64_t>(sb), info->num_scratch_items, scr, st);
+                             static_cast<int64_t>(sb), info->num_scratch_items, scr, bits, st);
     if (e == cudaSuccess)
       e = head_dim == 128 ? pkv::launch_prefill_pair(c, tq, tk, tv, rpt, info->num_prefill_items, pre, st)
                           : pkv::launch_prefill(c, tq, rpt, info->num_prefill_items, pre, st);
@@ -380,7 +404,7 @@ pkv_status pkv_attention_q8(const void *q, const int32_t *cu_seqlens_q, int32_t 
   cudaStream_t dst = side ? side->stream : st;
   if (e == cudaSuccess && side) e = cudaStreamWaitEvent(side->stream, side->fork, 0);
   if (e == cudaSuccess)
-    e = pkv::launch_decode_q8(a, tkc, tvc, k_scales, v_scales, info->num_decode_items, dec, dst);
+    e = pkv::launch_decode_q8(a, tkc, tvc, k_scales, v_scales, info->num_decode_items, dec, bits, dst);
   if (e == cudaSuccess) e = pkv::launch_merge(a, info->num_combine_items, comb, dst);
   if (side) {
     const cudaError_t j = cudaEventRecord(side->join, side->stream);
@@ -388,6 +412,32 @@ pkv_status pkv_attention_q8(const void *q, const int32_t *cu_seqlens_q, int32_t 
     if (e == cudaSuccess) e = w;
   }
   return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+pkv_status pkv_attention_q8(const void *q, const int32_t *cu_seqlens_q, int32_t num_seqs, int64_t total_q,
+                            const int32_t *seq_slot, const int32_t *context_lens, const int32_t *block_tables,
+                            int32_t max_slots, int32_t max_blocks_per_slot, int32_t block_size,
+                            const int8_t *k_codes, const void *k_scales, const int8_t *v_codes, const void *v_scales,
+                            int64_t num_blocks, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                            float scale, const int32_t *work, const pkv_work_info *info, void *out, void *workspace,
+                            uint64_t workspace_bytes, uint32_t *device_status, pkv_stream_t stream) {
+  return attention_quant(8, q, cu_seqlens_q, num_seqs, total_q, seq_slot, context_lens, block_tables, max_slots,
+                         max_blocks_per_slot, block_size, k_codes, k_scales, v_codes, v_scales, num_blocks,
+                         num_q_heads, num_kv_heads, head_dim, scale, work, info, out, workspace, workspace_bytes,
+                         device_status, stream);
+}
+
+pkv_status pkv_attention_q4(const void *q, const int32_t *cu_seqlens_q, int32_t num_seqs, int64_t total_q,
+                            const int32_t *seq_slot, const int32_t *context_lens, const int32_t *block_tables,
+                            int32_t max_slots, int32_t max_blocks_per_slot, int32_t block_size,
+                            const uint8_t *k_codes, const void *k_scales, const uint8_t *v_codes,
+                            const void *v_scales, int64_t num_blocks, int32_t num_q_heads, int32_t num_kv_heads,
+                            int32_t head_dim, float scale, const int32_t *work, const pkv_work_info *info, void *out,
+                            void *workspace, uint64_t workspace_bytes, uint32_t *device_status, pkv_stream_t stream) {
+  return attention_quant(4, q, cu_seqlens_q, num_seqs, total_q, seq_slot, context_lens, block_tables, max_slots,
+                         max_blocks_per_slot, block_size, reinterpret_cast<const int8_t *>(k_codes), k_scales,
+                         reinterpret_cast<const int8_t *>(v_codes), v_scales, num_blocks, num_q_heads, num_kv_heads,
+                         head_dim, scale, work, info, out, workspace, workspace_bytes, device_status, stream);
 }
 
 pkv_status pkv_check_device_status(uint32_t *device_status, pkv_stream_t stream, uint32_t *bits_out) {

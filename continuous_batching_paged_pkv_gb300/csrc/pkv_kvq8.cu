@@ -54,8 +54,9 @@ __device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) { return __
 // ---- quantising cache write ---------------------------------------------------
 
 // One warp per (k or v, token, kv head) row; lane l holds D/32 consecutive
-// values, so one scale group spans 1024/D lanes.
-template <int D>
+// values, so one scale group spans 1024/D lanes. BITS = 8: one code per byte;
+// BITS = 4: codes in [-7, 7], two per byte, the even value in the low nibble.
+template <int D, int BITS>
 __global__ void __launch_bounds__(256) cache_write_q8_kernel(
     const __nv_bfloat16 *__restrict__ k_new, const __nv_bfloat16 *__restrict__ v_new,
     const int64_t *__restrict__ slot_mapping, int64_t num_tokens, int8_t *__restrict__ k_codes,
@@ -97,8 +98,9 @@ __global__ void __launch_bounds__(256) cache_write_q8_kernel(
     for (int i = 0; i < VPL; ++i) amax = fmaxf(amax, fabsf(x[i]));
 #pragma unroll
     for (int o = 1; o < LPG; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(kAll, amax, o));
-    // d: the smallest power of two >= amax / 127 (float32 quotient), at least 2^-126
-    const uint32_t tb = __float_as_uint(__fdiv_rn(amax, 127.f));
+    // d: the smallest power of two >= amax / Q (float32 quotient), at least 2^-126
+    constexpr float Q = BITS == 8 ? 127.f : 7.f;
+    const uint32_t tb = __float_as_uint(__fdiv_rn(amax, Q));
     const uint32_t te = tb & 0x7F800000u;
     uint32_t db = (tb & 0x007FFFFFu) == 0 ? tb : te + 0x00800000u;
     if (te == 0) db = 0x00800000u;
@@ -109,16 +111,18 @@ __global__ void __launch_bounds__(256) cache_write_q8_kernel(
 #pragma unroll
     for (int i = 0; i < VPL; ++i) {
       float c = d > 0.f ? rintf(__fdiv_rn(x[i], d)) : 0.f;
-      c = fminf(fmaxf(c, -127.f), 127.f);
-      packed |= (static_cast<uint32_t>(static_cast<int32_t>(c)) & 0xFFu) << (8 * i);
+      c = fminf(fmaxf(c, -Q), Q);
+      packed |= (static_cast<uint32_t>(static_cast<int32_t>(c)) & ((1u << BITS) - 1)) << (BITS * i);
     }
     const int64_t blk = s / block_size, row = s % block_size;
     const int64_t prow = (blk * num_kv_heads + h) * block_size + row;
-    int8_t *dst = (is_v ? v_codes : k_codes) + prow * D + lane * VPL;
-    if constexpr (VPL == 4)
+    int8_t *dst = (is_v ? v_codes : k_codes) + (prow * D + lane * VPL) * BITS / 8;
+    if constexpr (VPL * BITS == 32)
       *reinterpret_cast<uint32_t *>(dst) = packed;
-    else
+    else if constexpr (VPL * BITS == 16)
       *reinterpret_cast<uint16_t *>(dst) = static_cast<uint16_t>(packed);
+    else
+      *reinterpret_cast<uint8_t *>(dst) = static_cast<uint8_t>(packed);
     if (lane % LPG == 0) (is_v ? v_scales : k_scales)[prow * (D / 32) + lane / LPG] = dq;
   }
 }
@@ -128,7 +132,7 @@ __global__ void __launch_bounds__(256) cache_write_q8_kernel(
 // Item (segment, slot, first scratch block, blocks). CTA (item, y) widens the
 // item's logical blocks y, y + gridDim.y, ... : block j of the slot becomes
 // scratch block first + j, and the scratch table row of the slot points there.
-template <int D>
+template <int D, int BITS>
 __global__ void __launch_bounds__(256) widen_q8_kernel(const StepArgs a, const int32_t *__restrict__ items,
                                                        const int8_t *__restrict__ k_codes,
                                                        const __nv_bfloat16 *__restrict__ k_scales,
@@ -167,18 +171,28 @@ __global__ void __launch_bounds__(256) widen_q8_kernel(const StepArgs a, const i
       const int64_t r = e / (D / 8), c8 = e % (D / 8);
       uint4 outv = make_uint4(0, 0, 0, 0);
       if (in_pool) {
-        const int8_t *codes = (is_v ? v_codes : k_codes) + (src_row0 + r) * D + c8 * 8;
+        const int8_t *codes = (is_v ? v_codes : k_codes) + ((src_row0 + r) * D + c8 * 8) * BITS / 8;
         const __nv_bfloat16 *sc = (is_v ? v_scales : k_scales) + (src_row0 + r) * NG + (c8 * 8) / 32;
-        const uint2 raw = __ldg(reinterpret_cast<const uint2 *>(codes));
         const float d = __bfloat162float(*sc);
         uint32_t w[4];
+        if constexpr (BITS == 8) {
+          const uint2 raw = __ldg(reinterpret_cast<const uint2 *>(codes));
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint32_t word = q < 2 ? raw.x : raw.y;
-          const int b0 = (q & 1) * 2;
-          const float lo = static_cast<float>(static_cast<int8_t>((word >> (8 * b0)) & 0xFF)) * d;
-          const float hi = static_cast<float>(static_cast<int8_t>((word >> (8 * (b0 + 1))) & 0xFF)) * d;
-          w[q] = pack_bf16x2(lo, hi);
+          for (int q = 0; q < 4; ++q) {
+            const uint32_t word = q < 2 ? raw.x : raw.y;
+            const int b0 = (q & 1) * 2;
+            const float lo = static_cast<float>(static_cast<int8_t>((word >> (8 * b0)) & 0xFF)) * d;
+            const float hi = static_cast<float>(static_cast<int8_t>((word >> (8 * (b0 + 1))) & 0xFF)) * d;
+            w[q] = pack_bf16x2(lo, hi);
+          }
+        } else {  // eight nibbles, value 2q in the low nibble of byte q; sign-extended by shifts
+          const uint32_t raw = __ldg(reinterpret_cast<const uint32_t *>(codes));
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float lo = static_cast<float>(static_cast<int32_t>(raw << (28 - 8 * q)) >> 28) * d;
+            const float hi = static_cast<float>(static_cast<int32_t>(raw << (24 - 8 * q)) >> 28) * d;
+            w[q] = pack_bf16x2(lo, hi);
+          }
         }
         outv = make_uint4(w[0], w[1], w[2], w[3]);
       }
@@ -190,12 +204,13 @@ __global__ void __launch_bounds__(256) widen_q8_kernel(const StepArgs a, const i
 // ---- split-KV decode over the codes ---------------------------------------------
 
 // NW warps per CTA (the ring depth follows from the shared memory they share).
-template <int D, int NW>
+template <int D, int NW, int BITS>
 struct Q8Cfg {
   static constexpr int kGroups = D / 32;
-  static constexpr int kCodeBytes = kSubKeys * D;              // K (or V) codes of one sub-tile
+  static constexpr int kCodeBytes = kSubKeys * D * BITS / 8;   // K (or V) codes of one sub-tile
   static constexpr int kScaleBytes = kSubKeys * kGroups * 2;   // their scales
-  static constexpr int kStages = (D == 128 ? 48 : 96) / NW;  // 6 or 12 at eight warps
+  static constexpr int kRowBytes = D * BITS / 8;               // one key's codes (128 or 64 bytes)
+  static constexpr int kStages = (D * BITS == 1024 ? 48 : 96) / NW;  // 6 or 12 at eight warps
   static constexpr int kVc = kStages * kCodeBytes;             // offsets inside a warp's ring
   static constexpr int kKs = 2 * kStages * kCodeBytes;
   static constexpr int kVs = kKs + kStages * kScaleBytes;
@@ -234,10 +249,45 @@ __device__ __forceinline__ uint32_t codes_to_bf16_pair(uint32_t ux, uint32_t uy,
   return prmt(__float_as_uint(fx), __float_as_uint(fy), 0x7632u);  // upper halves: exact for integers
 }
 
+// Eight 4-bit codes (a word, value 2i in the low nibble of byte i, two's
+// complement) -> four fp16 pairs of the integer values: (lo0, hi0) hold values
+// 0..3, (lo1, hi1) values 4..7. The nibbles are offset by 8 and placed under
+// the exponent of 1024.0, one subtraction of 1032 away from the code.
+__device__ __forceinline__ void nibbles_to_f16(uint32_t w, uint32_t &lo0, uint32_t &hi0, uint32_t &lo1,
+                                               uint32_t &hi1) {
+  const uint32_t x = w ^ 0x88888888u;
+  const uint32_t ev = x & 0x0F0F0F0Fu, od = (x >> 4) & 0x0F0F0F0Fu;  // values 0,2,4,6 and 1,3,5,7
+  const uint32_t t0 = prmt(ev, od, 0x5140u), t1 = prmt(ev, od, 0x7362u);  // values 0..3, 4..7 as bytes
+  const uint32_t m = 0x64086408u;                                      // 1032 in both halves
+  const uint32_t a0 = prmt(t0, 0x64646464u, 0x4140u), b0 = prmt(t0, 0x64646464u, 0x4342u);
+  const uint32_t a1 = prmt(t1, 0x64646464u, 0x4140u), b1 = prmt(t1, 0x64646464u, 0x4342u);
+  const __half2 hm = *reinterpret_cast<const __half2 *>(&m);
+  __half2 r;
+  r = __hsub2(*reinterpret_cast<const __half2 *>(&a0), hm);
+  lo0 = *reinterpret_cast<uint32_t *>(&r);
+  r = __hsub2(*reinterpret_cast<const __half2 *>(&b0), hm);
+  hi0 = *reinterpret_cast<uint32_t *>(&r);
+  r = __hsub2(*reinterpret_cast<const __half2 *>(&a1), hm);
+  lo1 = *reinterpret_cast<uint32_t *>(&r);
+  r = __hsub2(*reinterpret_cast<const __half2 *>(&b1), hm);
+  hi1 = *reinterpret_cast<uint32_t *>(&r);
+}
+
+// Nibble `n` of both halves of x (two keys' 4-bit codes, offset by 8) -> one
+// bf16 pair of the codes: 128 + u is a bfloat16 integer for u < 16.
+__device__ __forceinline__ uint32_t nibble_pair_to_bf16(uint32_t x, int n) {
+  const uint32_t t = ((x >> (4 * n)) & 0x000F000Fu) | 0x43004300u;
+  const __nv_bfloat162 r =
+      __hsub2(*reinterpret_cast<const __nv_bfloat162 *>(&t), __floats2bfloat162_rn(136.f, 136.f));
+  return *reinterpret_cast<const uint32_t *>(&r);
+}
+
 // Q'^T fragments (B operand, fp16) for k-step kk = 2 g + h: thread (column
-// lane/4, j = lane%4) holds q[column][32 g + 16 h + 4 j + 0..3], scaled by
-// 2^sh (per column) so that max |q'| < 2^15; `inv` receives 2^-sh.
-template <int D, int NT, bool MULTI>
+// lane/4, j = lane%4) holds q[column][32 g + 16 h + 4 j + 0..3] (8-bit codes)
+// or q[column][32 g + 8 j + 4 h + 0..3] (4-bit codes: a thread's code word
+// holds dims 32 g + 8 j .. + 7), scaled by 2^sh (per column) so that
+// max |q'| < 2^15; `inv` receives 2^-sh.
+template <int D, int NT, bool MULTI, int BITS>
 __device__ __forceinline__ void load_q_q8(uint32_t (&qf)[NT][D / 16][2], float (&inv)[NT], const Task &T,
                                           const StepArgs &a, int lane) {
   constexpr int KT = D / 16;
@@ -253,8 +303,8 @@ __device__ __forceinline__ void load_q_q8(uint32_t (&qf)[NT][D / 16][2], float (
     float mx = 0.f;
 #pragma unroll
     for (int kk = 0; kk < KT; ++kk) {
-      raw[kk] = valid ? __ldg(reinterpret_cast<const uint2 *>(qrow + 32 * (kk >> 1) + 16 * (kk & 1) + 4 * j))
-                      : make_uint2(0, 0);
+      const int dim0 = BITS == 8 ? 32 * (kk >> 1) + 16 * (kk & 1) + 4 * j : 32 * (kk >> 1) + 8 * j + 4 * (kk & 1);
+      raw[kk] = valid ? __ldg(reinterpret_cast<const uint2 *>(qrow + dim0)) : make_uint2(0, 0);
       mx = fmaxf(mx, fmaxf(fmaxf(fabsf(bf16_bits_to_float(raw[kk].x & 0xFFFFu)),
                                  fabsf(bf16_bits_to_float(raw[kk].x >> 16))),
                            fmaxf(fabsf(bf16_bits_to_float(raw[kk].y & 0xFFFFu)),
@@ -279,12 +329,14 @@ __device__ __forceinline__ void load_q_q8(uint32_t (&qf)[NT][D / 16][2], float (
   }
 }
 
-template <int D, int NT, bool MULTI, int NW>
+template <int D, int NT, bool MULTI, int NW, int BITS>
 __global__ void __launch_bounds__(NW * 32, 1)
     decode_q8_kernel(const __grid_constant__ CUtensorMap tmap_kc, const __grid_constant__ CUtensorMap tmap_vc,
                      const StepArgs a, const __nv_bfloat16 *__restrict__ k_scales,
                      const __nv_bfloat16 *__restrict__ v_scales, const int32_t *__restrict__ items, int num_items) {
-  using Cfg = Q8Cfg<D, NW>;
+  using Cfg = Q8Cfg<D, NW, BITS>;
+  static_assert(BITS == 8 || D == 128, "4-bit codes need head_dim 128 (64-byte code rows)");
+  constexpr int RB = Cfg::kRowBytes;  // code row layout: 128-byte rows (128B swizzle) or 64-byte (64B)
   constexpr int KT = D / 16;  // k-steps of QK^T, m-tiles of PV
   constexpr int NG = Cfg::kGroups;
   constexpr int NST = Cfg::kStages;
@@ -327,7 +379,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
   finalize(A, a, lane, 8 * NT, kMaxRows);
   uint32_t qA[NT][KT][2], qB[NT][KT][2];
   float invA[NT], invB[NT];
-  if (A.ok) load_q_q8<D, NT, MULTI>(qA, invA, A, a, lane);
+  if (A.ok) load_q_q8<D, NT, MULTI, BITS>(qA, invA, A, a, lane);
   bool qB_loaded = false;
 
   int P = 0, C = 0, pa = 0, pb = 0;
@@ -365,7 +417,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
       if (!B.finalized) {
         finalize(B, a, lane, 8 * NT, kMaxRows);
         if (B.ok) {
-          load_q_q8<D, NT, MULTI>(qB, invB, B, a, lane);
+          load_q_q8<D, NT, MULTI, BITS>(qB, invB, B, a, lane);
           qB_loaded = true;
         }
       }
@@ -384,7 +436,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
   const int G = a.group;
   const int ka = lane >> 2, kb = ka + 8, jq = lane & 3, k0 = jq * 2, r = lane >> 2;
   // per-thread code offsets inside a sub-tile (rows kb = ka + 8 and k0 + 8 share the swizzle phase)
-  const uint32_t koff = code_off<D>(ka, 4 * jq);  // + group/half chunk below
+  const uint32_t koff = code_off<RB>(ka, 4 * jq);  // + group/half chunk below
   int cstage = 0;
   uint32_t cphase = 0;
 
@@ -440,17 +492,36 @@ __global__ void __launch_bounds__(NW * 32, 1)
       for (int g = 0; g < NG; ++g)
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) sg[g][nt][0] = sg[g][nt][1] = sg[g][nt][2] = sg[g][nt][3] = 0.f;
+      if constexpr (BITS == 8) {
 #pragma unroll
-      for (int kk = 0; kk < KT; ++kk) {
-        // chunk 2g + h of rows ka / kb: the swizzle XORs the chunk index
-        const uint32_t off = koff ^ (static_cast<uint32_t>(kk) << 4);
-        const uint32_t wa = lds32(kc + off);
-        const uint32_t wb = lds32(kc + off + 8 * (D == 128 ? 128 : 64));
-        uint32_t af[4];
-        codes_to_f16(wa, af[0], af[2]);
-        codes_to_f16(wb, af[1], af[3]);
+        for (int kk = 0; kk < KT; ++kk) {
+          // chunk 2g + h of rows ka / kb: the swizzle XORs the chunk index
+          const uint32_t off = koff ^ (static_cast<uint32_t>(kk) << 4);
+          const uint32_t wa = lds32(kc + off);
+          const uint32_t wb = lds32(kc + off + 8 * RB);
+          uint32_t af[4];
+          codes_to_f16(wa, af[0], af[2]);
+          codes_to_f16(wb, af[1], af[3]);
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) mma_f16_16816(sg[kk >> 1][nt], af, qA[nt][kk][0], qA[nt][kk][1]);
+          for (int nt = 0; nt < NT; ++nt) mma_f16_16816(sg[kk >> 1][nt], af, qA[nt][kk][0], qA[nt][kk][1]);
+        }
+      } else {
+#pragma unroll
+        for (int g = 0; g < NG; ++g) {
+          // chunk g of rows ka / kb holds dims 32 g .. 32 g + 31; this thread's word, dims 32 g + 8 jq + 0..7,
+          // feeds k-steps 2 g (dims + 0..3) and 2 g + 1 (dims + 4..7)
+          const uint32_t off = koff ^ (static_cast<uint32_t>(g) << 4);
+          const uint32_t wa = lds32(kc + off);
+          const uint32_t wb = lds32(kc + off + 8 * RB);
+          uint32_t a0[4], a1[4];
+          nibbles_to_f16(wa, a0[0], a0[2], a1[0], a1[2]);
+          nibbles_to_f16(wb, a0[1], a0[3], a1[1], a1[3]);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            mma_f16_16816(sg[g][nt], a0, qA[nt][2 * g][0], qA[nt][2 * g][1]);
+            mma_f16_16816(sg[g][nt], a1, qA[nt][2 * g + 1][0], qA[nt][2 * g + 1][1]);
+          }
+        }
       }
       // group scales of keys ka and kb; V scales of the same keys, zero past the sub-tile's keys
       float dka[NG], dkb[NG], dva[NG], dvb[NG];
@@ -544,20 +615,39 @@ __global__ void __launch_bounds__(NW * 32, 1)
       // head_dim 32 g + 4 r + 2 h (+ 1); keys k0, k0 + 1 (+ 8).
 #pragma unroll
       for (int g = 0; g < NG; ++g) {
-        const int col = 32 * g + 4 * r;
-        const uint32_t u0 = lds32(vc + code_off<D>(k0, col)) ^ 0x80808080u;
-        const uint32_t u1 = lds32(vc + code_off<D>(k0 + 1, col)) ^ 0x80808080u;
-        const uint32_t u8 = lds32(vc + code_off<D>(k0 + 8, col)) ^ 0x80808080u;
-        const uint32_t u9 = lds32(vc + code_off<D>(k0 + 9, col)) ^ 0x80808080u;
+        if constexpr (BITS == 8) {
+          const int col = 32 * g + 4 * r;
+          const uint32_t u0 = lds32(vc + code_off<RB>(k0, col)) ^ 0x80808080u;
+          const uint32_t u1 = lds32(vc + code_off<RB>(k0 + 1, col)) ^ 0x80808080u;
+          const uint32_t u8 = lds32(vc + code_off<RB>(k0 + 8, col)) ^ 0x80808080u;
+          const uint32_t u9 = lds32(vc + code_off<RB>(k0 + 9, col)) ^ 0x80808080u;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t af[4];
-          af[0] = codes_to_bf16_pair(u0, u1, 2 * h);
-          af[1] = codes_to_bf16_pair(u0, u1, 2 * h + 1);
-          af[2] = codes_to_bf16_pair(u8, u9, 2 * h);
-          af[3] = codes_to_bf16_pair(u8, u9, 2 * h + 1);
+          for (int h = 0; h < 2; ++h) {
+            uint32_t af[4];
+            af[0] = codes_to_bf16_pair(u0, u1, 2 * h);
+            af[1] = codes_to_bf16_pair(u0, u1, 2 * h + 1);
+            af[2] = codes_to_bf16_pair(u8, u9, 2 * h);
+            af[3] = codes_to_bf16_pair(u8, u9, 2 * h + 1);
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(acc[nt][2 * g + h], af, pf[g][nt][0], pf[g][nt][1]);
+            for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(acc[nt][2 * g + h], af, pf[g][nt][0], pf[g][nt][1]);
+          }
+        } else {
+          // the four codes of dims 32 g + 4 r .. + 3 of a key are one 16-bit word (byte 16 g + 2 r)
+          const int col = 16 * g + 2 * r;
+          const uint32_t x01 = (lds16(vc + code_off<RB>(k0, col)) | (lds16(vc + code_off<RB>(k0 + 1, col)) << 16)) ^
+                               0x88888888u;
+          const uint32_t x89 =
+              (lds16(vc + code_off<RB>(k0 + 8, col)) | (lds16(vc + code_off<RB>(k0 + 9, col)) << 16)) ^ 0x88888888u;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint32_t af[4];
+            af[0] = nibble_pair_to_bf16(x01, 2 * h);
+            af[1] = nibble_pair_to_bf16(x01, 2 * h + 1);
+            af[2] = nibble_pair_to_bf16(x89, 2 * h);
+            af[3] = nibble_pair_to_bf16(x89, 2 * h + 1);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(acc[nt][2 * g + h], af, pf[g][nt][0], pf[g][nt][1]);
+          }
         }
       }
       __syncwarp();  // every read of this stage is consumed before the ring refills it
@@ -645,7 +735,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
           }
         }
       } else if (A.ok) {
-        load_q_q8<D, NT, MULTI>(qA, invA, A, a, lane);
+        load_q_q8<D, NT, MULTI, BITS>(qA, invA, A, a, lane);
       }
     }
     qB_loaded = false;
@@ -657,18 +747,18 @@ __global__ void __launch_bounds__(NW * 32, 1)
   }
 }
 
-template <int D, int NT, bool MULTI, int NW>
+template <int D, int NT, bool MULTI, int NW, int BITS>
 cudaError_t launch_decode_q8_w(const StepArgs &a, const CUtensorMap &tk, const CUtensorMap &tv,
                                const void *k_scales, const void *v_scales, int32_t num_items, const int32_t *items,
                                int grid, cudaStream_t stream) {
-  constexpr int smem = Q8Cfg<D, NW>::kSmem;
+  constexpr int smem = Q8Cfg<D, NW, BITS>::kSmem;
   static uint64_t configured = 0;  // one bit per device
   int dev = 0;
   cudaGetDevice(&dev);
   const uint64_t bit = 1ull << (dev & 63);
   if (!(configured & bit)) {
-    cudaError_t e =
-        cudaFuncSetAttribute(decode_q8_kernel<D, NT, MULTI, NW>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = cudaFuncSetAttribute(decode_q8_kernel<D, NT, MULTI, NW, BITS>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     configured |= bit;
   }
@@ -680,17 +770,17 @@ cudaError_t launch_decode_q8_w(const StepArgs &a, const CUtensorMap &tk, const C
   } else {
     b.task_counter = nullptr;
   }
-  return launch_pdl(decode_q8_kernel<D, NT, MULTI, NW>, dim3(grid), dim3(NW * 32), smem, stream, tk, tv, b,
+  return launch_pdl(decode_q8_kernel<D, NT, MULTI, NW, BITS>, dim3(grid), dim3(NW * 32), smem, stream, tk, tv, b,
                     static_cast<const __nv_bfloat16 *>(k_scales), static_cast<const __nv_bfloat16 *>(v_scales),
                     items, num_items);
 }
 
-// Eight warps x six stages (head_dim 128); single-row, single-tile steps with
-// more than three rounds of tasks run 12 warps x 4 stages instead: the code
-// conversions make a warp's sub-tile a long dependent chain, and more warps
-// per scheduler hide it once every warp has work (a small step's few busy
-// warps stream faster through deeper rings).
-template <int D, int NT, bool MULTI>
+// Eight warps (six stages at head_dim 128 with 8-bit codes, twice that with
+// 4-bit ones); single-row, single-tile steps with more than three rounds of
+// tasks run 12 warps instead: the code conversions make a warp's sub-tile a
+// long dependent chain, and more warps per scheduler hide it once every warp
+// has work (a small step's few busy warps stream faster through deeper rings).
+template <int D, int NT, bool MULTI, int BITS>
 cudaError_t launch_decode_q8_t(const StepArgs &a, const CUtensorMap &tk, const CUtensorMap &tv,
                                const void *k_scales, const void *v_scales, int32_t num_items, const int32_t *items,
                                cudaStream_t stream) {
@@ -701,9 +791,11 @@ cudaError_t launch_decode_q8_t(const StepArgs &a, const CUtensorMap &tk, const C
   const int grid = static_cast<int>(tasks < sms ? tasks : sms);
   if constexpr (D == 128 && NT == 1 && !MULTI) {
     if (tasks > 3ll * grid * 12)
-      return launch_decode_q8_w<D, NT, MULTI, 12>(a, tk, tv, k_scales, v_scales, num_items, items, grid, stream);
+      return launch_decode_q8_w<D, NT, MULTI, 12, BITS>(a, tk, tv, k_scales, v_scales, num_items, items, grid,
+                                                         stream);
   }
-  return launch_decode_q8_w<D, NT, MULTI, kWarpsQ8>(a, tk, tv, k_scales, v_scales, num_items, items, grid, stream);
+  return launch_decode_q8_w<D, NT, MULTI, kWarpsQ8, BITS>(a, tk, tv, k_scales, v_scales, num_items, items, grid,
+                                                           stream);
 }
 
 }  // namespace
@@ -711,7 +803,7 @@ cudaError_t launch_decode_q8_t(const StepArgs &a, const CUtensorMap &tk, const C
 cudaError_t launch_cache_write_q8(const void *k_new, const void *v_new, const int64_t *slot_mapping,
                                   int64_t num_tokens, void *k_codes, void *k_scales, void *v_codes, void *v_scales,
                                   int64_t num_blocks, int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
-                                  uint32_t *status, cudaStream_t stream) {
+                                  int32_t bits, uint32_t *status, cudaStream_t stream) {
   const int64_t rows = 2 * num_tokens * num_kv_heads;
   int64_t blocks = (rows + 7) / 8;  // 8 warps per CTA, one row each
   if (blocks > 152 * 16) blocks = 152 * 16;
@@ -722,48 +814,66 @@ cudaError_t launch_cache_write_q8(const void *k_new, const void *v_new, const in
   auto *vc = static_cast<int8_t *>(v_codes);
   auto *ksc = static_cast<__nv_bfloat16 *>(k_scales);
   auto *vsc = static_cast<__nv_bfloat16 *>(v_scales);
+  const int64_t prows = num_blocks * block_size;
+  if (bits == 4)
+    return launch_pdl(cache_write_q8_kernel<128, 4>, grid, dim3(256), 0, stream, kn, vn, slot_mapping, num_tokens,
+                      kc, ksc, vc, vsc, prows, block_size, num_kv_heads, status);
   if (head_dim == 128)
-    return launch_pdl(cache_write_q8_kernel<128>, grid, dim3(256), 0, stream, kn, vn, slot_mapping, num_tokens, kc,
-                      ksc, vc, vsc, num_blocks * block_size, block_size, num_kv_heads, status);
-  return launch_pdl(cache_write_q8_kernel<64>, grid, dim3(256), 0, stream, kn, vn, slot_mapping, num_tokens, kc, ksc,
-                    vc, vsc, num_blocks * block_size, block_size, num_kv_heads, status);
+    return launch_pdl(cache_write_q8_kernel<128, 8>, grid, dim3(256), 0, stream, kn, vn, slot_mapping, num_tokens,
+                      kc, ksc, vc, vsc, prows, block_size, num_kv_heads, status);
+  return launch_pdl(cache_write_q8_kernel<64, 8>, grid, dim3(256), 0, stream, kn, vn, slot_mapping, num_tokens, kc,
+                    ksc, vc, vsc, prows, block_size, num_kv_heads, status);
 }
 
 cudaError_t launch_widen_q8(const StepArgs &a, const void *k_codes, const void *k_scales, const void *v_codes,
                             const void *v_scales, void *k_out, void *v_out, int32_t *scratch_table,
-                            int64_t scratch_blocks, int32_t num_items, const int32_t *items, cudaStream_t stream) {
+                            int64_t scratch_blocks, int32_t num_items, const int32_t *items, int32_t bits,
+                            cudaStream_t stream) {
   if (num_items <= 0) return cudaSuccess;
   // about four CTAs per SM over all items; a CTA whose first block is past its item's end exits
   const int per_item = (4 * 152 + num_items - 1) / num_items;
-  const dim3 grid(static_cast<unsigned>(num_items), static_cast<unsigned>(per_item < 1 ? 1 : per_item > 512 ? 512 : per_item));
+  const dim3 grid(static_cast<unsigned>(num_items),
+                  static_cast<unsigned>(per_item < 1 ? 1 : per_item > 512 ? 512 : per_item));
   auto *kc = static_cast<const int8_t *>(k_codes);
   auto *vc = static_cast<const int8_t *>(v_codes);
   auto *ksc = static_cast<const __nv_bfloat16 *>(k_scales);
   auto *vsc = static_cast<const __nv_bfloat16 *>(v_scales);
   auto *ko = static_cast<__nv_bfloat16 *>(k_out);
   auto *vo = static_cast<__nv_bfloat16 *>(v_out);
-  if (a.head_dim == 128)
-    return launch_pdl(widen_q8_kernel<128>, grid, dim3(256), 0, stream, a, items, kc, ksc, vc, vsc, ko, vo,
+  if (bits == 4)
+    return launch_pdl(widen_q8_kernel<128, 4>, grid, dim3(256), 0, stream, a, items, kc, ksc, vc, vsc, ko, vo,
                       scratch_table, scratch_blocks);
-  return launch_pdl(widen_q8_kernel<64>, grid, dim3(256), 0, stream, a, items, kc, ksc, vc, vsc, ko, vo,
+  if (a.head_dim == 128)
+    return launch_pdl(widen_q8_kernel<128, 8>, grid, dim3(256), 0, stream, a, items, kc, ksc, vc, vsc, ko, vo,
+                      scratch_table, scratch_blocks);
+  return launch_pdl(widen_q8_kernel<64, 8>, grid, dim3(256), 0, stream, a, items, kc, ksc, vc, vsc, ko, vo,
                     scratch_table, scratch_blocks);
 }
 
 cudaError_t launch_decode_q8(const StepArgs &a, const CUtensorMap &tk, const CUtensorMap &tv, const void *k_scales,
-                             const void *v_scales, int32_t num_items, const int32_t *items, cudaStream_t stream) {
+                             const void *v_scales, int32_t num_items, const int32_t *items, int32_t bits,
+                             cudaStream_t stream) {
   if (num_items <= 0) return cudaSuccess;
   const bool multi = a.decode_rows_max > 1;
   const bool wide = a.group * (multi ? a.decode_rows_max : 1) > 8;
-  const int v = (a.head_dim == 128 ? 4 : 0) + (wide ? 2 : 0) + (multi ? 1 : 0);
-  switch (v) {
-    case 0: return launch_decode_q8_t<64, 1, false>(a, tk, tv, k_scales, v_scales, num_items, items, stream);
-    case 1: return launch_decode_q8_t<64, 1, true>(a, tk, tv, k_scales, v_scales, num_items, items, stream);
-    case 2: return launch_decode_q8_t<64, 2, false>(a, tk, tv, k_scales, v_scales, num_items, items, stream);
-    case 3: return launch_decode_q8_t<64, 2, true>(a, tk, tv, k_scales, v_scales, num_items, items, stream);
-    case 4: return launch_decode_q8_t<128, 1, false>(a, tk, tv, k_scales, v_scales, num_items, items, stream);
-    case 5: return launch_decode_q8_t<128, 1, true>(a, tk, tv, k_scales, v_scales, num_items, items, stream);
-    case 6: return launch_decode_q8_t<128, 2, false>(a, tk, tv, k_scales, v_scales, num_items, items, stream);
-    default: return launch_decode_q8_t<128, 2, true>(a, tk, tv, k_scales, v_scales, num_items, items, stream);
+  const int v = (wide ? 2 : 0) + (multi ? 1 : 0);
+  if (bits == 4) {  // head_dim 128 only
+    switch (v) {
+      case 0: return launch_decode_q8_t<128, 1, false, 4>(a, tk, tv, k_scales, v_scales, num_items, items, stream);
+      case 1: return launch_decode_q8_t<128, 1, true, 4>(a, tk, tv, k_scales, v_scales, num_items, items, stream);
+      case 2: return launch_decode_q8_t<128, 2, false, 4>(a, tk, tv, k_scales, v_scales, num_items, items, stream);
+      default: return launch_decode_q8_t<128, 2, true, 4>(a, tk, tv, k_scales, v_scales, num_items, items, stream);
+    }
+  }
+  switch (v + (a.head_dim == 128 ? 4 : 0)) {
+    case 0: return launch_decode_q8_t<64, 1, false, 8>(a, tk, tv, k_scales, v_scales, num_items, items, stream);
+    case 1: return launch_decode_q8_t<64, 1, true, 8>(a, tk, tv, k_scales, v_scales, num_items, items, stream);
+    case 2: return launch_decode_q8_t<64, 2, false, 8>(a, tk, tv, k_scales, v_scales, num_items, items, stream);
+    case 3: return launch_decode_q8_t<64, 2, true, 8>(a, tk, tv, k_scales, v_scales, num_items, items, stream);
+    case 4: return launch_decode_q8_t<128, 1, false, 8>(a, tk, tv, k_scales, v_scales, num_items, items, stream);
+    case 5: return launch_decode_q8_t<128, 1, true, 8>(a, tk, tv, k_scales, v_scales, num_items, items, stream);
+    case 6: return launch_decode_q8_t<128, 2, false, 8>(a, tk, tv, k_scales, v_scales, num_items, items, stream);
+    default: return launch_decode_q8_t<128, 2, true, 8>(a, tk, tv, k_scales, v_scales, num_items, items, stream);
   }
 }
 

@@ -56,12 +56,17 @@ def empty_pool(num_blocks, num_kv_heads, block_size, head_dim, device):
     return k, v
 
 
-def empty_pool_q8(num_blocks, num_kv_heads, block_size, head_dim, device):
-    """(k_codes, k_scales, v_codes, v_scales) of an 8-bit pool; scales of rows never written are NaN."""
+def empty_pool_q8(num_blocks, num_kv_heads, block_size, head_dim, device, bits: int = 8):
+    """(k_codes, k_scales, v_codes, v_scales) of an 8-bit (int8 codes) or 4-bit (uint8, two codes per byte)
+    pool; codes of rows never written hold the unused code -2^(bits-1), scales NaN."""
     import torch
 
-    codes = [torch.full((num_blocks, num_kv_heads, block_size, head_dim), -128, dtype=torch.int8, device=device)
-             for _ in range(2)]
+    if bits == 8:
+        codes = [torch.full((num_blocks, num_kv_heads, block_size, head_dim), -128, dtype=torch.int8, device=device)
+                 for _ in range(2)]
+    else:
+        codes = [torch.full((num_blocks, num_kv_heads, block_size, head_dim // 2), 0x88, dtype=torch.uint8,
+                            device=device) for _ in range(2)]
     scales = [torch.empty((num_blocks, num_kv_heads, block_size, head_dim // 32), dtype=torch.bfloat16,
                           device=device) for _ in range(2)]
     for t in scales:
@@ -89,7 +94,7 @@ class DeviceStep:
     workspace: object
     out: object
     status: object
-    kv: str = "bf16"          # pool format: "bf16", or "q8" (k_pool/v_pool hold the codes)
+    kv: str = "bf16"          # pool format: "bf16", "q8" or "q4" (k_pool/v_pool hold the codes)
     k_scales: object = None
     v_scales: object = None
 
@@ -101,17 +106,17 @@ class DeviceStep:
 def prepare(w, device="cuda", *, pools=None, kv: str = "bf16") -> DeviceStep:
     """Build the pool state before the step and upload the step's inputs.
 
-    ``kv="q8"`` keeps the pool in the 8-bit block-scaled format (history
-    written through ``pkv_cache_write_q8``)."""
+    ``kv="q8"`` / ``kv="q4"`` keep the pool in the 8-bit / 4-bit block-scaled
+    format (history written through ``pkv_cache_write_q8`` / ``_q4``)."""
     import torch
 
     pool = B.Pool(w.num_blocks, w.block_size, w.max_slots, w.max_blocks_per_slot)
     for slot in sorted(w.blocks):
         pool.admit_blocks(slot, w.blocks[slot])
     k_scales = v_scales = None
-    if kv == "q8":
+    if kv in ("q8", "q4"):
         k_pool, k_scales, v_pool, v_scales = pools if pools is not None else empty_pool_q8(
-            w.num_blocks, w.num_kv_heads, w.block_size, w.head_dim, device)
+            w.num_blocks, w.num_kv_heads, w.block_size, w.head_dim, device, bits=int(kv[1]))
     elif kv == "bf16":
         k_pool, v_pool = pools if pools is not None else empty_pool(
             w.num_blocks, w.num_kv_heads, w.block_size, w.head_dim, device)
@@ -125,9 +130,10 @@ def prepare(w, device="cuda", *, pools=None, kv: str = "bf16") -> DeviceStep:
     if len(hist.slot_mapping):
         hk = np.concatenate([w.hist_k[s.slot][: s.ctx - s.q_len] for s in w.segments])
         hv = np.concatenate([w.hist_v[s.slot][: s.ctx - s.q_len] for s in w.segments])
-        if kv == "q8":
-            B.pkv_cache_write_q8(_bf16_tensor(hk, device), _bf16_tensor(hv, device), _i64(hist.slot_mapping, device),
-                                 k_pool, k_scales, v_pool, v_scales, device_status=status)
+        if kv in ("q8", "q4"):
+            write = B.pkv_cache_write_q8 if kv == "q8" else B.pkv_cache_write_q4
+            write(_bf16_tensor(hk, device), _bf16_tensor(hv, device), _i64(hist.slot_mapping, device),
+                  k_pool, k_scales, v_pool, v_scales, device_status=status)
         else:
             B.pkv_cache_write(_bf16_tensor(hk, device), _bf16_tensor(hv, device), _i64(hist.slot_mapping, device),
                               k_pool, v_pool, device_status=status)
@@ -137,7 +143,7 @@ def prepare(w, device="cuda", *, pools=None, kv: str = "bf16") -> DeviceStep:
                                  max_blocks_per_slot=w.max_blocks_per_slot, block_size=w.block_size,
                                  num_q_heads=w.num_q_heads, num_kv_heads=w.num_kv_heads, head_dim=w.head_dim)
     ws = None
-    ws_bytes = int(info.workspace_bytes_q8 if kv == "q8" else info.workspace_bytes)
+    ws_bytes = int(info.workspace_bytes_q8 if kv in ("q8", "q4") else info.workspace_bytes)
     if ws_bytes:
         ws = torch.empty(ws_bytes, dtype=torch.uint8, device=device)
     out = torch.empty((w.total_q, w.num_q_heads, w.head_dim), dtype=torch.bfloat16, device=device)
@@ -152,19 +158,21 @@ def prepare(w, device="cuda", *, pools=None, kv: str = "bf16") -> DeviceStep:
 
 
 def run_cache_write(ds: DeviceStep, stream=None) -> None:
-    if ds.kv == "q8":
-        B.pkv_cache_write_q8(ds.k_new, ds.v_new, ds.slot_mapping, ds.k_pool, ds.k_scales, ds.v_pool, ds.v_scales,
-                             device_status=ds.status, stream=stream)
+    if ds.kv in ("q8", "q4"):
+        write = B.pkv_cache_write_q8 if ds.kv == "q8" else B.pkv_cache_write_q4
+        write(ds.k_new, ds.v_new, ds.slot_mapping, ds.k_pool, ds.k_scales, ds.v_pool, ds.v_scales,
+              device_status=ds.status, stream=stream)
     else:
         B.pkv_cache_write(ds.k_new, ds.v_new, ds.slot_mapping, ds.k_pool, ds.v_pool,
                           device_status=ds.status, stream=stream)
 
 
 def run_attention(ds: DeviceStep, stream=None) -> None:
-    if ds.kv == "q8":
-        B.pkv_attention_q8(ds.q, ds.cu_seqlens_q, ds.seq_slot, ds.context_lens, ds.block_tables, ds.k_pool,
-                           ds.k_scales, ds.v_pool, ds.v_scales, ds.work, ds.info, ds.out, ds.workspace,
-                           scale=ds.scale, device_status=ds.status, stream=stream)
+    if ds.kv in ("q8", "q4"):
+        attend = B.pkv_attention_q8 if ds.kv == "q8" else B.pkv_attention_q4
+        attend(ds.q, ds.cu_seqlens_q, ds.seq_slot, ds.context_lens, ds.block_tables, ds.k_pool, ds.k_scales,
+               ds.v_pool, ds.v_scales, ds.work, ds.info, ds.out, ds.workspace, scale=ds.scale,
+               device_status=ds.status, stream=stream)
     else:
         B.pkv_attention(ds.q, ds.cu_seqlens_q, ds.seq_slot, ds.context_lens, ds.block_tables, ds.k_pool,
                         ds.v_pool, ds.work, ds.info, ds.out, ds.workspace, scale=ds.scale,

@@ -460,6 +460,45 @@ pkv_status pkv_attention_q8(const void *q, const int32_t *cu_seqlens_q, int32_t 
                             uint64_t workspace_bytes, uint32_t *device_status, pkv_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * 4-bit block-scaled KV pool (head_dim 128). The same sources (Lucebox,
+ * §DeepSeek V4 Flash on Strix Halo and two GPUs: 4-bit KV) and the same rule
+ * as the 8-bit format with 7 in place of 127: per group of 32 values a
+ * power-of-two scale d, the smallest at or above amax / 7 (at least 2^-126,
+ * 0 when amax is 0), stored as a bfloat16, and codes round_half_even(x / d)
+ * clamped to [-7, 7], stored as 4-bit two's complement nibbles, two per byte,
+ * the even value in the low nibble. Every code * d is a bfloat16 number.
+ *
+ *   k_codes, v_codes   uint8 [num_blocks][num_kv_heads][block_size][head_dim / 2]
+ *   k_scales, v_scales bf16 [num_blocks][num_kv_heads][block_size][head_dim / 32]
+ * A row costs head_dim / 2 + head_dim / 16 bytes (72 at head_dim 128, against
+ * 256 for bf16).
+ * ---------------------------------------------------------------------- */
+
+/*
+ * pkv_cache_write_q8 for a 4-bit pool: same arguments, results (bit-exact
+ * with the format) and errors; PKV_ERR_UNSUPPORTED unless head_dim is 128.
+ */
+pkv_status pkv_cache_write_q4(const void *k_new, const void *v_new, const int64_t *slot_mapping,
+                              int64_t num_tokens, uint8_t *k_codes, void *k_scales, uint8_t *v_codes,
+                              void *v_scales, int64_t num_blocks, int32_t block_size, int32_t num_kv_heads,
+                              int32_t head_dim, uint32_t *device_status, pkv_stream_t stream);
+
+/*
+ * pkv_attention_q8 over a 4-bit pool: attention over code * scale, with the
+ * same arguments, workspace (info->workspace_bytes_q8), results and ordering
+ * rules; PKV_ERR_UNSUPPORTED unless head_dim is 128. Decode rows read the
+ * nibbles directly; prompt chunks read their histories widened to bf16.
+ */
+pkv_status pkv_attention_q4(const void *q, const int32_t *cu_seqlens_q, int32_t num_seqs, int64_t total_q,
+                            const int32_t *seq_slot, const int32_t *context_lens, const int32_t *block_tables,
+                            int32_t max_slots, int32_t max_blocks_per_slot, int32_t block_size,
+                            const uint8_t *k_codes, const void *k_scales, const uint8_t *v_codes,
+                            const void *v_scales, int64_t num_blocks, int32_t num_q_heads, int32_t num_kv_heads,
+                            int32_t head_dim, float scale, const int32_t *work, const pkv_work_info *info,
+                            void *out, void *workspace, uint64_t workspace_bytes, uint32_t *device_status,
+                            pkv_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Host-staged step: a whole step from host memory in one call.
  * [LB] §One scheduler, model-specific execution: the engine hands the lowered
  * step to its backend in one go. The pages give no host/device protocol; this

@@ -1,8 +1,10 @@
-"""GPU parity of the 8-bit block-scaled KV pool against ``oracle.kvquant``.
+"""GPU parity of the 8-bit and 4-bit block-scaled KV pools against ``oracle.kvquant``.
 
-* ``pkv_cache_write_q8`` must be bit-exact: codes and scales of every pool row,
-  including rows never written (which keep their fill);
-* ``pkv_attention_q8`` must match attention over the dequantised pool within
+* ``pkv_cache_write_q8`` / ``_q4`` must be bit-exact: codes (4-bit: two's
+  complement nibbles, the even value low, as ``oracle.kvquant.pack_nibbles``
+  stores them) and scales of every pool row, including rows never written
+  (which keep their fill);
+* ``pkv_attention_q8`` / ``_q4`` must match attention over the dequantised pool within
   the attention tolerance (max abs 2e-2, relative L2 1e-2), on decode rows,
   verify runs, prompt chunks (widened into the bf16 scratch pool) and mixed
   steps, over the same shapes as the bf16 path.
@@ -36,33 +38,34 @@ def cuda():
     return torch
 
 
-def _oracle_pool(w, blocks=None):
-    """The oracle's 8-bit pool after the step's cache write (history, then the step's rows)."""
+def _oracle_pool(w, bits=8):
+    """The oracle's block-scaled pool after the step's cache write (history, then the step's rows)."""
     st = oracle.prepare_step(w)
-    kq, ks = KQ.empty_pool(w.num_blocks, w.num_kv_heads, w.block_size, w.head_dim)
-    vq, vs = KQ.empty_pool(w.num_blocks, w.num_kv_heads, w.block_size, w.head_dim)
+    kq, ks = KQ.empty_pool(w.num_blocks, w.num_kv_heads, w.block_size, w.head_dim, bits)
+    vq, vs = KQ.empty_pool(w.num_blocks, w.num_kv_heads, w.block_size, w.head_dim, bits)
     segs = [(s.slot, s.q_len, s.ctx) for s in w.segments]
     hk = np.concatenate([w.hist_k[slot][:c - ql] for slot, ql, c in segs])
     hv = np.concatenate([w.hist_v[slot][:c - ql] for slot, ql, c in segs])
-    KQ.cache_write(kq, ks, vq, vs, hk, hv, st.history_mapping)
+    KQ.cache_write(kq, ks, vq, vs, hk, hv, st.history_mapping, bits)
     nk = np.concatenate([w.hist_k[slot][c - ql:c] for slot, ql, c in segs])
     nv = np.concatenate([w.hist_v[slot][c - ql:c] for slot, ql, c in segs])
-    KQ.cache_write(kq, ks, vq, vs, nk, nv, st.new_mapping)
+    KQ.cache_write(kq, ks, vq, vs, nk, nv, st.new_mapping, bits)
     return st, (kq, ks, vq, vs)
 
 
-def _run(w, rows=None, check_pool=True):
+def _run(w, rows=None, check_pool=True, bits=8):
     import torch
 
-    ds = R.prepare(w, kv="q8")
+    ds = R.prepare(w, kv=f"q{bits}")
     R.run_step(ds)
     torch.cuda.synchronize()
     assert B.pkv_check_device_status(ds.status) == 0
-    st, (kq, ks, vq, vs) = _oracle_pool(w)
+    st, (kq, ks, vq, vs) = _oracle_pool(w, bits)
     if check_pool:
         got = [ds.k_pool.cpu().numpy(), ds.k_scales.view(torch.int16).cpu().numpy().view(np.uint16),
                ds.v_pool.cpu().numpy(), ds.v_scales.view(torch.int16).cpu().numpy().view(np.uint16)]
-        for g, e, nm in zip(got, (kq, ks, vq, vs), ("k codes", "k scales", "v codes", "v scales")):
+        stored = (kq, ks, vq, vs) if bits == 8 else (KQ.pack_nibbles(kq), ks, KQ.pack_nibbles(vq), vs)
+        for g, e, nm in zip(got, stored, ("k codes", "k scales", "v codes", "v scales")):
             assert np.array_equal(g, e), f"{w.name}: {nm} differ from the oracle's"
     ref = KQ.attention_paged(w.q, st.packed.cu_seqlens_q, st.packed.seq_slot, st.context_lens, st.block_tables,
                              kq, ks, vq, vs, w.scale, num_q_heads=w.num_q_heads, rows=rows)
@@ -146,3 +149,42 @@ def test_many_rows_q8():
     w = W.random_step(41, [(1, c) for c in ctxs], num_q_heads=16, num_kv_heads=2, head_dim=128)
     rows = sorted({0, 1, 2, 100, 200, 358, 359})
     _run(w, rows=rows)
+
+
+
+# ---- 4-bit pool (head_dim 128) ----------------------------------------------------
+
+@pytest.mark.parametrize("case", sorted(SHAPES))
+@pytest.mark.parametrize("heads", [(32, 8), (40, 8), (64, 8), (16, 1)])
+def test_shapes_q4(case, heads):
+    hq, hkv = heads
+    w = W.random_step(zlib.crc32(f"q4/{case}/{hq}/{hkv}".encode()) % 1000, SHAPES[case], num_q_heads=hq,
+                      num_kv_heads=hkv, head_dim=128)
+    _run(w, bits=4)
+
+
+def test_peaked_softmax_q4():
+    w = W.random_step(6, [(1, 900), (64, 700)], num_q_heads=32, num_kv_heads=8, head_dim=128)
+    w.q = W.f32_to_bf16_bits(W.bf16_bits_to_f32(w.q) * 8.0)
+    _run(w, bits=4)
+
+
+def test_decode_five_clients_q4():
+    _run(W.make_step("decode5", 0, pool_blocks=4096), bits=4)
+
+
+def test_mixed_step_q4():
+    w = W.make_step("mixed", 0, pool_blocks=4096)
+    rows = sorted({0, 1, 255, 256, 511, *range(512, w.total_q)})
+    _run(w, rows=rows, bits=4)
+
+
+def test_many_rows_q4():
+    ctxs = [int(c) for c in np.random.default_rng(43).integers(1500, 2600, 360)]
+    w = W.random_step(43, [(1, c) for c in ctxs], num_q_heads=16, num_kv_heads=2, head_dim=128)
+    _run(w, rows=sorted({0, 1, 2, 100, 200, 358, 359}), bits=4)
+
+
+def test_q4_rejects_head_dim_64():
+    with pytest.raises(B.PkvError):
+        R.prepare(W.tiny(0), kv="q4")  # head_dim 64: the 4-bit pool is head_dim 128 only
