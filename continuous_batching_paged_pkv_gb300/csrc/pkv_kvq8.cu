@@ -1,6 +1,7 @@
-// 8-bit block-scaled KV pool: the quantising cache write, split-KV decode
-// attention straight from the 8-bit codes, and the widening of prompt-chunk
-// histories into a bf16 scratch pool for the tensor-core chunk kernel.
+// Block-scaled KV pools (8-bit codes; 4-bit codes at head_dim 128): the
+// quantising cache write, split-KV decode attention straight from the codes,
+// and the widening of prompt-chunk histories into a bf16 scratch pool for the
+// tensor-core chunk kernel. Every kernel is templated on the code width.
 //
 // Lucebox, "Continuous batching: Qwen3.8-27B at 301 tok/s across five
 // clients, up to 1.97x llama.cpp", §Qwen3.8-27B DFlash2 on the R9700 (vs
@@ -14,7 +15,10 @@
 // every code * d is a bfloat16 number, so widening codes to bf16 loses
 // nothing. Codes live in [num_blocks][Hkv][bs][D] int8, scales in
 // [num_blocks][Hkv][bs][D / 32] bf16: a row costs D + D / 16 bytes instead of
-// 2 D, so decode reads 53% of the bf16 pool's bytes.
+// 2 D, so decode reads 53% of the bf16 pool's bytes. The 4-bit format keeps
+// the groups and the scale rule with 7 in place of 127 and stores the codes as
+// two's complement nibbles, two per byte, the even value in the low nibble
+// ([num_blocks][Hkv][bs][D / 2] bytes): a row costs D / 2 + D / 16 bytes.
 //
 // Decode kernel (same task pipeline as the bf16 decode kernel: persistent
 // warps, a TMA ring per warp, work sorted longest first). Per 16-key sub-tile
@@ -32,7 +36,10 @@
 //   output address.
 // Codes become floats without conversion instructions: a byte b (offset by
 // 128) placed under the exponent of 1024.0 (fp16) or 2^23 (fp32) is that
-// power plus b, one subtraction away from the code.
+// power plus b, one subtraction away from the code. A nibble n (offset by 8)
+// goes under 1024.0 for K (fp16) and under 128.0 for V (bf16: 128 + n is
+// exact), so 4-bit codes take the same paths; their K words hold dims
+// 32 g + 8 j .. + 7 and q is loaded in that order.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
