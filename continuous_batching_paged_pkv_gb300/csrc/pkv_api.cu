@@ -361,6 +361,7 @@ static pkv_status attention_quant(int32_t bits, const void *q, const int32_t *cu
   // The chunk kernel reads a bf16 scratch pool: the chunk segments' histories,
   // widened block by block, with a scratch block table in the same shape.
   pkv::StepArgs c = a;
+  c.kv_from_previous = 1;  // the widening pass right before the chunk kernel fills its K/V
   void *scratch_k = nullptr, *scratch_v = nullptr;
   int32_t *scratch_table = nullptr;
   if (sb) {

@@ -35,6 +35,10 @@ struct StepArgs {
   // three static rounds (nullptr: every task is assigned statically). The
   // launch zeroes it on the stream first.
   uint32_t *task_counter;
+  // The chunk kernel's K/V pool is written by the kernel right before it (the
+  // 8-bit and 4-bit paths' widening pass): wait for it before any K/V load.
+  // Otherwise only the tiles holding this step's rows wait for the cache write.
+  int32_t kv_from_previous;
 };
 
 // Bytes of workspace after the span partials: the decode kernel's task counter.

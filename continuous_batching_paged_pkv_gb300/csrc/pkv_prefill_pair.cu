@@ -136,8 +136,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_pair_kernel(const __grid_
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = blockIdx.y;
   const uint32_t rank = cluster_ctarank();  // 0 issues the MMAs
+  // The work item, step metadata, q and the cached history are final when this
+  // grid starts (the kernel before it in the stream, the cache write, signals
+  // dependents only after its own wait); only the keys this step appends come
+  // from that kernel, and the producer waits for it before loading the first
+  // tile that holds them (before the first tile at all when the K/V source is
+  // a scratch pool the previous kernel fills).
   launch_dependents();
-  grid_dependency_wait();  // every input may come from the previous kernel in the stream
   const int4 it = reinterpret_cast<const int4 *>(items)[blockIdx.x >> 1];
   const int seg = it.x, slot = it.y, tile0 = it.z;
   const int G = a.group, P = rows_per_tile;
@@ -229,6 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_pair_kernel(const __grid_
     const int x = is_k ? (lane & 1) * 64 : static_cast<int>(rank) * 64;
     const int dst_off = is_k ? (lane & 1) * Lay::kKHalf + (lane >> 1) * kSubKeys * 128
                              : Lay::kKBytes + (lane - 8) * kSubKeys * 128;
+    bool waited = false;
     for (int j = 0; j < ntiles; ++j) {
       const int s = j % kStages;
       if (j >= kStages && !warp_wait_or_abort(bar + kKVEmpty + s, ((j - kStages) / kStages) & 1, abort_flag)) break;
@@ -242,6 +248,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_pair_kernel(const __grid_
       // The pair loads 4 boxes per visible sub-tile: two K halves (one CTA) and two V halves (one each).
       if (rank == 0 && lane == 0) mbar_arrive_expect_tx(bar + kKVFull + s, vs * 4 * 2048);
       const int urow = __shfl_sync(kFull, rows_cur, (j & 3) * 8 + (u & 7));
+      // wait for the kernel before: at the first tile holding rows the cache write appends, or at once
+      // when that kernel wrote the whole K/V source
+      if (!waited && (a.kv_from_previous || (j + 1) * kKeysPerTile > L - n)) {
+        grid_dependency_wait();
+        waited = true;
+      }
       if (lane < 16 && u < vs)
         tma_load_2d_pair(sKV + s * Lay::kStageBytes + dst_off, is_k ? &tmap_k : &tmap_v, x, urow, kv_full);
     }
