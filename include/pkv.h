@@ -338,10 +338,10 @@ pkv_status pkv_cache_write(const void *k_new, const void *v_new, const int64_t *
  * kernel. Calls that share a workspace must not overlap on the GPU. The pool must already hold this step's rows (pkv_cache_write
  * first, same stream). The kernels are launched with programmatic dependent
  * launch, so they may start while the previous kernel in the stream drains.
- * The decode kernel reads the step metadata, q and the cached history at
- * once and waits for that previous kernel only before reading the key spans
- * that hold this step's new rows; the chunk kernel waits before reading
- * anything. So the previous kernel must not signal dependents before the
+ * The decode and chunk kernels read the step metadata, q and the cached
+ * history at once and wait for that previous kernel only before reading the
+ * 16-key sub-tiles (decode) or 128-key tiles (chunk) that hold this step's
+ * new rows. So the previous kernel must not signal dependents before the
  * data it leaves for this call is complete: pkv_cache_write signals only
  * after every kernel before it has finished, and a kernel that does not use
  * programmatic dependent launch signals at its end. When a step has both prompt
