@@ -467,7 +467,8 @@ def run_ours(args, rank, world, local_rank):
                                  "kernels": "chunk + decode + span merge"}
     else:
         src = "pkv_kvq8.cu" if args.kv in ("q8", "q4") else "pkv_decode.cu"
-        traffic = profiled_traffic(src, args.workload) if dec_kernel in kernel else None
+        wl = args.workload if args.kv == "bf16" else f"{args.workload}_{args.kv}"
+        traffic = profiled_traffic(src, wl) if dec_kernel in kernel else None
         res["roofline"] = {"bound": "hbm", "kernel": kernel, "achieved": achieved, "peak": hbm, "unit": "GB/s",
                            "frac": achieved / hbm, "traffic": traffic,
                            "algorithmic_bytes_per_launch": kvb, "mean_launch_ms": attn_mean,
