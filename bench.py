@@ -445,12 +445,12 @@ def run_ours(args, rank, world, local_rank):
                               "step": statistics.median(step_ms)},
     }
     chunk_kernel = "prefill_pair_kernel" if w.head_dim == 128 else "prefill_kernel"
-    dec_kernel = "decode_q8_kernel" if args.kv in ("q8", "q4") else "decode_kernel"
+    dec_kernel = "decode_quant_kernel" if args.kv in ("q8", "q4") else "decode_kernel"
     if ds.info.num_prefill_items and args.kv == "bf16":
         # the chunk kernel dominates the library's time on steps that carry a prompt chunk
         bound, unit, kernel = "tensor", "TFLOP/s", chunk_kernel
     elif ds.info.num_prefill_items:
-        bound, unit, kernel = "hbm", "GB/s", "attention call: widen_q8 + chunk + decode_q8 + span merge kernels"
+        bound, unit, kernel = "hbm", "GB/s", "attention call: widen_quant + chunk + decode_quant + span merge kernels"
     elif ds.info.num_combine_items:
         bound, unit, kernel = "hbm", "GB/s", f"attention call: {dec_kernel} + span merge (merge_small/merge_wide)"
     else:
@@ -466,7 +466,7 @@ def run_ours(args, rank, world, local_rank):
         res["attention_call"] = {"kv_gbs": achieved, "pct_hbm_peak": 100.0 * achieved / hbm, "mean_ms": attn_mean,
                                  "kernels": "chunk + decode + span merge"}
     else:
-        src = "pkv_kvq8.cu" if args.kv in ("q8", "q4") else "pkv_decode.cu"
+        src = "pkv_kvquant.cu" if args.kv in ("q8", "q4") else "pkv_decode.cu"
         wl = args.workload if args.kv == "bf16" else f"{args.workload}_{args.kv}"
         traffic = profiled_traffic(src, wl) if dec_kernel in kernel else None
         res["roofline"] = {"bound": "hbm", "kernel": kernel, "achieved": achieved, "peak": hbm, "unit": "GB/s",

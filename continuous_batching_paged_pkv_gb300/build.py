@@ -20,7 +20,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_PATH = os.path.join(PKG, "libpkv.so")
 
-SOURCES = ["pkv_host.cpp", "pkv_step.cpp", "pkv_api.cu", "pkv_cache_write.cu", "pkv_decode.cu", "pkv_kvq8.cu", "pkv_prefill.cu", "pkv_prefill_pair.cu",
+SOURCES = ["pkv_host.cpp", "pkv_step.cpp", "pkv_api.cu", "pkv_cache_write.cu", "pkv_decode.cu", "pkv_kvquant.cu", "pkv_prefill.cu", "pkv_prefill_pair.cu",
            "pkv_static.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]

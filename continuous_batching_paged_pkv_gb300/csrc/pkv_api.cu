@@ -262,7 +262,7 @@ static pkv_status cache_write_quant(int32_t bits, const void *k_new, const void 
   if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_codes, 16) || !aligned(v_codes, 16) ||
       !aligned(k_scales, 16) || !aligned(v_scales, 16) || !aligned(slot_mapping, 8))
     return PKV_ERR_INVALID_ARG;
-  cudaError_t e = pkv::launch_cache_write_q8(k_new, v_new, slot_mapping, num_tokens, k_codes, k_scales, v_codes,
+  cudaError_t e = pkv::launch_cache_write_quant(k_new, v_new, slot_mapping, num_tokens, k_codes, k_scales, v_codes,
                                              v_scales, num_blocks, block_size, num_kv_heads, head_dim, bits,
                                              device_status, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
@@ -396,7 +396,7 @@ static pkv_status attention_quant(int32_t bits, const void *q, const int32_t *cu
   if (side) lock = std::unique_lock<std::mutex>(side->mu);
   cudaError_t e = side ? cudaEventRecord(side->fork, st) : cudaSuccess;
   if (e == cudaSuccess && info->num_prefill_items > 0) {
-    e = pkv::launch_widen_q8(a, k_codes, k_scales, v_codes, v_scales, scratch_k, scratch_v, scratch_table,
+    e = pkv::launch_widen_quant(a, k_codes, k_scales, v_codes, v_scales, scratch_k, scratch_v, scratch_table,
                              static_cast<int64_t>(sb), info->num_scratch_items, scr, bits, st);
     if (e == cudaSuccess)
       e = head_dim == 128 ? pkv::launch_prefill_pair(c, tq, tk, tv, rpt, info->num_prefill_items, pre, st)
@@ -405,7 +405,7 @@ static pkv_status attention_quant(int32_t bits, const void *q, const int32_t *cu
   cudaStream_t dst = side ? side->stream : st;
   if (e == cudaSuccess && side) e = cudaStreamWaitEvent(side->stream, side->fork, 0);
   if (e == cudaSuccess)
-    e = pkv::launch_decode_q8(a, tkc, tvc, k_scales, v_scales, info->num_decode_items, dec, bits, dst);
+    e = pkv::launch_decode_quant(a, tkc, tvc, k_scales, v_scales, info->num_decode_items, dec, bits, dst);
   if (e == cudaSuccess) e = pkv::launch_merge(a, info->num_combine_items, comb, dst);
   if (side) {
     const cudaError_t j = cudaEventRecord(side->join, side->stream);

@@ -62,14 +62,14 @@ cudaError_t launch_merge(const StepArgs &a, int32_t num_items, const int32_t *it
 // Block-scaled pools (bits = 8, or 4 at head_dim 128): quantising cache write,
 // decode over the codes, and the widening of prompt-chunk histories into a
 // bf16 scratch pool.
-cudaError_t launch_cache_write_q8(const void *k_new, const void *v_new, const int64_t *slot_mapping,
+cudaError_t launch_cache_write_quant(const void *k_new, const void *v_new, const int64_t *slot_mapping,
                                   int64_t num_tokens, void *k_codes, void *k_scales, void *v_codes, void *v_scales,
                                   int64_t num_blocks, int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
                                   int32_t bits, uint32_t *status, cudaStream_t stream);
-cudaError_t launch_decode_q8(const StepArgs &a, const CUtensorMap &tmap_k_codes, const CUtensorMap &tmap_v_codes,
+cudaError_t launch_decode_quant(const StepArgs &a, const CUtensorMap &tmap_k_codes, const CUtensorMap &tmap_v_codes,
                              const void *k_scales, const void *v_scales, int32_t num_items, const int32_t *items,
                              int32_t bits, cudaStream_t stream);
-cudaError_t launch_widen_q8(const StepArgs &a, const void *k_codes, const void *k_scales, const void *v_codes,
+cudaError_t launch_widen_quant(const StepArgs &a, const void *k_codes, const void *k_scales, const void *v_codes,
                             const void *v_scales, void *k_out, void *v_out, int32_t *scratch_table,
                             int64_t scratch_blocks, int32_t num_items, const int32_t *items, int32_t bits,
                             cudaStream_t stream);

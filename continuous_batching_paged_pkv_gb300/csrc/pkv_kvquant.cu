@@ -52,9 +52,9 @@
 namespace pkv {
 namespace {
 
-constexpr int kWarpsQ8 = 8;
+constexpr int kWarpsQuant = 8;
 constexpr uint32_t kAll = 0xffffffffu;
-constexpr float kRescaleQ8 = 8.0f;  // log2 units, as in the bf16 decode kernel
+constexpr float kRescaleQuant = 8.0f;  // log2 units, as in the bf16 decode kernel
 
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
 
@@ -64,7 +64,7 @@ __device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) { return __
 // values, so one scale group spans 1024/D lanes. BITS = 8: one code per byte;
 // BITS = 4: codes in [-7, 7], two per byte, the even value in the low nibble.
 template <int D, int BITS>
-__global__ void __launch_bounds__(256) cache_write_q8_kernel(
+__global__ void __launch_bounds__(256) cache_write_quant_kernel(
     const __nv_bfloat16 *__restrict__ k_new, const __nv_bfloat16 *__restrict__ v_new,
     const int64_t *__restrict__ slot_mapping, int64_t num_tokens, int8_t *__restrict__ k_codes,
     __nv_bfloat16 *__restrict__ k_scales, int8_t *__restrict__ v_codes, __nv_bfloat16 *__restrict__ v_scales,
@@ -140,7 +140,7 @@ __global__ void __launch_bounds__(256) cache_write_q8_kernel(
 // item's logical blocks y, y + gridDim.y, ... : block j of the slot becomes
 // scratch block first + j, and the scratch table row of the slot points there.
 template <int D, int BITS>
-__global__ void __launch_bounds__(256) widen_q8_kernel(const StepArgs a, const int32_t *__restrict__ items,
+__global__ void __launch_bounds__(256) widen_quant_kernel(const StepArgs a, const int32_t *__restrict__ items,
                                                        const int8_t *__restrict__ k_codes,
                                                        const __nv_bfloat16 *__restrict__ k_scales,
                                                        const int8_t *__restrict__ v_codes,
@@ -212,7 +212,7 @@ __global__ void __launch_bounds__(256) widen_q8_kernel(const StepArgs a, const i
 
 // NW warps per CTA (the ring depth follows from the shared memory they share).
 template <int D, int NW, int BITS>
-struct Q8Cfg {
+struct QuantCfg {
   static constexpr int kGroups = D / 32;
   static constexpr int kCodeBytes = kSubKeys * D * BITS / 8;   // K (or V) codes of one sub-tile
   static constexpr int kScaleBytes = kSubKeys * kGroups * 2;   // their scales
@@ -295,7 +295,7 @@ __device__ __forceinline__ uint32_t nibble_pair_to_bf16(uint32_t x, int n) {
 // holds dims 32 g + 8 j .. + 7), scaled by 2^sh (per column) so that
 // max |q'| < 2^15; `inv` receives 2^-sh.
 template <int D, int NT, bool MULTI, int BITS>
-__device__ __forceinline__ void load_q_q8(uint32_t (&qf)[NT][D / 16][2], float (&inv)[NT], const Task &T,
+__device__ __forceinline__ void load_q_quant(uint32_t (&qf)[NT][D / 16][2], float (&inv)[NT], const Task &T,
                                           const StepArgs &a, int lane) {
   constexpr int KT = D / 16;
 #pragma unroll
@@ -338,10 +338,10 @@ __device__ __forceinline__ void load_q_q8(uint32_t (&qf)[NT][D / 16][2], float (
 
 template <int D, int NT, bool MULTI, int NW, int BITS>
 __global__ void __launch_bounds__(NW * 32, 1)
-    decode_q8_kernel(const __grid_constant__ CUtensorMap tmap_kc, const __grid_constant__ CUtensorMap tmap_vc,
+    decode_quant_kernel(const __grid_constant__ CUtensorMap tmap_kc, const __grid_constant__ CUtensorMap tmap_vc,
                      const StepArgs a, const __nv_bfloat16 *__restrict__ k_scales,
                      const __nv_bfloat16 *__restrict__ v_scales, const int32_t *__restrict__ items, int num_items) {
-  using Cfg = Q8Cfg<D, NW, BITS>;
+  using Cfg = QuantCfg<D, NW, BITS>;
   static_assert(BITS == 8 || D == 128, "4-bit codes need head_dim 128 (64-byte code rows)");
   constexpr int RB = Cfg::kRowBytes;  // code row layout: 128-byte rows (128B swizzle) or 64-byte (64B)
   constexpr int KT = D / 16;  // k-steps of QK^T, m-tiles of PV
@@ -386,7 +386,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
   finalize(A, a, lane, 8 * NT, kMaxRows);
   uint32_t qA[NT][KT][2], qB[NT][KT][2];
   float invA[NT], invB[NT];
-  if (A.ok) load_q_q8<D, NT, MULTI, BITS>(qA, invA, A, a, lane);
+  if (A.ok) load_q_quant<D, NT, MULTI, BITS>(qA, invA, A, a, lane);
   bool qB_loaded = false;
 
   int P = 0, C = 0, pa = 0, pb = 0;
@@ -424,7 +424,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
       if (!B.finalized) {
         finalize(B, a, lane, 8 * NT, kMaxRows);
         if (B.ok) {
-          load_q_q8<D, NT, MULTI, BITS>(qB, invB, B, a, lane);
+          load_q_quant<D, NT, MULTI, BITS>(qB, invB, B, a, lane);
           qB_loaded = true;
         }
       }
@@ -583,14 +583,14 @@ __global__ void __launch_bounds__(NW * 32, 1)
           t = fmaxf(t, __shfl_xor_sync(kAll, t, 8));
           t = fmaxf(t, __shfl_xor_sync(kAll, t, 16));
           mx[nt][c] = t;
-          need |= t > m[nt][c] + kRescaleQ8;
+          need |= t > m[nt][c] + kRescaleQuant;
         }
       if (__any_sync(kAll, need)) {
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
           for (int c = 0; c < 2; ++c)
-            if (mx[nt][c] > m[nt][c] + kRescaleQ8) {
+            if (mx[nt][c] > m[nt][c] + kRescaleQuant) {
               const float corr = exp2f(m[nt][c] - mx[nt][c]);
               m[nt][c] = mx[nt][c];
               l[nt][c] *= corr;
@@ -742,7 +742,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
           }
         }
       } else if (A.ok) {
-        load_q_q8<D, NT, MULTI, BITS>(qA, invA, A, a, lane);
+        load_q_quant<D, NT, MULTI, BITS>(qA, invA, A, a, lane);
       }
     }
     qB_loaded = false;
@@ -755,16 +755,16 @@ __global__ void __launch_bounds__(NW * 32, 1)
 }
 
 template <int D, int NT, bool MULTI, int NW, int BITS>
-cudaError_t launch_decode_q8_w(const StepArgs &a, const CUtensorMap &tk, const CUtensorMap &tv,
+cudaError_t launch_decode_quant_w(const StepArgs &a, const CUtensorMap &tk, const CUtensorMap &tv,
                                const void *k_scales, const void *v_scales, int32_t num_items, const int32_t *items,
                                int grid, cudaStream_t stream) {
-  constexpr int smem = Q8Cfg<D, NW, BITS>::kSmem;
+  constexpr int smem = QuantCfg<D, NW, BITS>::kSmem;
   static uint64_t configured = 0;  // one bit per device
   int dev = 0;
   cudaGetDevice(&dev);
   const uint64_t bit = 1ull << (dev & 63);
   if (!(configured & bit)) {
-    cudaError_t e = cudaFuncSetAttribute(decode_q8_kernel<D, NT, MULTI, NW, BITS>,
+    cudaError_t e = cudaFuncSetAttribute(decode_quant_kernel<D, NT, MULTI, NW, BITS>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     configured |= bit;
@@ -777,7 +777,7 @@ cudaError_t launch_decode_q8_w(const StepArgs &a, const CUtensorMap &tk, const C
   } else {
     b.task_counter = nullptr;
   }
-  return launch_pdl(decode_q8_kernel<D, NT, MULTI, NW, BITS>, dim3(grid), dim3(NW * 32), smem, stream, tk, tv, b,
+  return launch_pdl(decode_quant_kernel<D, NT, MULTI, NW, BITS>, dim3(grid), dim3(NW * 32), smem, stream, tk, tv, b,
                     static_cast<const __nv_bfloat16 *>(k_scales), static_cast<const __nv_bfloat16 *>(v_scales),
                     items, num_items);
 }
@@ -788,7 +788,7 @@ cudaError_t launch_decode_q8_w(const StepArgs &a, const CUtensorMap &tk, const C
 // long dependent chain, and more warps per scheduler hide it once every warp
 // has work (a small step's few busy warps stream faster through deeper rings).
 template <int D, int NT, bool MULTI, int BITS>
-cudaError_t launch_decode_q8_t(const StepArgs &a, const CUtensorMap &tk, const CUtensorMap &tv,
+cudaError_t launch_decode_quant_t(const StepArgs &a, const CUtensorMap &tk, const CUtensorMap &tv,
                                const void *k_scales, const void *v_scales, int32_t num_items, const int32_t *items,
                                cudaStream_t stream) {
   int dev = 0, sms = 0;
@@ -798,16 +798,16 @@ cudaError_t launch_decode_q8_t(const StepArgs &a, const CUtensorMap &tk, const C
   const int grid = static_cast<int>(tasks < sms ? tasks : sms);
   if constexpr (D == 128 && NT == 1 && !MULTI) {
     if (tasks > 3ll * grid * 12)
-      return launch_decode_q8_w<D, NT, MULTI, 12, BITS>(a, tk, tv, k_scales, v_scales, num_items, items, grid,
+      return launch_decode_quant_w<D, NT, MULTI, 12, BITS>(a, tk, tv, k_scales, v_scales, num_items, items, grid,
                                                          stream);
   }
-  return launch_decode_q8_w<D, NT, MULTI, kWarpsQ8, BITS>(a, tk, tv, k_scales, v_scales, num_items, items, grid,
+  return launch_decode_quant_w<D, NT, MULTI, kWarpsQuant, BITS>(a, tk, tv, k_scales, v_scales, num_items, items, grid,
                                                            stream);
 }
 
 }  // namespace
 
-cudaError_t launch_cache_write_q8(const void *k_new, const void *v_new, const int64_t *slot_mapping,
+cudaError_t launch_cache_write_quant(const void *k_new, const void *v_new, const int64_t *slot_mapping,
                                   int64_t num_tokens, void *k_codes, void *k_scales, void *v_codes, void *v_scales,
                                   int64_t num_blocks, int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
                                   int32_t bits, uint32_t *status, cudaStream_t stream) {
@@ -823,16 +823,16 @@ cudaError_t launch_cache_write_q8(const void *k_new, const void *v_new, const in
   auto *vsc = static_cast<__nv_bfloat16 *>(v_scales);
   const int64_t prows = num_blocks * block_size;
   if (bits == 4)
-    return launch_pdl(cache_write_q8_kernel<128, 4>, grid, dim3(256), 0, stream, kn, vn, slot_mapping, num_tokens,
+    return launch_pdl(cache_write_quant_kernel<128, 4>, grid, dim3(256), 0, stream, kn, vn, slot_mapping, num_tokens,
                       kc, ksc, vc, vsc, prows, block_size, num_kv_heads, status);
   if (head_dim == 128)
-    return launch_pdl(cache_write_q8_kernel<128, 8>, grid, dim3(256), 0, stream, kn, vn, slot_mapping, num_tokens,
+    return launch_pdl(cache_write_quant_kernel<128, 8>, grid, dim3(256), 0, stream, kn, vn, slot_mapping, num_tokens,
                       kc, ksc, vc, vsc, prows, block_size, num_kv_heads, status);
-  return launch_pdl(cache_write_q8_kernel<64, 8>, grid, dim3(256), 0, stream, kn, vn, slot_mapping, num_tokens, kc,
+  return launch_pdl(cache_write_quant_kernel<64, 8>, grid, dim3(256), 0, stream, kn, vn, slot_mapping, num_tokens, kc,
                     ksc, vc, vsc, prows, block_size, num_kv_heads, status);
 }
 
-cudaError_t launch_widen_q8(const StepArgs &a, const void *k_codes, const void *k_scales, const void *v_codes,
+cudaError_t launch_widen_quant(const StepArgs &a, const void *k_codes, const void *k_scales, const void *v_codes,
                             const void *v_scales, void *k_out, void *v_out, int32_t *scratch_table,
                             int64_t scratch_blocks, int32_t num_items, const int32_t *items, int32_t bits,
                             cudaStream_t stream) {
@@ -848,16 +848,16 @@ cudaError_t launch_widen_q8(const StepArgs &a, const void *k_codes, const void *
   auto *ko = static_cast<__nv_bfloat16 *>(k_out);
   auto *vo = static_cast<__nv_bfloat16 *>(v_out);
   if (bits == 4)
-    return launch_pdl(widen_q8_kernel<128, 4>, grid, dim3(256), 0, stream, a, items, kc, ksc, vc, vsc, ko, vo,
+    return launch_pdl(widen_quant_kernel<128, 4>, grid, dim3(256), 0, stream, a, items, kc, ksc, vc, vsc, ko, vo,
                       scratch_table, scratch_blocks);
   if (a.head_dim == 128)
-    return launch_pdl(widen_q8_kernel<128, 8>, grid, dim3(256), 0, stream, a, items, kc, ksc, vc, vsc, ko, vo,
+    return launch_pdl(widen_quant_kernel<128, 8>, grid, dim3(256), 0, stream, a, items, kc, ksc, vc, vsc, ko, vo,
                       scratch_table, scratch_blocks);
-  return launch_pdl(widen_q8_kernel<64, 8>, grid, dim3(256), 0, stream, a, items, kc, ksc, vc, vsc, ko, vo,
+  return launch_pdl(widen_quant_kernel<64, 8>, grid, dim3(256), 0, stream, a, items, kc, ksc, vc, vsc, ko, vo,
                     scratch_table, scratch_blocks);
 }
 
-cudaError_t launch_decode_q8(const StepArgs &a, const CUtensorMap &tk, const CUtensorMap &tv, const void *k_scales,
+cudaError_t launch_decode_quant(const StepArgs &a, const CUtensorMap &tk, const CUtensorMap &tv, const void *k_scales,
                              const void *v_scales, int32_t num_items, const int32_t *items, int32_t bits,
                              cudaStream_t stream) {
   if (num_items <= 0) return cudaSuccess;
@@ -866,21 +866,21 @@ cudaError_t launch_decode_q8(const StepArgs &a, const CUtensorMap &tk, const CUt
   const int v = (wide ? 2 : 0) + (multi ? 1 : 0);
   if (bits == 4) {  // head_dim 128 only
     switch (v) {
-      case 0: return launch_decode_q8_t<128, 1, false, 4>(a, tk, tv, k_scales, v_scales, num_items, items, stream);
-      case 1: return launch_decode_q8_t<128, 1, true, 4>(a, tk, tv, k_scales, v_scales, num_items, items, stream);
-      case 2: return launch_decode_q8_t<128, 2, false, 4>(a, tk, tv, k_scales, v_scales, num_items, items, stream);
-      default: return launch_decode_q8_t<128, 2, true, 4>(a, tk, tv, k_scales, v_scales, num_items, items, stream);
+      case 0: return launch_decode_quant_t<128, 1, false, 4>(a, tk, tv, k_scales, v_scales, num_items, items, stream);
+      case 1: return launch_decode_quant_t<128, 1, true, 4>(a, tk, tv, k_scales, v_scales, num_items, items, stream);
+      case 2: return launch_decode_quant_t<128, 2, false, 4>(a, tk, tv, k_scales, v_scales, num_items, items, stream);
+      default: return launch_decode_quant_t<128, 2, true, 4>(a, tk, tv, k_scales, v_scales, num_items, items, stream);
     }
   }
   switch (v + (a.head_dim == 128 ? 4 : 0)) {
-    case 0: return launch_decode_q8_t<64, 1, false, 8>(a, tk, tv, k_scales, v_scales, num_items, items, stream);
-    case 1: return launch_decode_q8_t<64, 1, true, 8>(a, tk, tv, k_scales, v_scales, num_items, items, stream);
-    case 2: return launch_decode_q8_t<64, 2, false, 8>(a, tk, tv, k_scales, v_scales, num_items, items, stream);
-    case 3: return launch_decode_q8_t<64, 2, true, 8>(a, tk, tv, k_scales, v_scales, num_items, items, stream);
-    case 4: return launch_decode_q8_t<128, 1, false, 8>(a, tk, tv, k_scales, v_scales, num_items, items, stream);
-    case 5: return launch_decode_q8_t<128, 1, true, 8>(a, tk, tv, k_scales, v_scales, num_items, items, stream);
-    case 6: return launch_decode_q8_t<128, 2, false, 8>(a, tk, tv, k_scales, v_scales, num_items, items, stream);
-    default: return launch_decode_q8_t<128, 2, true, 8>(a, tk, tv, k_scales, v_scales, num_items, items, stream);
+    case 0: return launch_decode_quant_t<64, 1, false, 8>(a, tk, tv, k_scales, v_scales, num_items, items, stream);
+    case 1: return launch_decode_quant_t<64, 1, true, 8>(a, tk, tv, k_scales, v_scales, num_items, items, stream);
+    case 2: return launch_decode_quant_t<64, 2, false, 8>(a, tk, tv, k_scales, v_scales, num_items, items, stream);
+    case 3: return launch_decode_quant_t<64, 2, true, 8>(a, tk, tv, k_scales, v_scales, num_items, items, stream);
+    case 4: return launch_decode_quant_t<128, 1, false, 8>(a, tk, tv, k_scales, v_scales, num_items, items, stream);
+    case 5: return launch_decode_quant_t<128, 1, true, 8>(a, tk, tv, k_scales, v_scales, num_items, items, stream);
+    case 6: return launch_decode_quant_t<128, 2, false, 8>(a, tk, tv, k_scales, v_scales, num_items, items, stream);
+    default: return launch_decode_quant_t<128, 2, true, 8>(a, tk, tv, k_scales, v_scales, num_items, items, stream);
   }
 }
 
