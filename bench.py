@@ -233,11 +233,11 @@ def barrier(world):
 # CPU baseline: the oracle as it stands, on the host's cores.
 # ---------------------------------------------------------------------------
 
-def cpu_baseline(w, seconds: float, rows_per_run=None):
+def cpu_baseline(w, seconds: float, rows_per_run=None, threads=None):
     import oracle
 
     oracle.build()
-    cores = oracle.default_threads()
+    cores = threads or oracle.default_threads()
     st = oracle.prepare_step(w)
     seg_rows = []
     start = 0
@@ -490,6 +490,8 @@ def run_ours(args, rank, world, local_rank):
                                "the output) and the stream synchronised"}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+        one = cpu_baseline(w, args.cpu_seconds / 2, threads=1)  # the same oracle on one core
+        res["cpu_baseline"]["one_core"] = {"value": one["value"], "unit": one["unit"], "sample": one["sample"]}
     res["impl"] = "ours"
     return res
 
