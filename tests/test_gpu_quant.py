@@ -188,3 +188,11 @@ def test_many_rows_q4():
 def test_q4_rejects_head_dim_64():
     with pytest.raises(B.PkvError):
         R.prepare(W.tiny(0), kv="q4")  # head_dim 64: the 4-bit pool is head_dim 128 only
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+@pytest.mark.parametrize("bs", [32, 64])
+def test_other_block_sizes_quant(bits, bs):
+    w = W.random_step(bs + bits, [(1, 700), (40, 333), (1, 64), (9, 9), (3, 260)], num_q_heads=32, num_kv_heads=8,
+                      head_dim=128, block_size=bs)
+    _run(w, bits=bits)
