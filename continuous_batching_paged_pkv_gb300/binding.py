@@ -465,3 +465,37 @@ def pkv_step(layout: StageLayout, host_stage, device_stage, k_pool, v_pool, out,
         err.info = info
         raise err
     return info
+
+
+class StepCall:
+    """``pkv_step`` with its arguments bound once, for a serving loop that reuses the same buffers.
+
+    The constructor takes ``pkv_step``'s arguments and checks them; each call then only
+    invokes the library with the marshalled arguments (the staging buffer's contents, which
+    the caller refills between steps, are read by the library at the call). The buffers must
+    stay alive and in place while the object is used; this object holds references to them.
+    """
+
+    def __init__(self, layout: StageLayout, host_stage, device_stage, k_pool, v_pool, out, workspace=None, *,
+                 out_host=None, scale: float = 0.0, device_status=None, stream=None):
+        _need(out, "torch.bfloat16", "out")
+        _need(k_pool, "torch.bfloat16", "k_pool")
+        _need(v_pool, "torch.bfloat16", "v_pool")
+        nb, hkv, bs, d = k_pool.shape
+        hp, hn = _buf(host_stage)
+        dp, dn = _buf(device_stage)
+        wp, wn = _buf(workspace)
+        self.info = WorkInfo()
+        self._keep = (layout, host_stage, device_stage, k_pool, v_pool, out, workspace, out_host, device_status)
+        self._fn = _lib().pkv_step
+        self._args = (ctypes.byref(layout), hp, hn, dp, dn, _t_ptr(k_pool), _t_ptr(v_pool), nb, bs, float(scale),
+                      wp, wn, _t_ptr(out), _buf(out_host)[0], _t_ptr(device_status), _stream(stream),
+                      ctypes.byref(self.info))
+
+    def __call__(self) -> WorkInfo:
+        rc = self._fn(*self._args)
+        if rc != PKV_OK:
+            err = PkvError(rc, "pkv_step")
+            err.info = self.info
+            raise err
+        return self.info

@@ -71,6 +71,16 @@ def test_host_staged_step_matches_device_calls_and_oracle(name):
         k2, v2 = R.pool_bits(ds)
         assert np.array_equal(k2, pool_k) and np.array_equal(v2, pool_v)
 
+    # the same call with its arguments bound once, twice in a row, gives the same bits
+    call = B.StepCall(lay, stage.host, stage.device, ds.k_pool, ds.v_pool, out, ds.workspace, out_host=out_host,
+                      scale=w.scale, device_status=ds.status)
+    for _ in range(2):
+        out_host.view(torch.int16).fill_(R.SENTINEL_BITS)
+        call()
+        torch.cuda.synchronize()
+        assert np.array_equal(out_host.view(torch.int16).numpy(), want_bits), "bound step call differs"
+    assert B.pkv_check_device_status(ds.status) == 0
+
     st = oracle.prepare_step(w)
     ref = oracle.step_attention(w, st)
     got = out_host.float().numpy()
