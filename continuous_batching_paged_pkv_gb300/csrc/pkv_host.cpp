@@ -359,13 +359,25 @@ pkv_status pkv_plan_work(const int32_t *cu, int32_t num_seqs, const int32_t *seq
     int32_t w[4];
     int64_t cost;
   };
-  std::vector<Item> dec, pre, comb, scr;
+  std::vector<Item> dec, dec_short, pre, comb, scr;  // dec: full key spans; dec_short: shorter last spans
   int64_t scratch_blocks = 0;
   std::vector<uint8_t> used(static_cast<size_t>(max_slots), 0);
   const int32_t rows_per_tile = 128 / group;
   // Segments of up to 16 / group rows (decode rows and short verify runs) take
   // the split-KV decode path: rows x grouped heads fit its 16 MMA columns.
   const int32_t decode_rows = std::max<int32_t>(1, 16 / group);
+  {  // room for every decode span and merge row up front (checked again below)
+    int64_t spans = 0, rows = 0;
+    for (int32_t s = 0; s < num_seqs; ++s) {
+      const int32_t n = cu[s + 1] - cu[s], slot = seq_slot[s];
+      if (n <= 0 || n > decode_rows || slot < 0 || slot >= max_slots) continue;
+      const int64_t sp = ceil_div(std::max<int32_t>(context_lens[slot], 0), PKV_SPLIT_KEYS);
+      spans += sp;
+      rows += sp > 1 ? n : 0;
+    }
+    dec.reserve(static_cast<size_t>(std::min<int64_t>(spans, int64_t(1) << 24)));
+    comb.reserve(static_cast<size_t>(std::min<int64_t>(rows, int64_t(1) << 24)));
+  }
   int32_t partials = 0, rows_max = 0;
   for (int32_t s = 0; s < num_seqs; ++s) {
     const int32_t n = cu[s + 1] - cu[s];
@@ -387,7 +399,7 @@ pkv_status pkv_plan_work(const int32_t *cu, int32_t num_seqs, const int32_t *seq
       const int32_t base = spans > 1 ? partials : -1;
       for (int32_t sp = 0; sp < spans; ++sp) {
         const int64_t keys = std::min<int64_t>(PKV_SPLIT_KEYS, L - static_cast<int64_t>(sp) * PKV_SPLIT_KEYS);
-        dec.push_back({{s, slot, sp, base}, keys});
+        (keys == PKV_SPLIT_KEYS ? dec : dec_short).push_back({{s, slot, sp, base}, keys});
       }
       if (spans > 1) {
         for (int32_t i = 0; i < n; ++i)
@@ -415,7 +427,10 @@ pkv_status pkv_plan_work(const int32_t *cu, int32_t num_seqs, const int32_t *seq
   // Longest first, ties in their original order: the long items start early
   // and the short tails fill in behind them.
   auto by_cost = [](const Item &a, const Item &b) { return a.cost > b.cost; };
-  std::stable_sort(dec.begin(), dec.end(), by_cost);
+  // Full spans all cost the same and are already in order; only the short last spans
+  // (one per segment at most) need sorting behind them.
+  std::stable_sort(dec_short.begin(), dec_short.end(), by_cost);
+  dec.insert(dec.end(), dec_short.begin(), dec_short.end());
   std::stable_sort(pre.begin(), pre.end(), by_cost);
   std::stable_sort(comb.begin(), comb.end(), by_cost);  // long merges start first
 
