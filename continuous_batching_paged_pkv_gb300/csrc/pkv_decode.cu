@@ -162,6 +162,9 @@ __global__ void __launch_bounds__(NW * 32, 1)
 
   int P = 0, C = 0, pa = 0, pb = 0;
   int pstage = 0;  // P % NST
+  // Each history row is read once per step: its L2 lines go first, which keeps
+  // the span partials this grid writes in L2 for the merge.
+  const uint64_t policy = l2_evict_first_policy();
   auto issue = [&](const Task &T, int u) {
     // only the sub-tiles holding this step's rows wait for the cache write
     if (!waited && T.reads_new && T.key0 + (u + 1) * kSubKeys > T.L - T.nrows) {
@@ -176,8 +179,8 @@ __global__ void __launch_bounds__(NW * 32, 1)
         mbar_arrive_expect_tx(bar, Cfg::kStageBytes);
 #pragma unroll
         for (int h = 0; h < Cfg::kHalves; ++h) {
-          tma_load_2d(dst + h * Cfg::kHalfBytes, &tmap_k, h * 64, row, bar);
-          tma_load_2d(dst + Cfg::kTileBytes + h * Cfg::kHalfBytes, &tmap_v, h * 64, row, bar);
+          tma_load_2d_hint(dst + h * Cfg::kHalfBytes, &tmap_k, h * 64, row, bar, policy);
+          tma_load_2d_hint(dst + Cfg::kTileBytes + h * Cfg::kHalfBytes, &tmap_v, h * 64, row, bar, policy);
         }
       } else {
         mbar_arrive(bar);  // nothing loaded; the consumer masks this sub-tile out

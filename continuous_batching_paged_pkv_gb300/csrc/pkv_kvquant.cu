@@ -391,6 +391,9 @@ __global__ void __launch_bounds__(NW * 32, 1)
 
   int P = 0, C = 0, pa = 0, pb = 0;
   int pstage = 0;
+  // Each history row is read once per step: its L2 lines go first, which keeps
+  // the span partials this grid writes in L2 for the merge.
+  const uint64_t policy = l2_evict_first_policy();
   auto issue = [&](const Task &T, int u) {
     // only the sub-tiles holding this step's rows wait for the cache write
     if (!waited && T.reads_new && T.key0 + (u + 1) * kSubKeys > T.L - T.nrows) {
@@ -402,8 +405,8 @@ __global__ void __launch_bounds__(NW * 32, 1)
       uint64_t *bar = full + pstage;
       if (row >= 0) {
         mbar_arrive_expect_tx(bar, Cfg::kStageTx);
-        tma_load_2d(ring + pstage * Cfg::kCodeBytes, &tmap_kc, 0, row, bar);
-        tma_load_2d(ring + Cfg::kVc + pstage * Cfg::kCodeBytes, &tmap_vc, 0, row, bar);
+        tma_load_2d_hint(ring + pstage * Cfg::kCodeBytes, &tmap_kc, 0, row, bar, policy);
+        tma_load_2d_hint(ring + Cfg::kVc + pstage * Cfg::kCodeBytes, &tmap_vc, 0, row, bar, policy);
         bulk_load(ring + Cfg::kKs + pstage * Cfg::kScaleBytes, k_scales + static_cast<int64_t>(row) * NG,
                   Cfg::kScaleBytes, bar);
         bulk_load(ring + Cfg::kVs + pstage * Cfg::kScaleBytes, v_scales + static_cast<int64_t>(row) * NG,
