@@ -81,6 +81,23 @@ bool encode_pool(CUtensorMap *m, const void *pool, int64_t rows, int32_t head_di
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Key pool at head_dim 128 for the chunk kernel, seen as five dimensions
+// (column within a 64-column half, key within 8, half, group of 8 keys within
+// the block, block x kv head): one box is a whole 16-key sub-tile, 4 KiB,
+// landing as [key group][half][8 keys][128 B] in shared memory, so each
+// 8-key group of either half is one 128-byte-swizzle atom.
+bool encode_pool_subtiles(CUtensorMap *m, const void *pool, int64_t block_heads, int32_t block_size) {
+  EncodeFn enc = encoder();
+  if (!enc) return false;
+  cuuint64_t dims[5] = {64, 8, 2, static_cast<cuuint64_t>(block_size / 8), static_cast<cuuint64_t>(block_heads)};
+  cuuint64_t strides[4] = {256, 128, 2048, static_cast<cuuint64_t>(block_size) * 256};
+  cuuint32_t box[5] = {64, 8, 2, static_cast<cuuint32_t>(pkv::kSubKeys / 8), 1};
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(pool), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 8-bit codes [rows][D] -> boxes of 16 whole rows; 128-byte swizzle for
 // 128-byte rows (D = 128), 64-byte swizzle for 64-byte rows (D = 64).
 // Code rows of head_dim * bits / 8 bytes (128 or 64), 16-row boxes with the
@@ -198,11 +215,13 @@ pkv_status pkv_attention(const void *q, const int32_t *cu_seqlens_q, int32_t num
   a.task_counter =
       need ? reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(workspace) + acc_bytes + ml_bytes) : nullptr;
 
-  CUtensorMap tk, tv, tq;
+  CUtensorMap tk, tv, tq, tks;
   if (!encode_pool(&tk, k_pool, rows, head_dim) || !encode_pool(&tv, v_pool, rows, head_dim))
     return PKV_ERR_CUDA;
   const int32_t rpt = pkv::prefill_rows_per_tile(a.group);
-  if (info->num_prefill_items > 0 && !encode_q(&tq, q, total_q, num_q_heads, head_dim, a.group, rpt))
+  if (info->num_prefill_items > 0 &&
+      (!encode_q(&tq, q, total_q, num_q_heads, head_dim, a.group, rpt) ||
+       (head_dim == 128 && !encode_pool_subtiles(&tks, k_pool, num_blocks * num_kv_heads, block_size))))
     return PKV_ERR_CUDA;
 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -218,7 +237,7 @@ pkv_status pkv_attention(const void *q, const int32_t *cu_seqlens_q, int32_t num
   if (side) lock = std::unique_lock<std::mutex>(side->mu);
   cudaError_t e = side ? cudaEventRecord(side->fork, st) : cudaSuccess;
   if (e == cudaSuccess)
-    e = head_dim == 128 ? pkv::launch_prefill_pair(a, tq, tk, tv, rpt, info->num_prefill_items, pre, st)
+    e = head_dim == 128 ? pkv::launch_prefill_pair(a, tq, tks, tv, rpt, info->num_prefill_items, pre, st)
                         : pkv::launch_prefill(a, tq, rpt, info->num_prefill_items, pre, st);
   cudaStream_t dst = side ? side->stream : st;
   if (e == cudaSuccess && side) e = cudaStreamWaitEvent(side->stream, side->fork, 0);
@@ -382,7 +401,9 @@ static pkv_status attention_quant(int32_t bits, const void *q, const int32_t *cu
   if (info->num_prefill_items > 0) {
     const int64_t srows = static_cast<int64_t>(sb) * num_kv_heads * block_size;
     if (!encode_q(&tq, q, total_q, num_q_heads, head_dim, a.group, rpt) ||
-        !encode_pool(&tk, scratch_k, srows, head_dim) || !encode_pool(&tv, scratch_v, srows, head_dim))
+        !encode_pool(&tv, scratch_v, srows, head_dim) ||
+        (head_dim == 128 ? !encode_pool_subtiles(&tk, scratch_k, static_cast<int64_t>(sb) * num_kv_heads, block_size)
+                         : !encode_pool(&tk, scratch_k, srows, head_dim)))
       return PKV_ERR_CUDA;
   }
 

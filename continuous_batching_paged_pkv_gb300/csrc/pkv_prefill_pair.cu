@@ -12,14 +12,16 @@
 // (row m = position m/G, head m%G). The even CTA issues M = 256 MMAs that
 // span both tiles. B operands are split by N between the CTAs, so each SM
 // loads half of every K/V tile: the keys [64r, 64r+64) of K and the head_dim
-// columns [64r, 64r+64) of V, for CTA r. With 2 KiB TMA boxes (the largest
-// this pool layout allows) one SM receives about 27 B/clk; a 128-row tile
-// alone would need about 60 B/clk to keep its tensor core busy, a pair needs
-// half of that per SM.
+// columns [64r, 64r+64) of V, for CTA r. The TMA unit's cost is mostly per
+// box (about 70 SM cycles for a 2 KiB box): a K sub-tile (16 keys, both
+// halves of head_dim) is one 4 KiB box through a five-dimensional view of the
+// pool, a V sub-tile half one 2 KiB box (the half belongs to one CTA), so an
+// SM takes 12 boxes per tile. A 128-row tile alone would need about 60 B/clk
+// to keep its tensor core busy, a pair needs half of that per SM.
 //
 //   warp 0 (32 lanes)  TMA producer, both CTAs: Q once, then per 128-key tile
-//                      16 boxes of this CTA's halves, counted on the even
-//                      CTA's barriers; four stages.
+//                      12 boxes of this CTA's parts, counted on the even
+//                      CTA's barriers; six stages.
 //   warp 1 (one lane)  QK issuer, even CTA only: S_j = Q K_j^T (SS, M 256,
 //                      N 128 keys) into S/P buffer j % 3, as soon as that
 //                      buffer's previous P V product has finished.
@@ -67,10 +69,10 @@ constexpr uint32_t kNegInfBits = 0xff800000u;
 struct Layout {
   static constexpr int kQHalf = 128 * 128;                 // 128 rows x 128 B: one 64-column half of D
   static constexpr int kQBytes = 2 * kQHalf;
-  static constexpr int kKHalf = (kKeysPerTile / 2) * 128;  // this CTA's 64 keys x 128 B
-  static constexpr int kKBytes = 2 * kKHalf;
+  static constexpr int kKSub = kSubKeys * 256;              // one 16-key sub-tile of K: [2 groups][2 halves][8 keys][128 B]
+  static constexpr int kKBytes = (kKeysPerTile / 2 / kSubKeys) * kKSub;  // this CTA's 64 keys
   static constexpr int kVBytes = kKeysPerTile * 128;       // 128 keys x this CTA's 64 columns
-  static constexpr int kStageBytes = kKBytes + kVBytes;    // 32 KiB: 16 boxes of 2 KiB
+  static constexpr int kStageBytes = kKBytes + kVBytes;    // 32 KiB: 4 K boxes of 4 KiB, 8 V boxes of 2 KiB
   static constexpr int kBarOffset = kQBytes + kStages * kStageBytes;
   static constexpr int kSmem = kBarOffset + 256 + 1024;    // barriers/flags + alignment slack
 };
@@ -227,13 +229,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_pair_kernel(const __grid_
       for (int h = 0; h < 2; ++h)
         tma_load_3d_pair(sQ + h * Lay::kQHalf, &tmap_q, h * 64, g * G, row0 + pos0, q_full);
     }
-    // Lane l < 8 loads K sub-tile 4r + l/2, half l%2; lane 8 <= l < 16 loads
-    // V sub-tile l-8, this CTA's half of head_dim.
-    const bool is_k = lane < 8;
-    const int u = is_k ? static_cast<int>(rank) * 4 + (lane >> 1) : lane - 8;
-    const int x = is_k ? (lane & 1) * 64 : static_cast<int>(rank) * 64;
-    const int dst_off = is_k ? (lane & 1) * Lay::kKHalf + (lane >> 1) * kSubKeys * 128
-                             : Lay::kKBytes + (lane - 8) * kSubKeys * 128;
+    // Lane l < 4 loads K sub-tile 4r + l (both halves of head_dim, one box);
+    // lane 8 <= l < 16 loads V sub-tile l-8, this CTA's half of head_dim.
+    const bool is_k = lane < 4, is_v = lane >= 8 && lane < 16;
+    const int u = is_k ? static_cast<int>(rank) * 4 + lane : lane - 8;
+    const int dst_off = is_k ? lane * Lay::kKSub : Lay::kKBytes + (lane - 8) * kSubKeys * 128;
+    const int bs_shift = 31 - __clz(a.block_size);  // block sizes are powers of two
     bool waited = false;
     for (int j = 0; j < ntiles; ++j) {
       const int s = j % kStages;
@@ -254,8 +255,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_pair_kernel(const __grid_
         grid_dependency_wait();
         waited = true;
       }
-      if (lane < 16 && u < vs)
-        tma_load_2d_pair(sKV + s * Lay::kStageBytes + dst_off, is_k ? &tmap_k : &tmap_v, x, urow, kv_full);
+      if (is_k && u < vs)
+        tma_load_5d_pair(sKV + s * Lay::kStageBytes + dst_off, &tmap_k, 0, 0, 0, (urow & (a.block_size - 1)) >> 3,
+                         urow >> bs_shift, kv_full);
+      if (is_v && u < vs)
+        tma_load_2d_pair(sKV + s * Lay::kStageBytes + dst_off, &tmap_v, static_cast<int>(rank) * 64, urow, kv_full);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ QK issuer
@@ -272,10 +276,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_pair_kernel(const __grid_
         tc_fence_after();
         const uint32_t k_base = smem_addr(sKV + (j % kStages) * Lay::kStageBytes);
         for (int kk = 0; kk < D / 16; ++kk) {
+          // K: 8-key groups 2048 B apart, the second half of head_dim 1024 B after the first
           const uint32_t qoff = (kk >> 2) * Lay::kQHalf + (kk & 3) * 32;
-          const uint32_t koff = (kk >> 2) * Lay::kKHalf + (kk & 3) * 32;
+          const uint32_t koff = (kk >> 2) * 1024 + (kk & 3) * 32;
           tc_mma_ss_pair(tmem + s * 128, smem_desc_sw128(q_base + qoff, 16, 1024),
-                         smem_desc_sw128(k_base + koff, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+                         smem_desc_sw128(k_base + koff, 16, 2048), idesc_qk, kk > 0 ? 1u : 0u);
         }
         tc_commit_pair(bar + kSFull + s);
       }
