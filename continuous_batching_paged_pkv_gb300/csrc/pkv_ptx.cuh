@@ -88,26 +88,6 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
-// 2^x on the FMA pipe, to share the work of a softmax with the SFU.
-// Range reduction x = n + f with n = rint(x), taken from the low mantissa bits of
-// x + 1.5*2^23 (valid while |x| < 2^22), so f is in [-1/2, 1/2]; 2^f from the cubic
-// 1 + f(c1 + f(c2 + f c3)) whose coefficients were fitted to minimise the relative
-// error on that interval (max 1.02e-4, below bf16's 2^-9); 2^n is added straight
-// into the exponent field. x below -125 is clamped, giving 2^-125 (not 0).
-__device__ __forceinline__ float exp2_fma_poly(float x) {
-  x = fmaxf(x, -125.f);
-  const float t = x + 12582912.f;
-  const float f = x - (t - 12582912.f);
-  const float p = fmaf(f, fmaf(f, fmaf(f, 0.05500893f, 0.24221098f), 0.69328290f), 1.f);
-  return __uint_as_float(__float_as_uint(p) + (__float_as_uint(t) << 23));
-}
-
-// Two floats to bf16x2 by truncation (upper halves of the bit patterns; lo in
-// the low half). One byte permute on the integer pipe instead of a conversion.
-__device__ __forceinline__ uint32_t pack_bf16x2_trunc(float lo, float hi) {
-  return __byte_perm(__float_as_uint(lo), __float_as_uint(hi), 0x7632);
-}
-
 // Order this thread's generic-proxy shared-memory accesses before later
 // async-proxy (TMA, tcgen05.mma) accesses of the same memory.
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -168,15 +148,6 @@ __device__ __forceinline__ void add2(float &d0, float &d1, float a0, float a1) {
 }
 
 // ---- TMA --------------------------------------------------------------------
-
-__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int32_t x,
-                                            int32_t y, uint64_t *bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
-      : "memory");
-}
 
 // L2 policy for data read once per step: its lines are the first to go, so
 // a stream of them does not push out what is written for a later kernel.
