@@ -320,6 +320,8 @@ def pkv_attention_no_alloc(q, cu_seqlens_q, seq_slot, context_lens, block_tables
     for t, nm in ((cu_seqlens_q, "cu_seqlens_q"), (seq_slot, "seq_slot"), (context_lens, "context_lens"),
                   (block_tables, "block_tables"), (work, "work")):
         _need(t, "torch.int32", nm)
+    _need(k_pool, "torch.bfloat16", "k_pool")
+    _need(v_pool, "torch.bfloat16", "v_pool")
     nb, hkv, bs, d = k_pool.shape
     ms, mbps = block_tables.shape
     _check(_lib().pkv_attention_no_alloc(_t_ptr(q), _t_ptr(cu_seqlens_q), cu_seqlens_q.numel() - 1, q.shape[0],

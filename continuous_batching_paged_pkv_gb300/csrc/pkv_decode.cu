@@ -714,16 +714,10 @@ template <int D, int NT, bool MULTI, int NW = kWarps, int NS = 0>
 cudaError_t launch_decode_t(const StepArgs &a, const CUtensorMap &tk, const CUtensorMap &tv, int32_t num_items,
                             const int32_t *items, cudaStream_t stream) {
   constexpr int smem = DecodeCfg<D, NW, NS>::kSmem;
-  static uint64_t configured = 0;  // one bit per device
-  int dev = 0;
-  cudaGetDevice(&dev);
-  const uint64_t bit = 1ull << (dev & 63);
-  if (!(configured & bit)) {
-    cudaError_t e =
-        cudaFuncSetAttribute(decode_kernel<D, NT, MULTI, NW, NS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    configured |= bit;
-  }
+  static std::atomic<uint64_t> configured{0};  // one bit per device
+  if (const cudaError_t e = allow_smem_once(decode_kernel<D, NT, MULTI, NW, NS>, smem, configured);
+      e != cudaSuccess)
+    return e;
   const int64_t tasks = static_cast<int64_t>(num_items) * a.num_kv_heads;
   const int grid = static_cast<int>(tasks < sm_count() ? tasks : sm_count());
   // Past three static rounds, warps take tasks from the workspace counter, so

@@ -10,10 +10,11 @@
 // library's 8-bit format: every pool row (token, kv head) is cut into groups
 // of 32 values; a group keeps one power-of-two scale d, the smallest at or
 // above amax / 127 (at least 2^-126), stored as a bfloat16 (exact), and 32
-// int8 codes round_half_even(x / d) clamped to [-127, 127] -- the
-// shared-exponent choice of the OCP microscaling formats. x / d is exact and
-// every code * d is a bfloat16 number, so widening codes to bf16 loses
-// nothing. Codes live in [num_blocks][Hkv][bs][D] int8, scales in
+// int8 codes round_half_even(x / d) clamped to [-127, 127]. The power-of-two
+// ceiling is this library's own rule: x / d is exact and every code * d is a
+// bfloat16 number, so widening codes to bf16 loses nothing; the price is up to
+// one bit at the group maximum, whose code lands in [64, 127] rather than at
+// 127. Codes live in [num_blocks][Hkv][bs][D] int8, scales in
 // [num_blocks][Hkv][bs][D / 32] bf16: a row costs D + D / 16 bytes instead of
 // 2 D, so decode reads 53% of the bf16 pool's bytes. The 4-bit format keeps
 // the groups and the scale rule with 7 in place of 127 and stores the codes as
@@ -762,16 +763,10 @@ cudaError_t launch_decode_quant_w(const StepArgs &a, const CUtensorMap &tk, cons
                                const void *k_scales, const void *v_scales, int32_t num_items, const int32_t *items,
                                int grid, cudaStream_t stream) {
   constexpr int smem = QuantCfg<D, NW, BITS>::kSmem;
-  static uint64_t configured = 0;  // one bit per device
-  int dev = 0;
-  cudaGetDevice(&dev);
-  const uint64_t bit = 1ull << (dev & 63);
-  if (!(configured & bit)) {
-    cudaError_t e = cudaFuncSetAttribute(decode_quant_kernel<D, NT, MULTI, NW, BITS>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    configured |= bit;
-  }
+  static std::atomic<uint64_t> configured{0};  // one bit per device
+  if (const cudaError_t e = allow_smem_once(decode_quant_kernel<D, NT, MULTI, NW, BITS>, smem, configured);
+      e != cudaSuccess)
+    return e;
   const int64_t tasks = static_cast<int64_t>(num_items) * a.num_kv_heads;
   StepArgs b = a;  // past three static rounds, tasks come from the workspace counter
   if (b.task_counter && tasks > 3ll * grid * NW) {

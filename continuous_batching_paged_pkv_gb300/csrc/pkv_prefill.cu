@@ -416,15 +416,8 @@ template <int D>
 cudaError_t launch_prefill_t(const StepArgs &a, const CUtensorMap &tq, int32_t rows_per_tile, int32_t num_items,
                              const int32_t *items, cudaStream_t stream) {
   constexpr int smem = PrefillLayout<D>::kSmem;
-  static uint64_t configured = 0;  // one bit per device
-  int dev = 0;
-  cudaGetDevice(&dev);
-  const uint64_t bit = 1ull << (dev & 63);
-  if (!(configured & bit)) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    configured |= bit;
-  }
+  static std::atomic<uint64_t> configured{0};  // one bit per device
+  if (const cudaError_t e = allow_smem_once(prefill_kernel<D>, smem, configured); e != cudaSuccess) return e;
   dim3 grid(static_cast<unsigned>(num_items), static_cast<unsigned>(a.num_kv_heads));
   return launch_pdl(prefill_kernel<D>, grid, dim3(kThreads), smem, stream, tq, a, items, rows_per_tile);
 }

@@ -447,15 +447,8 @@ cudaError_t launch_prefill_pair(const StepArgs &a, const CUtensorMap &tq, const 
                                 const int32_t *items, cudaStream_t stream) {
   if (num_items <= 0) return cudaSuccess;
   constexpr int smem = Layout::kSmem;
-  static uint64_t configured = 0;  // one bit per device
-  int dev = 0;
-  cudaGetDevice(&dev);
-  const uint64_t bit = 1ull << (dev & 63);
-  if (!(configured & bit)) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    configured |= bit;
-  }
+  static std::atomic<uint64_t> configured{0};  // one bit per device
+  if (const cudaError_t e = allow_smem_once(prefill_pair_kernel, smem, configured); e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(2 * num_items), static_cast<unsigned>(a.num_kv_heads));
   cfg.blockDim = dim3(kThreads);

@@ -20,10 +20,12 @@ Q = 2^(B-1) - 1 (127 for 8 bits, 7 for 4 bits):
     amax = max |x|;  t = amax / Q;  d = the smallest power of two >= t
     (at least 2^-126; 0 when amax is 0);
     code = clamp(round_half_even(x / d), -Q, Q), or 0 when d is 0.
-  A power-of-two scale is the shared-exponent choice of the OCP microscaling
-  formats: x / d is exact, |x - code * d| <= d / 2, and every value a code
-  stands for is exactly a bfloat16 number (at most 7 significant bits times a
+  This power-of-two ceiling is this library's own reading (the pages fix no
+  rule). It makes x / d exact, |x - code * d| <= d / 2, and every value a code
+  stands for exactly a bfloat16 number (at most 7 significant bits times a
   power of two), so attention may widen codes to bfloat16 without rounding.
+  Its cost: rounding the scale up leaves the group maximum's code anywhere in
+  [(Q + 1) / 2, Q] rather than at Q, up to one bit of precision lost there.
 * storage: 8-bit codes one per byte; 4-bit codes two per byte, the code of
   the even value in the low nibble, each a 4-bit two's complement number
   (``pack_nibbles``). Scales are stored as in the 8-bit pool.

@@ -586,3 +586,59 @@ def test_planted_mistakes_are_caught(oracle_lib, tmp_path, name):
     so = _build_mutant(tmp_path, old, new)
     assert not _pins_pass(so), f"pins missed the planted mistake: {name}"
     assert _pins_pass(oracle.build()), "the unmodified oracle must pass its pins"
+
+
+# ---- the churn replay's row-subset attention ---------------------------------
+# The churn checks compare kernel rows with ContiguousHistory.attend(keep=...),
+# which computes each kept row as the last row of a shorter prefix. Pinned here
+# against the brute force over the whole contiguous history (a masked score
+# matrix, no prefix slicing), with histories built by several appends.
+
+def _subset_pin(history_cls) -> bool:
+    """True if ``history_cls.attend(keep=...)`` matches the brute force on every case."""
+    rng = np.random.default_rng(2024)
+    for n, chunks, hq, hkv, d in [(1, [5, 1], 4, 2, 16), (7, [16, 9, 7], 6, 2, 32), (64, [100, 37, 64], 4, 1, 16)]:
+        h = history_cls()
+        for c in chunks:
+            h.append(7, _rand(rng, (c, hkv, d)), _rand(rng, (c, hkv, d)))
+        k, v = np.concatenate(h.k[7]), np.concatenate(h.v[7])
+        q = _rand(rng, (n, hq, d))
+        keep = sorted({0, n - 1} | set(int(i) for i in rng.choice(n, size=min(n, 5), replace=False)))
+        for mult in (1.0, 8.0):
+            qq = W.f32_to_bf16_bits(W.bf16_bits_to_f32(q) * mult)
+            got = h.attend(7, qq, 1 / np.sqrt(d), keep=keep)
+            ref = brute_force(qq, k, v, 1 / np.sqrt(d))
+            if not np.allclose(got[keep], ref[keep], rtol=0, atol=1e-12):
+                return False
+            rest = [i for i in range(n) if i not in keep]
+            if rest and not np.isnan(got[rest]).all():
+                return False
+            if not np.allclose(h.attend(7, qq, 1 / np.sqrt(d)), ref, rtol=0, atol=1e-12):
+                return False
+    return True
+
+
+def test_history_subset_rows_match_bruteforce(oracle_lib):
+    assert _subset_pin(churn.ContiguousHistory)
+
+
+HISTORY_MUTANTS = {
+    "kept row sees one key fewer": ("L = len(k) - n + i + 1", "L = len(k) - n + i"),
+    "kept row sees one key more": ("L = len(k) - n + i + 1", "L = min(len(k), len(k) - n + i + 2)"),
+    "kept row takes the first row's prefix": ("L = len(k) - n + i + 1", "L = len(k) - n + 1"),
+    "kept row answers with the wrong query": ("attention_dense(q_rows[i:i + 1]", "attention_dense(q_rows[n - 1:n]"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(HISTORY_MUTANTS))
+def test_history_subset_planted_mistakes_are_caught(oracle_lib, name):
+    import inspect
+    import textwrap
+
+    old, new = HISTORY_MUTANTS[name]
+    src = textwrap.dedent(inspect.getsource(churn.ContiguousHistory.attend))
+    assert src.count(old) == 1, old
+    ns = dict(vars(churn))
+    exec(compile(src.replace(old, new), "<mutant>", "exec"), ns)
+    mutant = type("MutantHistory", (churn.ContiguousHistory,), {"attend": ns["attend"]})
+    assert not _subset_pin(mutant), f"pin missed the planted mistake: {name}"

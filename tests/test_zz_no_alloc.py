@@ -11,6 +11,7 @@ This file is collected last on purpose.
 import numpy as np
 import pytest
 
+import oracle
 from continuous_batching_paged_pkv_gb300 import binding as B
 from continuous_batching_paged_pkv_gb300 import build as libbuild
 from continuous_batching_paged_pkv_gb300 import runtime as R
@@ -28,6 +29,7 @@ def cuda():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     libbuild.build()
+    oracle.build()
     return torch
 
 
@@ -38,17 +40,40 @@ def _close(got, ref):
     assert err.max() <= MAX_ABS and rel <= MAX_REL_L2, (err.max(), rel)
 
 
-@pytest.mark.parametrize("make", [lambda: W.decode5(0), lambda: W.mixed(0),
-                                  lambda: W.random_step(3, [(1, 3000), (40, 333), (1, 70)], num_q_heads=32,
-                                                        num_kv_heads=8, head_dim=128)])
-def test_no_alloc_matches_pkv_attention_twice(cuda, make):
+def _many_decode_tasks():
+    """128 one-row decode slots at contexts of 4-8 key spans, 64 q / 8 kv heads:
+    about 6,000 (span, kv head) tasks, more than three rounds for every warp of
+    a 152-SM grid, so the decode kernel hands out the rest from the task
+    counter that lives in the scratch array; its partials (~26 MB) still fit."""
+    ctx = np.random.default_rng(11).integers(1024, 2049, size=128)
+    return W.random_step(11, [(1, int(c)) for c in ctx], num_q_heads=64, num_kv_heads=8, head_dim=128)
+
+
+CASES = {
+    "decode x5": lambda: W.decode5(0),
+    "mixed": lambda: W.mixed(0),
+    "ragged": lambda: W.random_step(3, [(1, 3000), (40, 333), (1, 70)], num_q_heads=32, num_kv_heads=8,
+                                    head_dim=128),
+    "many decode tasks": _many_decode_tasks,
+}
+
+
+@pytest.mark.parametrize("case", sorted(CASES))
+def test_no_alloc_matches_pkv_attention_bit_for_bit_twice(cuda, case):
+    """Same kernels, same work list: the outputs must be the same bits as
+    pkv_attention's, on two calls in a row (the second finds the scratch array,
+    task counter included, as the first left it)."""
     torch = cuda
-    w = make()
+    w = CASES[case]()
     ds = R.prepare(w)
     assert 0 < ds.info.workspace_bytes <= B.PKV_NO_ALLOC_SCRATCH_BYTES or ds.info.workspace_bytes == 0
     R.run_step(ds)
     torch.cuda.synchronize()
-    ref = R.out_f32(ds)
+    assert B.pkv_check_device_status(ds.status) == 0
+    ref_bits = ds.out.view(torch.int16).clone()
+    # the reference itself is checked against the oracle once
+    st = oracle.prepare_step(w)
+    _close(R.out_f32(ds), oracle.step_attention(w, st))
     for _ in range(2):
         out = torch.empty_like(ds.out)
         out.view(torch.int16).fill_(R.SENTINEL_BITS)
@@ -56,7 +81,7 @@ def test_no_alloc_matches_pkv_attention_twice(cuda, make):
                                  ds.v_pool, ds.work, ds.info, out, scale=w.scale, device_status=ds.status)
         torch.cuda.synchronize()
         assert B.pkv_check_device_status(ds.status) == 0
-        _close(out.float().cpu().numpy(), ref)
+        assert torch.equal(out.view(torch.int16), ref_bits), "no-alloc output differs from pkv_attention's"
 
 
 def test_no_alloc_rejects_a_step_larger_than_its_array(cuda):
