@@ -1,25 +1,32 @@
 #!/usr/bin/env python
-"""Benchmark of one paged-KV attention step (cache write + attention) on GB300.
+"""Benchmark of the paged-KV attention step (cache write + attention) on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload decode5|mixed|decode256|tiny]
+                    [--workload churn|decode5|mixed|decode256|chunk2048|verify4|verify8|verify16|tiny]
 
-Prints one JSON line. The default workload is one decode step for five
-clients (40 q / 8 kv heads, head_dim 128, block 16, contexts U[1024, 8192],
-65,536-block pool). Metric: KV bytes the attention must read (each sequence's
-K and V once per kv head, plus Q in and O out) per second of device time.
+Prints one JSON line. The default workload is the continuous-batching churn
+trace (arrivals, chunked prompts beside decode rows, retirements; 32 q / 8 kv
+heads, head_dim 128, block 16, 131,072-block pool): the decode + prefill mix
+the metric is quoted on. Its timed window starts at trace step 50 whatever W
+is (the trace is replayed up to there untimed, its last W steps as warm-up),
+so the K timed steps are steady-state steps: a 512-row prompt chunk beside a
+growing decode batch. Metric: KV bytes the attention must read (each
+sequence's K and V once per kv head, plus Q in and O out) per second of device
+time, and packed rows per second.
 
-Timing: W untimed warm-up steps, then K timed steps. Before each step a
-256 MiB buffer is overwritten (larger than the 129 MB L2) so no step finds its
-K/V in L2, and a second 256 MiB buffer is then read so that L2 holds clean
-lines (otherwise the flush's dirty lines would be written back to HBM inside
-the timed step). Both are outside the CUDA events that bracket the step. The
-timed region brackets whole steps only, so the step's kernels may overlap
-their launches; a second pass brackets each library call with its own events
-on the launching stream to give the attention call's own duration (the
-roofline figure) and the per-call breakdown. Under torchrun (N > 1) every rank
-runs an independent replica (the step has no exchange between GPUs); the
-job's time is the maximum over ranks.
+The same line carries, under ``configs``, every single-step workload (decode
+x5, mixed, decode x256, a 2048-row chunk, verify steps of 4/8/16 rows), each
+with its value, roofline, end-to-end figure and oracle CPU baseline.
+
+Timing: before each step a 256 MiB buffer is overwritten (larger than the
+129 MB L2) so no step finds its K/V in L2, and a second 256 MiB buffer is then
+read so that L2 holds clean lines (otherwise the flush's dirty lines would be
+written back inside the timed step). Both are outside the CUDA events that
+bracket the step. A second pass times the chunk kernel alone and the decode
+and merge kernels alone on the same step (same stream, same flush): the
+per-kernel rooflines. Under torchrun (N > 1) every rank runs an independent
+replica (the step has no exchange between GPUs); the job's time is the
+maximum over ranks.
 """
 
 from __future__ import annotations
@@ -67,25 +74,43 @@ WORKLOAD_TEXT = {
              "(contexts U[200, 4000]), 32 q / 8 kv heads, head_dim 128, block 16, 65,536-block pool",
     "decode256": "decode step, 256 slots x 1 row, 64 q / 8 kv heads, head_dim 128, block 16, "
                  "lognormal contexts (median 2048, clip [16, 32768]), fragmented 131,072-block pool",
+    "chunk2048": "prompt chunk, the final 2048 rows [6144, 8192) of an 8192-token prompt, nothing decoding, "
+                 "32 q / 8 kv heads, head_dim 128, block 16, 65,536-block pool",
+    "verify4": "verify step, 64 slots x 4 causal draft rows, contexts U[1024, 8192], 32 q / 8 kv heads, "
+               "head_dim 128, block 16, 131,072-block pool",
+    "verify8": "verify step, 64 slots x 8 causal draft rows, contexts U[1024, 8192], 32 q / 8 kv heads, "
+               "head_dim 128, block 16, 131,072-block pool",
+    "verify16": "verify step, 64 slots x 16 causal draft rows, contexts U[1024, 8192], 32 q / 8 kv heads, "
+                "head_dim 128, block 16, 131,072-block pool",
     "tiny": "tiny mixed step, 4 q / 2 kv heads, head_dim 64, block 16, 32 blocks",
     "churn": "continuous-batching trace: Poisson(2) arrivals per step, prompts U[128, 8192], outputs "
              "geometric (mean 256, max 4096), 64 slots, chunks of 512 (2048 while nothing decodes), "
              "32 q / 8 kv heads, head_dim 128, block 16, 131,072-block pool; each step planned by the "
              "library's scheduler, pool and lowering",
 }
+# Single-step workloads carried in the churn line's ``configs``.
+EXTRA_CONFIGS = ("decode5", "mixed", "decode256", "chunk2048", "verify4", "verify8", "verify16")
+# First timed step of the churn trace: by then a decode batch runs beside every
+# 512-row prompt chunk (the trace's steady state).
+CHURN_OFFSET = 50
+L2_NOTE = ("flushed before every step: 256 MiB written, then 256 MiB read so L2 holds clean lines; "
+           "both outside the timed events")
 
 
 def parse_args(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=4000)
-    p.add_argument("--warmup", type=int, default=50)
+    p.add_argument("--steps", type=int, default=150)
+    p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", choices=sorted(WORKLOAD_TEXT), default="decode5")
+    p.add_argument("--workload", choices=sorted(WORKLOAD_TEXT), default="churn")
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle CPU-baseline budget")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=300)
+    p.add_argument("--no-configs", action="store_true", help="churn line without the single-step configs")
+    p.add_argument("--config-steps", type=int, default=100, help="timed steps of each single-step config")
+    p.add_argument("--config-cpu-seconds", type=float, default=2.0)
     p.add_argument("--kv", choices=["bf16", "q8", "q4"], default="bf16",
                    help="pool format: bf16, or the 8-bit / 4-bit block-scaled pool (no end-to-end leg)")
     p.add_argument("--pool-blocks", type=int, default=None,
@@ -97,27 +122,29 @@ def parse_args(argv=None):
 # Work accounting (from the workload's shapes only).
 # ---------------------------------------------------------------------------
 
-def kv_bytes(w, kv: str = "bf16") -> int:
+def kv_bytes(w, kv: str = "bf16", segments=None) -> int:
     """Algorithmic bytes of the attention: K and V of every visible key once per kv head, Q in, O out.
 
     A key's row costs 2 * head_dim bytes in a bf16 pool, head_dim (8-bit) or
     head_dim / 2 (4-bit) bytes of codes plus head_dim / 32 bf16 scales in the
-    block-scaled pools."""
+    block-scaled pools. ``segments`` restricts the count to those segments."""
+    segs = w.segments if segments is None else segments
     codes = {"bf16": 0, "q8": w.head_dim, "q4": w.head_dim // 2}[kv]
     row = w.head_dim * 2 if kv == "bf16" else codes + w.head_dim // 16
-    kvb = sum(s.ctx for s in w.segments) * w.num_kv_heads * row * 2
-    return kvb + w.total_q * w.num_q_heads * w.head_dim * 2 * 2
+    kvb = sum(s.ctx for s in segs) * w.num_kv_heads * row * 2
+    return kvb + sum(s.q_len for s in segs) * w.num_q_heads * w.head_dim * 2 * 2
 
 
-def write_bytes(w) -> int:
-    return w.total_q * w.num_kv_heads * w.head_dim * 2 * 2 * 2  # K+V read and written
+def decode_path(w, s) -> bool:
+    """Segments of up to 16 / G rows run on the split-KV decode path, longer ones on the chunk kernel."""
+    return s.q_len <= max(1, 16 // (w.num_q_heads // w.num_kv_heads))
 
 
 def chunk_flops(w) -> int:
-    """Causal-only flops of the prompt-chunk rows: 4 * D * Hq * sum over rows of visible keys."""
+    """Causal-only flops of the chunk-path rows: 4 * D * Hq * sum over rows of visible keys."""
     tot = 0
     for s in w.segments:
-        if s.q_len > 1:
+        if s.q_len > 0 and not decode_path(w, s):
             first = s.ctx - s.q_len + 1
             tot += s.q_len * first + s.q_len * (s.q_len - 1) // 2
     return 4 * w.head_dim * w.num_q_heads * tot
@@ -162,6 +189,14 @@ class ClockSampler:
         self.gpu_id = gpu_id
         self.proc = None
         self.path = None
+
+    @classmethod
+    def for_device(cls, dev):
+        import torch
+
+        props = torch.cuda.get_device_properties(dev)
+        uuid = str(getattr(props, "uuid", "")) or None
+        return cls(("GPU-" + uuid) if uuid and not uuid.startswith("GPU-") else uuid)
 
     def start(self):
         fd, self.path = tempfile.mkstemp(suffix=".csv")
@@ -229,43 +264,65 @@ def barrier(world):
         dist.barrier()
 
 
+def mean(xs):
+    return sum(xs) / len(xs)
+
+
 # ---------------------------------------------------------------------------
 # CPU baseline: the oracle as it stands, on the host's cores.
 # ---------------------------------------------------------------------------
 
-def cpu_baseline(w, seconds: float, rows_per_run=None, threads=None):
+def cpu_baseline(w, seconds: float, threads=None):
+    """The oracle on whole steps of ``w`` (paged walk, fp64) for about ``seconds``."""
     import oracle
 
     oracle.build()
     cores = threads or oracle.default_threads()
     st = oracle.prepare_step(w)
-    seg_rows = []
-    start = 0
-    for s in w.segments:
-        seg_rows.append((start, s))
-        start += s.q_len
     done_bytes, runs = 0, 0
     t0 = time.perf_counter()
     while True:
-        if rows_per_run is None:
-            oracle.step_attention(w, st, threads=cores)
-            done_bytes += kv_bytes(w)
-        else:
-            r0, s = seg_rows[runs % len(seg_rows)]
-            oracle.step_attention(w, st, rows=list(range(r0, r0 + s.q_len)), threads=cores)
-            done_bytes += s.ctx * w.num_kv_heads * w.head_dim * 4 + s.q_len * w.num_q_heads * w.head_dim * 4
+        oracle.step_attention(w, st, threads=cores)
+        done_bytes += kv_bytes(w)
         runs += 1
         el = time.perf_counter() - t0
         if el >= seconds:
             break
     return {"value": done_bytes / el / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
-            "sample": f"{runs} run(s) of the oracle over " +
-                      ("the whole step" if rows_per_run is None else "one segment at a time, in turn") +
-                      f" in {el:.1f} s (fp64, {cores} threads)"}
+            "sample": f"{runs} run(s) of the oracle over the whole step in {el:.1f} s (fp64, {cores} threads)"}
+
+
+def churn_oracle_rows(samples, toks, hkv, hq, d, scale, seconds, threads=None):
+    """The oracle's dense attention on sampled churn rows (a segment's last row
+    over its whole history), spread evenly over the samples, about ``seconds`` of
+    oracle time on ``threads`` host threads (one row per thread at a time; each
+    batch's histories are generated outside the clock)."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    import oracle
+
+    oracle.build()
+    cores = threads or oracle.default_threads()
+    stride = max(1, len(samples) // 400)
+    picked = samples[::stride]
+    done_b, runs, el = 0, 0, 0.0
+    with ThreadPoolExecutor(max_workers=cores) as ex:
+        for b0 in range(0, len(picked), cores):
+            batch = [(toks.rows(rid, 0, L), qrow, L) for rid, L, qrow in picked[b0:b0 + cores]]
+            t0 = time.perf_counter()
+            list(ex.map(lambda it: oracle.attention_dense(it[1], it[0][0], it[0][1], scale), batch))
+            el += time.perf_counter() - t0
+            done_b += sum(L * hkv * d * 4 + hq * d * 4 for _, _, L in batch)
+            runs += len(batch)
+            if el >= seconds:
+                break
+    return {"value": done_b / el / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{runs} sampled rows of the timed trace steps (the last row of a segment, over its "
+                      f"whole history), fp64, {cores} threads one row each, {el:.1f} s of oracle time"}
 
 
 # ---------------------------------------------------------------------------
-# Arms.
+# Reference arm: the oracle on the host.
 # ---------------------------------------------------------------------------
 
 def run_reference(args, rank, world):
@@ -285,6 +342,7 @@ def run_reference(args, rank, world):
     for s in w.segments:
         segs.append((start, s))
         start += s.q_len
+
     # Each step is one segment of the workload (rotating), so K steps stay bounded.
     def one(i):
         r0, s = segs[i % len(segs)]
@@ -309,9 +367,17 @@ def run_reference(args, rank, world):
             "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def churn_window(args, num_steps):
+    """(first timed step, timed steps): the window starts at CHURN_OFFSET, or
+    earlier when K steps would run past the trace's end."""
+    timed = max(1, min(args.steps, num_steps))
+    first = min(CHURN_OFFSET, num_steps - timed)
+    return first, timed
+
+
 def run_reference_churn(args):
     """The churn trace as the oracle replays it (its own admission rules, no
-    library code); each timed step's rows sampled as in the churn arm."""
+    library code); rows of the timed window sampled as in the churn arm."""
     import numpy as np
 
     from oracle import churn
@@ -321,11 +387,11 @@ def run_reference_churn(args):
     reqs = W.churn_trace(args.seed, spec)
     ref = churn.ChurnReplay(reqs, max_slots=spec.max_slots, num_blocks=spec.num_blocks, block_size=spec.block_size)
     toks = W.TokenSource(args.seed, spec.num_q_heads, spec.num_kv_heads, spec.head_dim)
-    warm = max(args.warmup, 3)
+    first, timed = churn_window(args, spec.num_steps)
     samples = []
-    for step in range(warm + max(1, min(args.steps, spec.num_steps - warm))):
+    for step in range(first + timed):
         rows = ref.plan()
-        if step >= warm:
+        if step >= first:
             for r in rows:
                 samples.append((r.rid, r.begin + r.n, toks.rows(r.rid, r.begin + r.n - 1, r.begin + r.n)[2]))
         ref.commit(rows)
@@ -334,172 +400,233 @@ def run_reference_churn(args):
     return {"metric": METRIC, "value": cb["value"], "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": f"churn: {WORKLOAD_TEXT['churn']}", "sample": cb["sample"]},
+            "config": {"workload": f"churn: {WORKLOAD_TEXT['churn']}",
+                       "trace_steps": f"steps {first}..{first + timed - 1} sampled", "sample": cb["sample"]},
             "impl": "reference", "cpu_baseline": cb,
             "e2e": {"value": cb["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
-def run_ours(args, rank, world, local_rank):
-    import numpy as np
+# ---------------------------------------------------------------------------
+# Our arm: single steps.
+# ---------------------------------------------------------------------------
+
+def timed_calls(flush, stream, fns, n):
+    """Run ``fns`` ``n`` times, each time after an L2 flush, with events between
+    the calls: per call, a list of ``n`` durations in ms."""
+    import torch
+
+    out = [[] for _ in fns]
+    chunk = 500
+    done = 0
+    while done < n:
+        m = min(chunk, n - done)
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(fns) + 1)] for _ in range(m)]
+        for row in ev:
+            flush()
+            row[0].record(stream)
+            for f, e in zip(fns, row[1:]):
+                f()
+                e.record(stream)
+        torch.cuda.synchronize()
+        for row in ev:
+            for i in range(len(fns)):
+                out[i].append(row[i].elapsed_time(row[i + 1]))
+        done += m
+    return out
+
+
+def measure_step(name, w, dev, *, kv, steps, warmup, e2e_steps, flush, world=1, clocks=False):
+    """Device and end-to-end timings of one synthetic step (see the module docstring)."""
     import torch
 
     from continuous_batching_paged_pkv_gb300 import binding as B
-    from continuous_batching_paged_pkv_gb300 import build as libbuild
     from continuous_batching_paged_pkv_gb300 import runtime as R
+
+    ds = R.prepare(w, dev, kv=kv)
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        flush()
+        R.run_step(ds)
+    torch.cuda.synchronize()
+    if B.pkv_check_device_status(ds.status) != 0:
+        raise RuntimeError(f"{name}: device status reported an error during warm-up")
+
+    sampler = ClockSampler.for_device(dev) if clocks else None
+    if sampler:
+        sampler.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    # Timed region: one event pair around each whole step (cache write + attention).
+    (step_ms,) = timed_calls(flush, stream, [lambda: (R.run_cache_write(ds), R.run_attention(ds))], steps)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = sampler.stop() if sampler else None
+    # Breakdown pass (same stream, same flush): each call's own duration.
+    nb = max(steps // 4, 20)
+    write_ms, attn_ms = timed_calls(flush, stream, [lambda: R.run_cache_write(ds), lambda: R.run_attention(ds)], nb)
+    # Per-kernel passes: the same attention call with only the chunk items (the
+    # chunk kernel alone), and with only the decode and merge items.
+    chunk_ms = decode_ms = []
+    if kv == "bf16":
+        cw, dw = R.split_work(ds.work, ds.info)
+        if cw is not None:
+            (chunk_ms,) = timed_calls(flush, stream, [lambda: R.run_chunk_only(ds, cw)], nb)
+        if dw is not None:
+            (decode_ms,) = timed_calls(flush, stream, [lambda: R.run_decode_only(ds, dw)], nb)
+    if B.pkv_check_device_status(ds.status) != 0:
+        raise RuntimeError(f"{name}: device status reported an error during the timed steps")
+    e2e = run_e2e(w, ds, dev, flush, e2e_steps) if kv == "bf16" else None
+    info = ds.info
+    launches = (int(w.total_q > 0) + int(info.num_decode_items > 0) + int(info.num_prefill_items > 0)
+                + int(info.num_combine_items > 0))
+    del ds
+    torch.cuda.empty_cache()
+    return {"step_ms": step_ms, "write_ms": write_ms, "attn_ms": attn_ms, "chunk_ms": chunk_ms,
+            "decode_ms": decode_ms, "e2e": e2e, "clocks": clk, "launches": launches}
+
+
+def kernel_rooflines(w, m, kv, hbm, tflops, peak_src, workload):
+    """Per-kernel figures: the chunk kernel against the bf16 peak, the decode
+    and merge kernels against HBM. Returns (dict by kernel, the dominant one)."""
+    out = {}
+    if m["chunk_ms"]:
+        cm = mean(m["chunk_ms"])
+        fl = chunk_flops(w)
+        ach = fl / (cm / 1e3) / 1e12
+        src = "pkv_prefill_pair.cu" if w.head_dim == 128 else "pkv_prefill.cu"
+        out["chunk"] = {"bound": "tensor", "kernel": "prefill_pair_kernel" if w.head_dim == 128 else "prefill_kernel",
+                        "achieved": ach, "peak": tflops, "unit": "TFLOP/s", "frac": ach / tflops,
+                        "traffic": profiled_traffic(src, workload), "algorithmic_flop_per_launch": fl,
+                        "mean_launch_ms": cm,
+                        "peak_source": f"{peak_src} bf16 burst (the chunk kernel is timed alone)"}
+    if m["decode_ms"]:
+        dm = mean(m["decode_ms"])
+        db = kv_bytes(w, kv, [s for s in w.segments if s.q_len > 0 and decode_path(w, s)])
+        ach = db / (dm / 1e3) / 1e9
+        out["decode"] = {"bound": "hbm", "kernel": "decode_kernel + span merge (merge_small/merge_wide)",
+                         "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
+                         "traffic": profiled_traffic("pkv_decode.cu", workload) if not m["chunk_ms"] else None,
+                         "algorithmic_bytes_per_launch": db, "mean_launch_ms": dm,
+                         "peak_source": f"{peak_src} HBM copy bandwidth"}
+    if not out:
+        return out, None
+    dominant = max(out, key=lambda k: out[k]["mean_launch_ms"])
+    return out, dominant
+
+
+def single_line(name, w, m, *, kv, world, steps, cpu=None):
+    """The metric and its rooflines for one synthetic step workload."""
+    hbm, tflops, peak_src = peaks()
+    kvb = kv_bytes(w, kv)
+    total_ms, total_bytes = aggregate(sum(m["step_ms"]), kvb * steps, world)
+    value = total_bytes / (total_ms / 1e3) / 1e9
+    attn_mean = mean(m["attn_ms"])
+    achieved = kvb / (attn_mean / 1e3) / 1e9
+    res = {
+        "value": value, "unit": "GB/s", "ms_per_step": total_ms / steps,
+        "pct_hbm_peak": 100.0 * value / world / hbm,
+        "rows_per_s": world * w.total_q / (total_ms / steps / 1e3),
+        "step_breakdown_ms": {"cache_write": statistics.median(m["write_ms"]),
+                              "attention": statistics.median(m["attn_ms"]),
+                              "step": statistics.median(m["step_ms"])},
+        "attention_call": {"kv_gbs": achieved, "pct_hbm_peak": 100.0 * achieved / hbm, "mean_ms": attn_mean},
+    }
+    kernels, dominant = kernel_rooflines(w, m, kv, hbm, tflops, peak_src, name)
+    if kernels:
+        res["kernels"] = kernels
+    if dominant == "chunk":
+        res["roofline"] = kernels["chunk"]
+    elif dominant == "decode" and "chunk" not in kernels:
+        # decode-only steps: the attention call (decode + merge) is the kernel pair that bounds the step
+        dec = "decode_quant_kernel" if kv in ("q8", "q4") else "decode_kernel"
+        src = "pkv_kvquant.cu" if kv in ("q8", "q4") else "pkv_decode.cu"
+        wl = name if kv == "bf16" else f"{name}_{kv}"
+        res["roofline"] = {"bound": "hbm", "kernel": f"attention call: {dec} + span merge (merge_small/merge_wide)",
+                           "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                           "traffic": profiled_traffic(src, wl), "algorithmic_bytes_per_launch": kvb,
+                           "mean_launch_ms": attn_mean, "peak_source": f"{peak_src} HBM copy bandwidth"}
+    elif dominant == "decode":
+        res["roofline"] = kernels["decode"]
+    else:
+        res["roofline"] = {"bound": "hbm", "kernel": "attention call", "achieved": achieved, "peak": hbm,
+                           "unit": "GB/s", "frac": achieved / hbm, "traffic": None,
+                           "algorithmic_bytes_per_launch": kvb, "mean_launch_ms": attn_mean,
+                           "peak_source": f"{peak_src} HBM copy bandwidth"}
+    if m["e2e"]:
+        e = m["e2e"]
+        e_ms, e_units = aggregate(e["ms_total"], kvb * e["steps"], world)
+        res["e2e"] = {"value": e_units / (e_ms / 1e3) / 1e9, "unit": "GB/s",
+                      "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"],
+                      "steps": e["steps"], "ms_per_step": e_ms / e["steps"],
+                      "timed": "wall clock per step: one pkv_step call (work list planned on the host, "
+                               "H2D copy of the staged inputs, cache write, attention, D2H copy of "
+                               "the output) and the stream synchronised"}
+    if cpu:
+        res["cpu_baseline"] = cpu
+    return res
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    from continuous_batching_paged_pkv_gb300 import build as libbuild
     from continuous_batching_paged_pkv_gb300 import workloads as W
 
     libbuild.build()
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     w = W.make_step(args.workload, args.seed, pool_blocks=args.pool_blocks)
-    ds = R.prepare(w, dev, kv=args.kv)
-    stream = torch.cuda.current_stream()
-    kvb = kv_bytes(w, args.kv)
     flush = L2Flush(dev)
-    launches_per_step = (int(w.total_q > 0) + int(ds.info.num_decode_items > 0) + int(ds.info.num_prefill_items > 0)
-                         + int(ds.info.num_combine_items > 0))
-
-    for _ in range(args.warmup):
-        flush()
-        R.run_step(ds)
-    torch.cuda.synchronize()
-    if B.pkv_check_device_status(ds.status) != 0:
-        raise RuntimeError("device status reported an error during warm-up")
-
-    props = torch.cuda.get_device_properties(dev)
-    uuid = str(getattr(props, "uuid", "")) or None
-    clocks = ClockSampler(("GPU-" + uuid) if uuid and not uuid.startswith("GPU-") else uuid)
-    clocks.start()
-    barrier(world)
-    torch.cuda.synchronize()
-    # Timed region: one event pair around each whole step (cache write +
-    # attention), so the step's kernels may overlap their launches.
-    step_ms = []
-    chunk = 500
-    done = 0
-    while done < args.steps:
-        n = min(chunk, args.steps - done)
-        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
-        for e0, e2 in ev:
-            flush()
-            e0.record(stream)
-            R.run_cache_write(ds)
-            R.run_attention(ds)
-            e2.record(stream)
-        torch.cuda.synchronize()
-        step_ms.extend(e0.elapsed_time(e2) for e0, e2 in ev)
-        done += n
-    torch.cuda.synchronize()
-    barrier(world)
-    clk = clocks.stop()
-    # Breakdown pass (same stream, same flush): events between the two calls
-    # give each call's own duration; the attention call is the roofline kernel.
-    write_ms, attn_ms = [], []
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(max(args.steps // 4, 20))]
-    for e0, e1, e2 in ev:
-        flush()
-        e0.record(stream)
-        R.run_cache_write(ds)
-        e1.record(stream)
-        R.run_attention(ds)
-        e2.record(stream)
-    torch.cuda.synchronize()
-    for e0, e1, e2 in ev:
-        write_ms.append(e0.elapsed_time(e1))
-        attn_ms.append(e1.elapsed_time(e2))
-    # Chunk-kernel pass: the same call with only the prompt-chunk items of the
-    # work list launches the tensor-core chunk kernel alone (same inputs and
-    # output rows), so its own duration is measured on the launching stream.
-    chunk_ms = []
-    if ds.info.num_prefill_items and args.kv == "bf16":
-        wi = R.chunk_only(ds)
-        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(max(args.steps // 4, 20))]
-        for e0, e1 in ev:
-            flush()
-            e0.record(stream)
-            R.run_chunk_only(ds, wi)
-            e1.record(stream)
-        torch.cuda.synchronize()
-        chunk_ms = [e0.elapsed_time(e1) for e0, e1 in ev]
-    if B.pkv_check_device_status(ds.status) != 0:
-        raise RuntimeError("device status reported an error during the timed steps")
-
-    total_ms, total_bytes = aggregate(sum(step_ms), kvb * args.steps, world)
-    hbm, tflops, peak_src = peaks()
-    value = total_bytes / (total_ms / 1e3) / 1e9
-    attn_mean = sum(attn_ms) / len(attn_ms)
-    achieved = kvb / (attn_mean / 1e3) / 1e9
-    res = {
-        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": f"{args.workload}: {WORKLOAD_TEXT[args.workload]}",
-                   "rows_per_step": w.total_q, "kv_bytes_per_step": kvb, "kv_format": args.kv,
-                   "l2": "flushed before every step: 256 MiB written, then 256 MiB read so L2 holds clean lines; "
-                         "both outside the timed events",
-                   "parallelism": f"replicas x{world} (no exchange between GPUs)", "seed": args.seed,
-                   "pool_blocks": w.num_blocks},
-        "pct_hbm_peak": 100.0 * value / world / hbm,
-        "rows_per_s": world * w.total_q / (total_ms / args.steps / 1e3),
-        "step_breakdown_ms": {"cache_write": statistics.median(write_ms), "attention": statistics.median(attn_ms),
-                              "step": statistics.median(step_ms)},
-    }
-    chunk_kernel = "prefill_pair_kernel" if w.head_dim == 128 else "prefill_kernel"
-    dec_kernel = "decode_quant_kernel" if args.kv in ("q8", "q4") else "decode_kernel"
-    if ds.info.num_prefill_items and args.kv == "bf16":
-        # the chunk kernel dominates the library's time on steps that carry a prompt chunk
-        bound, unit, kernel = "tensor", "TFLOP/s", chunk_kernel
-    elif ds.info.num_prefill_items:
-        bound, unit, kernel = "hbm", "GB/s", "attention call: widen_quant + chunk + decode_quant + span merge kernels"
-    elif ds.info.num_combine_items:
-        bound, unit, kernel = "hbm", "GB/s", f"attention call: {dec_kernel} + span merge (merge_small/merge_wide)"
-    else:
-        bound, unit, kernel = "hbm", "GB/s", dec_kernel
-    if bound == "tensor":
-        chunk_mean = sum(chunk_ms) / len(chunk_ms)
-        ach = chunk_flops(w) / (chunk_mean / 1e3) / 1e12
-        src = "pkv_prefill_pair.cu" if w.head_dim == 128 else "pkv_prefill.cu"
-        res["roofline"] = {"bound": "tensor", "kernel": kernel, "achieved": ach, "peak": tflops,
-                           "unit": "TFLOP/s", "frac": ach / tflops, "traffic": profiled_traffic(src, args.workload),
-                           "algorithmic_flop_per_launch": chunk_flops(w), "mean_launch_ms": chunk_mean,
-                           "peak_source": f"{peak_src} bf16 burst (the chunk kernel is timed alone)"}
-        res["attention_call"] = {"kv_gbs": achieved, "pct_hbm_peak": 100.0 * achieved / hbm, "mean_ms": attn_mean,
-                                 "kernels": "chunk + decode + span merge"}
-    else:
-        src = "pkv_kvquant.cu" if args.kv in ("q8", "q4") else "pkv_decode.cu"
-        wl = args.workload if args.kv == "bf16" else f"{args.workload}_{args.kv}"
-        traffic = profiled_traffic(src, wl) if dec_kernel in kernel else None
-        res["roofline"] = {"bound": "hbm", "kernel": kernel, "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                           "frac": achieved / hbm, "traffic": traffic,
-                           "algorithmic_bytes_per_launch": kvb, "mean_launch_ms": attn_mean,
-                           "peak_source": f"{peak_src} HBM copy bandwidth"}
-    if chunk_ms:
-        res["chunk_kernel_ms"] = statistics.median(chunk_ms)
-    res["gpu_launches"] = launches_per_step * args.steps
-    res["clocks"] = clk
-
-    # ---- end to end through the C ABI, inputs from pinned host memory ----
-    e2e = run_e2e(args, w, ds, dev, flush) if args.kv == "bf16" else None
-    if e2e:
-        e_ms, e_units = aggregate(e2e["ms_total"], kvb * e2e["steps"], world)
-        res["e2e"] = {"value": e_units / (e_ms / 1e3) / 1e9, "unit": "GB/s",
-                      "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
-                      "steps": e2e["steps"], "ms_per_step": e_ms / e2e["steps"],
-                      "timed": "wall clock per step: one pkv_step call (work list planned on the host, "
-                               "one H2D copy of the staged inputs, cache write, attention, one D2H copy of "
-                               "the output) and the stream synchronised"}
+    m = measure_step(args.workload, w, dev, kv=args.kv, steps=args.steps, warmup=args.warmup,
+                     e2e_steps=args.e2e_steps, flush=flush, world=world, clocks=True)
+    cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        res["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+        cpu = cpu_baseline(w, args.cpu_seconds)
         one = cpu_baseline(w, args.cpu_seconds / 2, threads=1)  # the same oracle on one core
-        res["cpu_baseline"]["one_core"] = {"value": one["value"], "unit": one["unit"], "sample": one["sample"]}
+        cpu["one_core"] = {"value": one["value"], "unit": one["unit"], "sample": one["sample"]}
+    line = single_line(args.workload, w, m, kv=args.kv, world=world, steps=args.steps, cpu=cpu)
+    res = {"metric": METRIC, "value": line.pop("value"), "unit": line.pop("unit"), "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": line.pop("ms_per_step"),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+           "config": {"workload": f"{args.workload}: {WORKLOAD_TEXT[args.workload]}",
+                      "rows_per_step": w.total_q, "kv_bytes_per_step": kv_bytes(w, args.kv), "kv_format": args.kv,
+                      "l2": L2_NOTE, "parallelism": f"replicas x{world} (no exchange between GPUs)",
+                      "seed": args.seed, "pool_blocks": w.num_blocks}}
+    res.update(line)
+    res["gpu_launches"] = m["launches"] * args.steps
+    res["clocks"] = m["clocks"]
     res["impl"] = "ours"
     return res
 
 
-def run_e2e(args, w, ds, dev, flush):
+def run_configs(args, rank, world, dev, flush):
+    """Every single-step workload, each with its own figures (for the churn line's ``configs``)."""
+    import torch
+
+    from continuous_batching_paged_pkv_gb300 import workloads as W
+
+    out = {}
+    steps = max(args.config_steps, 20)
+    for name in EXTRA_CONFIGS:
+        w = W.make_step(name, args.seed)
+        m = measure_step(name, w, dev, kv="bf16", steps=steps, warmup=max(args.warmup, 3),
+                         e2e_steps=min(args.e2e_steps, 100), flush=flush, world=world)
+        cpu = None
+        if rank == 0 and world == 1 and not args.no_cpu_baseline:
+            cpu = cpu_baseline(w, args.config_cpu_seconds)
+        line = single_line(name, w, m, kv="bf16", world=world, steps=steps, cpu=cpu)
+        line["workload"] = WORKLOAD_TEXT[name]
+        line["steps"] = steps
+        out[name] = line
+        del w
+        torch.cuda.empty_cache()
+    return out
+
+
+def run_e2e(w, ds, dev, flush, e2e_steps):
     """The step through the one-call host path: the inputs sit in a page-locked
     staging buffer; the timed region is ``pkv_step`` (work list planned on the
-    host, one H2D copy, cache write, attention, one D2H copy of the output),
+    host, the H2D copy, cache write, attention, the D2H copy of the output),
     called through ``binding.StepCall`` (arguments bound once, as a serving loop
     reusing its buffers would), and the stream synchronisation."""
     import torch
@@ -507,7 +634,7 @@ def run_e2e(args, w, ds, dev, flush):
     from continuous_batching_paged_pkv_gb300 import binding as B
     from continuous_batching_paged_pkv_gb300 import runtime as R
 
-    if args.e2e_steps <= 0:
+    if e2e_steps <= 0:
         return None
     low = ds.lowered
     lay = B.pkv_stage_layout_init(w.total_q, len(w.segments), w.max_slots, w.max_blocks_per_slot, w.num_q_heads,
@@ -523,7 +650,7 @@ def run_e2e(args, w, ds, dev, flush):
     step = B.StepCall(lay, stage.host, stage.device, ds.k_pool, ds.v_pool, ds.out, ds.workspace, out_host=out_host,
                       scale=w.scale, device_status=ds.status, stream=stream)
     times = []
-    for i in range(args.e2e_steps + 5):
+    for i in range(e2e_steps + 5):
         flush()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
@@ -536,9 +663,14 @@ def run_e2e(args, w, ds, dev, flush):
     return {"ms_total": sum(times), "steps": len(times), "h2d": h2d, "d2h": d2h}
 
 
+# ---------------------------------------------------------------------------
+# Our arm: the churn trace.
+# ---------------------------------------------------------------------------
+
 def run_churn(args, rank, world, local_rank):
-    """The churn trace replayed through the library: host planning per step
-    outside the events, cache write + attention inside (L2 flushed first)."""
+    """The churn trace replayed through the library: every step runs (the pool
+    state is the trace's), host planning outside the events, cache write +
+    attention inside (L2 flushed first); steps before the window are untimed."""
     import numpy as np
     import torch
 
@@ -552,6 +684,8 @@ def run_churn(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     spec = W.ChurnSpec()
+    if args.pool_blocks:
+        spec = W.ChurnSpec(num_blocks=args.pool_blocks)
     reqs = W.churn_trace(args.seed, spec)
     bs, hq, hkv, d = spec.block_size, spec.num_q_heads, spec.num_kv_heads, spec.head_dim
     mbps = -(-(spec.prompt_max + spec.output_max + 1) // bs) + 1
@@ -563,15 +697,15 @@ def run_churn(args, rank, world, local_rank):
     flush = L2Flush(dev)
     stream = torch.cuda.current_stream()
     scale = 1.0 / np.sqrt(d)
-    warm = max(args.warmup, 3)
-    timed = max(1, min(args.steps, spec.num_steps - warm))
+    first, timed = churn_window(args, spec.num_steps)
     sample_cpu = not args.no_cpu_baseline and rank == 0 and world == 1
     cpu_rows = []  # (request, length, last q row) of timed segments, for the oracle baseline
 
-    step_ms, e2e_ms, step_bytes, step_rows, prefill_steps = [], [], [], [], 0
-    launches = h2d_tot = d2h_tot = 0
+    step_ms, e2e_ms, step_bytes, step_rows = [], [], [], []
+    chunk_ms, chunk_fl, dec_ms, dec_bytes, write_ms, attn_ms = [], [], [], [], [], []
+    prefill_steps = launches = h2d_tot = d2h_tot = 0
     clocks = stage = ws = None
-    for step in range(warm + timed):
+    for step in range(first + timed):
         rows = sch.plan()
         if not rows:
             sch.commit(rows)
@@ -596,13 +730,12 @@ def run_churn(args, rank, world, local_rank):
                    block_tables=pool.block_tables())
         out = torch.empty((T, hq, d), dtype=torch.bfloat16, device=dev)
         out_host = torch.empty(out.shape, dtype=torch.bfloat16, pin_memory=True)
-        ctx = sum(int(low.context_lens[r.slot]) for r in rows)
-        nbytes = ctx * hkv * d * 4 + T * hq * d * 4
-        is_timed = step >= warm
+        ctx = [int(low.context_lens[r.slot]) for r in rows]
+        nbytes = sum(ctx) * hkv * d * 4 + T * hq * d * 4
+        is_timed = step >= first
+        is_warm = step >= first - args.warmup
         if is_timed and clocks is None:
-            props = torch.cuda.get_device_properties(dev)
-            uuid = str(getattr(props, "uuid", "")) or None
-            clocks = ClockSampler(("GPU-" + uuid) if uuid and not uuid.startswith("GPU-") else uuid)
+            clocks = ClockSampler.for_device(dev)
             clocks.start()
 
         # end to end: one pkv_step call (work list, H2D, both calls, D2H), synchronised
@@ -616,21 +749,43 @@ def run_churn(args, rank, world, local_rank):
 
         # device time of the step alone (inputs resident in the device stage), same calls again
         v = stage.device_views(lay, info)
-        flush()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        B.pkv_cache_write(v["k_new"], v["v_new"], v["slot_mapping"], k_pool, v_pool, device_status=status)
-        B.pkv_attention(v["q"], v["cu_seqlens_q"], v["seq_slot"], v["context_lens"], v["block_tables"], k_pool,
-                        v_pool, v["work"], info, out, ws, scale=scale, device_status=status)
-        e1.record(stream)
+
+        def write():
+            B.pkv_cache_write(v["k_new"], v["v_new"], v["slot_mapping"], k_pool, v_pool, device_status=status)
+
+        def attend(work=v["work"], inf=info, space=ws):
+            B.pkv_attention(v["q"], v["cu_seqlens_q"], v["seq_slot"], v["context_lens"], v["block_tables"],
+                            k_pool, v_pool, work, inf, out, space, scale=scale, device_status=status)
+
+        if is_warm:
+            (st_ms,) = timed_calls(flush, stream, [lambda: (write(), attend())], 1)
+        else:
+            write()
+            attend()
+        if is_timed:
+            # breakdown: the two calls apart, then the chunk kernel alone and the decode + merge kernels alone
+            w_ms, a_ms = timed_calls(flush, stream, [write, attend], 1)
+            cw, dw = R.split_work(v["work"], info)
+            c_ms = timed_calls(flush, stream, [lambda: attend(cw[0], cw[1], None)], 1)[0] if cw else []
+            d_ms = timed_calls(flush, stream, [lambda: attend(dw[0], dw[1], ws)], 1)[0] if dw else []
         torch.cuda.synchronize()
         if B.pkv_check_device_status(status) != 0:
             raise RuntimeError(f"device status reported an error at churn step {step}")
         if is_timed:
-            step_ms.append(e0.elapsed_time(e1))
+            step_ms.extend(st_ms)
+            write_ms.extend(w_ms)
+            attn_ms.extend(a_ms)
             e2e_ms.append(e2e)
             step_bytes.append(nbytes)
             step_rows.append(T)
+            dec_rows = [(r, c) for r, c in zip(rows, ctx) if r.n <= max(1, 16 // (hq // hkv))]
+            chk_rows = [(r, c) for r, c in zip(rows, ctx) if r.n > max(1, 16 // (hq // hkv))]
+            if c_ms:
+                chunk_ms.extend(c_ms)
+                chunk_fl.append(4 * d * hq * sum(r.n * (c - r.n + 1) + r.n * (r.n - 1) // 2 for r, c in chk_rows))
+            if d_ms:
+                dec_ms.extend(d_ms)
+                dec_bytes.append(sum(c for _, c in dec_rows) * hkv * d * 4 + sum(r.n for r, _ in dec_rows) * hq * d * 4)
             prefill_steps += int(any(r.prefill for r in rows))
             launches += 1 + int(info.num_decode_items > 0) + int(info.num_prefill_items > 0) + \
                 int(info.num_combine_items > 0)
@@ -643,60 +798,67 @@ def run_churn(args, rank, world, local_rank):
 
     n = len(step_ms)
     tot_ms, tot_bytes = aggregate(sum(step_ms), sum(step_bytes), world)
-    hbm, _, peak_src = peaks()
+    hbm, tflops, peak_src = peaks()
     value = tot_bytes / (tot_ms / 1e3) / 1e9
     e_ms, _ = aggregate(sum(e2e_ms), sum(step_bytes), world)
+    kernels = {}
+    if chunk_ms:
+        ach = sum(chunk_fl) / (sum(chunk_ms) / 1e3) / 1e12
+        kernels["chunk"] = {"bound": "tensor", "kernel": "prefill_pair_kernel", "achieved": ach, "peak": tflops,
+                            "unit": "TFLOP/s", "frac": ach / tflops, "traffic": None,
+                            "algorithmic_flop_per_launch": sum(chunk_fl) / len(chunk_fl),
+                            "mean_launch_ms": mean(chunk_ms), "launches": len(chunk_ms),
+                            "total_ms": sum(chunk_ms),
+                            "peak_source": f"{peak_src} bf16 burst (the chunk kernel is timed alone, per step)"}
+    if dec_ms:
+        ach = sum(dec_bytes) / (sum(dec_ms) / 1e3) / 1e9
+        kernels["decode"] = {"bound": "hbm", "kernel": "decode_kernel + span merge (merge_small/merge_wide)",
+                             "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
+                             "traffic": profiled_traffic("pkv_decode.cu", "churn"),
+                             "algorithmic_bytes_per_launch": sum(dec_bytes) / len(dec_bytes),
+                             "mean_launch_ms": mean(dec_ms), "launches": len(dec_ms), "total_ms": sum(dec_ms),
+                             "peak_source": f"{peak_src} HBM copy bandwidth (decode and merge kernels timed "
+                                            f"alone, per step)"}
+    dominant = max(kernels, key=lambda k: kernels[k]["total_ms"]) if kernels else None
+    roofline = dict(kernels[dominant]) if dominant else {
+        "bound": "hbm", "kernel": "whole step", "achieved": value / world, "peak": hbm, "unit": "GB/s",
+        "frac": value / world / hbm, "traffic": None}
     res = {
-        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": n, "warmup": warm,
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": n, "warmup": args.warmup,
         "ms_per_step": tot_ms / n, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
         "config": {"workload": f"churn: {WORKLOAD_TEXT['churn']}",
-                   "trace_steps": f"{warm} untimed, then {n} timed, of {spec.num_steps}",
+                   "trace_steps": f"steps 0..{first - 1} replayed untimed (the last {min(args.warmup, first)} "
+                                  f"as timed-style warm-up), steps {first}..{first + n - 1} timed, of "
+                                  f"{spec.num_steps}",
+                   "timed_offset": first,
                    "steps_with_prompt_chunks": prefill_steps, "rows_per_step_mean": sum(step_rows) / n,
+                   "kv_bytes_per_step_mean": sum(step_bytes) / n,
                    "step_ms_p50": statistics.median(step_ms), "step_ms_p90": sorted(step_ms)[int(0.9 * (n - 1))],
-                   "step_ms_max": max(step_ms),
-                   "l2": "flushed before every step (256 MiB written, then 256 MiB read), outside the events",
+                   "step_ms_max": max(step_ms), "l2": L2_NOTE,
                    "parallelism": f"replicas x{world} (no exchange between GPUs)", "seed": args.seed,
                    "pool_blocks": spec.num_blocks},
         "pct_hbm_peak": 100.0 * value / world / hbm,
         "rows_per_s": world * sum(step_rows) / (tot_ms / 1e3),
-        "roofline": {"bound": "hbm", "kernel": "whole step (cache write + attention call), summed over the trace",
-                     "achieved": value / world, "peak": hbm, "unit": "GB/s", "frac": value / world / hbm,
-                     "traffic": None, "algorithmic_bytes_per_launch": sum(step_bytes) / n,
-                     "mean_launch_ms": sum(step_ms) / n, "peak_source": f"{peak_src} HBM copy bandwidth"},
+        "step_breakdown_ms": {"cache_write": mean(write_ms), "attention": mean(attn_ms), "step": mean(step_ms),
+                              "chunk_kernel_alone": mean(chunk_ms) if chunk_ms else None,
+                              "decode_and_merge_alone": mean(dec_ms) if dec_ms else None},
+        "roofline": roofline, "kernels": kernels, "roofline_kernel": dominant,
         "gpu_launches": launches, "clocks": clk,
         "e2e": {"value": tot_bytes / (e_ms / 1e3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d_tot // n,
                 "d2h_bytes_per_step": d2h_tot // n, "steps": n, "ms_per_step": e_ms / n,
-                "timed": "wall clock per step: one pkv_step call (work list planned on the host, one H2D "
-                         "copy of the staged inputs, cache write, attention, one D2H copy of the output) and "
-                         "the stream synchronised (K/V/q generation, scheduling and staging outside)"},
+                "timed": "wall clock per step: one pkv_step call (work list planned on the host, H2D copy of "
+                         "the staged inputs, cache write, attention, D2H copy of the output) and the stream "
+                         "synchronised (K/V/q generation, scheduling and staging outside)"},
         "impl": "ours",
     }
     if cpu_rows:
         res["cpu_baseline"] = churn_oracle_rows(cpu_rows, toks, hkv, hq, d, scale, args.cpu_seconds)
+    del k_pool, v_pool, stage, ws
+    torch.cuda.empty_cache()
+    if not args.no_configs and args.kv == "bf16":
+        res["configs"] = run_configs(args, rank, world, dev, flush)
     return res
-
-
-def churn_oracle_rows(samples, toks, hkv, hq, d, scale, seconds):
-    """The oracle's dense attention on sampled churn rows (a segment's last row
-    over its whole history), spread evenly over the samples, ~`seconds` of work."""
-    import oracle
-
-    oracle.build()
-    stride = max(1, len(samples) // 400)
-    done_b, runs, el = 0, 0, 0.0
-    for rid, L, qrow in samples[::stride]:
-        k, v, _ = toks.rows(rid, 0, L)  # the history, generated outside the clock
-        t0 = time.perf_counter()
-        oracle.attention_dense(qrow, k, v, scale)
-        el += time.perf_counter() - t0
-        done_b += L * hkv * d * 4 + hq * d * 4
-        runs += 1
-        if el >= seconds:
-            break
-    return {"value": done_b / el / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"{runs} sampled rows of the timed trace steps (the last row of a segment, over its "
-                      f"whole history), fp64, one thread, {el:.1f} s of oracle time"}
 
 
 def main(argv=None):

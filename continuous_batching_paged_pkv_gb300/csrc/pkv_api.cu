@@ -235,13 +235,16 @@ pkv_status pkv_attention(const void *q, const int32_t *cu_seqlens_q, int32_t num
   SideStream *side = (info->num_prefill_items > 0 && info->num_decode_items > 0) ? side_stream() : nullptr;
   std::unique_lock<std::mutex> lock;
   if (side) lock = std::unique_lock<std::mutex>(side->mu);
+  // With decode segments of at most 8 (row, q head) columns, a CTA of each
+  // kernel fits on every SM, so both kinds of rows share all SMs.
+  const bool beside = side && head_dim == 128 && a.group * (a.decode_rows_max > 1 ? a.decode_rows_max : 1) <= 8;
   cudaError_t e = side ? cudaEventRecord(side->fork, st) : cudaSuccess;
   if (e == cudaSuccess)
-    e = head_dim == 128 ? pkv::launch_prefill_pair(a, tq, tks, tv, rpt, info->num_prefill_items, pre, st)
+    e = head_dim == 128 ? pkv::launch_prefill_pair(a, tq, tks, tv, rpt, info->num_prefill_items, pre, beside, st)
                         : pkv::launch_prefill(a, tq, rpt, info->num_prefill_items, pre, st);
   cudaStream_t dst = side ? side->stream : st;
   if (e == cudaSuccess && side) e = cudaStreamWaitEvent(side->stream, side->fork, 0);
-  if (e == cudaSuccess) e = pkv::launch_decode(a, tk, tv, info->num_decode_items, dec, dst);
+  if (e == cudaSuccess) e = pkv::launch_decode(a, tk, tv, info->num_decode_items, dec, beside, dst);
   if (e == cudaSuccess) e = pkv::launch_merge(a, info->num_combine_items, comb, dst);
   if (side) {
     // join even after a failed launch, so the caller's stream never runs ahead of queued work
@@ -420,7 +423,7 @@ static pkv_status attention_quant(int32_t bits, const void *q, const int32_t *cu
     e = pkv::launch_widen_quant(a, k_codes, k_scales, v_codes, v_scales, scratch_k, scratch_v, scratch_table,
                              static_cast<int64_t>(sb), info->num_scratch_items, scr, bits, st);
     if (e == cudaSuccess)
-      e = head_dim == 128 ? pkv::launch_prefill_pair(c, tq, tk, tv, rpt, info->num_prefill_items, pre, st)
+      e = head_dim == 128 ? pkv::launch_prefill_pair(c, tq, tk, tv, rpt, info->num_prefill_items, pre, false, st)
                           : pkv::launch_prefill(c, tq, rpt, info->num_prefill_items, pre, st);
   }
   cudaStream_t dst = side ? side->stream : st;

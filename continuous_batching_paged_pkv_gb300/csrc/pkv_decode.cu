@@ -750,11 +750,17 @@ cudaError_t launch_decode_128(const StepArgs &a, const CUtensorMap &tk, const CU
 }  // namespace
 
 cudaError_t launch_decode(const StepArgs &a, const CUtensorMap &tk, const CUtensorMap &tv, int32_t num_items,
-                          const int32_t *items, cudaStream_t stream) {
+                          const int32_t *items, bool beside_chunk, cudaStream_t stream) {
   if (num_items <= 0) return cudaSuccess;
   // one column per (row, q head) of a segment: 8 columns per tile, 16 at most
   const bool multi = a.decode_rows_max > 1;
   const bool wide = a.group * (multi ? a.decode_rows_max : 1) > 8;
+  if (beside_chunk && a.head_dim == 128 && !wide) {
+    // one 8-column tile (at most ~208 registers): small enough to share an SM with a chunk CTA
+    constexpr int W = kDecodeWarpsBesideChunk, S = kDecodeStagesBesideChunk;
+    return multi ? launch_decode_t<128, 1, true, W, S>(a, tk, tv, num_items, items, stream)
+                 : launch_decode_t<128, 1, false, W, S>(a, tk, tv, num_items, items, stream);
+  }
   const int v = (a.head_dim == 128 ? 4 : 0) + (wide ? 2 : 0) + (multi ? 1 : 0);
   switch (v) {
     case 0: return launch_decode_t<64, 1, false>(a, tk, tv, num_items, items, stream);

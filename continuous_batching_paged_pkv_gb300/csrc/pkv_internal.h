@@ -55,8 +55,10 @@ cudaError_t launch_copy_blocks(const int32_t *pairs, int64_t num_pairs, void *co
                                const int64_t *block_bytes, int32_t num_arrays, int64_t num_blocks, uint32_t *status,
                                cudaStream_t stream);
 
+// `beside_chunk`: the chunk kernel of the same step runs at the same time
+// (head_dim 128 takes the small per-SM footprint described below).
 cudaError_t launch_decode(const StepArgs &a, const CUtensorMap &tmap_k, const CUtensorMap &tmap_v,
-                          int32_t num_items, const int32_t *items, cudaStream_t stream);
+                          int32_t num_items, const int32_t *items, bool beside_chunk, cudaStream_t stream);
 
 // One CTA per (row of a multi-span segment, group of q heads): merges that row's span partials.
 cudaError_t launch_merge(const StepArgs &a, int32_t num_items, const int32_t *items, cudaStream_t stream);
@@ -79,9 +81,24 @@ cudaError_t launch_widen_quant(const StepArgs &a, const void *k_codes, const voi
 cudaError_t launch_prefill(const StepArgs &a, const CUtensorMap &tmap_q, int32_t rows_per_tile,
                            int32_t num_items, const int32_t *items, cudaStream_t stream);
 // head_dim 128: items are tile pairs, run by clusters of two CTAs.
+// `beside_decode`: the step also has decode rows, whose kernel runs at the
+// same time; the chunk kernel then keeps fewer K/V stages so that a decode CTA
+// fits beside each of its CTAs.
 cudaError_t launch_prefill_pair(const StepArgs &a, const CUtensorMap &tmap_q, const CUtensorMap &tmap_k,
                                 const CUtensorMap &tmap_v, int32_t rows_per_tile, int32_t num_items,
-                                const int32_t *items, cudaStream_t stream);
+                                const int32_t *items, bool beside_decode, cudaStream_t stream);
+
+// A step with both prompt chunks and decode rows (head_dim 128) runs one CTA
+// of each kernel on every SM: the chunk kernel with kPairStagesBesideDecode
+// K/V stages (129 KiB of shared memory, 7 warps x 232 registers), the decode
+// kernel with kDecodeWarpsBesideChunk warps of kDecodeStagesBesideChunk
+// stages (81 KiB, 2 warps x at most 208 registers); together they stay within
+// an SM's 228 KiB of shared memory and 64 Ki registers. The tensor-bound chunk
+// tiles and the HBM-bound decode streams then share every SM instead of
+// queueing for SMs.
+constexpr int kPairStagesBesideDecode = 3;
+constexpr int kDecodeWarpsBesideChunk = 4;
+constexpr int kDecodeStagesBesideChunk = 2;
 
 // Launch with programmatic stream serialization: the kernel may start while
 // the previous kernel in the stream drains; it calls griddepcontrol.wait
@@ -102,9 +119,13 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
-// Raises a kernel's dynamic shared-memory limit to `smem`, once per device.
-// `done` holds one bit per device (devices past 63 set the attribute on every
-// call); two host threads racing on a first call both set it, which is harmless.
+// Raises a kernel's dynamic shared-memory limit to `smem`, once per device,
+// and asks for the largest shared-memory carve-out of the SM's L1 storage: a
+// CTA of another kernel can join an SM only under the carve-out that SM was
+// configured with, so the kernels meant to share SMs (a chunk CTA beside a
+// decode CTA) must all ask for the same, largest one.
+// `done` holds one bit per device (devices past 63 set the attributes on every
+// call); two host threads racing on a first call both set them, which is harmless.
 template <typename Kernel>
 cudaError_t allow_smem_once(Kernel *kernel, int smem, std::atomic<uint64_t> &done) {
   int dev = 0;
@@ -113,6 +134,8 @@ cudaError_t allow_smem_once(Kernel *kernel, int smem, std::atomic<uint64_t> &don
   const uint64_t bit = dev >= 0 && dev < 64 ? 1ull << dev : 0;
   if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
   if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
   return e;
 }

@@ -57,16 +57,29 @@ namespace {
 constexpr int D = 128;
 constexpr int kKeysPerTile = 128;
 constexpr int kSubPerTile = kKeysPerTile / kSubKeys;  // 8 sub-tiles of 16 keys
-constexpr int kStages = 6;  // K/V tiles in flight: the producer runs well ahead of the MMAs
 constexpr int kTmemCols = 512;
 constexpr int kSBufs = 3;      // S/P buffers in TMEM
 constexpr int kOCol = 384;
-constexpr int kThreads = 224;  // producer, QK issuer, 4 softmax warps, PV issuer
+// Warps 0-3 (one warpgroup): softmax, one per TMEM lane quarter. Warps 4-7:
+// TMA producer, QK issuer, PV issuer, and one idle warp that completes the
+// warpgroup. The kernel launches with kLaunchRegs registers per thread; the
+// softmax warpgroup then raises its share to kSoftmaxRegs and the other
+// warpgroup lowers its own to kOtherRegs (the sum is unchanged), so each SM
+// sub-partition holds one softmax warp and one other warp in 9,728 registers
+// and keeps room for a decode warp of the same step beside them.
+constexpr int kThreads = 256;
+constexpr int kWarpProducer = 4, kWarpQK = 5, kWarpPV = 6;
+constexpr int kLaunchRegs = 152, kSoftmaxRegs = 216, kOtherRegs = 88;
+static_assert(kSoftmaxRegs + kOtherRegs == 2 * kLaunchRegs, "register shares must add up to the launch's");
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when the max grows by > 256x
 constexpr uint32_t kFull = 0xffffffffu;
 constexpr uint32_t kNegInfBits = 0xff800000u;
 
+// NST K/V tiles in flight: six when the chunk kernel has its SMs to itself (the
+// producer runs well ahead of the MMAs), three when a decode CTA shares each SM.
+template <int NST>
 struct Layout {
+  static constexpr int kStages = NST;
   static constexpr int kQHalf = 128 * 128;                 // 128 rows x 128 B: one 64-column half of D
   static constexpr int kQBytes = 2 * kQHalf;
   static constexpr int kKSub = kSubKeys * 256;              // one 16-key sub-tile of K: [2 groups][2 halves][8 keys][128 B]
@@ -76,20 +89,22 @@ struct Layout {
   static constexpr int kBarOffset = kQBytes + kStages * kStageBytes;
   static constexpr int kSmem = kBarOffset + 256 + 1024;    // barriers/flags + alignment slack
 };
-static_assert(Layout::kSmem <= 232448, "dynamic shared memory per CTA");
+static_assert(Layout<6>::kSmem <= 232448, "dynamic shared memory per CTA");
 
-enum Bar : int {
-  kQFull = 0,                     // even CTA: both Q tiles
-  kKVFull = 1,                    // +stage; even CTA: both CTAs' halves of a K/V tile
-  kKVEmpty = kKVFull + kStages,   // +stage; both CTAs
-  kSFull = kKVEmpty + kStages,    // +buffer (3); both CTAs
-  kPReady = kSFull + kSBufs,      // +buffer (3); even CTA: one arrival per softmax warp of the pair
-  kPVDone = kPReady + kSBufs,     // +buffer (3); both CTAs
-  kDrain = kPVDone + kSBufs,      // QK issuer's MMAs complete
-  kDrainPV = kDrain + 1,          // PV issuer's MMAs complete
-  kNumBars = kDrainPV + 1
+// Barrier indices for NST stages.
+template <int NST>
+struct Bars {
+  static constexpr int kQFull = 0;                     // even CTA: both Q tiles
+  static constexpr int kKVFull = 1;                    // +stage; even CTA: both CTAs' halves of a K/V tile
+  static constexpr int kKVEmpty = kKVFull + NST;       // +stage; both CTAs
+  static constexpr int kSFull = kKVEmpty + NST;        // +buffer (3); both CTAs
+  static constexpr int kPReady = kSFull + kSBufs;      // +buffer (3); even CTA: one arrival per softmax warp of the pair
+  static constexpr int kPVDone = kPReady + kSBufs;     // +buffer (3); both CTAs
+  static constexpr int kDrain = kPVDone + kSBufs;      // QK issuer's MMAs complete
+  static constexpr int kDrainPV = kDrain + 1;          // PV issuer's MMAs complete
+  static constexpr int kNumBars = kDrainPV + 1;
+  static_assert(kNumBars * 8 + 8 <= 256, "barriers, TMEM address and abort flag fit their 256 bytes");
 };
-static_assert(kNumBars * 8 + 8 <= 256, "barriers, TMEM address and abort flag fit their 256 bytes");
 
 __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
   return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
@@ -120,13 +135,18 @@ __device__ __forceinline__ bool warp_wait_or_abort(uint64_t *bar, uint32_t parit
   return __all_sync(kFull, wait_or_abort(bar, parity, abort));
 }
 
-__global__ void __launch_bounds__(kThreads, 1) prefill_pair_kernel(const __grid_constant__ CUtensorMap tmap_q,
+template <int NST>
+__global__ void __maxnreg__(kLaunchRegs) prefill_pair_kernel(const __grid_constant__ CUtensorMap tmap_q,
                                                                    const __grid_constant__ CUtensorMap tmap_k,
                                                                    const __grid_constant__ CUtensorMap tmap_v,
                                                                    const StepArgs a,
                                                                    const int32_t *__restrict__ items,
                                                                    int rows_per_tile) {
-  using Lay = Layout;
+  using Lay = Layout<NST>;
+  constexpr int kStages = NST;
+  constexpr int kQFull = Bars<NST>::kQFull, kKVFull = Bars<NST>::kKVFull, kKVEmpty = Bars<NST>::kKVEmpty;
+  constexpr int kSFull = Bars<NST>::kSFull, kPReady = Bars<NST>::kPReady, kPVDone = Bars<NST>::kPVDone;
+  constexpr int kDrain = Bars<NST>::kDrain, kDrainPV = Bars<NST>::kDrainPV, kNumBars = Bars<NST>::kNumBars;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = align1024(smem_raw);
   uint8_t *sQ = smem;
@@ -190,7 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_pair_kernel(const __grid_
     }
     fence_proxy_async_smem();
   }
-  if (warp == 1) {
+  if (warp == kWarpQK) {
     tmem_alloc_pair(tmem_slot, kTmemCols);
     tmem_relinquish_pair();
   }
@@ -199,7 +219,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_pair_kernel(const __grid_
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
+  if (warp >= 4) {
+   setmaxnreg_dec<kOtherRegs>();
+   if (warp == kWarpProducer) {
     // ------------------------------------------------------------ producer
     // Pool rows of the 16-key sub-tiles, four tiles per warp-wide load: lane l
     // covers sub-tile l % 8 of tile t0 + l / 8. The block IDs of the next group
@@ -261,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_pair_kernel(const __grid_
       if (is_v && u < vs)
         tma_load_2d_pair(sKV + s * Lay::kStageBytes + dst_off, &tmap_v, static_cast<int>(rank) * 64, urow, kv_full);
     }
-  } else if (warp == 1) {
+  } else if (warp == kWarpQK) {
     // ------------------------------------------------------------ QK issuer
     if (rank == 0 && lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(256, kKeysPerTile, 0, 0);
@@ -288,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_pair_kernel(const __grid_
       if (!wait_or_abort(bar + kDrain, 0, abort_flag) && a.status) atomicOr(a.status, PKV_DEV_TIMEOUT);
     }
     __syncwarp();
-  } else if (warp == 6) {
+  } else if (warp == kWarpPV) {
     // ------------------------------------------------------------ PV issuer
     if (rank == 0 && lane == 0) {
       constexpr uint32_t idesc_pv = idesc_bf16_f32(256, D, 0, 1);
@@ -311,9 +333,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_pair_kernel(const __grid_
       if (!wait_or_abort(bar + kDrainPV, 0, abort_flag) && a.status) atomicOr(a.status, PKV_DEV_TIMEOUT);
     }
     __syncwarp();
+   }
   } else {
     // ------------------------------------------------------------ softmax
-    const int qw = warp & 3;
+    setmaxnreg_inc<kSoftmaxRegs>();
+    const int qw = warp;
     const int mrow = qw * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(qw * 32) << 16;
     const int pos = mrow / G, hh = mrow % G;
@@ -392,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_pair_kernel(const __grid_
         const int tail = (kSubKeys - valid % kSubKeys) % kSubKeys;
         if (tail) {
           uint8_t *sV = sKV + (j % kStages) * Lay::kStageBytes + Lay::kKBytes;
-          for (int i = threadIdx.x - 64; i < tail * 8; i += 128)
+          for (int i = threadIdx.x; i < tail * 8; i += 128)
             *reinterpret_cast<uint4 *>(sV + (valid + i / 8) * 128 + (i % 8) * 16) = make_uint4(0, 0, 0, 0);
           fence_proxy_async_smem();
         }
@@ -434,21 +458,18 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_pair_kernel(const __grid_
   tc_fence_before();
   cluster_sync();  // both CTAs are done with TMEM and the MMAs have drained
   if (*abort_flag && threadIdx.x == 0 && a.status) atomicOr(a.status, PKV_DEV_TIMEOUT);
-  if (warp == 1) {
+  if (warp == kWarpQK) {
     tc_fence_after();
     tmem_dealloc_pair(tmem, kTmemCols);
   }
 }
 
-}  // namespace
-
-cudaError_t launch_prefill_pair(const StepArgs &a, const CUtensorMap &tq, const CUtensorMap &tk,
-                                const CUtensorMap &tv, int32_t rows_per_tile, int32_t num_items,
-                                const int32_t *items, cudaStream_t stream) {
-  if (num_items <= 0) return cudaSuccess;
-  constexpr int smem = Layout::kSmem;
+template <int NST>
+cudaError_t launch_pair_t(const StepArgs &a, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                          int32_t rows_per_tile, int32_t num_items, const int32_t *items, cudaStream_t stream) {
+  constexpr int smem = Layout<NST>::kSmem;
   static std::atomic<uint64_t> configured{0};  // one bit per device
-  if (const cudaError_t e = allow_smem_once(prefill_pair_kernel, smem, configured); e != cudaSuccess) return e;
+  if (const cudaError_t e = allow_smem_once(prefill_pair_kernel<NST>, smem, configured); e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(2 * num_items), static_cast<unsigned>(a.num_kv_heads));
   cfg.blockDim = dim3(kThreads);
@@ -463,7 +484,17 @@ cudaError_t launch_prefill_pair(const StepArgs &a, const CUtensorMap &tq, const 
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, prefill_pair_kernel, tq, tk, tv, a, items, rows_per_tile);
+  return cudaLaunchKernelEx(&cfg, prefill_pair_kernel<NST>, tq, tk, tv, a, items, rows_per_tile);
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_pair(const StepArgs &a, const CUtensorMap &tq, const CUtensorMap &tk,
+                                const CUtensorMap &tv, int32_t rows_per_tile, int32_t num_items,
+                                const int32_t *items, bool beside_decode, cudaStream_t stream) {
+  if (num_items <= 0) return cudaSuccess;
+  return beside_decode ? launch_pair_t<kPairStagesBesideDecode>(a, tq, tk, tv, rows_per_tile, num_items, items, stream)
+                       : launch_pair_t<6>(a, tq, tk, tv, rows_per_tile, num_items, items, stream);
 }
 
 }  // namespace pkv

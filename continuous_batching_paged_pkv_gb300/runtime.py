@@ -179,20 +179,55 @@ def run_attention(ds: DeviceStep, stream=None) -> None:
                         device_status=ds.status, stream=stream)
 
 
+def split_work(work, info):
+    """Two (work, info) pairs from one bf16 step's work list: the prompt-chunk
+    items alone (an attention call with them launches the chunk kernel alone),
+    and the decode items with their merge items (the decode and merge kernels
+    alone). Either is None when the step has no such items. Both compute the
+    same output rows as the whole list does for those segments."""
+    words = B.PKV_WORK_WORDS_PER_ITEM
+    nd, npf, nc = info.num_decode_items, info.num_prefill_items, info.num_combine_items
+    chunk = dec = None
+    if npf:
+        ci = B.WorkInfo()
+        ci.num_prefill_items = npf
+        ci.work_words = npf * words
+        chunk = (work[nd * words:(nd + npf) * words].contiguous(), ci)
+    if nd:
+        import torch
+
+        di = B.WorkInfo()
+        di.num_decode_items, di.num_combine_items = nd, nc
+        di.num_partials, di.decode_rows_max = info.num_partials, info.decode_rows_max
+        di.workspace_bytes = info.workspace_bytes
+        di.work_words = (nd + nc) * words
+        parts = [work[:nd * words], work[(nd + npf) * words:(nd + npf + nc) * words]]
+        dec = (torch.cat(parts).contiguous(), di)
+    return chunk, dec
+
+
 def chunk_only(ds: DeviceStep):
     """(work, info) holding only the step's prompt-chunk items: an attention call
     with them launches the chunk kernel alone, on the same inputs and outputs."""
-    info = B.WorkInfo()
-    info.num_prefill_items = ds.info.num_prefill_items
-    info.work_words = ds.info.num_prefill_items * B.PKV_WORK_WORDS_PER_ITEM
-    off = ds.info.num_decode_items * B.PKV_WORK_WORDS_PER_ITEM
-    return ds.work[off: off + info.work_words].contiguous(), info
+    return split_work(ds.work, ds.info)[0]
+
+
+def decode_only(ds: DeviceStep):
+    """(work, info) holding only the step's decode and merge items."""
+    return split_work(ds.work, ds.info)[1]
 
 
 def run_chunk_only(ds: DeviceStep, work_info, stream=None) -> None:
     work, info = work_info
     B.pkv_attention(ds.q, ds.cu_seqlens_q, ds.seq_slot, ds.context_lens, ds.block_tables, ds.k_pool,
                     ds.v_pool, work, info, ds.out, None, scale=ds.scale, device_status=ds.status, stream=stream)
+
+
+def run_decode_only(ds: DeviceStep, work_info, stream=None) -> None:
+    work, info = work_info
+    B.pkv_attention(ds.q, ds.cu_seqlens_q, ds.seq_slot, ds.context_lens, ds.block_tables, ds.k_pool,
+                    ds.v_pool, work, info, ds.out, ds.workspace, scale=ds.scale, device_status=ds.status,
+                    stream=stream)
 
 
 def run_step(ds: DeviceStep, stream=None) -> None:

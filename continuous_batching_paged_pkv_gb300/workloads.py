@@ -239,6 +239,36 @@ def decode256(seed: int = 0, threads=None, pool_blocks: int = 131072) -> StepInp
                    np.asarray(free, dtype=np.int32), threads)
 
 
+def chunk2048(seed: int = 0, threads=None, pool_blocks: int = 65536) -> StepInputs:
+    """A prompt chunk of the size taken while nothing decodes: 32 q / 8 kv heads, head_dim 128.
+
+    Slot 0 runs the final chunk [6144, 8192) of an 8,192-token prompt (2,048
+    rows, each seeing 6,145 to 8,192 keys); its admission reserved
+    ceil(8193 / 16) = 513 blocks, off a shuffled free list of the pool.
+    """
+    (rt,) = _rngs(seed, 1, 0)
+    free = [int(b) for b in rt.permutation(pool_blocks)]
+    segs = [Segment(0, 2048, 8192)]
+    blocks = {0: _take(free, 513)}
+    return _finish("chunk2048", seed, 32, 8, 128, 16, pool_blocks, 1, 520, segs, blocks,
+                   np.asarray(free, dtype=np.int32), threads, notes={"prompt_len": 8192, "chunk": (6144, 8192)})
+
+
+def verify(n: int, seed: int = 0, threads=None, pool_blocks: int = 131072) -> StepInputs:
+    """Speculative verification step: 64 slots each check ``n`` draft rows (causal), 32 q / 8 kv heads.
+
+    Contexts after the step are uniform in [1024, 8192]; the n rows of a slot
+    sit at its last n positions. Block tables come off a shuffled free list.
+    """
+    rt, rl = _rngs(seed, 2, 10, n)
+    free = [int(b) for b in rt.permutation(pool_blocks)]
+    ctx = rl.integers(1024, 8193, size=64)
+    segs = [Segment(i, n, int(c)) for i, c in enumerate(ctx)]
+    blocks = {s.slot: _take(free, -(-s.ctx // 16)) for s in segs}
+    return _finish(f"verify{n}", seed, 32, 8, 128, 16, pool_blocks, 64, 512, segs, blocks,
+                   np.asarray(free, dtype=np.int32), threads)
+
+
 def random_step(seed: int, shapes: list[tuple[int, int]], *, num_q_heads=4, num_kv_heads=2,
                 head_dim=64, block_size=16, num_blocks=None, max_slots=None,
                 slots: list[int] | None = None, threads=None) -> StepInputs:
@@ -261,7 +291,9 @@ def random_step(seed: int, shapes: list[tuple[int, int]], *, num_q_heads=4, num_
                    np.asarray(free, dtype=np.int32), threads)
 
 
-WORKLOADS = {"tiny": tiny, "decode5": decode5, "mixed": mixed, "decode256": decode256}
+WORKLOADS = {"tiny": tiny, "decode5": decode5, "mixed": mixed, "decode256": decode256, "chunk2048": chunk2048,
+             "verify4": lambda seed=0, **kw: verify(4, seed, **kw), "verify8": lambda seed=0, **kw: verify(8, seed, **kw),
+             "verify16": lambda seed=0, **kw: verify(16, seed, **kw)}
 
 
 def make_step(name: str, seed: int = 0, threads=None, pool_blocks: int | None = None) -> StepInputs:

@@ -93,6 +93,19 @@ def test_large_decode_batch():
     run_and_check(W.decode256(0), full_pool=False)
 
 
+def test_full_2048_row_chunk_at_offset_6144():
+    """The chunk size taken while nothing decodes, every element against the oracle:
+    2048 rows [6144, 8192) of an 8192-token prompt, 32 q / 8 kv heads, head_dim 128."""
+    run_and_check(W.chunk2048(0), full_pool=False)
+
+
+def test_full_2048_row_chunk_beside_decode_rows():
+    """A 2048-row chunk at offset 4096 packed with decode rows and a short verify run."""
+    w = W.random_step(2048, [(2048, 6144), (1, 3000), (3, 700), (1, 17)], num_q_heads=32, num_kv_heads=8,
+                      head_dim=128)
+    run_and_check(w, full_pool=False)
+
+
 EDGE_SHAPES = {
     "single key and tiny contexts": [(1, 1), (1, 2), (1, 15), (1, 16), (1, 17)],
     "span boundaries": [(1, 511), (1, 512), (1, 513), (1, 1024), (1, 1025), (1, 1536)],
