@@ -114,6 +114,8 @@ EDGE_SHAPES = {
     # short causal runs (verify rows); at small groups they take the decode path,
     # and a run across a span boundary leaves its first rows with an empty last span
     "verify runs": [(2, 257), (3, 258), (4, 257), (4, 513), (8, 520), (16, 777), (5, 5), (2, 2)],
+    # runs of several row groups (ragged last group, across span boundaries), and one just past the limit
+    "long verify runs": [(12, 600), (16, 1000), (9, 257), (7, 513), (20, 700), (33, 800), (64, 300), (13, 13)],
 }
 
 

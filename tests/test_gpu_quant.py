@@ -86,6 +86,7 @@ def test_tiny_step_q8():
 SHAPES = {
     "decode rows across spans": [(1, 1), (1, 17), (1, 257), (1, 511), (1, 1025), (1, 3000)],
     "verify runs": [(2, 257), (3, 258), (4, 513), (2, 2), (8, 520)],
+    "long verify runs": [(12, 600), (16, 1000), (9, 257), (13, 13)],
     "prompt chunks": [(33, 100), (129, 300), (7, 7), (200, 200)],
     "mixed": [(40, 333), (1, 700), (1, 64), (9, 9), (2, 300)],
 }
