@@ -559,8 +559,11 @@ def single_line(name, w, m, *, kv, world, steps, cpu=None):
                       "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"],
                       "steps": e["steps"], "ms_per_step": e_ms / e["steps"],
                       "timed": "wall clock per step: one pkv_step call (work list planned on the host, "
-                               "H2D copy of the staged inputs, cache write, attention, D2H copy of "
-                               "the output) and the stream synchronised"}
+                               + ("the staged inputs read by the kernels in place from pinned host memory, cache "
+                                  "write, attention, the output written straight to pinned host memory"
+                                  if e["in_place"] else
+                                  "H2D copy of the staged inputs, cache write, attention, D2H copy of the output")
+                               + ") and the stream synchronised"}
     if cpu:
         res["cpu_baseline"] = cpu
     return res
@@ -648,19 +651,20 @@ def run_e2e(w, ds, dev, flush, e2e_steps):
     d2h = out_host.numel() * 2
     stream = torch.cuda.current_stream()
     step = B.StepCall(lay, stage.host, stage.device, ds.k_pool, ds.v_pool, ds.out, ds.workspace, out_host=out_host,
-                      scale=w.scale, device_status=ds.status, stream=stream)
+                      scale=w.scale, device_status=ds.status, stream=stream, in_place=True)
     times = []
     for i in range(e2e_steps + 5):
         flush()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        step()
+        info = step()
         stream.synchronize()
         if i >= 5:
             times.append((time.perf_counter() - t0) * 1e3)
     if B.pkv_check_device_status(ds.status) != 0:
         raise RuntimeError("device status reported an error in the end-to-end steps")
-    return {"ms_total": sum(times), "steps": len(times), "h2d": h2d, "d2h": d2h}
+    in_place = info.num_prefill_items == 0 and h2d <= B.PKV_STEP_IN_PLACE_MAX_BYTES
+    return {"ms_total": sum(times), "steps": len(times), "h2d": h2d, "d2h": d2h, "in_place": in_place}
 
 
 # ---------------------------------------------------------------------------

@@ -32,6 +32,8 @@ PKV_ERR_NO_BLOCKS = 7
 PKV_SPLIT_KEYS = 256
 PKV_NO_ALLOC_SCRATCH_BYTES = 32 << 20
 PKV_WORK_WORDS_PER_ITEM = 4
+PKV_STEP_IN_PLACE = 1
+PKV_STEP_IN_PLACE_MAX_BYTES = 1 << 20
 
 
 class PkvError(RuntimeError):
@@ -112,7 +114,7 @@ def _lib():
                                   ctypes.POINTER(WorkInfo), p, p, u64, p, p], ctypes.c_int),
             "pkv_stage_layout_init": ([ctypes.POINTER(StageLayout), i64, i32, i32, i32, i32, i32, i32], ctypes.c_int),
             "pkv_step": ([ctypes.POINTER(StageLayout), p, u64, p, u64, p, p, i64, i32, f32, p, u64, p, p, p, p,
-                          ctypes.POINTER(WorkInfo)], ctypes.c_int),
+                          ctypes.POINTER(WorkInfo), ctypes.c_uint32], ctypes.c_int),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -446,9 +448,11 @@ def _buf(b):
 
 
 def pkv_step(layout: StageLayout, host_stage, device_stage, k_pool, v_pool, out, workspace=None, *,
-             out_host=None, scale: float = 0.0, device_status=None, stream=None) -> WorkInfo:
+             out_host=None, scale: float = 0.0, device_status=None, stream=None, in_place: bool = False) -> WorkInfo:
     """One step from the host staging buffer (see ``include/pkv.h``). Returns the step's work info.
 
+    ``in_place`` passes PKV_STEP_IN_PLACE: a small step without prompt chunks is then read
+    from ``host_stage`` and written to ``out_host`` in place, without the two copies.
     On an error the raised PkvError carries ``info`` (filled where the library got that far).
     """
     _need(out, "torch.bfloat16", "out")
@@ -461,7 +465,7 @@ def pkv_step(layout: StageLayout, host_stage, device_stage, k_pool, v_pool, out,
     info = WorkInfo()
     rc = _lib().pkv_step(ctypes.byref(layout), hp, hn, dp, dn, _t_ptr(k_pool), _t_ptr(v_pool), nb, bs, float(scale),
                          wp, wn, _t_ptr(out), _buf(out_host)[0], _t_ptr(device_status), _stream(stream),
-                         ctypes.byref(info))
+                         ctypes.byref(info), PKV_STEP_IN_PLACE if in_place else 0)
     if rc != PKV_OK:
         err = PkvError(rc, "pkv_step")
         err.info = info
@@ -479,7 +483,7 @@ class StepCall:
     """
 
     def __init__(self, layout: StageLayout, host_stage, device_stage, k_pool, v_pool, out, workspace=None, *,
-                 out_host=None, scale: float = 0.0, device_status=None, stream=None):
+                 out_host=None, scale: float = 0.0, device_status=None, stream=None, in_place: bool = False):
         _need(out, "torch.bfloat16", "out")
         _need(k_pool, "torch.bfloat16", "k_pool")
         _need(v_pool, "torch.bfloat16", "v_pool")
@@ -492,7 +496,7 @@ class StepCall:
         self._fn = _lib().pkv_step
         self._args = (ctypes.byref(layout), hp, hn, dp, dn, _t_ptr(k_pool), _t_ptr(v_pool), nb, bs, float(scale),
                       wp, wn, _t_ptr(out), _buf(out_host)[0], _t_ptr(device_status), _stream(stream),
-                      ctypes.byref(self.info))
+                      ctypes.byref(self.info), PKV_STEP_IN_PLACE if in_place else 0)
 
     def __call__(self) -> WorkInfo:
         rc = self._fn(*self._args)

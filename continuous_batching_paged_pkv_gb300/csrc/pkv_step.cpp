@@ -1,6 +1,8 @@
 // Host-staged step: the step's inputs travel to the device as one copy from a
 // single host staging buffer, the work list is planned straight into that
-// buffer, and the output comes back as one copy. Everything is enqueued on the
+// buffer, and the output comes back as one copy (or, for small steps without
+// prompt chunks on request, the kernels read the staging buffer in place and
+// write the output straight to host memory). Everything is enqueued on the
 // caller's stream; nothing here synchronises.
 #include <cuda_runtime.h>
 
@@ -14,6 +16,17 @@ namespace {
 constexpr uint64_t kAlign = 256;
 
 uint64_t align_up(uint64_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
+
+// Device address of host memory the device can reach (page-locked under unified
+// addressing), or nullptr.
+void *device_view(void *host) {
+  cudaPointerAttributes at{};
+  if (cudaPointerGetAttributes(&at, host) != cudaSuccess) {
+    cudaGetLastError();  // clear the error of an unknown pointer
+    return nullptr;
+  }
+  return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
+}
 
 }  // namespace
 
@@ -60,7 +73,7 @@ pkv_status pkv_step(const pkv_stage_layout *layout, void *host_stage, uint64_t h
                     void *device_stage, uint64_t device_stage_bytes, void *k_pool, void *v_pool,
                     int64_t num_blocks, int32_t block_size, float scale, void *workspace,
                     uint64_t workspace_bytes, void *out, void *out_host, uint32_t *device_status,
-                    pkv_stream_t stream, pkv_work_info *info_out) {
+                    pkv_stream_t stream, pkv_work_info *info_out, uint32_t options) {
   if (!layout || !host_stage || !device_stage || host_stage_bytes < layout->work ||
       (reinterpret_cast<uintptr_t>(device_stage) & (kAlign - 1)) != 0)
     return PKV_ERR_INVALID_ARG;
@@ -83,11 +96,25 @@ pkv_status pkv_step(const pkv_stage_layout *layout, void *host_stage, uint64_t h
   if (bytes > device_stage_bytes || info.workspace_bytes > workspace_bytes) return PKV_ERR_WORKSPACE_TOO_SMALL;
   if (L.total_q > 0 && !out) return PKV_ERR_INVALID_ARG;
 
-  // 2. one copy in
+  // 2. one copy in, or (small steps without prompt chunks, on request) the
+  //    staged inputs read in place and the output written straight to out_host
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  if (cudaMemcpyAsync(device_stage, host_stage, bytes, cudaMemcpyHostToDevice, cs) != cudaSuccess)
-    return PKV_ERR_CUDA;
-  uint8_t *d = static_cast<uint8_t *>(device_stage);
+  uint8_t *d = nullptr;
+  void *out_dev = out;
+  if ((options & PKV_STEP_IN_PLACE) && info.num_prefill_items == 0 && bytes <= PKV_STEP_IN_PLACE_MAX_BYTES) {
+    void *hv = device_view(host_stage);
+    void *outv = out_host ? device_view(out_host) : out;
+    if (hv && outv) {
+      d = static_cast<uint8_t *>(hv);
+      out_dev = outv;
+    }
+  }
+  const bool in_place = d != nullptr;
+  if (!in_place) {
+    if (cudaMemcpyAsync(device_stage, host_stage, bytes, cudaMemcpyHostToDevice, cs) != cudaSuccess)
+      return PKV_ERR_CUDA;
+    d = static_cast<uint8_t *>(device_stage);
+  }
 
   // 3-4. the cache write, then attention, from the staged copies
   st = pkv_cache_write(d + L.k_new, d + L.v_new, reinterpret_cast<const int64_t *>(d + L.slot_mapping), L.total_q,
@@ -98,12 +125,12 @@ pkv_status pkv_step(const pkv_stage_layout *layout, void *host_stage, uint64_t h
                      reinterpret_cast<const int32_t *>(d + L.context_lens),
                      reinterpret_cast<const int32_t *>(d + L.block_tables), L.max_slots, L.max_blocks_per_slot,
                      block_size, k_pool, v_pool, num_blocks, L.num_q_heads, L.num_kv_heads, L.head_dim, scale,
-                     reinterpret_cast<const int32_t *>(d + L.work), &info, out, workspace, workspace_bytes,
+                     reinterpret_cast<const int32_t *>(d + L.work), &info, out_dev, workspace, workspace_bytes,
                      device_status, stream);
   if (st != PKV_OK) return st;
 
-  // 5. one copy out
-  if (out_host && L.total_q > 0) {
+  // 5. one copy out (none when the output went straight to out_host)
+  if (out_host && L.total_q > 0 && !in_place) {
     const uint64_t out_bytes = static_cast<uint64_t>(L.total_q) * L.num_q_heads * L.head_dim * 2;
     if (cudaMemcpyAsync(out_host, out, out_bytes, cudaMemcpyDeviceToHost, cs) != cudaSuccess) return PKV_ERR_CUDA;
   }

@@ -552,12 +552,27 @@ pkv_status pkv_stage_layout_init(pkv_stage_layout *layout, int64_t total_q, int3
  * cu_seqlens_q must end at layout->total_q. Any error from steps 1-2 returns
  * before anything is enqueued; an error from steps 3-5 is returned as
  * soon as it happens, with the earlier steps already enqueued.
+ *
+ * `options` (bit flags, 0 for none):
+ *   PKV_STEP_IN_PLACE — a step without prompt chunks whose staged bytes
+ *   (inputs and work list) are at most PKV_STEP_IN_PLACE_MAX_BYTES skips both
+ *   copies when the device can address host_stage and out_host (page-locked
+ *   memory under unified addressing, as cudaPointerGetAttributes reports it):
+ *   the kernels read the staged inputs from host_stage in place and the
+ *   output rows are written straight into out_host (into `out` when out_host
+ *   is NULL). Such a step leaves device_stage, and `out` when out_host is
+ *   given, untouched. For small steps each copy costs more in
+ *   latency than its bytes; reading in place over the host link costs a few
+ *   dependent accesses instead. Any other step, or when the device cannot
+ *   address the buffers, runs the copies as above.
  */
+#define PKV_STEP_IN_PLACE 1u
+#define PKV_STEP_IN_PLACE_MAX_BYTES (1u << 20)
 pkv_status pkv_step(const pkv_stage_layout *layout, void *host_stage, uint64_t host_stage_bytes,
                     void *device_stage, uint64_t device_stage_bytes, void *k_pool, void *v_pool,
                     int64_t num_blocks, int32_t block_size, float scale, void *workspace,
                     uint64_t workspace_bytes, void *out, void *out_host, uint32_t *device_status,
-                    pkv_stream_t stream, pkv_work_info *info_out);
+                    pkv_stream_t stream, pkv_work_info *info_out, uint32_t options);
 
 /*
  * Synchronise `stream`, read *device_status (device memory), clear it, and

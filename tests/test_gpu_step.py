@@ -89,6 +89,45 @@ def test_host_staged_step_matches_device_calls_and_oracle(name):
     assert np.isfinite(got).all() and err <= MAX_ABS and rel <= MAX_REL_L2, (err, rel)
 
 
+@pytest.mark.parametrize("name", ["decode5", "tiny"])
+def test_in_place_step_matches_device_calls(name):
+    """PKV_STEP_IN_PLACE: a small step without prompt chunks reads the staging buffer in place
+    and writes its output straight to out_host (the device stage and `out` stay untouched), bit
+    for bit the same as the separate device calls; a step with a prompt chunk (tiny) takes the
+    copies and writes `out` as before."""
+    import torch
+
+    w = W.make_step(name, 0)
+    ds = R.prepare(w)
+    R.run_step(ds)
+    torch.cuda.synchronize()
+    assert B.pkv_check_device_status(ds.status) == 0
+    want_bits = ds.out.view(torch.int16).cpu().numpy()
+    low = ds.lowered
+    lay = B.pkv_stage_layout_init(w.total_q, len(w.segments), w.max_slots, w.max_blocks_per_slot, w.num_q_heads,
+                                  w.num_kv_heads, w.head_dim)
+    stage = R.HostStage(lay.work + 4 * int(ds.info.work_words) + 4096, "cuda")
+    stage.fill(lay, q=w.q, k_new=w.new_k(), v_new=w.new_v(), slot_mapping=low.slot_mapping,
+               cu_seqlens_q=low.cu_seqlens_q, seq_slot=low.seq_slot, context_lens=low.context_lens,
+               block_tables=ds.pool.block_tables())
+    stage.device.fill_(0x5A)
+    out = torch.empty_like(ds.out)
+    out.view(torch.int16).fill_(R.SENTINEL_BITS)
+    out_host = torch.empty(out.shape, dtype=torch.bfloat16, pin_memory=True)
+    call = B.StepCall(lay, stage.host, stage.device, ds.k_pool, ds.v_pool, out, ds.workspace, out_host=out_host,
+                      scale=w.scale, device_status=ds.status, in_place=True)
+    for _ in range(2):  # twice: nothing left over from the first call decides the second
+        out_host.view(torch.int16).fill_(R.SENTINEL_BITS)
+        info = call()
+        torch.cuda.synchronize()
+        assert B.pkv_check_device_status(ds.status) == 0
+        assert np.array_equal(out_host.view(torch.int16).numpy(), want_bits), "in-place step differs"
+    copied = info.num_prefill_items > 0
+    assert copied == (name == "tiny")
+    assert bool((stage.device[:64] != 0x5A).any()) == copied, "the device stage is written only by the copy"
+    assert np.array_equal(out.view(torch.int16).cpu().numpy(), want_bits) == copied, "`out` only on the copy path"
+
+
 def test_host_staged_step_views_feed_the_device_calls():
     """The device views of a staged step drive pkv_cache_write / pkv_attention to the same bits."""
     import torch

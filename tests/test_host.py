@@ -404,7 +404,7 @@ def test_step_rejects_bad_staging_before_any_device_work():
         info = B.WorkInfo()
         rc = B._lib().pkv_step(ctypes.byref(lay), p(h), h.nbytes, p(d_), d_.nbytes, p(pools), p(pools), 4, 16,
                                0.0, None if ws is None else p(ws), 0 if ws is None else ws.nbytes, p(out), None,
-                               None, None, ctypes.byref(info))
+                               None, None, ctypes.byref(info), 0)
         return B.STATUS_NAMES[rc], info
 
     # workspace missing: slot 0 has 3 spans, so partials are needed
