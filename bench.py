@@ -809,7 +809,8 @@ def run_churn(args, rank, world, local_rank):
     if chunk_ms:
         ach = sum(chunk_fl) / (sum(chunk_ms) / 1e3) / 1e12
         kernels["chunk"] = {"bound": "tensor", "kernel": "prefill_pair_kernel", "achieved": ach, "peak": tflops,
-                            "unit": "TFLOP/s", "frac": ach / tflops, "traffic": None,
+                            "unit": "TFLOP/s", "frac": ach / tflops,
+                            "traffic": profiled_traffic("pkv_prefill_pair.cu", "churn"),
                             "algorithmic_flop_per_launch": sum(chunk_fl) / len(chunk_fl),
                             "mean_launch_ms": mean(chunk_ms), "launches": len(chunk_ms),
                             "total_ms": sum(chunk_ms),
