@@ -7,10 +7,10 @@
 Prints one JSON line. The default workload is the continuous-batching churn
 trace (arrivals, chunked prompts beside decode rows, retirements; 32 q / 8 kv
 heads, head_dim 128, block 16, 131,072-block pool): the decode + prefill mix
-the metric is quoted on. Its timed window starts at trace step 50 whatever W
-is (the trace is replayed up to there untimed, its last W steps as warm-up),
-so the K timed steps are steady-state steps: a 512-row prompt chunk beside a
-growing decode batch. Metric: KV bytes the attention must read (each
+the metric is quoted on. Its K timed steps are spread evenly over the trace's
+steady state, steps 50 to 199 (a 512-row prompt chunk beside a decode batch
+that grows from 6 to over 20 rows), whatever W is; every step of the trace
+runs in order, the W steps before step 50 as timed-style warm-up. Metric: KV bytes the attention must read (each
 sequence's K and V once per kv head, plus Q in and O out) per second of device
 time, and packed rows per second.
 
@@ -90,8 +90,8 @@ WORKLOAD_TEXT = {
 }
 # Single-step workloads carried in the churn line's ``configs``.
 EXTRA_CONFIGS = ("decode5", "mixed", "decode256", "chunk2048", "verify4", "verify8", "verify16")
-# First timed step of the churn trace: by then a decode batch runs beside every
-# 512-row prompt chunk (the trace's steady state).
+# Start of the churn trace's steady state: from here a decode batch runs beside
+# every 512-row prompt chunk; the timed steps are spread over the rest of the trace.
 CHURN_OFFSET = 50
 L2_NOTE = ("flushed before every step: 256 MiB written, then 256 MiB read so L2 holds clean lines; "
            "both outside the timed events")
@@ -372,11 +372,23 @@ def run_reference(args, rank, world):
 
 
 def churn_window(args, num_steps):
-    """(first timed step, timed steps): the window starts at CHURN_OFFSET, or
-    earlier when K steps would run past the trace's end."""
+    """The trace steps to time: K = --steps of them, spread evenly over the
+    steady-state range [CHURN_OFFSET, num_steps) (every step of it when K covers
+    the range; the window moves earlier when K is larger still). Every step runs
+    in trace order; the W steps before the first timed one are timed-style
+    warm-up."""
     timed = max(1, min(args.steps, num_steps))
     first = min(CHURN_OFFSET, num_steps - timed)
-    return first, timed
+    span = num_steps - first
+    return [first + (i * span) // timed for i in range(timed)]
+
+
+def describe_window(steps, num_steps, warmup):
+    first = steps[0]
+    every = "every step" if len(steps) == num_steps - first else f"{len(steps)} steps spread evenly"
+    return (f"steps 0..{first - 1} replayed untimed (the last {min(warmup, first)} as timed-style warm-up); "
+            f"{every} of {first}..{num_steps - 1} timed ({', '.join(map(str, steps[:4]))}, ..., {steps[-1]}), "
+            f"the steps between them replayed untimed")
 
 
 def run_reference_churn(args):
@@ -391,11 +403,12 @@ def run_reference_churn(args):
     reqs = W.churn_trace(args.seed, spec)
     ref = churn.ChurnReplay(reqs, max_slots=spec.max_slots, num_blocks=spec.num_blocks, block_size=spec.block_size)
     toks = W.TokenSource(args.seed, spec.num_q_heads, spec.num_kv_heads, spec.head_dim)
-    first, timed = churn_window(args, spec.num_steps)
+    window = churn_window(args, spec.num_steps)
+    timed_set = set(window)
     samples = []
-    for step in range(first + timed):
+    for step in range(window[-1] + 1):
         rows = ref.plan()
-        if step >= first:
+        if step in timed_set:
             for r in rows:
                 samples.append((r.rid, r.begin + r.n, toks.rows(r.rid, r.begin + r.n - 1, r.begin + r.n)[2]))
         ref.commit(rows)
@@ -405,7 +418,7 @@ def run_reference_churn(args):
             "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": f"churn: {WORKLOAD_TEXT['churn']}",
-                       "trace_steps": f"steps {first}..{first + timed - 1} sampled", "sample": cb["sample"]},
+                       "trace_steps": describe_window(window, spec.num_steps, args.warmup), "sample": cb["sample"]},
             "impl": "reference", "cpu_baseline": cb,
             "e2e": {"value": cb["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
@@ -705,7 +718,8 @@ def run_churn(args, rank, world, local_rank):
     flush = L2Flush(dev)
     stream = torch.cuda.current_stream()
     scale = 1.0 / np.sqrt(d)
-    first, timed = churn_window(args, spec.num_steps)
+    window = churn_window(args, spec.num_steps)
+    timed_set, first = set(window), window[0]
     sample_cpu = not args.no_cpu_baseline and rank == 0 and world == 1
     cpu_rows = []  # (request, length, last q row) of timed segments, for the oracle baseline
 
@@ -713,7 +727,7 @@ def run_churn(args, rank, world, local_rank):
     chunk_ms, chunk_fl, dec_ms, dec_bytes, write_ms, attn_ms = [], [], [], [], [], []
     prefill_steps = launches = h2d_tot = d2h_tot = 0
     clocks = stage = ws = None
-    for step in range(first + timed):
+    for step in range(window[-1] + 1):
         rows = sch.plan()
         if not rows:
             sch.commit(rows)
@@ -740,8 +754,8 @@ def run_churn(args, rank, world, local_rank):
         out_host = torch.empty(out.shape, dtype=torch.bfloat16, pin_memory=True)
         ctx = [int(low.context_lens[r.slot]) for r in rows]
         nbytes = sum(ctx) * hkv * d * 4 + T * hq * d * 4
-        is_timed = step >= first
-        is_warm = step >= first - args.warmup
+        is_timed = step in timed_set
+        is_warm = is_timed or first - args.warmup <= step < first
         if is_timed and clocks is None:
             clocks = ClockSampler.for_device(dev)
             clocks.start()
@@ -837,10 +851,8 @@ def run_churn(args, rank, world, local_rank):
         "ms_per_step": tot_ms / n, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
         "config": {"workload": f"churn: {WORKLOAD_TEXT['churn']}",
-                   "trace_steps": f"steps 0..{first - 1} replayed untimed (the last {min(args.warmup, first)} "
-                                  f"as timed-style warm-up), steps {first}..{first + n - 1} timed, of "
-                                  f"{spec.num_steps}",
-                   "timed_offset": first,
+                   "trace_steps": describe_window(window, spec.num_steps, args.warmup),
+                   "timed_steps": window,
                    "steps_with_prompt_chunks": prefill_steps, "rows_per_step_mean": sum(step_rows) / n,
                    "kv_bytes_per_step_mean": sum(step_bytes) / n,
                    "step_ms_p50": statistics.median(step_ms), "step_ms_p90": sorted(step_ms)[int(0.9 * (n - 1))],
