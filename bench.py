@@ -385,10 +385,10 @@ def churn_window(args, num_steps):
 
 def describe_window(steps, num_steps, warmup):
     first = steps[0]
-    every = "every step" if len(steps) == num_steps - first else f"{len(steps)} steps spread evenly"
+    every = "every step of" if len(steps) == num_steps - first else f"{len(steps)} steps spread evenly over"
     return (f"steps 0..{first - 1} replayed untimed (the last {min(warmup, first)} as timed-style warm-up); "
-            f"{every} of {first}..{num_steps - 1} timed ({', '.join(map(str, steps[:4]))}, ..., {steps[-1]}), "
-            f"the steps between them replayed untimed")
+            f"{every} {first}..{num_steps - 1} timed ({', '.join(map(str, steps[:4]))}, ..., {steps[-1]})"
+            + ("" if every.startswith("every") else ", the steps between them replayed untimed"))
 
 
 def run_reference_churn(args):
