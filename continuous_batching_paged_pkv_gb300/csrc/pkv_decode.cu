@@ -292,8 +292,10 @@ __global__ void __launch_bounds__(NW * 32, 1)
       }
 
       // Online softmax; this thread holds keys lane/4 and lane/4 + 8 of heads
-      // (lane%4)*2 + {0, 1}.
-      float x[NT][2][2], mx[NT][2];
+      // (lane%4)*2 + {0, 1}. A column's maximum moves only when a logit passes
+      // it by the lazy margin: each lane tests its own two keys, and only then
+      // does the warp reduce the column maxima.
+      float x[NT][2][2];
       bool need = false;
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
@@ -303,21 +305,20 @@ __global__ void __launch_bounds__(NW * 32, 1)
           const int vis = MULTI ? min(v, vis0 + static_cast<int>((colrow >> (8 * (nt * 2 + c))) & 0xFF)) : v;
           x[nt][c][0] = ka < vis ? (s0[nt][c] + s1[nt][c]) * sl2 : -INFINITY;
           x[nt][c][1] = kb < vis ? (s0[nt][c + 2] + s1[nt][c + 2]) * sl2 : -INFINITY;
-          float t = fmaxf(x[nt][c][0], x[nt][c][1]);
-          t = fmaxf(t, __shfl_xor_sync(kFull, t, 4));
-          t = fmaxf(t, __shfl_xor_sync(kFull, t, 8));
-          t = fmaxf(t, __shfl_xor_sync(kFull, t, 16));
-          mx[nt][c] = t;
-          need |= t > m[nt][c] + kRescale;
+          need |= fmaxf(x[nt][c][0], x[nt][c][1]) > m[nt][c] + kRescale;
         }
       if (__any_sync(kFull, need)) {
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-          for (int c = 0; c < 2; ++c)
-            if (mx[nt][c] > m[nt][c] + kRescale) {
-              const float corr = exp2f(m[nt][c] - mx[nt][c]);
-              m[nt][c] = mx[nt][c];
+          for (int c = 0; c < 2; ++c) {
+            float t = fmaxf(x[nt][c][0], x[nt][c][1]);
+            t = fmaxf(t, __shfl_xor_sync(kFull, t, 4));
+            t = fmaxf(t, __shfl_xor_sync(kFull, t, 8));
+            t = fmaxf(t, __shfl_xor_sync(kFull, t, 16));
+            if (t > m[nt][c] + kRescale) {
+              const float corr = exp2f(m[nt][c] - t);
+              m[nt][c] = t;
               l[nt][c] *= corr;
 #pragma unroll
               for (int mt = 0; mt < KT; ++mt) {
@@ -325,6 +326,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
                 acc[nt][mt][c + 2] *= corr;
               }
             }
+          }
       }
       uint32_t pf[NT][2];
 #pragma unroll

@@ -24,23 +24,29 @@
 // Decode kernel (same task pipeline as the bf16 decode kernel: persistent
 // warps, a TMA ring per warp, work sorted longest first). Per 16-key sub-tile
 // a stage holds the K and V codes (TMA, swizzled like the bf16 tiles) and
-// their scales (one bulk copy each). Math, per warp:
-//   S^T = K Q^T as fp16 MMAs over the integer codes (exact in fp16), one
-//   accumulator per scale group; the group scales multiply the four partial
-//   sums in fp32. Q is widened to fp16 after a power-of-two rescale per
-//   column (max |q'| < 2^15), undone in the softmax scale, so fp16's range
-//   never clips a query.
-//   O^T += V^T P^T as bf16 MMAs over the integer codes (exact in bf16), with
-//   each V scale folded into P: the m-tiles of one scale group share one
-//   scaled copy of P^T. head_dim is permuted inside each tile so that every
-//   thread reads whole 4-byte words of codes; the permutation is undone in the
-//   output address.
-// Codes become floats without conversion instructions: a byte b (offset by
-// 128) placed under the exponent of 1024.0 (fp16) or 2^23 (fp32) is that
-// power plus b, one subtraction away from the code. A nibble n (offset by 8)
-// goes under 1024.0 for K (fp16) and under 128.0 for V (bf16: 128 + n is
-// exact), so 4-bit codes take the same paths; their K words hold dims
-// 32 g + 8 j .. + 7 and q is loaded in that order.
+// their scales (one bulk copy each). Both products are fp16 MMAs over offset
+// codes: an 8-bit code c enters as the fp16 integer 1152 + c (its byte XOR
+// 0x80 placed under the exponent of 1024.0), a 4-bit code as 1032 + c (its
+// nibble XOR 8), one or two integer instructions per pair of codes and no
+// float subtraction. The offsets come out in fp32:
+//   S^T = K Q^T: the accumulator of each scale group starts at -offset times
+//   the sum of that group's query values, so it ends at the group's partial
+//   dot product; the group scales then fold the partial sums into a logit. Q
+//   is widened to fp16 after a power-of-two rescale per column (max |q'| <
+//   2^15), undone in the softmax scale, so fp16's range never clips a query.
+//   O^T += V^T P'^T with P' = 2^7 p dv / Dref: p the softmax weight (at most
+//   2^8 under the lazy rescale), dv the key's V scale of the group and Dref
+//   the largest V scale the task has met in that group (a running maximum;
+//   the group's accumulators are rescaled when it grows), so P' < 2^15 fits
+//   fp16. After each m-tile's MMA a second one with A = -offset (every
+//   element) and the same P' subtracts offset times the sub-tile's P' sums,
+//   so the accumulator never carries more than one sub-tile's offset; the
+//   task's end multiplies by Dref (the 2^7 cancels against the row sum, which
+//   adds the same scaled weights).
+// head_dim is permuted inside each tile so that every thread reads whole
+// words of codes: the permutation is undone in the output address, and for
+// 4-bit K by loading q in the same order (a thread's K word holds dims
+// 32 g + 8 j .. + 7, paired (0, 4), (1, 5), (2, 6), (3, 7) in the MMA).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -238,62 +244,42 @@ __device__ __forceinline__ uint32_t code_off(int row, int col) {
     return row * 64 + ((((col >> 4) ^ ((row >> 1) & 3))) << 4) + (col & 15);
 }
 
-// Four codes (a word, two's complement) -> two fp16 pairs of the integer values.
-__device__ __forceinline__ void codes_to_f16(uint32_t w, uint32_t &lo, uint32_t &hi) {
-  const uint32_t u = w ^ 0x80808080u;                  // offset by 128
-  const uint32_t m = 0x64806480u;                      // 1152 = 1024 + 128 in both halves
-  const uint32_t a = prmt(u, 0x64646464u, 0x4140u);    // 1024 + u0, 1024 + u1
-  const uint32_t b = prmt(u, 0x64646464u, 0x4342u);    // 1024 + u2, 1024 + u3
-  __half2 ha = __hsub2(*reinterpret_cast<const __half2 *>(&a), *reinterpret_cast<const __half2 *>(&m));
-  __half2 hb = __hsub2(*reinterpret_cast<const __half2 *>(&b), *reinterpret_cast<const __half2 *>(&m));
-  lo = *reinterpret_cast<uint32_t *>(&ha);
-  hi = *reinterpret_cast<uint32_t *>(&hb);
+// Offset under which a code enters the fp16 MMAs: 1152 + c (8-bit), 1032 + c (4-bit).
+template <int BITS>
+constexpr float kCodeOffset = BITS == 8 ? 1152.f : 1032.f;
+
+// Four 8-bit codes (a word, two's complement) -> two fp16 pairs of 1152 + code:
+// lo holds codes 0 and 1, hi codes 2 and 3.
+__device__ __forceinline__ void codes_to_f16_off(uint32_t w, uint32_t &lo, uint32_t &hi) {
+  const uint32_t u = w ^ 0x80808080u;  // offset by 128
+  lo = prmt(u, 0x64646464u, 0x4140u);   // under the exponent of 1024.0
+  hi = prmt(u, 0x64646464u, 0x4342u);
 }
 
-// Code byte `sel` of word x and of word y -> one bf16 pair (x's in the low half).
-__device__ __forceinline__ uint32_t codes_to_bf16_pair(uint32_t ux, uint32_t uy, uint32_t sel) {
-  const float fx = __uint_as_float(prmt(ux, 0x4B000000u, 0x7540u | sel)) - 8388736.f;  // 2^23 + 128
-  const float fy = __uint_as_float(prmt(uy, 0x4B000000u, 0x7540u | sel)) - 8388736.f;
-  return prmt(__float_as_uint(fx), __float_as_uint(fy), 0x7632u);  // upper halves: exact for integers
+// Byte J of word x and of word y (8-bit codes) -> the fp16 pair (1152 + x_J, 1152 + y_J).
+template <int J>
+__device__ __forceinline__ uint32_t code_pair_f16_off(uint32_t x, uint32_t y) {
+  constexpr uint32_t sel = J | (J << 4) | ((4 + J) << 8) | ((4 + J) << 12);
+  return (prmt(x, y, sel) & 0x00FF00FFu) ^ 0x64806480u;
 }
 
-// Eight 4-bit codes (a word, value 2i in the low nibble of byte i, two's
-// complement) -> four fp16 pairs of the integer values: (lo0, hi0) hold values
-// 0..3, (lo1, hi1) values 4..7. The nibbles are offset by 8 and placed under
-// the exponent of 1024.0, one subtraction of 1032 away from the code.
-__device__ __forceinline__ void nibbles_to_f16(uint32_t w, uint32_t &lo0, uint32_t &hi0, uint32_t &lo1,
-                                               uint32_t &hi1) {
-  const uint32_t x = w ^ 0x88888888u;
-  const uint32_t ev = x & 0x0F0F0F0Fu, od = (x >> 4) & 0x0F0F0F0Fu;  // values 0,2,4,6 and 1,3,5,7
-  const uint32_t t0 = prmt(ev, od, 0x5140u), t1 = prmt(ev, od, 0x7362u);  // values 0..3, 4..7 as bytes
-  const uint32_t m = 0x64086408u;                                      // 1032 in both halves
-  const uint32_t a0 = prmt(t0, 0x64646464u, 0x4140u), b0 = prmt(t0, 0x64646464u, 0x4342u);
-  const uint32_t a1 = prmt(t1, 0x64646464u, 0x4140u), b1 = prmt(t1, 0x64646464u, 0x4342u);
-  const __half2 hm = *reinterpret_cast<const __half2 *>(&m);
-  __half2 r;
-  r = __hsub2(*reinterpret_cast<const __half2 *>(&a0), hm);
-  lo0 = *reinterpret_cast<uint32_t *>(&r);
-  r = __hsub2(*reinterpret_cast<const __half2 *>(&b0), hm);
-  hi0 = *reinterpret_cast<uint32_t *>(&r);
-  r = __hsub2(*reinterpret_cast<const __half2 *>(&a1), hm);
-  lo1 = *reinterpret_cast<uint32_t *>(&r);
-  r = __hsub2(*reinterpret_cast<const __half2 *>(&b1), hm);
-  hi1 = *reinterpret_cast<uint32_t *>(&r);
+// Nibble S of both 16-bit halves of x (4-bit codes) -> the fp16 pair of 1032 + code.
+template <int S>
+__device__ __forceinline__ uint32_t nibble_pair_f16_off(uint32_t x) {
+  return ((x >> (4 * S)) & 0x000F000Fu) ^ 0x64086408u;
 }
 
-// Nibble `n` of both halves of x (two keys' 4-bit codes, offset by 8) -> one
-// bf16 pair of the codes: 128 + u is a bfloat16 integer for u < 16.
-__device__ __forceinline__ uint32_t nibble_pair_to_bf16(uint32_t x, int n) {
-  const uint32_t t = ((x >> (4 * n)) & 0x000F000Fu) | 0x43004300u;
-  const __nv_bfloat162 r =
-      __hsub2(*reinterpret_cast<const __nv_bfloat162 *>(&t), __floats2bfloat162_rn(136.f, 136.f));
-  return *reinterpret_cast<const uint32_t *>(&r);
+// Scale of group g from bf16 pairs packed two per word, as fp32.
+template <int G2>
+__device__ __forceinline__ float group_scale(const uint32_t (&w)[G2], int g) {
+  return __uint_as_float((g & 1) ? (w[g >> 1] & 0xFFFF0000u) : (w[g >> 1] << 16));
 }
 
 // Q'^T fragments (B operand, fp16) for k-step kk = 2 g + h: thread (column
-// lane/4, j = lane%4) holds q[column][32 g + 16 h + 4 j + 0..3] (8-bit codes)
-// or q[column][32 g + 8 j + 4 h + 0..3] (4-bit codes: a thread's code word
-// holds dims 32 g + 8 j .. + 7), scaled by 2^sh (per column) so that
+// lane/4, j = lane%4) holds, for 8-bit codes, q[column][32 g + 16 h + 4 j +
+// 0..3] ((0, 1) in the first register, (2, 3) in the second); for 4-bit codes,
+// with p = 32 g + 8 j, (p + 2 h, p + 2 h + 4) and (p + 2 h + 1, p + 2 h + 5),
+// the pairs the nibble words give. Scaled by 2^sh (per column) so that
 // max |q'| < 2^15; `inv` receives 2^-sh.
 template <int D, int NT, bool MULTI, int BITS>
 __device__ __forceinline__ void load_q_quant(uint32_t (&qf)[NT][D / 16][2], float (&inv)[NT], const Task &T,
@@ -307,17 +293,33 @@ __device__ __forceinline__ void load_q_quant(uint32_t (&qf)[NT][D / 16][2], floa
     const __nv_bfloat16 *qrow = static_cast<const __nv_bfloat16 *>(a.q) +
                                 ((static_cast<size_t>(T.row0) + i) * a.num_q_heads + T.g * a.group + h) * D;
     const int j = lane & 3;
-    uint2 raw[KT];
+    uint32_t raw[KT][2];  // bf16 pairs in fragment order
+    if constexpr (BITS == 8) {
+#pragma unroll
+      for (int kk = 0; kk < KT; ++kk) {
+        const uint2 r = valid ? __ldg(reinterpret_cast<const uint2 *>(qrow + 32 * (kk >> 1) + 16 * (kk & 1) + 4 * j))
+                              : make_uint2(0, 0);
+        raw[kk][0] = r.x;
+        raw[kk][1] = r.y;
+      }
+    } else {
+#pragma unroll
+      for (int g = 0; g < KT / 2; ++g) {
+        const __nv_bfloat16 *p = qrow + 32 * g + 8 * j;
+        const uint2 r0 = valid ? __ldg(reinterpret_cast<const uint2 *>(p)) : make_uint2(0, 0);      // dims 0..3
+        const uint2 r1 = valid ? __ldg(reinterpret_cast<const uint2 *>(p + 4)) : make_uint2(0, 0);  // dims 4..7
+        raw[2 * g][0] = prmt(r0.x, r1.x, 0x5410u);      // (0, 4)
+        raw[2 * g][1] = prmt(r0.x, r1.x, 0x7632u);      // (1, 5)
+        raw[2 * g + 1][0] = prmt(r0.y, r1.y, 0x5410u);  // (2, 6)
+        raw[2 * g + 1][1] = prmt(r0.y, r1.y, 0x7632u);  // (3, 7)
+      }
+    }
     float mx = 0.f;
 #pragma unroll
-    for (int kk = 0; kk < KT; ++kk) {
-      const int dim0 = BITS == 8 ? 32 * (kk >> 1) + 16 * (kk & 1) + 4 * j : 32 * (kk >> 1) + 8 * j + 4 * (kk & 1);
-      raw[kk] = valid ? __ldg(reinterpret_cast<const uint2 *>(qrow + dim0)) : make_uint2(0, 0);
-      mx = fmaxf(mx, fmaxf(fmaxf(fabsf(bf16_bits_to_float(raw[kk].x & 0xFFFFu)),
-                                 fabsf(bf16_bits_to_float(raw[kk].x >> 16))),
-                           fmaxf(fabsf(bf16_bits_to_float(raw[kk].y & 0xFFFFu)),
-                                 fabsf(bf16_bits_to_float(raw[kk].y >> 16)))));
-    }
+    for (int kk = 0; kk < KT; ++kk)
+#pragma unroll
+      for (int b = 0; b < 2; ++b)
+        mx = fmaxf(mx, fmaxf(fabsf(bf16_bits_to_float(raw[kk][b] & 0xFFFFu)), fabsf(bf16_bits_to_float(raw[kk][b] >> 16))));
     mx = fmaxf(mx, __shfl_xor_sync(kAll, mx, 1));
     mx = fmaxf(mx, __shfl_xor_sync(kAll, mx, 2));
     // exponent of mx (its float bits; 0 and subnormals read as -127)
@@ -326,15 +328,58 @@ __device__ __forceinline__ void load_q_quant(uint32_t (&qf)[NT][D / 16][2], floa
     const float f = __uint_as_float(static_cast<uint32_t>(sh + 127) << 23);
     inv[nt] = __uint_as_float(static_cast<uint32_t>(127 - sh) << 23);
 #pragma unroll
-    for (int kk = 0; kk < KT; ++kk) {
-      __half2 lo = __floats2half2_rn(bf16_bits_to_float(raw[kk].x & 0xFFFFu) * f,
-                                     bf16_bits_to_float(raw[kk].x >> 16) * f);
-      __half2 hi = __floats2half2_rn(bf16_bits_to_float(raw[kk].y & 0xFFFFu) * f,
-                                     bf16_bits_to_float(raw[kk].y >> 16) * f);
-      qf[nt][kk][0] = *reinterpret_cast<uint32_t *>(&lo);
-      qf[nt][kk][1] = *reinterpret_cast<uint32_t *>(&hi);
+    for (int kk = 0; kk < KT; ++kk)
+#pragma unroll
+      for (int b = 0; b < 2; ++b) {
+        __half2 v = __floats2half2_rn(bf16_bits_to_float(raw[kk][b] & 0xFFFFu) * f,
+                                      bf16_bits_to_float(raw[kk][b] >> 16) * f);
+        qf[nt][kk][b] = *reinterpret_cast<uint32_t *>(&v);
+      }
+  }
+}
+
+// The q rows of task T's columns pulled into L1 ahead of load_q_quant (the
+// four threads of a column cover its D * 2 bytes).
+template <int D, int NT, bool MULTI>
+__device__ __forceinline__ void prefetch_q(const Task &T, const StepArgs &a, int lane) {
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int col = nt * 8 + (lane >> 2);
+    if (col < (MULTI ? T.nrows : 1) * a.group) {
+      const int i = MULTI ? col / a.group : 0, h = MULTI ? col % a.group : col;
+      const char *p = reinterpret_cast<const char *>(static_cast<const __nv_bfloat16 *>(a.q) +
+                                                     ((static_cast<size_t>(T.row0) + i) * a.num_q_heads +
+                                                      T.g * a.group + h) * D) +
+                      (lane & 3) * (D / 2);
+      asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
     }
   }
+}
+
+// Start value of each scale group's S^T accumulator: -offset times the sum of
+// the group's 32 query values (the fp16 values the MMA reads) of columns
+// 2 (lane % 4) + c, which removes the code offset from the group's dot product.
+template <int D, int NT, int BITS>
+__device__ __forceinline__ void key_offsets(float (&kinit)[D / 32][NT][2], const uint32_t (&qf)[NT][D / 16][2],
+                                            int lane) {
+  const int jq = lane & 3;
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int g = 0; g < D / 32; ++g) {
+      float s = 0.f;
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+          const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&qf[nt][2 * g + h][b]));
+          s += f.x + f.y;
+        }
+      s += __shfl_xor_sync(kAll, s, 1);  // the four threads of a column hold its 32 values
+      s += __shfl_xor_sync(kAll, s, 2);
+      kinit[g][nt][0] = -kCodeOffset<BITS> * __shfl_sync(kAll, s, (2 * jq) * 4);
+      kinit[g][nt][1] = -kCodeOffset<BITS> * __shfl_sync(kAll, s, (2 * jq + 1) * 4);
+    }
 }
 
 template <int D, int NT, bool MULTI, int NW, int BITS>
@@ -347,8 +392,10 @@ __global__ void __launch_bounds__(NW * 32, 1)
   constexpr int RB = Cfg::kRowBytes;  // code row layout: 128-byte rows (128B swizzle) or 64-byte (64B)
   constexpr int KT = D / 16;  // k-steps of QK^T, m-tiles of PV
   constexpr int NG = Cfg::kGroups;
+  constexpr int NG2 = NG / 2;  // words of packed bf16 scales per key
   constexpr int NST = Cfg::kStages;
   constexpr int kMaxRows = MULTI ? 16 : 1;
+  constexpr float kHeadroom = 7.f;  // log2 of the factor that lifts P' towards fp16's top
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -385,10 +432,9 @@ __global__ void __launch_bounds__(NW * 32, 1)
     if (tC < num_tasks) rawC = load_item(items, tC, hkv);
   }
   finalize(A, a, lane, 8 * NT, kMaxRows);
-  uint32_t qA[NT][KT][2], qB[NT][KT][2];
-  float invA[NT], invB[NT];
+  uint32_t qA[NT][KT][2];
+  float invA[NT];
   if (A.ok) load_q_quant<D, NT, MULTI, BITS>(qA, invA, A, a, lane);
-  bool qB_loaded = false;
 
   int P = 0, C = 0, pa = 0, pb = 0;
   int pstage = 0;
@@ -427,10 +473,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
     if (B.t >= 0) {
       if (!B.finalized) {
         finalize(B, a, lane, 8 * NT, kMaxRows);
-        if (B.ok) {
-          load_q_quant<D, NT, MULTI, BITS>(qB, invB, B, a, lane);
-          qB_loaded = true;
-        }
+        if (B.ok) prefetch_q<D, NT, MULTI>(B, a, lane);  // loaded when B becomes current
       }
       if (pb < B.units) {
         issue(B, pb++);
@@ -448,6 +491,9 @@ __global__ void __launch_bounds__(NW * 32, 1)
   const int ka = lane >> 2, kb = ka + 8, jq = lane & 3, k0 = jq * 2, r = lane >> 2;
   // per-thread code offsets inside a sub-tile (rows kb = ka + 8 and k0 + 8 share the swizzle phase)
   const uint32_t koff = code_off<RB>(ka, 4 * jq);  // + group/half chunk below
+  // fp16 pairs of -offset (-1152 or -1032): A of the MMA that takes the code offset out of O^T
+  constexpr uint32_t kNegOffBits = BITS == 8 ? 0xE480E480u : 0xE408E408u;
+  const uint32_t kNegOff[4] = {kNegOffBits, kNegOffBits, kNegOffBits, kNegOffBits};
   int cstage = 0;
   uint32_t cphase = 0;
 
@@ -463,6 +509,15 @@ __global__ void __launch_bounds__(NW * 32, 1)
 #pragma unroll
       for (int mt = 0; mt < KT; ++mt) acc[nt][mt][0] = acc[nt][mt][1] = acc[nt][mt][2] = acc[nt][mt][3] = 0.f;
     }
+    // running maximum V scale of each group (packed bf16 bits, 0 before the first) and its reciprocal
+    uint32_t vref[NG2];
+    float vinv[NG];
+#pragma unroll
+    for (int i = 0; i < NG2; ++i) vref[i] = 0u;
+#pragma unroll
+    for (int g = 0; g < NG; ++g) vinv[g] = 0.f;
+    float kinit[NG][NT][2];
+    key_offsets<D, NT, BITS>(kinit, qA, lane);
     const int nrows = MULTI ? A.nrows : 1;
     uint32_t colrow = 0;
     if (MULTI) {
@@ -497,106 +552,100 @@ __global__ void __launch_bounds__(NW * 32, 1)
       const uint32_t ks = ring_addr + Cfg::kKs + stage * Cfg::kScaleBytes;
       const uint32_t vs = ring_addr + Cfg::kVs + stage * Cfg::kScaleBytes;
 
-      // S^T = K Q^T per scale group (integer codes, fp16 MMA)
-      float sg[NG][NT][4];
-#pragma unroll
-      for (int g = 0; g < NG; ++g)
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) sg[g][nt][0] = sg[g][nt][1] = sg[g][nt][2] = sg[g][nt][3] = 0.f;
-      if constexpr (BITS == 8) {
-#pragma unroll
-        for (int kk = 0; kk < KT; ++kk) {
-          // chunk 2g + h of rows ka / kb: the swizzle XORs the chunk index
-          const uint32_t off = koff ^ (static_cast<uint32_t>(kk) << 4);
-          const uint32_t wa = lds32(kc + off);
-          const uint32_t wb = lds32(kc + off + 8 * RB);
-          uint32_t af[4];
-          codes_to_f16(wa, af[0], af[2]);
-          codes_to_f16(wb, af[1], af[3]);
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) mma_f16_16816(sg[kk >> 1][nt], af, qA[nt][kk][0], qA[nt][kk][1]);
-        }
+      // group scales of keys ka and kb (packed bf16); V scales zero past the sub-tile's keys
+      uint32_t kwa[NG2], kwb[NG2], vwa[NG2], vwb[NG2];
+      if constexpr (NG == 4) {
+        const uint2 x0 = lds64(ks + ka * 8), x1 = lds64(ks + kb * 8);
+        const uint2 y0 = lds64(vs + ka * 8), y1 = lds64(vs + kb * 8);
+        kwa[0] = x0.x; kwa[1] = x0.y; kwb[0] = x1.x; kwb[1] = x1.y;
+        vwa[0] = y0.x; vwa[1] = y0.y; vwb[0] = y1.x; vwb[1] = y1.y;
       } else {
+        kwa[0] = lds32(ks + ka * 4); kwb[0] = lds32(ks + kb * 4);
+        vwa[0] = lds32(vs + ka * 4); vwb[0] = lds32(vs + kb * 4);
+      }
 #pragma unroll
-        for (int g = 0; g < NG; ++g) {
-          // chunk g of rows ka / kb holds dims 32 g .. 32 g + 31; this thread's word, dims 32 g + 8 jq + 0..7,
-          // feeds k-steps 2 g (dims + 0..3) and 2 g + 1 (dims + 4..7)
+      for (int i = 0; i < NG2; ++i) {
+        vwa[i] = ka < v ? vwa[i] : 0u;
+        vwb[i] = kb < v ? vwb[i] : 0u;
+      }
+
+      // S^T = K Q^T per scale group over the offset codes, each group's
+      // accumulator starting at -offset * its query sum; the group scales fold
+      // the partial sums into the logits of keys ka (0, 1) and kb (2, 3)
+      float sacc[NT][4];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
+#pragma unroll
+      for (int g = 0; g < NG; ++g) {
+        float sg[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          sg[nt][0] = sg[nt][2] = kinit[g][nt][0];
+          sg[nt][1] = sg[nt][3] = kinit[g][nt][1];
+        }
+        if constexpr (BITS == 8) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            // chunk 2g + h of rows ka / kb: the swizzle XORs the chunk index
+            const int kk = 2 * g + h;
+            const uint32_t off = koff ^ (static_cast<uint32_t>(kk) << 4);
+            const uint32_t wa = lds32(kc + off);
+            const uint32_t wb = lds32(kc + off + 8 * RB);
+            uint32_t af[4];
+            codes_to_f16_off(wa, af[0], af[2]);
+            codes_to_f16_off(wb, af[1], af[3]);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) mma_f16_16816(sg[nt], af, qA[nt][kk][0], qA[nt][kk][1]);
+          }
+        } else {
+          // chunk g of rows ka / kb holds dims 32 g .. 32 g + 31; this thread's word holds dims 32 g + 8 jq + 0..7
           const uint32_t off = koff ^ (static_cast<uint32_t>(g) << 4);
           const uint32_t wa = lds32(kc + off);
           const uint32_t wb = lds32(kc + off + 8 * RB);
-          uint32_t a0[4], a1[4];
-          nibbles_to_f16(wa, a0[0], a0[2], a1[0], a1[2]);
-          nibbles_to_f16(wb, a0[1], a0[3], a1[1], a1[3]);
+          const uint32_t a0[4] = {nibble_pair_f16_off<0>(wa), nibble_pair_f16_off<0>(wb), nibble_pair_f16_off<1>(wa),
+                                  nibble_pair_f16_off<1>(wb)};
+          const uint32_t a1[4] = {nibble_pair_f16_off<2>(wa), nibble_pair_f16_off<2>(wb), nibble_pair_f16_off<3>(wa),
+                                  nibble_pair_f16_off<3>(wb)};
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
-            mma_f16_16816(sg[g][nt], a0, qA[nt][2 * g][0], qA[nt][2 * g][1]);
-            mma_f16_16816(sg[g][nt], a1, qA[nt][2 * g + 1][0], qA[nt][2 * g + 1][1]);
+            mma_f16_16816(sg[nt], a0, qA[nt][2 * g][0], qA[nt][2 * g][1]);
+            mma_f16_16816(sg[nt], a1, qA[nt][2 * g + 1][0], qA[nt][2 * g + 1][1]);
           }
         }
-      }
-      // group scales of keys ka and kb; V scales of the same keys, zero past the sub-tile's keys
-      float dka[NG], dkb[NG], dva[NG], dvb[NG];
-      {
-        uint32_t w[4];
-        if constexpr (NG == 4) {
-          const uint2 x0 = lds64(ks + ka * 8), x1 = lds64(ks + kb * 8);
-          const uint2 y0 = lds64(vs + ka * 8), y1 = lds64(vs + kb * 8);
-          w[0] = x0.x; w[1] = x0.y; w[2] = x1.x; w[3] = x1.y;
+        const float dka = group_scale(kwa, g), dkb = group_scale(kwb, g);
 #pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            dka[g] = bf16_bits_to_float((w[g >> 1] >> (16 * (g & 1))) & 0xFFFFu);
-            dkb[g] = bf16_bits_to_float((w[2 + (g >> 1)] >> (16 * (g & 1))) & 0xFFFFu);
-          }
-          w[0] = y0.x; w[1] = y0.y; w[2] = y1.x; w[3] = y1.y;
-#pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            dva[g] = ka < v ? bf16_bits_to_float((w[g >> 1] >> (16 * (g & 1))) & 0xFFFFu) : 0.f;
-            dvb[g] = kb < v ? bf16_bits_to_float((w[2 + (g >> 1)] >> (16 * (g & 1))) & 0xFFFFu) : 0.f;
-          }
-        } else {
-          const uint32_t x0 = lds32(ks + ka * 4), x1 = lds32(ks + kb * 4);
-          const uint32_t y0 = lds32(vs + ka * 4), y1 = lds32(vs + kb * 4);
-#pragma unroll
-          for (int g = 0; g < 2; ++g) {
-            dka[g] = bf16_bits_to_float((x0 >> (16 * g)) & 0xFFFFu);
-            dkb[g] = bf16_bits_to_float((x1 >> (16 * g)) & 0xFFFFu);
-            dva[g] = ka < v ? bf16_bits_to_float((y0 >> (16 * g)) & 0xFFFFu) : 0.f;
-            dvb[g] = kb < v ? bf16_bits_to_float((y1 >> (16 * g)) & 0xFFFFu) : 0.f;
-          }
+        for (int nt = 0; nt < NT; ++nt) {
+          fma2(sacc[nt][0], sacc[nt][1], dka, dka, sg[nt][0], sg[nt][1], sacc[nt][0], sacc[nt][1]);
+          fma2(sacc[nt][2], sacc[nt][3], dkb, dkb, sg[nt][2], sg[nt][3], sacc[nt][2], sacc[nt][3]);
         }
       }
 
-      // online softmax (keys ka, kb of columns 2 jq + c)
-      float x[NT][2][2], mx[NT][2];
+      // online softmax (keys ka, kb of columns 2 jq + c); the warp reduces the
+      // column maxima only when some lane's logit passes its column's maximum
+      // by the lazy margin
+      float x[NT][2][2];
       bool need = false;
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-          float sa = 0.f, sb = 0.f;
-#pragma unroll
-          for (int g = 0; g < NG; ++g) {
-            sa = fmaf(dka[g], sg[g][nt][c], sa);
-            sb = fmaf(dkb[g], sg[g][nt][c + 2], sb);
-          }
           const int vis = MULTI ? min(v, vis0 + static_cast<int>((colrow >> (8 * (nt * 2 + c))) & 0xFF)) : v;
-          x[nt][c][0] = ka < vis ? sa * sl2c[nt][c] : -INFINITY;
-          x[nt][c][1] = kb < vis ? sb * sl2c[nt][c] : -INFINITY;
-          float t = fmaxf(x[nt][c][0], x[nt][c][1]);
-          t = fmaxf(t, __shfl_xor_sync(kAll, t, 4));
-          t = fmaxf(t, __shfl_xor_sync(kAll, t, 8));
-          t = fmaxf(t, __shfl_xor_sync(kAll, t, 16));
-          mx[nt][c] = t;
-          need |= t > m[nt][c] + kRescaleQuant;
+          x[nt][c][0] = ka < vis ? sacc[nt][c] * sl2c[nt][c] : -INFINITY;
+          x[nt][c][1] = kb < vis ? sacc[nt][c + 2] * sl2c[nt][c] : -INFINITY;
+          need |= fmaxf(x[nt][c][0], x[nt][c][1]) > m[nt][c] + kRescaleQuant;
         }
       if (__any_sync(kAll, need)) {
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-          for (int c = 0; c < 2; ++c)
-            if (mx[nt][c] > m[nt][c] + kRescaleQuant) {
-              const float corr = exp2f(m[nt][c] - mx[nt][c]);
-              m[nt][c] = mx[nt][c];
+          for (int c = 0; c < 2; ++c) {
+            float t = fmaxf(x[nt][c][0], x[nt][c][1]);
+            t = fmaxf(t, __shfl_xor_sync(kAll, t, 4));
+            t = fmaxf(t, __shfl_xor_sync(kAll, t, 8));
+            t = fmaxf(t, __shfl_xor_sync(kAll, t, 16));
+            if (t > m[nt][c] + kRescaleQuant) {
+              const float corr = ex2_approx(m[nt][c] - t);
+              m[nt][c] = t;
               l[nt][c] *= corr;
 #pragma unroll
               for (int mt = 0; mt < KT; ++mt) {
@@ -604,61 +653,108 @@ __global__ void __launch_bounds__(NW * 32, 1)
                 acc[nt][mt][c + 2] *= corr;
               }
             }
+          }
       }
-      // P (fp32), then one scaled bf16 copy of P^T per V scale group
-      uint32_t pf[NG][NT][2];
+
+      // Dref: the running maximum V scale per group; a group's accumulators follow it when it grows
+      {
+        uint32_t vn[NG2], grow = 0;
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        const float m0 = m[nt][0] == -INFINITY ? 0.f : m[nt][0];
-        const float m1 = m[nt][1] == -INFINITY ? 0.f : m[nt][1];
-        const float p00 = exp2f(x[nt][0][0] - m0), p01 = exp2f(x[nt][0][1] - m0);  // column c=0: keys ka, kb
-        const float p10 = exp2f(x[nt][1][0] - m1), p11 = exp2f(x[nt][1][1] - m1);  // column c=1
-        l[nt][0] += p00 + p01;
-        l[nt][1] += p10 + p11;
+        for (int i = 0; i < NG2; ++i) {
+          vn[i] = max_u16x2(max_u16x2(vwa[i], vwb[i]), vref[i]);  // positive bf16: bit order is value order
+          grow |= vn[i] ^ vref[i];
+        }
+        if (__any_sync(kAll, grow != 0)) {
 #pragma unroll
-        for (int g = 0; g < NG; ++g) {
-          pf[g][nt][0] = movmatrix_trans(pack_bf16x2(p00 * dva[g], p10 * dva[g]));
-          pf[g][nt][1] = movmatrix_trans(pack_bf16x2(p01 * dvb[g], p11 * dvb[g]));
+          for (int i = 0; i < NG2; ++i)
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) vn[i] = max_u16x2(vn[i], __shfl_xor_sync(kAll, vn[i], o));
+#pragma unroll
+          for (int g = 0; g < NG; ++g) {
+            const float dn = group_scale(vn, g), dold = group_scale(vref, g);
+            if (dn != dold) {
+              const float inv = __frcp_rn(dn);  // exact: dn is a power of two >= 2^-126
+              const float f = dold * inv;       // 0 when the group had no scale yet (its sums are 0)
+              vinv[g] = inv;
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  acc[nt][2 * g][e] *= f;
+                  acc[nt][2 * g + 1][e] *= f;
+                }
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < NG2; ++i) vref[i] = vn[i];
         }
       }
 
-      // O^T += V^T P'^T (integer codes, bf16 MMA). m-tile 2g + h, rows r / r + 8:
-      // head_dim 32 g + 4 r + 2 h (+ 1); keys k0, k0 + 1 (+ 8).
+      // P' = 2^7 p dv / Dref (fp32), one fp16 copy of P'^T per V scale group
+      float ra[NG], rb[NG];
 #pragma unroll
       for (int g = 0; g < NG; ++g) {
+        ra[g] = group_scale(vwa, g) * vinv[g];
+        rb[g] = group_scale(vwb, g) * vinv[g];
+      }
+      uint32_t pf[NG][NT][2];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const float m0 = (m[nt][0] == -INFINITY ? 0.f : m[nt][0]) - kHeadroom;
+        const float m1 = (m[nt][1] == -INFINITY ? 0.f : m[nt][1]) - kHeadroom;
+        const float p00 = ex2_approx(x[nt][0][0] - m0), p01 = ex2_approx(x[nt][0][1] - m0);  // column c=0: ka, kb
+        const float p10 = ex2_approx(x[nt][1][0] - m1), p11 = ex2_approx(x[nt][1][1] - m1);  // column c=1
+        add2(l[nt][0], l[nt][1], p00, p10);
+        add2(l[nt][0], l[nt][1], p01, p11);
+#pragma unroll
+        for (int g = 0; g < NG; ++g) {
+          float a0, a1, b0, b1;
+          mul2(a0, a1, p00, p10, ra[g], ra[g]);
+          mul2(b0, b1, p01, p11, rb[g], rb[g]);
+          pf[g][nt][0] = movmatrix_trans(pack_f16x2(a0, a1));
+          pf[g][nt][1] = movmatrix_trans(pack_f16x2(b0, b1));
+        }
+      }
+
+      // O^T += V^T P'^T over the offset codes, then -offset * P' sums; m-tile
+      // 2g + h, rows r / r + 8: head_dim 32 g + 4 r + 2 h (+ 1); keys k0, k0 + 1 (+ 8).
+#pragma unroll
+      for (int g = 0; g < NG; ++g) {
+        uint32_t af0[4], af1[4];
         if constexpr (BITS == 8) {
           const int col = 32 * g + 4 * r;
-          const uint32_t u0 = lds32(vc + code_off<RB>(k0, col)) ^ 0x80808080u;
-          const uint32_t u1 = lds32(vc + code_off<RB>(k0 + 1, col)) ^ 0x80808080u;
-          const uint32_t u8 = lds32(vc + code_off<RB>(k0 + 8, col)) ^ 0x80808080u;
-          const uint32_t u9 = lds32(vc + code_off<RB>(k0 + 9, col)) ^ 0x80808080u;
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            uint32_t af[4];
-            af[0] = codes_to_bf16_pair(u0, u1, 2 * h);
-            af[1] = codes_to_bf16_pair(u0, u1, 2 * h + 1);
-            af[2] = codes_to_bf16_pair(u8, u9, 2 * h);
-            af[3] = codes_to_bf16_pair(u8, u9, 2 * h + 1);
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(acc[nt][2 * g + h], af, pf[g][nt][0], pf[g][nt][1]);
-          }
+          const uint32_t u0 = lds32(vc + code_off<RB>(k0, col));
+          const uint32_t u1 = lds32(vc + code_off<RB>(k0 + 1, col));
+          const uint32_t u8 = lds32(vc + code_off<RB>(k0 + 8, col));
+          const uint32_t u9 = lds32(vc + code_off<RB>(k0 + 9, col));
+          af0[0] = code_pair_f16_off<0>(u0, u1);
+          af0[1] = code_pair_f16_off<1>(u0, u1);
+          af0[2] = code_pair_f16_off<0>(u8, u9);
+          af0[3] = code_pair_f16_off<1>(u8, u9);
+          af1[0] = code_pair_f16_off<2>(u0, u1);
+          af1[1] = code_pair_f16_off<3>(u0, u1);
+          af1[2] = code_pair_f16_off<2>(u8, u9);
+          af1[3] = code_pair_f16_off<3>(u8, u9);
         } else {
           // the four codes of dims 32 g + 4 r .. + 3 of a key are one 16-bit word (byte 16 g + 2 r)
           const int col = 16 * g + 2 * r;
-          const uint32_t x01 = (lds16(vc + code_off<RB>(k0, col)) | (lds16(vc + code_off<RB>(k0 + 1, col)) << 16)) ^
-                               0x88888888u;
-          const uint32_t x89 =
-              (lds16(vc + code_off<RB>(k0 + 8, col)) | (lds16(vc + code_off<RB>(k0 + 9, col)) << 16)) ^ 0x88888888u;
+          const uint32_t x01 = lds16(vc + code_off<RB>(k0, col)) | (lds16(vc + code_off<RB>(k0 + 1, col)) << 16);
+          const uint32_t x89 = lds16(vc + code_off<RB>(k0 + 8, col)) | (lds16(vc + code_off<RB>(k0 + 9, col)) << 16);
+          af0[0] = nibble_pair_f16_off<0>(x01);
+          af0[1] = nibble_pair_f16_off<1>(x01);
+          af0[2] = nibble_pair_f16_off<0>(x89);
+          af0[3] = nibble_pair_f16_off<1>(x89);
+          af1[0] = nibble_pair_f16_off<2>(x01);
+          af1[1] = nibble_pair_f16_off<3>(x01);
+          af1[2] = nibble_pair_f16_off<2>(x89);
+          af1[3] = nibble_pair_f16_off<3>(x89);
+        }
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            uint32_t af[4];
-            af[0] = nibble_pair_to_bf16(x01, 2 * h);
-            af[1] = nibble_pair_to_bf16(x01, 2 * h + 1);
-            af[2] = nibble_pair_to_bf16(x89, 2 * h);
-            af[3] = nibble_pair_to_bf16(x89, 2 * h + 1);
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(acc[nt][2 * g + h], af, pf[g][nt][0], pf[g][nt][1]);
-          }
+        for (int nt = 0; nt < NT; ++nt) {
+          mma_f16_16816(acc[nt][2 * g], af0, pf[g][nt][0], pf[g][nt][1]);
+          mma_f16_16816(acc[nt][2 * g + 1], af1, pf[g][nt][0], pf[g][nt][1]);
+          mma_f16_16816(acc[nt][2 * g], kNegOff, pf[g][nt][0], pf[g][nt][1]);
+          mma_f16_16816(acc[nt][2 * g + 1], kNegOff, pf[g][nt][0], pf[g][nt][1]);
         }
       }
       __syncwarp();  // every read of this stage is consumed before the ring refills it
@@ -690,28 +786,39 @@ __global__ void __launch_bounds__(NW * 32, 1)
           const int col = nt * 8 + jq * 2 + c;
           if (col < nrows * G) {
             const int i = MULTI ? col / G : 0, hh = MULTI ? col % G : col;
+            // o = acc * Dref: sum over keys of p dv code, times 2^7
+            float o[NG][4];
+#pragma unroll
+            for (int g = 0; g < NG; ++g) {
+              const float d = group_scale(vref, g);
+              o[g][0] = acc[nt][2 * g][c] * d;
+              o[g][1] = acc[nt][2 * g][c + 2] * d;
+              o[g][2] = acc[nt][2 * g + 1][c] * d;
+              o[g][3] = acc[nt][2 * g + 1][c + 2] * d;
+            }
             if (A.pbase < 0) {
               __nv_bfloat16 *out = reinterpret_cast<__nv_bfloat16 *>(a.out) +
                                    ((static_cast<size_t>(A.row0) + i) * a.num_q_heads + hbase + hh) * D + 4 * r;
-              const float inv = 1.f / l[nt][c];
+              const float inv = 1.f / l[nt][c];  // l also carries the 2^7
 #pragma unroll
               for (int g = 0; g < NG; ++g) {
                 uint2 pk;
-                pk.x = pack_bf16x2(acc[nt][2 * g][c] * inv, acc[nt][2 * g][c + 2] * inv);
-                pk.y = pack_bf16x2(acc[nt][2 * g + 1][c] * inv, acc[nt][2 * g + 1][c + 2] * inv);
+                pk.x = pack_bf16x2(o[g][0] * inv, o[g][1] * inv);
+                pk.y = pack_bf16x2(o[g][2] * inv, o[g][3] * inv);
                 *reinterpret_cast<uint2 *>(out + 32 * g) = pk;
               }
             } else {
+              // span partials in the merge's units: sums of p dv code and of p
+              constexpr float kDown = 1.f / 128.f;
               const size_t pi = (static_cast<size_t>(A.pbase + A.span * nrows + i) * a.num_q_heads + hbase + hh);
               float *pacc = a.partial_acc + pi * D + 4 * r;
 #pragma unroll
               for (int g = 0; g < NG; ++g)
                 *reinterpret_cast<float4 *>(pacc + 32 * g) =
-                    make_float4(acc[nt][2 * g][c], acc[nt][2 * g][c + 2], acc[nt][2 * g + 1][c],
-                                acc[nt][2 * g + 1][c + 2]);
+                    make_float4(o[g][0] * kDown, o[g][1] * kDown, o[g][2] * kDown, o[g][3] * kDown);
               if (r == 0) {
                 a.partial_ml[pi * 2] = m[nt][c];
-                a.partial_ml[pi * 2 + 1] = l[nt][c];
+                a.partial_ml[pi * 2 + 1] = l[nt][c] * kDown;
               }
             }
           }
@@ -735,21 +842,8 @@ __global__ void __launch_bounds__(NW * 32, 1)
     pb = 0;
     if (A.t >= 0) {
       if (!A.finalized) finalize(A, a, lane, 8 * NT, kMaxRows);
-      if (qB_loaded) {
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          invA[nt] = invB[nt];
-#pragma unroll
-          for (int kk = 0; kk < KT; ++kk) {
-            qA[nt][kk][0] = qB[nt][kk][0];
-            qA[nt][kk][1] = qB[nt][kk][1];
-          }
-        }
-      } else if (A.ok) {
-        load_q_quant<D, NT, MULTI, BITS>(qA, invA, A, a, lane);
-      }
+      if (A.ok) load_q_quant<D, NT, MULTI, BITS>(qA, invA, A, a, lane);
     }
-    qB_loaded = false;
     expand(B, next_t < num_tasks ? next_t : -1, rawC, a, lane);
     tC = after;
     if (tC < num_tasks) rawC = load_item(items, tC, hkv);
