@@ -360,7 +360,7 @@ __device__ __forceinline__ void prefetch_q(const Task &T, const StepArgs &a, int
 // the group's 32 query values (the fp16 values the MMA reads) of columns
 // 2 (lane % 4) + c, which removes the code offset from the group's dot product.
 template <int D, int NT, int BITS>
-__device__ __forceinline__ void key_offsets(float (&kinit)[D / 32][NT][2], const uint32_t (&qf)[NT][D / 16][2],
+__device__ __forceinline__ void key_offsets(float (&kinit)[D / 32][NT][4], const uint32_t (&qf)[NT][D / 16][2],
                                             int lane) {
   const int jq = lane & 3;
 #pragma unroll
@@ -377,8 +377,9 @@ __device__ __forceinline__ void key_offsets(float (&kinit)[D / 32][NT][2], const
         }
       s += __shfl_xor_sync(kAll, s, 1);  // the four threads of a column hold its 32 values
       s += __shfl_xor_sync(kAll, s, 2);
-      kinit[g][nt][0] = -kCodeOffset<BITS> * __shfl_sync(kAll, s, (2 * jq) * 4);
-      kinit[g][nt][1] = -kCodeOffset<BITS> * __shfl_sync(kAll, s, (2 * jq + 1) * 4);
+      // the accumulator layout: (key ka, column 2 jq), (ka, 2 jq + 1), (kb, 2 jq), (kb, 2 jq + 1)
+      kinit[g][nt][0] = kinit[g][nt][2] = -kCodeOffset<BITS> * __shfl_sync(kAll, s, (2 * jq) * 4);
+      kinit[g][nt][1] = kinit[g][nt][3] = -kCodeOffset<BITS> * __shfl_sync(kAll, s, (2 * jq + 1) * 4);
     }
 }
 
@@ -491,6 +492,10 @@ __global__ void __launch_bounds__(NW * 32, 1)
   const int ka = lane >> 2, kb = ka + 8, jq = lane & 3, k0 = jq * 2, r = lane >> 2;
   // per-thread code offsets inside a sub-tile (rows kb = ka + 8 and k0 + 8 share the swizzle phase)
   const uint32_t koff = code_off<RB>(ka, 4 * jq);  // + group/half chunk below
+  // V codes of group 0 (dims 4 r .. + 3) in rows k0 and k0 + 1; group g XORs g << kGroupShift into the chunk bits
+  constexpr int kGroupShift = BITS == 8 ? 5 : 4;  // 32 or 16 bytes of codes per scale group
+  const uint32_t voff0 = code_off<RB>(k0, BITS == 8 ? 4 * r : 2 * r);
+  const uint32_t voff1 = code_off<RB>(k0 + 1, BITS == 8 ? 4 * r : 2 * r);
   // fp16 pairs of -offset (-1152 or -1032): A of the MMA that takes the code offset out of O^T
   constexpr uint32_t kNegOffBits = BITS == 8 ? 0xE480E480u : 0xE408E408u;
   const uint32_t kNegOff[4] = {kNegOffBits, kNegOffBits, kNegOffBits, kNegOffBits};
@@ -502,9 +507,12 @@ __global__ void __launch_bounds__(NW * 32, 1)
     uint32_t claim = 0;
     if (counter && tC < num_tasks && lane == 0) claim = atomicAdd(counter, 1u);
     float m[NT][2], l[NT][2], acc[NT][KT][4];
+    float mr[NT][2], m0h[NT][2];  // per column: m + the lazy margin, and (m, 0 before any key) - headroom
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       m[nt][0] = m[nt][1] = -INFINITY;
+      mr[nt][0] = mr[nt][1] = -INFINITY;
+      m0h[nt][0] = m0h[nt][1] = -kHeadroom;
       l[nt][0] = l[nt][1] = 0.f;
 #pragma unroll
       for (int mt = 0; mt < KT; ++mt) acc[nt][mt][0] = acc[nt][mt][1] = acc[nt][mt][2] = acc[nt][mt][3] = 0.f;
@@ -516,7 +524,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
     for (int i = 0; i < NG2; ++i) vref[i] = 0u;
 #pragma unroll
     for (int g = 0; g < NG; ++g) vinv[g] = 0.f;
-    float kinit[NG][NT][2];
+    float kinit[NG][NT][4];
     key_offsets<D, NT, BITS>(kinit, qA, lane);
     const int nrows = MULTI ? A.nrows : 1;
     uint32_t colrow = 0;
@@ -547,7 +555,9 @@ __global__ void __launch_bounds__(NW * 32, 1)
       const int kbase = A.key0 + u * kSubKeys;
       const int v = row >= 0 ? min(kSubKeys, A.key1 - kbase) : 0;
       const int vis0 = A.L - nrows - kbase + 1;
-      const uint32_t kc = ring_addr + stage * Cfg::kCodeBytes;
+      // this thread's K words of rows ka (and kb, 8 rows on) at chunk 0; a chunk index is XORed into
+      // the swizzled chunk bits (the stage base is a multiple of 128)
+      const uint32_t kbase0 = ring_addr + stage * Cfg::kCodeBytes + koff;
       const uint32_t vc = ring_addr + Cfg::kVc + stage * Cfg::kCodeBytes;
       const uint32_t ks = ring_addr + Cfg::kKs + stage * Cfg::kScaleBytes;
       const uint32_t vs = ring_addr + Cfg::kVs + stage * Cfg::kScaleBytes;
@@ -577,38 +587,40 @@ __global__ void __launch_bounds__(NW * 32, 1)
       for (int nt = 0; nt < NT; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
 #pragma unroll
       for (int g = 0; g < NG; ++g) {
-        float sg[NT][4];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          sg[nt][0] = sg[nt][2] = kinit[g][nt][0];
-          sg[nt][1] = sg[nt][3] = kinit[g][nt][1];
-        }
+        float sg[NT][4];  // the group's first MMA starts from kinit (no copy: kinit lives on)
         if constexpr (BITS == 8) {
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             // chunk 2g + h of rows ka / kb: the swizzle XORs the chunk index
             const int kk = 2 * g + h;
-            const uint32_t off = koff ^ (static_cast<uint32_t>(kk) << 4);
-            const uint32_t wa = lds32(kc + off);
-            const uint32_t wb = lds32(kc + off + 8 * RB);
+            const uint32_t ka_addr = kbase0 ^ (static_cast<uint32_t>(kk) << 4);
+            const uint32_t wa = lds32(ka_addr);
+            const uint32_t wb = lds32(ka_addr + 8 * RB);
             uint32_t af[4];
             codes_to_f16_off(wa, af[0], af[2]);
             codes_to_f16_off(wb, af[1], af[3]);
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) mma_f16_16816(sg[nt], af, qA[nt][kk][0], qA[nt][kk][1]);
+            for (int nt = 0; nt < NT; ++nt) {
+              if (h == 0)
+                mma_f16_16816_from(sg[nt], af, qA[nt][kk][0], qA[nt][kk][1], kinit[g][nt][0], kinit[g][nt][1],
+                                   kinit[g][nt][2], kinit[g][nt][3]);
+              else
+                mma_f16_16816(sg[nt], af, qA[nt][kk][0], qA[nt][kk][1]);
+            }
           }
         } else {
           // chunk g of rows ka / kb holds dims 32 g .. 32 g + 31; this thread's word holds dims 32 g + 8 jq + 0..7
-          const uint32_t off = koff ^ (static_cast<uint32_t>(g) << 4);
-          const uint32_t wa = lds32(kc + off);
-          const uint32_t wb = lds32(kc + off + 8 * RB);
+          const uint32_t ka_addr = kbase0 ^ (static_cast<uint32_t>(g) << 4);
+          const uint32_t wa = lds32(ka_addr);
+          const uint32_t wb = lds32(ka_addr + 8 * RB);
           const uint32_t a0[4] = {nibble_pair_f16_off<0>(wa), nibble_pair_f16_off<0>(wb), nibble_pair_f16_off<1>(wa),
                                   nibble_pair_f16_off<1>(wb)};
           const uint32_t a1[4] = {nibble_pair_f16_off<2>(wa), nibble_pair_f16_off<2>(wb), nibble_pair_f16_off<3>(wa),
                                   nibble_pair_f16_off<3>(wb)};
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
-            mma_f16_16816(sg[nt], a0, qA[nt][2 * g][0], qA[nt][2 * g][1]);
+            mma_f16_16816_from(sg[nt], a0, qA[nt][2 * g][0], qA[nt][2 * g][1], kinit[g][nt][0], kinit[g][nt][1],
+                               kinit[g][nt][2], kinit[g][nt][3]);
             mma_f16_16816(sg[nt], a1, qA[nt][2 * g + 1][0], qA[nt][2 * g + 1][1]);
           }
         }
@@ -632,7 +644,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
           const int vis = MULTI ? min(v, vis0 + static_cast<int>((colrow >> (8 * (nt * 2 + c))) & 0xFF)) : v;
           x[nt][c][0] = ka < vis ? sacc[nt][c] * sl2c[nt][c] : -INFINITY;
           x[nt][c][1] = kb < vis ? sacc[nt][c + 2] * sl2c[nt][c] : -INFINITY;
-          need |= fmaxf(x[nt][c][0], x[nt][c][1]) > m[nt][c] + kRescaleQuant;
+          need |= fmaxf(x[nt][c][0], x[nt][c][1]) > mr[nt][c];
         }
       if (__any_sync(kAll, need)) {
 #pragma unroll
@@ -643,9 +655,11 @@ __global__ void __launch_bounds__(NW * 32, 1)
             t = fmaxf(t, __shfl_xor_sync(kAll, t, 4));
             t = fmaxf(t, __shfl_xor_sync(kAll, t, 8));
             t = fmaxf(t, __shfl_xor_sync(kAll, t, 16));
-            if (t > m[nt][c] + kRescaleQuant) {
+            if (t > mr[nt][c]) {
               const float corr = ex2_approx(m[nt][c] - t);
               m[nt][c] = t;
+              mr[nt][c] = t + kRescaleQuant;
+              m0h[nt][c] = t - kHeadroom;
               l[nt][c] *= corr;
 #pragma unroll
               for (int mt = 0; mt < KT; ++mt) {
@@ -693,15 +707,14 @@ __global__ void __launch_bounds__(NW * 32, 1)
       // P' = 2^7 p dv / Dref (fp32), one fp16 copy of P'^T per V scale group
       float ra[NG], rb[NG];
 #pragma unroll
-      for (int g = 0; g < NG; ++g) {
-        ra[g] = group_scale(vwa, g) * vinv[g];
-        rb[g] = group_scale(vwb, g) * vinv[g];
+      for (int i = 0; i < NG2; ++i) {
+        mul2(ra[2 * i], ra[2 * i + 1], group_scale(vwa, 2 * i), group_scale(vwa, 2 * i + 1), vinv[2 * i], vinv[2 * i + 1]);
+        mul2(rb[2 * i], rb[2 * i + 1], group_scale(vwb, 2 * i), group_scale(vwb, 2 * i + 1), vinv[2 * i], vinv[2 * i + 1]);
       }
       uint32_t pf[NG][NT][2];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
-        const float m0 = (m[nt][0] == -INFINITY ? 0.f : m[nt][0]) - kHeadroom;
-        const float m1 = (m[nt][1] == -INFINITY ? 0.f : m[nt][1]) - kHeadroom;
+        const float m0 = m0h[nt][0], m1 = m0h[nt][1];
         const float p00 = ex2_approx(x[nt][0][0] - m0), p01 = ex2_approx(x[nt][0][1] - m0);  // column c=0: ka, kb
         const float p10 = ex2_approx(x[nt][1][0] - m1), p11 = ex2_approx(x[nt][1][1] - m1);  // column c=1
         add2(l[nt][0], l[nt][1], p00, p10);
@@ -718,15 +731,20 @@ __global__ void __launch_bounds__(NW * 32, 1)
 
       // O^T += V^T P'^T over the offset codes, then -offset * P' sums; m-tile
       // 2g + h, rows r / r + 8: head_dim 32 g + 4 r + 2 h (+ 1); keys k0, k0 + 1 (+ 8).
+      // rows k0 and k0 + 1 of group 0; a group's chunk differs only in the
+      // bits the swizzle XORs (the stage base is a multiple of 128), and rows
+      // k0 + 8, k0 + 9 sit 8 rows further with the same swizzle phase
+      const uint32_t va0 = vc + voff0, va1 = vc + voff1;
 #pragma unroll
       for (int g = 0; g < NG; ++g) {
         uint32_t af0[4], af1[4];
+        const uint32_t ga0 = va0 ^ (static_cast<uint32_t>(g) << kGroupShift);
+        const uint32_t ga1 = va1 ^ (static_cast<uint32_t>(g) << kGroupShift);
         if constexpr (BITS == 8) {
-          const int col = 32 * g + 4 * r;
-          const uint32_t u0 = lds32(vc + code_off<RB>(k0, col));
-          const uint32_t u1 = lds32(vc + code_off<RB>(k0 + 1, col));
-          const uint32_t u8 = lds32(vc + code_off<RB>(k0 + 8, col));
-          const uint32_t u9 = lds32(vc + code_off<RB>(k0 + 9, col));
+          const uint32_t u0 = lds32(ga0);
+          const uint32_t u1 = lds32(ga1);
+          const uint32_t u8 = lds32(ga0 + 8 * RB);
+          const uint32_t u9 = lds32(ga1 + 8 * RB);
           af0[0] = code_pair_f16_off<0>(u0, u1);
           af0[1] = code_pair_f16_off<1>(u0, u1);
           af0[2] = code_pair_f16_off<0>(u8, u9);
@@ -737,9 +755,8 @@ __global__ void __launch_bounds__(NW * 32, 1)
           af1[3] = code_pair_f16_off<3>(u8, u9);
         } else {
           // the four codes of dims 32 g + 4 r .. + 3 of a key are one 16-bit word (byte 16 g + 2 r)
-          const int col = 16 * g + 2 * r;
-          const uint32_t x01 = lds16(vc + code_off<RB>(k0, col)) | (lds16(vc + code_off<RB>(k0 + 1, col)) << 16);
-          const uint32_t x89 = lds16(vc + code_off<RB>(k0 + 8, col)) | (lds16(vc + code_off<RB>(k0 + 9, col)) << 16);
+          const uint32_t x01 = lds16(ga0) | (lds16(ga1) << 16);
+          const uint32_t x89 = lds16(ga0 + 8 * RB) | (lds16(ga1 + 8 * RB) << 16);
           af0[0] = nibble_pair_f16_off<0>(x01);
           af0[1] = nibble_pair_f16_off<1>(x01);
           af0[2] = nibble_pair_f16_off<0>(x89);
