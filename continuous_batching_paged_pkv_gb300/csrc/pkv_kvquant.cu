@@ -47,6 +47,9 @@
 // words of codes: the permutation is undone in the output address, and for
 // 4-bit K by loading q in the same order (a thread's K word holds dims
 // 32 g + 8 j .. + 7, paired (0, 4), (1, 5), (2, 6), (3, 7) in the MMA).
+// 4-bit codes in odd nibbles are placed without a shift as 1152 + 16 c: for
+// K the matching q values are taken at 1/16 (exact), for V the offset MMA
+// takes 1152 on those rows and the output takes 1/16 of them.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -263,11 +266,12 @@ __device__ __forceinline__ uint32_t code_pair_f16_off(uint32_t x, uint32_t y) {
   return (prmt(x, y, sel) & 0x00FF00FFu) ^ 0x64806480u;
 }
 
-// Nibble S of both 16-bit halves of x (4-bit codes) -> the fp16 pair of 1032 + code.
-template <int S>
-__device__ __forceinline__ uint32_t nibble_pair_f16_off(uint32_t x) {
-  return ((x >> (4 * S)) & 0x000F000Fu) ^ 0x64086408u;
-}
+// Nibble 0 of both 16-bit halves of x (4-bit codes) -> the fp16 pair of 1032 + code.
+__device__ __forceinline__ uint32_t nibble_lo_f16_off(uint32_t x) { return (x & 0x000F000Fu) ^ 0x64086408u; }
+
+// Nibble 1 of both 16-bit halves of x -> the fp16 pair of 1152 + 16 code (the
+// nibble, XOR 8, lands in mantissa bits 4..7 under the exponent of 1024.0).
+__device__ __forceinline__ uint32_t nibble_hi_f16_off(uint32_t x) { return (x & 0x00F000F0u) ^ 0x64806480u; }
 
 // Scale of group g from bf16 pairs packed two per word, as fp32.
 template <int G2>
@@ -331,8 +335,9 @@ __device__ __forceinline__ void load_q_quant(uint32_t (&qf)[NT][D / 16][2], floa
     for (int kk = 0; kk < KT; ++kk)
 #pragma unroll
       for (int b = 0; b < 2; ++b) {
-        __half2 v = __floats2half2_rn(bf16_bits_to_float(raw[kk][b] & 0xFFFFu) * f,
-                                      bf16_bits_to_float(raw[kk][b] >> 16) * f);
+        const float fb = BITS == 4 && b == 1 ? f * 0.0625f : f;  // 4-bit odd nibbles enter as 16 c
+        __half2 v = __floats2half2_rn(bf16_bits_to_float(raw[kk][b] & 0xFFFFu) * fb,
+                                      bf16_bits_to_float(raw[kk][b] >> 16) * fb);
         qf[nt][kk][b] = *reinterpret_cast<uint32_t *>(&v);
       }
   }
@@ -367,19 +372,21 @@ __device__ __forceinline__ void key_offsets(float (&kinit)[D / 32][NT][4], const
   for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
     for (int g = 0; g < D / 32; ++g) {
+      // first registers of a k-step meet codes at offset kCodeOffset, second
+      // ones 1152 (4-bit odd nibbles, whose q values are at 1/16)
       float s = 0.f;
 #pragma unroll
       for (int h = 0; h < 2; ++h)
 #pragma unroll
         for (int b = 0; b < 2; ++b) {
           const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&qf[nt][2 * g + h][b]));
-          s += f.x + f.y;
+          s += (b == 0 ? kCodeOffset<BITS> : 1152.f) * (f.x + f.y);
         }
       s += __shfl_xor_sync(kAll, s, 1);  // the four threads of a column hold its 32 values
       s += __shfl_xor_sync(kAll, s, 2);
       // the accumulator layout: (key ka, column 2 jq), (ka, 2 jq + 1), (kb, 2 jq), (kb, 2 jq + 1)
-      kinit[g][nt][0] = kinit[g][nt][2] = -kCodeOffset<BITS> * __shfl_sync(kAll, s, (2 * jq) * 4);
-      kinit[g][nt][1] = kinit[g][nt][3] = -kCodeOffset<BITS> * __shfl_sync(kAll, s, (2 * jq + 1) * 4);
+      kinit[g][nt][0] = kinit[g][nt][2] = -__shfl_sync(kAll, s, (2 * jq) * 4);
+      kinit[g][nt][1] = kinit[g][nt][3] = -__shfl_sync(kAll, s, (2 * jq + 1) * 4);
     }
 }
 
@@ -497,8 +504,9 @@ __global__ void __launch_bounds__(NW * 32, 1)
   const uint32_t voff0 = code_off<RB>(k0, BITS == 8 ? 4 * r : 2 * r);
   const uint32_t voff1 = code_off<RB>(k0 + 1, BITS == 8 ? 4 * r : 2 * r);
   // fp16 pairs of -offset (-1152 or -1032): A of the MMA that takes the code offset out of O^T
-  constexpr uint32_t kNegOffBits = BITS == 8 ? 0xE480E480u : 0xE408E408u;
-  const uint32_t kNegOff[4] = {kNegOffBits, kNegOffBits, kNegOffBits, kNegOffBits};
+  // (rows r + 8 of a 4-bit m-tile hold odd nibbles, at 1152 + 16 c)
+  constexpr uint32_t kNegOffLo = BITS == 8 ? 0xE480E480u : 0xE408E408u;
+  const uint32_t kNegOff[4] = {kNegOffLo, 0xE480E480u, kNegOffLo, 0xE480E480u};
   int cstage = 0;
   uint32_t cphase = 0;
 
@@ -613,10 +621,11 @@ __global__ void __launch_bounds__(NW * 32, 1)
           const uint32_t ka_addr = kbase0 ^ (static_cast<uint32_t>(g) << 4);
           const uint32_t wa = lds32(ka_addr);
           const uint32_t wb = lds32(ka_addr + 8 * RB);
-          const uint32_t a0[4] = {nibble_pair_f16_off<0>(wa), nibble_pair_f16_off<0>(wb), nibble_pair_f16_off<1>(wa),
-                                  nibble_pair_f16_off<1>(wb)};
-          const uint32_t a1[4] = {nibble_pair_f16_off<2>(wa), nibble_pair_f16_off<2>(wb), nibble_pair_f16_off<3>(wa),
-                                  nibble_pair_f16_off<3>(wb)};
+          const uint32_t wa8 = wa >> 8, wb8 = wb >> 8;  // nibbles 2, 3 (and 6, 7) into place
+          const uint32_t a0[4] = {nibble_lo_f16_off(wa), nibble_lo_f16_off(wb), nibble_hi_f16_off(wa),
+                                  nibble_hi_f16_off(wb)};
+          const uint32_t a1[4] = {nibble_lo_f16_off(wa8), nibble_lo_f16_off(wb8), nibble_hi_f16_off(wa8),
+                                  nibble_hi_f16_off(wb8)};
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
             mma_f16_16816_from(sg[nt], a0, qA[nt][2 * g][0], qA[nt][2 * g][1], kinit[g][nt][0], kinit[g][nt][1],
@@ -757,14 +766,15 @@ __global__ void __launch_bounds__(NW * 32, 1)
           // the four codes of dims 32 g + 4 r .. + 3 of a key are one 16-bit word (byte 16 g + 2 r)
           const uint32_t x01 = lds16(ga0) | (lds16(ga1) << 16);
           const uint32_t x89 = lds16(ga0 + 8 * RB) | (lds16(ga1 + 8 * RB) << 16);
-          af0[0] = nibble_pair_f16_off<0>(x01);
-          af0[1] = nibble_pair_f16_off<1>(x01);
-          af0[2] = nibble_pair_f16_off<0>(x89);
-          af0[3] = nibble_pair_f16_off<1>(x89);
-          af1[0] = nibble_pair_f16_off<2>(x01);
-          af1[1] = nibble_pair_f16_off<3>(x01);
-          af1[2] = nibble_pair_f16_off<2>(x89);
-          af1[3] = nibble_pair_f16_off<3>(x89);
+          const uint32_t y01 = x01 >> 8, y89 = x89 >> 8;  // nibbles 2, 3 into place
+          af0[0] = nibble_lo_f16_off(x01);
+          af0[1] = nibble_hi_f16_off(x01);  // rows r + 8: 16 c
+          af0[2] = nibble_lo_f16_off(x89);
+          af0[3] = nibble_hi_f16_off(x89);
+          af1[0] = nibble_lo_f16_off(y01);
+          af1[1] = nibble_hi_f16_off(y01);
+          af1[2] = nibble_lo_f16_off(y89);
+          af1[3] = nibble_hi_f16_off(y89);
         }
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
@@ -808,10 +818,11 @@ __global__ void __launch_bounds__(NW * 32, 1)
 #pragma unroll
             for (int g = 0; g < NG; ++g) {
               const float d = group_scale(vref, g);
+              const float d8 = BITS == 4 ? d * 0.0625f : d;  // rows r + 8 of 4-bit codes carry 16 c
               o[g][0] = acc[nt][2 * g][c] * d;
-              o[g][1] = acc[nt][2 * g][c + 2] * d;
+              o[g][1] = acc[nt][2 * g][c + 2] * d8;
               o[g][2] = acc[nt][2 * g + 1][c] * d;
-              o[g][3] = acc[nt][2 * g + 1][c + 2] * d;
+              o[g][3] = acc[nt][2 * g + 1][c + 2] * d8;
             }
             if (A.pbase < 0) {
               __nv_bfloat16 *out = reinterpret_cast<__nv_bfloat16 *>(a.out) +
