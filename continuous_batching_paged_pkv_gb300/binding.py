@@ -47,7 +47,8 @@ class WorkInfo(ctypes.Structure):
                 ("num_combine_items", ctypes.c_int32), ("num_partials", ctypes.c_int32),
                 ("work_words", ctypes.c_int64), ("workspace_bytes", ctypes.c_uint64),
                 ("decode_rows_max", ctypes.c_int32), ("num_scratch_items", ctypes.c_int32),
-                ("scratch_blocks", ctypes.c_int64), ("workspace_bytes_q8", ctypes.c_uint64)]
+                ("scratch_blocks", ctypes.c_int64), ("workspace_bytes_q8", ctypes.c_uint64),
+                ("num_long_combine_items", ctypes.c_int32)]
 
 
 class StageLayout(ctypes.Structure):

@@ -181,6 +181,8 @@ pkv_status pkv_attention(const void *q, const int32_t *cu_seqlens_q, int32_t num
   if (need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 256)))
     return PKV_ERR_WORKSPACE_TOO_SMALL;
   if ((info->num_combine_items > 0) != (info->num_partials > 0)) return PKV_ERR_INVALID_ARG;
+  if (info->num_long_combine_items < 0 || info->num_long_combine_items > info->num_combine_items)
+    return PKV_ERR_INVALID_ARG;
   // a decode-path segment's (row, q head) columns fit one 16-column tile
   if (info->decode_rows_max < 0 ||
       (info->num_decode_items > 0 && info->decode_rows_max * (num_q_heads / num_kv_heads) > 16))
@@ -245,7 +247,7 @@ pkv_status pkv_attention(const void *q, const int32_t *cu_seqlens_q, int32_t num
   cudaStream_t dst = side ? side->stream : st;
   if (e == cudaSuccess && side) e = cudaStreamWaitEvent(side->stream, side->fork, 0);
   if (e == cudaSuccess) e = pkv::launch_decode(a, tk, tv, info->num_decode_items, dec, beside, dst);
-  if (e == cudaSuccess) e = pkv::launch_merge(a, info->num_combine_items, comb, dst);
+  if (e == cudaSuccess) e = pkv::launch_merge(a, info->num_combine_items, info->num_long_combine_items, comb, dst);
   if (side) {
     // join even after a failed launch, so the caller's stream never runs ahead of queued work
     const cudaError_t j = cudaEventRecord(side->join, side->stream);
@@ -346,6 +348,8 @@ static pkv_status attention_quant(int32_t bits, const void *q, const int32_t *cu
   if (need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 256)))
     return PKV_ERR_WORKSPACE_TOO_SMALL;
   if ((info->num_combine_items > 0) != (info->num_partials > 0)) return PKV_ERR_INVALID_ARG;
+  if (info->num_long_combine_items < 0 || info->num_long_combine_items > info->num_combine_items)
+    return PKV_ERR_INVALID_ARG;
   if (info->decode_rows_max < 0 ||
       (info->num_decode_items > 0 && info->decode_rows_max * (num_q_heads / num_kv_heads) > 16))
     return PKV_ERR_INVALID_ARG;
@@ -430,7 +434,7 @@ static pkv_status attention_quant(int32_t bits, const void *q, const int32_t *cu
   if (e == cudaSuccess && side) e = cudaStreamWaitEvent(side->stream, side->fork, 0);
   if (e == cudaSuccess)
     e = pkv::launch_decode_quant(a, tkc, tvc, k_scales, v_scales, info->num_decode_items, dec, bits, dst);
-  if (e == cudaSuccess) e = pkv::launch_merge(a, info->num_combine_items, comb, dst);
+  if (e == cudaSuccess) e = pkv::launch_merge(a, info->num_combine_items, info->num_long_combine_items, comb, dst);
   if (side) {
     const cudaError_t j = cudaEventRecord(side->join, side->stream);
     const cudaError_t w = j == cudaSuccess ? cudaStreamWaitEvent(st, side->join, 0) : j;

@@ -489,8 +489,8 @@ struct MergeRow {
 };
 
 // Decode a merge item and check it against the step metadata.
-__device__ __forceinline__ MergeRow merge_row(const StepArgs &a, const int32_t *items) {
-  const int4 it = __ldg(reinterpret_cast<const int4 *>(items) + blockIdx.x);
+__device__ __forceinline__ MergeRow merge_row(const StepArgs &a, const int32_t *items, int item) {
+  const int4 it = __ldg(reinterpret_cast<const int4 *>(items) + item);
   // word 2: spans | row index << 16 | (rows - 1) << 24; word 3: the partial
   // entry of (span 0, this row); span s of the row is entry word3 + s * rows.
   MergeRow r;
@@ -545,17 +545,17 @@ __device__ __forceinline__ void store_merged(const StepArgs &a, int row, int h, 
 // ...; the column's maximum and its ordered group sums go across the four
 // lanes by shuffles. 128 threads hold D / 4 columns x 4 lanes of 128 / D q heads.
 template <int D>
-__global__ void __launch_bounds__(kMergeThreads) merge_small_kernel(const StepArgs a,
-                                                                    const int32_t *__restrict__ items) {
+__device__ __forceinline__ void merge_small_body(const StepArgs &a, const int32_t *__restrict__ items, int item,
+                                                 int head_group) {
   constexpr int F = D / 4;             // float4 columns per q head
   constexpr int WPH = F / 8;           // warps per q head (8 columns per warp)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int h = blockIdx.y * (kMergeThreads / (4 * F)) + warp / WPH;
+  const int h = head_group * (kMergeThreads / (4 * F)) + warp / WPH;
   const int col = (warp % WPH) * 8 + (lane >> 2), w = lane & 3;
   // The work item and step metadata are final when this grid starts (the
   // decode kernel starts only after everything before the cache write has
   // finished); only the partials need the decode grid to finish (the wait below).
-  const MergeRow r = merge_row(a, items);
+  const MergeRow r = merge_row(a, items, item);
   grid_dependency_wait();  // partials come from the decode kernel
   if (r.bad) {
     if (threadIdx.x == 0 && a.status) atomicOr(a.status, PKV_DEV_BAD_SEGMENT);
@@ -627,19 +627,25 @@ __global__ void __launch_bounds__(kMergeThreads) merge_small_kernel(const StepAr
   if (w == 0) store_merged<D>(a, r.row, h, col, lt, at);
 }
 
+template <int D>
+__global__ void __launch_bounds__(kMergeThreads) merge_small_kernel(const StepArgs a,
+                                                                    const int32_t *__restrict__ items) {
+  merge_small_body<D>(a, items, blockIdx.x, blockIdx.y);
+}
+
 // One thread per float4 column; 128 threads hold 128 / (D / 4) q heads. The
 // CTA stages its heads' (max, denominator) pairs kPiece spans at a time in
 // shared memory; each thread reads the maxima from there, then folds its
 // groups in order, each group's eight sums loaded at once.
 template <int D>
-__global__ void __launch_bounds__(kMergeThreads) merge_wide_kernel(const StepArgs a,
-                                                                   const int32_t *__restrict__ items) {
+__device__ __forceinline__ void merge_wide_body(const StepArgs &a, const int32_t *__restrict__ items, int item,
+                                                int head_group) {
   constexpr int F = D / 4;                // float4 columns per q head
   constexpr int HPC = kMergeThreads / F;  // q heads per CTA
   __shared__ float s_m[HPC][kPiece], s_l[HPC][kPiece];
   const int hl = static_cast<int>(threadIdx.x) / F, col = threadIdx.x % F;
-  const int h0 = blockIdx.y * HPC, h = h0 + hl;
-  const MergeRow r = merge_row(a, items);
+  const int h0 = head_group * HPC, h = h0 + hl;
+  const MergeRow r = merge_row(a, items, item);
   grid_dependency_wait();  // partials come from the decode kernel
   if (r.bad) {  // uniform over the CTA
     if (threadIdx.x == 0 && a.status) atomicOr(a.status, PKV_DEV_BAD_SEGMENT);
@@ -697,6 +703,26 @@ __global__ void __launch_bounds__(kMergeThreads) merge_wide_kernel(const StepArg
     }
   }
   if (live) store_merged<D>(a, r.row, h, col, lt, at);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kMergeThreads) merge_wide_kernel(const StepArgs a,
+                                                                   const int32_t *__restrict__ items) {
+  merge_wide_body<D>(a, items, blockIdx.x, blockIdx.y);
+}
+
+// Both layouts in one grid: the first `num_long` items (rows of more than two
+// span groups, first in the list) take four lanes per column, the rest one;
+// the grid's first long_ctas CTAs are the long items' (item, head group)s.
+template <int D>
+__global__ void __launch_bounds__(kMergeThreads) merge_mixed_kernel(const StepArgs a,
+                                                                    const int32_t *__restrict__ items,
+                                                                    int num_long, int long_groups, int wide_groups) {
+  const int b = static_cast<int>(blockIdx.x), long_ctas = num_long * long_groups;
+  if (b < long_ctas)
+    merge_small_body<D>(a, items, b / long_groups, b % long_groups);
+  else
+    merge_wide_body<D>(a, items, num_long + (b - long_ctas) / wide_groups, (b - long_ctas) % wide_groups);
 }
 
 int sm_count() {
@@ -776,22 +802,33 @@ cudaError_t launch_decode(const StepArgs &a, const CUtensorMap &tk, const CUtens
   }
 }
 
-cudaError_t launch_merge(const StepArgs &a, int32_t num_items, const int32_t *items, cudaStream_t stream) {
+cudaError_t launch_merge(const StepArgs &a, int32_t num_items, int32_t num_long, const int32_t *items,
+                         cudaStream_t stream) {
   if (num_items <= 0) return cudaSuccess;
   const int f = a.head_dim / 4;  // float4 columns per q head
   const dim3 block(kMergeThreads);
-  // Four lanes per column while that fits about one wave of CTAs, else one.
-  const int64_t small_ctas = static_cast<int64_t>(num_items) * ((a.num_q_heads * 4 * f + kMergeThreads - 1) / kMergeThreads);
+  const int small_groups = (a.num_q_heads * 4 * f + kMergeThreads - 1) / kMergeThreads;
+  const int wide_groups = (a.num_q_heads * f + kMergeThreads - 1) / kMergeThreads;
+  // Four lanes per column while that fits about one wave of CTAs, else one,
+  // except for the rows of more than two span groups (first in the list):
+  // their group chain would otherwise set the kernel's end.
+  const int64_t small_ctas = static_cast<int64_t>(num_items) * small_groups;
   if (small_ctas <= 2ll * sm_count()) {
-    const int hpc = kMergeThreads / (4 * f);
-    const dim3 grid(static_cast<unsigned>(num_items), static_cast<unsigned>((a.num_q_heads + hpc - 1) / hpc));
+    const dim3 grid(static_cast<unsigned>(num_items), static_cast<unsigned>(small_groups));
     if (a.head_dim == 128) return launch_pdl(merge_small_kernel<128>, grid, block, 0, stream, a, items);
     return launch_pdl(merge_small_kernel<64>, grid, block, 0, stream, a, items);
   }
-  const int hpc = kMergeThreads / f;
-  const dim3 grid(static_cast<unsigned>(num_items), static_cast<unsigned>((a.num_q_heads + hpc - 1) / hpc));
-  if (a.head_dim == 128) return launch_pdl(merge_wide_kernel<128>, grid, block, 0, stream, a, items);
-  return launch_pdl(merge_wide_kernel<64>, grid, block, 0, stream, a, items);
+  if (num_long <= 0) {
+    const dim3 grid(static_cast<unsigned>(num_items), static_cast<unsigned>(wide_groups));
+    if (a.head_dim == 128) return launch_pdl(merge_wide_kernel<128>, grid, block, 0, stream, a, items);
+    return launch_pdl(merge_wide_kernel<64>, grid, block, 0, stream, a, items);
+  }
+  const int64_t ctas = static_cast<int64_t>(num_long) * small_groups +
+                       static_cast<int64_t>(num_items - num_long) * wide_groups;
+  const dim3 grid(static_cast<unsigned>(ctas));
+  if (a.head_dim == 128)
+    return launch_pdl(merge_mixed_kernel<128>, grid, block, 0, stream, a, items, num_long, small_groups, wide_groups);
+  return launch_pdl(merge_mixed_kernel<64>, grid, block, 0, stream, a, items, num_long, small_groups, wide_groups);
 }
 
 }  // namespace pkv

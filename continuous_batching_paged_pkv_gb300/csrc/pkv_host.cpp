@@ -437,6 +437,10 @@ pkv_status pkv_plan_work(const int32_t *cu, int32_t num_seqs, const int32_t *seq
   info->num_decode_items = static_cast<int32_t>(dec.size());
   info->num_prefill_items = static_cast<int32_t>(pre.size());
   info->num_combine_items = static_cast<int32_t>(comb.size());
+  // merges of more than kLongMergeSpans spans come first (sorted above); the
+  // merge launch gives them four lanes per column
+  info->num_long_combine_items = static_cast<int32_t>(
+      std::count_if(comb.begin(), comb.end(), [](const Item &it) { return it.cost > pkv::kLongMergeSpans; }));
   info->num_partials = partials;
   info->decode_rows_max = rows_max;
   info->num_scratch_items = static_cast<int32_t>(scr.size());

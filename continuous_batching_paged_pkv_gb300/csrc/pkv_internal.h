@@ -43,6 +43,9 @@ struct StepArgs {
   int32_t kv_from_previous;
 };
 
+// Rows of more spans than this are merged with four lanes per column.
+constexpr int kLongMergeSpans = 24;
+
 // Bytes of workspace after the span partials: the decode kernel's task counter.
 constexpr uint64_t kCounterBytes = 256;
 
@@ -60,8 +63,11 @@ cudaError_t launch_copy_blocks(const int32_t *pairs, int64_t num_pairs, void *co
 cudaError_t launch_decode(const StepArgs &a, const CUtensorMap &tmap_k, const CUtensorMap &tmap_v,
                           int32_t num_items, const int32_t *items, bool beside_chunk, cudaStream_t stream);
 
-// One CTA per (row of a multi-span segment, group of q heads): merges that row's span partials.
-cudaError_t launch_merge(const StepArgs &a, int32_t num_items, const int32_t *items, cudaStream_t stream);
+// One CTA per (row of a multi-span segment, group of q heads): merges that
+// row's span partials. The first `num_long` items (rows of more than two
+// span groups) may take four lanes per column.
+cudaError_t launch_merge(const StepArgs &a, int32_t num_items, int32_t num_long, const int32_t *items,
+                         cudaStream_t stream);
 
 // Block-scaled pools (bits = 8, or 4 at head_dim 128): quantising cache write,
 // decode over the codes, and the widening of prompt-chunk histories into a

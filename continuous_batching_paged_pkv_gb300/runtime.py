@@ -198,6 +198,7 @@ def split_work(work, info):
 
         di = B.WorkInfo()
         di.num_decode_items, di.num_combine_items = nd, nc
+        di.num_long_combine_items = info.num_long_combine_items
         di.num_partials, di.decode_rows_max = info.num_partials, info.decode_rows_max
         di.workspace_bytes = info.workspace_bytes
         di.work_words = (nd + nc) * words
