@@ -809,11 +809,12 @@ cudaError_t launch_merge(const StepArgs &a, int32_t num_items, int32_t num_long,
   const dim3 block(kMergeThreads);
   const int small_groups = (a.num_q_heads * 4 * f + kMergeThreads - 1) / kMergeThreads;
   const int wide_groups = (a.num_q_heads * f + kMergeThreads - 1) / kMergeThreads;
-  // Four lanes per column while that fits about one wave of CTAs, else one,
-  // except for the rows of more than two span groups (first in the list):
-  // their group chain would otherwise set the kernel's end.
+  // Four lanes per column while that fits one wave of CTAs (six per SM at
+  // their 80 registers), else one, except for the rows of more than
+  // kLongMergeSpans spans (first in the list): their group chain would
+  // otherwise set the kernel's end.
   const int64_t small_ctas = static_cast<int64_t>(num_items) * small_groups;
-  if (small_ctas <= 2ll * sm_count()) {
+  if (small_ctas <= 6ll * sm_count()) {
     const dim3 grid(static_cast<unsigned>(num_items), static_cast<unsigned>(small_groups));
     if (a.head_dim == 128) return launch_pdl(merge_small_kernel<128>, grid, block, 0, stream, a, items);
     return launch_pdl(merge_small_kernel<64>, grid, block, 0, stream, a, items);
