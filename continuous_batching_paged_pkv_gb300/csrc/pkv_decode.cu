@@ -627,10 +627,12 @@ __device__ __forceinline__ void merge_small_body(const StepArgs &a, const int32_
   if (w == 0) store_merged<D>(a, r.row, h, col, lt, at);
 }
 
+// One-dimensional grids, item-major: every head group of the first (longest)
+// rows is issued before any CTA of a later row.
 template <int D>
 __global__ void __launch_bounds__(kMergeThreads) merge_small_kernel(const StepArgs a,
-                                                                    const int32_t *__restrict__ items) {
-  merge_small_body<D>(a, items, blockIdx.x, blockIdx.y);
+                                                                    const int32_t *__restrict__ items, int groups) {
+  merge_small_body<D>(a, items, static_cast<int>(blockIdx.x) / groups, static_cast<int>(blockIdx.x) % groups);
 }
 
 // One thread per float4 column; 128 threads hold 128 / (D / 4) q heads. The
@@ -707,8 +709,8 @@ __device__ __forceinline__ void merge_wide_body(const StepArgs &a, const int32_t
 
 template <int D>
 __global__ void __launch_bounds__(kMergeThreads) merge_wide_kernel(const StepArgs a,
-                                                                   const int32_t *__restrict__ items) {
-  merge_wide_body<D>(a, items, blockIdx.x, blockIdx.y);
+                                                                   const int32_t *__restrict__ items, int groups) {
+  merge_wide_body<D>(a, items, static_cast<int>(blockIdx.x) / groups, static_cast<int>(blockIdx.x) % groups);
 }
 
 // Both layouts in one grid: the first `num_long` items (rows of more than two
@@ -815,14 +817,14 @@ cudaError_t launch_merge(const StepArgs &a, int32_t num_items, int32_t num_long,
   // otherwise set the kernel's end.
   const int64_t small_ctas = static_cast<int64_t>(num_items) * small_groups;
   if (small_ctas <= 6ll * sm_count()) {
-    const dim3 grid(static_cast<unsigned>(num_items), static_cast<unsigned>(small_groups));
-    if (a.head_dim == 128) return launch_pdl(merge_small_kernel<128>, grid, block, 0, stream, a, items);
-    return launch_pdl(merge_small_kernel<64>, grid, block, 0, stream, a, items);
+    const dim3 grid(static_cast<unsigned>(small_ctas));
+    if (a.head_dim == 128) return launch_pdl(merge_small_kernel<128>, grid, block, 0, stream, a, items, small_groups);
+    return launch_pdl(merge_small_kernel<64>, grid, block, 0, stream, a, items, small_groups);
   }
   if (num_long <= 0) {
-    const dim3 grid(static_cast<unsigned>(num_items), static_cast<unsigned>(wide_groups));
-    if (a.head_dim == 128) return launch_pdl(merge_wide_kernel<128>, grid, block, 0, stream, a, items);
-    return launch_pdl(merge_wide_kernel<64>, grid, block, 0, stream, a, items);
+    const dim3 grid(static_cast<unsigned>(static_cast<int64_t>(num_items) * wide_groups));
+    if (a.head_dim == 128) return launch_pdl(merge_wide_kernel<128>, grid, block, 0, stream, a, items, wide_groups);
+    return launch_pdl(merge_wide_kernel<64>, grid, block, 0, stream, a, items, wide_groups);
   }
   const int64_t ctas = static_cast<int64_t>(num_long) * small_groups +
                        static_cast<int64_t>(num_items - num_long) * wide_groups;

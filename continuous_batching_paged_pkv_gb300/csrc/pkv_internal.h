@@ -44,7 +44,7 @@ struct StepArgs {
 };
 
 // Rows of more spans than this are merged with four lanes per column.
-constexpr int kLongMergeSpans = 24;
+constexpr int kLongMergeSpans = 64;
 
 // Bytes of workspace after the span partials: the decode kernel's task counter.
 constexpr uint64_t kCounterBytes = 256;

@@ -260,7 +260,7 @@ typedef struct pkv_work_info {
     int32_t num_scratch_items; /* (segment) items of the 8-bit pool's chunk path, one per chunk segment */
     int64_t scratch_blocks;    /* bf16 scratch blocks those items widen the chunks' histories into */
     uint64_t workspace_bytes_q8; /* device workspace pkv_attention_q8 needs (may be 0) */
-    int32_t num_long_combine_items; /* the first merge items, whose rows have more than 16 spans */
+    int32_t num_long_combine_items; /* the first merge items, whose rows have more than 64 spans */
 } pkv_work_info;
 
 /*
