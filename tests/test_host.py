@@ -265,6 +265,23 @@ def _work(cu, slots, ctx, **kw):
     return B.pkv_plan_work(np.array(cu), np.array(slots), np.array(ctx), **args)
 
 
+def test_long_merge_rows_come_first_and_are_counted():
+    """Rows of more than 64 spans are counted in num_long_combine_items and lead the merge list
+    (the merge launch gives exactly those rows four lanes per column)."""
+    S = B.PKV_SPLIT_KEYS
+    ctx = np.zeros(8, np.int32)
+    ctx[[0, 1, 2, 3, 4]] = [3 * S, 65 * S, 64 * S, 100 * S + 7, 2 * S]  # spans 3, 65, 64, 101, 2
+    cu = [0, 1, 2, 3, 4, 5]
+    work, info = B.pkv_plan_work(np.array(cu), np.array([0, 1, 2, 3, 4]), ctx, max_slots=8,
+                                 max_blocks_per_slot=2048, block_size=16, num_q_heads=32, num_kv_heads=8,
+                                 head_dim=128)
+    assert info.num_combine_items == 5 and info.num_long_combine_items == 2
+    items = work.reshape(-1, 4)
+    comb = items[info.num_decode_items + info.num_prefill_items:][:info.num_combine_items]
+    spans = [int(c[2]) & 0xFFFF for c in comb]
+    assert spans == sorted(spans, reverse=True) and spans[:2] == [101, 65]
+
+
 def test_work_list_items():
     S = B.PKV_SPLIT_KEYS
     ctx = np.zeros(8, np.int32)
