@@ -38,8 +38,8 @@
 //   2^8 under the lazy rescale), dv the key's V scale of the group and Dref
 //   the largest V scale the task has met in that group (a running maximum;
 //   the group's accumulators are rescaled when it grows), so P' < 2^15 fits
-//   fp16. After each m-tile's MMA a second one with A = -offset (every
-//   element) and the same P' subtracts offset times the sub-tile's P' sums,
+//   fp16. After each m-tile's MMA a second one with A = -offset (each row's
+//   own offset) and the same P' subtracts offset times the sub-tile's P' sums,
 //   so the accumulator never carries more than one sub-tile's offset; the
 //   task's end multiplies by Dref (the 2^7 cancels against the row sum, which
 //   adds the same scaled weights).
