@@ -211,17 +211,21 @@ def test_batch_of_one_equals_in_batch():
 
 @pytest.mark.parametrize("heads,d", [((16, 2), 64), ((8, 1), 128)])
 def test_merge_kernels_agree_bit_for_bit(heads, d):
-    """A step of many split rows is merged by the many-row kernel; the same rows in a step of their
-    own are merged by the few-row kernel. Both follow one fixed order of operations, so the rows
-    must come out bit-identical -- also for rows of more than 32 spans (several rounds per lane)
-    and of more than 64 spans (several shared-memory pieces)."""
+    """A step of many split rows is merged by the many-row kernel (one lane per column, four for
+    rows of more than 64 spans); the same rows in a step of their own are merged by the few-row
+    kernel. Both follow one fixed order of operations, so the rows must come out bit-identical --
+    also for rows of more than 32 spans (several rounds per lane) and of more than 64 spans
+    (several shared-memory pieces in the one-lane layout, the four-lane layout in the mixed one)."""
     hq, hkv = heads
-    ctxs = [int(c) for c in np.random.default_rng(31).integers(300, 2500, 44)] + [9000, 17000, 20001, 513]
+    ctxs = [int(c) for c in np.random.default_rng(31).integers(300, 2500, 150)] + [9000, 17000, 20001, 513]
     shapes = [(1, c) for c in ctxs]
     w = W.random_step(31, shapes, num_q_heads=hq, num_kv_heads=hkv, head_dim=d)
-    _, got_full, _ = run_and_check(w)
+    # more four-lane CTAs (8 per row here) than one wave of six per SM on 152 SMs: the full step
+    # takes the one-lane layout, with its rows of more than 64 spans (17000, 20001) in four lanes
+    assert len(ctxs) * 8 > 6 * 152
+    _, got_full, _ = run_and_check(w, full_pool=False, rows=[0, 1, 150, 151, 152, 153])
     full = _out_rows(w, got_full)
-    pick = [44, 45, 46, 3]
+    pick = [150, 151, 152, 3]
     sub = W.random_step(31, shapes, num_q_heads=hq, num_kv_heads=hkv, head_dim=d)
     sub.segments = [w.segments[i] for i in pick]
     sub.q = np.concatenate([w.q[i:i + 1] for i in pick])  # one row per segment, in packed order
