@@ -21,7 +21,9 @@ with its value, roofline, end-to-end figure and oracle CPU baseline.
 Timing: before each step a 256 MiB buffer is overwritten (larger than the
 129 MB L2) so no step finds its K/V in L2, and a second 256 MiB buffer is then
 read so that L2 holds clean lines (otherwise the flush's dirty lines would be
-written back inside the timed step). Both are outside the CUDA events that
+written back inside the timed step). A ~0.2 ms GPU busy-wait follows, during
+which the host queues the step's launches, so the events bracket GPU work and
+not the host's enqueue time. All of it is outside the CUDA events that
 bracket the step. A second pass times the chunk kernel alone and the decode
 and merge kernels alone on the same step (same stream, same flush): the
 per-kernel rooflines. Under torchrun (N > 1) every rank runs an independent
@@ -427,9 +429,18 @@ def run_reference_churn(args):
 # Our arm: single steps.
 # ---------------------------------------------------------------------------
 
+# GPU cycles of busy-wait between the L2 flush and the first event of a timed
+# call (~0.2 ms at 2 GHz): the host queues every launch of the call while it
+# runs, so the events bracket the call's GPU work and not the host's enqueue
+# time (which the end-to-end leg measures).
+QUEUE_SPIN_CYCLES = 400_000
+QUEUE_NOTE = "every timed call queued behind a ~0.2 ms GPU busy-wait after the flush, before its first event"
+
+
 def timed_calls(flush, stream, fns, n):
-    """Run ``fns`` ``n`` times, each time after an L2 flush, with events between
-    the calls: per call, a list of ``n`` durations in ms."""
+    """Run ``fns`` ``n`` times, each time after an L2 flush and a short GPU
+    busy-wait, with events between the calls: per call, a list of ``n``
+    durations in ms."""
     import torch
 
     out = [[] for _ in fns]
@@ -440,6 +451,7 @@ def timed_calls(flush, stream, fns, n):
         ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(fns) + 1)] for _ in range(m)]
         for row in ev:
             flush()
+            torch.cuda._sleep(QUEUE_SPIN_CYCLES)
             row[0].record(stream)
             for f, e in zip(fns, row[1:]):
                 f()
@@ -610,7 +622,7 @@ def run_ours(args, rank, world, local_rank):
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
            "config": {"workload": f"{args.workload}: {WORKLOAD_TEXT[args.workload]}",
                       "rows_per_step": w.total_q, "kv_bytes_per_step": kv_bytes(w, args.kv), "kv_format": args.kv,
-                      "l2": L2_NOTE, "parallelism": f"replicas x{world} (no exchange between GPUs)",
+                      "l2": L2_NOTE, "queue": QUEUE_NOTE, "parallelism": f"replicas x{world} (no exchange between GPUs)",
                       "seed": args.seed, "pool_blocks": w.num_blocks}}
     res.update(line)
     res["gpu_launches"] = m["launches"] * args.steps
@@ -856,7 +868,7 @@ def run_churn(args, rank, world, local_rank):
                    "steps_with_prompt_chunks": prefill_steps, "rows_per_step_mean": sum(step_rows) / n,
                    "kv_bytes_per_step_mean": sum(step_bytes) / n,
                    "step_ms_p50": statistics.median(step_ms), "step_ms_p90": sorted(step_ms)[int(0.9 * (n - 1))],
-                   "step_ms_max": max(step_ms), "l2": L2_NOTE,
+                   "step_ms_max": max(step_ms), "l2": L2_NOTE, "queue": QUEUE_NOTE,
                    "parallelism": f"replicas x{world} (no exchange between GPUs)", "seed": args.seed,
                    "pool_blocks": spec.num_blocks},
         "pct_hbm_peak": 100.0 * value / world / hbm,
