@@ -90,8 +90,10 @@ WORKLOAD_TEXT = {
              "32 q / 8 kv heads, head_dim 128, block 16, 131,072-block pool; each step planned by the "
              "library's scheduler, pool and lowering",
 }
-# Single-step workloads carried in the churn line's ``configs``.
-EXTRA_CONFIGS = ("decode5", "mixed", "decode256", "chunk2048", "verify4", "verify8", "verify16")
+# Single-step workloads carried in the churn line's ``configs``: (workload, pool format).
+EXTRA_CONFIGS = (("decode5", "bf16"), ("mixed", "bf16"), ("decode256", "bf16"), ("chunk2048", "bf16"),
+                 ("verify4", "bf16"), ("verify8", "bf16"), ("verify16", "bf16"),
+                 ("decode256", "q8"), ("decode256", "q4"))
 # Start of the churn trace's steady state: from here a decode batch runs beside
 # every 512-row prompt chunk; the timed steps are spread over the rest of the trace.
 CHURN_OFFSET = 50
@@ -532,9 +534,12 @@ def kernel_rooflines(w, m, kv, hbm, tflops, peak_src, workload):
         dm = mean(m["decode_ms"])
         db = kv_bytes(w, kv, [s for s in w.segments if s.q_len > 0 and decode_path(w, s)])
         ach = db / (dm / 1e3) / 1e9
-        out["decode"] = {"bound": "hbm", "kernel": "decode_kernel + span merge (merge_small/merge_wide)",
+        quant = kv in ("q8", "q4")
+        dec = "decode_quant_kernel" if quant else "decode_kernel"
+        src, wl = ("pkv_kvquant.cu", f"{workload}_{kv}") if quant else ("pkv_decode.cu", workload)
+        out["decode"] = {"bound": "hbm", "kernel": f"{dec} + span merge (merge_small/merge_wide)",
                          "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
-                         "traffic": profiled_traffic("pkv_decode.cu", workload) if not m["chunk_ms"] else None,
+                         "traffic": profiled_traffic(src, wl) if not m["chunk_ms"] else None,
                          "algorithmic_bytes_per_launch": db, "mean_launch_ms": dm,
                          "peak_source": f"{peak_src} HBM copy bandwidth"}
     if not out:
@@ -588,10 +593,11 @@ def single_line(name, w, m, *, kv, world, steps, cpu=None):
                       "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"],
                       "steps": e["steps"], "ms_per_step": e_ms / e["steps"],
                       "timed": "wall clock per step: one pkv_step call (work list planned on the host, "
-                               + ("the staged inputs read by the kernels in place from pinned host memory, cache "
-                                  "write, attention, the output written straight to pinned host memory"
-                                  if e["in_place"] else
-                                  "H2D copy of the staged inputs, cache write, attention, D2H copy of the output")
+                               + ("the staged inputs read by the kernels in place from pinned host memory"
+                                  if e["in_place"] else "H2D copy of the staged inputs")
+                               + ", cache write, attention, "
+                               + ("the output written by the kernels straight to pinned host memory"
+                                  if e["out_direct"] else "D2H copy of the output")
                                + ") and the stream synchronised"}
     if cpu:
         res["cpu_baseline"] = cpu
@@ -639,17 +645,24 @@ def run_configs(args, rank, world, dev, flush):
 
     out = {}
     steps = max(args.config_steps, 20)
-    for name in EXTRA_CONFIGS:
+    for name, kv in EXTRA_CONFIGS:
         w = W.make_step(name, args.seed)
-        m = measure_step(name, w, dev, kv="bf16", steps=steps, warmup=max(args.warmup, 3),
+        m = measure_step(name, w, dev, kv=kv, steps=steps, warmup=max(args.warmup, 3),
                          e2e_steps=min(args.e2e_steps, 100), flush=flush, world=world)
         cpu = None
-        if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        if rank == 0 and world == 1 and not args.no_cpu_baseline and kv == "bf16":
             cpu = cpu_baseline(w, args.config_cpu_seconds)
-        line = single_line(name, w, m, kv="bf16", world=world, steps=steps, cpu=cpu)
+        line = single_line(name, w, m, kv=kv, world=world, steps=steps, cpu=cpu)
         line["workload"] = WORKLOAD_TEXT[name]
         line["steps"] = steps
-        out[name] = line
+        if kv != "bf16":
+            # KV GB/s counts the pool's own bytes (codes and group scales)
+            line["kv_format"] = kv
+            line["kv_bytes_per_step"] = kv_bytes(w, kv)
+            line["e2e"] = None
+            line["note"] = ("quantised pool: the host-staged one-call path (e2e) serves bf16 pools only; the "
+                            "oracle baseline is on the bf16 line of the same workload")
+        out[name if kv == "bf16" else f"{name}_{kv}"] = line
         del w
         torch.cuda.empty_cache()
     return out
@@ -660,7 +673,10 @@ def run_e2e(w, ds, dev, flush, e2e_steps):
     staging buffer; the timed region is ``pkv_step`` (work list planned on the
     host, the H2D copy, cache write, attention, the D2H copy of the output),
     called through ``binding.StepCall`` (arguments bound once, as a serving loop
-    reusing its buffers would), and the stream synchronisation."""
+    reusing its buffers would), and the stream synchronisation. With
+    PKV_STEP_IN_PLACE, steps without prompt chunks write their output straight
+    to the pinned host buffer instead of the copy out, and small ones read their
+    inputs in place instead of the copy in."""
     import torch
 
     from continuous_batching_paged_pkv_gb300 import binding as B
@@ -692,8 +708,10 @@ def run_e2e(w, ds, dev, flush, e2e_steps):
             times.append((time.perf_counter() - t0) * 1e3)
     if B.pkv_check_device_status(ds.status) != 0:
         raise RuntimeError("device status reported an error in the end-to-end steps")
-    in_place = info.num_prefill_items == 0 and h2d <= B.PKV_STEP_IN_PLACE_MAX_BYTES
-    return {"ms_total": sum(times), "steps": len(times), "h2d": h2d, "d2h": d2h, "in_place": in_place}
+    out_direct = info.num_prefill_items == 0
+    in_place = out_direct and h2d <= B.PKV_STEP_IN_PLACE_MAX_BYTES
+    return {"ms_total": sum(times), "steps": len(times), "h2d": h2d, "d2h": d2h, "in_place": in_place,
+            "out_direct": out_direct}
 
 
 # ---------------------------------------------------------------------------

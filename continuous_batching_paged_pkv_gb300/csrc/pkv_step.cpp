@@ -1,9 +1,9 @@
 // Host-staged step: the step's inputs travel to the device as one copy from a
 // single host staging buffer, the work list is planned straight into that
-// buffer, and the output comes back as one copy (or, for small steps without
-// prompt chunks on request, the kernels read the staging buffer in place and
-// write the output straight to host memory). Everything is enqueued on the
-// caller's stream; nothing here synchronises.
+// buffer, and the output comes back as one copy (or, for steps without prompt
+// chunks on request, the kernels write the output straight to host memory,
+// and for small ones also read the staging buffer in place). Everything is
+// enqueued on the caller's stream; nothing here synchronises.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -97,16 +97,18 @@ pkv_status pkv_step(const pkv_stage_layout *layout, void *host_stage, uint64_t h
   if (L.total_q > 0 && !out) return PKV_ERR_INVALID_ARG;
 
   // 2. one copy in, or (small steps without prompt chunks, on request) the
-  //    staged inputs read in place and the output written straight to out_host
+  //    staged inputs read in place; steps without prompt chunks (on request)
+  //    write the output straight to out_host
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   uint8_t *d = nullptr;
   void *out_dev = out;
-  if ((options & PKV_STEP_IN_PLACE) && info.num_prefill_items == 0 && bytes <= PKV_STEP_IN_PLACE_MAX_BYTES) {
-    void *hv = device_view(host_stage);
+  bool out_direct = false;  // the kernels write the output rows straight into out_host
+  if ((options & PKV_STEP_IN_PLACE) && info.num_prefill_items == 0) {
     void *outv = out_host ? device_view(out_host) : out;
-    if (hv && outv) {
-      d = static_cast<uint8_t *>(hv);
+    if (outv) {
       out_dev = outv;
+      out_direct = out_host != nullptr;
+      if (bytes <= PKV_STEP_IN_PLACE_MAX_BYTES) d = static_cast<uint8_t *>(device_view(host_stage));
     }
   }
   const bool in_place = d != nullptr;
@@ -130,7 +132,7 @@ pkv_status pkv_step(const pkv_stage_layout *layout, void *host_stage, uint64_t h
   if (st != PKV_OK) return st;
 
   // 5. one copy out (none when the output went straight to out_host)
-  if (out_host && L.total_q > 0 && !in_place) {
+  if (out_host && L.total_q > 0 && !out_direct) {
     const uint64_t out_bytes = static_cast<uint64_t>(L.total_q) * L.num_q_heads * L.head_dim * 2;
     if (cudaMemcpyAsync(out_host, out, out_bytes, cudaMemcpyDeviceToHost, cs) != cudaSuccess) return PKV_ERR_CUDA;
   }

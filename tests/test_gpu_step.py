@@ -152,3 +152,44 @@ def test_host_staged_step_views_feed_the_device_calls():
     torch.cuda.synchronize()
     assert B.pkv_check_device_status(ds.status) == 0
     assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+
+
+@pytest.mark.parametrize("name", ["verify4", "mixed"])
+def test_in_place_output_of_larger_steps(name):
+    """PKV_STEP_IN_PLACE on steps above the in-place input size: a step without prompt
+    chunks (verify4, 2 MiB of queries) copies its inputs in and writes its output rows
+    straight into out_host, so `out` keeps its sentinel; a step with a prompt chunk (mixed)
+    takes both copies. Bit for bit the same as the separate device calls either way."""
+    import torch
+
+    w = W.make_step(name, 0)
+    ds = R.prepare(w)
+    R.run_step(ds)
+    torch.cuda.synchronize()
+    assert B.pkv_check_device_status(ds.status) == 0
+    want_bits = ds.out.view(torch.int16).cpu().numpy()
+    low = ds.lowered
+    lay = B.pkv_stage_layout_init(w.total_q, len(w.segments), w.max_slots, w.max_blocks_per_slot, w.num_q_heads,
+                                  w.num_kv_heads, w.head_dim)
+    assert lay.work > B.PKV_STEP_IN_PLACE_MAX_BYTES
+    stage = R.HostStage(lay.work + 4 * int(ds.info.work_words) + 4096, "cuda")
+    stage.fill(lay, q=w.q, k_new=w.new_k(), v_new=w.new_v(), slot_mapping=low.slot_mapping,
+               cu_seqlens_q=low.cu_seqlens_q, seq_slot=low.seq_slot, context_lens=low.context_lens,
+               block_tables=ds.pool.block_tables())
+    stage.device.fill_(0x5A)
+    out = torch.empty_like(ds.out)
+    out.view(torch.int16).fill_(R.SENTINEL_BITS)
+    out_host = torch.empty(out.shape, dtype=torch.bfloat16, pin_memory=True)
+    call = B.StepCall(lay, stage.host, stage.device, ds.k_pool, ds.v_pool, out, ds.workspace, out_host=out_host,
+                      scale=w.scale, device_status=ds.status, in_place=True)
+    for _ in range(2):
+        out_host.view(torch.int16).fill_(R.SENTINEL_BITS)
+        info = call()
+        torch.cuda.synchronize()
+        assert B.pkv_check_device_status(ds.status) == 0
+        assert np.array_equal(out_host.view(torch.int16).numpy(), want_bits), "in-place output differs"
+    chunked = info.num_prefill_items > 0
+    assert chunked == (name == "mixed")
+    assert bool((stage.device[:64] != 0x5A).any()), "inputs above the in-place size are copied in"
+    out_written = not bool((out.view(torch.int16) == R.SENTINEL_BITS).all())
+    assert out_written == chunked, "`out` is written only when the step keeps its copy out"
