@@ -16,15 +16,18 @@ time, and packed rows per second.
 
 The same line carries, under ``configs``, every single-step workload (decode
 x5, mixed, decode x256, a 2048-row chunk, verify steps of 4/8/16 rows), each
-with its value, roofline, end-to-end figure and oracle CPU baseline.
+with its value, roofline, end-to-end figure and oracle CPU baseline, and the
+256-row decode step over 8-bit and 4-bit pools.
 
 Timing: before each step a 256 MiB buffer is overwritten (larger than the
 129 MB L2) so no step finds its K/V in L2, and a second 256 MiB buffer is then
 read so that L2 holds clean lines (otherwise the flush's dirty lines would be
 written back inside the timed step). A ~0.2 ms GPU busy-wait follows, during
 which the host queues the step's launches, so the events bracket GPU work and
-not the host's enqueue time. All of it is outside the CUDA events that
-bracket the step. A second pass times the chunk kernel alone and the decode
+not the host's enqueue time; Python's cyclic garbage collector is off while
+steps are timed (a collection inside the enqueue would outlast the busy-wait)
+and runs between trace steps instead. All of it is outside the CUDA events
+that bracket the step. A second pass times the chunk kernel alone and the decode
 and merge kernels alone on the same step (same stream, same flush): the
 per-kernel rooflines. Under torchrun (N > 1) every rank runs an independent
 replica (the step has no exchange between GPUs); the job's time is the
@@ -34,6 +37,8 @@ maximum over ranks.
 from __future__ import annotations
 
 import argparse
+import contextlib
+import gc
 import hashlib
 import json
 import math
@@ -439,6 +444,22 @@ QUEUE_SPIN_CYCLES = 400_000
 QUEUE_NOTE = "every timed call queued behind a ~0.2 ms GPU busy-wait after the flush, before its first event"
 
 
+@contextlib.contextmanager
+def gc_paused():
+    """Python's cyclic garbage collector off, after one full collection. A
+    collection that lands inside a timed call stalls the host for about a
+    millisecond while it enqueues the step, many times a short step's length
+    (reference counting still frees everything that is not in a cycle)."""
+    was = gc.isenabled()
+    gc.collect()
+    gc.disable()
+    try:
+        yield
+    finally:
+        if was:
+            gc.enable()
+
+
 def timed_calls(flush, stream, fns, n):
     """Run ``fns`` ``n`` times, each time after an L2 flush and a short GPU
     busy-wait, with events between the calls: per call, a list of ``n``
@@ -466,8 +487,13 @@ def timed_calls(flush, stream, fns, n):
     return out
 
 
-def measure_step(name, w, dev, *, kv, steps, warmup, e2e_steps, flush, world=1, clocks=False):
+def measure_step(name, w, dev, **kw):
     """Device and end-to-end timings of one synthetic step (see the module docstring)."""
+    with gc_paused():
+        return _measure_step(name, w, dev, **kw)
+
+
+def _measure_step(name, w, dev, *, kv, steps, warmup, e2e_steps, flush, world=1, clocks=False):
     import torch
 
     from continuous_batching_paged_pkv_gb300 import binding as B
@@ -757,95 +783,97 @@ def run_churn(args, rank, world, local_rank):
     chunk_ms, chunk_fl, dec_ms, dec_bytes, write_ms, attn_ms = [], [], [], [], [], []
     prefill_steps = launches = h2d_tot = d2h_tot = 0
     clocks = stage = ws = None
-    for step in range(window[-1] + 1):
-        rows = sch.plan()
-        if not rows:
+    with gc_paused():
+        for step in range(window[-1] + 1):
+            gc.collect()  # outside every timed region; the collector is off inside them
+            rows = sch.plan()
+            if not rows:
+                sch.commit(rows)
+                continue
+            low = pool.lower([(r.slot, r.n) for r in rows])
+            parts = [toks.rows(r.rid, r.begin, r.begin + r.n) for r in rows]
+            host = {"k": np.concatenate([p[0] for p in parts]), "v": np.concatenate([p[1] for p in parts]),
+                    "q": np.concatenate([p[2] for p in parts])}
+            T = len(host["q"])
+            lay = B.pkv_stage_layout_init(T, len(rows), spec.max_slots, mbps, hq, hkv, d)
+            # sizing only (outside the timed region): the step plans its own work list again inside
+            _, info0 = B.pkv_plan_work(low.cu_seqlens_q, low.seq_slot, low.context_lens, max_slots=spec.max_slots,
+                                       max_blocks_per_slot=mbps, block_size=bs, num_q_heads=hq, num_kv_heads=hkv,
+                                       head_dim=d)
+            need = lay.work + 4 * int(info0.work_words)
+            if stage is None or stage.nbytes < need:
+                stage = R.HostStage(max(need, 32 << 20), dev)
+            if ws is None or ws.numel() < int(info0.workspace_bytes):
+                ws = torch.empty(max(int(info0.workspace_bytes), 64 << 20), dtype=torch.uint8, device=dev)
+            stage.fill(lay, q=host["q"], k_new=host["k"], v_new=host["v"], slot_mapping=low.slot_mapping,
+                       cu_seqlens_q=low.cu_seqlens_q, seq_slot=low.seq_slot, context_lens=low.context_lens,
+                       block_tables=pool.block_tables())
+            out = torch.empty((T, hq, d), dtype=torch.bfloat16, device=dev)
+            out_host = torch.empty(out.shape, dtype=torch.bfloat16, pin_memory=True)
+            ctx = [int(low.context_lens[r.slot]) for r in rows]
+            nbytes = sum(ctx) * hkv * d * 4 + T * hq * d * 4
+            is_timed = step in timed_set
+            is_warm = is_timed or first - args.warmup <= step < first
+            if is_timed and clocks is None:
+                clocks = ClockSampler.for_device(dev)
+                clocks.start()
+
+            # end to end: one pkv_step call (work list, H2D, both calls, D2H), synchronised
+            flush()
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            info = B.pkv_step(lay, stage.host, stage.device, k_pool, v_pool, out, ws, out_host=out_host, scale=scale,
+                              device_status=status, stream=stream)
+            stream.synchronize()
+            e2e = (time.perf_counter() - t0) * 1e3
+
+            # device time of the step alone (inputs resident in the device stage), same calls again
+            v = stage.device_views(lay, info)
+
+            def write():
+                B.pkv_cache_write(v["k_new"], v["v_new"], v["slot_mapping"], k_pool, v_pool, device_status=status)
+
+            def attend(work=v["work"], inf=info, space=ws):
+                B.pkv_attention(v["q"], v["cu_seqlens_q"], v["seq_slot"], v["context_lens"], v["block_tables"],
+                                k_pool, v_pool, work, inf, out, space, scale=scale, device_status=status)
+
+            if is_warm:
+                (st_ms,) = timed_calls(flush, stream, [lambda: (write(), attend())], 1)
+            else:
+                write()
+                attend()
+            if is_timed:
+                # breakdown: the two calls apart, then the chunk kernel alone and the decode + merge kernels alone
+                w_ms, a_ms = timed_calls(flush, stream, [write, attend], 1)
+                cw, dw = R.split_work(v["work"], info)
+                c_ms = timed_calls(flush, stream, [lambda: attend(cw[0], cw[1], None)], 1)[0] if cw else []
+                d_ms = timed_calls(flush, stream, [lambda: attend(dw[0], dw[1], ws)], 1)[0] if dw else []
+            torch.cuda.synchronize()
+            if B.pkv_check_device_status(status) != 0:
+                raise RuntimeError(f"device status reported an error at churn step {step}")
+            if is_timed:
+                step_ms.extend(st_ms)
+                write_ms.extend(w_ms)
+                attn_ms.extend(a_ms)
+                e2e_ms.append(e2e)
+                step_bytes.append(nbytes)
+                step_rows.append(T)
+                dec_rows = [(r, c) for r, c in zip(rows, ctx) if r.n <= max(1, 16 // (hq // hkv))]
+                chk_rows = [(r, c) for r, c in zip(rows, ctx) if r.n > max(1, 16 // (hq // hkv))]
+                if c_ms:
+                    chunk_ms.extend(c_ms)
+                    chunk_fl.append(4 * d * hq * sum(r.n * (c - r.n + 1) + r.n * (r.n - 1) // 2 for r, c in chk_rows))
+                if d_ms:
+                    dec_ms.extend(d_ms)
+                    dec_bytes.append(sum(c for _, c in dec_rows) * hkv * d * 4 + sum(r.n for r, _ in dec_rows) * hq * d * 4)
+                prefill_steps += int(any(r.prefill for r in rows))
+                launches += 1 + int(info.num_decode_items > 0) + int(info.num_prefill_items > 0) + \
+                    int(info.num_combine_items > 0)
+                h2d_tot += lay.work + 4 * int(info.work_words)
+                d2h_tot += out_host.numel() * 2
+            if sample_cpu and is_timed:
+                cpu_rows.extend((r.rid, r.begin + r.n, p[2][-1:]) for r, p in zip(rows, parts))
             sch.commit(rows)
-            continue
-        low = pool.lower([(r.slot, r.n) for r in rows])
-        parts = [toks.rows(r.rid, r.begin, r.begin + r.n) for r in rows]
-        host = {"k": np.concatenate([p[0] for p in parts]), "v": np.concatenate([p[1] for p in parts]),
-                "q": np.concatenate([p[2] for p in parts])}
-        T = len(host["q"])
-        lay = B.pkv_stage_layout_init(T, len(rows), spec.max_slots, mbps, hq, hkv, d)
-        # sizing only (outside the timed region): the step plans its own work list again inside
-        _, info0 = B.pkv_plan_work(low.cu_seqlens_q, low.seq_slot, low.context_lens, max_slots=spec.max_slots,
-                                   max_blocks_per_slot=mbps, block_size=bs, num_q_heads=hq, num_kv_heads=hkv,
-                                   head_dim=d)
-        need = lay.work + 4 * int(info0.work_words)
-        if stage is None or stage.nbytes < need:
-            stage = R.HostStage(max(need, 32 << 20), dev)
-        if ws is None or ws.numel() < int(info0.workspace_bytes):
-            ws = torch.empty(max(int(info0.workspace_bytes), 64 << 20), dtype=torch.uint8, device=dev)
-        stage.fill(lay, q=host["q"], k_new=host["k"], v_new=host["v"], slot_mapping=low.slot_mapping,
-                   cu_seqlens_q=low.cu_seqlens_q, seq_slot=low.seq_slot, context_lens=low.context_lens,
-                   block_tables=pool.block_tables())
-        out = torch.empty((T, hq, d), dtype=torch.bfloat16, device=dev)
-        out_host = torch.empty(out.shape, dtype=torch.bfloat16, pin_memory=True)
-        ctx = [int(low.context_lens[r.slot]) for r in rows]
-        nbytes = sum(ctx) * hkv * d * 4 + T * hq * d * 4
-        is_timed = step in timed_set
-        is_warm = is_timed or first - args.warmup <= step < first
-        if is_timed and clocks is None:
-            clocks = ClockSampler.for_device(dev)
-            clocks.start()
-
-        # end to end: one pkv_step call (work list, H2D, both calls, D2H), synchronised
-        flush()
-        torch.cuda.synchronize()
-        t0 = time.perf_counter()
-        info = B.pkv_step(lay, stage.host, stage.device, k_pool, v_pool, out, ws, out_host=out_host, scale=scale,
-                          device_status=status, stream=stream)
-        stream.synchronize()
-        e2e = (time.perf_counter() - t0) * 1e3
-
-        # device time of the step alone (inputs resident in the device stage), same calls again
-        v = stage.device_views(lay, info)
-
-        def write():
-            B.pkv_cache_write(v["k_new"], v["v_new"], v["slot_mapping"], k_pool, v_pool, device_status=status)
-
-        def attend(work=v["work"], inf=info, space=ws):
-            B.pkv_attention(v["q"], v["cu_seqlens_q"], v["seq_slot"], v["context_lens"], v["block_tables"],
-                            k_pool, v_pool, work, inf, out, space, scale=scale, device_status=status)
-
-        if is_warm:
-            (st_ms,) = timed_calls(flush, stream, [lambda: (write(), attend())], 1)
-        else:
-            write()
-            attend()
-        if is_timed:
-            # breakdown: the two calls apart, then the chunk kernel alone and the decode + merge kernels alone
-            w_ms, a_ms = timed_calls(flush, stream, [write, attend], 1)
-            cw, dw = R.split_work(v["work"], info)
-            c_ms = timed_calls(flush, stream, [lambda: attend(cw[0], cw[1], None)], 1)[0] if cw else []
-            d_ms = timed_calls(flush, stream, [lambda: attend(dw[0], dw[1], ws)], 1)[0] if dw else []
-        torch.cuda.synchronize()
-        if B.pkv_check_device_status(status) != 0:
-            raise RuntimeError(f"device status reported an error at churn step {step}")
-        if is_timed:
-            step_ms.extend(st_ms)
-            write_ms.extend(w_ms)
-            attn_ms.extend(a_ms)
-            e2e_ms.append(e2e)
-            step_bytes.append(nbytes)
-            step_rows.append(T)
-            dec_rows = [(r, c) for r, c in zip(rows, ctx) if r.n <= max(1, 16 // (hq // hkv))]
-            chk_rows = [(r, c) for r, c in zip(rows, ctx) if r.n > max(1, 16 // (hq // hkv))]
-            if c_ms:
-                chunk_ms.extend(c_ms)
-                chunk_fl.append(4 * d * hq * sum(r.n * (c - r.n + 1) + r.n * (r.n - 1) // 2 for r, c in chk_rows))
-            if d_ms:
-                dec_ms.extend(d_ms)
-                dec_bytes.append(sum(c for _, c in dec_rows) * hkv * d * 4 + sum(r.n for r, _ in dec_rows) * hq * d * 4)
-            prefill_steps += int(any(r.prefill for r in rows))
-            launches += 1 + int(info.num_decode_items > 0) + int(info.num_prefill_items > 0) + \
-                int(info.num_combine_items > 0)
-            h2d_tot += lay.work + 4 * int(info.work_words)
-            d2h_tot += out_host.numel() * 2
-        if sample_cpu and is_timed:
-            cpu_rows.extend((r.rid, r.begin + r.n, p[2][-1:]) for r, p in zip(rows, parts))
-        sch.commit(rows)
     clk = clocks.stop() if clocks is not None else {}
 
     n = len(step_ms)
