@@ -594,9 +594,10 @@ def single_line(name, w, m, *, kv, world, steps, cpu=None):
     kernels, dominant = kernel_rooflines(w, m, kv, hbm, tflops, peak_src, name)
     if kernels:
         res["kernels"] = kernels
+    decode_only = all(decode_path(w, s) for s in w.segments if s.q_len > 0)
     if dominant == "chunk":
         res["roofline"] = kernels["chunk"]
-    elif dominant == "decode" and "chunk" not in kernels:
+    elif (dominant == "decode" and "chunk" not in kernels) or (dominant is None and decode_only):
         # decode-only steps: the attention call (decode + merge) is the kernel pair that bounds the step
         dec = "decode_quant_kernel" if kv in ("q8", "q4") else "decode_kernel"
         src = "pkv_kvquant.cu" if kv in ("q8", "q4") else "pkv_decode.cu"
