@@ -452,8 +452,8 @@ def pkv_step(layout: StageLayout, host_stage, device_stage, k_pool, v_pool, out,
              out_host=None, scale: float = 0.0, device_status=None, stream=None, in_place: bool = False) -> WorkInfo:
     """One step from the host staging buffer (see ``include/pkv.h``). Returns the step's work info.
 
-    ``in_place`` passes PKV_STEP_IN_PLACE: a step without prompt chunks then writes its
-    output straight into ``out_host`` (no copy out), and a small one also reads its inputs
+    ``in_place`` passes PKV_STEP_IN_PLACE: the step then writes its output straight into
+    ``out_host`` (no copy out), and a small one without prompt chunks also reads its inputs
     from ``host_stage`` in place (no copy in).
     On an error the raised PkvError carries ``info`` (filled where the library got that far).
     """

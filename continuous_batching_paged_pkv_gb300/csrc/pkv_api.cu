@@ -158,6 +158,20 @@ pkv_status pkv_attention(const void *q, const int32_t *cu_seqlens_q, int32_t num
                          int32_t num_kv_heads, int32_t head_dim, float scale, const int32_t *work,
                          const pkv_work_info *info, void *out, void *workspace, uint64_t workspace_bytes,
                          uint32_t *device_status, pkv_stream_t stream) {
+  return pkv::attention(q, cu_seqlens_q, num_seqs, total_q, seq_slot, context_lens, block_tables, max_slots,
+                        max_blocks_per_slot, block_size, k_pool, v_pool, num_blocks, num_q_heads, num_kv_heads,
+                        head_dim, scale, work, info, out, workspace, workspace_bytes, device_status, stream, false);
+}
+
+}  // extern "C"
+
+pkv_status pkv::attention(const void *q, const int32_t *cu_seqlens_q, int32_t num_seqs, int64_t total_q,
+                          const int32_t *seq_slot, const int32_t *context_lens, const int32_t *block_tables,
+                          int32_t max_slots, int32_t max_blocks_per_slot, int32_t block_size, const void *k_pool,
+                          const void *v_pool, int64_t num_blocks, int32_t num_q_heads, int32_t num_kv_heads,
+                          int32_t head_dim, float scale, const int32_t *work, const pkv_work_info *info, void *out,
+                          void *workspace, uint64_t workspace_bytes, uint32_t *device_status, pkv_stream_t stream,
+                          bool out_on_host) {
   if (!info || num_seqs < 0 || total_q < 0 || max_slots <= 0 || max_blocks_per_slot <= 0 || num_blocks <= 0)
     return PKV_ERR_INVALID_ARG;
   if (!supported_shape(block_size, num_q_heads, num_kv_heads, head_dim)) return PKV_ERR_UNSUPPORTED;
@@ -211,6 +225,7 @@ pkv_status pkv_attention(const void *q, const int32_t *cu_seqlens_q, int32_t num
   a.scale_log2 = s * 1.4426950408889634f;
   a.work = work;
   a.out = out;
+  a.out_on_host = out_on_host ? 1 : 0;
   a.partial_acc = static_cast<float *>(workspace);
   a.partial_ml = need ? reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + acc_bytes) : nullptr;
   a.status = device_status;
@@ -256,6 +271,8 @@ pkv_status pkv_attention(const void *q, const int32_t *cu_seqlens_q, int32_t num
   }
   return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
+
+extern "C" {
 
 pkv_status pkv_copy_blocks(const int32_t *pairs, int64_t num_pairs, void *const *arrays,
                            const int64_t *block_bytes, int32_t num_arrays, int64_t num_blocks,

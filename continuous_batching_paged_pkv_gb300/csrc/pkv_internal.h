@@ -41,7 +41,22 @@ struct StepArgs {
   // 8-bit and 4-bit paths' widening pass): wait for it before any K/V load.
   // Otherwise only the tiles holding this step's rows wait for the cache write.
   int32_t kv_from_previous;
+  // `out` is page-locked host memory reached through its device address: the
+  // chunk kernel then stages its rows in shared memory and stores whole rows,
+  // which the host link carries at its copy rate (one 16-byte piece of 32
+  // different rows per store it carries far slower).
+  int32_t out_on_host;
 };
+
+// pkv_attention with the output's location: out_on_host marks `out` as host
+// memory (pkv_step's output written straight to the caller's host buffer).
+pkv_status attention(const void *q, const int32_t *cu_seqlens_q, int32_t num_seqs, int64_t total_q,
+                     const int32_t *seq_slot, const int32_t *context_lens, const int32_t *block_tables,
+                     int32_t max_slots, int32_t max_blocks_per_slot, int32_t block_size, const void *k_pool,
+                     const void *v_pool, int64_t num_blocks, int32_t num_q_heads, int32_t num_kv_heads,
+                     int32_t head_dim, float scale, const int32_t *work, const pkv_work_info *info, void *out,
+                     void *workspace, uint64_t workspace_bytes, uint32_t *device_status, pkv_stream_t stream,
+                     bool out_on_host);
 
 // Rows of more spans than this are merged with four lanes per column.
 constexpr int kLongMergeSpans = 64;

@@ -340,8 +340,7 @@ __global__ void __maxnreg__(kLaunchRegs) prefill_pair_kernel(const __grid_consta
     const int qw = warp;
     const int mrow = qw * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(qw * 32) << 16;
-    const int pos = mrow / G, hh = mrow % G;
-    const bool row_valid = mrow < G * P && pos < rows;
+    const int pos = mrow / G;
     const int p_row = L - n + pos0 + pos;  // last visible key of this row (inclusive)
     const float sl2 = a.scale_log2;
     const uint32_t p_ready0 = cluster_addr(bar + kPReady, 0);
@@ -435,21 +434,62 @@ __global__ void __maxnreg__(kLaunchRegs) prefill_pair_kernel(const __grid_consta
     if (ok && warp_wait_or_abort(bar + kPVDone + (ntiles - 1) % kSBufs, ((ntiles - 1) / kSBufs) & 1, abort_flag)) {
       tc_fence_after();
       const float inv = 1.f / (l_sum + l_odd);
-      __nv_bfloat16 *orow = reinterpret_cast<__nv_bfloat16 *>(a.out) +
-                            (static_cast<size_t>(row0 + pos0 + pos) * a.num_q_heads + g * G + hh) * D;
+      constexpr int kRowBytes = D * 2, kChunks = kRowBytes / 16;
+      if (!a.out_on_host) {
+        // each thread stores its own row, 64 bytes per TMEM load (the loads are warp-wide)
+        const bool row_valid = mrow < G * P && pos < rows;
+        uint4 *orow = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(a.out) +
+                                                (static_cast<size_t>(row0 + pos0 + pos) * a.num_q_heads + g * G +
+                                                 mrow % G) * D);
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t ov[32];
-        tmem_ld32(tmem + lane_base + kOCol + c * 32, ov);
-        tmem_wait_ld();
-        if (row_valid) {
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t ov[32];
+          tmem_ld32(tmem + lane_base + kOCol + c * 32, ov);
+          tmem_wait_ld();
+          if (row_valid) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              pk[i] = pack_bf16x2(__uint_as_float(ov[2 * i]) * inv, __uint_as_float(ov[2 * i + 1]) * inv);
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              orow[c * 4 + v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+          }
+        }
+      } else {
+        // Output in host memory: the rows leave through shared memory, the Q
+        // tile (no longer read once the last P.V is done, its S consumed
+        // above). Each warp stages its 32 rows (16-byte chunk k of row r at
+        // chunk k ^ (r % 16), which keeps the banks apart both ways), then a
+        // half-warp stores one whole 256-byte row per instruction.
+        static_assert(kChunks == 16 && 4 * 32 * kRowBytes <= Lay::kQBytes, "four warps' rows fit in the Q tile");
+        uint8_t *stage = sQ + qw * 32 * kRowBytes;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t ov[32];
+          tmem_ld32(tmem + lane_base + kOCol + c * 32, ov);
+          tmem_wait_ld();
           uint32_t pk[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i)
             pk[i] = pack_bf16x2(__uint_as_float(ov[2 * i]) * inv, __uint_as_float(ov[2 * i + 1]) * inv);
-          uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
 #pragma unroll
-          for (int v = 0; v < 4; ++v) dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+          for (int v = 0; v < 4; ++v)
+            *reinterpret_cast<uint4 *>(stage + lane * kRowBytes + (((c * 4 + v) ^ (lane & 15)) << 4)) =
+                make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+        }
+        __syncwarp();
+        const int k = lane % kChunks;
+#pragma unroll 4
+        for (int r0 = 0; r0 < 32; r0 += 32 / kChunks) {
+          const int r = r0 + lane / kChunks, mr = qw * 32 + r;
+          const int rpos = mr / G, rhh = mr % G;
+          if (mr < G * P && rpos < rows) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(stage + r * kRowBytes + ((k ^ (r & 15)) << 4));
+            reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(a.out) +
+                                      (static_cast<size_t>(row0 + pos0 + rpos) * a.num_q_heads + g * G + rhh) *
+                                          D)[k] = v;
+          }
         }
       }
     }

@@ -1,8 +1,8 @@
 // Host-staged step: the step's inputs travel to the device as one copy from a
 // single host staging buffer, the work list is planned straight into that
-// buffer, and the output comes back as one copy (or, for steps without prompt
-// chunks on request, the kernels write the output straight to host memory,
-// and for small ones also read the staging buffer in place). Everything is
+// buffer, and the output comes back as one copy (or, on request, the kernels
+// write the output straight to host memory, and for small steps without
+// prompt chunks also read the staging buffer in place). Everything is
 // enqueued on the caller's stream; nothing here synchronises.
 #include <cuda_runtime.h>
 
@@ -10,6 +10,7 @@
 #include <cstring>
 
 #include "pkv.h"
+#include "pkv_internal.h"
 
 namespace {
 
@@ -97,18 +98,19 @@ pkv_status pkv_step(const pkv_stage_layout *layout, void *host_stage, uint64_t h
   if (L.total_q > 0 && !out) return PKV_ERR_INVALID_ARG;
 
   // 2. one copy in, or (small steps without prompt chunks, on request) the
-  //    staged inputs read in place; steps without prompt chunks (on request)
-  //    write the output straight to out_host
+  //    staged inputs read in place; on request the output goes straight to
+  //    out_host
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   uint8_t *d = nullptr;
   void *out_dev = out;
   bool out_direct = false;  // the kernels write the output rows straight into out_host
-  if ((options & PKV_STEP_IN_PLACE) && info.num_prefill_items == 0) {
+  if (options & PKV_STEP_IN_PLACE) {
     void *outv = out_host ? device_view(out_host) : out;
     if (outv) {
       out_dev = outv;
       out_direct = out_host != nullptr;
-      if (bytes <= PKV_STEP_IN_PLACE_MAX_BYTES) d = static_cast<uint8_t *>(device_view(host_stage));
+      if (info.num_prefill_items == 0 && bytes <= PKV_STEP_IN_PLACE_MAX_BYTES)
+        d = static_cast<uint8_t *>(device_view(host_stage));
     }
   }
   const bool in_place = d != nullptr;
@@ -122,13 +124,13 @@ pkv_status pkv_step(const pkv_stage_layout *layout, void *host_stage, uint64_t h
   st = pkv_cache_write(d + L.k_new, d + L.v_new, reinterpret_cast<const int64_t *>(d + L.slot_mapping), L.total_q,
                        k_pool, v_pool, num_blocks, block_size, L.num_kv_heads, L.head_dim, device_status, stream);
   if (st != PKV_OK) return st;
-  st = pkv_attention(d + L.q, reinterpret_cast<const int32_t *>(d + L.cu_seqlens_q), L.num_seqs, L.total_q,
-                     reinterpret_cast<const int32_t *>(d + L.seq_slot),
-                     reinterpret_cast<const int32_t *>(d + L.context_lens),
-                     reinterpret_cast<const int32_t *>(d + L.block_tables), L.max_slots, L.max_blocks_per_slot,
-                     block_size, k_pool, v_pool, num_blocks, L.num_q_heads, L.num_kv_heads, L.head_dim, scale,
-                     reinterpret_cast<const int32_t *>(d + L.work), &info, out_dev, workspace, workspace_bytes,
-                     device_status, stream);
+  st = pkv::attention(d + L.q, reinterpret_cast<const int32_t *>(d + L.cu_seqlens_q), L.num_seqs, L.total_q,
+                      reinterpret_cast<const int32_t *>(d + L.seq_slot),
+                      reinterpret_cast<const int32_t *>(d + L.context_lens),
+                      reinterpret_cast<const int32_t *>(d + L.block_tables), L.max_slots, L.max_blocks_per_slot,
+                      block_size, k_pool, v_pool, num_blocks, L.num_q_heads, L.num_kv_heads, L.head_dim, scale,
+                      reinterpret_cast<const int32_t *>(d + L.work), &info, out_dev, workspace, workspace_bytes,
+                      device_status, stream, out_direct);
   if (st != PKV_OK) return st;
 
   // 5. one copy out (none when the output went straight to out_host)

@@ -555,20 +555,20 @@ pkv_status pkv_stage_layout_init(pkv_stage_layout *layout, int64_t total_q, int3
  * soon as it happens, with the earlier steps already enqueued.
  *
  * `options` (bit flags, 0 for none):
- *   PKV_STEP_IN_PLACE — a step without prompt chunks skips the copy out when
- *   the device can address out_host (page-locked memory under unified
- *   addressing, as cudaPointerGetAttributes reports it): its output rows are
- *   written straight into out_host, and `out` is left untouched. If its staged
- *   bytes (inputs and work list) are also at most PKV_STEP_IN_PLACE_MAX_BYTES
- *   and the device can address host_stage, it skips the copy in as well: the
- *   kernels read the staged inputs from host_stage in place and device_stage
- *   is left untouched (with out_host NULL such a step writes `out`). For
- *   small steps each copy costs more in latency than its bytes; reading in
- *   place over the host link costs a few dependent accesses instead. The
- *   decode and merge kernels store whole row pieces per warp, so their output
- *   crosses the host link as it is produced; the chunk kernel stores one row
- *   per thread, so steps with prompt chunks keep both copies. Without device
- *   addresses for the buffers the step runs the copies as above.
+ *   PKV_STEP_IN_PLACE — the step skips the copy out when the device can
+ *   address out_host (page-locked memory under unified addressing, as
+ *   cudaPointerGetAttributes reports it): its output rows are written straight
+ *   into out_host as the kernels produce them, and `out` is left untouched
+ *   (the head_dim 128 chunk kernel then stages its rows in shared memory so
+ *   that every store carries whole 256-byte rows over the host link). A step
+ *   without prompt chunks whose staged bytes (inputs and work list) are at
+ *   most PKV_STEP_IN_PLACE_MAX_BYTES also skips the copy in when the device
+ *   can address host_stage: the kernels read the staged inputs from
+ *   host_stage in place and device_stage is left untouched (with out_host
+ *   NULL such a step writes `out`). For small steps each copy costs more in
+ *   latency than its bytes; reading in place over the host link costs a few
+ *   dependent accesses instead. Without device addresses for the buffers the
+ *   step runs the copies as above.
  */
 #define PKV_STEP_IN_PLACE 1u
 #define PKV_STEP_IN_PLACE_MAX_BYTES (1u << 20)
