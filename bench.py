@@ -217,6 +217,13 @@ class ClockSampler:
             self.proc = subprocess.Popen(cmd, stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
+        # nvidia-smi's start-up (its driver queries) must not overlap the timed
+        # region: wait for its first sample, for at most 10 s
+        t0 = time.perf_counter()
+        while self.proc is not None and self.proc.poll() is None and time.perf_counter() - t0 < 10.0:
+            if os.path.getsize(self.path) > 0:
+                break
+            time.sleep(0.05)
         time.sleep(0.4)
 
     def stop(self):
