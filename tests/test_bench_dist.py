@@ -54,3 +54,44 @@ def test_work_accounting_for_the_mixed_step():
     # chunk rows 1024..1535 see 1025..1536 keys: 4 * D * Hq * sum
     assert bench.chunk_flops(w) == 4 * 128 * 32 * sum(range(1025, 1537))
     assert bench.kv_bytes(w) == sum(s.ctx for s in w.segments) * 8 * 128 * 4 + 516 * 32 * 128 * 4
+
+
+def test_gc_is_paused_inside_and_restored_after():
+    import gc
+
+    import bench
+
+    assert gc.isenabled()
+    with bench.gc_paused():
+        assert not gc.isenabled()
+    assert gc.isenabled()
+    gc.disable()
+    try:
+        with bench.gc_paused():
+            assert not gc.isenabled()
+        assert not gc.isenabled(), "a collector that was off stays off"
+    finally:
+        gc.enable()
+
+
+def test_clock_sampler_waits_for_the_first_sample(tmp_path, monkeypatch):
+    """A stand-in for nvidia-smi that needs a second before its first sample: start()
+    returns only after that sample, and stop() reads the clocks and event reasons."""
+    import time
+
+    import bench
+
+    fake = tmp_path / "nvidia-smi"
+    fake.write_text("#!/bin/sh\nsleep 1\n"
+                    "while true; do echo '0, 2070, 2070, 812.5, 0x4, Not Active, Not Active, Not Active, Active'; "
+                    "sleep 0.1; done\n")
+    fake.chmod(0o755)
+    monkeypatch.setenv("PATH", f"{tmp_path}{os.pathsep}{os.environ['PATH']}")
+    sampler = bench.ClockSampler(None)
+    t0 = time.perf_counter()
+    sampler.start()
+    assert time.perf_counter() - t0 >= 1.0
+    assert os.path.getsize(sampler.path) > 0
+    clk = sampler.stop()
+    assert clk["sm_mhz"] == 2070.0 and clk["sm_max_mhz"] == 2070.0
+    assert clk["reasons"] == ["sw_power_cap"] and clk["samples"] >= 3
