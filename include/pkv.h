@@ -506,7 +506,8 @@ pkv_status pkv_attention_q4(const void *q, const int32_t *cu_seqlens_q, int32_t 
  * one is the library's design: every per-step input sits in one caller-owned
  * host staging buffer at offsets fixed by pkv_stage_layout_init, so a step is
  * one host-to-device copy, the cache write, the attention call and one
- * device-to-host copy of the output, all on `stream`.
+ * device-to-host copy of the output (or, with PKV_STEP_IN_PLACE, the output
+ * written by the kernels straight into host memory), all on `stream`.
  * ---------------------------------------------------------------------- */
 typedef struct pkv_stage_layout {
     /* shapes the layout was made for */
