@@ -313,6 +313,75 @@ def test_work_list_items():
     assert info.workspace_bytes_q8 == info.workspace_bytes + 2 * a256(96 * 8 * 16 * 128 * 2) + a256(8 * 128 * 4)
 
 
+def _model_work_list(cu, slots, ctx, group, head_dim, block_size):
+    """The work list's rules restated: decode segments (at most 16 / group rows) cut into
+    PKV_SPLIT_KEYS-key spans, full spans in segment order and then each segment's shorter last
+    span, longest first; chunk tiles of 128 / group rows (pairs at head_dim 128), the pair
+    that sees the most keys first; one merge item per row of a multi-span segment, rows of the
+    most spans first; one scratch item per chunk segment. Equal costs keep their order."""
+    S = B.PKV_SPLIT_KEYS
+    decode_rows, rpt, step = max(1, 16 // group), 128 // group, 2 if head_dim == 128 else 1
+    full, tails, pre, rows, scr = [], [], [], [], []
+    partials = scratch = 0
+    for s in range(len(slots)):
+        n, slot = cu[s + 1] - cu[s], slots[s]
+        L = int(ctx[slot])
+        if n == 0:
+            continue
+        if n <= decode_rows:
+            spans = -(-L // S)
+            base = partials if spans > 1 else -1
+            full += [[s, slot, sp, base] for sp in range(L // S)]
+            if L % S:
+                tails.append((L % S, s, [s, slot, L // S, base]))
+            if spans > 1:
+                rows.append((spans, s, [[s, slot, spans | (i << 16) | ((n - 1) << 24), base + i] for i in range(n)]))
+                partials += spans * n
+        else:
+            nblk = -(-L // block_size)
+            scr.append([s, slot, scratch, nblk])
+            scratch += nblk
+            tiles = -(-n // rpt)
+            for t in range(0, tiles, step):
+                count = min(step, tiles - t)
+                pre.append((L - n + min(n, (t + count) * rpt), len(pre), [s, slot, t, count]))
+    order = lambda x: (-x[0], x[1])
+    dec = full + [t[2] for t in sorted(tails, key=order)]
+    comb = [r for _, _, rr in sorted(rows, key=order) for r in rr]
+    return dec, [p[2] for p in sorted(pre, key=order)], comb, scr, partials, scratch
+
+
+def test_work_list_matches_its_rules_on_random_steps():
+    rng = np.random.default_rng(7)
+    for _ in range(300):
+        hkv = int(rng.choice([1, 2, 8]))
+        group = int(rng.choice([1, 2, 4, 5, 8, 16]))
+        head_dim, bs = int(rng.choice([64, 128])), int(rng.choice([16, 32, 64]))
+        max_slots, mbps = 24, 512
+        nseg = int(rng.integers(0, 12))
+        slots = [int(x) for x in rng.permutation(max_slots)[:nseg]]
+        kind = rng.random(nseg)
+        n = np.where(kind < 0.55, 1, np.where(kind < 0.8, rng.integers(1, 17, nseg), rng.integers(17, 600, nseg)))
+        n = np.where(rng.random(nseg) < 0.05, 0, n).astype(int)
+        ctx = np.zeros(max_slots, np.int32)
+        for i, slot in enumerate(slots):
+            L = int(rng.integers(max(int(n[i]), 1), min(mbps * bs, 40000) + 1))
+            whole = (L // 256) * 256  # some contexts end on a span boundary
+            ctx[slot] = whole if whole >= max(int(n[i]), 1) and rng.random() < 0.3 else L
+        cu = [0] + np.cumsum(n).tolist()
+        work, info = _work(cu, slots, ctx, max_slots=max_slots, max_blocks_per_slot=mbps, block_size=bs,
+                           num_q_heads=hkv * group, num_kv_heads=hkv, head_dim=head_dim)
+        dec, pre, comb, scr, partials, scratch = _model_work_list(cu, slots, ctx, group, head_dim, bs)
+        items = np.asarray(work)[:int(info.work_words)].reshape(-1, 4).tolist()
+        assert items == dec + pre + comb + scr
+        assert (info.num_decode_items, info.num_prefill_items, info.num_combine_items, info.num_scratch_items) == \
+            (len(dec), len(pre), len(comb), len(scr))
+        assert info.num_partials == partials and info.scratch_blocks == scratch
+        assert info.num_long_combine_items == sum((c[2] & 0xFFFF) > 64 for c in comb)
+        decode_n = [x for x in n if 0 < x <= max(1, 16 // group)]
+        assert info.decode_rows_max == (max(decode_n) if decode_n else 0)
+
+
 @pytest.mark.parametrize("cu,slots,ctx_pairs,err", [
     ([0, 5], [0], {0: 4}, B.STATUS_NAMES[1]),            # rows > context
     ([0, 1, 2], [1, 1], {1: 9}, B.STATUS_NAMES[1]),      # duplicate slot
