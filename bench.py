@@ -680,9 +680,20 @@ def run_configs(args, rank, world, dev, flush):
     out = {}
     steps = max(args.config_steps, 20)
     for name, kv in EXTRA_CONFIGS:
+        key = name if kv == "bf16" else f"{name}_{kv}"
         w = W.make_step(name, args.seed)
-        m = measure_step(name, w, dev, kv=kv, steps=steps, warmup=max(args.warmup, 3),
-                         e2e_steps=min(args.e2e_steps, 100), flush=flush, world=world)
+        try:
+            m = measure_step(name, w, dev, kv=kv, steps=steps, warmup=max(args.warmup, 3),
+                             e2e_steps=min(args.e2e_steps, 100), flush=flush, world=world)
+        except (RuntimeError, MemoryError) as e:
+            if world > 1:
+                raise  # the ranks' barriers must stay paired
+            # one configuration's failure (say, no room for its pool) is reported in the
+            # line instead of taking the churn figures down with it
+            out[key] = {"workload": WORKLOAD_TEXT[name], "error": f"{type(e).__name__}: {e}"[:300]}
+            del w
+            torch.cuda.empty_cache()
+            continue
         cpu = None
         if rank == 0 and world == 1 and not args.no_cpu_baseline and kv == "bf16":
             cpu = cpu_baseline(w, args.config_cpu_seconds)
@@ -696,7 +707,7 @@ def run_configs(args, rank, world, dev, flush):
             line["e2e"] = None
             line["note"] = ("quantised pool: the host-staged one-call path (e2e) serves bf16 pools only; the "
                             "oracle baseline is on the bf16 line of the same workload")
-        out[name if kv == "bf16" else f"{name}_{kv}"] = line
+        out[key] = line
         del w
         torch.cuda.empty_cache()
     return out

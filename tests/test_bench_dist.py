@@ -95,3 +95,23 @@ def test_clock_sampler_waits_for_the_first_sample(tmp_path, monkeypatch):
     clk = sampler.stop()
     assert clk["sm_mhz"] == 2070.0 and clk["sm_max_mhz"] == 2070.0
     assert clk["reasons"] == ["sw_power_cap"] and clk["samples"] >= 3
+
+
+def test_a_failed_config_is_reported_not_fatal(monkeypatch):
+    """One configuration that cannot run (here every one: the measurement raises) leaves an
+    error entry under its key; the line still forms."""
+    import types
+
+    import bench
+    from continuous_batching_paged_pkv_gb300 import workloads as W
+
+    monkeypatch.setattr(W, "make_step", lambda name, seed=0, **kw: types.SimpleNamespace(name=name))
+
+    def boom(name, w, dev, **kw):
+        raise MemoryError(f"no room for the {kw['kv']} pool of {name}")
+
+    monkeypatch.setattr(bench, "measure_step", boom)
+    args = types.SimpleNamespace(config_steps=20, warmup=3, e2e_steps=0, no_cpu_baseline=True, seed=0)
+    out = bench.run_configs(args, 0, 1, "cpu", flush=None)
+    assert set(out) == {n if kv == "bf16" else f"{n}_{kv}" for n, kv in bench.EXTRA_CONFIGS}
+    assert out["decode256_q8"]["error"] == "MemoryError: no room for the q8 pool of decode256"
